@@ -1,0 +1,172 @@
+/*
+ * qmv.h - C ABI of the GB300 (sm_103a) quantized matrix-vector library.
+ *
+ * Quantized formats (colibri PR #418 "Vulkan backend: expert tier + dense +
+ * MLA attention on any Vulkan 1.2 GPU"):
+ *   int4-gs64  two offset-binary nibbles per byte, value = nibble - 8
+ *              (commit "opt-in Vulkan int4/int8 quantized GEMV"), element 2j
+ *              in the LOW nibble of byte j and 2j+1 in the high nibble (the
+ *              pages do not state the order; this is the library's reading),
+ *              bytes in K order; one fp32 scale per 64 consecutive K values
+ *              applied to that group's partial dot product (commit "grouped
+ *              scales in the Vulkan kernels", fmt 4, group size 64).
+ *              Weights [rows][K/2] uint8, scales [rows][K/64] fp32, row-major.
+ *   int8-row   int8 weights [rows][K] with one fp32 scale per row (same
+ *              GEMV commit, fmt 1).
+ *
+ * Conventions for every entry point:
+ *   - All array arguments are DEVICE pointers (memory the caller allocated on
+ *     the current CUDA device). The caller owns every buffer; the library
+ *     never allocates, frees or synchronises.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and is complete when the stream is. Calls can be
+ *     captured into CUDA graphs.
+ *   - Arguments are validated on the host before anything is enqueued. On a
+ *     nonzero return nothing was enqueued and no output was touched.
+ *   - Shapes are row-major and contiguous. K, H and I must be multiples of 64.
+ *   - Activations may have any finite fp32 value; each kernel rescales them
+ *     by a power of two internally, which changes no result bit pattern beyond
+ *     the stated tolerance.
+ *   - Accuracy: the fp32 paths return y with
+ *         |y - y_exact| <= 2e-5 * sum_k |w_k * x_k|
+ *     per output (w the dequantized weight), the bf16 prefill path with 1e-2.
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, so CUDA callers pass their streams unchanged. */
+typedef struct CUstream_st *qmv_stream_t;
+
+typedef enum {
+    QMV_OK = 0,
+    QMV_EINVAL = -1,     /* null pointer, bad count, unsupported group size   */
+    QMV_ESHAPE = -2,     /* a dimension is not a multiple of 64 or too large   */
+    QMV_EWORKSPACE = -3, /* workspace pointer null, misaligned or too small    */
+    QMV_ECUDA = -4,      /* a CUDA launch failed (see cudaGetLastError)        */
+    QMV_ETIMEOUT = -5,   /* a bounded device-side wait gave up                 */
+    QMV_EALIGN = -6      /* a pointer is not aligned as documented             */
+} qmv_status;
+
+/* Library version as 10000*major + 100*minor + patch. */
+int qmv_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *qmv_status_str(int status);
+
+/* ---------------------------------------------------------------- GEMV */
+
+/* Dense int4 grouped-scale GEMV (colibri PR #418, commits "opt-in Vulkan
+ * int4/int8 quantized GEMV" and "grouped scales in the Vulkan kernels"):
+ *     y[s][i] = sum_g scales[i][g] * sum_{k in group g} (nibble(i,k) - 8) * x[s][k]
+ *   wq      [N][K/2] uint8, 16-byte aligned
+ *   scales  [N][K/gs] fp32, 4-byte aligned
+ *   x       [S][K] fp32, 4-byte aligned
+ *   y       [S][N] fp32 (written, fp32-accumulated)
+ *   gs must be 64; K a multiple of 64; 1 <= N, 1 <= S, K <= 65536.
+ * Errors: QMV_EINVAL (null pointer, gs != 64, N or S < 1), QMV_ESHAPE (K),
+ *         QMV_EALIGN, QMV_ECUDA. */
+int qmv_int4_gs(const uint8_t *wq, const float *scales, int N, int K, int gs, const float *x,
+                float *y, int S, qmv_stream_t stream);
+
+/* Dense int8 per-row-scale GEMV (same commit, fmt 1):
+ *     y[s][i] = row_scale[i] * sum_k w[i][k] * x[s][k]
+ *   w [N][K] int8 (16-byte aligned), row_scale [N] fp32, x [S][K] fp32, y [S][N] fp32.
+ *   K a multiple of 64, K <= 65536; N, S >= 1. Errors as qmv_int4_gs. */
+int qmv_int8_row(const int8_t *w, const float *row_scale, int N, int K, const float *x,
+                 float *y, int S, qmv_stream_t stream);
+
+/* ---------------------------------------------------------------- MoE */
+
+/* Device-resident int4-gs64 expert weights (the analogue of the pages'
+ * uploaded-once weight handle). All experts live in one pool each:
+ *   gu_q [E][2I][H/2] uint8: gate rows 0..I-1, then up rows I..2I-1 (reading:
+ *        the pages fuse gate and up but do not state the stacking order)
+ *   gu_s [E][2I][H/64] fp32
+ *   dn_q [E][H][I/2] uint8, dn_s [E][H][I/64] fp32
+ * The descriptor itself is a HOST struct; it is read during the call only. */
+typedef struct {
+    const uint8_t *gu_q;
+    const float *gu_s;
+    const uint8_t *dn_q;
+    const float *dn_s;
+    int32_t E, H, I, gs;
+} qmv_moe_int4;
+
+/* Top-k routing: for each token, the k experts with the largest logits
+ * (fp32 comparison; equal logits keep the lower expert index first), in
+ * descending logit order, with weights = softmax over all experts restricted
+ * to the chosen k and renormalised to sum to one (equivalently
+ * exp(l_e - l_max) / sum over the chosen). NaN logits are never chosen
+ * ahead of finite ones.
+ *   logits [T][E] fp32; ids [T][k] int32 (written); w [T][k] fp32 (written).
+ *   1 <= k <= min(E, 32), E <= 1024, T >= 0 (T == 0 enqueues nothing). */
+int moe_route_topk(const float *logits, int T, int E, int k, int32_t *ids, float *w,
+                   qmv_stream_t stream);
+
+/* Token -> expert grouping (so each expert's weights are read once per batch,
+ * colibri PR #418 "coli_vk_expert_group"). Pair p = t*k + j.
+ *   offsets [E+1] int32: exclusive prefix sum of the per-expert pair counts
+ *   list    [T*k] int32: pair ids grouped by expert, ascending inside a group
+ *   uexp    [E]   int32: the experts with at least one pair, ascending
+ *   n_used  [1]   int32: how many entries of uexp are valid
+ *   status  [1]   int32: OR-ed with 1 when an id is outside [0, E); such a
+ *                 pair is left out of every list. Not cleared by this call.
+ *   T*k <= 1 << 20, E <= 1024. */
+int moe_group(const int32_t *ids, int T, int k, int E, int32_t *offsets, int32_t *list,
+              int32_t *uexp, int32_t *n_used, int32_t *status, qmv_stream_t stream);
+
+/* Fused gate+up with SiLU*mul for every grouped pair (colibri PR #418,
+ * commit "qmatmul_gate_up.comp + coli_vk_gate_up"): for each expert e in
+ * uexp and each pair p = t*k + j routed to e,
+ *     h[p][c] = SiLU(gate_e[c] . x[t]) * (up_e[c] . x[t]),   SiLU(g) = g / (1 + e^-g)
+ *   x [T][H] fp32; h [T*k][I] fp32 (rows of pairs that no expert serves are
+ *   left untouched). offsets/list/uexp/n_used as written by moe_group.
+ *   ws: device scratch of at least moe_workspace_bytes(m, T, k) bytes,
+ *   256-byte aligned (the activations are converted into it first). */
+int moe_gate_up_silu(const qmv_moe_int4 *m, const float *x, int T, int k,
+                     const int32_t *offsets, const int32_t *list, const int32_t *uexp,
+                     const int32_t *n_used, float *h, void *ws, size_t ws_bytes,
+                     qmv_stream_t stream);
+
+/* Down projection of every grouped pair (colibri PR #418, "coli_vk_expert_group"):
+ *     y[p][i] = down_e[i] . h[p]          y [T*k][H] fp32 (pairs not served: untouched)
+ * and the weighted combine (PR #1338, weighted accumulation of expert outputs):
+ *     out[t][i] = sum_{j < k, ids[t][j] valid} w[t][j] * y[t*k + j][i]
+ *   summed in slot order, so results are deterministic. out [T][H] fp32.
+ *   moe_down takes the same workspace as moe_gate_up_silu. moe_combine reads
+ *   ids to skip pairs whose id is outside [0, E). */
+int moe_down(const qmv_moe_int4 *m, const float *h, int T, int k, const int32_t *offsets,
+             const int32_t *list, const int32_t *uexp, const int32_t *n_used, float *y,
+             void *ws, size_t ws_bytes, qmv_stream_t stream);
+int moe_combine(const float *y, const int32_t *ids, const float *w, int T, int k, int E, int H,
+                float *out, qmv_stream_t stream);
+
+/* Workspace of the MoE entry points that take one, in bytes (256-byte aligned segments). */
+size_t moe_workspace_bytes(const qmv_moe_int4 *m, int T, int k);
+
+/* Whole MoE expert FFN for a decode micro-batch (colibri PR #418,
+ * "coli_vk_expert_group": fused gate+up+SiLU, then down, hidden kept on the
+ * device; PR #1338: weighted accumulation). Equivalent to moe_group,
+ * moe_gate_up_silu, moe_down and moe_combine in sequence:
+ *     out[t] = sum_j w[t][j] * down_e(SiLU(gate_e x[t]) * up_e x[t]),  e = ids[t][j]
+ *   x [T][H] fp32, ids [T][k] int32, w [T][k] fp32, out [T][H] fp32.
+ *   ws: device workspace of at least moe_workspace_bytes(m, T, k) bytes,
+ *   256-byte aligned, owned by the caller, not shared between concurrent calls.
+ *   The first int32 of ws is the device status word of moe_group (cleared at
+ *   the start of the call). */
+int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids,
+                        const float *w, int k, float *out, void *ws, size_t ws_bytes,
+                        qmv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMV_H */

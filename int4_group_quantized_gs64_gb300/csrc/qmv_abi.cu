@@ -1,0 +1,195 @@
+// qmv_abi.cu - the extern "C" entry points declared in include/qmv.h.
+//
+// Every entry point validates its arguments on the host and returns a
+// negative qmv_status before enqueuing anything (so a failed call leaves its
+// outputs alone, as the pages require of a failed take: colibri PR #1338,
+// fake-Vulkan gate comment), then calls the launchers of qmv_internal.h.
+#include <stdint.h>
+
+#include "../../include/qmv.h"
+#include "qmv_internal.h"
+
+namespace {
+
+constexpr int kMaxK = 65536;
+constexpr int kMaxE = 1024;
+constexpr int kMaxPairs = 1 << 20;
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline cudaStream_t cs(qmv_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline int from_cuda(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ECUDA; }
+
+int check_moe(const qmv_moe_int4 *m) {
+    if (!m || !m->gu_q || !m->gu_s || !m->dn_q || !m->dn_s) return QMV_EINVAL;
+    if (m->gs != 64 || m->E < 1 || m->E > kMaxE) return QMV_EINVAL;
+    if (m->H < 64 || m->I < 64 || m->H % 64 || m->I % 64 || m->H > kMaxK || m->I > kMaxK)
+        return QMV_ESHAPE;
+    if (!aligned(m->gu_q, 16) || !aligned(m->dn_q, 16) || !aligned(m->gu_s, 4) ||
+        !aligned(m->dn_s, 4))
+        return QMV_EALIGN;
+    return QMV_OK;
+}
+
+qmv::MoeDims dims(const qmv_moe_int4 *m) {
+    return qmv::MoeDims{m->gu_q, m->gu_s, m->dn_q, m->dn_s, m->E, m->H, m->I};
+}
+
+int check_group_args(const int32_t *offsets, const int32_t *list, const int32_t *uexp,
+                     const int32_t *n_used) {
+    if (!offsets || !list || !uexp || !n_used) return QMV_EINVAL;
+    if (!aligned(offsets, 4) || !aligned(list, 4) || !aligned(uexp, 4) || !aligned(n_used, 4))
+        return QMV_EALIGN;
+    return QMV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qmv_version(void) { return 100; }
+
+const char *qmv_status_str(int status) {
+    switch (status) {
+        case QMV_OK: return "ok";
+        case QMV_EINVAL: return "invalid argument";
+        case QMV_ESHAPE: return "unsupported shape";
+        case QMV_EWORKSPACE: return "workspace missing, misaligned or too small";
+        case QMV_ECUDA: return "CUDA launch failed";
+        case QMV_ETIMEOUT: return "device wait timed out";
+        case QMV_EALIGN: return "pointer misaligned";
+        default: return "unknown status";
+    }
+}
+
+int qmv_int4_gs(const uint8_t *wq, const float *scales, int N, int K, int gs, const float *x,
+                float *y, int S, qmv_stream_t stream) {
+    if (!wq || !scales || !x || !y || N < 1 || S < 1 || gs != 64) return QMV_EINVAL;
+    if (K < 64 || K % 64 || K > kMaxK) return QMV_ESHAPE;
+    if (!aligned(wq, 16) || !aligned(scales, 4) || !aligned(x, 4) || !aligned(y, 4))
+        return QMV_EALIGN;
+    return from_cuda(qmv::launch_dense_int4(wq, scales, N, K, x, y, S, cs(stream)));
+}
+
+int qmv_int8_row(const int8_t *w, const float *row_scale, int N, int K, const float *x, float *y,
+                 int S, qmv_stream_t stream) {
+    if (!w || !row_scale || !x || !y || N < 1 || S < 1) return QMV_EINVAL;
+    if (K < 64 || K % 64 || K > kMaxK) return QMV_ESHAPE;
+    if (!aligned(w, 16) || !aligned(row_scale, 4) || !aligned(x, 4) || !aligned(y, 4))
+        return QMV_EALIGN;
+    return from_cuda(qmv::launch_dense_int8(w, row_scale, N, K, x, y, S, cs(stream)));
+}
+
+int moe_route_topk(const float *logits, int T, int E, int k, int32_t *ids, float *w,
+                   qmv_stream_t stream) {
+    if (T < 0 || E < 1 || E > kMaxE || k < 1 || k > E || k > 32) return QMV_EINVAL;
+    if (T == 0) return QMV_OK;
+    if (!logits || !ids || !w) return QMV_EINVAL;
+    if (!aligned(logits, 4) || !aligned(ids, 4) || !aligned(w, 4)) return QMV_EALIGN;
+    return from_cuda(qmv::launch_route(logits, T, E, k, ids, w, cs(stream)));
+}
+
+int moe_group(const int32_t *ids, int T, int k, int E, int32_t *offsets, int32_t *list,
+              int32_t *uexp, int32_t *n_used, int32_t *status, qmv_stream_t stream) {
+    if (T < 0 || k < 1 || E < 1 || E > kMaxE || (int64_t)T * k > kMaxPairs) return QMV_EINVAL;
+    if (!status || (T > 0 && !ids)) return QMV_EINVAL;
+    int r = check_group_args(offsets, list, uexp, n_used);
+    if (r) return r;
+    if (!aligned(status, 4) || (ids && !aligned(ids, 4))) return QMV_EALIGN;
+    return from_cuda(qmv::launch_group(ids, T * k, E, offsets, list, uexp, n_used, status,
+                                       cs(stream)));
+}
+
+int moe_gate_up_silu(const qmv_moe_int4 *m, const float *x, int T, int k, const int32_t *offsets,
+                     const int32_t *list, const int32_t *uexp, const int32_t *n_used, float *h,
+                     void *ws, size_t ws_bytes, qmv_stream_t stream) {
+    int r = check_moe(m);
+    if (r) return r;
+    if (T < 0 || k < 1 || (int64_t)T * k > kMaxPairs) return QMV_EINVAL;
+    if (T == 0) return QMV_OK;
+    if (!x || !h) return QMV_EINVAL;
+    if ((r = check_group_args(offsets, list, uexp, n_used))) return r;
+    if (!aligned(x, 4) || !aligned(h, 4)) return QMV_EALIGN;
+    const qmv::MoeWorkspace L = qmv::moe_ws_layout(m->E, m->H, m->I, T, k);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return QMV_EWORKSPACE;
+    char *b = static_cast<char *>(ws);
+    float *xfac = reinterpret_cast<float *>(b + L.xfac);
+    cudaError_t e = qmv::launch_split(x, T, m->H, b + L.xcells, xfac, cs(stream));
+    if (e == cudaSuccess)
+        e = qmv::launch_gate_up(dims(m), b + L.xcells, xfac, T, k, offsets, list, uexp, n_used, h,
+                                cs(stream));
+    return from_cuda(e);
+}
+
+int moe_down(const qmv_moe_int4 *m, const float *h, int T, int k, const int32_t *offsets,
+             const int32_t *list, const int32_t *uexp, const int32_t *n_used, float *y, void *ws,
+             size_t ws_bytes, qmv_stream_t stream) {
+    int r = check_moe(m);
+    if (r) return r;
+    if (T < 0 || k < 1 || (int64_t)T * k > kMaxPairs) return QMV_EINVAL;
+    if (T == 0) return QMV_OK;
+    if (!h || !y) return QMV_EINVAL;
+    if ((r = check_group_args(offsets, list, uexp, n_used))) return r;
+    if (!aligned(h, 4) || !aligned(y, 4)) return QMV_EALIGN;
+    const qmv::MoeWorkspace L = qmv::moe_ws_layout(m->E, m->H, m->I, T, k);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return QMV_EWORKSPACE;
+    char *b = static_cast<char *>(ws);
+    float *hfac = reinterpret_cast<float *>(b + L.hfac);
+    cudaError_t e = qmv::launch_split(h, T * k, m->I, b + L.hcells, hfac, cs(stream));
+    if (e == cudaSuccess)
+        e = qmv::launch_down(dims(m), b + L.hcells, hfac, T, k, offsets, list, uexp, n_used, y,
+                             cs(stream));
+    return from_cuda(e);
+}
+
+int moe_combine(const float *y, const int32_t *ids, const float *w, int T, int k, int E, int H,
+                float *out, qmv_stream_t stream) {
+    if (T < 0 || k < 1 || E < 1 || H < 1 || (int64_t)T * k > kMaxPairs) return QMV_EINVAL;
+    if (T == 0) return QMV_OK;
+    if (!y || !ids || !w || !out) return QMV_EINVAL;
+    if (!aligned(y, 4) || !aligned(ids, 4) || !aligned(w, 4) || !aligned(out, 4)) return QMV_EALIGN;
+    return from_cuda(qmv::launch_combine(y, ids, w, T, k, E, H, out, cs(stream)));
+}
+
+size_t moe_workspace_bytes(const qmv_moe_int4 *m, int T, int k) {
+    if (check_moe(m) || T < 0 || k < 1 || (int64_t)T * k > kMaxPairs) return 0;
+    return qmv::moe_ws_layout(m->E, m->H, m->I, T, k).total;
+}
+
+int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids,
+                        const float *w, int k, float *out, void *ws, size_t ws_bytes,
+                        qmv_stream_t stream) {
+    int r = check_moe(m);
+    if (r) return r;
+    if (T < 0 || k < 1 || k > m->E || (int64_t)T * k > kMaxPairs) return QMV_EINVAL;
+    if (T == 0) return QMV_OK;
+    if (!x || !ids || !w || !out) return QMV_EINVAL;
+    if (!aligned(x, 4) || !aligned(ids, 4) || !aligned(w, 4) || !aligned(out, 4)) return QMV_EALIGN;
+    const qmv::MoeWorkspace L = qmv::moe_ws_layout(m->E, m->H, m->I, T, k);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return QMV_EWORKSPACE;
+    char *b = static_cast<char *>(ws);
+    int32_t *status = reinterpret_cast<int32_t *>(b + L.status);
+    int32_t *offsets = reinterpret_cast<int32_t *>(b + L.offsets);
+    int32_t *list = reinterpret_cast<int32_t *>(b + L.list);
+    int32_t *uexp = reinterpret_cast<int32_t *>(b + L.uexp);
+    int32_t *n_used = reinterpret_cast<int32_t *>(b + L.n_used);
+    float *xfac = reinterpret_cast<float *>(b + L.xfac);
+    float *h = reinterpret_cast<float *>(b + L.h);
+    float *hfac = reinterpret_cast<float *>(b + L.hfac);
+    float *y = reinterpret_cast<float *>(b + L.y);
+    const cudaStream_t st = cs(stream);
+    const qmv::MoeDims d = dims(m);
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = qmv::launch_group(ids, T * k, m->E, offsets, list, uexp, n_used, status, st);
+    if (e == cudaSuccess) e = qmv::launch_split(x, T, m->H, b + L.xcells, xfac, st);
+    if (e == cudaSuccess)
+        e = qmv::launch_gate_up(d, b + L.xcells, xfac, T, k, offsets, list, uexp, n_used, h, st);
+    if (e == cudaSuccess) e = qmv::launch_split(h, T * k, m->I, b + L.hcells, hfac, st);
+    if (e == cudaSuccess)
+        e = qmv::launch_down(d, b + L.hcells, hfac, T, k, offsets, list, uexp, n_used, y, st);
+    if (e == cudaSuccess) e = qmv::launch_combine(y, ids, w, T, k, m->E, m->H, out, st);
+    return from_cuda(e);
+}
+
+}  // extern "C"

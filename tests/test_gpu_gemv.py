@@ -1,0 +1,126 @@
+"""Dense int4-gs64 and int8-row GEMV on the GPU against the fp64 oracle."""
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+from tests.gpu_util import TOL_FP32, norm_err
+
+torch = pytest.importorskip("torch")
+q = pytest.importorskip("int4_group_quantized_gs64_gb300")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    q.build()
+    q.lib()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run_int4(wq, sc, x):
+    y = q.qmv_int4_gs(dev(wq), dev(sc), dev(x))
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def run_int8(w, r, x):
+    y = q.qmv_int8_row(dev(w), dev(r), dev(x))
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("N,K", [(1024, 1024), (14336, 4096)], ids=["1024x1024", "14336x4096"])
+def test_int4_workloads(N, K):
+    wq, sc, x = datagen.dense_int4(N, K, 1)
+    y = run_int4(wq, sc, x)
+    ref, den = oracle.qmv_int4_gs(wq, sc, x, 64, with_den=True)
+    assert norm_err(y, ref, den) <= TOL_FP32
+
+
+def test_int8_workload():
+    w, r, x = datagen.dense_int8(14336, 4096, 1)
+    y = run_int8(w, r, x)
+    ref, den = oracle.qmv_int8_row(w, r, x)
+    assert norm_err(y, ref, den) <= TOL_FP32
+
+
+SHAPES = [(1, 64, 1), (17, 64, 3), (100, 192, 5), (63, 1088, 4), (65, 4096, 8), (33, 640, 16),
+          (40, 256, 17), (16, 16384, 2), (128, 2048, 33)]
+
+
+@pytest.mark.parametrize("N,K,S", SHAPES)
+def test_int4_shapes(N, K, S):
+    rng = np.random.default_rng(N * 7919 + K + S)
+    wq = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sc = (np.abs(rng.normal(0, 0.02, size=(N, K // 64))) + 1e-4).astype(np.float32)
+    x = rng.normal(size=(S, K)).astype(np.float32)
+    y = run_int4(wq, sc, x)
+    ref, den = oracle.qmv_int4_gs(wq, sc, x, 64, with_den=True)
+    assert norm_err(y, ref, den) <= TOL_FP32
+
+
+@pytest.mark.parametrize("N,K,S", SHAPES)
+def test_int8_shapes(N, K, S):
+    rng = np.random.default_rng(N * 31 + K + S)
+    w = rng.integers(-128, 128, size=(N, K)).astype(np.int8)
+    r = np.abs(rng.normal(0, 0.01, size=N)).astype(np.float32)
+    x = rng.normal(size=(S, K)).astype(np.float32)
+    y = run_int8(w, r, x)
+    ref, den = oracle.qmv_int8_row(w, r, x)
+    assert norm_err(y, ref, den) <= TOL_FP32
+
+
+def test_int4_all_equal_nibbles_bit_exact():
+    """nibble == c, dyadic scales, small-integer x: every step is exact in fp32 too."""
+    rng = np.random.default_rng(5)
+    N, K = 96, 512
+    x = rng.integers(-20, 21, size=(2, K)).astype(np.float32)
+    s = (2.0 ** rng.integers(-8, 2, size=(N, K // 64))).astype(np.float32)
+    for c in (0, 3, 8, 15):
+        wq = np.full((N, K // 2), c | (c << 4), np.uint8)
+        y = run_int4(wq, s, x)
+        ref = oracle.qmv_int4_gs(wq, s, x, 64)
+        assert np.array_equal(y.astype(np.float64), ref), c
+        if c == 8:
+            assert not np.any(y)
+
+
+def test_zero_and_extreme_activations():
+    rng = np.random.default_rng(9)
+    N, K = 80, 1024
+    wq = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sc = (np.abs(rng.normal(0, 0.02, size=(N, K // 64))) + 1e-4).astype(np.float32)
+    x = np.zeros((1, K), np.float32)
+    assert not np.any(run_int4(wq, sc, x))
+    for mag in (1e-30, 1e-6, 1e6, 1e30):
+        x = (rng.normal(size=(2, K)) * mag).astype(np.float32)
+        ref, den = oracle.qmv_int4_gs(wq, sc, x, 64, with_den=True)
+        assert norm_err(run_int4(wq, sc, x), ref, den) <= TOL_FP32, mag
+    # one huge outlier among unit values
+    x = rng.normal(size=(1, K)).astype(np.float32)
+    x[0, 17] = 3e4
+    ref, den = oracle.qmv_int4_gs(wq, sc, x, 64, with_den=True)
+    assert norm_err(run_int4(wq, sc, x), ref, den) <= TOL_FP32
+
+
+def test_deterministic():
+    wq, sc, x = datagen.dense_int4(4096, 4096, 3)
+    a = run_int4(wq, sc, x)
+    b = run_int4(wq, sc, x)
+    assert np.array_equal(a, b)
+
+
+def test_bad_arguments_leave_output_untouched():
+    y = torch.full((1, 64), 7.0, device="cuda")
+    wq = torch.zeros((64, 48), dtype=torch.uint8, device="cuda")   # K = 96: not a multiple of 64
+    sc = torch.ones((64, 1), device="cuda")
+    x = torch.ones((1, 96), device="cuda")
+    with pytest.raises(q.QmvError):
+        q.qmv_int4_gs(wq, sc, x, y=y)
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)

@@ -1,0 +1,200 @@
+"""MoE decode on the GPU against the fp64 oracle: routing and grouping
+bit-exact, gate+up+SiLU, down and the weighted combine within 2e-5."""
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+from tests.gpu_util import TOL_FP32, TOL_W, moe_oracle, norm_err
+
+torch = pytest.importorskip("torch")
+q = pytest.importorskip("int4_group_quantized_gs64_gb300")
+
+pytestmark = pytest.mark.gpu
+
+W2 = datagen.WORKLOADS[2]
+W3 = datagen.WORKLOADS[3]
+W4 = datagen.WORKLOADS[4]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    q.build()
+    q.lib()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+@pytest.fixture(scope="module")
+def pool_160():
+    """All 160 experts of the H 6144 / I 2048 workloads on the device (3.4 GB)."""
+    wts = datagen.moe_weights(160, 6144, 2048)
+    m = q.MoeInt4Weights.from_numpy(wts)
+    del wts
+    return m
+
+
+# ------------------------------------------------------------------ routing / grouping
+
+@pytest.mark.parametrize("wl", [W2, W3, W4], ids=["w2", "w3", "w4"])
+def test_route_matches_oracle(wl):
+    _, logits = datagen.moe_inputs(wl["T"], wl["E"], 64, hot=wl["hot"])
+    ids, w = q.moe_route_topk(dev(logits), wl["k"])
+    torch.cuda.synchronize()
+    rid, rw = oracle.route_topk(logits, wl["k"])
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.allclose(w.cpu().numpy(), rw, rtol=TOL_W, atol=0)
+
+
+def test_route_ties_and_nan():
+    logits = np.array([[1.0, 3.0, 3.0, 0.5, 2.0, 3.0, -np.inf, 0.0],
+                       [np.nan, 1.0, 1.0, 1.0, 1.0, 1.0, 1.0, 1.0]], np.float32)
+    ids, w = q.moe_route_topk(dev(logits), 4)
+    torch.cuda.synchronize()
+    ids = ids.cpu().numpy()
+    assert ids[0].tolist() == [1, 2, 5, 4]
+    assert ids[1].tolist() == [1, 2, 3, 4]
+    rid, rw = oracle.route_topk(logits[:1], 4)
+    assert np.array_equal(ids[:1], rid)
+    assert np.allclose(w.cpu().numpy()[0], rw[0], rtol=TOL_W, atol=0)
+    assert np.allclose(w.cpu().numpy()[1], 0.25, rtol=TOL_W)
+
+
+def test_route_many_experts_and_k32():
+    rng = np.random.default_rng(3)
+    logits = rng.normal(size=(37, 1024)).astype(np.float32)
+    ids, w = q.moe_route_topk(dev(logits), 32)
+    torch.cuda.synchronize()
+    rid, rw = oracle.route_topk(logits, 32)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.allclose(w.cpu().numpy(), rw, rtol=TOL_W, atol=0)
+
+
+@pytest.mark.parametrize("T,k,E", [(1, 8, 256), (8, 8, 160), (512, 8, 160), (33, 2, 7),
+                                   (3000, 4, 1024), (5, 3, 6)])
+def test_group_matches_oracle(T, k, E):
+    rng = np.random.default_rng(T + k + E)
+    ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    off, lst, uexp, nu, st = q.moe_group(dev(ids), E)
+    torch.cuda.synchronize()
+    roff, rlst, ruexp = oracle.group(ids, E)
+    assert np.array_equal(off.cpu().numpy(), roff)
+    assert np.array_equal(lst.cpu().numpy(), rlst)
+    n = int(nu.cpu()[0])
+    assert n == len(ruexp) and np.array_equal(uexp.cpu().numpy()[:n], ruexp)
+    assert int(st.cpu()[0]) == 0
+
+
+def test_group_flags_bad_ids():
+    ids = np.array([[0, 5], [9, 1], [-1, 2]], np.int32)  # 9 and -1 are outside [0, 6)
+    off, lst, uexp, nu, st = q.moe_group(dev(ids), 6)
+    torch.cuda.synchronize()
+    assert int(st.cpu()[0]) == 1
+    good = ids.copy()
+    assert off.cpu().numpy()[-1] == 4
+    assert lst.cpu().numpy()[:4].tolist() == [0, 3, 5, 1]
+
+
+# ------------------------------------------------------------------ FFN stages
+
+def _route_oracle(wl, T=None):
+    T = wl["T"] if T is None else T
+    x, logits = datagen.moe_inputs(T, wl["E"], wl["H"], hot=wl["hot"])
+    ids, w = oracle.route_topk(logits, wl["k"])
+    return x, ids, w.astype(np.float32)
+
+
+def test_w2_full_layer():
+    wl = W2
+    wts = datagen.moe_weights(wl["E"], wl["H"], wl["I"])
+    m = q.MoeInt4Weights.from_numpy(wts)
+    x, ids, w = _route_oracle(wl)
+    out = q.moe_expert_ffn_int4(m, dev(x), dev(ids), dev(w))
+    torch.cuda.synchronize()
+    ref = moe_oracle(wl["E"], wl["H"], wl["I"], x.astype(np.float64), ids, w, weights=wts)
+    assert norm_err(out.cpu().numpy(), ref["out"], ref["den"]) <= TOL_FP32
+
+
+def test_w2_stages_hidden():
+    wl = W2
+    wts = datagen.moe_weights(wl["E"], wl["H"], wl["I"])
+    m = q.MoeInt4Weights.from_numpy(wts)
+    x, ids, w = _route_oracle(wl)
+    dids = dev(ids)
+    off, lst, uexp, nu, _ = q.moe_group(dids, wl["E"])
+    h = q.moe_gate_up_silu(m, dev(x), wl["k"], off, lst, uexp, nu)
+    y = q.moe_down(m, h, wl["T"], wl["k"], off, lst, uexp, nu)
+    out = q.moe_combine(y, dids, dev(w), wl["E"])
+    torch.cuda.synchronize()
+    ref = moe_oracle(wl["E"], wl["H"], wl["I"], x.astype(np.float64), ids, w, want_h=True,
+                     weights=wts)
+    assert norm_err(h.cpu().numpy(), ref["h"], ref["hden"]) <= TOL_FP32
+    assert norm_err(out.cpu().numpy(), ref["out"], ref["den"]) <= TOL_FP32
+
+
+def test_w3_full_layer(pool_160):
+    wl = W3
+    x, ids, w = _route_oracle(wl)
+    out = q.moe_expert_ffn_int4(pool_160, dev(x), dev(ids), dev(w))
+    torch.cuda.synchronize()
+    ref = moe_oracle(wl["E"], wl["H"], wl["I"], x.astype(np.float64), ids, w, want_h=False)
+    assert norm_err(out.cpu().numpy(), ref["out"], ref["den"]) <= TOL_FP32
+
+
+def test_w3_hidden(pool_160):
+    wl = W3
+    x, ids, w = _route_oracle(wl)
+    dids = dev(ids)
+    off, lst, uexp, nu, _ = q.moe_group(dids, wl["E"])
+    h = q.moe_gate_up_silu(pool_160, dev(x), wl["k"], off, lst, uexp, nu)
+    torch.cuda.synchronize()
+    ref = moe_oracle(wl["E"], wl["H"], wl["I"], x.astype(np.float64), ids, w, want_h=True)
+    assert norm_err(h.cpu().numpy(), ref["h"], ref["hden"]) <= TOL_FP32
+
+
+@pytest.mark.parametrize("T,k,E,H,I", [(5, 3, 6, 128, 192), (33, 2, 7, 64, 64), (1, 1, 1, 256, 128),
+                                       (40, 4, 3, 192, 320), (2, 8, 8, 1024, 512)])
+def test_ffn_shapes(T, k, E, H, I):
+    """Odd shapes: ragged token counts per expert, > 16 tokens on one expert
+    (several passes), a single expert, k = E."""
+    rng = np.random.default_rng(T * 100 + k + E)
+    wts = dict(
+        gu_q=rng.integers(0, 256, size=(E, 2 * I, H // 2), dtype=np.uint8),
+        gu_s=(np.abs(rng.normal(0, 0.02, size=(E, 2 * I, H // 64))) + 1e-4).astype(np.float32),
+        dn_q=rng.integers(0, 256, size=(E, H, I // 2), dtype=np.uint8),
+        dn_s=(np.abs(rng.normal(0, 0.02, size=(E, H, I // 64))) + 1e-4).astype(np.float32),
+    )
+    m = q.MoeInt4Weights.from_numpy(wts)
+    x = rng.normal(size=(T, H)).astype(np.float32)
+    logits = rng.normal(size=(T, E)).astype(np.float32)
+    ids, w = oracle.route_topk(logits, k)
+    w = w.astype(np.float32)
+    out = q.moe_expert_ffn_int4(m, dev(x), dev(ids), dev(w))
+    torch.cuda.synchronize()
+    ref = oracle.moe_ffn(wts, x.astype(np.float64), ids, w)
+    assert norm_err(out.cpu().numpy(), ref["out"], ref["den"]) <= TOL_FP32
+
+
+def test_ffn_bad_ids_flag_and_skip():
+    rng = np.random.default_rng(77)
+    E, H, I, T, k = 4, 128, 64, 3, 2
+    wts = datagen.moe_weights(E, H, I)
+    m = q.MoeInt4Weights.from_numpy(wts)
+    x = rng.normal(size=(T, H)).astype(np.float32)
+    ids = np.array([[0, 1], [7, 2], [3, -2]], np.int32)
+    w = np.full((T, k), 0.5, np.float32)
+    ws = torch.empty(q.moe_workspace_bytes(m, T, k), dtype=torch.uint8, device="cuda")
+    out = q.moe_expert_ffn_int4(m, dev(x), dev(ids), dev(w), ws=ws)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).cpu()[0]) == 1
+    ref = moe_oracle(E, H, I, x.astype(np.float64), ids, w, weights=wts)
+    assert norm_err(out.cpu().numpy(), ref["out"], ref["den"]) <= TOL_FP32
+
+
+def test_ffn_deterministic(pool_160):
+    x, ids, w = _route_oracle(W3)
+    a = q.moe_expert_ffn_int4(pool_160, dev(x), dev(ids), dev(w)).cpu().numpy()
+    b = q.moe_expert_ffn_int4(pool_160, dev(x), dev(ids), dev(w)).cpu().numpy()
+    assert np.array_equal(a, b)
