@@ -1,0 +1,458 @@
+"""Benchmark of the int4-gs64 MoE decode hot path on GB300.
+
+Default workload (one step): the MoE decode micro-batch of 8 tokens, hidden
+6144, 160 experts, expert intermediate 2048, top-8, router logits N(0,1) with
++2 on 16 seeded "hot" experts: routing (moe_route_topk), then the expert FFN
+(moe_expert_ffn_int4: grouping, fused gate+up+SiLU, down, weighted combine).
+The metric is achieved HBM bandwidth over the algorithmic bytes of a step
+(packed weights + scales of the experts the batch touches, plus activations
+in and out). Inputs are synthetic and seeded (datagen); a step rotates over
+8 seeded micro-batches, and every step reads ~0.6 GB of expert weights, far
+more than the 129 MB L2, so no step is served from L2.
+
+Also measured and reported under "rows" (not part of the step): the dense
+int4-gs64 and int8-row GEMV 14336 x 4096 (16 / 8 rotating weight copies) and
+the 1-token MoE layer H 2048 / E 256 / I 512 (8 rotating routings).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+N > 1 runs N independent replicas under torchrun (the path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "int4-gs64 MoE expert GEMV HBM GB/s and % of 8 TB/s; µs/decode-token layer"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+EXPERT_BYTES = lambda H, I: 3 * H * I // 2 + 3 * H * I // 64 * 4  # noqa: E731
+W3 = dict(H=6144, E=160, I=2048, k=8, T=8, hot=16)
+W2 = dict(H=2048, E=256, I=512, k=8, T=1, hot=0)
+ROTATE = 8
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ workload
+
+def w3_batches(wl, n):
+    """n seeded micro-batches: x, logits, and the oracle-independent union size."""
+    import datagen
+    out = []
+    for b in range(n):
+        x, logits = datagen.moe_inputs(wl["T"], wl["E"], wl["H"], hot=wl["hot"],
+                                       token_start=b * wl["T"])
+        top = np.argsort(-logits, axis=1, kind="stable")[:, : wl["k"]]
+        out.append(dict(x=x, logits=logits, U=len(np.unique(top))))
+    return out
+
+
+def step_bytes(wl, U):
+    act = wl["T"] * wl["H"] * 4 * 2 + wl["T"] * wl["E"] * 4 + wl["T"] * wl["k"] * 8
+    return U * EXPERT_BYTES(wl["H"], wl["I"]) + act
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"qmv_clocks_{os.getpid()}.csv")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU baseline (oracle)
+
+def cpu_baseline(wl, batch, budget_s: float = 15.0):
+    """The fp64 oracle, as it stands, on the host cores: routing of the whole
+    batch, then the FFN of as many tokens as fit in ~budget_s, scaled to the
+    whole micro-batch."""
+    import datagen
+    import oracle
+    threads = os.cpu_count() or 1
+    oracle.set_threads(threads)
+    x, logits = batch["x"], batch["logits"]
+    t0 = time.perf_counter()
+    ids, w = oracle.route_topk(logits, wl["k"])
+    t_route = time.perf_counter() - t0
+    n_tok, t_ffn = 0, 0.0
+    while n_tok < wl["T"] and (n_tok == 0 or t_ffn * (n_tok + 1) / n_tok < budget_s):
+        t = n_tok
+        touched = np.unique(ids[t])
+        sub = datagen.moe_weights(wl["E"], wl["H"], wl["I"], experts=touched)
+        pos = {int(e): i for i, e in enumerate(touched)}
+        mids = np.array([[pos[int(e)] for e in ids[t]]], np.int32)
+        t1 = time.perf_counter()
+        oracle.moe_ffn(sub, x[t:t + 1].astype(np.float64), mids, w[t:t + 1].astype(np.float32))
+        t_ffn += time.perf_counter() - t1
+        n_tok += 1
+    t_step = t_route + t_ffn * wl["T"] / n_tok
+    return dict(t_step=t_step, cores=oracle.get_threads(),
+                sample=f"routing of all {wl['T']} tokens + expert FFN of {n_tok} of {wl['T']} "
+                       f"tokens (8 experts each), scaled to the micro-batch")
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import datagen  # noqa: F401
+    import oracle  # noqa: F401
+    wl = W3
+    batches = w3_batches(wl, 1)
+    per = []
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state: untimed warm-up steps are skipped
+    for s in range(args.steps):
+        r = cpu_baseline(wl, batches[0], budget_s=max(2.0, 60.0 / max(args.steps, 1)))
+        per.append(r)
+    t = statistics.mean(r["t_step"] for r in per)
+    B = step_bytes(wl, batches[0]["U"])
+    value = B / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded datagen)",
+        "config": {"workload": "MoE decode H6144 E160 I2048 top8, 8 tokens, 16 hot experts",
+                   "global_batch": wl["T"], "parallelism": "none (host oracle)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": per[0]["cores"],
+                         "kind": "oracle", "sample": per[0]["sample"]},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ GPU timing helpers
+
+def graph_of(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # warm (also binds lazily-loaded state before capture)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    return g
+
+
+def time_graphs(graphs, iters, stream):
+    import torch
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        s.record(stream)
+        for i in range(iters):
+            graphs[i % len(graphs)].replay()
+        e.record(stream)
+    e.synchronize()
+    return s.elapsed_time(e) * 1e-3 / iters
+
+
+def load_traffic(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if it still matches the source."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))[kernel]
+    except Exception:
+        return None
+    h = hashlib.sha256()
+    for f in sorted(d.get("sources", [])):
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return d["bytes_per_launch"] if h.hexdigest() == d.get("sha256") else None
+
+
+# ------------------------------------------------------------------ ours
+
+def run_ours(args):
+    import torch
+    import datagen
+    import int4_group_quantized_gs64_gb300 as q
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q.build()
+    q.lib()
+    stream = torch.cuda.Stream(device=dev)
+    wl = W3
+
+    # ---- workload: all 160 experts resident (3.4 GB), 8 rotating micro-batches
+    wts = datagen.moe_weights(wl["E"], wl["H"], wl["I"])
+    m = q.MoeInt4Weights.from_numpy(wts, dev)
+    del wts
+    batches = w3_batches(wl, ROTATE)
+    T, k = wl["T"], wl["k"]
+    xs = [torch.from_numpy(b["x"]).to(dev) for b in batches]
+    ls = [torch.from_numpy(b["logits"]).to(dev) for b in batches]
+    ids = [torch.empty((T, k), dtype=torch.int32, device=dev) for _ in batches]
+    wv = [torch.empty((T, k), dtype=torch.float32, device=dev) for _ in batches]
+    outs = [torch.empty((T, wl["H"]), dtype=torch.float32, device=dev) for _ in batches]
+    wsb = q.moe_workspace_bytes(m, T, k)
+    wss = [torch.empty(wsb, dtype=torch.uint8, device=dev) for _ in batches]
+    B_mean = statistics.mean(step_bytes(wl, b["U"]) for b in batches)
+    U_mean = statistics.mean(b["U"] for b in batches)
+
+    def step(i):
+        def f():
+            q.moe_route_topk(ls[i], k, ids=ids[i], w=wv[i], stream=stream)
+            q.moe_expert_ffn_int4(m, xs[i], ids[i], wv[i], out=outs[i], ws=wss[i], stream=stream)
+        return f
+
+    graphs = [graph_of(step(i), stream) for i in range(ROTATE)]
+    launches_per_step = 5  # route, group+split, gate+up, down, combine
+
+    # ---- warm-up, then a short untimed soak so the clock sampler sees the load
+    clocks = ClockSampler(local)
+    time_graphs(graphs, max(args.warmup, 3), stream)
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.5:
+        time_graphs(graphs, 64, stream)
+
+    # ---- timed region: K steps, barrier + synchronize on both sides
+    if ws_n > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_step = time_graphs(graphs, args.steps, stream)
+    torch.cuda.synchronize()
+    if ws_n > 1:
+        tt = torch.tensor([t_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step = float(tt.item())
+        dist.barrier()
+    clk = clocks.stop()
+
+    # ---- dominant kernel (gate+up) alone, CUDA events on the launching stream
+    ws0 = wss[0]
+    with torch.cuda.stream(stream):
+        q.moe_route_topk(ls[0], k, ids=ids[0], w=wv[0], stream=stream)
+        q.moe_ffn_prepare(m, xs[0], ids[0], ws0, stream=stream)
+    kt = []
+    for r in range(20):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            q.moe_ffn_gate_up(m, T, k, ws0, stream=stream)
+            ev1.record(stream)
+            q.moe_ffn_down(m, T, k, ws0, stream=stream)  # keeps L2 honest between repeats
+        ev1.synchronize()
+        if r >= 3:
+            kt.append(ev0.elapsed_time(ev1) * 1e-3)
+    t_gu = statistics.mean(kt)
+    gu_bytes = batches[0]["U"] * (2 * wl["I"] * wl["H"] // 2 + 2 * wl["I"] * wl["H"] // 64 * 4) \
+        + T * wl["H"] * 4 + T * k * wl["I"] * 4
+    peak, peak_kind = peaks()
+    roofline = {"bound": "hbm", "kernel": "k_gate_up", "achieved": gu_bytes / t_gu / 1e9,
+                "peak": peak, "unit": "GB/s", "frac": gu_bytes / t_gu / 1e9 / peak,
+                "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "traffic": load_traffic("k_gate_up"),
+                "bytes_per_launch": gu_bytes, "us_per_launch": t_gu * 1e6}
+
+    # ---- end to end through the public API with pinned host buffers
+    hx = [torch.from_numpy(b["x"]).pin_memory() for b in batches]
+    hl = [torch.from_numpy(b["logits"]).pin_memory() for b in batches]
+    ho = [torch.empty((T, wl["H"]), dtype=torch.float32).pin_memory() for _ in batches]
+    h2d = hx[0].numel() * 4 + hl[0].numel() * 4
+    d2h = ho[0].numel() * 4
+    for i in range(3):
+        with torch.cuda.stream(stream):
+            xs[i].copy_(hx[i], non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(args.steps, 10)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for s in range(n_e2e):
+            i = s % ROTATE
+            xs[i].copy_(hx[i], non_blocking=True)
+            ls[i].copy_(hl[i], non_blocking=True)
+            q.moe_route_topk(ls[i], k, ids=ids[i], w=wv[i], stream=stream)
+            q.moe_expert_ffn_int4(m, xs[i], ids[i], wv[i], out=outs[i], ws=wss[i], stream=stream)
+            ho[i].copy_(outs[i], non_blocking=True)
+        e1.record(stream)
+    e1.synchronize()
+    t_e2e = e0.elapsed_time(e1) * 1e-3 / n_e2e
+
+    rows = measure_rows(q, datagen, dev, stream, peak) if rank == 0 and not args.quick else {}
+
+    if rank != 0:
+        return 0
+    value = ws_n * B_mean / t_step / 1e9
+    cpu = None
+    if ws_n == 1 and not args.no_cpu:
+        cb = cpu_baseline(wl, batches[0])
+        cpu = {"value": step_bytes(wl, batches[0]["U"]) / cb["t_step"] / 1e9, "unit": "GB/s",
+               "cores": cb["cores"], "kind": "oracle", "sample": cb["sample"]}
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp16x2-split MMA, fp32 accumulate",
+        "data": "synthetic (seeded datagen, no trained weights)",
+        "config": {"workload": "MoE decode H6144 E160 I2048 top8, 8 tokens, 16 hot experts",
+                   "global_batch": T * ws_n, "seq_len": 1, "parallelism": f"replicas x{ws_n}",
+                   "experts_touched_mean": U_mean, "bytes_per_step_mean": B_mean,
+                   "l2": "inputs larger than L2 (~0.6 GB of weights per step vs 129 MB L2); "
+                         "8 rotating micro-batches",
+                   "timing": "CUDA graph replay of K steps between CUDA events"},
+        "pct_of_8TBs": value / ws_n / NOMINAL_HBM_GBS * 100,
+        "us_per_layer": t_step * 1e6, "us_per_decode_token_layer": t_step * 1e6 / T,
+        "token_eq_per_s": ws_n * T / t_step,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": ws_n * B_mean / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "us_per_step": t_e2e * 1e6},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "rows": rows,
+    }
+    print(json.dumps(line))
+    if ws_n > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_rows(q, datagen, dev, stream, peak):
+    """Other rows of the hot path, each with its own roofline fraction."""
+    import torch
+    rows = {}
+    # dense int4-gs64 and int8-row GEMV, 14336 x 4096, one token
+    N, K = 14336, 4096
+    wq, sc, x = datagen.dense_int4(N, K, 1)
+    C = 16
+    wqs = [torch.from_numpy(wq).to(dev) for _ in range(C)]
+    scs = [torch.from_numpy(sc).to(dev) for _ in range(C)]
+    xd = torch.from_numpy(x).to(dev)
+    y = torch.empty((1, N), device=dev)
+    wsd = torch.empty(q.qmv_gemv_workspace_bytes(K, 1), dtype=torch.uint8, device=dev)
+    gs = [graph_of(lambda i=i: q.qmv_int4_gs(wqs[i], scs[i], xd, y=y, ws=wsd, stream=stream), stream)
+          for i in range(C)]
+    time_graphs(gs, 32, stream)
+    t = time_graphs(gs, 256, stream)
+    Bq = wq.nbytes + sc.nbytes + x.nbytes + N * 4
+    rows["int4_gemv_14336x4096"] = {"us": t * 1e6, "GBs": Bq / t / 1e9, "frac": Bq / t / 1e9 / peak,
+                                    "bytes": Bq, "launches_per_call": 2}
+    del wqs, scs, gs
+    w8, r8, x8 = datagen.dense_int8(N, K, 1)
+    C8 = 8
+    w8s = [torch.from_numpy(w8).to(dev) for _ in range(C8)]
+    r8d = torch.from_numpy(r8).to(dev)
+    gs = [graph_of(lambda i=i: q.qmv_int8_row(w8s[i], r8d, xd, y=y, ws=wsd, stream=stream), stream)
+          for i in range(C8)]
+    time_graphs(gs, 32, stream)
+    t = time_graphs(gs, 256, stream)
+    B8 = w8.nbytes + r8.nbytes + x.nbytes + N * 4
+    rows["int8_gemv_14336x4096"] = {"us": t * 1e6, "GBs": B8 / t / 1e9, "frac": B8 / t / 1e9 / peak,
+                                    "bytes": B8, "launches_per_call": 2}
+    del w8s, gs
+    # MoE decode, 1 token, H 2048 / E 256 / I 512 (pool 453 MB)
+    wl = W2
+    wts = datagen.moe_weights(wl["E"], wl["H"], wl["I"])
+    m2 = q.MoeInt4Weights.from_numpy(wts, dev)
+    del wts
+    bs = w3_batches(wl, ROTATE)
+    x2 = [torch.from_numpy(b["x"]).to(dev) for b in bs]
+    l2 = [torch.from_numpy(b["logits"]).to(dev) for b in bs]
+    i2 = [torch.empty((1, 8), dtype=torch.int32, device=dev) for _ in bs]
+    w2 = [torch.empty((1, 8), dtype=torch.float32, device=dev) for _ in bs]
+    o2 = [torch.empty((1, wl["H"]), device=dev) for _ in bs]
+    ws2 = [torch.empty(q.moe_workspace_bytes(m2, 1, 8), dtype=torch.uint8, device=dev) for _ in bs]
+
+    def f2(i):
+        return lambda: (q.moe_route_topk(l2[i], 8, ids=i2[i], w=w2[i], stream=stream),
+                        q.moe_expert_ffn_int4(m2, x2[i], i2[i], w2[i], out=o2[i], ws=ws2[i],
+                                              stream=stream))
+    gs = [graph_of(f2(i), stream) for i in range(ROTATE)]
+    time_graphs(gs, 32, stream)
+    t = time_graphs(gs, 256, stream)
+    B2 = statistics.mean(step_bytes(wl, b["U"]) for b in bs)
+    rows["moe_decode_h2048_e256_i512_1tok"] = {"us": t * 1e6, "GBs": B2 / t / 1e9,
+                                               "frac": B2 / t / 1e9 / peak, "bytes": B2,
+                                               "launches_per_call": 5}
+    return rows
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="skip the extra rows")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -62,6 +62,12 @@ const char *qmv_status_str(int status);
 
 /* ---------------------------------------------------------------- GEMV */
 
+/* Scratch needed by qmv_int4_gs / qmv_int8_row for S tokens of length K, in
+ * bytes (a multiple of 256; 0 for unsupported sizes). The activations are
+ * converted there into fp16 hi/lo fragments with one power-of-two factor per
+ * 64-wide group before the weights are streamed. */
+size_t qmv_gemv_workspace_bytes(int K, int S);
+
 /* Dense int4 grouped-scale GEMV (colibri PR #418, commits "opt-in Vulkan
  * int4/int8 quantized GEMV" and "grouped scales in the Vulkan kernels"):
  *     y[s][i] = sum_g scales[i][g] * sum_{k in group g} (nibble(i,k) - 8) * x[s][k]
@@ -69,18 +75,21 @@ const char *qmv_status_str(int status);
  *   scales  [N][K/gs] fp32, 4-byte aligned
  *   x       [S][K] fp32, 4-byte aligned
  *   y       [S][N] fp32 (written, fp32-accumulated)
+ *   ws      device scratch of at least qmv_gemv_workspace_bytes(K, S) bytes,
+ *           256-byte aligned, not shared with a concurrent call
  *   gs must be 64; K a multiple of 64; 1 <= N, 1 <= S, K <= 65536.
  * Errors: QMV_EINVAL (null pointer, gs != 64, N or S < 1), QMV_ESHAPE (K),
- *         QMV_EALIGN, QMV_ECUDA. */
+ *         QMV_EALIGN, QMV_EWORKSPACE, QMV_ECUDA. */
 int qmv_int4_gs(const uint8_t *wq, const float *scales, int N, int K, int gs, const float *x,
-                float *y, int S, qmv_stream_t stream);
+                float *y, int S, void *ws, size_t ws_bytes, qmv_stream_t stream);
 
 /* Dense int8 per-row-scale GEMV (same commit, fmt 1):
  *     y[s][i] = row_scale[i] * sum_k w[i][k] * x[s][k]
- *   w [N][K] int8 (16-byte aligned), row_scale [N] fp32, x [S][K] fp32, y [S][N] fp32.
- *   K a multiple of 64, K <= 65536; N, S >= 1. Errors as qmv_int4_gs. */
+ *   w [N][K] int8 (16-byte aligned), row_scale [N] fp32, x [S][K] fp32, y [S][N] fp32,
+ *   ws as for qmv_int4_gs. K a multiple of 64, K <= 65536; N, S >= 1.
+ *   Errors as qmv_int4_gs. */
 int qmv_int8_row(const int8_t *w, const float *row_scale, int N, int K, const float *x,
-                 float *y, int S, qmv_stream_t stream);
+                 float *y, int S, void *ws, size_t ws_bytes, qmv_stream_t stream);
 
 /* ---------------------------------------------------------------- MoE */
 
@@ -164,6 +173,26 @@ size_t moe_workspace_bytes(const qmv_moe_int4 *m, int T, int k);
 int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids,
                         const float *w, int k, float *out, void *ws, size_t ws_bytes,
                         qmv_stream_t stream);
+
+/* The four phases of moe_expert_ffn_int4, for callers that interleave other
+ * work or time the phases (the pages split their expert group the same way
+ * into issue and take). All four take the same workspace; each phase reads
+ * what the previous one left there, so they must run in this order on one
+ * stream, with T and k unchanged:
+ *   moe_ffn_prepare  clears the status word, groups the pairs (moe_group) and
+ *                    converts x into fp16 hi/lo cells with per-group factors;
+ *   moe_ffn_gate_up  h = SiLU(gate x) * up x for every served pair, kept in the
+ *                    workspace both as fp32 and as cells for the down pass;
+ *   moe_ffn_down     y = down h per pair, in the workspace;
+ *   moe_ffn_combine  out[t] = sum_j w[t][j] * y[t*k + j], slot order. */
+int moe_ffn_prepare(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids, int k,
+                    void *ws, size_t ws_bytes, qmv_stream_t stream);
+int moe_ffn_gate_up(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
+                    qmv_stream_t stream);
+int moe_ffn_down(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
+                 qmv_stream_t stream);
+int moe_ffn_combine(const qmv_moe_int4 *m, const int32_t *ids, const float *w, int T, int k,
+                    float *out, void *ws, size_t ws_bytes, qmv_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -59,8 +59,9 @@ def lib():
         sig = {
             "qmv_version": ([], i32),
             "qmv_status_str": ([i32], ctypes.c_char_p),
-            "qmv_int4_gs": ([vp, vp, i32, i32, i32, vp, vp, i32, vp], i32),
-            "qmv_int8_row": ([vp, vp, i32, i32, vp, vp, i32, vp], i32),
+            "qmv_gemv_workspace_bytes": ([i32, i32], sz),
+            "qmv_int4_gs": ([vp, vp, i32, i32, i32, vp, vp, i32, vp, sz, vp], i32),
+            "qmv_int8_row": ([vp, vp, i32, i32, vp, vp, i32, vp, sz, vp], i32),
             "moe_route_topk": ([vp, i32, i32, i32, vp, vp, vp], i32),
             "moe_group": ([vp, i32, i32, i32, vp, vp, vp, vp, vp, vp], i32),
             "moe_gate_up_silu": ([P, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp], i32),
@@ -68,6 +69,10 @@ def lib():
             "moe_combine": ([vp, vp, vp, i32, i32, i32, i32, vp, vp], i32),
             "moe_workspace_bytes": ([P, i32, i32], sz),
             "moe_expert_ffn_int4": ([P, vp, i32, vp, vp, i32, vp, vp, sz, vp], i32),
+            "moe_ffn_prepare": ([P, vp, i32, vp, i32, vp, sz, vp], i32),
+            "moe_ffn_gate_up": ([P, i32, i32, vp, sz, vp], i32),
+            "moe_ffn_down": ([P, i32, i32, vp, sz, vp], i32),
+            "moe_ffn_combine": ([P, vp, vp, i32, i32, vp, vp, sz, vp], i32),
             "moe_prefill_workspace_bytes": ([P, i32, i32], sz),
             "moe_expert_ffn_int4_prefill": ([P, vp, i32, vp, vp, i32, vp, vp, sz, vp], i32),
         }
@@ -111,7 +116,11 @@ def _need(t, dtype, name):
 
 # ------------------------------------------------------------------ GEMV
 
-def qmv_int4_gs(wq, scales, x, y=None, gs: int = 64, stream=None):
+def qmv_gemv_workspace_bytes(K: int, S: int) -> int:
+    return int(lib().qmv_gemv_workspace_bytes(K, S))
+
+
+def qmv_int4_gs(wq, scales, x, y=None, gs: int = 64, ws=None, stream=None):
     """y[S][N] = int4-gs64 W[N][K] . x[S][K]  (wq uint8 [N][K/2], scales fp32 [N][K/64])."""
     import torch
     _need(wq, torch.uint8, "wq"); _need(scales, torch.float32, "scales"); _need(x, torch.float32, "x")
@@ -121,12 +130,14 @@ def qmv_int4_gs(wq, scales, x, y=None, gs: int = 64, stream=None):
     if y is None:
         y = torch.empty((S, N), dtype=torch.float32, device=x.device)
     _need(y, torch.float32, "y")
+    if ws is None:
+        ws = _workspace(qmv_gemv_workspace_bytes(K, S), x.device)
     _check("qmv_int4_gs", lib().qmv_int4_gs(_ptr(wq), _ptr(scales), N, K, gs, _ptr(x2), _ptr(y), S,
-                                            _stream(stream)))
+                                            _ptr(ws), ws.numel(), _stream(stream)))
     return y
 
 
-def qmv_int8_row(w, row_scale, x, y=None, stream=None):
+def qmv_int8_row(w, row_scale, x, y=None, ws=None, stream=None):
     """y[S][N] = row_scale[N] * (w[N][K] . x[S][K])  (w int8)."""
     import torch
     _need(w, torch.int8, "w"); _need(row_scale, torch.float32, "row_scale"); _need(x, torch.float32, "x")
@@ -136,8 +147,10 @@ def qmv_int8_row(w, row_scale, x, y=None, stream=None):
     if y is None:
         y = torch.empty((S, N), dtype=torch.float32, device=x.device)
     _need(y, torch.float32, "y")
+    if ws is None:
+        ws = _workspace(qmv_gemv_workspace_bytes(K, S), x.device)
     _check("qmv_int8_row", lib().qmv_int8_row(_ptr(w), _ptr(row_scale), N, K, _ptr(x2), _ptr(y), S,
-                                              _stream(stream)))
+                                              _ptr(ws), ws.numel(), _stream(stream)))
     return y
 
 
@@ -260,6 +273,28 @@ def moe_expert_ffn_int4(m: MoeInt4Weights, x, ids, w, out=None, ws=None, stream=
     _check("moe_expert_ffn_int4", lib().moe_expert_ffn_int4(
         m.desc, _ptr(x), T, _ptr(ids), _ptr(w), k, _ptr(out), _ptr(ws), ws.numel(),
         _stream(stream)))
+    return out
+
+
+def moe_ffn_prepare(m: MoeInt4Weights, x, ids, ws, stream=None):
+    T, k = ids.shape
+    _check("moe_ffn_prepare", lib().moe_ffn_prepare(m.desc, _ptr(x), T, _ptr(ids), k, _ptr(ws),
+                                                    ws.numel(), _stream(stream)))
+
+
+def moe_ffn_gate_up(m: MoeInt4Weights, T: int, k: int, ws, stream=None):
+    _check("moe_ffn_gate_up", lib().moe_ffn_gate_up(m.desc, T, k, _ptr(ws), ws.numel(),
+                                                    _stream(stream)))
+
+
+def moe_ffn_down(m: MoeInt4Weights, T: int, k: int, ws, stream=None):
+    _check("moe_ffn_down", lib().moe_ffn_down(m.desc, T, k, _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_ffn_combine(m: MoeInt4Weights, ids, w, out, ws, stream=None):
+    T, k = ids.shape
+    _check("moe_ffn_combine", lib().moe_ffn_combine(m.desc, _ptr(ids), _ptr(w), T, k, _ptr(out),
+                                                    _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 

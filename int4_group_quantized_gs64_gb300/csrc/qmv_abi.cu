@@ -44,6 +44,21 @@ int check_group_args(const int32_t *offsets, const int32_t *list, const int32_t 
     return QMV_OK;
 }
 
+int ffn_check(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
+                     qmv::MoeWorkspace &L) {
+    int r = check_moe(m);
+    if (r) return r;
+    if (T < 1 || k < 1 || k > m->E || (int64_t)T * k > kMaxPairs) return QMV_EINVAL;
+    L = qmv::moe_ws_layout(m->E, m->H, m->I, T, k);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return QMV_EWORKSPACE;
+    return QMV_OK;
+}
+
+template <class T>
+T *at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
 }  // namespace
 
 extern "C" {
@@ -63,22 +78,29 @@ const char *qmv_status_str(int status) {
     }
 }
 
+size_t qmv_gemv_workspace_bytes(int K, int S) {
+    if (K < 64 || K % 64 || K > kMaxK || S < 1) return 0;
+    return (qmv::dense_scratch_bytes(K, S) + 255) & ~(size_t)255;
+}
+
 int qmv_int4_gs(const uint8_t *wq, const float *scales, int N, int K, int gs, const float *x,
-                float *y, int S, qmv_stream_t stream) {
+                float *y, int S, void *ws, size_t ws_bytes, qmv_stream_t stream) {
     if (!wq || !scales || !x || !y || N < 1 || S < 1 || gs != 64) return QMV_EINVAL;
     if (K < 64 || K % 64 || K > kMaxK) return QMV_ESHAPE;
     if (!aligned(wq, 16) || !aligned(scales, 4) || !aligned(x, 4) || !aligned(y, 4))
         return QMV_EALIGN;
-    return from_cuda(qmv::launch_dense_int4(wq, scales, N, K, x, y, S, cs(stream)));
+    if (!ws || !aligned(ws, 256) || ws_bytes < qmv_gemv_workspace_bytes(K, S)) return QMV_EWORKSPACE;
+    return from_cuda(qmv::launch_dense_int4(wq, scales, N, K, x, y, S, ws, cs(stream)));
 }
 
 int qmv_int8_row(const int8_t *w, const float *row_scale, int N, int K, const float *x, float *y,
-                 int S, qmv_stream_t stream) {
+                 int S, void *ws, size_t ws_bytes, qmv_stream_t stream) {
     if (!w || !row_scale || !x || !y || N < 1 || S < 1) return QMV_EINVAL;
     if (K < 64 || K % 64 || K > kMaxK) return QMV_ESHAPE;
     if (!aligned(w, 16) || !aligned(row_scale, 4) || !aligned(x, 4) || !aligned(y, 4))
         return QMV_EALIGN;
-    return from_cuda(qmv::launch_dense_int8(w, row_scale, N, K, x, y, S, cs(stream)));
+    if (!ws || !aligned(ws, 256) || ws_bytes < qmv_gemv_workspace_bytes(K, S)) return QMV_EWORKSPACE;
+    return from_cuda(qmv::launch_dense_int8(w, row_scale, N, K, x, y, S, ws, cs(stream)));
 }
 
 int moe_route_topk(const float *logits, int T, int E, int k, int32_t *ids, float *w,
@@ -101,6 +123,11 @@ int moe_group(const int32_t *ids, int T, int k, int E, int32_t *offsets, int32_t
                                        cs(stream)));
 }
 
+size_t moe_workspace_bytes(const qmv_moe_int4 *m, int T, int k) {
+    if (check_moe(m) || T < 0 || k < 1 || (int64_t)T * k > kMaxPairs) return 0;
+    return qmv::moe_ws_layout(m->E, m->H, m->I, T, k).total;
+}
+
 int moe_gate_up_silu(const qmv_moe_int4 *m, const float *x, int T, int k, const int32_t *offsets,
                      const int32_t *list, const int32_t *uexp, const int32_t *n_used, float *h,
                      void *ws, size_t ws_bytes, qmv_stream_t stream) {
@@ -114,11 +141,14 @@ int moe_gate_up_silu(const qmv_moe_int4 *m, const float *x, int T, int k, const 
     const qmv::MoeWorkspace L = qmv::moe_ws_layout(m->E, m->H, m->I, T, k);
     if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return QMV_EWORKSPACE;
     char *b = static_cast<char *>(ws);
+    int32_t *pass_ofs = reinterpret_cast<int32_t *>(b + L.pass_ofs);
     float *xfac = reinterpret_cast<float *>(b + L.xfac);
-    cudaError_t e = qmv::launch_split(x, T, m->H, b + L.xcells, xfac, cs(stream));
+    const cudaStream_t st = cs(stream);
+    cudaError_t e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
+    if (e == cudaSuccess) e = qmv::launch_split(x, T, m->H, b + L.xcells, xfac, st);
     if (e == cudaSuccess)
-        e = qmv::launch_gate_up(dims(m), b + L.xcells, xfac, T, k, offsets, list, uexp, n_used, h,
-                                cs(stream));
+        e = qmv::launch_gate_up(dims(m), b + L.xcells, xfac, k, offsets, list, uexp, n_used,
+                                pass_ofs, h, b + L.hcells, reinterpret_cast<float *>(b + L.hfac), st);
     return from_cuda(e);
 }
 
@@ -135,11 +165,14 @@ int moe_down(const qmv_moe_int4 *m, const float *h, int T, int k, const int32_t 
     const qmv::MoeWorkspace L = qmv::moe_ws_layout(m->E, m->H, m->I, T, k);
     if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return QMV_EWORKSPACE;
     char *b = static_cast<char *>(ws);
+    int32_t *pass_ofs = reinterpret_cast<int32_t *>(b + L.pass_ofs);
     float *hfac = reinterpret_cast<float *>(b + L.hfac);
-    cudaError_t e = qmv::launch_split(h, T * k, m->I, b + L.hcells, hfac, cs(stream));
+    const cudaStream_t st = cs(stream);
+    cudaError_t e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
+    if (e == cudaSuccess) e = qmv::launch_split(h, T * k, m->I, b + L.hcells, hfac, st);
     if (e == cudaSuccess)
-        e = qmv::launch_down(dims(m), b + L.hcells, hfac, T, k, offsets, list, uexp, n_used, y,
-                             cs(stream));
+        e = qmv::launch_down(dims(m), b + L.hcells, hfac, offsets, list, uexp, n_used, pass_ofs, y,
+                             st);
     return from_cuda(e);
 }
 
@@ -149,47 +182,74 @@ int moe_combine(const float *y, const int32_t *ids, const float *w, int T, int k
     if (T == 0) return QMV_OK;
     if (!y || !ids || !w || !out) return QMV_EINVAL;
     if (!aligned(y, 4) || !aligned(ids, 4) || !aligned(w, 4) || !aligned(out, 4)) return QMV_EALIGN;
-    return from_cuda(qmv::launch_combine(y, ids, w, T, k, E, H, out, cs(stream)));
+    return from_cuda(qmv::launch_combine(y, ids, w, T, k, E, H, out, cs(stream), false));
 }
 
-size_t moe_workspace_bytes(const qmv_moe_int4 *m, int T, int k) {
-    if (check_moe(m) || T < 0 || k < 1 || (int64_t)T * k > kMaxPairs) return 0;
-    return qmv::moe_ws_layout(m->E, m->H, m->I, T, k).total;
+int moe_ffn_prepare(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids, int k,
+                    void *ws, size_t ws_bytes, qmv_stream_t stream) {
+    qmv::MoeWorkspace L;
+    int r = ffn_check(m, T, k, ws, ws_bytes, L);
+    if (r) return r;
+    if (!x || !ids) return QMV_EINVAL;
+    if (!aligned(x, 4) || !aligned(ids, 4)) return QMV_EALIGN;
+    const cudaStream_t st = cs(stream);
+    cudaError_t e = cudaMemsetAsync(at<int32_t>(ws, L.status), 0, sizeof(int32_t), st);
+    if (e == cudaSuccess)
+        e = qmv::launch_group_split(ids, T, k, m->E, at<int32_t>(ws, L.offsets),
+                                    at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
+                                    at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs),
+                                    at<int32_t>(ws, L.status), x, m->H, at<void>(ws, L.xcells),
+                                    at<float>(ws, L.xfac), st);
+    return from_cuda(e);
+}
+
+int moe_ffn_gate_up(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
+                    qmv_stream_t stream) {
+    qmv::MoeWorkspace L;
+    int r = ffn_check(m, T, k, ws, ws_bytes, L);
+    if (r) return r;
+    return from_cuda(qmv::launch_gate_up(
+        dims(m), at<void>(ws, L.xcells), at<float>(ws, L.xfac), k, at<int32_t>(ws, L.offsets),
+        at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp), at<int32_t>(ws, L.n_used),
+        at<int32_t>(ws, L.pass_ofs), at<float>(ws, L.h), at<void>(ws, L.hcells),
+        at<float>(ws, L.hfac), cs(stream)));
+}
+
+int moe_ffn_down(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
+                 qmv_stream_t stream) {
+    qmv::MoeWorkspace L;
+    int r = ffn_check(m, T, k, ws, ws_bytes, L);
+    if (r) return r;
+    return from_cuda(qmv::launch_down(dims(m), at<void>(ws, L.hcells), at<float>(ws, L.hfac),
+                                      at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list),
+                                      at<int32_t>(ws, L.uexp), at<int32_t>(ws, L.n_used),
+                                      at<int32_t>(ws, L.pass_ofs), at<float>(ws, L.y), cs(stream)));
+}
+
+int moe_ffn_combine(const qmv_moe_int4 *m, const int32_t *ids, const float *w, int T, int k,
+                    float *out, void *ws, size_t ws_bytes, qmv_stream_t stream) {
+    qmv::MoeWorkspace L;
+    int r = ffn_check(m, T, k, ws, ws_bytes, L);
+    if (r) return r;
+    if (!ids || !w || !out) return QMV_EINVAL;
+    if (!aligned(ids, 4) || !aligned(w, 4) || !aligned(out, 4)) return QMV_EALIGN;
+    return from_cuda(qmv::launch_combine(at<float>(ws, L.y), ids, w, T, k, m->E, m->H, out,
+                                         cs(stream), true));
 }
 
 int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids,
                         const float *w, int k, float *out, void *ws, size_t ws_bytes,
                         qmv_stream_t stream) {
-    int r = check_moe(m);
+    if (T == 0 && !check_moe(m) && k >= 1 && k <= m->E) return QMV_OK;
+    qmv::MoeWorkspace L;
+    int r = ffn_check(m, T, k, ws, ws_bytes, L);
     if (r) return r;
-    if (T < 0 || k < 1 || k > m->E || (int64_t)T * k > kMaxPairs) return QMV_EINVAL;
-    if (T == 0) return QMV_OK;
     if (!x || !ids || !w || !out) return QMV_EINVAL;
     if (!aligned(x, 4) || !aligned(ids, 4) || !aligned(w, 4) || !aligned(out, 4)) return QMV_EALIGN;
-    const qmv::MoeWorkspace L = qmv::moe_ws_layout(m->E, m->H, m->I, T, k);
-    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return QMV_EWORKSPACE;
-    char *b = static_cast<char *>(ws);
-    int32_t *status = reinterpret_cast<int32_t *>(b + L.status);
-    int32_t *offsets = reinterpret_cast<int32_t *>(b + L.offsets);
-    int32_t *list = reinterpret_cast<int32_t *>(b + L.list);
-    int32_t *uexp = reinterpret_cast<int32_t *>(b + L.uexp);
-    int32_t *n_used = reinterpret_cast<int32_t *>(b + L.n_used);
-    float *xfac = reinterpret_cast<float *>(b + L.xfac);
-    float *h = reinterpret_cast<float *>(b + L.h);
-    float *hfac = reinterpret_cast<float *>(b + L.hfac);
-    float *y = reinterpret_cast<float *>(b + L.y);
-    const cudaStream_t st = cs(stream);
-    const qmv::MoeDims d = dims(m);
-    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
-    if (e == cudaSuccess) e = qmv::launch_group(ids, T * k, m->E, offsets, list, uexp, n_used, status, st);
-    if (e == cudaSuccess) e = qmv::launch_split(x, T, m->H, b + L.xcells, xfac, st);
-    if (e == cudaSuccess)
-        e = qmv::launch_gate_up(d, b + L.xcells, xfac, T, k, offsets, list, uexp, n_used, h, st);
-    if (e == cudaSuccess) e = qmv::launch_split(h, T * k, m->I, b + L.hcells, hfac, st);
-    if (e == cudaSuccess)
-        e = qmv::launch_down(d, b + L.hcells, hfac, T, k, offsets, list, uexp, n_used, y, st);
-    if (e == cudaSuccess) e = qmv::launch_combine(y, ids, w, T, k, m->E, m->H, out, st);
-    return from_cuda(e);
+    if ((r = moe_ffn_prepare(m, x, T, ids, k, ws, ws_bytes, stream))) return r;
+    if ((r = moe_ffn_gate_up(m, T, k, ws, ws_bytes, stream))) return r;
+    if ((r = moe_ffn_down(m, T, k, ws, ws_bytes, stream))) return r;
+    return moe_ffn_combine(m, ids, w, T, k, out, ws, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -8,11 +8,12 @@
 
 namespace qmv {
 
-// Dense GEMV, any S (passes of up to 16 tokens).
+// Dense GEMV, any S (passes of up to 16 tokens). scratch: dense_scratch_bytes(K, S).
+size_t dense_scratch_bytes(int K, int S);
 cudaError_t launch_dense_int4(const uint8_t *wq, const float *scales, int N, int K,
-                              const float *x, float *y, int S, cudaStream_t st);
+                              const float *x, float *y, int S, void *scratch, cudaStream_t st);
 cudaError_t launch_dense_int8(const int8_t *w, const float *row_scale, int N, int K,
-                              const float *x, float *y, int S, cudaStream_t st);
+                              const float *x, float *y, int S, void *scratch, cudaStream_t st);
 
 struct MoeDims {
     const uint8_t *gu_q;
@@ -26,20 +27,28 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids,
                          cudaStream_t st);
 cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int32_t *list,
                          int32_t *uexp, int32_t *n_used, int32_t *status, cudaStream_t st);
-// Activation rows [R][K] fp32 -> fragment cells [R][K/64][4][4] uint4 + fac[R] (2^-sigma).
+// Grouping plus the split of the T activation rows, in one launch.
+cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
+                               int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
+                               int32_t *status, const float *x, int H, void *xcells, float *xfac,
+                               cudaStream_t st);
+cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
+                          int32_t *pass_ofs, cudaStream_t st, bool pdl);
+// Activation rows [R][K] fp32 -> fragment cells [R][K/64][16] uint4 + factors [R][K/64].
 cudaError_t launch_split(const float *v, int R, int K, void *cells, float *fac, cudaStream_t st);
-cudaError_t launch_gate_up(const MoeDims &m, const void *xcells, const float *xfac, int T, int k,
+cudaError_t launch_gate_up(const MoeDims &m, const void *xcells, const float *xfac, int k,
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
-                           const int32_t *n_used, float *h, cudaStream_t st);
-cudaError_t launch_down(const MoeDims &m, const void *hcells, const float *hfac, int T, int k,
+                           const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,
+                           float *hfac, cudaStream_t st);
+cudaError_t launch_down(const MoeDims &m, const void *hcells, const float *hfac,
                         const int32_t *offsets, const int32_t *list, const int32_t *uexp,
-                        const int32_t *n_used, float *y, cudaStream_t st);
+                        const int32_t *n_used, const int32_t *pass_ofs, float *y, cudaStream_t st);
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int T, int k, int E,
-                           int H, float *out, cudaStream_t st);
+                           int H, float *out, cudaStream_t st, bool pdl);
 
-// Workspace layout of the whole decode FFN.
+// Workspace layout of the MoE entry points (256-byte aligned segments).
 struct MoeWorkspace {
-    size_t status, offsets, list, uexp, n_used, xcells, xfac, h, hcells, hfac, y, total;
+    size_t status, offsets, list, uexp, n_used, pass_ofs, xcells, xfac, h, hcells, hfac, y, total;
 };
 MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k);
 

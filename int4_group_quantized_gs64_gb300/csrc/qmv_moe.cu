@@ -15,6 +15,7 @@
 #include <limits.h>
 
 #include "qmv_internal.h"
+#include "qmv_launch.cuh"
 #include "qmv_rows.cuh"
 
 namespace qmv {
@@ -71,19 +72,52 @@ __global__ void __launch_bounds__(256)
 
 // ------------------------------------------------------------------ grouping
 
-// One CTA of 1024 threads. Counting by shared atomics, a block scan for the
-// offsets, and a single warp that fills the lists in pair order (ranks from
-// __match_any_sync), which keeps every list ascending.
-__global__ void __launch_bounds__(1024)
-    k_group(const int32_t *__restrict__ ids, int P, int E, int32_t *__restrict__ offsets,
-            int32_t *__restrict__ list, int32_t *__restrict__ uexp, int32_t *__restrict__ n_used,
-            int32_t *__restrict__ status) {
-    __shared__ int32_t cnt[1024], run[1024];
-    __shared__ int32_t warp_tot[32], warp_tot2[32];
+// Exclusive block scan of three per-thread values (blockDim.x == 1024).
+__device__ __forceinline__ void block_scan3(int a, int b, int c, int &ea, int &eb, int &ec,
+                                            int *tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int ia = a, ib = b, ic = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xFFFFFFFFu, ia, o);
+        const int y = __shfl_up_sync(0xFFFFFFFFu, ib, o);
+        const int z = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+        if (lane >= o) { ia += x; ib += y; ic += z; }
+    }
+    if (lane == 31) { tot[warp] = ia; tot[32 + warp] = ib; tot[64 + warp] = ic; }
+    __syncthreads();
+    if (warp == 0) {
+        int va = tot[lane], vb = tot[32 + lane], vc = tot[64 + lane];
+        int sa = va, sb = vb, sc = vc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xFFFFFFFFu, sa, o);
+            const int y = __shfl_up_sync(0xFFFFFFFFu, sb, o);
+            const int z = __shfl_up_sync(0xFFFFFFFFu, sc, o);
+            if (lane >= o) { sa += x; sb += y; sc += z; }
+        }
+        tot[lane] = sa - va;
+        tot[32 + lane] = sb - vb;
+        tot[64 + lane] = sc - vc;
+    }
+    __syncthreads();
+    ea = tot[warp] + ia - a;
+    eb = tot[32 + warp] + ib - b;
+    ec = tot[64 + warp] + ic - c;
+}
+
+// Grouping on one CTA of 1024 threads: counts by shared atomics; block scans
+// give the offsets, the slots of the used experts and the pass offsets (one
+// pass = up to kMaxTok pairs of one expert); a single warp then fills the
+// lists in pair order (ranks from __match_any_sync), keeping them ascending.
+__device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets,
+                          int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
+                          int32_t *status) {
+    __shared__ int32_t cnt[1024], run[1024], tot[96];
     __shared__ int bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) bad = 0;
-    for (int e = tid; e < 1024; e += blockDim.x) cnt[e] = 0;
+    cnt[tid] = 0;
     __syncthreads();
     for (int p = tid; p < P; p += blockDim.x) {
         const int e = ids[p];
@@ -91,41 +125,23 @@ __global__ void __launch_bounds__(1024)
         else atomicAdd(&cnt[e], 1);
     }
     __syncthreads();
-    // Exclusive scans over the experts: counts -> offsets, used flags -> uexp slots.
     const int c = tid < E ? cnt[tid] : 0;
     const int f = c > 0 ? 1 : 0;
-    int ic = c, ifl = f;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int a = __shfl_up_sync(0xFFFFFFFFu, ic, o);
-        const int b = __shfl_up_sync(0xFFFFFFFFu, ifl, o);
-        if (lane >= o) { ic += a; ifl += b; }
-    }
-    if (lane == 31) { warp_tot[warp] = ic; warp_tot2[warp] = ifl; }
-    __syncthreads();
-    if (warp == 0) {
-        int a = warp_tot[lane], b = warp_tot2[lane];
-        int ia = a, ib = b;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int x1 = __shfl_up_sync(0xFFFFFFFFu, ia, o);
-            const int x2 = __shfl_up_sync(0xFFFFFFFFu, ib, o);
-            if (lane >= o) { ia += x1; ib += x2; }
-        }
-        warp_tot[lane] = ia - a;   // exclusive prefix of warp totals
-        warp_tot2[lane] = ib - b;
-    }
-    __syncthreads();
-    const int excl = warp_tot[warp] + ic - c;
-    const int exflag = warp_tot2[warp] + ifl - f;
+    const int np = (c + kMaxTok - 1) / kMaxTok;
+    int ec, ef, ep;
+    block_scan3(c, f, np, ec, ef, ep, tot);
     if (tid < E) {
-        offsets[tid] = excl;
-        run[tid] = excl;
-        if (f) uexp[exflag] = tid;
+        offsets[tid] = ec;
+        run[tid] = ec;
+        if (f) {
+            uexp[ef] = tid;
+            if (pass_ofs) pass_ofs[ef] = ep;
+        }
     }
     if (tid == E - 1) {
-        offsets[E] = excl + c;
-        *n_used = exflag + f;
+        offsets[E] = ec + c;
+        *n_used = ef + f;
+        if (pass_ofs) pass_ofs[ef + f] = ep + np;
     }
     __syncthreads();
     if (warp == 0) {
@@ -146,206 +162,326 @@ __global__ void __launch_bounds__(1024)
     if (tid == 0 && bad) atomicOr(status, 1);
 }
 
-// ------------------------------------------------------------------ activation split
+// Splits activation row r (1024 threads): per 64-wide group, max |v| ->
+// power-of-two factor -> 16 fp16 hi/lo cells (int4 register order).
+__device__ void split_row_cta(const float *__restrict__ row, int K, uint4 *cells, float *fac) {
+    __shared__ float buf[32][64];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = K / kGroup;
+    for (int g = warp; g < G; g += blockDim.x >> 5) {
+        const float a = row[g * kGroup + lane], b = row[g * kGroup + 32 + lane];
+        const int e = split_exponent(warp_max(fmaxf(fabsf(a), fabsf(b))));
+        const float mul = ldexpf(1.0f, e);
+        buf[warp][lane] = a * mul;
+        buf[warp][32 + lane] = b * mul;
+        __syncwarp();
+        if (lane < 16) {
+            int k0, k1, k2, k3;
+            frag_ks<false>(0, lane >> 2, lane & 3, k0, k1, k2, k3);
+            cells[(size_t)g * 16 + lane] =
+                make_cell(buf[warp][k0], buf[warp][k1], buf[warp][k2], buf[warp][k3]);
+        }
+        if (lane == 0) fac[g] = ldexpf(1.0f, -e);
+        __syncwarp();
+    }
+}
 
-// One CTA per row: max |v| -> power-of-two rescale, then the fragment cells.
-__global__ void __launch_bounds__(256)
-    k_split(const float *__restrict__ v, int K, uint4 *__restrict__ cells,
-            float *__restrict__ fac) {
-    __shared__ float red[8];
-    const int r = blockIdx.x, tid = threadIdx.x;
-    const float *row = v + (size_t)r * K;
-    float m = 0.0f;
-    for (int k = tid; k < K; k += blockDim.x) m = fmaxf(m, fabsf(row[k]));
-    m = warp_max(m);
-    if ((tid & 31) == 0) red[tid >> 5] = m;
-    __syncthreads();
-    if (tid < 32) {
-        float mm = tid < (int)(blockDim.x >> 5) ? red[tid] : 0.0f;
-        mm = warp_max(mm);
-        if (tid == 0) red[0] = mm;
+// CTA 0 groups the pairs; CTA 1 + t splits token row t of x.
+__global__ void __launch_bounds__(1024)
+    k_group_split(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets, int32_t *list,
+                  int32_t *uexp, int32_t *n_used, int32_t *pass_ofs, int32_t *status,
+                  const float *__restrict__ x, int H, uint4 *xcells, float *xfac) {
+    pdl_trigger();
+    if (blockIdx.x == 0) {
+        group_cta(ids, P, E, offsets, list, uexp, n_used, pass_ofs, status);
+    } else {
+        const int t = blockIdx.x - 1;
+        const int G = H / kGroup;
+        split_row_cta(x + (size_t)t * H, H, xcells + (size_t)t * G * 16, xfac + (size_t)t * G);
     }
-    __syncthreads();
-    const int e = split_exponent(red[0]);
-    const float mul = ldexpf(1.0f, e);
-    if (tid == 0) fac[r] = ldexpf(1.0f, -e);
-    const int G = K / kGroup;
-    uint4 *out = cells + (size_t)r * G * 16;
-    for (int c = tid; c < G * 16; c += blockDim.x) {
-        const int g = c >> 4, m4 = (c >> 2) & 3, q = c & 3;
-        int k0, k1, k2, k3;
-        frag_ks<false>(g, m4, q, k0, k1, k2, k3);
-        out[c] = make_cell(row[k0] * mul, row[k1] * mul, row[k2] * mul, row[k3] * mul);
+}
+
+// Pass offsets for externally grouped pairs (the staged entry points).
+__global__ void __launch_bounds__(1024)
+    k_passes(const int32_t *__restrict__ offsets, const int32_t *__restrict__ uexp,
+             const int32_t *__restrict__ n_used, int32_t *pass_ofs) {
+    __shared__ int32_t tot[96];
+    const int nu = *n_used;
+    int carry = 0;
+    for (int base = 0; base < nu; base += 1024) {
+        const int u = base + threadIdx.x;
+        int np = 0;
+        if (u < nu) {
+            const int e = uexp[u];
+            np = (offsets[e + 1] - offsets[e] + kMaxTok - 1) / kMaxTok;
+        }
+        int ea, eb, ec;
+        block_scan3(np, 0, 0, ea, eb, ec, tot);
+        if (u < nu) pass_ofs[u] = carry + ea;
+        if (threadIdx.x == 1023) tot[95] = ea + np;
+        __syncthreads();
+        carry += tot[95];
+        __syncthreads();
     }
+    if (threadIdx.x == 0) pass_ofs[nu] = carry;
+}
+
+// ------------------------------------------------------------------ expert items
+//
+// An item of the gate+up / down kernels is (pass, row tile): a pass is up to
+// kMaxTok pairs of one expert. Items are numbered pass-major, so a CTA's
+// contiguous item range mostly stays on one expert and pass.
+
+struct PassInfo {
+    int e, beg, ntok;  // expert, first list index of the pass, pairs in the pass
+};
+
+__device__ __forceinline__ PassInfo pass_info(int pi, const int32_t *pass_ofs,
+                                              const int32_t *uexp, const int32_t *offsets,
+                                              int nu) {
+    int lo = 0, hi = nu - 1;  // largest u with pass_ofs[u] <= pi
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pass_ofs[mid] <= pi) lo = mid; else hi = mid - 1;
+    }
+    PassInfo r;
+    r.e = uexp[lo];
+    const int pass = pi - pass_ofs[lo];
+    const int b = offsets[r.e], cnt = offsets[r.e + 1] - b;
+    r.beg = b + pass * kMaxTok;
+    r.ntok = min(kMaxTok, cnt - pass * kMaxTok);
+    return r;
+}
+
+struct MoeTile {
+    const uint8_t *q;   // weight pool
+    const float *s;     // scale pool
+    const int32_t *pass_ofs, *uexp, *offsets;
+    size_t eq, es;      // per-expert strides (bytes, floats)
+    size_t rowBytes;
+    int G, tiles, nu, i0, rows_per_warp_tile_base, nrows_total;
+    int gate_up;        // 1: warps 0-3 gate rows, 4-7 up rows (I = nrows_total / 2)
+    mutable int c_pi = -1, c_e = 0;
+
+    __device__ __forceinline__ TileSrc operator()(int item, int wp) const {
+        const int it = i0 + item;
+        const int pi = it / tiles, tl = it - pi * tiles;
+        if (pi != c_pi) {
+            c_e = pass_info(pi, pass_ofs, uexp, offsets, nu).e;
+            c_pi = pi;
+        }
+        int row;
+        if (gate_up) {
+            const int I = nrows_total / 2;
+            row = (wp < 4) ? tl * 64 + 16 * wp : I + tl * 64 + 16 * (wp - 4);
+        } else {
+            row = tl * 128 + 16 * wp;
+        }
+        int nrows = nrows_total - row;
+        if (nrows <= 0) { row = nrows_total - 1; nrows = 1; }
+        return TileSrc{q + c_e * eq + (size_t)row * rowBytes, s + c_e * es + (size_t)row * G,
+                       rowBytes, nrows};
+    }
+};
+
+constexpr int kMoeWarps = 8;
+constexpr int kMoeBudget = 64 * 1024;
+constexpr int kEpiBytes = (2 * 64 * kMaxTok + kMoeWarps * 64) * 4;
+
+__device__ __forceinline__ void cta_items(int total, int &i0, int &i1) {
+    i0 = (int)((long long)blockIdx.x * total / gridDim.x);
+    i1 = (int)((long long)(blockIdx.x + 1) * total / gridDim.x);
 }
 
 // ------------------------------------------------------------------ gate + up + SiLU
 
-struct ExpertTokens {
-    int e, beg, cnt;
-};
-
-__device__ __forceinline__ bool expert_of_block(const int32_t *offsets, const int32_t *uexp,
-                                                const int32_t *n_used, int tiles,
-                                                ExpertTokens &et, int &tile) {
-    const int u = blockIdx.x / tiles;
-    tile = blockIdx.x - u * tiles;
-    if (u >= *n_used) return false;
-    et.e = uexp[u];
-    et.beg = offsets[et.e];
-    et.cnt = offsets[et.e + 1] - et.beg;
-    return true;
-}
-
-// Warps 0,1: gate rows j0 + 16w; warps 2,3: the matching up rows. One tile =
-// 32 hidden units for every token of the expert.
-template <int NB>
-__device__ __forceinline__ void gate_up_pass(const MoeDims &m, const uint4 *xcells,
-                                             const float *xfac, int k, const int32_t *list,
-                                             const ExpertTokens &et, int tok0, int ntok, int j0,
-                                             float *h, uint4 *cells, int *s_rows, int *s_pair,
-                                             float *s_fac, float *s_gate) {
+template <int NB, class WS>
+__device__ __forceinline__ void gate_up_item(WS &ws, int it, int jt, const PassInfo &pinf,
+                                             bool reuse, const StageCells &stage, int I, int k,
+                                             float *h, uint4 *hcells, float *hfac, uint8_t *smem,
+                                             const int *s_pair) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
-    const int H = m.H, I = m.I, G = H / kGroup;
-    const int rowInMat = (warp < 2) ? (j0 + 16 * warp) : (I + j0 + 16 * (warp - 2));
-    const size_t eq = (size_t)et.e * 2 * I * (H / 2);
-    const size_t es = (size_t)et.e * 2 * I * G;
-    const int rA = rowInMat + gid, rB = rowInMat + gid + 8;
-
-    WeightRing<false> ring;
-    ring.init(m.gu_q + eq + (size_t)rA * (H / 2), m.gu_q + eq + (size_t)rB * (H / 2),
-              m.gu_s + es + (size_t)rA * G, m.gu_s + es + (size_t)rB * G, G, q);
-    ring.prologue();
-
-    if (threadIdx.x < ntok) {
-        const int p = list[et.beg + tok0 + threadIdx.x];
-        const int t = p / k;
-        s_pair[threadIdx.x] = p;
-        s_rows[threadIdx.x] = t;
-        s_fac[threadIdx.x] = xfac[t];
-    }
-    StageFromCells stage{xcells, s_rows, ntok, G, cells};
+    const int ntok = pinf.ntok;
+    uint4 *cells = reinterpret_cast<uint4 *>(smem + kMoeWarps * kRingBytes);
+    float *fac = reinterpret_cast<float *>(smem + kMoeWarps * kRingBytes + kMoeBudget);
+    float *gbuf = fac + kMoeBudget / 256;
+    float *hbuf = gbuf + 64 * kMaxTok;
+    float *wbuf = hbuf + 64 * kMaxTok;
     float acc[NB][2];
-    rows_mainloop<NB, false>(ring, cells, ntok, stage, acc);
+    run_item<NB, false>(ws, it, cells, fac, kMoeBudget, ntok, reuse, stage, acc);
 
-    // gate warps publish g; up warps form h = SiLU(g) * u.
-    if (warp < 2) {
+    if (warp < 4) {
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
             const int s = 4 * nb + q;
             if (s < ntok) {
-                s_gate[(16 * warp + gid) * kMaxTok + s] = acc[nb][0] * s_fac[s];
-                s_gate[(16 * warp + gid + 8) * kMaxTok + s] = acc[nb][1] * s_fac[s];
+                gbuf[(16 * warp + gid) * kMaxTok + s] = acc[nb][0];
+                gbuf[(16 * warp + gid + 8) * kMaxTok + s] = acc[nb][1];
             }
         }
     }
     __syncthreads();
-    if (warp >= 2) {
-        const int lr = 16 * (warp - 2) + gid;
+    const int j0 = jt * 64;
+    if (warp >= 4) {
+        const int lr = 16 * (warp - 4) + gid;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
             const int s = 4 * nb + q;
             if (s < ntok) {
-                const float u0 = acc[nb][0] * s_fac[s], u1 = acc[nb][1] * s_fac[s];
-                const float g0 = s_gate[lr * kMaxTok + s], g1 = s_gate[(lr + 8) * kMaxTok + s];
+                const float g0 = gbuf[lr * kMaxTok + s], g1 = gbuf[(lr + 8) * kMaxTok + s];
+                const float h0 = g0 / (1.0f + expf(-g0)) * acc[nb][0];
+                const float h1 = g1 / (1.0f + expf(-g1)) * acc[nb][1];
+                hbuf[lr * kMaxTok + s] = h0;
+                hbuf[(lr + 8) * kMaxTok + s] = h1;
                 const size_t hb = (size_t)s_pair[s] * I + j0;
-                h[hb + lr] = g0 / (1.0f + expf(-g0)) * u0;
-                h[hb + lr + 8] = g1 / (1.0f + expf(-g1)) * u1;
+                h[hb + lr] = h0;
+                h[hb + lr + 8] = h1;
             }
         }
     }
-    __syncthreads();  // s_gate / s_pair reused by the next pass
+    __syncthreads();
+    // fp16 hi/lo cells of h for the down projection: this tile is group jt of h.
+    const int Gd = I / kGroup;
+    for (int s = warp; s < ntok; s += kMoeWarps) {
+        const float a = hbuf[lane * kMaxTok + s], b = hbuf[(32 + lane) * kMaxTok + s];
+        const int e = split_exponent(warp_max(fmaxf(fabsf(a), fabsf(b))));
+        const float mul = ldexpf(1.0f, e);
+        wbuf[warp * 64 + lane] = a * mul;
+        wbuf[warp * 64 + 32 + lane] = b * mul;
+        __syncwarp();
+        const size_t cb = (size_t)s_pair[s] * Gd + jt;
+        if (lane < 16) {
+            int k0, k1, k2, k3;
+            frag_ks<false>(0, lane >> 2, lane & 3, k0, k1, k2, k3);
+            hcells[cb * 16 + lane] = make_cell(wbuf[warp * 64 + k0], wbuf[warp * 64 + k1],
+                                               wbuf[warp * 64 + k2], wbuf[warp * 64 + k3]);
+        }
+        if (lane == 0) hfac[cb] = ldexpf(1.0f, -e);
+        __syncwarp();
+    }
+    __syncthreads();
 }
 
-__global__ void __launch_bounds__(kCtaThreads)
+__global__ void __launch_bounds__(32 * kMoeWarps, 1)
     k_gate_up(MoeDims m, const uint4 *__restrict__ xcells, const float *__restrict__ xfac, int k,
               const int32_t *__restrict__ offsets, const int32_t *__restrict__ list,
               const int32_t *__restrict__ uexp, const int32_t *__restrict__ n_used,
-              float *__restrict__ h) {
-    extern __shared__ uint4 cells[];
+              const int32_t *__restrict__ pass_ofs, float *__restrict__ h,
+              uint4 *__restrict__ hcells, float *__restrict__ hfac) {
+    extern __shared__ __align__(16) uint8_t smem[];
     __shared__ int s_rows[kMaxTok], s_pair[kMaxTok];
-    __shared__ float s_fac[kMaxTok];
-    __shared__ float s_gate[32 * kMaxTok];
-    const int tiles = m.I / 32;
-    ExpertTokens et;
-    int tile;
-    if (!expert_of_block(offsets, uexp, n_used, tiles, et, tile)) return;
-    const int j0 = tile * 32;
-    for (int tok0 = 0; tok0 < et.cnt; tok0 += kMaxTok) {
-        const int ntok = min(kMaxTok, et.cnt - tok0);
-        if (ntok <= 4)
-            gate_up_pass<1>(m, xcells, xfac, k, list, et, tok0, ntok, j0, h, cells, s_rows, s_pair,
-                            s_fac, s_gate);
-        else if (ntok <= 8)
-            gate_up_pass<2>(m, xcells, xfac, k, list, et, tok0, ntok, j0, h, cells, s_rows, s_pair,
-                            s_fac, s_gate);
+    pdl_wait();  // grouping and x cells come from the previous kernel
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = m.H, I = m.I, G = H / kGroup;
+    const int nu = *n_used;
+    if (nu == 0) return;
+    const int tiles = I / 64;
+    const int total = pass_ofs[nu] * tiles;
+    int i0, i1;
+    cta_items(total, i0, i1);
+    if (i0 >= i1) return;
+    const int ns = G / 4;
+    MoeTile tile{m.gu_q, m.gu_s, pass_ofs, uexp, offsets, (size_t)2 * I * (H / 2),
+                 (size_t)2 * I * G, (size_t)H / 2, G, tiles, nu, i0, 0, 2 * I, 1};
+    WarpStream<false, MoeTile> ws{smem + warp * kRingBytes, tile, G, ns, (i1 - i0) * ns, 0,
+                                  warp, lane};
+    ws.prologue();
+
+    int cur_pi = -1;
+    PassInfo pinf{};
+    for (int it = 0; it < i1 - i0; ++it) {
+        const int gi = i0 + it, pi = gi / tiles, jt = gi - pi * tiles;
+        bool reuse = pi == cur_pi;
+        if (!reuse) {
+            pinf = pass_info(pi, pass_ofs, uexp, offsets, nu);
+            cur_pi = pi;
+            __syncthreads();  // previous item's epilogue is done with s_pair
+            if (threadIdx.x < pinf.ntok) {
+                const int p = list[pinf.beg + threadIdx.x];
+                s_pair[threadIdx.x] = p;
+                s_rows[threadIdx.x] = p / k;
+            }
+        }
+        const StageCells stage{xcells, xfac, s_rows, pinf.ntok, G};
+        if (pinf.ntok <= 4)
+            gate_up_item<1>(ws, it, jt, pinf, reuse, stage, I, k, h, hcells, hfac, smem, s_pair);
+        else if (pinf.ntok <= 8)
+            gate_up_item<2>(ws, it, jt, pinf, reuse, stage, I, k, h, hcells, hfac, smem, s_pair);
         else
-            gate_up_pass<4>(m, xcells, xfac, k, list, et, tok0, ntok, j0, h, cells, s_rows, s_pair,
-                            s_fac, s_gate);
+            gate_up_item<4>(ws, it, jt, pinf, reuse, stage, I, k, h, hcells, hfac, smem, s_pair);
     }
+    cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------ down
 
-template <int NB>
-__device__ __forceinline__ void down_pass(const MoeDims &m, const uint4 *hcells, const float *hfac,
-                                          const int32_t *list, const ExpertTokens &et, int tok0,
-                                          int ntok, int i0, float *y, uint4 *cells, int *s_pair,
-                                          float *s_fac) {
+template <int NB, class WS>
+__device__ __forceinline__ void down_item(WS &ws, int it, int tl, const PassInfo &pinf,
+                                          bool reuse, const StageCells &stage, int H, float *y,
+                                          uint8_t *smem, const int *s_pair) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
-    const int H = m.H, I = m.I, G = I / kGroup;
-    const int row0 = i0 + 16 * warp;
-    const int rA = min(row0 + gid, H - 1), rB = min(row0 + gid + 8, H - 1);
-    const size_t eq = (size_t)et.e * H * (I / 2);
-    const size_t es = (size_t)et.e * H * G;
-
-    WeightRing<false> ring;
-    ring.init(m.dn_q + eq + (size_t)rA * (I / 2), m.dn_q + eq + (size_t)rB * (I / 2),
-              m.dn_s + es + (size_t)rA * G, m.dn_s + es + (size_t)rB * G, G, q);
-    ring.prologue();
-
-    if (threadIdx.x < ntok) {
-        const int p = list[et.beg + tok0 + threadIdx.x];
-        s_pair[threadIdx.x] = p;
-        s_fac[threadIdx.x] = hfac[p];
-    }
-    StageFromCells stage{hcells, s_pair, ntok, G, cells};
+    uint4 *cells = reinterpret_cast<uint4 *>(smem + kMoeWarps * kRingBytes);
+    float *fac = reinterpret_cast<float *>(smem + kMoeWarps * kRingBytes + kMoeBudget);
     float acc[NB][2];
-    rows_mainloop<NB, false>(ring, cells, ntok, stage, acc);
+    run_item<NB, false>(ws, it, cells, fac, kMoeBudget, pinf.ntok, reuse, stage, acc);
+    const int row0 = tl * 128 + 16 * warp;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
         const int s = 4 * nb + q;
-        if (s < ntok) {
+        if (s < pinf.ntok) {
             const size_t yb = (size_t)s_pair[s] * H;
-            if (row0 + gid < H) y[yb + row0 + gid] = acc[nb][0] * s_fac[s];
-            if (row0 + gid + 8 < H) y[yb + row0 + gid + 8] = acc[nb][1] * s_fac[s];
+            if (row0 + gid < H) y[yb + row0 + gid] = acc[nb][0];
+            if (row0 + gid + 8 < H) y[yb + row0 + gid + 8] = acc[nb][1];
         }
     }
-    __syncthreads();
 }
 
-__global__ void __launch_bounds__(kCtaThreads)
+__global__ void __launch_bounds__(32 * kMoeWarps, 1)
     k_down(MoeDims m, const uint4 *__restrict__ hcells, const float *__restrict__ hfac,
            const int32_t *__restrict__ offsets, const int32_t *__restrict__ list,
            const int32_t *__restrict__ uexp, const int32_t *__restrict__ n_used,
-           float *__restrict__ y) {
-    extern __shared__ uint4 cells[];
+           const int32_t *__restrict__ pass_ofs, float *__restrict__ y) {
+    extern __shared__ __align__(16) uint8_t smem[];
     __shared__ int s_pair[kMaxTok];
-    __shared__ float s_fac[kMaxTok];
-    const int tiles = (m.H + 16 * kWarps - 1) / (16 * kWarps);
-    ExpertTokens et;
-    int tile;
-    if (!expert_of_block(offsets, uexp, n_used, tiles, et, tile)) return;
-    const int i0 = tile * 16 * kWarps;
-    for (int tok0 = 0; tok0 < et.cnt; tok0 += kMaxTok) {
-        const int ntok = min(kMaxTok, et.cnt - tok0);
-        if (ntok <= 4)
-            down_pass<1>(m, hcells, hfac, list, et, tok0, ntok, i0, y, cells, s_pair, s_fac);
-        else if (ntok <= 8)
-            down_pass<2>(m, hcells, hfac, list, et, tok0, ntok, i0, y, cells, s_pair, s_fac);
+    // The grouping was complete before the previous kernel started its main
+    // work, so the item map and the weights can be read before the wait.
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = m.H, I = m.I, G = I / kGroup;
+    const int nu = *n_used;
+    if (nu == 0) { pdl_wait(); pdl_trigger(); return; }
+    const int tiles = (H + 127) / 128;
+    const int total = pass_ofs[nu] * tiles;
+    int i0, i1;
+    cta_items(total, i0, i1);
+    const int ns = G / 4;
+    MoeTile tile{m.dn_q, m.dn_s, pass_ofs, uexp, offsets, (size_t)H * (I / 2), (size_t)H * G,
+                 (size_t)I / 2, G, tiles, nu, i0, 0, H, 0};
+    WarpStream<false, MoeTile> ws{smem + warp * kRingBytes, tile, G, ns, (i1 - i0) * ns, 0,
+                                  warp, lane};
+    ws.prologue();
+    pdl_wait();  // h cells come from the gate+up kernel
+    pdl_trigger();
+
+    int cur_pi = -1;
+    PassInfo pinf{};
+    for (int it = 0; it < i1 - i0; ++it) {
+        const int gi = i0 + it, pi = gi / tiles, tl = gi - pi * tiles;
+        const bool reuse = pi == cur_pi;
+        if (!reuse) {
+            pinf = pass_info(pi, pass_ofs, uexp, offsets, nu);
+            cur_pi = pi;
+            __syncthreads();
+            if (threadIdx.x < pinf.ntok) s_pair[threadIdx.x] = list[pinf.beg + threadIdx.x];
+        }
+        const StageCells stage{hcells, hfac, s_pair, pinf.ntok, G};
+        if (pinf.ntok <= 4)
+            down_item<1>(ws, it, tl, pinf, reuse, stage, H, y, smem, s_pair);
+        else if (pinf.ntok <= 8)
+            down_item<2>(ws, it, tl, pinf, reuse, stage, H, y, smem, s_pair);
         else
-            down_pass<4>(m, hcells, hfac, list, et, tok0, ntok, i0, y, cells, s_pair, s_fac);
+            down_item<4>(ws, it, tl, pinf, reuse, stage, H, y, smem, s_pair);
     }
+    cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------ combine
@@ -353,6 +489,8 @@ __global__ void __launch_bounds__(kCtaThreads)
 __global__ void __launch_bounds__(256)
     k_combine(const float *__restrict__ y, const int32_t *__restrict__ ids,
               const float *__restrict__ w, int k, int E, int H, float *__restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.y;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= H) return;
@@ -367,6 +505,14 @@ __global__ void __launch_bounds__(256)
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+size_t moe_smem() { return engine_smem(kMoeWarps, kMoeBudget, kEpiBytes); }
+
+int moe_grid(void (*k)(MoeDims, const uint4 *, const float *, int, const int32_t *,
+                       const int32_t *, const int32_t *, const int32_t *, const int32_t *,
+                       float *, uint4 *, float *)) {
+    return sm_count() * max_ctas_per_sm(k, 32 * kMoeWarps, moe_smem());
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
@@ -375,54 +521,59 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids,
                          cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int per = 8;  // tokens (warps) per CTA
-    k_route<<<(T + per - 1) / per, 32 * per, 0, st>>>(logits, T, E, k, ids, w);
-    return cudaGetLastError();
+    return launch(k_route, dim3((T + per - 1) / per), dim3(32 * per), 0, st, false, logits, T, E,
+                  k, ids, w);
 }
 
 cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int32_t *list,
                          int32_t *uexp, int32_t *n_used, int32_t *status, cudaStream_t st) {
-    k_group<<<1, 1024, 0, st>>>(ids, P, E, offsets, list, uexp, n_used, status);
-    return cudaGetLastError();
+    return launch(k_group_split, dim3(1), dim3(1024), 0, st, false, ids, P, E, offsets, list, uexp,
+                  n_used, (int32_t *)nullptr, status, (const float *)nullptr, 64,
+                  (uint4 *)nullptr, (float *)nullptr);
 }
 
-cudaError_t launch_split(const float *v, int R, int K, void *cells, float *fac, cudaStream_t st) {
-    if (R == 0) return cudaSuccess;
-    k_split<<<R, 256, 0, st>>>(v, K, static_cast<uint4 *>(cells), fac);
-    return cudaGetLastError();
+cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
+                               int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
+                               int32_t *status, const float *x, int H, void *xcells, float *xfac,
+                               cudaStream_t st) {
+    return launch(k_group_split, dim3(1 + T), dim3(1024), 0, st, false, ids, T * k, E, offsets,
+                  list, uexp, n_used, pass_ofs, status, x, H, static_cast<uint4 *>(xcells), xfac);
 }
 
-cudaError_t launch_gate_up(const MoeDims &m, const void *xcells, const float *xfac, int T, int k,
+cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
+                          int32_t *pass_ofs, cudaStream_t st, bool pdl) {
+    return launch(k_passes, dim3(1), dim3(1024), 0, st, pdl, offsets, uexp, n_used, pass_ofs);
+}
+
+cudaError_t launch_gate_up(const MoeDims &m, const void *xcells, const float *xfac, int k,
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
-                           const int32_t *n_used, float *h, cudaStream_t st) {
-    const int P = T * k;
-    const int maxU = P < m.E ? P : m.E;
-    if (maxU == 0) return cudaSuccess;
-    const int tiles = m.I / 32;
-    const size_t smem = (size_t)kCellBudget;
-    k_gate_up<<<maxU * tiles, kCtaThreads, smem, st>>>(
-        m, static_cast<const uint4 *>(xcells), xfac, k, offsets, list, uexp, n_used, h);
-    return cudaGetLastError();
+                           const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,
+                           float *hfac, cudaStream_t st) {
+    const size_t smem = moe_smem();
+    cudaError_t e = set_smem(k_gate_up, smem);
+    if (e != cudaSuccess) return e;
+    return launch(k_gate_up, dim3(moe_grid(k_gate_up)), dim3(32 * kMoeWarps), smem, st, true, m,
+                  static_cast<const uint4 *>(xcells), xfac, k, offsets, list, uexp, n_used,
+                  pass_ofs, h, static_cast<uint4 *>(hcells), hfac);
 }
 
-cudaError_t launch_down(const MoeDims &m, const void *hcells, const float *hfac, int T, int k,
+cudaError_t launch_down(const MoeDims &m, const void *hcells, const float *hfac,
                         const int32_t *offsets, const int32_t *list, const int32_t *uexp,
-                        const int32_t *n_used, float *y, cudaStream_t st) {
-    const int P = T * k;
-    const int maxU = P < m.E ? P : m.E;
-    if (maxU == 0) return cudaSuccess;
-    const int tiles = (m.H + 16 * kWarps - 1) / (16 * kWarps);
-    const size_t smem = (size_t)kCellBudget;
-    k_down<<<maxU * tiles, kCtaThreads, smem, st>>>(m, static_cast<const uint4 *>(hcells), hfac,
-                                                    offsets, list, uexp, n_used, y);
-    return cudaGetLastError();
+                        const int32_t *n_used, const int32_t *pass_ofs, float *y, cudaStream_t st) {
+    const size_t smem = moe_smem();
+    cudaError_t e = set_smem(k_down, smem);
+    if (e != cudaSuccess) return e;
+    const int grid = sm_count() * max_ctas_per_sm(k_down, 32 * kMoeWarps, smem);
+    return launch(k_down, dim3(grid), dim3(32 * kMoeWarps), smem, st, true, m,
+                  static_cast<const uint4 *>(hcells), hfac, offsets, list, uexp, n_used, pass_ofs,
+                  y);
 }
 
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int T, int k, int E,
-                           int H, float *out, cudaStream_t st) {
+                           int H, float *out, cudaStream_t st, bool pdl) {
     if (T == 0) return cudaSuccess;
-    dim3 grid((H + 255) / 256, T);
-    k_combine<<<grid, 256, 0, st>>>(y, ids, w, k, E, H, out);
-    return cudaGetLastError();
+    return launch(k_combine, dim3((H + 255) / 256, T), dim3(256), 0, st, pdl, y, ids, w, k, E, H,
+                  out);
 }
 
 MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k) {
@@ -434,11 +585,12 @@ MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k) {
     L.list = o; o = align256(o + 4 * P);
     L.uexp = o; o = align256(o + 4 * (size_t)E);
     L.n_used = o; o = align256(o + 4);
+    L.pass_ofs = o; o = align256(o + 4 * (size_t)(E + 1));
     L.xcells = o; o = align256(o + 4 * (size_t)T * H);
-    L.xfac = o; o = align256(o + 4 * (size_t)T);
+    L.xfac = o; o = align256(o + 4 * (size_t)T * (H / 64));
     L.h = o; o = align256(o + 4 * P * I);
     L.hcells = o; o = align256(o + 4 * P * I);
-    L.hfac = o; o = align256(o + 4 * P);
+    L.hfac = o; o = align256(o + 4 * P * (I / 64));
     L.y = o; o = align256(o + 4 * P * H);
     L.total = o;
     return L;

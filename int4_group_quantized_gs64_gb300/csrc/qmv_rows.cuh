@@ -1,126 +1,222 @@
 // qmv_rows.cuh - the streaming row engine shared by the dense and MoE decode kernels.
 //
-// A CTA of kWarps warps owns kWarps 16-row tiles of one weight matrix (rows
-// may come from different matrices, e.g. gate and up). Each warp streams its
-// two rows per lane straight from HBM into a register ring kDepth groups deep
-// (8 bytes of int4 or 16 bytes of int8 per row per group, plus the group
-// scale), so every warp keeps kDepth * 512..1024 bytes in flight without
-// waiting on shared memory. The activation fragments of the CTA's tokens are
-// staged in shared memory one chunk of groups at a time; a chunk is a
-// multiple of kDepth groups, so the ring continues across chunk boundaries.
+// Weights: every warp owns a 16-row tile and streams it from HBM through its
+// own shared-memory ring of kStages stages with cp.async (16-byte copies that
+// bypass L1). A stage holds 128 bytes of each of the 16 rows (4 int4 groups or
+// 2 int8 groups) plus the 16 x 4 group scales. The 16-byte chunks of a row are
+// XOR-swizzled by (row & 7) so the fragment reads below are bank-conflict free.
+// kStages - 1 stages (~11.5 KB per warp) are in flight while one is consumed,
+// without holding any of it in registers.
+//
+// Work: a CTA walks a contiguous range of work items (an item is one row tile
+// of every warp, e.g. 64 or 128 rows of one expert matrix); the warp rings run
+// on across items, so they never drain inside a CTA.
+//
+// Activations: fragment cells (see qmv_device.cuh) plus one power-of-two
+// factor per (row, group) are staged in shared memory one chunk of groups at a
+// time; a chunk is a multiple of the stage size.
 #pragma once
-
-#include <type_traits>
 
 #include "qmv_device.cuh"
 
 namespace qmv {
 
-constexpr int kWarps = 4;                 // warps (16-row tiles) per CTA
-constexpr int kCtaThreads = 32 * kWarps;
-constexpr int kDepth = 8;                 // groups in flight per warp
-constexpr int kMaxTok = 16;               // tokens per pass (4 MMA column blocks)
-constexpr int kCellBudget = 32 * 1024;    // bytes of activation cells per chunk
-
-// Groups per chunk for ntok tokens: 256 bytes of cells per token per group.
-__host__ __device__ inline int chunk_groups(int ntok) {
-    int c = kCellBudget / (256 * (ntok < 1 ? 1 : ntok));
-    c = (c / kDepth) * kDepth;
-    return c < kDepth ? kDepth : c;
-}
+constexpr int kStages = 6;
+constexpr int kStageWBytes = 16 * 128;                 // weights of one stage
+constexpr int kStageBytes = kStageWBytes + 16 * 4 * 4; // + 16 rows x 4 scales
+constexpr int kRingBytes = kStages * kStageBytes;      // per warp
+constexpr int kMaxTok = 16;                            // tokens per pass (4 MMA blocks)
 
 template <bool kInt8>
-struct WeightRing {
-    using W = typename std::conditional<kInt8, uint4, uint2>::type;
-    static constexpr int kGroupBytes = kInt8 ? 64 : 32;
-    static constexpr int kLaneBytes = kInt8 ? 16 : 8;
+struct Fmt {
+    static constexpr int kGPS = kInt8 ? 2 : 4;          // groups per stage
+    static constexpr int kGroupBytes = kInt8 ? 64 : 32; // bytes of one row per group
+};
 
-    W ra[kDepth], rb[kDepth];
-    float sa[kDepth], sb[kDepth];
-    const uint8_t *pA, *pB;
-    const float *sA, *sB;
-    int G;
+// Groups per activation chunk for ntok tokens within `budget` bytes of cells
+// (256 bytes per token per group); a multiple of 4 groups (both formats).
+__host__ __device__ inline int chunk_groups(int ntok, int budget) {
+    int c = budget / (256 * (ntok < 1 ? 1 : ntok));
+    c &= ~3;
+    return c < 4 ? 4 : c;
+}
 
-    // rowA / rowB: byte address of the two rows this lane streams; scaleA / B:
-    // their group scales (ignored for int8).
-    __device__ __forceinline__ void init(const uint8_t *rowA, const uint8_t *rowB,
-                                         const float *scaleA, const float *scaleB, int groups,
-                                         int q) {
-        pA = rowA + kLaneBytes * q;
-        pB = rowB + kLaneBytes * q;
-        sA = scaleA;
-        sB = scaleB;
-        G = groups;
-    }
+// ------------------------------------------------------------------ cp.async
 
-    __device__ __forceinline__ void load(int slot_unused, int g, W &a, W &b, float &s0,
-                                         float &s1) {
-        (void)slot_unused;
-        if constexpr (kInt8) {
-            a = ldg_stream_u4(pA + (size_t)g * kGroupBytes);
-            b = ldg_stream_u4(pB + (size_t)g * kGroupBytes);
-            s0 = s1 = 1.0f;
-        } else {
-            a = ldg_stream_u2(pA + (size_t)g * kGroupBytes);
-            b = ldg_stream_u2(pB + (size_t)g * kGroupBytes);
-            s0 = ldg_stream_f32(sA + g);
-            s1 = ldg_stream_f32(sB + g);
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Programmatic dependent launch: wait for the previous kernel's results /
+// let the next kernel's CTAs start. Both are no-ops without the launch attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ tile source
+
+// The 16 rows of one warp tile: row r at w + r * rowBytes (rows >= nrows are
+// replaced by row nrows-1, which is read but never stored), its scales at
+// s + r * G.
+struct TileSrc {
+    const uint8_t *w;
+    const float *s;
+    size_t rowBytes;
+    int nrows;
+};
+
+template <bool kInt8>
+__device__ __forceinline__ void issue_stage(uint8_t *slot, const TileSrc &t, int stage, int G,
+                                            int lane) {
+    const int g0 = stage * Fmt<kInt8>::kGPS;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int i = lane + 32 * j;
+        const int r = i >> 3, c = i & 7;
+        const int grp = g0 + (kInt8 ? (c >> 2) : (c >> 1));
+        if (grp < G) {
+            const int rr = r < t.nrows ? r : t.nrows - 1;
+            const uint8_t *src =
+                t.w + (size_t)rr * t.rowBytes + (size_t)g0 * Fmt<kInt8>::kGroupBytes + c * 16;
+            cp_async16(slot + r * 128 + ((c ^ (r & 7)) << 4), src);
         }
     }
-
-    __device__ __forceinline__ void prologue() {
+    if constexpr (!kInt8) {
+        float *ss = reinterpret_cast<float *>(slot + kStageWBytes);
 #pragma unroll
-        for (int d = 0; d < kDepth; ++d)
-            if (d < G) load(d, d, ra[d], rb[d], sa[d], sb[d]);
+        for (int j = 0; j < 2; ++j) {
+            const int i = lane + 32 * j;
+            const int r = i >> 2, gg = i & 3;
+            if (g0 + gg < G) {
+                const int rr = r < t.nrows ? r : t.nrows - 1;
+                cp_async4(ss + r * 4 + gg, t.s + (size_t)rr * G + g0 + gg);
+            }
+        }
+    }
+}
+
+// Activation cells of the current chunk: cells[(gl*4 + m)*4 + q][s] (16 B),
+// factors fac[gl][s].
+struct Chunk {
+    const uint4 *cells;
+    const float *fac;
+    int ntok;
+};
+
+// Consume one stage: groups [g0, g0 + GPS) of the chunk starting at group gc,
+// stopping at gEnd. Accumulates scale * factor * (hi + lo) per row and token.
+template <int NB, bool kInt8>
+__device__ __forceinline__ void compute_stage(const uint8_t *slot, int g0, int gc, int gEnd,
+                                              const Chunk &ch, float c2[2][NB][2]) {
+    const int lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
+    const float *ss = reinterpret_cast<const float *>(slot + kStageWBytes);
+#pragma unroll
+    for (int gl = 0; gl < Fmt<kInt8>::kGPS; ++gl) {
+        const int g = g0 + gl;
+        if (g < gEnd) {
+            float dd[NB][4];
+            float s0 = 1.0f, s8 = 1.0f;
+            if constexpr (kInt8) {
+                const int c = 4 * gl + q;
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(slot + gid * 128 + ((c ^ gid) << 4));
+                const uint4 w8 =
+                    *reinterpret_cast<const uint4 *>(slot + (gid + 8) * 128 + ((c ^ gid) << 4));
+                tile_group_int8<NB>(w0, w8, ch.cells, ch.ntok, g - gc, q, gid, dd);
+            } else {
+                const int c = 2 * gl + (q >> 1);
+                const int off = ((c ^ gid) << 4) + ((q & 1) << 3);
+                const uint2 w0 = *reinterpret_cast<const uint2 *>(slot + gid * 128 + off);
+                const uint2 w8 = *reinterpret_cast<const uint2 *>(slot + (gid + 8) * 128 + off);
+                s0 = ss[gid * 4 + gl];
+                s8 = ss[(gid + 8) * 4 + gl];
+                tile_group_int4<NB>(w0, w8, ch.cells, ch.ntok, g - gc, q, gid, dd);
+            }
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                const int s = 4 * nb + q;
+                const float f = s < ch.ntok ? ch.fac[(g - gc) * ch.ntok + s] : 0.0f;
+                c2[gl & 1][nb][0] = fmaf(s0 * f, dd[nb][0] + dd[nb][1], c2[gl & 1][nb][0]);
+                c2[gl & 1][nb][1] = fmaf(s8 * f, dd[nb][2] + dd[nb][3], c2[gl & 1][nb][1]);
+            }
+        }
+    }
+}
+
+// Per-warp weight stream over the CTA's items. TileFn(item, warp) -> TileSrc.
+template <bool kInt8, class TileFn>
+struct WarpStream {
+    uint8_t *ring;  // this warp's kRingBytes
+    TileFn tile;
+    int G, ns, total;  // groups per row, stages per item, stages of all items
+    int next;          // next global stage to issue
+    int warp, lane;
+
+    __device__ __forceinline__ void issue_next() {
+        if (next < total) {
+            const int item = next / ns, s = next - item * ns;
+            issue_stage<kInt8>(ring + (next % kStages) * kStageBytes, tile(item, warp), s, G, lane);
+        }
+        cp_async_commit();  // possibly empty: keeps the group count uniform
+        ++next;
+    }
+    __device__ __forceinline__ void prologue() {
+        for (int i = 0; i < kStages - 1; ++i) issue_next();
+    }
+    // Wait for stage j (global index), refill the slot freed by stage j-1.
+    __device__ __forceinline__ const uint8_t *acquire(int j) {
+        cp_async_wait<kStages - 2>();
+        __syncwarp();
+        issue_next();
+        return ring + (j % kStages) * kStageBytes;
     }
 };
 
-// Main loop over all groups. `stage(gc, ng)` must write the activation cells
-// of groups [gc, gc + ng) into `cells` (all threads take part; no barriers
-// inside). acc[nb][0 / 1]: rows gid / gid+8 for token 4*nb + q, sum of scaled
-// group partials (before the per-token unscale).
-template <int NB, bool kInt8, class Stage>
-__device__ __forceinline__ void rows_mainloop(WeightRing<kInt8> &ring, uint4 *cells, int ntok,
-                                              const Stage &stage, float acc[NB][2]) {
-    const int lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
-    const int G = ring.G;
-    const int CG = chunk_groups(ntok);
+// Runs one item for up to 4*NB tokens: chunks of activations are staged by
+// `stage(gc, ng, cells, fac)` (all threads; no barriers inside) unless
+// `reuse` says the previous item left the full K in shared memory.
+// acc[nb][0 / 1]: rows gid / gid+8 of this warp, token 4*nb + q.
+template <int NB, bool kInt8, class TileFn, class Stage>
+__device__ __forceinline__ void run_item(WarpStream<kInt8, TileFn> &ws, int item, uint4 *cells,
+                                         float *fac, int budget, int ntok, bool reuse,
+                                         const Stage &stage, float acc[NB][2]) {
+    const int G = ws.G;
+    const int CG = chunk_groups(ntok, budget);
+    constexpr int GPS = Fmt<kInt8>::kGPS;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = 0.0f;
-
+    int j = item * ws.ns;
     for (int gc = 0; gc < G; gc += CG) {
         const int ng = min(CG, G - gc);
-        __syncthreads();  // all warps are done reading the previous chunk
-        stage(gc, ng);
-        __syncthreads();
-        float c2[2][NB][2];  // two alternating accumulators halve the add depth
+        if (!(reuse && ng == G)) {
+            __syncthreads();  // every warp is done with the previous chunk
+            stage(gc, ng, cells, fac);
+            __syncthreads();
+        }
+        const Chunk ch{cells, fac, ntok};
+        float c2[2][NB][2];
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) c2[h][nb][0] = c2[h][nb][1] = 0.0f;
-
-        for (int g = gc; g < gc + ng; g += kDepth) {
-#pragma unroll
-            for (int d = 0; d < kDepth; ++d) {
-                const int gg = g + d;
-                if (gg < gc + ng) {
-                    const auto a0 = ring.ra[d];
-                    const auto a8 = ring.rb[d];
-                    const float s0 = ring.sa[d], s8 = ring.sb[d];
-                    if (gg + kDepth < G)
-                        ring.load(d, gg + kDepth, ring.ra[d], ring.rb[d], ring.sa[d], ring.sb[d]);
-                    float dd[NB][4];
-                    if constexpr (kInt8)
-                        tile_group_int8<NB>(a0, a8, cells, ntok, gg - gc, q, gid, dd);
-                    else
-                        tile_group_int4<NB>(a0, a8, cells, ntok, gg - gc, q, gid, dd);
-#pragma unroll
-                    for (int nb = 0; nb < NB; ++nb) {
-                        c2[d & 1][nb][0] = fmaf(s0, dd[nb][0] + dd[nb][1], c2[d & 1][nb][0]);
-                        c2[d & 1][nb][1] = fmaf(s8, dd[nb][2] + dd[nb][3], c2[d & 1][nb][1]);
-                    }
-                }
-            }
+        for (int g0 = gc; g0 < gc + ng; g0 += GPS, ++j) {
+            const uint8_t *slot = ws.acquire(j);
+            compute_stage<NB, kInt8>(slot, g0, gc, gc + ng, ch, c2);
         }
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
@@ -130,22 +226,32 @@ __device__ __forceinline__ void rows_mainloop(WeightRing<kInt8> &ring, uint4 *ce
     }
 }
 
-// Copies pre-split activation cells (layout [row][G][4][4] uint4, see
-// qmv_device.cuh) of the CTA's token rows into the chunk buffer
-// cells[(gl*4 + m)*4 + q][s].
-struct StageFromCells {
-    const uint4 *src;      // cells of all rows
-    const int *rows;       // shared: cell row of each token slot
+// Stages cells + factors of `ntok` activation rows (cell rows `rows[s]`,
+// layout [row][G][16] uint4 and [row][G] factors) for groups [gc, gc+ng).
+struct StageCells {
+    const uint4 *src;
+    const float *fsrc;
+    const int *rows;  // shared memory
     int ntok, G;
-    uint4 *cells;
-    __device__ __forceinline__ void operator()(int gc, int ng) const {
+    __device__ __forceinline__ void operator()(int gc, int ng, uint4 *cells, float *fac) const {
         const int total = ng * 16 * ntok;
         for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
             const int s = idx % ntok;
             const int r = idx / ntok;
             cells[idx] = src[(size_t)rows[s] * G * 16 + (size_t)gc * 16 + r];
         }
+        for (int idx = threadIdx.x; idx < ng * ntok; idx += blockDim.x) {
+            const int s = idx % ntok;
+            const int gl = idx / ntok;
+            fac[idx] = fsrc[(size_t)rows[s] * G + gc + gl];
+        }
     }
 };
+
+// Shared memory of a CTA: `warps` rings, `budget` bytes of cells, factors
+// (ng * ntok <= budget / 256 floats), then `extra` bytes of epilogue scratch.
+__host__ __device__ inline size_t engine_smem(int warps, int budget, int extra) {
+    return (size_t)warps * kRingBytes + budget + budget / 64 + extra;
+}
 
 }  // namespace qmv

@@ -37,7 +37,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("qmv_int4_gs", "qmv_int8_row", "moe_route_topk", "moe_group", "moe_gate_up_silu",
+    for n in ("qmv_gemv_workspace_bytes", "qmv_int4_gs", "qmv_int8_row", "moe_route_topk", "moe_group", "moe_gate_up_silu",
               "moe_down", "moe_combine", "moe_workspace_bytes", "moe_expert_ffn_int4"):
         assert n in names
 
@@ -58,17 +58,25 @@ FAKE = 0x10000  # a 64 KiB-aligned non-null address: never dereferenced, validat
 
 def test_dense_validation(L):
     p = ctypes.c_void_p(FAKE)
-    assert L.qmv_int4_gs(None, p, 8, 64, 64, p, p, 1, None) == EINVAL
-    assert L.qmv_int4_gs(p, p, 8, 64, 32, p, p, 1, None) == EINVAL      # gs != 64
-    assert L.qmv_int4_gs(p, p, 0, 64, 64, p, p, 1, None) == EINVAL      # N < 1
-    assert L.qmv_int4_gs(p, p, 8, 64, 64, p, p, 0, None) == EINVAL      # S < 1
-    assert L.qmv_int4_gs(p, p, 8, 96, 64, p, p, 1, None) == ESHAPE      # ragged K
-    assert L.qmv_int4_gs(p, p, 8, 0, 64, p, p, 1, None) == ESHAPE
-    assert L.qmv_int4_gs(ctypes.c_void_p(FAKE + 8), p, 8, 64, 64, p, p, 1, None) == EALIGN
-    assert L.qmv_int4_gs(p, ctypes.c_void_p(FAKE + 2), 8, 64, 64, p, p, 1, None) == EALIGN
-    assert L.qmv_int8_row(p, None, 8, 64, p, p, 1, None) == EINVAL
-    assert L.qmv_int8_row(p, p, 8, 100, p, p, 1, None) == ESHAPE
-    assert L.qmv_int8_row(ctypes.c_void_p(FAKE + 4), p, 8, 64, p, p, 1, None) == EALIGN
+    need = L.qmv_gemv_workspace_bytes(64, 1)
+    assert need >= 64 * 4 and need % 256 == 0
+    assert L.qmv_gemv_workspace_bytes(96, 1) == 0 and L.qmv_gemv_workspace_bytes(64, 0) == 0
+    ok = (p, need, None)
+    assert L.qmv_int4_gs(None, p, 8, 64, 64, p, p, 1, *ok) == EINVAL
+    assert L.qmv_int4_gs(p, p, 8, 64, 32, p, p, 1, *ok) == EINVAL      # gs != 64
+    assert L.qmv_int4_gs(p, p, 0, 64, 64, p, p, 1, *ok) == EINVAL      # N < 1
+    assert L.qmv_int4_gs(p, p, 8, 64, 64, p, p, 0, *ok) == EINVAL      # S < 1
+    assert L.qmv_int4_gs(p, p, 8, 96, 64, p, p, 1, *ok) == ESHAPE      # ragged K
+    assert L.qmv_int4_gs(p, p, 8, 0, 64, p, p, 1, *ok) == ESHAPE
+    assert L.qmv_int4_gs(ctypes.c_void_p(FAKE + 8), p, 8, 64, 64, p, p, 1, *ok) == EALIGN
+    assert L.qmv_int4_gs(p, ctypes.c_void_p(FAKE + 2), 8, 64, 64, p, p, 1, *ok) == EALIGN
+    assert L.qmv_int4_gs(p, p, 8, 64, 64, p, p, 1, None, need, None) == EWORKSPACE
+    assert L.qmv_int4_gs(p, p, 8, 64, 64, p, p, 1, p, need - 1, None) == EWORKSPACE
+    assert L.qmv_int4_gs(p, p, 8, 64, 64, p, p, 1, ctypes.c_void_p(FAKE + 128), need, None) == EWORKSPACE
+    assert L.qmv_int8_row(p, None, 8, 64, p, p, 1, *ok) == EINVAL
+    assert L.qmv_int8_row(p, p, 8, 100, p, p, 1, *ok) == ESHAPE
+    assert L.qmv_int8_row(ctypes.c_void_p(FAKE + 4), p, 8, 64, p, p, 1, *ok) == EALIGN
+    assert L.qmv_int8_row(p, p, 8, 64, p, p, 1, p, 0, None) == EWORKSPACE
 
 
 def test_route_and_group_validation(L):

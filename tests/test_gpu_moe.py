@@ -155,7 +155,7 @@ def test_w3_hidden(pool_160):
 
 
 @pytest.mark.parametrize("T,k,E,H,I", [(5, 3, 6, 128, 192), (33, 2, 7, 64, 64), (1, 1, 1, 256, 128),
-                                       (40, 4, 3, 192, 320), (2, 8, 8, 1024, 512)])
+                                       (40, 3, 3, 192, 320), (2, 8, 8, 1024, 512)])
 def test_ffn_shapes(T, k, E, H, I):
     """Odd shapes: ragged token counts per expert, > 16 tokens on one expert
     (several passes), a single expert, k = E."""
