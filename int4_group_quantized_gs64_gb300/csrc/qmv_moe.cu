@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(1024)
     k_passes(const int32_t *__restrict__ offsets, const int32_t *__restrict__ uexp,
              const int32_t *__restrict__ n_used, int32_t *pass_ofs) {
     __shared__ int32_t tot[96];
+    __shared__ int32_t s_last;
     const int nu = *n_used;
     int carry = 0;
     for (int base = 0; base < nu; base += 1024) {
@@ -217,9 +218,9 @@ __global__ void __launch_bounds__(1024)
         int ea, eb, ec;
         block_scan3(np, 0, 0, ea, eb, ec, tot);
         if (u < nu) pass_ofs[u] = carry + ea;
-        if (threadIdx.x == 1023) tot[95] = ea + np;
+        if (threadIdx.x == 1023) s_last = ea + np;
         __syncthreads();
-        carry += tot[95];
+        carry += s_last;
         __syncthreads();
     }
     if (threadIdx.x == 0) pass_ofs[nu] = carry;
