@@ -122,23 +122,27 @@ __device__ __forceinline__ void dequant_int8_word(uint32_t w, uint32_t &pa, uint
 
 // ------------------------------------------------------------------ activation fragments
 //
-// Activation fragment layout. For a row v[K] (one token's activations) and a
-// group g, MMA step m (0..3) and quad lane q (0..3), one 16-byte cell holds
-//   { hi(b0), hi(b1), lo(b0), lo(b1) }
-// with b0 = half2(v[k0], v[k1]), b1 = half2(v[k2], v[k3]) and the k's of the
-// weight format's register order:
-//   int4: kA = 64g + 16q + 8(m/2) + 2(m%2); (k0, k1, k2, k3) = (kA, kA+4, kA+1, kA+5)
-//   int8: kA = 64g + 16q + 4m;              (k0, k1, k2, k3) = (kA, kA+2, kA+1, kA+3)
-// Cells are stored [g][m][q] per row (256 bytes per group), rows contiguous.
+// Activation fragment layout. For one row v[K] (a token's activations,
+// already multiplied by the group's power-of-two factor) and one 64-wide
+// group, the B operands of the four MMA steps m = 0..3 for quad lane q are
+//   b0(m, q) = half2(v[k0], v[k1]),  b1(m, q) = half2(v[k2], v[k3])
+// with the k's of the weight format's register order:
+//   int4: kA = 16q + 8(m/2) + 2(m%2); (k0, k1, k2, k3) = (kA, kA+4, kA+1, kA+5)
+//   int8: kA = 16q + 4m;              (k0, k1, k2, k3) = (kA, kA+2, kA+1, kA+3)
+// Each value is split into hi = fp16(v) and lo = fp16(v - hi) ("part" 0 / 1).
+// A group of one row is 16 units of 16 bytes (256 bytes):
+//   unit (mh, q, part), index (mh*4 + q)*2 + part, holds
+//   { b0(2mh, q), b1(2mh, q), b0(2mh+1, q), b1(2mh+1, q) } of that part,
+// so a lane fetches the operands of two MMA steps with one 16-byte load, and
+// the 32 lanes of a warp read 512 contiguous bytes (no bank conflicts).
 
 template <bool kInt8>
-__device__ __forceinline__ void frag_ks(int g, int m, int q, int &k0, int &k1, int &k2,
-                                        int &k3) {
+__device__ __forceinline__ void frag_ks(int m, int q, int &k0, int &k1, int &k2, int &k3) {
     if (!kInt8) {
-        const int kA = g * kGroup + 16 * q + 8 * (m >> 1) + 2 * (m & 1);
+        const int kA = 16 * q + 8 * (m >> 1) + 2 * (m & 1);
         k0 = kA; k1 = kA + 4; k2 = kA + 1; k3 = kA + 5;
     } else {
-        const int kA = g * kGroup + 16 * q + 4 * m;
+        const int kA = 16 * q + 4 * m;
         k0 = kA; k1 = kA + 2; k2 = kA + 1; k3 = kA + 3;
     }
 }
@@ -147,19 +151,27 @@ __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
     return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
 
-// Split four scaled values into the 16-byte fragment cell.
-__device__ __forceinline__ uint4 make_cell(float v0, float v1, float v2, float v3) {
-    const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-    const __half h2 = __float2half_rn(v2), h3 = __float2half_rn(v3);
-    const __half l0 = __float2half_rn(v0 - __half2float(h0));
-    const __half l1 = __float2half_rn(v1 - __half2float(h1));
-    const __half l2 = __float2half_rn(v2 - __half2float(h2));
-    const __half l3 = __float2half_rn(v3 - __half2float(h3));
-    return make_uint4(pack_half2(h0, h1), pack_half2(h2, h3), pack_half2(l0, l1),
-                      pack_half2(l2, l3));
+__device__ __forceinline__ __half split_part(float v, int part) {
+    const __half h = __float2half_rn(v);
+    return part ? __float2half_rn(v - __half2float(h)) : h;
 }
 
-// Power-of-two exponent that maps max|v| into [2^13, 2^14); 0 for an all-zero row.
+// Unit u (0..15) of a group, from its 64 scaled values v[0..63].
+template <bool kInt8>
+__device__ __forceinline__ uint4 make_unit(const float *v, int u) {
+    const int part = u & 1, q = (u >> 1) & 3, mh = u >> 3;
+    uint32_t r[4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        int k0, k1, k2, k3;
+        frag_ks<kInt8>(2 * mh + i, q, k0, k1, k2, k3);
+        r[2 * i] = pack_half2(split_part(v[k0], part), split_part(v[k1], part));
+        r[2 * i + 1] = pack_half2(split_part(v[k2], part), split_part(v[k3], part));
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// Power-of-two exponent that maps max|v| into [2^13, 2^14); 0 for an all-zero group.
 __device__ __forceinline__ int split_exponent(float amax) {
     if (!(amax > 0.0f) || !isfinite(amax)) return 0;
     int e;
@@ -177,74 +189,60 @@ __device__ __forceinline__ float warp_max(float v) {
 // ------------------------------------------------------------------ tile compute
 //
 // One warp computes a 16-row tile for up to 4*NB tokens. Lane (gid = lane/4,
-// q = lane%4) owns rows gid and gid+8 of the tile; after the MMA it holds, for
-// token 4*nb + q, the values of rows gid (d[0] + d[1]: hi + lo columns) and
-// gid+8 (d[2] + d[3]).
-//
-// Activation cells of the current chunk sit in shared memory as
-// cell[(gl*4 + m)*4 + q][s] (16 bytes each, ntok cells per (gl, m, q)).
+// q = lane%4) owns rows gid and gid+8; after the MMAs it holds, for token
+// 4*nb + q, rows gid (d[0] + d[1]: hi + lo columns) and gid+8 (d[2] + d[3]).
+// bp[nb] points at the lane's first unit of the current group for block nb
+// (token 4*nb + gid/2, clamped to the last token, part gid & 1); units of
+// the same lane for mh = 1 sit 8 units further.
 
 template <int NB>
-__device__ __forceinline__ void load_b(const uint4 *cells, int ntok, int gl, int m, int q,
-                                       int gid, int nb, uint32_t &b0, uint32_t &b1) {
-    const int s = 4 * nb + (gid >> 1);
-    if (s < ntok) {
-        const uint2 *p = reinterpret_cast<const uint2 *>(cells + ((gl * 4 + m) * 4 + q) * ntok + s);
-        const uint2 v = p[gid & 1];
-        b0 = v.x;
-        b1 = v.y;
-    } else {
-        b0 = 0u;
-        b1 = 0u;
-    }
-}
-
-// Group partials of one int4 16-row tile: words (x, y) of rows gid / gid+8.
-template <int NB>
-__device__ __forceinline__ void tile_group_int4(uint2 w0, uint2 w8, const uint4 *cells, int ntok,
-                                                int gl, int q, int gid, float d[NB][4]) {
+__device__ __forceinline__ void tile_group_int4(uint2 w0, uint2 w8, const uint4 *const bp[NB],
+                                                float d[NB][4]) {
     uint32_t p0[4], p8[4], a[4];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) d[nb][0] = d[nb][1] = d[nb][2] = d[nb][3] = 0.0f;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        dequant_int4_word(half ? w0.y : w0.x, p0);
-        dequant_int4_word(half ? w8.y : w8.x, p8);
+    for (int mh = 0; mh < 2; ++mh) {
+        uint4 b[NB];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) b[nb] = bp[nb][8 * mh];
+        dequant_int4_word(mh ? w0.y : w0.x, p0);
+        dequant_int4_word(mh ? w8.y : w8.x, p8);
 #pragma unroll
         for (int mm = 0; mm < 2; ++mm) {
-            const int m = 2 * half + mm;
             a[0] = p0[2 * mm];
             a[1] = p8[2 * mm];
             a[2] = p0[2 * mm + 1];
             a[3] = p8[2 * mm + 1];
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-                uint32_t b0, b1;
-                load_b<NB>(cells, ntok, gl, m, q, gid, nb, b0, b1);
-                mma_16816(d[nb], a, b0, b1);
-            }
+            for (int nb = 0; nb < NB; ++nb)
+                mma_16816(d[nb], a, mm ? b[nb].z : b[nb].x, mm ? b[nb].w : b[nb].y);
         }
     }
 }
 
-// Same for int8: 16 bytes of row gid (w0) and of row gid+8 (w8).
+// int8: 16 bytes of row gid (w0) and of row gid+8 (w8); MMA step m uses word m.
 template <int NB>
-__device__ __forceinline__ void tile_group_int8(uint4 w0, uint4 w8, const uint4 *cells, int ntok,
-                                                int gl, int q, int gid, float d[NB][4]) {
+__device__ __forceinline__ void tile_group_int8(uint4 w0, uint4 w8, const uint4 *const bp[NB],
+                                                float d[NB][4]) {
     const uint32_t r0[4] = {w0.x, w0.y, w0.z, w0.w};
     const uint32_t r8[4] = {w8.x, w8.y, w8.z, w8.w};
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) d[nb][0] = d[nb][1] = d[nb][2] = d[nb][3] = 0.0f;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        uint32_t a[4];
-        dequant_int8_word(r0[m], a[0], a[2]);
-        dequant_int8_word(r8[m], a[1], a[3]);
+    for (int mh = 0; mh < 2; ++mh) {
+        uint4 b[NB];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-            uint32_t b0, b1;
-            load_b<NB>(cells, ntok, gl, m, q, gid, nb, b0, b1);
-            mma_16816(d[nb], a, b0, b1);
+        for (int nb = 0; nb < NB; ++nb) b[nb] = bp[nb][8 * mh];
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm) {
+            const int m = 2 * mh + mm;
+            uint32_t a[4];
+            dequant_int8_word(r0[m], a[0], a[2]);
+            dequant_int8_word(r8[m], a[1], a[3]);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+                mma_16816(d[nb], a, mm ? b[nb].z : b[nb].x, mm ? b[nb].w : b[nb].y);
         }
     }
 }

@@ -21,6 +21,8 @@ namespace qmv {
 namespace {
 
 constexpr int kDenseWarps = 4;                 // 64-row items
+constexpr int kDenseStages = 8;                // weight stages per warp ring
+constexpr int kDenseRing = kDenseStages * kStageBytes;
 constexpr int kDenseBudget = 32 * 1024;
 
 // ------------------------------------------------------------------ split
@@ -43,12 +45,7 @@ __global__ void __launch_bounds__(256)
         buf[warp][lane] = a * mul;
         buf[warp][32 + lane] = b * mul;
         __syncwarp();
-        if (lane < 16) {
-            int k0, k1, k2, k3;
-            frag_ks<kInt8>(0, lane >> 2, lane & 3, k0, k1, k2, k3);
-            cells[((size_t)r * G + g) * 16 + lane] =
-                make_cell(buf[warp][k0], buf[warp][k1], buf[warp][k2], buf[warp][k3]);
-        }
+        if (lane < 16) cells[((size_t)r * G + g) * 16 + lane] = make_unit<kInt8>(buf[warp], lane);
         if (lane == 0) fac[(size_t)r * G + g] = ldexpf(1.0f, -e);
         __syncwarp();
     }
@@ -101,15 +98,15 @@ __global__ void __launch_bounds__(32 * kDenseWarps)
         return TileSrc{w + (size_t)row0 * rowBytes, kInt8 ? nullptr : scales + (size_t)row0 * G,
                        rowBytes, nrows};
     };
-    WarpStream<kInt8, decltype(tile)> ws{smem + warp * kRingBytes, tile, G, ns, (i1 - i0) * ns,
+    WarpStream<kInt8, kDenseStages, decltype(tile)> ws{smem + warp * kDenseRing, tile, G, ns, (i1 - i0) * ns,
                                          0, warp, lane};
     ws.prologue();  // weights are call inputs: safe to read before the wait
 
     pdl_wait();     // cells and factors come from k_split
     pdl_trigger();
     if (threadIdx.x < kMaxTok) s_rows[threadIdx.x] = threadIdx.x;
-    uint4 *cells = reinterpret_cast<uint4 *>(smem + kDenseWarps * kRingBytes);
-    float *fac = reinterpret_cast<float *>(smem + kDenseWarps * kRingBytes + kDenseBudget);
+    uint4 *cells = reinterpret_cast<uint4 *>(smem + kDenseWarps * kDenseRing);
+    float *fac = reinterpret_cast<float *>(smem + kDenseWarps * kDenseRing + kDenseBudget);
     const StageCells stage{xcells, xfac, s_rows, ntok, G};
 
     for (int it = 0; it < i1 - i0; ++it) {
@@ -117,10 +114,8 @@ __global__ void __launch_bounds__(32 * kDenseWarps)
         const bool reuse = it > 0;
         if (ntok <= 4)
             dense_item<1, kInt8>(ws, it, row0, N, scales, y, cells, fac, ntok, reuse, stage);
-        else if (ntok <= 8)
-            dense_item<2, kInt8>(ws, it, row0, N, scales, y, cells, fac, ntok, reuse, stage);
         else
-            dense_item<4, kInt8>(ws, it, row0, N, scales, y, cells, fac, ntok, reuse, stage);
+            dense_item<2, kInt8>(ws, it, row0, N, scales, y, cells, fac, ntok, reuse, stage);
     }
     cp_async_wait<0>();
 }
@@ -128,7 +123,7 @@ __global__ void __launch_bounds__(32 * kDenseWarps)
 template <bool kInt8>
 cudaError_t launch_dense(const uint8_t *w, const float *scales, int N, int K, const float *x,
                          float *y, int S, void *xcells, float *xfac, cudaStream_t st) {
-    const size_t smem = engine_smem(kDenseWarps, kDenseBudget, 0);
+    const size_t smem = engine_smem(kDenseWarps, kDenseStages, kDenseBudget, 0);
     cudaError_t e = set_smem(k_dense<kInt8>, smem);
     if (e != cudaSuccess) return e;
     const int nitems = (N + 16 * kDenseWarps - 1) / (16 * kDenseWarps);

@@ -174,12 +174,7 @@ __device__ void split_row_cta(const float *__restrict__ row, int K, uint4 *cells
         buf[warp][lane] = a * mul;
         buf[warp][32 + lane] = b * mul;
         __syncwarp();
-        if (lane < 16) {
-            int k0, k1, k2, k3;
-            frag_ks<false>(0, lane >> 2, lane & 3, k0, k1, k2, k3);
-            cells[(size_t)g * 16 + lane] =
-                make_cell(buf[warp][k0], buf[warp][k1], buf[warp][k2], buf[warp][k3]);
-        }
+        if (lane < 16) cells[(size_t)g * 16 + lane] = make_unit<false>(buf[warp], lane);
         if (lane == 0) fac[g] = ldexpf(1.0f, -e);
         __syncwarp();
     }
@@ -285,7 +280,9 @@ struct MoeTile {
 };
 
 constexpr int kMoeWarps = 8;
-constexpr int kMoeBudget = 64 * 1024;
+constexpr int kMoeStages = 4;  // 2 CTAs (16 warps) per SM
+constexpr int kMoeRing = kMoeStages * kStageBytes;
+constexpr int kMoeBudget = 32 * 1024;
 constexpr int kEpiBytes = (2 * 64 * kMaxTok + kMoeWarps * 64) * 4;
 
 __device__ __forceinline__ void cta_items(int total, int &i0, int &i1) {
@@ -302,8 +299,8 @@ __device__ __forceinline__ void gate_up_item(WS &ws, int it, int jt, const PassI
                                              const int *s_pair) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
     const int ntok = pinf.ntok;
-    uint4 *cells = reinterpret_cast<uint4 *>(smem + kMoeWarps * kRingBytes);
-    float *fac = reinterpret_cast<float *>(smem + kMoeWarps * kRingBytes + kMoeBudget);
+    uint4 *cells = reinterpret_cast<uint4 *>(smem + kMoeWarps * kMoeRing);
+    float *fac = reinterpret_cast<float *>(smem + kMoeWarps * kMoeRing + kMoeBudget);
     float *gbuf = fac + kMoeBudget / 256;
     float *hbuf = gbuf + 64 * kMaxTok;
     float *wbuf = hbuf + 64 * kMaxTok;
@@ -350,19 +347,14 @@ __device__ __forceinline__ void gate_up_item(WS &ws, int it, int jt, const PassI
         wbuf[warp * 64 + 32 + lane] = b * mul;
         __syncwarp();
         const size_t cb = (size_t)s_pair[s] * Gd + jt;
-        if (lane < 16) {
-            int k0, k1, k2, k3;
-            frag_ks<false>(0, lane >> 2, lane & 3, k0, k1, k2, k3);
-            hcells[cb * 16 + lane] = make_cell(wbuf[warp * 64 + k0], wbuf[warp * 64 + k1],
-                                               wbuf[warp * 64 + k2], wbuf[warp * 64 + k3]);
-        }
+        if (lane < 16) hcells[cb * 16 + lane] = make_unit<false>(wbuf + warp * 64, lane);
         if (lane == 0) hfac[cb] = ldexpf(1.0f, -e);
         __syncwarp();
     }
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(32 * kMoeWarps, 1)
+__global__ void __launch_bounds__(32 * kMoeWarps, 2)
     k_gate_up(MoeDims m, const uint4 *__restrict__ xcells, const float *__restrict__ xfac, int k,
               const int32_t *__restrict__ offsets, const int32_t *__restrict__ list,
               const int32_t *__restrict__ uexp, const int32_t *__restrict__ n_used,
@@ -381,10 +373,10 @@ __global__ void __launch_bounds__(32 * kMoeWarps, 1)
     int i0, i1;
     cta_items(total, i0, i1);
     if (i0 >= i1) return;
-    const int ns = G / 4;
+    const int ns = (G + 3) / 4;
     MoeTile tile{m.gu_q, m.gu_s, pass_ofs, uexp, offsets, (size_t)2 * I * (H / 2),
                  (size_t)2 * I * G, (size_t)H / 2, G, tiles, nu, i0, 0, 2 * I, 1};
-    WarpStream<false, MoeTile> ws{smem + warp * kRingBytes, tile, G, ns, (i1 - i0) * ns, 0,
+    WarpStream<false, kMoeStages, MoeTile> ws{smem + warp * kMoeRing, tile, G, ns, (i1 - i0) * ns, 0,
                                   warp, lane};
     ws.prologue();
 
@@ -406,10 +398,8 @@ __global__ void __launch_bounds__(32 * kMoeWarps, 1)
         const StageCells stage{xcells, xfac, s_rows, pinf.ntok, G};
         if (pinf.ntok <= 4)
             gate_up_item<1>(ws, it, jt, pinf, reuse, stage, I, k, h, hcells, hfac, smem, s_pair);
-        else if (pinf.ntok <= 8)
-            gate_up_item<2>(ws, it, jt, pinf, reuse, stage, I, k, h, hcells, hfac, smem, s_pair);
         else
-            gate_up_item<4>(ws, it, jt, pinf, reuse, stage, I, k, h, hcells, hfac, smem, s_pair);
+            gate_up_item<2>(ws, it, jt, pinf, reuse, stage, I, k, h, hcells, hfac, smem, s_pair);
     }
     cp_async_wait<0>();
 }
@@ -421,8 +411,8 @@ __device__ __forceinline__ void down_item(WS &ws, int it, int tl, const PassInfo
                                           bool reuse, const StageCells &stage, int H, float *y,
                                           uint8_t *smem, const int *s_pair) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
-    uint4 *cells = reinterpret_cast<uint4 *>(smem + kMoeWarps * kRingBytes);
-    float *fac = reinterpret_cast<float *>(smem + kMoeWarps * kRingBytes + kMoeBudget);
+    uint4 *cells = reinterpret_cast<uint4 *>(smem + kMoeWarps * kMoeRing);
+    float *fac = reinterpret_cast<float *>(smem + kMoeWarps * kMoeRing + kMoeBudget);
     float acc[NB][2];
     run_item<NB, false>(ws, it, cells, fac, kMoeBudget, pinf.ntok, reuse, stage, acc);
     const int row0 = tl * 128 + 16 * warp;
@@ -437,7 +427,7 @@ __device__ __forceinline__ void down_item(WS &ws, int it, int tl, const PassInfo
     }
 }
 
-__global__ void __launch_bounds__(32 * kMoeWarps, 1)
+__global__ void __launch_bounds__(32 * kMoeWarps, 2)
     k_down(MoeDims m, const uint4 *__restrict__ hcells, const float *__restrict__ hfac,
            const int32_t *__restrict__ offsets, const int32_t *__restrict__ list,
            const int32_t *__restrict__ uexp, const int32_t *__restrict__ n_used,
@@ -454,10 +444,10 @@ __global__ void __launch_bounds__(32 * kMoeWarps, 1)
     const int total = pass_ofs[nu] * tiles;
     int i0, i1;
     cta_items(total, i0, i1);
-    const int ns = G / 4;
+    const int ns = (G + 3) / 4;
     MoeTile tile{m.dn_q, m.dn_s, pass_ofs, uexp, offsets, (size_t)H * (I / 2), (size_t)H * G,
                  (size_t)I / 2, G, tiles, nu, i0, 0, H, 0};
-    WarpStream<false, MoeTile> ws{smem + warp * kRingBytes, tile, G, ns, (i1 - i0) * ns, 0,
+    WarpStream<false, kMoeStages, MoeTile> ws{smem + warp * kMoeRing, tile, G, ns, (i1 - i0) * ns, 0,
                                   warp, lane};
     ws.prologue();
     pdl_wait();  // h cells come from the gate+up kernel
@@ -477,10 +467,8 @@ __global__ void __launch_bounds__(32 * kMoeWarps, 1)
         const StageCells stage{hcells, hfac, s_pair, pinf.ntok, G};
         if (pinf.ntok <= 4)
             down_item<1>(ws, it, tl, pinf, reuse, stage, H, y, smem, s_pair);
-        else if (pinf.ntok <= 8)
-            down_item<2>(ws, it, tl, pinf, reuse, stage, H, y, smem, s_pair);
         else
-            down_item<4>(ws, it, tl, pinf, reuse, stage, H, y, smem, s_pair);
+            down_item<2>(ws, it, tl, pinf, reuse, stage, H, y, smem, s_pair);
     }
     cp_async_wait<0>();
 }
@@ -506,7 +494,7 @@ __global__ void __launch_bounds__(256)
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-size_t moe_smem() { return engine_smem(kMoeWarps, kMoeBudget, kEpiBytes); }
+size_t moe_smem() { return engine_smem(kMoeWarps, kMoeStages, kMoeBudget, kEpiBytes); }
 
 int moe_grid(void (*k)(MoeDims, const uint4 *, const float *, int, const int32_t *,
                        const int32_t *, const int32_t *, const int32_t *, const int32_t *,

@@ -5,8 +5,8 @@
 // bypass L1). A stage holds 128 bytes of each of the 16 rows (4 int4 groups or
 // 2 int8 groups) plus the 16 x 4 group scales. The 16-byte chunks of a row are
 // XOR-swizzled by (row & 7) so the fragment reads below are bank-conflict free.
-// kStages - 1 stages (~11.5 KB per warp) are in flight while one is consumed,
-// without holding any of it in registers.
+// NS - 1 stages are in flight while one is consumed, without holding any of
+// it in registers.
 //
 // Work: a CTA walks a contiguous range of work items (an item is one row tile
 // of every warp, e.g. 64 or 128 rows of one expert matrix); the warp rings run
@@ -21,11 +21,9 @@
 
 namespace qmv {
 
-constexpr int kStages = 6;
 constexpr int kStageWBytes = 16 * 128;                 // weights of one stage
 constexpr int kStageBytes = kStageWBytes + 16 * 4 * 4; // + 16 rows x 4 scales
-constexpr int kRingBytes = kStages * kStageBytes;      // per warp
-constexpr int kMaxTok = 16;                            // tokens per pass (4 MMA blocks)
+constexpr int kMaxTok = 8;                             // tokens per pass (2 MMA blocks)
 
 template <bool kInt8>
 struct Fmt {
@@ -111,57 +109,66 @@ __device__ __forceinline__ void issue_stage(uint8_t *slot, const TileSrc &t, int
     }
 }
 
-// Activation cells of the current chunk: cells[(gl*4 + m)*4 + q][s] (16 B),
-// factors fac[gl][s].
-struct Chunk {
-    const uint4 *cells;
-    const float *fac;
-    int ntok;
-};
-
 // Consume one stage: groups [g0, g0 + GPS) of the chunk starting at group gc,
-// stopping at gEnd. Accumulates scale * factor * (hi + lo) per row and token.
+// stopping at gEnd. Activation units of the chunk are cells[gl][s][16] and
+// factors fac[gl][s] (gl = g - gc, s < ntok). Accumulates
+// scale * factor * (hi + lo) per row and token.
 template <int NB, bool kInt8>
 __device__ __forceinline__ void compute_stage(const uint8_t *slot, int g0, int gc, int gEnd,
-                                              const Chunk &ch, float c2[2][NB][2]) {
+                                              const uint4 *cells, const float *fac, int ntok,
+                                              float c2[2][NB][2]) {
     const int lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
-    const float *ss = reinterpret_cast<const float *>(slot + kStageWBytes);
+    float4 sA = make_float4(1.f, 1.f, 1.f, 1.f), sB = sA;
+    if constexpr (!kInt8) {
+        const float *ss = reinterpret_cast<const float *>(slot + kStageWBytes);
+        sA = *reinterpret_cast<const float4 *>(ss + gid * 4);
+        sB = *reinterpret_cast<const float4 *>(ss + (gid + 8) * 4);
+    }
+    const float sa[4] = {sA.x, sA.y, sA.z, sA.w}, sb[4] = {sB.x, sB.y, sB.z, sB.w};
+    int sB_tok[NB], sD_tok[NB];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        sB_tok[nb] = min(4 * nb + (gid >> 1), ntok - 1);  // token of this lane's B column
+        sD_tok[nb] = min(4 * nb + q, ntok - 1);           // token of this lane's D columns
+    }
 #pragma unroll
     for (int gl = 0; gl < Fmt<kInt8>::kGPS; ++gl) {
         const int g = g0 + gl;
         if (g < gEnd) {
+            const int glc = g - gc;
+            const uint4 *bp[NB];
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+                bp[nb] = cells + (glc * ntok + sB_tok[nb]) * 16 + q * 2 + (gid & 1);
             float dd[NB][4];
-            float s0 = 1.0f, s8 = 1.0f;
             if constexpr (kInt8) {
                 const int c = 4 * gl + q;
                 const uint4 w0 = *reinterpret_cast<const uint4 *>(slot + gid * 128 + ((c ^ gid) << 4));
                 const uint4 w8 =
                     *reinterpret_cast<const uint4 *>(slot + (gid + 8) * 128 + ((c ^ gid) << 4));
-                tile_group_int8<NB>(w0, w8, ch.cells, ch.ntok, g - gc, q, gid, dd);
+                tile_group_int8<NB>(w0, w8, bp, dd);
             } else {
                 const int c = 2 * gl + (q >> 1);
                 const int off = ((c ^ gid) << 4) + ((q & 1) << 3);
                 const uint2 w0 = *reinterpret_cast<const uint2 *>(slot + gid * 128 + off);
                 const uint2 w8 = *reinterpret_cast<const uint2 *>(slot + (gid + 8) * 128 + off);
-                s0 = ss[gid * 4 + gl];
-                s8 = ss[(gid + 8) * 4 + gl];
-                tile_group_int4<NB>(w0, w8, ch.cells, ch.ntok, g - gc, q, gid, dd);
+                tile_group_int4<NB>(w0, w8, bp, dd);
             }
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
-                const int s = 4 * nb + q;
-                const float f = s < ch.ntok ? ch.fac[(g - gc) * ch.ntok + s] : 0.0f;
-                c2[gl & 1][nb][0] = fmaf(s0 * f, dd[nb][0] + dd[nb][1], c2[gl & 1][nb][0]);
-                c2[gl & 1][nb][1] = fmaf(s8 * f, dd[nb][2] + dd[nb][3], c2[gl & 1][nb][1]);
+                const float f = fac[glc * ntok + sD_tok[nb]];
+                c2[gl & 1][nb][0] = fmaf(sa[gl] * f, dd[nb][0] + dd[nb][1], c2[gl & 1][nb][0]);
+                c2[gl & 1][nb][1] = fmaf(sb[gl] * f, dd[nb][2] + dd[nb][3], c2[gl & 1][nb][1]);
             }
         }
     }
 }
 
-// Per-warp weight stream over the CTA's items. TileFn(item, warp) -> TileSrc.
-template <bool kInt8, class TileFn>
+// Per-warp weight stream over the CTA's items, NS stages deep.
+// TileFn(item, warp) -> TileSrc.
+template <bool kInt8, int NS, class TileFn>
 struct WarpStream {
-    uint8_t *ring;  // this warp's kRingBytes
+    uint8_t *ring;  // this warp's NS * kStageBytes
     TileFn tile;
     int G, ns, total;  // groups per row, stages per item, stages of all items
     int next;          // next global stage to issue
@@ -170,20 +177,20 @@ struct WarpStream {
     __device__ __forceinline__ void issue_next() {
         if (next < total) {
             const int item = next / ns, s = next - item * ns;
-            issue_stage<kInt8>(ring + (next % kStages) * kStageBytes, tile(item, warp), s, G, lane);
+            issue_stage<kInt8>(ring + (next % NS) * kStageBytes, tile(item, warp), s, G, lane);
         }
         cp_async_commit();  // possibly empty: keeps the group count uniform
         ++next;
     }
     __device__ __forceinline__ void prologue() {
-        for (int i = 0; i < kStages - 1; ++i) issue_next();
+        for (int i = 0; i < NS - 1; ++i) issue_next();
     }
     // Wait for stage j (global index), refill the slot freed by stage j-1.
     __device__ __forceinline__ const uint8_t *acquire(int j) {
-        cp_async_wait<kStages - 2>();
+        cp_async_wait<NS - 2>();
         __syncwarp();
         issue_next();
-        return ring + (j % kStages) * kStageBytes;
+        return ring + (j % NS) * kStageBytes;
     }
 };
 
@@ -191,8 +198,8 @@ struct WarpStream {
 // `stage(gc, ng, cells, fac)` (all threads; no barriers inside) unless
 // `reuse` says the previous item left the full K in shared memory.
 // acc[nb][0 / 1]: rows gid / gid+8 of this warp, token 4*nb + q.
-template <int NB, bool kInt8, class TileFn, class Stage>
-__device__ __forceinline__ void run_item(WarpStream<kInt8, TileFn> &ws, int item, uint4 *cells,
+template <int NB, bool kInt8, int NS, class TileFn, class Stage>
+__device__ __forceinline__ void run_item(WarpStream<kInt8, NS, TileFn> &ws, int item, uint4 *cells,
                                          float *fac, int budget, int ntok, bool reuse,
                                          const Stage &stage, float acc[NB][2]) {
     const int G = ws.G;
@@ -208,7 +215,6 @@ __device__ __forceinline__ void run_item(WarpStream<kInt8, TileFn> &ws, int item
             stage(gc, ng, cells, fac);
             __syncthreads();
         }
-        const Chunk ch{cells, fac, ntok};
         float c2[2][NB][2];
 #pragma unroll
         for (int h = 0; h < 2; ++h)
@@ -216,7 +222,7 @@ __device__ __forceinline__ void run_item(WarpStream<kInt8, TileFn> &ws, int item
             for (int nb = 0; nb < NB; ++nb) c2[h][nb][0] = c2[h][nb][1] = 0.0f;
         for (int g0 = gc; g0 < gc + ng; g0 += GPS, ++j) {
             const uint8_t *slot = ws.acquire(j);
-            compute_stage<NB, kInt8>(slot, g0, gc, gc + ng, ch, c2);
+            compute_stage<NB, kInt8>(slot, g0, gc, gc + ng, cells, fac, ntok, c2);
         }
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
@@ -226,23 +232,23 @@ __device__ __forceinline__ void run_item(WarpStream<kInt8, TileFn> &ws, int item
     }
 }
 
-// Stages cells + factors of `ntok` activation rows (cell rows `rows[s]`,
-// layout [row][G][16] uint4 and [row][G] factors) for groups [gc, gc+ng).
+// Stages units + factors of `ntok` activation rows (rows `rows[s]` of the
+// global layout [row][G][16 units] and [row][G] factors) for groups
+// [gc, gc+ng) into cells[gl][s][16] and fac[gl][s].
 struct StageCells {
     const uint4 *src;
     const float *fsrc;
     const int *rows;  // shared memory
     int ntok, G;
     __device__ __forceinline__ void operator()(int gc, int ng, uint4 *cells, float *fac) const {
-        const int total = ng * 16 * ntok;
+        const int total = ng * ntok * 16;
         for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-            const int s = idx % ntok;
-            const int r = idx / ntok;
-            cells[idx] = src[(size_t)rows[s] * G * 16 + (size_t)gc * 16 + r];
+            const int u = idx & 15, r = idx >> 4;
+            const int s = r % ntok, gl = r / ntok;
+            cells[idx] = src[((size_t)rows[s] * G + gc + gl) * 16 + u];
         }
         for (int idx = threadIdx.x; idx < ng * ntok; idx += blockDim.x) {
-            const int s = idx % ntok;
-            const int gl = idx / ntok;
+            const int s = idx % ntok, gl = idx / ntok;
             fac[idx] = fsrc[(size_t)rows[s] * G + gc + gl];
         }
     }
@@ -250,8 +256,8 @@ struct StageCells {
 
 // Shared memory of a CTA: `warps` rings, `budget` bytes of cells, factors
 // (ng * ntok <= budget / 256 floats), then `extra` bytes of epilogue scratch.
-__host__ __device__ inline size_t engine_smem(int warps, int budget, int extra) {
-    return (size_t)warps * kRingBytes + budget + budget / 64 + extra;
+__host__ __device__ inline size_t engine_smem(int warps, int stages, int budget, int extra) {
+    return (size_t)warps * stages * kStageBytes + budget + budget / 64 + extra;
 }
 
 }  // namespace qmv
