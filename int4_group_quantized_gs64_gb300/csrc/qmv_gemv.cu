@@ -54,12 +54,12 @@ __global__ void __launch_bounds__(256)
 // ------------------------------------------------------------------ dense
 
 template <int NB, bool kInt8, class WS>
-__device__ __forceinline__ void dense_item(WS &ws, int item, int row0, int N, const float *scales,
+__device__ __forceinline__ void dense_item(WS &ws, int &cslot, int row0, int N, const float *scales,
                                            float *y, uint4 *cells, float *fac, int ntok, bool reuse,
                                            const StageCells &stage) {
     const int lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
     float acc[NB][2];
-    run_item<NB, kInt8>(ws, item, cells, fac, kDenseBudget, ntok, reuse, stage, acc);
+    run_item<NB, kInt8>(ws, cslot, cells, fac, kDenseBudget, ntok, reuse, stage, acc);
     const int rA = row0 + gid, rB = row0 + gid + 8;
     float ra = 1.0f, rb = 1.0f;
     if constexpr (kInt8) {
@@ -76,6 +76,106 @@ __device__ __forceinline__ void dense_item(WS &ws, int item, int row0, int N, co
     }
 }
 
+// Rows of warp wp in item `item` of this CTA's range.
+template <bool kInt8>
+struct DenseTile {
+    const uint8_t *w;
+    const float *scales;
+    size_t rowBytes;
+    int N, G, i0;
+    __device__ __forceinline__ TileSrc operator()(int item, int wp) const {
+        int row0 = (i0 + item) * 16 * kDenseWarps + 16 * wp;
+        int nrows = N - row0;
+        if (nrows <= 0) { row0 = N - 1; nrows = 1; }
+        return TileSrc{w + (size_t)row0 * rowBytes, kInt8 ? nullptr : scales + (size_t)row0 * G,
+                       rowBytes, nrows, G};
+    }
+};
+
+// K-split items: 16 rows per item, warp ks streams groups [ga, gb) of them.
+template <bool kInt8>
+struct DenseSplitTile {
+    const uint8_t *w;
+    const float *scales;
+    size_t rowBytes;
+    int N, G, i0, ga;
+    __device__ __forceinline__ TileSrc operator()(int item, int) const {
+        int row0 = (i0 + item) * 16;
+        int nrows = N - row0;
+        if (nrows <= 0) { row0 = N - 1; nrows = 1; }
+        return TileSrc{w + (size_t)row0 * rowBytes + (size_t)ga * Fmt<kInt8>::kGroupBytes,
+                       kInt8 ? nullptr : scales + (size_t)row0 * G + ga, rowBytes, nrows, G};
+    }
+};
+
+// Dense GEMV for up to 4 tokens whose split activations fit in shared
+// memory: every 16-row item is shared by the 4 warps of the CTA, warp ks
+// taking a quarter of the K groups; partial sums meet in shared memory and
+// are added in warp order (deterministic).
+template <bool kInt8>
+__global__ void __launch_bounds__(32 * kDenseWarps)
+    k_dense_ks(const uint8_t *__restrict__ w, const float *__restrict__ scales, int N, int K,
+               const uint4 *__restrict__ xcells, const float *__restrict__ xfac,
+               float *__restrict__ y, int ntok) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float red[kDenseWarps][16][4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
+    const int G = K / kGroup;
+    const int gq = (G + kDenseWarps - 1) / kDenseWarps;
+    const int ga = min(G, warp * gq), gb = min(G, ga + gq);
+    const int nitems = (N + 15) / 16;
+    const int i0 = (int)((long long)blockIdx.x * nitems / gridDim.x);
+    const int i1 = (int)((long long)(blockIdx.x + 1) * nitems / gridDim.x);
+    const size_t rowBytes = kInt8 ? (size_t)K : (size_t)K / 2;
+
+    DenseSplitTile<kInt8> tile{w, scales, rowBytes, N, G, i0, ga};
+    WarpStream<kInt8, kDenseStages, DenseSplitTile<kInt8>> ws;
+    ws.init(smem + warp * kDenseRing, tile, gb - ga, gb > ga ? i1 - i0 : 0, warp, lane);
+    ws.prologue();  // weights are call inputs: safe to read before the wait
+    int cslot = 0;
+
+    pdl_wait();     // cells and factors come from k_split
+    pdl_trigger();
+    uint4 *cells = reinterpret_cast<uint4 *>(smem + kDenseWarps * kDenseRing);
+    float *fac = reinterpret_cast<float *>(smem + kDenseWarps * kDenseRing + kDenseBudget);
+    for (int idx = threadIdx.x; idx < G * ntok * 16; idx += blockDim.x) {
+        const int u = idx & 15, r = idx >> 4, s = r % ntok, g = r / ntok;
+        cells[idx] = xcells[((size_t)s * G + g) * 16 + u];
+    }
+    for (int idx = threadIdx.x; idx < G * ntok; idx += blockDim.x)
+        fac[idx] = xfac[(size_t)(idx % ntok) * G + idx / ntok];
+    __syncthreads();
+    const int sb = min(gid >> 1, ntok - 1), sd = min(q, ntok - 1);
+    const uint4 *bp0 = cells + (ga * ntok + sb) * 16 + q * 2 + (gid & 1);
+    const float *fp0 = fac + ga * ntok + sd;
+
+    for (int it = 0; it < i1 - i0; ++it) {
+        float acc[1][2] = {{0.f, 0.f}};
+        if (gb > ga) run_staged<kInt8>(ws, cslot, bp0, fp0, ntok, acc);
+        red[warp][gid][q] = acc[0][0];
+        red[warp][gid + 8][q] = acc[0][1];
+        __syncthreads();
+        if (warp == 0 && q < ntok) {
+            const int row0 = (i0 + it) * 16;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < kDenseWarps; ++k) {
+                a0 += red[k][gid][q];
+                a1 += red[k][gid + 8][q];
+            }
+            const int rA = row0 + gid, rB = row0 + gid + 8;
+            if constexpr (kInt8) {
+                if (rA < N) a0 *= scales[rA];
+                if (rB < N) a1 *= scales[rB];
+            }
+            if (rA < N) y[(size_t)q * N + rA] = a0;
+            if (rB < N) y[(size_t)q * N + rB] = a1;
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+}
+
 template <bool kInt8>
 __global__ void __launch_bounds__(32 * kDenseWarps)
     k_dense(const uint8_t *__restrict__ w, const float *__restrict__ scales, int N, int K,
@@ -85,22 +185,16 @@ __global__ void __launch_bounds__(32 * kDenseWarps)
     __shared__ int s_rows[kMaxTok];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = K / kGroup;
-    const int ns = (G + Fmt<kInt8>::kGPS - 1) / Fmt<kInt8>::kGPS;
     const int nitems = (N + 16 * kDenseWarps - 1) / (16 * kDenseWarps);
     const int i0 = (int)((long long)blockIdx.x * nitems / gridDim.x);
     const int i1 = (int)((long long)(blockIdx.x + 1) * nitems / gridDim.x);
     const size_t rowBytes = kInt8 ? (size_t)K : (size_t)K / 2;
 
-    auto tile = [=](int item, int wp) {
-        int row0 = (i0 + item) * 16 * kDenseWarps + 16 * wp;
-        int nrows = N - row0;
-        if (nrows <= 0) { row0 = N - 1; nrows = 1; }
-        return TileSrc{w + (size_t)row0 * rowBytes, kInt8 ? nullptr : scales + (size_t)row0 * G,
-                       rowBytes, nrows};
-    };
-    WarpStream<kInt8, kDenseStages, decltype(tile)> ws{smem + warp * kDenseRing, tile, G, ns, (i1 - i0) * ns,
-                                         0, warp, lane};
+    DenseTile<kInt8> tile{w, scales, rowBytes, N, G, i0};
+    WarpStream<kInt8, kDenseStages, DenseTile<kInt8>> ws;
+    ws.init(smem + warp * kDenseRing, tile, G, i1 - i0, warp, lane);
     ws.prologue();  // weights are call inputs: safe to read before the wait
+    int cslot = 0;
 
     pdl_wait();     // cells and factors come from k_split
     pdl_trigger();
@@ -113,9 +207,9 @@ __global__ void __launch_bounds__(32 * kDenseWarps)
         const int row0 = (i0 + it) * 16 * kDenseWarps + 16 * warp;
         const bool reuse = it > 0;
         if (ntok <= 4)
-            dense_item<1, kInt8>(ws, it, row0, N, scales, y, cells, fac, ntok, reuse, stage);
+            dense_item<1, kInt8>(ws, cslot, row0, N, scales, y, cells, fac, ntok, reuse, stage);
         else
-            dense_item<2, kInt8>(ws, it, row0, N, scales, y, cells, fac, ntok, reuse, stage);
+            dense_item<2, kInt8>(ws, cslot, row0, N, scales, y, cells, fac, ntok, reuse, stage);
     }
     cp_async_wait<0>();
 }
@@ -131,6 +225,19 @@ cudaError_t launch_dense(const uint8_t *w, const float *scales, int N, int K, co
     const int grid = nitems < slots ? nitems : slots;
     e = launch(k_split<kInt8>, dim3(S), dim3(256), 0, st, false, x, K,
                static_cast<uint4 *>(xcells), xfac);
+    const int G = K / kGroup;
+    if (S <= 4 && (size_t)G * S * 256 <= (size_t)kDenseBudget) {
+        // one pass, K split over the 4 warps of a CTA
+        e = (e == cudaSuccess) ? set_smem(k_dense_ks<kInt8>, smem) : e;
+        const int items = (N + 15) / 16;
+        const int slots_ks =
+            sm_count() * max_ctas_per_sm(k_dense_ks<kInt8>, 32 * kDenseWarps, smem);
+        if (e == cudaSuccess)
+            e = launch(k_dense_ks<kInt8>, dim3(items < slots_ks ? items : slots_ks),
+                       dim3(32 * kDenseWarps), smem, st, true, w, scales, N, K,
+                       static_cast<const uint4 *>(xcells), (const float *)xfac, y, S);
+        return e;
+    }
     for (int s0 = 0; s0 < S && e == cudaSuccess; s0 += kMaxTok) {
         const int ntok = S - s0 < kMaxTok ? S - s0 : kMaxTok;
         e = launch(k_dense<kInt8>, dim3(grid), dim3(32 * kDenseWarps), smem, st, true, w, scales, N,

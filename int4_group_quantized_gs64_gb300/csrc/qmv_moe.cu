@@ -293,7 +293,7 @@ __device__ __forceinline__ void cta_items(int total, int &i0, int &i1) {
 // ------------------------------------------------------------------ gate + up + SiLU
 
 template <int NB, class WS>
-__device__ __forceinline__ void gate_up_item(WS &ws, int it, int jt, const PassInfo &pinf,
+__device__ __forceinline__ void gate_up_item(WS &ws, int &cslot, int jt, const PassInfo &pinf,
                                              bool reuse, const StageCells &stage, int I, int k,
                                              float *h, uint4 *hcells, float *hfac, uint8_t *smem,
                                              const int *s_pair) {
@@ -305,7 +305,7 @@ __device__ __forceinline__ void gate_up_item(WS &ws, int it, int jt, const PassI
     float *hbuf = gbuf + 64 * kMaxTok;
     float *wbuf = hbuf + 64 * kMaxTok;
     float acc[NB][2];
-    run_item<NB, false>(ws, it, cells, fac, kMoeBudget, ntok, reuse, stage, acc);
+    run_item<NB, false>(ws, cslot, cells, fac, kMoeBudget, ntok, reuse, stage, acc);
 
     if (warp < 4) {
 #pragma unroll
@@ -373,12 +373,12 @@ __global__ void __launch_bounds__(32 * kMoeWarps, 2)
     int i0, i1;
     cta_items(total, i0, i1);
     if (i0 >= i1) return;
-    const int ns = (G + 3) / 4;
     MoeTile tile{m.gu_q, m.gu_s, pass_ofs, uexp, offsets, (size_t)2 * I * (H / 2),
                  (size_t)2 * I * G, (size_t)H / 2, G, tiles, nu, i0, 0, 2 * I, 1};
-    WarpStream<false, kMoeStages, MoeTile> ws{smem + warp * kMoeRing, tile, G, ns, (i1 - i0) * ns, 0,
-                                  warp, lane};
+    WarpStream<false, kMoeStages, MoeTile> ws;
+    ws.init(smem + warp * kMoeRing, tile, G, i1 - i0, warp, lane);
     ws.prologue();
+    int cslot = 0;
 
     int cur_pi = -1;
     PassInfo pinf{};
@@ -397,9 +397,9 @@ __global__ void __launch_bounds__(32 * kMoeWarps, 2)
         }
         const StageCells stage{xcells, xfac, s_rows, pinf.ntok, G};
         if (pinf.ntok <= 4)
-            gate_up_item<1>(ws, it, jt, pinf, reuse, stage, I, k, h, hcells, hfac, smem, s_pair);
+            gate_up_item<1>(ws, cslot, jt, pinf, reuse, stage, I, k, h, hcells, hfac, smem, s_pair);
         else
-            gate_up_item<2>(ws, it, jt, pinf, reuse, stage, I, k, h, hcells, hfac, smem, s_pair);
+            gate_up_item<2>(ws, cslot, jt, pinf, reuse, stage, I, k, h, hcells, hfac, smem, s_pair);
     }
     cp_async_wait<0>();
 }
@@ -407,14 +407,14 @@ __global__ void __launch_bounds__(32 * kMoeWarps, 2)
 // ------------------------------------------------------------------ down
 
 template <int NB, class WS>
-__device__ __forceinline__ void down_item(WS &ws, int it, int tl, const PassInfo &pinf,
+__device__ __forceinline__ void down_item(WS &ws, int &cslot, int tl, const PassInfo &pinf,
                                           bool reuse, const StageCells &stage, int H, float *y,
                                           uint8_t *smem, const int *s_pair) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
     uint4 *cells = reinterpret_cast<uint4 *>(smem + kMoeWarps * kMoeRing);
     float *fac = reinterpret_cast<float *>(smem + kMoeWarps * kMoeRing + kMoeBudget);
     float acc[NB][2];
-    run_item<NB, false>(ws, it, cells, fac, kMoeBudget, pinf.ntok, reuse, stage, acc);
+    run_item<NB, false>(ws, cslot, cells, fac, kMoeBudget, pinf.ntok, reuse, stage, acc);
     const int row0 = tl * 128 + 16 * warp;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
@@ -444,12 +444,12 @@ __global__ void __launch_bounds__(32 * kMoeWarps, 2)
     const int total = pass_ofs[nu] * tiles;
     int i0, i1;
     cta_items(total, i0, i1);
-    const int ns = (G + 3) / 4;
     MoeTile tile{m.dn_q, m.dn_s, pass_ofs, uexp, offsets, (size_t)H * (I / 2), (size_t)H * G,
                  (size_t)I / 2, G, tiles, nu, i0, 0, H, 0};
-    WarpStream<false, kMoeStages, MoeTile> ws{smem + warp * kMoeRing, tile, G, ns, (i1 - i0) * ns, 0,
-                                  warp, lane};
+    WarpStream<false, kMoeStages, MoeTile> ws;
+    ws.init(smem + warp * kMoeRing, tile, G, i1 - i0, warp, lane);
     ws.prologue();
+    int cslot = 0;
     pdl_wait();  // h cells come from the gate+up kernel
     pdl_trigger();
 
@@ -466,9 +466,9 @@ __global__ void __launch_bounds__(32 * kMoeWarps, 2)
         }
         const StageCells stage{hcells, hfac, s_pair, pinf.ntok, G};
         if (pinf.ntok <= 4)
-            down_item<1>(ws, it, tl, pinf, reuse, stage, H, y, smem, s_pair);
+            down_item<1>(ws, cslot, tl, pinf, reuse, stage, H, y, smem, s_pair);
         else
-            down_item<2>(ws, it, tl, pinf, reuse, stage, H, y, smem, s_pair);
+            down_item<2>(ws, cslot, tl, pinf, reuse, stage, H, y, smem, s_pair);
     }
     cp_async_wait<0>();
 }

@@ -77,86 +77,85 @@ struct TileSrc {
     const float *s;
     size_t rowBytes;
     int nrows;
+    int sstride;  // floats between the scale rows (0: the stream's group count)
 };
 
-template <bool kInt8>
-__device__ __forceinline__ void issue_stage(uint8_t *slot, const TileSrc &t, int stage, int G,
-                                            int lane) {
-    const int g0 = stage * Fmt<kInt8>::kGPS;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int i = lane + 32 * j;
-        const int r = i >> 3, c = i & 7;
-        const int grp = g0 + (kInt8 ? (c >> 2) : (c >> 1));
-        if (grp < G) {
-            const int rr = r < t.nrows ? r : t.nrows - 1;
-            const uint8_t *src =
-                t.w + (size_t)rr * t.rowBytes + (size_t)g0 * Fmt<kInt8>::kGroupBytes + c * 16;
-            cp_async16(slot + r * 128 + ((c ^ (r & 7)) << 4), src);
-        }
-    }
-    if constexpr (!kInt8) {
-        float *ss = reinterpret_cast<float *>(slot + kStageWBytes);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int i = lane + 32 * j;
-            const int r = i >> 2, gg = i & 3;
-            if (g0 + gg < G) {
-                const int rr = r < t.nrows ? r : t.nrows - 1;
-                cp_async4(ss + r * 4 + gg, t.s + (size_t)rr * G + g0 + gg);
-            }
-        }
-    }
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// Consume one stage: groups [g0, g0 + GPS) of the chunk starting at group gc,
-// stopping at gEnd. Activation units of the chunk are cells[gl][s][16] and
-// factors fac[gl][s] (gl = g - gc, s < ntok). Accumulates
-// scale * factor * (hi + lo) per row and token.
+__device__ __forceinline__ void cp_async16_s(uint32_t dst, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async4_s(uint32_t dst, const void *gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(gmem) : "memory");
+}
+
+// Per-lane smem offsets of a stage slot, fixed for the whole kernel:
+//   weights: lane copies chunk c = lane & 7 of rows lane/8 + 4j (j = 0..3);
+//   scales (int4): lane copies scale lane & 3 of rows lane/4 + 8j (j = 0, 1);
+//   fragments: row gid's 8 (int4) or 16 (int8) bytes of group gl of the stage.
+template <bool kInt8>
+struct LaneMap {
+    uint32_t wdst[4], sdst[2];
+    uint32_t frag[Fmt<kInt8>::kGPS];
+    __device__ __forceinline__ void init(int lane) {
+        const int c = lane & 7, gid = lane >> 2, q = lane & 3;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = (lane >> 3) + 4 * j;
+            wdst[j] = r * 128 + ((c ^ (r & 7)) << 4);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) sdst[j] = kStageWBytes + (((lane >> 2) + 8 * j) * 4 + (lane & 3)) * 4;
+#pragma unroll
+        for (int gl = 0; gl < Fmt<kInt8>::kGPS; ++gl) {
+            if constexpr (kInt8)
+                frag[gl] = gid * 128 + (((4 * gl + q) ^ gid) << 4);
+            else
+                frag[gl] = gid * 128 + (((2 * gl + (q >> 1)) ^ gid) << 4) + ((q & 1) << 3);
+        }
+    }
+};
+
+// Consume one stage: `ng` (<= GPS) groups of the stage, the first of which is
+// group glc0 of the current activation chunk. bp / fp: this lane's B units
+// and factors at glc0 (see tile_group_*). Accumulates
+// scale * factor * (hi + lo) per row and token into c2.
 template <int NB, bool kInt8>
-__device__ __forceinline__ void compute_stage(const uint8_t *slot, int g0, int gc, int gEnd,
-                                              const uint4 *cells, const float *fac, int ntok,
-                                              float c2[2][NB][2]) {
-    const int lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
+__device__ __forceinline__ void compute_stage(uint32_t slot, const uint8_t *slotp,
+                                              const LaneMap<kInt8> &lm, int ng,
+                                              const uint4 *const bp0[NB], const float *const fp0[NB],
+                                              int ustride, float c2[2][NB][2]) {
+    const int gid = (threadIdx.x & 31) >> 2;
+    (void)slot;
     float4 sA = make_float4(1.f, 1.f, 1.f, 1.f), sB = sA;
     if constexpr (!kInt8) {
-        const float *ss = reinterpret_cast<const float *>(slot + kStageWBytes);
+        const float *ss = reinterpret_cast<const float *>(slotp + kStageWBytes);
         sA = *reinterpret_cast<const float4 *>(ss + gid * 4);
         sB = *reinterpret_cast<const float4 *>(ss + (gid + 8) * 4);
     }
     const float sa[4] = {sA.x, sA.y, sA.z, sA.w}, sb[4] = {sB.x, sB.y, sB.z, sB.w};
-    int sB_tok[NB], sD_tok[NB];
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-        sB_tok[nb] = min(4 * nb + (gid >> 1), ntok - 1);  // token of this lane's B column
-        sD_tok[nb] = min(4 * nb + q, ntok - 1);           // token of this lane's D columns
-    }
 #pragma unroll
     for (int gl = 0; gl < Fmt<kInt8>::kGPS; ++gl) {
-        const int g = g0 + gl;
-        if (g < gEnd) {
-            const int glc = g - gc;
+        if (gl < ng) {
             const uint4 *bp[NB];
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
-                bp[nb] = cells + (glc * ntok + sB_tok[nb]) * 16 + q * 2 + (gid & 1);
+            for (int nb = 0; nb < NB; ++nb) bp[nb] = bp0[nb] + gl * ustride;
             float dd[NB][4];
             if constexpr (kInt8) {
-                const int c = 4 * gl + q;
-                const uint4 w0 = *reinterpret_cast<const uint4 *>(slot + gid * 128 + ((c ^ gid) << 4));
-                const uint4 w8 =
-                    *reinterpret_cast<const uint4 *>(slot + (gid + 8) * 128 + ((c ^ gid) << 4));
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(slotp + lm.frag[gl]);
+                const uint4 w8 = *reinterpret_cast<const uint4 *>(slotp + lm.frag[gl] + 1024);
                 tile_group_int8<NB>(w0, w8, bp, dd);
             } else {
-                const int c = 2 * gl + (q >> 1);
-                const int off = ((c ^ gid) << 4) + ((q & 1) << 3);
-                const uint2 w0 = *reinterpret_cast<const uint2 *>(slot + gid * 128 + off);
-                const uint2 w8 = *reinterpret_cast<const uint2 *>(slot + (gid + 8) * 128 + off);
+                const uint2 w0 = *reinterpret_cast<const uint2 *>(slotp + lm.frag[gl]);
+                const uint2 w8 = *reinterpret_cast<const uint2 *>(slotp + lm.frag[gl] + 1024);
                 tile_group_int4<NB>(w0, w8, bp, dd);
             }
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
-                const float f = fac[glc * ntok + sD_tok[nb]];
+                const float f = fp0[nb][gl * (ustride >> 4)];
                 c2[gl & 1][nb][0] = fmaf(sa[gl] * f, dd[nb][0] + dd[nb][1], c2[gl & 1][nb][0]);
                 c2[gl & 1][nb][1] = fmaf(sb[gl] * f, dd[nb][2] + dd[nb][3], c2[gl & 1][nb][1]);
             }
@@ -165,49 +164,129 @@ __device__ __forceinline__ void compute_stage(const uint8_t *slot, int g0, int g
 }
 
 // Per-warp weight stream over the CTA's items, NS stages deep.
-// TileFn(item, warp) -> TileSrc.
+// TileFn(item, warp) -> TileSrc (called once per item).
 template <bool kInt8, int NS, class TileFn>
 struct WarpStream {
-    uint8_t *ring;  // this warp's NS * kStageBytes
+    uint8_t *ring;     // this warp's NS * kStageBytes
+    uint32_t ring_s;   // same, as a shared-window address
     TileFn tile;
-    int G, ns, total;  // groups per row, stages per item, stages of all items
-    int next;          // next global stage to issue
+    int G, ns, nitems;
+    int it_item, it_s;  // next stage to issue
+    const uint8_t *wsrc[4];
+    const float *ssrc[2];
+    int nfull;          // stages of an item that hold GPS whole groups
+    int slot;           // slot of the next issue
+    LaneMap<kInt8> lm;
     int warp, lane;
 
+    __device__ __forceinline__ void init(uint8_t *ring_, TileFn tile_, int G_, int nitems_,
+                                         int warp_, int lane_) {
+        ring = ring_;
+        ring_s = smem_u32(ring_);
+        tile = tile_;
+        G = G_;
+        ns = (G_ + Fmt<kInt8>::kGPS - 1) / Fmt<kInt8>::kGPS;
+        nfull = G_ / Fmt<kInt8>::kGPS;
+        nitems = nitems_;
+        it_item = 0;
+        it_s = 0;
+        slot = 0;
+        warp = warp_;
+        lane = lane_;
+        lm.init(lane_);
+        if (nitems > 0) set_item(0);
+    }
+
+    __device__ __forceinline__ void set_item(int item) {
+        const TileSrc t = tile(item, warp);
+        const int c = lane & 7;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = (lane >> 3) + 4 * j;
+            const int rr = r < t.nrows ? r : t.nrows - 1;
+            wsrc[j] = t.w + (size_t)rr * t.rowBytes + c * 16;
+        }
+        if constexpr (!kInt8) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int r = (lane >> 2) + 8 * j;
+                const int rr = r < t.nrows ? r : t.nrows - 1;
+                ssrc[j] = t.s + (size_t)rr * (t.sstride ? t.sstride : G) + (lane & 3);
+            }
+        }
+    }
+
     __device__ __forceinline__ void issue_next() {
-        if (next < total) {
-            const int item = next / ns, s = next - item * ns;
-            issue_stage<kInt8>(ring + (next % NS) * kStageBytes, tile(item, warp), s, G, lane);
+        if (it_item < nitems) {
+            const uint32_t base = ring_s + slot * kStageBytes;
+            const size_t wofs = (size_t)it_s * 128;
+            const int g0 = it_s * Fmt<kInt8>::kGPS;
+            if (it_s < nfull) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cp_async16_s(base + lm.wdst[j], wsrc[j] + wofs);
+                if constexpr (!kInt8) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) cp_async4_s(base + lm.sdst[j], ssrc[j] + g0);
+                }
+            } else {
+                const int c = lane & 7;
+                const int grp = g0 + (kInt8 ? (c >> 2) : (c >> 1));
+                if (grp < G) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) cp_async16_s(base + lm.wdst[j], wsrc[j] + wofs);
+                }
+                if constexpr (!kInt8) {
+                    if (g0 + (lane & 3) < G) {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) cp_async4_s(base + lm.sdst[j], ssrc[j] + g0);
+                    }
+                }
+            }
+            if (++it_s == ns) {
+                it_s = 0;
+                if (++it_item < nitems) set_item(it_item);
+            }
         }
         cp_async_commit();  // possibly empty: keeps the group count uniform
-        ++next;
+        slot = (slot + 1 == NS) ? 0 : slot + 1;
     }
     __device__ __forceinline__ void prologue() {
         for (int i = 0; i < NS - 1; ++i) issue_next();
     }
-    // Wait for stage j (global index), refill the slot freed by stage j-1.
-    __device__ __forceinline__ const uint8_t *acquire(int j) {
+    // Wait for the oldest outstanding stage (slot `cslot`), then refill the
+    // slot that the previous stage freed.
+    __device__ __forceinline__ void acquire() {
         cp_async_wait<NS - 2>();
         __syncwarp();
         issue_next();
-        return ring + (j % NS) * kStageBytes;
     }
 };
 
 // Runs one item for up to 4*NB tokens: chunks of activations are staged by
 // `stage(gc, ng, cells, fac)` (all threads; no barriers inside) unless
 // `reuse` says the previous item left the full K in shared memory.
+// cslot: slot of the next stage to consume (advanced here).
 // acc[nb][0 / 1]: rows gid / gid+8 of this warp, token 4*nb + q.
 template <int NB, bool kInt8, int NS, class TileFn, class Stage>
-__device__ __forceinline__ void run_item(WarpStream<kInt8, NS, TileFn> &ws, int item, uint4 *cells,
-                                         float *fac, int budget, int ntok, bool reuse,
-                                         const Stage &stage, float acc[NB][2]) {
+__device__ __forceinline__ void run_item(WarpStream<kInt8, NS, TileFn> &ws, int &cslot,
+                                         uint4 *cells, float *fac, int budget, int ntok,
+                                         bool reuse, const Stage &stage, float acc[NB][2]) {
+    const int lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
     const int G = ws.G;
     const int CG = chunk_groups(ntok, budget);
     constexpr int GPS = Fmt<kInt8>::kGPS;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = 0.0f;
-    int j = item * ws.ns;
+    const int ustride = ntok * 16;  // units per group in the chunk
+    const uint4 *bl[NB];
+    const float *fl[NB];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        const int sb = min(4 * nb + (gid >> 1), ntok - 1);  // token of this lane's B column
+        const int sd = min(4 * nb + q, ntok - 1);           // token of this lane's D columns
+        bl[nb] = cells + sb * 16 + q * 2 + (gid & 1);
+        fl[nb] = fac + sd;
+    }
     for (int gc = 0; gc < G; gc += CG) {
         const int ng = min(CG, G - gc);
         if (!(reuse && ng == G)) {
@@ -220,9 +299,20 @@ __device__ __forceinline__ void run_item(WarpStream<kInt8, NS, TileFn> &ws, int 
         for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) c2[h][nb][0] = c2[h][nb][1] = 0.0f;
-        for (int g0 = gc; g0 < gc + ng; g0 += GPS, ++j) {
-            const uint8_t *slot = ws.acquire(j);
-            compute_stage<NB, kInt8>(slot, g0, gc, gc + ng, cells, fac, ntok, c2);
+        const uint4 *bp[NB];
+        const float *fp[NB];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) { bp[nb] = bl[nb]; fp[nb] = fl[nb]; }
+        for (int glc = 0; glc < ng; glc += GPS) {
+            ws.acquire();
+            const uint8_t *slotp = ws.ring + cslot * kStageBytes;
+            compute_stage<NB, kInt8>(0u, slotp, ws.lm, min(GPS, ng - glc), bp, fp, ustride, c2);
+            cslot = (cslot + 1 == NS) ? 0 : cslot + 1;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                bp[nb] += GPS * ustride;
+                fp[nb] += GPS * ntok;
+            }
         }
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
@@ -230,6 +320,31 @@ __device__ __forceinline__ void run_item(WarpStream<kInt8, NS, TileFn> &ws, int 
             acc[nb][1] += c2[0][nb][1] + c2[1][nb][1];
         }
     }
+}
+
+// Runs the whole group range of one item against activation units that are
+// already in shared memory (bp0 / fp0: this lane's units and factors at the
+// first group of the range), NB = 1 token block. Used by the K-split dense
+// kernel; acc: rows gid / gid+8, token q.
+template <bool kInt8, int NS, class TileFn>
+__device__ __forceinline__ void run_staged(WarpStream<kInt8, NS, TileFn> &ws, int &cslot,
+                                           const uint4 *bp0, const float *fp0, int ntok,
+                                           float acc[1][2]) {
+    constexpr int GPS = Fmt<kInt8>::kGPS;
+    const int ustride = ntok * 16;
+    float c2[2][1][2] = {{{0.f, 0.f}}, {{0.f, 0.f}}};
+    const uint4 *bp[1] = {bp0};
+    const float *fp[1] = {fp0};
+    for (int glc = 0; glc < ws.G; glc += GPS) {
+        ws.acquire();
+        const uint8_t *slotp = ws.ring + cslot * kStageBytes;
+        compute_stage<1, kInt8>(0u, slotp, ws.lm, min(GPS, ws.G - glc), bp, fp, ustride, c2);
+        cslot = (cslot + 1 == NS) ? 0 : cslot + 1;
+        bp[0] += GPS * ustride;
+        fp[0] += GPS * ntok;
+    }
+    acc[0][0] = c2[0][0][0] + c2[1][0][0];
+    acc[0][1] = c2[0][0][1] + c2[1][0][1];
 }
 
 // Stages units + factors of `ntok` activation rows (rows `rows[s]` of the
