@@ -194,6 +194,27 @@ int moe_ffn_down(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
 int moe_ffn_combine(const qmv_moe_int4 *m, const int32_t *ids, const float *w, int T, int k,
                     float *out, void *ws, size_t ws_bytes, qmv_stream_t stream);
 
+/* Workspace of moe_expert_ffn_int4_prefill, in bytes (0 for unsupported sizes). */
+size_t moe_prefill_workspace_bytes(const qmv_moe_int4 *m, int T, int k);
+
+/* Batched MoE prefill on the tcgen05 tensor cores (colibri PR #418 PR summary
+ * names cooperative-matrix prefill kernels as the next step for batched
+ * prompts; the math is that of moe_expert_ffn_int4):
+ *     out[t] = sum_j w[t][j] * down_e(SiLU(gate_e x[t]) * up_e x[t]),  e = ids[t][j]
+ * with bf16 operands and fp32 accumulation: the weights are dequantized to
+ * bf16 with their group scale folded in, h is rounded to bf16 between the two
+ * projections; expected accuracy |out - exact| <= 1e-2 * sum |w * down * h|.
+ *   x_bf16 [T][H] bfloat16 bit patterns, 16-byte aligned; ids [T][k] int32;
+ *   w [T][k] fp32; out [T][H] fp32.
+ *   Each expert's tokens are processed in passes of up to 64, each pass
+ *   reading the expert's weights once. I must be a multiple of 128.
+ *   ws: at least moe_prefill_workspace_bytes(m, T, k) bytes, 256-byte aligned;
+ *   its first int32 is a status word: bit 0 = an id outside [0, E) (pair
+ *   skipped), bit 1 = a tensor-core wait timed out (output not valid). */
+int moe_expert_ffn_int4_prefill(const qmv_moe_int4 *m, const uint16_t *x_bf16, int T,
+                                const int32_t *ids, const float *w, int k, float *out, void *ws,
+                                size_t ws_bytes, qmv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -252,4 +252,45 @@ int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int3
     return moe_ffn_combine(m, ids, w, T, k, out, ws, ws_bytes, stream);
 }
 
+size_t moe_prefill_workspace_bytes(const qmv_moe_int4 *m, int T, int k) {
+    if (check_moe(m) || m->I % 128 || T < 0 || k < 1 || (int64_t)T * k > kMaxPairs) return 0;
+    return qmv::prefill_ws_layout(m->E, m->H, m->I, T, k).total;
+}
+
+int moe_expert_ffn_int4_prefill(const qmv_moe_int4 *m, const uint16_t *x_bf16, int T,
+                                const int32_t *ids, const float *w, int k, float *out, void *ws,
+                                size_t ws_bytes, qmv_stream_t stream) {
+    int r = check_moe(m);
+    if (r) return r;
+    if (m->I % 128) return QMV_ESHAPE;
+    if (T < 0 || k < 1 || k > m->E || (int64_t)T * k > kMaxPairs) return QMV_EINVAL;
+    if (T == 0) return QMV_OK;
+    if (!x_bf16 || !ids || !w || !out) return QMV_EINVAL;
+    if (!aligned(x_bf16, 16) || !aligned(ids, 4) || !aligned(w, 4) || !aligned(out, 4))
+        return QMV_EALIGN;
+    const qmv::PrefillWorkspace L = qmv::prefill_ws_layout(m->E, m->H, m->I, T, k);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return QMV_EWORKSPACE;
+    const cudaStream_t st = cs(stream);
+    const qmv::MoeDims d = dims(m);
+    int32_t *status = at<int32_t>(ws, L.status);
+    int32_t *offsets = at<int32_t>(ws, L.offsets), *list = at<int32_t>(ws, L.list);
+    int32_t *uexp = at<int32_t>(ws, L.uexp), *n_used = at<int32_t>(ws, L.n_used);
+    int32_t *pass_ofs = at<int32_t>(ws, L.pass_ofs);
+    uint16_t *h = at<uint16_t>(ws, L.h);
+    float *y = at<float>(ws, L.y);
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess)
+        e = qmv::launch_group_split(ids, T, k, m->E, offsets, list, uexp, n_used, pass_ofs, status,
+                                    nullptr, m->H, nullptr, nullptr, st,
+                                    qmv::prefill_pass_tokens());
+    if (e == cudaSuccess)
+        e = qmv::launch_prefill(d, 0, x_bf16, k, offsets, list, uexp, n_used, pass_ofs, h, y,
+                                status, st);
+    if (e == cudaSuccess)
+        e = qmv::launch_prefill(d, 1, h, k, offsets, list, uexp, n_used, pass_ofs, h, y, status,
+                                st);
+    if (e == cudaSuccess) e = qmv::launch_combine(y, ids, w, T, k, m->E, m->H, out, st, true);
+    return from_cuda(e);
+}
+
 }  // extern "C"

@@ -191,12 +191,11 @@ __device__ __forceinline__ float warp_max(float v) {
 // One warp computes a 16-row tile for up to 4*NB tokens. Lane (gid = lane/4,
 // q = lane%4) owns rows gid and gid+8; after the MMAs it holds, for token
 // 4*nb + q, rows gid (d[0] + d[1]: hi + lo columns) and gid+8 (d[2] + d[3]).
-// bp[nb] points at the lane's first unit of the current group for block nb
-// (token 4*nb + gid/2, clamped to the last token, part gid & 1); units of
-// the same lane for mh = 1 sit 8 units further.
+// bu[nb][mh]: the lane's B unit for MMA steps 2mh, 2mh+1 of block nb (token
+// 4*nb + gid/2, clamped to the last token, part gid & 1).
 
 template <int NB>
-__device__ __forceinline__ void tile_group_int4(uint2 w0, uint2 w8, const uint4 *const bp[NB],
+__device__ __forceinline__ void tile_group_int4(uint2 w0, uint2 w8, const uint4 (&bu)[NB][2],
                                                 float d[NB][4]) {
     uint32_t p0[4], p8[4], a[4];
 #pragma unroll
@@ -205,7 +204,7 @@ __device__ __forceinline__ void tile_group_int4(uint2 w0, uint2 w8, const uint4 
     for (int mh = 0; mh < 2; ++mh) {
         uint4 b[NB];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) b[nb] = bp[nb][8 * mh];
+        for (int nb = 0; nb < NB; ++nb) b[nb] = bu[nb][mh];
         dequant_int4_word(mh ? w0.y : w0.x, p0);
         dequant_int4_word(mh ? w8.y : w8.x, p8);
 #pragma unroll
@@ -223,7 +222,7 @@ __device__ __forceinline__ void tile_group_int4(uint2 w0, uint2 w8, const uint4 
 
 // int8: 16 bytes of row gid (w0) and of row gid+8 (w8); MMA step m uses word m.
 template <int NB>
-__device__ __forceinline__ void tile_group_int8(uint4 w0, uint4 w8, const uint4 *const bp[NB],
+__device__ __forceinline__ void tile_group_int8(uint4 w0, uint4 w8, const uint4 (&bu)[NB][2],
                                                 float d[NB][4]) {
     const uint32_t r0[4] = {w0.x, w0.y, w0.z, w0.w};
     const uint32_t r8[4] = {w8.x, w8.y, w8.z, w8.w};
@@ -233,7 +232,7 @@ __device__ __forceinline__ void tile_group_int8(uint4 w0, uint4 w8, const uint4 
     for (int mh = 0; mh < 2; ++mh) {
         uint4 b[NB];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) b[nb] = bp[nb][8 * mh];
+        for (int nb = 0; nb < NB; ++nb) b[nb] = bu[nb][mh];
 #pragma unroll
         for (int mm = 0; mm < 2; ++mm) {
             const int m = 2 * mh + mm;

@@ -108,74 +108,6 @@ struct DenseSplitTile {
     }
 };
 
-// Dense GEMV for up to 4 tokens whose split activations fit in shared
-// memory: every 16-row item is shared by the 4 warps of the CTA, warp ks
-// taking a quarter of the K groups; partial sums meet in shared memory and
-// are added in warp order (deterministic).
-template <bool kInt8>
-__global__ void __launch_bounds__(32 * kDenseWarps)
-    k_dense_ks(const uint8_t *__restrict__ w, const float *__restrict__ scales, int N, int K,
-               const uint4 *__restrict__ xcells, const float *__restrict__ xfac,
-               float *__restrict__ y, int ntok) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ float red[kDenseWarps][16][4];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
-    const int G = K / kGroup;
-    const int gq = (G + kDenseWarps - 1) / kDenseWarps;
-    const int ga = min(G, warp * gq), gb = min(G, ga + gq);
-    const int nitems = (N + 15) / 16;
-    const int i0 = (int)((long long)blockIdx.x * nitems / gridDim.x);
-    const int i1 = (int)((long long)(blockIdx.x + 1) * nitems / gridDim.x);
-    const size_t rowBytes = kInt8 ? (size_t)K : (size_t)K / 2;
-
-    DenseSplitTile<kInt8> tile{w, scales, rowBytes, N, G, i0, ga};
-    WarpStream<kInt8, kDenseStages, DenseSplitTile<kInt8>> ws;
-    ws.init(smem + warp * kDenseRing, tile, gb - ga, gb > ga ? i1 - i0 : 0, warp, lane);
-    ws.prologue();  // weights are call inputs: safe to read before the wait
-    int cslot = 0;
-
-    pdl_wait();     // cells and factors come from k_split
-    pdl_trigger();
-    uint4 *cells = reinterpret_cast<uint4 *>(smem + kDenseWarps * kDenseRing);
-    float *fac = reinterpret_cast<float *>(smem + kDenseWarps * kDenseRing + kDenseBudget);
-    for (int idx = threadIdx.x; idx < G * ntok * 16; idx += blockDim.x) {
-        const int u = idx & 15, r = idx >> 4, s = r % ntok, g = r / ntok;
-        cells[idx] = xcells[((size_t)s * G + g) * 16 + u];
-    }
-    for (int idx = threadIdx.x; idx < G * ntok; idx += blockDim.x)
-        fac[idx] = xfac[(size_t)(idx % ntok) * G + idx / ntok];
-    __syncthreads();
-    const int sb = min(gid >> 1, ntok - 1), sd = min(q, ntok - 1);
-    const uint4 *bp0 = cells + (ga * ntok + sb) * 16 + q * 2 + (gid & 1);
-    const float *fp0 = fac + ga * ntok + sd;
-
-    for (int it = 0; it < i1 - i0; ++it) {
-        float acc[1][2] = {{0.f, 0.f}};
-        if (gb > ga) run_staged<kInt8>(ws, cslot, bp0, fp0, ntok, acc);
-        red[warp][gid][q] = acc[0][0];
-        red[warp][gid + 8][q] = acc[0][1];
-        __syncthreads();
-        if (warp == 0 && q < ntok) {
-            const int row0 = (i0 + it) * 16;
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int k = 0; k < kDenseWarps; ++k) {
-                a0 += red[k][gid][q];
-                a1 += red[k][gid + 8][q];
-            }
-            const int rA = row0 + gid, rB = row0 + gid + 8;
-            if constexpr (kInt8) {
-                if (rA < N) a0 *= scales[rA];
-                if (rB < N) a1 *= scales[rB];
-            }
-            if (rA < N) y[(size_t)q * N + rA] = a0;
-            if (rB < N) y[(size_t)q * N + rB] = a1;
-        }
-        __syncthreads();
-    }
-    cp_async_wait<0>();
-}
-
 template <bool kInt8>
 __global__ void __launch_bounds__(32 * kDenseWarps)
     k_dense(const uint8_t *__restrict__ w, const float *__restrict__ scales, int N, int K,
@@ -214,6 +146,75 @@ __global__ void __launch_bounds__(32 * kDenseWarps)
     cp_async_wait<0>();
 }
 
+// Dense GEMV for up to 4 tokens whose split activations fit in shared
+// memory: every 16-row item is shared by the 8 warps of the CTA, warp ks
+// taking an eighth of the K groups; partial sums meet in shared memory and
+// are added in warp order (deterministic).
+constexpr int kKsWarps = 8;
+constexpr int kKsStages = 4;
+constexpr int kKsRing = kKsStages * kStageBytes;
+
+template <bool kInt8>
+__global__ void __launch_bounds__(32 * kKsWarps)
+    k_dense_ks(const uint8_t *__restrict__ w, const float *__restrict__ scales, int N, int K,
+               const uint4 *__restrict__ xcells, const float *__restrict__ xfac,
+               float *__restrict__ y, int ntok) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float red[kKsWarps][16][4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
+    const int G = K / kGroup;
+    const int gq = (G + kKsWarps - 1) / kKsWarps;
+    const int ga = min(G, warp * gq), gb = min(G, ga + gq);
+    const int nitems = (N + 15) / 16;
+    const int i0 = (int)((long long)blockIdx.x * nitems / gridDim.x);
+    const int i1 = (int)((long long)(blockIdx.x + 1) * nitems / gridDim.x);
+    const size_t rowBytes = kInt8 ? (size_t)K : (size_t)K / 2;
+
+    DenseSplitTile<kInt8> tile{w, scales, rowBytes, N, G, i0, ga};
+    WarpStream<kInt8, kKsStages, DenseSplitTile<kInt8>> ws;
+    ws.init(smem + warp * kKsRing, tile, gb - ga, gb > ga ? i1 - i0 : 0, warp, lane);
+    ws.prologue();  // weights are call inputs: safe to read before the wait
+    int cslot = 0;
+
+    pdl_wait();     // cells and factors come from k_split
+    pdl_trigger();
+    // token-major activation units: same layout as in global memory
+    uint4 *cells = reinterpret_cast<uint4 *>(smem + kKsWarps * kKsRing);
+    float *fac = reinterpret_cast<float *>(smem + kKsWarps * kKsRing + kDenseBudget);
+    for (int idx = threadIdx.x; idx < G * ntok * 16; idx += blockDim.x) cells[idx] = xcells[idx];
+    for (int idx = threadIdx.x; idx < G * ntok; idx += blockDim.x) fac[idx] = xfac[idx];
+    __syncthreads();
+    const int sb = min(gid >> 1, ntok - 1), sd = min(q, ntok - 1);
+    const uint4 *bp0 = cells + (sb * G + ga) * 16 + q * 2 + (gid & 1);
+    const float *fp0 = fac + sd * G + ga;
+
+    for (int it = 0; it < i1 - i0; ++it) {
+        float acc[1][2] = {{0.f, 0.f}};
+        if (gb > ga) run_staged<kInt8>(ws, cslot, bp0, fp0, acc);
+        red[warp][gid][q] = acc[0][0];
+        red[warp][gid + 8][q] = acc[0][1];
+        __syncthreads();
+        if (warp == 0 && q < ntok) {
+            const int row0 = (i0 + it) * 16;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < kKsWarps; ++k) {
+                a0 += red[k][gid][q];
+                a1 += red[k][gid + 8][q];
+            }
+            const int rA = row0 + gid, rB = row0 + gid + 8;
+            if constexpr (kInt8) {
+                if (rA < N) a0 *= scales[rA];
+                if (rB < N) a1 *= scales[rB];
+            }
+            if (rA < N) y[(size_t)q * N + rA] = a0;
+            if (rB < N) y[(size_t)q * N + rB] = a1;
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+}
+
 template <bool kInt8>
 cudaError_t launch_dense(const uint8_t *w, const float *scales, int N, int K, const float *x,
                          float *y, int S, void *xcells, float *xfac, cudaStream_t st) {
@@ -227,14 +228,15 @@ cudaError_t launch_dense(const uint8_t *w, const float *scales, int N, int K, co
                static_cast<uint4 *>(xcells), xfac);
     const int G = K / kGroup;
     if (S <= 4 && (size_t)G * S * 256 <= (size_t)kDenseBudget) {
-        // one pass, K split over the 4 warps of a CTA
-        e = (e == cudaSuccess) ? set_smem(k_dense_ks<kInt8>, smem) : e;
+        // one pass, K split over the warps of a CTA
+        const size_t smem_ks = (size_t)kKsWarps * kKsRing + kDenseBudget + kDenseBudget / 64;
+        e = (e == cudaSuccess) ? set_smem(k_dense_ks<kInt8>, smem_ks) : e;
         const int items = (N + 15) / 16;
         const int slots_ks =
-            sm_count() * max_ctas_per_sm(k_dense_ks<kInt8>, 32 * kDenseWarps, smem);
+            sm_count() * max_ctas_per_sm(k_dense_ks<kInt8>, 32 * kKsWarps, smem_ks);
         if (e == cudaSuccess)
             e = launch(k_dense_ks<kInt8>, dim3(items < slots_ks ? items : slots_ks),
-                       dim3(32 * kDenseWarps), smem, st, true, w, scales, N, K,
+                       dim3(32 * kKsWarps), smem_ks, st, true, w, scales, N, K,
                        static_cast<const uint4 *>(xcells), (const float *)xfac, y, S);
         return e;
     }

@@ -31,7 +31,7 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int
 cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
                                int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
-                               cudaStream_t st);
+                               cudaStream_t st, int pass_tok = 8);
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
                           int32_t *pass_ofs, cudaStream_t st, bool pdl);
 // Activation rows [R][K] fp32 -> fragment cells [R][K/64][16] uint4 + factors [R][K/64].
@@ -46,10 +46,23 @@ cudaError_t launch_down(const MoeDims &m, const void *hcells, const float *hfac,
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int T, int k, int E,
                            int H, float *out, cudaStream_t st, bool pdl);
 
+// Prefill (tcgen05): mode 0 = gate+up+SiLU (B = x bf16 rows, writes h bf16),
+// mode 1 = down (B = h bf16 rows, writes y fp32). Passes of prefill_pass_tokens().
+cudaError_t launch_prefill(const MoeDims &m, int mode, const uint16_t *b, int k,
+                           const int32_t *offsets, const int32_t *list, const int32_t *uexp,
+                           const int32_t *n_used, const int32_t *pass_ofs, uint16_t *h, float *y,
+                           int32_t *status, cudaStream_t st);
+int prefill_pass_tokens();
+
 // Workspace layout of the MoE entry points (256-byte aligned segments).
 struct MoeWorkspace {
     size_t status, offsets, list, uexp, n_used, pass_ofs, xcells, xfac, h, hcells, hfac, y, total;
 };
 MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k);
+
+struct PrefillWorkspace {
+    size_t status, offsets, list, uexp, n_used, pass_ofs, h, y, total;
+};
+PrefillWorkspace prefill_ws_layout(int E, int H, int I, int T, int k);
 
 }  // namespace qmv

@@ -112,7 +112,7 @@ __device__ __forceinline__ void block_scan3(int a, int b, int c, int &ea, int &e
 // lists in pair order (ranks from __match_any_sync), keeping them ascending.
 __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets,
                           int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
-                          int32_t *status) {
+                          int32_t *status, int pass_tok) {
     __shared__ int32_t cnt[1024], run[1024], tot[96];
     __shared__ int bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -127,7 +127,7 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
     __syncthreads();
     const int c = tid < E ? cnt[tid] : 0;
     const int f = c > 0 ? 1 : 0;
-    const int np = (c + kMaxTok - 1) / kMaxTok;
+    const int np = (c + pass_tok - 1) / pass_tok;
     int ec, ef, ep;
     block_scan3(c, f, np, ec, ef, ep, tot);
     if (tid < E) {
@@ -184,10 +184,10 @@ __device__ void split_row_cta(const float *__restrict__ row, int K, uint4 *cells
 __global__ void __launch_bounds__(1024)
     k_group_split(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets, int32_t *list,
                   int32_t *uexp, int32_t *n_used, int32_t *pass_ofs, int32_t *status,
-                  const float *__restrict__ x, int H, uint4 *xcells, float *xfac) {
+                  const float *__restrict__ x, int H, uint4 *xcells, float *xfac, int pass_tok) {
     pdl_trigger();
     if (blockIdx.x == 0) {
-        group_cta(ids, P, E, offsets, list, uexp, n_used, pass_ofs, status);
+        group_cta(ids, P, E, offsets, list, uexp, n_used, pass_ofs, status, pass_tok);
     } else {
         const int t = blockIdx.x - 1;
         const int G = H / kGroup;
@@ -248,6 +248,14 @@ __device__ __forceinline__ PassInfo pass_info(int pi, const int32_t *pass_ofs,
     return r;
 }
 
+constexpr int kMoeWarps = 16;  // one CTA of 16 warps per SM
+constexpr int kMoeStages = 4;
+constexpr int kMoeRing = kMoeStages * kStageBytes;
+constexpr int kMoeBudget = 64 * 1024;
+constexpr int kGuRows = 16 * kMoeWarps / 2;  // hidden units per gate+up item (128)
+constexpr int kDnRows = 16 * kMoeWarps;      // output rows per down item (256)
+constexpr int kEpiBytes = (2 * kGuRows * kMaxTok + kMoeWarps * 64) * 4;
+
 struct MoeTile {
     const uint8_t *q;   // weight pool
     const float *s;     // scale pool
@@ -268,9 +276,10 @@ struct MoeTile {
         int row;
         if (gate_up) {
             const int I = nrows_total / 2;
-            row = (wp < 4) ? tl * 64 + 16 * wp : I + tl * 64 + 16 * (wp - 4);
+            const int half = kMoeWarps / 2;
+            row = (wp < half) ? tl * kGuRows + 16 * wp : I + tl * kGuRows + 16 * (wp - half);
         } else {
-            row = tl * 128 + 16 * wp;
+            row = tl * kDnRows + 16 * wp;
         }
         int nrows = nrows_total - row;
         if (nrows <= 0) { row = nrows_total - 1; nrows = 1; }
@@ -279,11 +288,6 @@ struct MoeTile {
     }
 };
 
-constexpr int kMoeWarps = 8;
-constexpr int kMoeStages = 4;  // 2 CTAs (16 warps) per SM
-constexpr int kMoeRing = kMoeStages * kStageBytes;
-constexpr int kMoeBudget = 32 * 1024;
-constexpr int kEpiBytes = (2 * 64 * kMaxTok + kMoeWarps * 64) * 4;
 
 __device__ __forceinline__ void cta_items(int total, int &i0, int &i1) {
     i0 = (int)((long long)blockIdx.x * total / gridDim.x);
@@ -297,17 +301,18 @@ __device__ __forceinline__ void gate_up_item(WS &ws, int &cslot, int jt, const P
                                              bool reuse, const StageCells &stage, int I, int k,
                                              float *h, uint4 *hcells, float *hfac, uint8_t *smem,
                                              const int *s_pair) {
+    constexpr int half = kMoeWarps / 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
     const int ntok = pinf.ntok;
     uint4 *cells = reinterpret_cast<uint4 *>(smem + kMoeWarps * kMoeRing);
     float *fac = reinterpret_cast<float *>(smem + kMoeWarps * kMoeRing + kMoeBudget);
     float *gbuf = fac + kMoeBudget / 256;
-    float *hbuf = gbuf + 64 * kMaxTok;
-    float *wbuf = hbuf + 64 * kMaxTok;
+    float *hbuf = gbuf + kGuRows * kMaxTok;
+    float *wbuf = hbuf + kGuRows * kMaxTok;
     float acc[NB][2];
     run_item<NB, false>(ws, cslot, cells, fac, kMoeBudget, ntok, reuse, stage, acc);
 
-    if (warp < 4) {
+    if (warp < half) {
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
             const int s = 4 * nb + q;
@@ -318,9 +323,9 @@ __device__ __forceinline__ void gate_up_item(WS &ws, int &cslot, int jt, const P
         }
     }
     __syncthreads();
-    const int j0 = jt * 64;
-    if (warp >= 4) {
-        const int lr = 16 * (warp - 4) + gid;
+    const int j0 = jt * kGuRows;
+    if (warp >= half) {
+        const int lr = 16 * (warp - half) + gid;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
             const int s = 4 * nb + q;
@@ -331,30 +336,35 @@ __device__ __forceinline__ void gate_up_item(WS &ws, int &cslot, int jt, const P
                 hbuf[lr * kMaxTok + s] = h0;
                 hbuf[(lr + 8) * kMaxTok + s] = h1;
                 const size_t hb = (size_t)s_pair[s] * I + j0;
-                h[hb + lr] = h0;
-                h[hb + lr + 8] = h1;
+                if (j0 + lr < I) h[hb + lr] = h0;
+                if (j0 + lr + 8 < I) h[hb + lr + 8] = h1;
             }
         }
     }
     __syncthreads();
-    // fp16 hi/lo cells of h for the down projection: this tile is group jt of h.
+    // fp16 hi/lo units of h for the down projection: groups 2jt, 2jt+1 of h.
     const int Gd = I / kGroup;
-    for (int s = warp; s < ntok; s += kMoeWarps) {
-        const float a = hbuf[lane * kMaxTok + s], b = hbuf[(32 + lane) * kMaxTok + s];
-        const int e = split_exponent(warp_max(fmaxf(fabsf(a), fabsf(b))));
-        const float mul = ldexpf(1.0f, e);
-        wbuf[warp * 64 + lane] = a * mul;
-        wbuf[warp * 64 + 32 + lane] = b * mul;
-        __syncwarp();
-        const size_t cb = (size_t)s_pair[s] * Gd + jt;
-        if (lane < 16) hcells[cb * 16 + lane] = make_unit<false>(wbuf + warp * 64, lane);
-        if (lane == 0) hfac[cb] = ldexpf(1.0f, -e);
-        __syncwarp();
+    for (int idx = warp; idx < ntok * 2; idx += kMoeWarps) {
+        const int s = idx >> 1, gg = idx & 1;
+        const int gd = jt * 2 + gg;
+        if (gd < Gd) {
+            const float a = hbuf[(gg * 64 + lane) * kMaxTok + s];
+            const float b = hbuf[(gg * 64 + 32 + lane) * kMaxTok + s];
+            const int e = split_exponent(warp_max(fmaxf(fabsf(a), fabsf(b))));
+            const float mul = ldexpf(1.0f, e);
+            wbuf[warp * 64 + lane] = a * mul;
+            wbuf[warp * 64 + 32 + lane] = b * mul;
+            __syncwarp();
+            const size_t cb = (size_t)s_pair[s] * Gd + gd;
+            if (lane < 16) hcells[cb * 16 + lane] = make_unit<false>(wbuf + warp * 64, lane);
+            if (lane == 0) hfac[cb] = ldexpf(1.0f, -e);
+            __syncwarp();
+        }
     }
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(32 * kMoeWarps, 2)
+__global__ void __launch_bounds__(32 * kMoeWarps, 1)
     k_gate_up(MoeDims m, const uint4 *__restrict__ xcells, const float *__restrict__ xfac, int k,
               const int32_t *__restrict__ offsets, const int32_t *__restrict__ list,
               const int32_t *__restrict__ uexp, const int32_t *__restrict__ n_used,
@@ -368,7 +378,7 @@ __global__ void __launch_bounds__(32 * kMoeWarps, 2)
     const int H = m.H, I = m.I, G = H / kGroup;
     const int nu = *n_used;
     if (nu == 0) return;
-    const int tiles = I / 64;
+    const int tiles = (I + kGuRows - 1) / kGuRows;
     const int total = pass_ofs[nu] * tiles;
     int i0, i1;
     cta_items(total, i0, i1);
@@ -415,7 +425,7 @@ __device__ __forceinline__ void down_item(WS &ws, int &cslot, int tl, const Pass
     float *fac = reinterpret_cast<float *>(smem + kMoeWarps * kMoeRing + kMoeBudget);
     float acc[NB][2];
     run_item<NB, false>(ws, cslot, cells, fac, kMoeBudget, pinf.ntok, reuse, stage, acc);
-    const int row0 = tl * 128 + 16 * warp;
+    const int row0 = tl * kDnRows + 16 * warp;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
         const int s = 4 * nb + q;
@@ -427,7 +437,7 @@ __device__ __forceinline__ void down_item(WS &ws, int &cslot, int tl, const Pass
     }
 }
 
-__global__ void __launch_bounds__(32 * kMoeWarps, 2)
+__global__ void __launch_bounds__(32 * kMoeWarps, 1)
     k_down(MoeDims m, const uint4 *__restrict__ hcells, const float *__restrict__ hfac,
            const int32_t *__restrict__ offsets, const int32_t *__restrict__ list,
            const int32_t *__restrict__ uexp, const int32_t *__restrict__ n_used,
@@ -440,7 +450,7 @@ __global__ void __launch_bounds__(32 * kMoeWarps, 2)
     const int H = m.H, I = m.I, G = I / kGroup;
     const int nu = *n_used;
     if (nu == 0) { pdl_wait(); pdl_trigger(); return; }
-    const int tiles = (H + 127) / 128;
+    const int tiles = (H + kDnRows - 1) / kDnRows;
     const int total = pass_ofs[nu] * tiles;
     int i0, i1;
     cta_items(total, i0, i1);
@@ -518,15 +528,16 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int
                          int32_t *uexp, int32_t *n_used, int32_t *status, cudaStream_t st) {
     return launch(k_group_split, dim3(1), dim3(1024), 0, st, false, ids, P, E, offsets, list, uexp,
                   n_used, (int32_t *)nullptr, status, (const float *)nullptr, 64,
-                  (uint4 *)nullptr, (float *)nullptr);
+                  (uint4 *)nullptr, (float *)nullptr, (int)kMaxTok);
 }
 
 cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
                                int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
-                               cudaStream_t st) {
-    return launch(k_group_split, dim3(1 + T), dim3(1024), 0, st, false, ids, T * k, E, offsets,
-                  list, uexp, n_used, pass_ofs, status, x, H, static_cast<uint4 *>(xcells), xfac);
+                               cudaStream_t st, int pass_tok) {
+    return launch(k_group_split, dim3(x ? 1 + T : 1), dim3(1024), 0, st, false, ids, T * k, E,
+                  offsets, list, uexp, n_used, pass_ofs, status, x, H, static_cast<uint4 *>(xcells),
+                  xfac, pass_tok);
 }
 
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
@@ -580,6 +591,22 @@ MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k) {
     L.h = o; o = align256(o + 4 * P * I);
     L.hcells = o; o = align256(o + 4 * P * I);
     L.hfac = o; o = align256(o + 4 * P * (I / 64));
+    L.y = o; o = align256(o + 4 * P * H);
+    L.total = o;
+    return L;
+}
+
+PrefillWorkspace prefill_ws_layout(int E, int H, int I, int T, int k) {
+    PrefillWorkspace L{};
+    const size_t P = (size_t)T * k;
+    size_t o = 0;
+    L.status = o; o = align256(o + 4);
+    L.offsets = o; o = align256(o + 4 * (size_t)(E + 1));
+    L.list = o; o = align256(o + 4 * P);
+    L.uexp = o; o = align256(o + 4 * (size_t)E);
+    L.n_used = o; o = align256(o + 4);
+    L.pass_ofs = o; o = align256(o + 4 * (size_t)(E + 1));
+    L.h = o; o = align256(o + 2 * P * I);
     L.y = o; o = align256(o + 4 * P * H);
     L.total = o;
     return L;

@@ -17,6 +17,8 @@
 // time; a chunk is a multiple of the stage size.
 #pragma once
 
+#include <type_traits>
+
 #include "qmv_device.cuh"
 
 namespace qmv {
@@ -119,45 +121,59 @@ struct LaneMap {
     }
 };
 
-// Consume one stage: `ng` (<= GPS) groups of the stage, the first of which is
-// group glc0 of the current activation chunk. bp / fp: this lane's B units
-// and factors at glc0 (see tile_group_*). Accumulates
-// scale * factor * (hi + lo) per row and token into c2.
+// Consume one stage: `ng` (<= GPS) groups of the stage. Activation units of
+// the chunk are token-major, cells[s][gl][16], factors fac[s][gl]; bp0 / fp0
+// point at this lane's unit / factor for the stage's first group, so the
+// group offsets below are compile-time. Loads of two groups are issued before
+// their math. Accumulates scale * factor * (hi + lo) per row and token.
 template <int NB, bool kInt8>
-__device__ __forceinline__ void compute_stage(uint32_t slot, const uint8_t *slotp,
-                                              const LaneMap<kInt8> &lm, int ng,
-                                              const uint4 *const bp0[NB], const float *const fp0[NB],
-                                              int ustride, float c2[2][NB][2]) {
+__device__ __forceinline__ void compute_stage(const uint8_t *slotp, const LaneMap<kInt8> &lm,
+                                              int ng, const uint4 *const bp0[NB],
+                                              const float *const fp0[NB], float c2[2][NB][2]) {
+    using W = typename std::conditional<kInt8, uint4, uint2>::type;
+    constexpr int GPS = Fmt<kInt8>::kGPS;
     const int gid = (threadIdx.x & 31) >> 2;
-    (void)slot;
-    float4 sA = make_float4(1.f, 1.f, 1.f, 1.f), sB = sA;
+    float sa[4] = {1.f, 1.f, 1.f, 1.f}, sb[4] = {1.f, 1.f, 1.f, 1.f};
     if constexpr (!kInt8) {
         const float *ss = reinterpret_cast<const float *>(slotp + kStageWBytes);
-        sA = *reinterpret_cast<const float4 *>(ss + gid * 4);
-        sB = *reinterpret_cast<const float4 *>(ss + (gid + 8) * 4);
+        const float4 A = *reinterpret_cast<const float4 *>(ss + gid * 4);
+        const float4 B = *reinterpret_cast<const float4 *>(ss + (gid + 8) * 4);
+        sa[0] = A.x; sa[1] = A.y; sa[2] = A.z; sa[3] = A.w;
+        sb[0] = B.x; sb[1] = B.y; sb[2] = B.z; sb[3] = B.w;
     }
-    const float sa[4] = {sA.x, sA.y, sA.z, sA.w}, sb[4] = {sB.x, sB.y, sB.z, sB.w};
 #pragma unroll
-    for (int gl = 0; gl < Fmt<kInt8>::kGPS; ++gl) {
-        if (gl < ng) {
-            const uint4 *bp[NB];
+    for (int h = 0; h < GPS; h += 2) {
+        W w0[2], w8[2];
+        uint4 bu[2][NB][2];
+        float f[2][NB];
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) bp[nb] = bp0[nb] + gl * ustride;
-            float dd[NB][4];
-            if constexpr (kInt8) {
-                const uint4 w0 = *reinterpret_cast<const uint4 *>(slotp + lm.frag[gl]);
-                const uint4 w8 = *reinterpret_cast<const uint4 *>(slotp + lm.frag[gl] + 1024);
-                tile_group_int8<NB>(w0, w8, bp, dd);
-            } else {
-                const uint2 w0 = *reinterpret_cast<const uint2 *>(slotp + lm.frag[gl]);
-                const uint2 w8 = *reinterpret_cast<const uint2 *>(slotp + lm.frag[gl] + 1024);
-                tile_group_int4<NB>(w0, w8, bp, dd);
+        for (int i = 0; i < 2; ++i) {
+            const int gl = h + i;
+            if (gl < ng) {
+                w0[i] = *reinterpret_cast<const W *>(slotp + lm.frag[gl]);
+                w8[i] = *reinterpret_cast<const W *>(slotp + lm.frag[gl] + 1024);
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                    bu[i][nb][0] = bp0[nb][gl * 16];
+                    bu[i][nb][1] = bp0[nb][gl * 16 + 8];
+                    f[i][nb] = fp0[nb][gl];
+                }
             }
+        }
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-                const float f = fp0[nb][gl * (ustride >> 4)];
-                c2[gl & 1][nb][0] = fmaf(sa[gl] * f, dd[nb][0] + dd[nb][1], c2[gl & 1][nb][0]);
-                c2[gl & 1][nb][1] = fmaf(sb[gl] * f, dd[nb][2] + dd[nb][3], c2[gl & 1][nb][1]);
+        for (int i = 0; i < 2; ++i) {
+            const int gl = h + i;
+            if (gl < ng) {
+                float dd[NB][4];
+                if constexpr (kInt8)
+                    tile_group_int8<NB>(w0[i], w8[i], bu[i], dd);
+                else
+                    tile_group_int4<NB>(w0[i], w8[i], bu[i], dd);
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                    c2[i][nb][0] = fmaf(sa[gl] * f[i][nb], dd[nb][0] + dd[nb][1], c2[i][nb][0]);
+                    c2[i][nb][1] = fmaf(sb[gl] * f[i][nb], dd[nb][2] + dd[nb][3], c2[i][nb][1]);
+                }
             }
         }
     }
@@ -277,15 +293,13 @@ __device__ __forceinline__ void run_item(WarpStream<kInt8, NS, TileFn> &ws, int 
     constexpr int GPS = Fmt<kInt8>::kGPS;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = 0.0f;
-    const int ustride = ntok * 16;  // units per group in the chunk
     const uint4 *bl[NB];
     const float *fl[NB];
+    int sbt[NB], sdt[NB];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-        const int sb = min(4 * nb + (gid >> 1), ntok - 1);  // token of this lane's B column
-        const int sd = min(4 * nb + q, ntok - 1);           // token of this lane's D columns
-        bl[nb] = cells + sb * 16 + q * 2 + (gid & 1);
-        fl[nb] = fac + sd;
+        sbt[nb] = min(4 * nb + (gid >> 1), ntok - 1);  // token of this lane's B column
+        sdt[nb] = min(4 * nb + q, ntok - 1);           // token of this lane's D columns
     }
     for (int gc = 0; gc < G; gc += CG) {
         const int ng = min(CG, G - gc);
@@ -294,24 +308,25 @@ __device__ __forceinline__ void run_item(WarpStream<kInt8, NS, TileFn> &ws, int 
             stage(gc, ng, cells, fac);
             __syncthreads();
         }
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            bl[nb] = cells + (sbt[nb] * ng) * 16 + q * 2 + (gid & 1);
+            fl[nb] = fac + sdt[nb] * ng;
+        }
         float c2[2][NB][2];
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) c2[h][nb][0] = c2[h][nb][1] = 0.0f;
-        const uint4 *bp[NB];
-        const float *fp[NB];
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) { bp[nb] = bl[nb]; fp[nb] = fl[nb]; }
         for (int glc = 0; glc < ng; glc += GPS) {
             ws.acquire();
             const uint8_t *slotp = ws.ring + cslot * kStageBytes;
-            compute_stage<NB, kInt8>(0u, slotp, ws.lm, min(GPS, ng - glc), bp, fp, ustride, c2);
+            compute_stage<NB, kInt8>(slotp, ws.lm, min(GPS, ng - glc), bl, fl, c2);
             cslot = (cslot + 1 == NS) ? 0 : cslot + 1;
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
-                bp[nb] += GPS * ustride;
-                fp[nb] += GPS * ntok;
+                bl[nb] += GPS * 16;
+                fl[nb] += GPS;
             }
         }
 #pragma unroll
@@ -328,20 +343,18 @@ __device__ __forceinline__ void run_item(WarpStream<kInt8, NS, TileFn> &ws, int 
 // kernel; acc: rows gid / gid+8, token q.
 template <bool kInt8, int NS, class TileFn>
 __device__ __forceinline__ void run_staged(WarpStream<kInt8, NS, TileFn> &ws, int &cslot,
-                                           const uint4 *bp0, const float *fp0, int ntok,
-                                           float acc[1][2]) {
+                                           const uint4 *bp0, const float *fp0, float acc[1][2]) {
     constexpr int GPS = Fmt<kInt8>::kGPS;
-    const int ustride = ntok * 16;
     float c2[2][1][2] = {{{0.f, 0.f}}, {{0.f, 0.f}}};
     const uint4 *bp[1] = {bp0};
     const float *fp[1] = {fp0};
     for (int glc = 0; glc < ws.G; glc += GPS) {
         ws.acquire();
         const uint8_t *slotp = ws.ring + cslot * kStageBytes;
-        compute_stage<1, kInt8>(0u, slotp, ws.lm, min(GPS, ws.G - glc), bp, fp, ustride, c2);
+        compute_stage<1, kInt8>(slotp, ws.lm, min(GPS, ws.G - glc), bp, fp, c2);
         cslot = (cslot + 1 == NS) ? 0 : cslot + 1;
-        bp[0] += GPS * ustride;
-        fp[0] += GPS * ntok;
+        bp[0] += GPS * 16;
+        fp[0] += GPS;
     }
     acc[0][0] = c2[0][0][0] + c2[1][0][0];
     acc[0][1] = c2[0][0][1] + c2[1][0][1];
@@ -349,21 +362,20 @@ __device__ __forceinline__ void run_staged(WarpStream<kInt8, NS, TileFn> &ws, in
 
 // Stages units + factors of `ntok` activation rows (rows `rows[s]` of the
 // global layout [row][G][16 units] and [row][G] factors) for groups
-// [gc, gc+ng) into cells[gl][s][16] and fac[gl][s].
+// [gc, gc+ng) into the token-major chunk cells[s][gl][16] and fac[s][gl].
 struct StageCells {
     const uint4 *src;
     const float *fsrc;
     const int *rows;  // shared memory
     int ntok, G;
     __device__ __forceinline__ void operator()(int gc, int ng, uint4 *cells, float *fac) const {
-        const int total = ng * ntok * 16;
-        for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-            const int u = idx & 15, r = idx >> 4;
-            const int s = r % ntok, gl = r / ntok;
-            cells[idx] = src[((size_t)rows[s] * G + gc + gl) * 16 + u];
+        const int per = ng * 16;
+        for (int idx = threadIdx.x; idx < ntok * per; idx += blockDim.x) {
+            const int s = idx / per, rem = idx - s * per;
+            cells[idx] = src[((size_t)rows[s] * G + gc) * 16 + rem];
         }
         for (int idx = threadIdx.x; idx < ng * ntok; idx += blockDim.x) {
-            const int s = idx % ntok, gl = idx / ntok;
+            const int s = idx / ng, gl = idx - s * ng;
             fac[idx] = fsrc[(size_t)rows[s] * G + gc + gl];
         }
     }
