@@ -91,6 +91,27 @@ int qmv_int4_gs(const uint8_t *wq, const float *scales, int N, int K, int gs, co
 int qmv_int8_row(const int8_t *w, const float *row_scale, int N, int K, const float *x,
                  float *y, int S, void *ws, size_t ws_bytes, qmv_stream_t stream);
 
+/* The dense int4-gs64 GEMV of qmv_int4_gs for callers that cannot allocate
+ * device memory: code that must never make the device synchronise (cudaMalloc
+ * and cudaFree can), hosts that forbid device allocation after start-up, and
+ * C callers with nowhere to keep a workspace between calls. Same arguments
+ * and results as qmv_int4_gs, minus the workspace; the pages have no
+ * counterpart of this entry point.
+ *   Scratch: one file-scope device array inside the library (266,240 bytes,
+ *   held by every GPU that loads the library until the process exits), so
+ *   S * K must be at most 65536; larger calls return QMV_EWORKSPACE and
+ *   enqueue nothing.
+ *   The first call on a device looks up the array's device address (a host
+ *   call, cudaGetSymbolAddress); make that first call before any stream
+ *   capture.
+ *   Every call uses the same array and overwrites all of it that it reads, so
+ *   nothing carries over between calls, but calls whose work overlaps on the
+ *   GPU (different streams, or different host threads on one device) race on
+ *   it: order them on one stream.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+int qmv_int4_gs_noalloc(const uint8_t *wq, const float *scales, int N, int K, int gs,
+                        const float *x, float *y, int S, qmv_stream_t stream);
+
 /* ---------------------------------------------------------------- MoE */
 
 /* Device-resident int4-gs64 expert weights (the analogue of the pages'
