@@ -340,7 +340,7 @@ def run_ours(args):
     e1.synchronize()
     t_e2e = e0.elapsed_time(e1) * 1e-3 / n_e2e
 
-    rows = measure_rows(q, datagen, dev, stream, peak) if rank == 0 and not args.quick else {}
+    rows = measure_rows(q, datagen, dev, stream, peak, m) if rank == 0 and not args.quick else {}
 
     if rank != 0:
         return 0
@@ -378,10 +378,33 @@ def run_ours(args):
     return 0
 
 
-def measure_rows(q, datagen, dev, stream, peak):
+def measure_rows(q, datagen, dev, stream, peak, pool):
     """Other rows of the hot path, each with its own roofline fraction."""
     import torch
     rows = {}
+    # MoE prefill, 512 tokens on the tcgen05 path, same 160-expert pool
+    wl4 = dict(H=6144, E=160, I=2048, k=8, T=512)
+    xb, lg = datagen.moe_inputs(wl4["T"], wl4["E"], wl4["H"], xdtype="bf16")
+    xbd = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    lgd = torch.from_numpy(lg).to(dev)
+    i4 = torch.empty((wl4["T"], 8), dtype=torch.int32, device=dev)
+    w4 = torch.empty((wl4["T"], 8), dtype=torch.float32, device=dev)
+    o4 = torch.empty((wl4["T"], wl4["H"]), dtype=torch.float32, device=dev)
+    ws4 = torch.empty(q.moe_prefill_workspace_bytes(pool, wl4["T"], 8), dtype=torch.uint8,
+                      device=dev)
+    g4 = [graph_of(lambda: (q.moe_route_topk(lgd, 8, ids=i4, w=w4, stream=stream),
+                            q.moe_expert_ffn_int4_prefill(pool, xbd, i4, w4, out=o4, ws=ws4,
+                                                          stream=stream)), stream)]
+    time_graphs(g4, 3, stream)
+    t = time_graphs(g4, 10, stream)
+    U4 = len(np.unique(np.argsort(-lg, axis=1, kind="stable")[:, :8]))
+    B4 = U4 * EXPERT_BYTES(wl4["H"], wl4["I"]) + xb.nbytes + o4.numel() * 4
+    F4 = 2 * wl4["T"] * 8 * 3 * wl4["H"] * wl4["I"]
+    rows["moe_prefill_h6144_e160_i2048_512tok"] = {
+        "us": t * 1e6, "GBs": B4 / t / 1e9, "frac": B4 / t / 1e9 / peak, "bytes": B4,
+        "experts_touched": U4, "tflops": F4 / t / 1e12, "launches_per_call": 6,
+        "path": "tcgen05 kind::f16 (bf16), A dequantized into TMEM"}
+    del ws4, o4
     # dense int4-gs64 and int8-row GEMV, 14336 x 4096, one token
     N, K = 14336, 4096
     wq, sc, x = datagen.dense_int4(N, K, 1)
