@@ -146,9 +146,16 @@ int moe_gate_up_silu(const qmv_moe_int4 *m, const float *x, int T, int k, const 
     const cudaStream_t st = cs(stream);
     cudaError_t e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
     if (e == cudaSuccess) e = qmv::launch_split(x, T, m->H, b + L.xcells, xfac, st);
-    if (e == cudaSuccess)
-        e = qmv::launch_gate_up(dims(m), b + L.xcells, xfac, k, offsets, list, uexp, n_used,
-                                pass_ofs, h, b + L.hcells, reinterpret_cast<float *>(b + L.hfac), st);
+    if (e == cudaSuccess) {
+        float *hfac = reinterpret_cast<float *>(b + L.hfac);
+        if (qmv::tma_moe_supported(dims(m)))
+            e = qmv::launch_moe_tma(dims(m), 0, b + L.xcells, xfac, k, offsets, list, uexp, n_used,
+                                    pass_ofs, h, b + L.hcells, hfac, nullptr,
+                                    reinterpret_cast<int32_t *>(b + L.status), st);
+        else
+            e = qmv::launch_gate_up(dims(m), b + L.xcells, xfac, k, offsets, list, uexp, n_used,
+                                    pass_ofs, h, b + L.hcells, hfac, st);
+    }
     return from_cuda(e);
 }
 
@@ -170,9 +177,15 @@ int moe_down(const qmv_moe_int4 *m, const float *h, int T, int k, const int32_t 
     const cudaStream_t st = cs(stream);
     cudaError_t e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
     if (e == cudaSuccess) e = qmv::launch_split(h, T * k, m->I, b + L.hcells, hfac, st);
-    if (e == cudaSuccess)
-        e = qmv::launch_down(dims(m), b + L.hcells, hfac, offsets, list, uexp, n_used, pass_ofs, y,
-                             st);
+    if (e == cudaSuccess) {
+        if (qmv::tma_moe_supported(dims(m)))
+            e = qmv::launch_moe_tma(dims(m), 1, b + L.hcells, hfac, k, offsets, list, uexp, n_used,
+                                    pass_ofs, nullptr, nullptr, nullptr, y,
+                                    reinterpret_cast<int32_t *>(b + L.status), st);
+        else
+            e = qmv::launch_down(dims(m), b + L.hcells, hfac, offsets, list, uexp, n_used, pass_ofs,
+                                 y, st);
+    }
     return from_cuda(e);
 }
 
@@ -208,6 +221,13 @@ int moe_ffn_gate_up(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_byt
     qmv::MoeWorkspace L;
     int r = ffn_check(m, T, k, ws, ws_bytes, L);
     if (r) return r;
+    if (qmv::tma_moe_supported(dims(m)))
+        return from_cuda(qmv::launch_moe_tma(
+            dims(m), 0, at<void>(ws, L.xcells), at<float>(ws, L.xfac), k,
+            at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
+            at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs), at<float>(ws, L.h),
+            at<void>(ws, L.hcells), at<float>(ws, L.hfac), nullptr, at<int32_t>(ws, L.status),
+            cs(stream)));
     return from_cuda(qmv::launch_gate_up(
         dims(m), at<void>(ws, L.xcells), at<float>(ws, L.xfac), k, at<int32_t>(ws, L.offsets),
         at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp), at<int32_t>(ws, L.n_used),
@@ -220,6 +240,12 @@ int moe_ffn_down(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
     qmv::MoeWorkspace L;
     int r = ffn_check(m, T, k, ws, ws_bytes, L);
     if (r) return r;
+    if (qmv::tma_moe_supported(dims(m)))
+        return from_cuda(qmv::launch_moe_tma(
+            dims(m), 1, at<void>(ws, L.hcells), at<float>(ws, L.hfac), k,
+            at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
+            at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs), nullptr, nullptr, nullptr,
+            at<float>(ws, L.y), at<int32_t>(ws, L.status), cs(stream)));
     return from_cuda(qmv::launch_down(dims(m), at<void>(ws, L.hcells), at<float>(ws, L.hfac),
                                       at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list),
                                       at<int32_t>(ws, L.uexp), at<int32_t>(ws, L.n_used),

@@ -54,6 +54,14 @@ cudaError_t launch_prefill(const MoeDims &m, int mode, const uint16_t *b, int k,
                            int32_t *status, cudaStream_t st);
 int prefill_pass_tokens();
 
+// TMA-fed decode kernels (qmv_moe_tma.cu): mode 0 = gate+up (cells = x units,
+// writes h, h units, h factors), mode 1 = down (cells = h units, writes y).
+bool tma_moe_supported(const MoeDims &m);
+cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const float *cfac, int k,
+                           const int32_t *offsets, const int32_t *list, const int32_t *uexp,
+                           const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,
+                           float *hfac, float *y, int32_t *status, cudaStream_t st);
+
 // Workspace layout of the MoE entry points (256-byte aligned segments).
 struct MoeWorkspace {
     size_t status, offsets, list, uexp, n_used, pass_ofs, xcells, xfac, h, hcells, hfac, y, total;
