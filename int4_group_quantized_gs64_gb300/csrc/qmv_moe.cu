@@ -30,14 +30,24 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // ------------------------------------------------------------------ routing
 
-// One warp per token; lane L owns experts L, L+32, ... (E <= 1024).
-__global__ void __launch_bounds__(256)
+// One warp per token; the token's logits are staged in shared memory once,
+// lane L owns experts L, L+32, ... (E <= 1024).
+constexpr int kRouteWarps = 8;
+
+__global__ void __launch_bounds__(32 * kRouteWarps)
     k_route(const float *__restrict__ logits, int T, int E, int k, int32_t *__restrict__ ids,
             float *__restrict__ w) {
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    __shared__ float sl[kRouteWarps][1024];
+    const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+    const int t = blockIdx.x * kRouteWarps + wl;
     if (t >= T) return;
     const float *l = logits + (size_t)t * E;
+    float *row = sl[wl];
+    for (int e = lane; e < E; e += 32) {
+        const float v = l[e];
+        row[e] = (v != v) ? -INFINITY : v;  // NaN never ahead of a finite logit
+    }
+    __syncwarp();
     uint32_t taken = 0u;
     int my_id = 0;
     float my_l = -INFINITY;
@@ -47,8 +57,7 @@ __global__ void __launch_bounds__(256)
         for (int i = 0; lane + 32 * i < E; ++i) {
             if ((taken >> i) & 1u) continue;
             const int e = lane + 32 * i;
-            float v = l[e];
-            if (v != v) v = -INFINITY;  // NaN never ahead of a finite logit
+            const float v = row[e];
             if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
         }
 #pragma unroll
@@ -519,9 +528,8 @@ int moe_grid(void (*k)(MoeDims, const uint4 *, const float *, int, const int32_t
 cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w,
                          cudaStream_t st) {
     if (T == 0) return cudaSuccess;
-    const int per = 8;  // tokens (warps) per CTA
-    return launch(k_route, dim3((T + per - 1) / per), dim3(32 * per), 0, st, false, logits, T, E,
-                  k, ids, w);
+    return launch(k_route, dim3((T + kRouteWarps - 1) / kRouteWarps), dim3(32 * kRouteWarps), 0,
+                  st, false, logits, T, E, k, ids, w);
 }
 
 cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int32_t *list,

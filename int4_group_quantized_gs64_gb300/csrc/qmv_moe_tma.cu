@@ -119,8 +119,38 @@ __device__ __forceinline__ TItem t_item(const TmaArgs &a, int nu, int tiles, int
     return r;
 }
 
-// One stage of two 16-row tiles (smem rows ra.. and rb..) against the staged
-// activation units; like compute_stage but the B operands are shared.
+// One group of two 16-row tiles (smem rows ra.. and rb..) against the staged
+// activation units; the B operands are shared by the two tiles.
+template <int NB, int GL>
+__device__ __forceinline__ void group2(const uint8_t *wa, const uint8_t *wb, int gid, int q,
+                                       float sa0, float sa8, float sb0, float sb8,
+                                       const uint4 *const bp0[NB], const float *const fp0[NB],
+                                       float cA[2][NB][2], float cB[2][NB][2]) {
+    const int off = (((2 * GL + (q >> 1)) ^ gid) << 4) + ((q & 1) << 3);
+    const uint2 wA0 = *reinterpret_cast<const uint2 *>(wa + off);
+    const uint2 wA8 = *reinterpret_cast<const uint2 *>(wa + 1024 + off);
+    const uint2 wB0 = *reinterpret_cast<const uint2 *>(wb + off);
+    const uint2 wB8 = *reinterpret_cast<const uint2 *>(wb + 1024 + off);
+    uint4 bu[NB][2];
+    float f[NB];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        bu[nb][0] = bp0[nb][GL * 16];
+        bu[nb][1] = bp0[nb][GL * 16 + 8];
+        f[nb] = fp0[nb][GL];
+    }
+    float dA[NB][4], dB[NB][4];
+    tile_group_int4<NB>(wA0, wA8, bu, dA);
+    tile_group_int4<NB>(wB0, wB8, bu, dB);
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        cA[GL & 1][nb][0] = fmaf(sa0 * f[nb], dA[nb][0] + dA[nb][1], cA[GL & 1][nb][0]);
+        cA[GL & 1][nb][1] = fmaf(sa8 * f[nb], dA[nb][2] + dA[nb][3], cA[GL & 1][nb][1]);
+        cB[GL & 1][nb][0] = fmaf(sb0 * f[nb], dB[nb][0] + dB[nb][1], cB[GL & 1][nb][0]);
+        cB[GL & 1][nb][1] = fmaf(sb8 * f[nb], dB[nb][2] + dB[nb][3], cB[GL & 1][nb][1]);
+    }
+}
+
 template <int NB>
 __device__ __forceinline__ void compute_stage2(const uint8_t *slot, int ra, int rb, int ng,
                                                const uint4 *const bp0[NB],
@@ -132,37 +162,17 @@ __device__ __forceinline__ void compute_stage2(const uint8_t *slot, int ra, int 
     const float4 sA8 = *reinterpret_cast<const float4 *>(ss + (ra + gid + 8) * 4);
     const float4 sB0 = *reinterpret_cast<const float4 *>(ss + (rb + gid) * 4);
     const float4 sB8 = *reinterpret_cast<const float4 *>(ss + (rb + gid + 8) * 4);
-    const float a0[4] = {sA0.x, sA0.y, sA0.z, sA0.w}, a8[4] = {sA8.x, sA8.y, sA8.z, sA8.w};
-    const float b0[4] = {sB0.x, sB0.y, sB0.z, sB0.w}, b8[4] = {sB8.x, sB8.y, sB8.z, sB8.w};
     const uint8_t *wa = slot + (ra + gid) * 128;
     const uint8_t *wb = slot + (rb + gid) * 128;
-#pragma unroll
-    for (int gl = 0; gl < 4; ++gl) {
-        if (gl < ng) {
-            const int off = (((2 * gl + (q >> 1)) ^ gid) << 4) + ((q & 1) << 3);
-            const uint2 wA0 = *reinterpret_cast<const uint2 *>(wa + off);
-            const uint2 wA8 = *reinterpret_cast<const uint2 *>(wa + 1024 + off);
-            const uint2 wB0 = *reinterpret_cast<const uint2 *>(wb + off);
-            const uint2 wB8 = *reinterpret_cast<const uint2 *>(wb + 1024 + off);
-            uint4 bu[NB][2];
-            float f[NB];
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-                bu[nb][0] = bp0[nb][gl * 16];
-                bu[nb][1] = bp0[nb][gl * 16 + 8];
-                f[nb] = fp0[nb][gl];
-            }
-            float dA[NB][4], dB[NB][4];
-            tile_group_int4<NB>(wA0, wA8, bu, dA);
-            tile_group_int4<NB>(wB0, wB8, bu, dB);
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-                cA[gl & 1][nb][0] = fmaf(a0[gl] * f[nb], dA[nb][0] + dA[nb][1], cA[gl & 1][nb][0]);
-                cA[gl & 1][nb][1] = fmaf(a8[gl] * f[nb], dA[nb][2] + dA[nb][3], cA[gl & 1][nb][1]);
-                cB[gl & 1][nb][0] = fmaf(b0[gl] * f[nb], dB[nb][0] + dB[nb][1], cB[gl & 1][nb][0]);
-                cB[gl & 1][nb][1] = fmaf(b8[gl] * f[nb], dB[nb][2] + dB[nb][3], cB[gl & 1][nb][1]);
-            }
-        }
+    if (ng == 4) {  // full stage: straight-line code
+        group2<NB, 0>(wa, wb, gid, q, sA0.x, sA8.x, sB0.x, sB8.x, bp0, fp0, cA, cB);
+        group2<NB, 1>(wa, wb, gid, q, sA0.y, sA8.y, sB0.y, sB8.y, bp0, fp0, cA, cB);
+        group2<NB, 2>(wa, wb, gid, q, sA0.z, sA8.z, sB0.z, sB8.z, bp0, fp0, cA, cB);
+        group2<NB, 3>(wa, wb, gid, q, sA0.w, sA8.w, sB0.w, sB8.w, bp0, fp0, cA, cB);
+    } else {
+        group2<NB, 0>(wa, wb, gid, q, sA0.x, sA8.x, sB0.x, sB8.x, bp0, fp0, cA, cB);
+        if (ng > 1) group2<NB, 1>(wa, wb, gid, q, sA0.y, sA8.y, sB0.y, sB8.y, bp0, fp0, cA, cB);
+        if (ng > 2) group2<NB, 2>(wa, wb, gid, q, sA0.z, sA8.z, sB0.z, sB8.z, bp0, fp0, cA, cB);
     }
 }
 
@@ -312,8 +322,9 @@ __device__ __forceinline__ void t_epilogue(const TmaArgs &a, const TShared &sh, 
 __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant__ TmaArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ TShared sh;
-    uint8_t *ring = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    // 1024-byte alignment by an offset on the shared array itself, so the
+    // compiler keeps shared-window addressing (LDS) for every access.
+    uint8_t *ring = smem_raw + ((1024u - (tc05::smem_addr(smem_raw) & 1023u)) & 1023u);
     uint4 *cells = reinterpret_cast<uint4 *>(ring + kTStages * kTStage);
     float *fac = reinterpret_cast<float *>(ring + kTStages * kTStage + kTBudget);
     float *epi = fac + kTBudget / 256;

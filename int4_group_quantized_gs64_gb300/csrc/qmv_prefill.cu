@@ -108,25 +108,42 @@ __device__ __forceinline__ int pf_brow(const PfArgs &a, int pair) {
     return a.by_pair ? pair : pair / a.k;
 }
 
-// One K group of loads into a slot: own row's packed bytes and scale, and the
-// threads' share of the B tile.
-__device__ __forceinline__ void pf_issue(const PfArgs &a, const PfItem &it, int kg, uint8_t *slot,
-                                         int t) {
-    const int row = pf_row(a, it.tile, t);
-    const uint8_t *wsrc = a.wq + it.e * a.eq + (size_t)row * (a.K / 2) + kg * 32;
-    const uint32_t sW = tc05::smem_addr(slot);
-    cp_async16_s(sW + t * 16, wsrc);
-    cp_async16_s(sW + 4096 + t * 16, wsrc + 16);
-    cp_async4_s(sW + kPfWBytes + t * 4, a.ws + it.e * a.es + (size_t)row * (a.K / 64) + kg);
-    const uint32_t sB = sW + kPfWBytes + kPfSBytes;
-    for (int c = t; c < it.npad * 8; c += kPfThreads) {
-        const int n = c >> 3, ch = c & 7;
-        const int nn = n < it.ntok ? n : it.ntok - 1;
-        const int brow = pf_brow(a, a.list[it.beg + nn]);
-        const uint16_t *src = a.b + (size_t)brow * a.K + kg * 64 + ch * 8;
-        cp_async16_s(sB + (n >> 3) * 1024 + (n & 7) * 128 + ((ch ^ (n & 7)) << 4), src);
+// Per-thread copy sources of the current item: its weight row, its scale row
+// and up to two B-tile chunks (token row, 16-byte chunk), advanced per group.
+struct PfCursor {
+    const uint8_t *wrow;
+    const float *srow;
+    const uint16_t *bsrc[2];
+    uint32_t bdst[2];
+    int nb;  // B chunks this thread copies (0..2)
+
+    __device__ __forceinline__ void set(const PfArgs &a, const PfItem &it, int t) {
+        const int row = pf_row(a, it.tile, t);
+        wrow = a.wq + it.e * a.eq + (size_t)row * (a.K / 2);
+        srow = a.ws + it.e * a.es + (size_t)row * (a.K / 64);
+        nb = 0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int c = t + i * kPfThreads;
+            const int n = c >> 3, ch = c & 7;
+            const int nn = min(n, it.ntok - 1);
+            const bool on = c < it.npad * 8;
+            const int brow = on ? pf_brow(a, a.list[it.beg + nn]) : 0;
+            bsrc[i] = a.b + (size_t)brow * a.K + ch * 8;
+            bdst[i] = kPfWBytes + kPfSBytes + (n >> 3) * 1024 + (n & 7) * 128 + ((ch ^ (n & 7)) << 4);
+            nb += on ? 1 : 0;
+        }
     }
-}
+    // One K group of loads into the slot at shared address sW.
+    __device__ __forceinline__ void issue(uint32_t sW, int kg, int t) const {
+        const uint8_t *w = wrow + kg * 32;
+        cp_async16_s(sW + t * 16, w);
+        cp_async16_s(sW + 4096 + t * 16, w + 16);
+        cp_async4_s(sW + kPfWBytes + t * 4, srow + kg);
+        if (nb > 0) cp_async16_s(sW + bdst[0], bsrc[0] + kg * 64);
+        if (nb > 1) cp_async16_s(sW + bdst[1], bsrc[1] + kg * 64);
+    }
+};
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
     uint32_t d;
@@ -181,8 +198,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(PfArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t mbar[2];
     __shared__ uint32_t tmem_base_s;
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    // 1024-byte alignment by an offset on the shared array itself, so the
+    // compiler keeps shared-window addressing (LDS) for every access.
+    uint8_t *smem = smem_raw + ((1024u - (tc05::smem_addr(smem_raw) & 1023u)) & 1023u);
     const int t = threadIdx.x, warp = t >> 5;
 
     if (warp == 0) tc05::tmem_alloc(&tmem_base_s, kTmemCols);
@@ -208,14 +226,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(PfArgs a) {
 
     // issue-side cursor
     int is_item = 0, is_kg = 0;
-    PfItem is_it{};
-    if (total > 0) is_it = pf_item(a, nu, i0);
+    PfCursor cur{};
+    if (total > 0) cur.set(a, pf_item(a, nu, i0), t);
+    const uint32_t smem_s = tc05::smem_addr(smem);
     auto issue_next = [&](int j) {
         if (j < total) {
-            pf_issue(a, is_it, is_kg, smem + (j % kPfSlots) * kPfSlotBytes, t);
+            cur.issue(smem_s + (j % kPfSlots) * kPfSlotBytes, is_kg, t);
             if (++is_kg == G) {
                 is_kg = 0;
-                if (++is_item < i1 - i0) is_it = pf_item(a, nu, i0 + is_item);
+                if (++is_item < i1 - i0) cur.set(a, pf_item(a, nu, i0 + is_item), t);
             }
         }
         cp_async_commit();
