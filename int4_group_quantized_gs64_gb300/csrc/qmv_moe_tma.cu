@@ -7,11 +7,10 @@
 // "coli_vk_expert_group", "grouped scales in the Vulkan kernels"). What
 // changes is how the weights arrive: one producer warp issues 3-D tensor-map
 // loads (cp.async.bulk.tensor, 128-byte swizzle) of 256 rows x 128 bytes plus
-// their scales per stage into a 4-stage ring guarded by mbarriers, so the 8
-// consumer warps spend no instructions on copies. Each consumer warp owns two
-// 16-row tiles that share the activation operands: for gate+up the gate and
-// up rows of the same 16 hidden units (so SiLU(g) * u is formed in
-// registers), for down two adjacent 16-row tiles.
+// their scales per stage into a 4-stage ring guarded by mbarriers, so the 16
+// consumer warps spend no instructions on copies. Consumer warp w owns stage
+// rows 16w..16w+15: for gate+up warps 0-7 hold gate rows and warps 8-15 the
+// up rows of the same 128 hidden units; for down, 256 consecutive rows.
 //
 // Every mbarrier wait is bounded. Consumers vote after each wait so that they
 // all leave the loop at the same stage; the producer gives up when the
@@ -30,7 +29,7 @@ namespace qmv {
 
 namespace {
 
-constexpr int kTConsumers = 8;
+constexpr int kTConsumers = 16;
 constexpr int kTThreads = 32 * (kTConsumers + 1);
 constexpr int kTStages = 4;
 constexpr int kTRows = 256;                          // weight rows per stage
@@ -40,7 +39,7 @@ constexpr int kTStage = kTStageW + kTStageS;         // 36 KB
 constexpr int kTBudget = 64 * 1024;
 constexpr int kTGuJ = 128;                           // hidden units per gate+up item
 constexpr int kTDnRows = 256;                        // output rows per down item
-constexpr int kTEpi = (kTGuJ * kMaxTok + kTConsumers * 64) * 4;
+constexpr int kTEpi = (2 * kTGuJ * kMaxTok + kTConsumers * 64) * 4;
 constexpr int kTSmem = kTStages * kTStage + kTBudget + kTBudget / 64 + kTEpi + 1024;
 constexpr uint32_t kTWait = 1u << 24;
 
@@ -119,18 +118,14 @@ __device__ __forceinline__ TItem t_item(const TmaArgs &a, int nu, int tiles, int
     return r;
 }
 
-// One group of two 16-row tiles (smem rows ra.. and rb..) against the staged
-// activation units; the B operands are shared by the two tiles.
+// One group of this warp's 16-row tile (smem rows r0..r0+15 of the stage).
 template <int NB, int GL>
-__device__ __forceinline__ void group2(const uint8_t *wa, const uint8_t *wb, int gid, int q,
-                                       float sa0, float sa8, float sb0, float sb8,
+__device__ __forceinline__ void group1(const uint8_t *wa, int gid, int q, float s0, float s8,
                                        const uint4 *const bp0[NB], const float *const fp0[NB],
-                                       float cA[2][NB][2], float cB[2][NB][2]) {
+                                       float c[2][NB][2]) {
     const int off = (((2 * GL + (q >> 1)) ^ gid) << 4) + ((q & 1) << 3);
-    const uint2 wA0 = *reinterpret_cast<const uint2 *>(wa + off);
-    const uint2 wA8 = *reinterpret_cast<const uint2 *>(wa + 1024 + off);
-    const uint2 wB0 = *reinterpret_cast<const uint2 *>(wb + off);
-    const uint2 wB8 = *reinterpret_cast<const uint2 *>(wb + 1024 + off);
+    const uint2 w0 = *reinterpret_cast<const uint2 *>(wa + off);
+    const uint2 w8 = *reinterpret_cast<const uint2 *>(wa + 1024 + off);
     uint4 bu[NB][2];
     float f[NB];
 #pragma unroll
@@ -139,40 +134,33 @@ __device__ __forceinline__ void group2(const uint8_t *wa, const uint8_t *wb, int
         bu[nb][1] = bp0[nb][GL * 16 + 8];
         f[nb] = fp0[nb][GL];
     }
-    float dA[NB][4], dB[NB][4];
-    tile_group_int4<NB>(wA0, wA8, bu, dA);
-    tile_group_int4<NB>(wB0, wB8, bu, dB);
+    float d[NB][4];
+    tile_group_int4<NB>(w0, w8, bu, d);
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-        cA[GL & 1][nb][0] = fmaf(sa0 * f[nb], dA[nb][0] + dA[nb][1], cA[GL & 1][nb][0]);
-        cA[GL & 1][nb][1] = fmaf(sa8 * f[nb], dA[nb][2] + dA[nb][3], cA[GL & 1][nb][1]);
-        cB[GL & 1][nb][0] = fmaf(sb0 * f[nb], dB[nb][0] + dB[nb][1], cB[GL & 1][nb][0]);
-        cB[GL & 1][nb][1] = fmaf(sb8 * f[nb], dB[nb][2] + dB[nb][3], cB[GL & 1][nb][1]);
+        c[GL & 1][nb][0] = fmaf(s0 * f[nb], d[nb][0] + d[nb][1], c[GL & 1][nb][0]);
+        c[GL & 1][nb][1] = fmaf(s8 * f[nb], d[nb][2] + d[nb][3], c[GL & 1][nb][1]);
     }
 }
 
 template <int NB>
-__device__ __forceinline__ void compute_stage2(const uint8_t *slot, int ra, int rb, int ng,
+__device__ __forceinline__ void compute_stage1(const uint8_t *slot, int r0, int ng,
                                                const uint4 *const bp0[NB],
-                                               const float *const fp0[NB], float cA[2][NB][2],
-                                               float cB[2][NB][2]) {
+                                               const float *const fp0[NB], float c[2][NB][2]) {
     const int lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
     const float *ss = reinterpret_cast<const float *>(slot + kTStageW);
-    const float4 sA0 = *reinterpret_cast<const float4 *>(ss + (ra + gid) * 4);
-    const float4 sA8 = *reinterpret_cast<const float4 *>(ss + (ra + gid + 8) * 4);
-    const float4 sB0 = *reinterpret_cast<const float4 *>(ss + (rb + gid) * 4);
-    const float4 sB8 = *reinterpret_cast<const float4 *>(ss + (rb + gid + 8) * 4);
-    const uint8_t *wa = slot + (ra + gid) * 128;
-    const uint8_t *wb = slot + (rb + gid) * 128;
+    const float4 s0 = *reinterpret_cast<const float4 *>(ss + (r0 + gid) * 4);
+    const float4 s8 = *reinterpret_cast<const float4 *>(ss + (r0 + gid + 8) * 4);
+    const uint8_t *wa = slot + (r0 + gid) * 128;
     if (ng == 4) {  // full stage: straight-line code
-        group2<NB, 0>(wa, wb, gid, q, sA0.x, sA8.x, sB0.x, sB8.x, bp0, fp0, cA, cB);
-        group2<NB, 1>(wa, wb, gid, q, sA0.y, sA8.y, sB0.y, sB8.y, bp0, fp0, cA, cB);
-        group2<NB, 2>(wa, wb, gid, q, sA0.z, sA8.z, sB0.z, sB8.z, bp0, fp0, cA, cB);
-        group2<NB, 3>(wa, wb, gid, q, sA0.w, sA8.w, sB0.w, sB8.w, bp0, fp0, cA, cB);
+        group1<NB, 0>(wa, gid, q, s0.x, s8.x, bp0, fp0, c);
+        group1<NB, 1>(wa, gid, q, s0.y, s8.y, bp0, fp0, c);
+        group1<NB, 2>(wa, gid, q, s0.z, s8.z, bp0, fp0, c);
+        group1<NB, 3>(wa, gid, q, s0.w, s8.w, bp0, fp0, c);
     } else {
-        group2<NB, 0>(wa, wb, gid, q, sA0.x, sA8.x, sB0.x, sB8.x, bp0, fp0, cA, cB);
-        if (ng > 1) group2<NB, 1>(wa, wb, gid, q, sA0.y, sA8.y, sB0.y, sB8.y, bp0, fp0, cA, cB);
-        if (ng > 2) group2<NB, 2>(wa, wb, gid, q, sA0.z, sA8.z, sB0.z, sB8.z, bp0, fp0, cA, cB);
+        group1<NB, 0>(wa, gid, q, s0.x, s8.x, bp0, fp0, c);
+        if (ng > 1) group1<NB, 1>(wa, gid, q, s0.y, s8.y, bp0, fp0, c);
+        if (ng > 2) group1<NB, 2>(wa, gid, q, s0.z, s8.z, bp0, fp0, c);
     }
 }
 
@@ -184,18 +172,18 @@ struct TShared {
 };
 
 // Consumer side of one item: returns false when a wait timed out (all
-// consumers agree). acc*: tile A / tile B sums, rows gid / gid+8, token 4nb+q.
+// consumers agree). acc: rows gid / gid+8 of this warp's tile, token 4nb+q.
+// Warp w owns stage rows 16w..16w+15 (gate+up: warps 0-7 gate, 8-15 up).
 template <int NB>
 __device__ __forceinline__ bool t_consume_item(const TmaArgs &a, TShared &sh, uint8_t *ring,
                                                uint4 *cells, float *fac, int ntok, bool reuse,
-                                               int &j, float accA[NB][2], float accB[NB][2]) {
+                                               int &j, float acc[NB][2]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
     const int G = a.G;
     const int CG = chunk_groups(ntok, kTBudget);
-    const int ra = a.mode == 0 ? 16 * warp : 32 * warp;
-    const int rb = a.mode == 0 ? 128 + 16 * warp : 32 * warp + 16;
+    const int r0 = 16 * warp;
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb) accA[nb][0] = accA[nb][1] = accB[nb][0] = accB[nb][1] = 0.f;
+    for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = 0.f;
     int sbt[NB], sdt[NB];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
@@ -224,18 +212,17 @@ __device__ __forceinline__ bool t_consume_item(const TmaArgs &a, TShared &sh, ui
             bp[nb] = cells + (sbt[nb] * ng) * 16 + q * 2 + (gid & 1);
             fp[nb] = fac + sdt[nb] * ng;
         }
-        float cA[2][NB][2], cB[2][NB][2];
+        float c[2][NB][2];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
-                cA[h2][nb][0] = cA[h2][nb][1] = cB[h2][nb][0] = cB[h2][nb][1] = 0.f;
+            for (int nb = 0; nb < NB; ++nb) c[h2][nb][0] = c[h2][nb][1] = 0.f;
         for (int glc = 0; glc < ng; glc += 4, ++j) {
             const int slot = j % kTStages;
             bool ok = tc05::mbar_wait(&sh.full[slot], (uint32_t)((j / kTStages) & 1), kTWait);
             ok = consumers_and(ok);
             if (!ok) return false;
-            compute_stage2<NB>(ring + slot * kTStage, ra, rb, min(4, ng - glc), bp, fp, cA, cB);
+            compute_stage1<NB>(ring + slot * kTStage, r0, min(4, ng - glc), bp, fp, c);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.empty[slot]);
 #pragma unroll
@@ -246,10 +233,8 @@ __device__ __forceinline__ bool t_consume_item(const TmaArgs &a, TShared &sh, ui
         }
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-            accA[nb][0] += cA[0][nb][0] + cA[1][nb][0];
-            accA[nb][1] += cA[0][nb][1] + cA[1][nb][1];
-            accB[nb][0] += cB[0][nb][0] + cB[1][nb][0];
-            accB[nb][1] += cB[0][nb][1] + cB[1][nb][1];
+            acc[nb][0] += c[0][nb][0] + c[1][nb][0];
+            acc[nb][1] += c[0][nb][1] + c[1][nb][1];
         }
     }
     return true;
@@ -257,44 +242,56 @@ __device__ __forceinline__ bool t_consume_item(const TmaArgs &a, TShared &sh, ui
 
 template <int NB>
 __device__ __forceinline__ void t_epilogue(const TmaArgs &a, const TShared &sh, float *epi,
-                                           const TItem &it, const float accA[NB][2],
-                                           const float accB[NB][2]) {
+                                           const TItem &it, const float acc[NB][2]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
     const int ntok = it.ntok;
     if (a.mode == 1) {
         const int H = a.H;
-        const int r0 = it.tile * kTDnRows + 32 * warp;
+        const int r0 = it.tile * kTDnRows + 16 * warp;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
             const int s = 4 * nb + q;
             if (s < ntok) {
                 float *yb = a.y + (size_t)sh.pairs[s] * H;
-                if (r0 + gid < H) yb[r0 + gid] = accA[nb][0];
-                if (r0 + gid + 8 < H) yb[r0 + gid + 8] = accA[nb][1];
-                if (r0 + 16 + gid < H) yb[r0 + 16 + gid] = accB[nb][0];
-                if (r0 + 24 + gid < H) yb[r0 + 24 + gid] = accB[nb][1];
+                if (r0 + gid < H) yb[r0 + gid] = acc[nb][0];
+                if (r0 + gid + 8 < H) yb[r0 + gid + 8] = acc[nb][1];
             }
         }
         return;
     }
-    // gate+up: tile A = gate, tile B = up for the same hidden units
+    // gate+up: warps 0-7 hold gate rows, warps 8-15 the up rows of the same units
+    constexpr int half = kTConsumers / 2;
     const int I = a.I;
-    float *hbuf = epi;
-    float *wbuf = epi + kTGuJ * kMaxTok;
+    float *gbuf = epi;
+    float *hbuf = epi + kTGuJ * kMaxTok;
+    float *wbuf = epi + 2 * kTGuJ * kMaxTok;
     const int j0 = it.tile * kTGuJ;
-    const int lr = 16 * warp + gid;
+    if (warp < half) {
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-        const int s = 4 * nb + q;
-        if (s < ntok) {
-            const float g0 = accA[nb][0], g1 = accA[nb][1];
-            const float h0 = g0 / (1.0f + expf(-g0)) * accB[nb][0];
-            const float h1 = g1 / (1.0f + expf(-g1)) * accB[nb][1];
-            hbuf[lr * kMaxTok + s] = h0;
-            hbuf[(lr + 8) * kMaxTok + s] = h1;
-            float *hb = a.h + (size_t)sh.pairs[s] * I + j0;
-            if (j0 + lr < I) hb[lr] = h0;
-            if (j0 + lr + 8 < I) hb[lr + 8] = h1;
+        for (int nb = 0; nb < NB; ++nb) {
+            const int s = 4 * nb + q;
+            if (s < ntok) {
+                gbuf[(16 * warp + gid) * kMaxTok + s] = acc[nb][0];
+                gbuf[(16 * warp + gid + 8) * kMaxTok + s] = acc[nb][1];
+            }
+        }
+    }
+    consumers_sync();
+    if (warp >= half) {
+        const int lr = 16 * (warp - half) + gid;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const int s = 4 * nb + q;
+            if (s < ntok) {
+                const float g0 = gbuf[lr * kMaxTok + s], g1 = gbuf[(lr + 8) * kMaxTok + s];
+                const float h0 = g0 / (1.0f + expf(-g0)) * acc[nb][0];
+                const float h1 = g1 / (1.0f + expf(-g1)) * acc[nb][1];
+                hbuf[lr * kMaxTok + s] = h0;
+                hbuf[(lr + 8) * kMaxTok + s] = h1;
+                float *hb = a.h + (size_t)sh.pairs[s] * I + j0;
+                if (j0 + lr < I) hb[lr] = h0;
+                if (j0 + lr + 8 < I) hb[lr + 8] = h1;
+            }
         }
     }
     consumers_sync();
@@ -412,13 +409,13 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
                 cur_pi = pi;
             }
             if (it.ntok <= 4) {
-                float accA[1][2], accB[1][2];
-                ok = t_consume_item<1>(a, sh, ring, cells, fac, it.ntok, reuse, j, accA, accB);
-                if (ok) t_epilogue<1>(a, sh, epi, it, accA, accB);
+                float acc[1][2];
+                ok = t_consume_item<1>(a, sh, ring, cells, fac, it.ntok, reuse, j, acc);
+                if (ok) t_epilogue<1>(a, sh, epi, it, acc);
             } else {
-                float accA[2][2], accB[2][2];
-                ok = t_consume_item<2>(a, sh, ring, cells, fac, it.ntok, reuse, j, accA, accB);
-                if (ok) t_epilogue<2>(a, sh, epi, it, accA, accB);
+                float acc[2][2];
+                ok = t_consume_item<2>(a, sh, ring, cells, fac, it.ntok, reuse, j, acc);
+                if (ok) t_epilogue<2>(a, sh, epi, it, acc);
             }
         }
         if (!ok && threadIdx.x == 0) atomicOr(a.status, 2);
