@@ -12,9 +12,11 @@
 // rows 16w..16w+15: for gate+up warps 0-7 hold gate rows and warps 8-15 the
 // up rows of the same 128 hidden units; for down, 256 consecutive rows.
 //
-// Every mbarrier wait is bounded. Consumers vote after each wait so that they
-// all leave the loop at the same stage; the producer gives up when the
-// consumers stop releasing slots; the status word records bit 1.
+// Every mbarrier wait is bounded. A consumer warp whose wait runs out stops
+// waiting but keeps computing (on whatever the slot holds) and keeps every
+// barrier, so all warps finish; the producer gives up when the consumers stop
+// releasing slots and drains its loads before exiting; bit 1 of the status
+// word records the failure (the outputs are then not valid).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -81,18 +83,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *mbar) {
                  : "memory");
 }
 
-// Named barrier over the consumer warps, returning the AND of `ok`.
-__device__ __forceinline__ bool consumers_and(bool ok) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)ok), "n"(32 * kTConsumers)
-        : "memory");
-    return r != 0;
-}
-
 __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kTConsumers) : "memory");
 }
@@ -118,31 +108,43 @@ __device__ __forceinline__ TItem t_item(const TmaArgs &a, int nu, int tiles, int
     return r;
 }
 
-// One group of this warp's 16-row tile (smem rows r0..r0+15 of the stage).
-template <int NB, int GL>
-__device__ __forceinline__ void group1(const uint8_t *wa, int gid, int q, float s0, float s8,
-                                       const uint4 *const bp0[NB], const float *const fp0[NB],
-                                       float c[2][NB][2]) {
-    const int off = (((2 * GL + (q >> 1)) ^ gid) << 4) + ((q & 1) << 3);
-    const uint2 w0 = *reinterpret_cast<const uint2 *>(wa + off);
-    const uint2 w8 = *reinterpret_cast<const uint2 *>(wa + 1024 + off);
+// Fragments of one group of this warp's 16-row tile (smem rows r0..r0+15).
+template <int NB>
+struct GroupFrag {
+    uint2 w0, w8;
     uint4 bu[NB][2];
     float f[NB];
+};
+
+template <int NB, int GL>
+__device__ __forceinline__ void group_load(const uint8_t *wa, int gid, int q,
+                                           const uint4 *const bp0[NB], const float *const fp0[NB],
+                                           GroupFrag<NB> &g) {
+    const int off = (((2 * GL + (q >> 1)) ^ gid) << 4) + ((q & 1) << 3);
+    g.w0 = *reinterpret_cast<const uint2 *>(wa + off);
+    g.w8 = *reinterpret_cast<const uint2 *>(wa + 1024 + off);
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-        bu[nb][0] = bp0[nb][GL * 16];
-        bu[nb][1] = bp0[nb][GL * 16 + 8];
-        f[nb] = fp0[nb][GL];
-    }
-    float d[NB][4];
-    tile_group_int4<NB>(w0, w8, bu, d);
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-        c[GL & 1][nb][0] = fmaf(s0 * f[nb], d[nb][0] + d[nb][1], c[GL & 1][nb][0]);
-        c[GL & 1][nb][1] = fmaf(s8 * f[nb], d[nb][2] + d[nb][3], c[GL & 1][nb][1]);
+        g.bu[nb][0] = bp0[nb][GL * 16];
+        g.bu[nb][1] = bp0[nb][GL * 16 + 8];
+        g.f[nb] = fp0[nb][GL];
     }
 }
 
+template <int NB, int GL>
+__device__ __forceinline__ void group_math(const GroupFrag<NB> &g, float s0, float s8,
+                                           float c[2][NB][2]) {
+    float d[NB][4];
+    tile_group_int4<NB>(g.w0, g.w8, g.bu, d);
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        c[GL & 1][nb][0] = fmaf(s0 * g.f[nb], d[nb][0] + d[nb][1], c[GL & 1][nb][0]);
+        c[GL & 1][nb][1] = fmaf(s8 * g.f[nb], d[nb][2] + d[nb][3], c[GL & 1][nb][1]);
+    }
+}
+
+// One stage of this warp's tile: the fragments of two groups are loaded
+// before their math, so shared-memory latency overlaps the previous math.
 template <int NB>
 __device__ __forceinline__ void compute_stage1(const uint8_t *slot, int r0, int ng,
                                                const uint4 *const bp0[NB],
@@ -152,16 +154,15 @@ __device__ __forceinline__ void compute_stage1(const uint8_t *slot, int r0, int 
     const float4 s0 = *reinterpret_cast<const float4 *>(ss + (r0 + gid) * 4);
     const float4 s8 = *reinterpret_cast<const float4 *>(ss + (r0 + gid + 8) * 4);
     const uint8_t *wa = slot + (r0 + gid) * 128;
-    if (ng == 4) {  // full stage: straight-line code
-        group1<NB, 0>(wa, gid, q, s0.x, s8.x, bp0, fp0, c);
-        group1<NB, 1>(wa, gid, q, s0.y, s8.y, bp0, fp0, c);
-        group1<NB, 2>(wa, gid, q, s0.z, s8.z, bp0, fp0, c);
-        group1<NB, 3>(wa, gid, q, s0.w, s8.w, bp0, fp0, c);
-    } else {
-        group1<NB, 0>(wa, gid, q, s0.x, s8.x, bp0, fp0, c);
-        if (ng > 1) group1<NB, 1>(wa, gid, q, s0.y, s8.y, bp0, fp0, c);
-        if (ng > 2) group1<NB, 2>(wa, gid, q, s0.z, s8.z, bp0, fp0, c);
-    }
+    GroupFrag<NB> g0, g1;
+    group_load<NB, 0>(wa, gid, q, bp0, fp0, g0);
+    if (ng > 1) group_load<NB, 1>(wa, gid, q, bp0, fp0, g1);
+    group_math<NB, 0>(g0, s0.x, s8.x, c);
+    if (ng > 2) group_load<NB, 2>(wa, gid, q, bp0, fp0, g0);
+    if (ng > 1) group_math<NB, 1>(g1, s0.y, s8.y, c);
+    if (ng > 3) group_load<NB, 3>(wa, gid, q, bp0, fp0, g1);
+    if (ng > 2) group_math<NB, 2>(g0, s0.z, s8.z, c);
+    if (ng > 3) group_math<NB, 3>(g1, s0.w, s8.w, c);
 }
 
 struct TShared {
@@ -171,13 +172,14 @@ struct TShared {
     int pairs[kMaxTok];
 };
 
-// Consumer side of one item: returns false when a wait timed out (all
-// consumers agree). acc: rows gid / gid+8 of this warp's tile, token 4nb+q.
+// Consumer side of one item. A wait that runs out sets `failed`; from then on
+// the warp stops waiting but keeps the same sequence of barriers, so every
+// warp reaches the end. acc: rows gid / gid+8 of this warp's tile, token 4nb+q.
 // Warp w owns stage rows 16w..16w+15 (gate+up: warps 0-7 gate, 8-15 up).
 template <int NB>
-__device__ __forceinline__ bool t_consume_item(const TmaArgs &a, TShared &sh, uint8_t *ring,
+__device__ __forceinline__ void t_consume_item(const TmaArgs &a, TShared &sh, uint8_t *ring,
                                                uint4 *cells, float *fac, int ntok, bool reuse,
-                                               int &j, float acc[NB][2]) {
+                                               int &j, bool &failed, float acc[NB][2]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
     const int G = a.G;
     const int CG = chunk_groups(ntok, kTBudget);
@@ -219,9 +221,9 @@ __device__ __forceinline__ bool t_consume_item(const TmaArgs &a, TShared &sh, ui
             for (int nb = 0; nb < NB; ++nb) c[h2][nb][0] = c[h2][nb][1] = 0.f;
         for (int glc = 0; glc < ng; glc += 4, ++j) {
             const int slot = j % kTStages;
-            bool ok = tc05::mbar_wait(&sh.full[slot], (uint32_t)((j / kTStages) & 1), kTWait);
-            ok = consumers_and(ok);
-            if (!ok) return false;
+            if (!failed &&
+                !tc05::mbar_wait(&sh.full[slot], (uint32_t)((j / kTStages) & 1), kTWait))
+                failed = true;
             compute_stage1<NB>(ring + slot * kTStage, r0, min(4, ng - glc), bp, fp, c);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.empty[slot]);
@@ -237,7 +239,6 @@ __device__ __forceinline__ bool t_consume_item(const TmaArgs &a, TShared &sh, ui
             acc[nb][1] += c[0][nb][1] + c[1][nb][1];
         }
     }
-    return true;
 }
 
 template <int NB>
@@ -316,7 +317,7 @@ __device__ __forceinline__ void t_epilogue(const TmaArgs &a, const TShared &sh, 
     consumers_sync();
 }
 
-__global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant__ TmaArgs a) {
+__global__ void __maxnreg__(120) k_moe_tma(const __grid_constant__ TmaArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ TShared sh;
     // 1024-byte alignment by an offset on the shared array itself, so the
@@ -394,8 +395,8 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
     } else {
         // ---------------- consumers
         int j = 0, cur_pi = -1;
-        bool ok = true;
-        for (int item = i0; item < i1 && ok; ++item) {
+        bool failed = false;
+        for (int item = i0; item < i1; ++item) {
             const TItem it = t_item(a, nu, tiles, item);
             const int pi = item / tiles;
             const bool reuse = pi == cur_pi;
@@ -410,15 +411,15 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
             }
             if (it.ntok <= 4) {
                 float acc[1][2];
-                ok = t_consume_item<1>(a, sh, ring, cells, fac, it.ntok, reuse, j, acc);
-                if (ok) t_epilogue<1>(a, sh, epi, it, acc);
+                t_consume_item<1>(a, sh, ring, cells, fac, it.ntok, reuse, j, failed, acc);
+                t_epilogue<1>(a, sh, epi, it, acc);
             } else {
                 float acc[2][2];
-                ok = t_consume_item<2>(a, sh, ring, cells, fac, it.ntok, reuse, j, acc);
-                if (ok) t_epilogue<2>(a, sh, epi, it, acc);
+                t_consume_item<2>(a, sh, ring, cells, fac, it.ntok, reuse, j, failed, acc);
+                t_epilogue<2>(a, sh, epi, it, acc);
             }
         }
-        if (!ok && threadIdx.x == 0) atomicOr(a.status, 2);
+        if (failed && (threadIdx.x & 31) == 0) atomicOr(a.status, 2);
     }
     __syncthreads();
 }
