@@ -225,6 +225,25 @@ def load_traffic(kernel: str):
     return d["bytes_per_launch"] if h.hexdigest() == d.get("sha256") else None
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(t_step: float, device=None) -> float:
+    """The slowest rank's step time (every rank gets it); t_step itself on one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return t_step
+    tt = torch.tensor([t_step], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_value(world_size: int, bytes_per_step: float, t_step: float) -> float:
+    """Replicas each run the full step on their own micro-batches: the job moves
+    world_size x bytes_per_step in the slowest rank's step time (GB/s)."""
+    return world_size * bytes_per_step / t_step / 1e9
+
+
 # ------------------------------------------------------------------ ours
 
 def run_ours(args):
@@ -282,9 +301,7 @@ def run_ours(args):
     t_step = time_graphs(graphs, args.steps, stream)
     torch.cuda.synchronize()
     if ws_n > 1:
-        tt = torch.tensor([t_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step = float(tt.item())
+        t_step = max_over_ranks(t_step, dev)
         dist.barrier()
     clk = clocks.stop()
 
@@ -308,11 +325,12 @@ def run_ours(args):
     gu_bytes = batches[0]["U"] * (2 * wl["I"] * wl["H"] // 2 + 2 * wl["I"] * wl["H"] // 64 * 4) \
         + T * wl["H"] * 4 + T * k * wl["I"] * 4
     peak, peak_kind = peaks()
-    roofline = {"bound": "hbm", "kernel": "k_gate_up", "achieved": gu_bytes / t_gu / 1e9,
+    gu_kernel = "k_moe_tma" if q.moe_weight_path(m) == 1 else "k_gate_up"
+    roofline = {"bound": "hbm", "kernel": gu_kernel, "achieved": gu_bytes / t_gu / 1e9,
                 "peak": peak, "unit": "GB/s", "frac": gu_bytes / t_gu / 1e9 / peak,
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
-                "traffic": load_traffic("k_gate_up"),
+                "traffic": load_traffic(gu_kernel + " gate+up"),
                 "bytes_per_launch": gu_bytes, "us_per_launch": t_gu * 1e6}
 
     # ---- end to end through the public API with pinned host buffers
@@ -339,12 +357,14 @@ def run_ours(args):
         e1.record(stream)
     e1.synchronize()
     t_e2e = e0.elapsed_time(e1) * 1e-3 / n_e2e
+    if ws_n > 1:
+        t_e2e = max_over_ranks(t_e2e, dev)
 
     rows = measure_rows(q, datagen, dev, stream, peak, m) if rank == 0 and not args.quick else {}
 
     if rank != 0:
         return 0
-    value = ws_n * B_mean / t_step / 1e9
+    value = whole_job_value(ws_n, B_mean, t_step)
     cpu = None
     if ws_n == 1 and not args.no_cpu:
         cb = cpu_baseline(wl, batches[0])
@@ -366,7 +386,7 @@ def run_ours(args):
         "token_eq_per_s": ws_n * T / t_step,
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": ws_n * B_mean / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_value(ws_n, B_mean, t_e2e), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "us_per_step": t_e2e * 1e6},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,

@@ -189,8 +189,9 @@ size_t moe_workspace_bytes(const qmv_moe_int4 *m, int T, int k);
  *   x [T][H] fp32, ids [T][k] int32, w [T][k] fp32, out [T][H] fp32.
  *   ws: device workspace of at least moe_workspace_bytes(m, T, k) bytes,
  *   256-byte aligned, owned by the caller, not shared between concurrent calls.
- *   The first int32 of ws is the device status word of moe_group (cleared at
- *   the start of the call). */
+ *   The first int32 of ws is a device status word, cleared at the start of
+ *   the call: bit 0 = an id outside [0, E) (that pair skipped, as moe_group),
+ *   bit 1 = a bounded wait on the weight stream ran out (out not valid). */
 int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids,
                         const float *w, int k, float *out, void *ws, size_t ws_bytes,
                         qmv_stream_t stream);
@@ -214,6 +215,16 @@ int moe_ffn_down(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
                  qmv_stream_t stream);
 int moe_ffn_combine(const qmv_moe_int4 *m, const int32_t *ids, const float *w, int T, int k,
                     float *out, void *ws, size_t ws_bytes, qmv_stream_t stream);
+
+/* Which weight stream the decode gate+up and down kernels of this descriptor
+ * use (no counterpart on the pages; it names the kernel a profile shows):
+ *   1  tensor-map bulk copies (TMA) into an mbarrier-guarded ring, taken when
+ *      H/64 and I/64 are multiples of 4 and the four pools are 16-byte aligned;
+ *   0  per-warp cp.async rings otherwise.
+ * Both compute the same result. Host only, enqueues nothing.
+ * Errors: those of the descriptor check shared by every MoE call (QMV_EINVAL,
+ * QMV_ESHAPE, QMV_EALIGN). */
+int moe_weight_path(const qmv_moe_int4 *m);
 
 /* Workspace of moe_expert_ffn_int4_prefill, in bytes (0 for unsupported sizes). */
 size_t moe_prefill_workspace_bytes(const qmv_moe_int4 *m, int T, int k);

@@ -73,6 +73,7 @@ def lib():
             "moe_ffn_gate_up": ([P, i32, i32, vp, sz, vp], i32),
             "moe_ffn_down": ([P, i32, i32, vp, sz, vp], i32),
             "moe_ffn_combine": ([P, vp, vp, i32, i32, vp, vp, sz, vp], i32),
+            "moe_weight_path": ([P], i32),
             "moe_prefill_workspace_bytes": ([P, i32, i32], sz),
             "moe_expert_ffn_int4_prefill": ([P, vp, i32, vp, vp, i32, vp, vp, sz, vp], i32),
         }
@@ -296,6 +297,14 @@ def moe_ffn_combine(m: MoeInt4Weights, ids, w, out, ws, stream=None):
     _check("moe_ffn_combine", lib().moe_ffn_combine(m.desc, _ptr(ids), _ptr(w), T, k, _ptr(out),
                                                     _ptr(ws), ws.numel(), _stream(stream)))
     return out
+
+
+def moe_weight_path(m: MoeInt4Weights) -> int:
+    """1: decode kernels stream weights by tensor-map (TMA) copies; 0: cp.async rings."""
+    r = int(lib().moe_weight_path(m.desc))
+    if r < 0:
+        _check("moe_weight_path", r)
+    return r
 
 
 def moe_prefill_workspace_bytes(m: MoeInt4Weights, T: int, k: int) -> int:

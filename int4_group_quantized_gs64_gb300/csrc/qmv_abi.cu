@@ -144,14 +144,17 @@ int moe_gate_up_silu(const qmv_moe_int4 *m, const float *x, int T, int k, const 
     int32_t *pass_ofs = reinterpret_cast<int32_t *>(b + L.pass_ofs);
     float *xfac = reinterpret_cast<float *>(b + L.xfac);
     const cudaStream_t st = cs(stream);
-    cudaError_t e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
+    int32_t *cnt = reinterpret_cast<int32_t *>(b + L.sk_cnt);
+    float *part = reinterpret_cast<float *>(b + L.sk_part);
+    cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * qmv::kSkMaxCtas, st);
+    if (e == cudaSuccess) e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
     if (e == cudaSuccess) e = qmv::launch_split(x, T, m->H, b + L.xcells, xfac, st);
     if (e == cudaSuccess) {
         float *hfac = reinterpret_cast<float *>(b + L.hfac);
         if (qmv::tma_moe_supported(dims(m)))
             e = qmv::launch_moe_tma(dims(m), 0, b + L.xcells, xfac, k, offsets, list, uexp, n_used,
                                     pass_ofs, h, b + L.hcells, hfac, nullptr,
-                                    reinterpret_cast<int32_t *>(b + L.status), st);
+                                    reinterpret_cast<int32_t *>(b + L.status), cnt, part, st);
         else
             e = qmv::launch_gate_up(dims(m), b + L.xcells, xfac, k, offsets, list, uexp, n_used,
                                     pass_ofs, h, b + L.hcells, hfac, st);
@@ -175,13 +178,16 @@ int moe_down(const qmv_moe_int4 *m, const float *h, int T, int k, const int32_t 
     int32_t *pass_ofs = reinterpret_cast<int32_t *>(b + L.pass_ofs);
     float *hfac = reinterpret_cast<float *>(b + L.hfac);
     const cudaStream_t st = cs(stream);
-    cudaError_t e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
+    int32_t *cnt = reinterpret_cast<int32_t *>(b + L.sk_cnt) + qmv::kSkMaxCtas;
+    float *part = reinterpret_cast<float *>(b + L.sk_part);
+    cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * qmv::kSkMaxCtas, st);
+    if (e == cudaSuccess) e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
     if (e == cudaSuccess) e = qmv::launch_split(h, T * k, m->I, b + L.hcells, hfac, st);
     if (e == cudaSuccess) {
         if (qmv::tma_moe_supported(dims(m)))
             e = qmv::launch_moe_tma(dims(m), 1, b + L.hcells, hfac, k, offsets, list, uexp, n_used,
                                     pass_ofs, nullptr, nullptr, nullptr, y,
-                                    reinterpret_cast<int32_t *>(b + L.status), st);
+                                    reinterpret_cast<int32_t *>(b + L.status), cnt, part, st);
         else
             e = qmv::launch_down(dims(m), b + L.hcells, hfac, offsets, list, uexp, n_used, pass_ofs,
                                  y, st);
@@ -206,7 +212,7 @@ int moe_ffn_prepare(const qmv_moe_int4 *m, const float *x, int T, const int32_t 
     if (!x || !ids) return QMV_EINVAL;
     if (!aligned(x, 4) || !aligned(ids, 4)) return QMV_EALIGN;
     const cudaStream_t st = cs(stream);
-    cudaError_t e = cudaMemsetAsync(at<int32_t>(ws, L.status), 0, sizeof(int32_t), st);
+    cudaError_t e = cudaMemsetAsync(at<int32_t>(ws, L.status), 0, L.status_bytes, st);
     if (e == cudaSuccess)
         e = qmv::launch_group_split(ids, T, k, m->E, at<int32_t>(ws, L.offsets),
                                     at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
@@ -227,7 +233,7 @@ int moe_ffn_gate_up(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_byt
             at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
             at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs), at<float>(ws, L.h),
             at<void>(ws, L.hcells), at<float>(ws, L.hfac), nullptr, at<int32_t>(ws, L.status),
-            cs(stream)));
+            at<int32_t>(ws, L.sk_cnt), at<float>(ws, L.sk_part), cs(stream)));
     return from_cuda(qmv::launch_gate_up(
         dims(m), at<void>(ws, L.xcells), at<float>(ws, L.xfac), k, at<int32_t>(ws, L.offsets),
         at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp), at<int32_t>(ws, L.n_used),
@@ -245,7 +251,8 @@ int moe_ffn_down(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
             dims(m), 1, at<void>(ws, L.hcells), at<float>(ws, L.hfac), k,
             at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
             at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs), nullptr, nullptr, nullptr,
-            at<float>(ws, L.y), at<int32_t>(ws, L.status), cs(stream)));
+            at<float>(ws, L.y), at<int32_t>(ws, L.status), at<int32_t>(ws, L.sk_cnt) + qmv::kSkMaxCtas,
+            at<float>(ws, L.sk_part), cs(stream)));
     return from_cuda(qmv::launch_down(dims(m), at<void>(ws, L.hcells), at<float>(ws, L.hfac),
                                       at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list),
                                       at<int32_t>(ws, L.uexp), at<int32_t>(ws, L.n_used),
@@ -261,6 +268,12 @@ int moe_ffn_combine(const qmv_moe_int4 *m, const int32_t *ids, const float *w, i
     if (!aligned(ids, 4) || !aligned(w, 4) || !aligned(out, 4)) return QMV_EALIGN;
     return from_cuda(qmv::launch_combine(at<float>(ws, L.y), ids, w, T, k, m->E, m->H, out,
                                          cs(stream), true));
+}
+
+int moe_weight_path(const qmv_moe_int4 *m) {
+    const int r = check_moe(m);
+    if (r) return r;
+    return qmv::tma_moe_supported(dims(m)) ? 1 : 0;
 }
 
 int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids,

@@ -56,15 +56,25 @@ int prefill_pass_tokens();
 
 // TMA-fed decode kernels (qmv_moe_tma.cu): mode 0 = gate+up (cells = x units,
 // writes h, h units, h factors), mode 1 = down (cells = h units, writes y).
+// The weight stages of all items are shared out evenly over the CTAs; an item
+// split between CTAs leaves partial sums in `part` and the last CTA to finish
+// it (counted in cnt, which must be zero at launch and is zero again after
+// the kernel) adds them and writes the item.
+constexpr int kSkMaxCtas = 256;                 // CTAs of one launch, at most
+constexpr int kSkPartFloats = 2 * 256 * 8;      // per CTA: 2 slots x 256 rows x 8 tokens
 bool tma_moe_supported(const MoeDims &m);
 cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const float *cfac, int k,
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                            const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,
-                           float *hfac, float *y, int32_t *status, cudaStream_t st);
+                           float *hfac, float *y, int32_t *status, int32_t *cnt, float *part,
+                           cudaStream_t st);
 
-// Workspace layout of the MoE entry points (256-byte aligned segments).
+// Workspace layout of the MoE entry points (256-byte aligned segments). The
+// status word and the split counters (kSkMaxCtas for gate+up, then kSkMaxCtas
+// for down) are adjacent, so one memset of status_bytes clears them all.
 struct MoeWorkspace {
-    size_t status, offsets, list, uexp, n_used, pass_ofs, xcells, xfac, h, hcells, hfac, y, total;
+    size_t status, sk_cnt, status_bytes, offsets, list, uexp, n_used, pass_ofs, xcells, xfac, h,
+        hcells, hfac, y, sk_part, total;
 };
 MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k);
 

@@ -588,7 +588,10 @@ MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k) {
     MoeWorkspace L{};
     const size_t P = (size_t)T * k;
     size_t o = 0;
-    L.status = o; o = align256(o + 4);
+    L.status = o;
+    L.sk_cnt = o + 4;
+    L.status_bytes = 4 + 4 * 2 * (size_t)kSkMaxCtas;
+    o = align256(o + L.status_bytes);
     L.offsets = o; o = align256(o + 4 * (size_t)(E + 1));
     L.list = o; o = align256(o + 4 * P);
     L.uexp = o; o = align256(o + 4 * (size_t)E);
@@ -600,6 +603,7 @@ MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k) {
     L.hcells = o; o = align256(o + 4 * P * I);
     L.hfac = o; o = align256(o + 4 * P * (I / 64));
     L.y = o; o = align256(o + 4 * P * H);
+    L.sk_part = o; o = align256(o + 4 * (size_t)kSkMaxCtas * kSkPartFloats);
     L.total = o;
     return L;
 }

@@ -117,6 +117,12 @@ def test_moe_validation(L):
     assert L.moe_gate_up_silu(ctypes.byref(d), p, 3, 2, p, p, p, p, p, ws, need - 1, None) == EWORKSPACE
     assert L.moe_down(ctypes.byref(d), p, 3, 2, p, p, p, p, p, ws, need - 1, None) == EWORKSPACE
     assert L.moe_combine(p, p, None, 3, 2, 8, 128, p, None) == EINVAL
+    # weight-path query: same descriptor rule; a valid descriptor answers 0 or 1
+    assert L.moe_weight_path(None) == EINVAL
+    assert L.moe_weight_path(ctypes.byref(_desc(gs=32))) == EINVAL
+    assert L.moe_weight_path(ctypes.byref(_desc(I=96))) == ESHAPE
+    assert L.moe_weight_path(ctypes.byref(bad)) == EALIGN
+    assert L.moe_weight_path(ctypes.byref(d)) in (0, 1)
 
 
 def test_workspace_grows_with_tokens(L):

@@ -155,10 +155,12 @@ def test_w3_hidden(pool_160):
 
 
 @pytest.mark.parametrize("T,k,E,H,I", [(5, 3, 6, 128, 192), (33, 2, 7, 64, 64), (1, 1, 1, 256, 128),
-                                       (40, 3, 3, 192, 320), (2, 8, 8, 1024, 512)])
+                                       (40, 3, 3, 192, 320), (2, 8, 8, 1024, 512),
+                                       (40, 3, 3, 256, 256), (17, 4, 5, 512, 768)])
 def test_ffn_shapes(T, k, E, H, I):
     """Odd shapes: ragged token counts per expert, > 16 tokens on one expert
-    (several passes), a single expert, k = E."""
+    (several passes), a single expert, k = E. Shapes with H/64 and I/64
+    multiples of 4 run the tensor-map (TMA) kernels, the rest the cp.async ones."""
     rng = np.random.default_rng(T * 100 + k + E)
     wts = dict(
         gu_q=rng.integers(0, 256, size=(E, 2 * I, H // 2), dtype=np.uint8),
@@ -167,6 +169,7 @@ def test_ffn_shapes(T, k, E, H, I):
         dn_s=(np.abs(rng.normal(0, 0.02, size=(E, H, I // 64))) + 1e-4).astype(np.float32),
     )
     m = q.MoeInt4Weights.from_numpy(wts)
+    assert q.moe_weight_path(m) == int((H // 64) % 4 == 0 and (I // 64) % 4 == 0)
     x = rng.normal(size=(T, H)).astype(np.float32)
     logits = rng.normal(size=(T, E)).astype(np.float32)
     ids, w = oracle.route_topk(logits, k)
@@ -198,3 +201,27 @@ def test_ffn_deterministic(pool_160):
     a = q.moe_expert_ffn_int4(pool_160, dev(x), dev(ids), dev(w)).cpu().numpy()
     b = q.moe_expert_ffn_int4(pool_160, dev(x), dev(ids), dev(w)).cpu().numpy()
     assert np.array_equal(a, b)
+
+
+def test_ffn_phases_repeat_match_fused():
+    """The four phases reproduce the fused call bit for bit, also when gate+up
+    and down run again on one prepared workspace (items split between CTAs
+    leave their counters at zero for the next launch)."""
+    wl = W2
+    wts = datagen.moe_weights(wl["E"], wl["H"], wl["I"])
+    m = q.MoeInt4Weights.from_numpy(wts)
+    x, ids, w = _route_oracle(wl)
+    dx, dids, dw = dev(x), dev(ids), dev(w)
+    fused = q.moe_expert_ffn_int4(m, dx, dids, dw).cpu().numpy()
+    T, k = ids.shape
+    ws = torch.empty(q.moe_workspace_bytes(m, T, k), dtype=torch.uint8, device="cuda")
+    q.moe_ffn_prepare(m, dx, dids, ws)
+    outs = []
+    for _ in range(3):
+        q.moe_ffn_gate_up(m, T, k, ws)
+        q.moe_ffn_down(m, T, k, ws)
+        out = torch.empty((T, wl["H"]), dtype=torch.float32, device="cuda")
+        outs.append(q.moe_ffn_combine(m, dids, dw, out, ws).cpu().numpy())
+    assert int(ws[:4].view(torch.int32).cpu()[0]) == 0
+    for o in outs:
+        assert np.array_equal(o, fused)
