@@ -225,6 +225,34 @@ def load_traffic(kernel: str):
     return d["bytes_per_launch"] if h.hexdigest() == d.get("sha256") else None
 
 
+# ------------------------------------------------------------------ profiling case
+
+def run_profile_case(args):
+    """Small case for ncu captures: the 8-token layer shape (H 6144, I 2048,
+    top-8, 8 tokens) over a pool of only `--profile-experts` experts, run for
+    `--steps` steps without timing. Inputs stay larger than L2 (about 21
+    experts, 0.45 GB, are touched per step with 40 experts)."""
+    import torch
+    import datagen
+    import int4_group_quantized_gs64_gb300 as q
+    q.build()
+    dev = torch.device("cuda")
+    E, H, I, T, k = args.profile_experts, W3["H"], W3["I"], W3["T"], W3["k"]
+    m = q.MoeInt4Weights.from_numpy(datagen.moe_weights(E, H, I), dev)
+    x, logits = datagen.moe_inputs(T, E, H, hot=min(W3["hot"], E // 2))
+    xd, ld = torch.from_numpy(x).to(dev), torch.from_numpy(logits).to(dev)
+    ws = torch.empty(q.moe_workspace_bytes(m, T, k), dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    for _ in range(args.steps):
+        ids, w = q.moe_route_topk(ld, k)
+        q.moe_expert_ffn_int4(m, xd, ids, w, out=out, ws=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": f"MoE decode H{H} I{I} top{k}, {T} tokens, {E}-expert pool",
+                      "experts_touched": int(len(np.unique(ids.cpu().numpy()))),
+                      "steps": args.steps, "launches_per_step": 5}))
+    return 0
+
+
 # ------------------------------------------------------------------ ranks
 
 def max_over_ranks(t_step: float, device=None) -> float:
@@ -489,7 +517,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip the extra rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--profile-experts", type=int, default=0,
+                    help="run the small ncu case with this many experts instead of the bench")
     args = ap.parse_args()
+    if args.profile_experts > 0:
+        return run_profile_case(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
