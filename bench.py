@@ -356,7 +356,7 @@ def run_ours(args):
     gu_bytes = batches[0]["U"] * (2 * wl["I"] * wl["H"] // 2 + 2 * wl["I"] * wl["H"] // 64 * 4) \
         + T * wl["H"] * 4 + T * k * wl["I"] * 4
     peak, peak_kind = peaks()
-    gu_kernel = "k_moe_tc" if q.moe_weight_path(m) == 1 else "k_gate_up"
+    gu_kernel = "k_moe_tma" if q.moe_weight_path(m) == 1 else "k_gate_up"
     roofline = {"bound": "hbm", "kernel": gu_kernel, "achieved": gu_bytes / t_gu / 1e9,
                 "peak": peak, "unit": "GB/s", "frac": gu_bytes / t_gu / 1e9 / peak,
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"

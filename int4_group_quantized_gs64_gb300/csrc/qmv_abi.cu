@@ -148,12 +148,11 @@ int moe_gate_up_silu(const qmv_moe_int4 *m, const float *x, int T, int k, const 
     float *part = reinterpret_cast<float *>(b + L.sk_part);
     cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * qmv::kSkMaxCtas, st);
     if (e == cudaSuccess) e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
-    const int fmt = qmv::tc_moe_supported(dims(m)) ? 1 : 0;
-    if (e == cudaSuccess) e = qmv::launch_split(x, T, m->H, b + L.xcells, xfac, st, fmt);
+    if (e == cudaSuccess) e = qmv::launch_split(x, T, m->H, b + L.xcells, xfac, st);
     if (e == cudaSuccess) {
         float *hfac = reinterpret_cast<float *>(b + L.hfac);
-        if (qmv::tc_moe_supported(dims(m)))
-            e = qmv::launch_moe_tc(dims(m), 0, b + L.xcells, xfac, k, offsets, list, uexp, n_used,
+        if (qmv::tma_moe_supported(dims(m)))
+            e = qmv::launch_moe_tma(dims(m), 0, b + L.xcells, xfac, k, offsets, list, uexp, n_used,
                                     pass_ofs, h, b + L.hcells, hfac, nullptr,
                                     reinterpret_cast<int32_t *>(b + L.status), cnt, part, st);
         else
@@ -183,11 +182,10 @@ int moe_down(const qmv_moe_int4 *m, const float *h, int T, int k, const int32_t 
     float *part = reinterpret_cast<float *>(b + L.sk_part);
     cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * qmv::kSkMaxCtas, st);
     if (e == cudaSuccess) e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
-    const int fmt = qmv::tc_moe_supported(dims(m)) ? 1 : 0;
-    if (e == cudaSuccess) e = qmv::launch_split(h, T * k, m->I, b + L.hcells, hfac, st, fmt);
+    if (e == cudaSuccess) e = qmv::launch_split(h, T * k, m->I, b + L.hcells, hfac, st);
     if (e == cudaSuccess) {
-        if (qmv::tc_moe_supported(dims(m)))
-            e = qmv::launch_moe_tc(dims(m), 1, b + L.hcells, hfac, k, offsets, list, uexp, n_used,
+        if (qmv::tma_moe_supported(dims(m)))
+            e = qmv::launch_moe_tma(dims(m), 1, b + L.hcells, hfac, k, offsets, list, uexp, n_used,
                                     pass_ofs, nullptr, nullptr, nullptr, y,
                                     reinterpret_cast<int32_t *>(b + L.status), cnt, part, st);
         else
@@ -220,8 +218,7 @@ int moe_ffn_prepare(const qmv_moe_int4 *m, const float *x, int T, const int32_t 
                                     at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
                                     at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs),
                                     at<int32_t>(ws, L.status), x, m->H, at<void>(ws, L.xcells),
-                                    at<float>(ws, L.xfac), st, 8,
-                                    qmv::tc_moe_supported(dims(m)) ? 1 : 0);
+                                    at<float>(ws, L.xfac), st);
     return from_cuda(e);
 }
 
@@ -230,8 +227,8 @@ int moe_ffn_gate_up(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_byt
     qmv::MoeWorkspace L;
     int r = ffn_check(m, T, k, ws, ws_bytes, L);
     if (r) return r;
-    if (qmv::tc_moe_supported(dims(m)))
-        return from_cuda(qmv::launch_moe_tc(
+    if (qmv::tma_moe_supported(dims(m)))
+        return from_cuda(qmv::launch_moe_tma(
             dims(m), 0, at<void>(ws, L.xcells), at<float>(ws, L.xfac), k,
             at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
             at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs), at<float>(ws, L.h),
@@ -249,8 +246,8 @@ int moe_ffn_down(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
     qmv::MoeWorkspace L;
     int r = ffn_check(m, T, k, ws, ws_bytes, L);
     if (r) return r;
-    if (qmv::tc_moe_supported(dims(m)))
-        return from_cuda(qmv::launch_moe_tc(
+    if (qmv::tma_moe_supported(dims(m)))
+        return from_cuda(qmv::launch_moe_tma(
             dims(m), 1, at<void>(ws, L.hcells), at<float>(ws, L.hfac), k,
             at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
             at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs), nullptr, nullptr, nullptr,
@@ -276,7 +273,7 @@ int moe_ffn_combine(const qmv_moe_int4 *m, const int32_t *ids, const float *w, i
 int moe_weight_path(const qmv_moe_int4 *m) {
     const int r = check_moe(m);
     if (r) return r;
-    return qmv::tc_moe_supported(dims(m)) ? 1 : 0;
+    return qmv::tma_moe_supported(dims(m)) ? 1 : 0;
 }
 
 int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids,

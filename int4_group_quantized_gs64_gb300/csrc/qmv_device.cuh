@@ -171,18 +171,6 @@ __device__ __forceinline__ uint4 make_unit(const float *v, int u) {
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// ------------------------------------------------------------------ activation rows
-//
-// Layout for the tensor-core decode kernels (qmv_moe_tc.cu): one 64-wide group
-// of one activation row is two rows of 64 fp16, hi then lo (256 bytes), in the
-// K order in which those kernels lay the dequantized weights into tensor
-// memory. One weight word (8 nibbles, elements e0..e7) yields the half2 pairs
-// (e0,e4), (e1,e5), (e2,e6), (e3,e7) (dequant_int4_word), so MMA position
-// kappa of a group holds element tc_elem(kappa).
-__host__ __device__ __forceinline__ int tc_elem(int kappa) {
-    return 8 * (kappa >> 3) + ((kappa & 7) >> 1) + 4 * (kappa & 1);
-}
-
 // Power-of-two exponent that maps max|v| into [2^13, 2^14); 0 for an all-zero group.
 __device__ __forceinline__ int split_exponent(float amax) {
     if (!(amax > 0.0f) || !isfinite(amax)) return 0;
@@ -196,20 +184,6 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
-}
-
-// Warp-wide: one group of one row into its hi and lo rows (32 words each) and
-// its factor. Lane l passes a = v[tc_elem(2l)], b = v[tc_elem(2l + 1)] of the
-// unscaled group values.
-__device__ __forceinline__ void split_group_rows(float a, float b, uint32_t *hi, uint32_t *lo,
-                                                 float *fac, int lane) {
-    const int e = split_exponent(warp_max(fmaxf(fabsf(a), fabsf(b))));
-    const float mul = ldexpf(1.0f, e);
-    a *= mul;
-    b *= mul;
-    hi[lane] = pack_half2(split_part(a, 0), split_part(b, 0));
-    lo[lane] = pack_half2(split_part(a, 1), split_part(b, 1));
-    if (lane == 0) *fac = ldexpf(1.0f, -e);
 }
 
 // ------------------------------------------------------------------ tile compute

@@ -251,29 +251,8 @@ cudaError_t launch_dense(const uint8_t *w, const float *scales, int N, int K, co
 
 }  // namespace
 
-// One CTA per activation row; warp w converts groups w, w + nwarps, ... into
-// hi / lo rows in the tensor-core K order.
-__global__ void __launch_bounds__(256)
-    k_split_rows(const float *__restrict__ v, int K, uint32_t *__restrict__ rows,
-                 float *__restrict__ fac) {
-    pdl_trigger();
-    const int r = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = K / kGroup;
-    const float *row = v + (size_t)r * K;
-    const int e0 = tc_elem(2 * lane);
-    for (int g = warp; g < G; g += blockDim.x >> 5) {
-        uint32_t *dst = rows + ((size_t)r * G + g) * 64;
-        split_group_rows(row[g * kGroup + e0], row[g * kGroup + e0 + 4], dst, dst + 32,
-                         fac + (size_t)r * G + g, lane);
-    }
-}
-
-cudaError_t launch_split(const float *v, int R, int K, void *cells, float *fac, cudaStream_t st,
-                         int fmt) {
+cudaError_t launch_split(const float *v, int R, int K, void *cells, float *fac, cudaStream_t st) {
     if (R == 0) return cudaSuccess;
-    if (fmt == 1)
-        return launch(k_split_rows, dim3(R), dim3(256), 0, st, false, v, K,
-                      static_cast<uint32_t *>(cells), fac);
     return launch(k_split<false>, dim3(R), dim3(256), 0, st, false, v, K,
                   static_cast<uint4 *>(cells), fac);
 }

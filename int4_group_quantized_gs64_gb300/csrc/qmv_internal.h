@@ -31,14 +31,11 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int
 cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
                                int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
-                               cudaStream_t st, int pass_tok = 8, int fmt = 0);
+                               cudaStream_t st, int pass_tok = 8);
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
                           int32_t *pass_ofs, cudaStream_t st, bool pdl);
-// Activation rows [R][K] fp32 -> per 64-group factors [R][K/64] and either
-// fragment cells [R][K/64][16] uint4 (fmt 0) or hi / lo rows [R][K/64][2][64]
-// fp16 in the tensor-core K order (fmt 1); both 256 bytes per group.
-cudaError_t launch_split(const float *v, int R, int K, void *cells, float *fac, cudaStream_t st,
-                         int fmt = 0);
+// Activation rows [R][K] fp32 -> fragment cells [R][K/64][16] uint4 + factors [R][K/64].
+cudaError_t launch_split(const float *v, int R, int K, void *cells, float *fac, cudaStream_t st);
 cudaError_t launch_gate_up(const MoeDims &m, const void *xcells, const float *xfac, int k,
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                            const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,
@@ -57,21 +54,20 @@ cudaError_t launch_prefill(const MoeDims &m, int mode, const uint16_t *b, int k,
                            int32_t *status, cudaStream_t st);
 int prefill_pass_tokens();
 
-// Tensor-core decode kernels (qmv_moe_tc.cu): mode 0 = gate+up (act = x as
-// activation rows, writes h, h rows, h factors), mode 1 = down (act = h rows,
-// writes y). Activation rows: [row][K/64][2][64] fp16 (hi, lo; tc_elem order).
+// TMA-fed decode kernels (qmv_moe_tma.cu): mode 0 = gate+up (cells = x units,
+// writes h, h units, h factors), mode 1 = down (cells = h units, writes y).
 // The weight stages of all items are shared out evenly over the CTAs; an item
 // split between CTAs leaves partial sums in `part` and the last CTA to finish
 // it (counted in cnt, which must be zero at launch and is zero again after
 // the kernel) adds them and writes the item.
 constexpr int kSkMaxCtas = 256;                 // CTAs of one launch, at most
 constexpr int kSkPartFloats = 2 * 256 * 8;      // per CTA: 2 slots x 256 rows x 8 tokens
-bool tc_moe_supported(const MoeDims &m);
-cudaError_t launch_moe_tc(const MoeDims &m, int mode, const void *act, const float *afac, int k,
-                          const int32_t *offsets, const int32_t *list, const int32_t *uexp,
-                          const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hrows,
-                          float *hfac, float *y, int32_t *status, int32_t *cnt, float *part,
-                          cudaStream_t st);
+bool tma_moe_supported(const MoeDims &m);
+cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const float *cfac, int k,
+                           const int32_t *offsets, const int32_t *list, const int32_t *uexp,
+                           const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,
+                           float *hfac, float *y, int32_t *status, int32_t *cnt, float *part,
+                           cudaStream_t st);
 
 // Workspace layout of the MoE entry points (256-byte aligned segments). The
 // status word and the split counters (kSkMaxCtas for gate+up, then kSkMaxCtas

@@ -189,31 +189,18 @@ __device__ void split_row_cta(const float *__restrict__ row, int K, uint4 *cells
     }
 }
 
-// CTA 0 groups the pairs; CTA 1 + t splits token row t of x (fmt 0: fragment
-// units, fmt 1: hi / lo rows for the tensor-core kernels).
+// CTA 0 groups the pairs; CTA 1 + t splits token row t of x.
 __global__ void __launch_bounds__(1024)
     k_group_split(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets, int32_t *list,
                   int32_t *uexp, int32_t *n_used, int32_t *pass_ofs, int32_t *status,
-                  const float *__restrict__ x, int H, uint4 *xcells, float *xfac, int pass_tok,
-                  int fmt) {
+                  const float *__restrict__ x, int H, uint4 *xcells, float *xfac, int pass_tok) {
     pdl_trigger();
     if (blockIdx.x == 0) {
         group_cta(ids, P, E, offsets, list, uexp, n_used, pass_ofs, status, pass_tok);
     } else {
         const int t = blockIdx.x - 1;
         const int G = H / kGroup;
-        if (fmt == 1) {
-            const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, e0 = tc_elem(2 * lane);
-            const float *row = x + (size_t)t * H;
-            uint32_t *rows = reinterpret_cast<uint32_t *>(xcells);
-            for (int g = warp; g < G; g += blockDim.x >> 5) {
-                uint32_t *dst = rows + ((size_t)t * G + g) * 64;
-                split_group_rows(row[g * kGroup + e0], row[g * kGroup + e0 + 4], dst, dst + 32,
-                                 xfac + (size_t)t * G + g, lane);
-            }
-        } else {
-            split_row_cta(x + (size_t)t * H, H, xcells + (size_t)t * G * 16, xfac + (size_t)t * G);
-        }
+        split_row_cta(x + (size_t)t * H, H, xcells + (size_t)t * G * 16, xfac + (size_t)t * G);
     }
 }
 
@@ -549,16 +536,16 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int
                          int32_t *uexp, int32_t *n_used, int32_t *status, cudaStream_t st) {
     return launch(k_group_split, dim3(1), dim3(1024), 0, st, false, ids, P, E, offsets, list, uexp,
                   n_used, (int32_t *)nullptr, status, (const float *)nullptr, 64,
-                  (uint4 *)nullptr, (float *)nullptr, (int)kMaxTok, 0);
+                  (uint4 *)nullptr, (float *)nullptr, (int)kMaxTok);
 }
 
 cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
                                int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
-                               cudaStream_t st, int pass_tok, int fmt) {
+                               cudaStream_t st, int pass_tok) {
     return launch(k_group_split, dim3(x ? 1 + T : 1), dim3(1024), 0, st, false, ids, T * k, E,
                   offsets, list, uexp, n_used, pass_ofs, status, x, H, static_cast<uint4 *>(xcells),
-                  xfac, pass_tok, fmt);
+                  xfac, pass_tok);
 }
 
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,

@@ -1,0 +1,647 @@
+// qmv_moe_tma.cu - MoE decode gate+up and down kernels fed by the Tensor
+// Memory Accelerator.
+//
+// Same arithmetic as k_gate_up / k_down (qmv_moe.cu): exact fp16 weights in
+// registers, fp16 hi/lo activations, warp MMA per 64-group, group scale in
+// fp32 (colibri PR #418, "qmatmul_gate_up.comp + coli_vk_gate_up",
+// "coli_vk_expert_group", "grouped scales in the Vulkan kernels"). What
+// changes is how the operands arrive: one producer warp fills a 4-stage ring
+// guarded by mbarriers. A stage holds 256 weight rows x 4 groups (two 3-D
+// tensor-map loads of 128 rows x 128 bytes, 128-byte swizzle), their scales,
+// and the activation units and factors of the same 4 groups for every token
+// of the pass (one bulk copy each per token), so the 16 consumer warps spend
+// no instructions on copies and never wait on a block barrier inside an item.
+// Consumer warp w owns stage rows 16w..16w+15: for gate+up warps 0-7 hold
+// gate rows and warps 8-15 the up rows of the same 128 hidden units; for
+// down, 256 consecutive rows.
+//
+// Work split: the stages of all items (item-major) are shared out evenly over
+// the CTAs, so every SM streams the same number of weight bytes. An item
+// whose stages fall to several CTAs is finished by the last of them to
+// arrive (an atomic counter; nobody waits for anybody), which adds the
+// partial sums in CTA order and writes the item.
+//
+// Every mbarrier wait is bounded. A consumer warp whose wait runs out stops
+// waiting but keeps computing (on whatever the slot holds) and keeps every
+// barrier, so all warps finish; the producer gives up when the consumers stop
+// releasing slots and drains its loads before exiting; bit 1 of the status
+// word records the failure (the outputs are then not valid).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "qmv_internal.h"
+#include "qmv_launch.cuh"
+#include "qmv_rows.cuh"
+#include "tc05.cuh"
+
+namespace qmv {
+
+namespace {
+
+constexpr int kTConsumers = 16;
+constexpr int kTThreads = 32 * (kTConsumers + 1);
+constexpr int kTStages = 4;
+constexpr int kTRows = 256;                          // weight rows per stage
+constexpr int kTStageW = kTRows * 128;               // 32 KB of packed weights
+constexpr int kTStageS = kTRows * 16;                // 4 KB of scales
+constexpr int kTActTok = 4 * 16 * 16;                // units of 4 groups, one token: 1 KB
+constexpr int kTFacTok = 16;                         // factors of 4 groups, one token
+constexpr int kTOffA = kTStageW + kTStageS;
+constexpr int kTOffF = kTOffA + kMaxTok * kTActTok;
+constexpr int kTStage = (kTOffF + kMaxTok * kTFacTok + 1023) / 1024 * 1024;  // 45 KB
+constexpr int kTGuJ = 128;                           // hidden units per gate+up item
+constexpr int kTDnRows = 256;                        // output rows per down item
+constexpr int kTEpi = (2 * kTGuJ * kMaxTok + kTConsumers * 64) * 4;
+constexpr int kTSmem = kTStages * kTStage + kTEpi + 1024;
+constexpr uint32_t kTWait = 1u << 24;
+
+static_assert(kTStage % 1024 == 0, "stages must stay 1024-aligned for the 128B swizzle");
+static_assert(kSkPartFloats == 2 * kTRows * kMaxTok, "partial-sum slots must match the stage");
+
+struct TmaArgs {
+    CUtensorMap wmap;    // weights: uint8 [E][rows][K/2], box 128 B x 128 rows, 128B swizzle
+    CUtensorMap smap;    // scales: f32 [E][rows][K/64], box 4 x 128 rows
+    int mode;            // 0: gate+up, 1: down
+    int G, I, H, k;
+    const int32_t *offsets, *list, *uexp, *n_used, *pass_ofs;
+    const uint4 *cells;  // activation units [row][G][16]
+    const float *cfac;   // their factors [row][G]
+    float *h;            // gate+up: h fp32 [P][I]
+    uint4 *hcells;       // gate+up: units of h [P][I/64][16]
+    float *hfac;         // gate+up: factors of h [P][I/64]
+    float *y;            // down: y [P][H]
+    int32_t *status;
+    int32_t *cnt;        // per CTA: contributors done on the split item that starts in it
+    float *part;         // per CTA: partial sums [2][kTRows][kMaxTok] (head / tail item)
+};
+
+__device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                          int c2, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(mbar)
+        : "memory");
+}
+
+// Contiguous global -> shared copy (16-byte aligned ends, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(mbar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     tc05::smem_addr(mbar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc05::smem_addr(mbar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kTConsumers) : "memory");
+}
+
+struct TItem {
+    int e, beg, ntok, tile;
+};
+
+// Walks the passes of the grouped pairs in order. `lo` indexes the used
+// experts (uexp); passes of used expert lo are pass_ofs[lo] .. pass_ofs[lo+1]-1.
+struct PassCursor {
+    int lo, pi, e, beg, ntok;
+
+    __device__ __forceinline__ void seek(const TmaArgs &a, int nu, int p) {
+        int l = 0, hgh = nu - 1;
+        while (l < hgh) {
+            const int mid = (l + hgh + 1) >> 1;
+            if (a.pass_ofs[mid] <= p) l = mid; else hgh = mid - 1;
+        }
+        lo = l;
+        pi = -1;
+        to(a, p);
+    }
+    // Moves forward to pass p (p >= the current pass).
+    __device__ __forceinline__ void to(const TmaArgs &a, int p) {
+        if (p == pi) return;
+        while (a.pass_ofs[lo + 1] <= p) ++lo;
+        pi = p;
+        e = a.uexp[lo];
+        const int pass = p - a.pass_ofs[lo];
+        const int b = a.offsets[e], cnt = a.offsets[e + 1] - b;
+        beg = b + pass * kMaxTok;
+        ntok = min(kMaxTok, cnt - pass * kMaxTok);
+    }
+};
+
+// Shared-memory row (within a 16-row tile) that holds MMA row gid (and gid + 8
+// at +8). With the 128-byte swizzle, rows {0,2,4,6} and {1,3,5,7} each spread
+// one 16-byte chunk pair over all 32 banks, so the 64-bit weight loads of a
+// half-warp are conflict-free.
+__device__ __forceinline__ int tile_row(int gid) { return 2 * (gid & 3) + (gid >> 2); }
+
+// Fragments of one group of this warp's 16-row tile (smem rows r0..r0+15).
+template <int NB>
+struct GroupFrag {
+    uint2 w0, w8;
+    uint4 bu[NB][2];
+    float f[NB];
+};
+
+template <int NB, int GL>
+__device__ __forceinline__ void group_load(const uint8_t *wa, int pr, int q,
+                                           const uint4 *const bp0[NB], const float *const fp0[NB],
+                                           GroupFrag<NB> &g) {
+    const int off = (((2 * GL + (q >> 1)) ^ pr) << 4) + ((q & 1) << 3);
+    g.w0 = *reinterpret_cast<const uint2 *>(wa + off);
+    g.w8 = *reinterpret_cast<const uint2 *>(wa + 1024 + off);
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        g.bu[nb][0] = bp0[nb][GL * 16];
+        g.bu[nb][1] = bp0[nb][GL * 16 + 8];
+        g.f[nb] = fp0[nb][GL];
+    }
+}
+
+template <int NB, int GL>
+__device__ __forceinline__ void group_math(const GroupFrag<NB> &g, float s0, float s8,
+                                           float c[2][NB][2]) {
+    float d[NB][4];
+    tile_group_int4<NB>(g.w0, g.w8, g.bu, d);
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        c[GL & 1][nb][0] = fmaf(s0 * g.f[nb], d[nb][0] + d[nb][1], c[GL & 1][nb][0]);
+        c[GL & 1][nb][1] = fmaf(s8 * g.f[nb], d[nb][2] + d[nb][3], c[GL & 1][nb][1]);
+    }
+}
+
+// One stage of this warp's tile: four groups, each loaded then used.
+template <int NB>
+__device__ __forceinline__ void compute_stage(const uint8_t *slot, int r0,
+                                              const uint4 *const bp[NB],
+                                              const float *const fp[NB], float c[2][NB][2]) {
+    const int lane = threadIdx.x & 31, q = lane & 3, pr = tile_row(lane >> 2);
+    const float *s0 = reinterpret_cast<const float *>(slot + kTStageW) + (r0 + pr) * 4;
+    const float *s8 = s0 + 32;
+    const uint8_t *wa = slot + (r0 + pr) * 128;
+    GroupFrag<NB> g;
+    group_load<NB, 0>(wa, pr, q, bp, fp, g);
+    group_math<NB, 0>(g, s0[0], s8[0], c);
+    group_load<NB, 1>(wa, pr, q, bp, fp, g);
+    group_math<NB, 1>(g, s0[1], s8[1], c);
+    group_load<NB, 2>(wa, pr, q, bp, fp, g);
+    group_math<NB, 2>(g, s0[2], s8[2], c);
+    group_load<NB, 3>(wa, pr, q, bp, fp, g);
+    group_math<NB, 3>(g, s0[3], s8[3], c);
+}
+
+struct TShared {
+    uint64_t full[kTStages];
+    uint64_t empty[kTStages];
+    long long ub[kSkMaxCtas + 1];  // first stage of each CTA's range (consumers' copy)
+    int pairs[kMaxTok];
+    int last;
+};
+
+// Consumer side of stages [kb0, kb1) of one item. A wait that runs out sets
+// `failed`; from then on the warp stops waiting but keeps the same sequence
+// of barriers, so every warp reaches the end. acc: rows tile_row(gid) and +8 of this
+// warp's tile, token 4nb+q.
+template <int NB>
+__device__ __forceinline__ void t_consume(TShared &sh, const uint8_t *ring, int ntok, int kb0,
+                                          int kb1, int &j, bool &failed, float acc[NB][2]) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
+    const int r0 = 16 * warp;
+    int ob[NB], of[NB];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        ob[nb] = min(4 * nb + (gid >> 1), ntok - 1) * (kTActTok / 16) + q * 2 + (gid & 1);
+        of[nb] = min(4 * nb + q, ntok - 1) * (kTFacTok / 4);
+    }
+    float c[2][NB][2];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) c[h2][nb][0] = c[h2][nb][1] = 0.f;
+    for (int kb = kb0; kb < kb1; ++kb, ++j) {
+        const int slot = j % kTStages;
+        if (!failed &&
+            !tc05::mbar_wait(&sh.full[slot], (uint32_t)((j / kTStages) & 1), kTWait))
+            failed = true;
+        const uint8_t *sp = ring + slot * kTStage;
+        const uint4 *bp[NB];
+        const float *fp[NB];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            bp[nb] = reinterpret_cast<const uint4 *>(sp + kTOffA) + ob[nb];
+            fp[nb] = reinterpret_cast<const float *>(sp + kTOffF) + of[nb];
+        }
+        compute_stage<NB>(sp, r0, bp, fp, c);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.empty[slot]);
+    }
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        acc[nb][0] = c[0][nb][0] + c[1][nb][0];
+        acc[nb][1] = c[0][nb][1] + c[1][nb][1];
+    }
+}
+
+template <int NB>
+__device__ __forceinline__ void t_epilogue(const TmaArgs &a, const TShared &sh, float *epi,
+                                           int tile, int ntok, const float acc[NB][2]) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3;
+    const int pr = tile_row(lane >> 2);
+    if (a.mode == 1) {
+        const int H = a.H;
+        const int r0 = tile * kTDnRows + 16 * warp + pr;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const int s = 4 * nb + q;
+            if (s < ntok) {
+                float *yb = a.y + (size_t)sh.pairs[s] * H;
+                if (r0 < H) yb[r0] = acc[nb][0];
+                if (r0 + 8 < H) yb[r0 + 8] = acc[nb][1];
+            }
+        }
+        return;
+    }
+    // gate+up: warps 0-7 hold gate rows, warps 8-15 the up rows of the same units
+    constexpr int half = kTConsumers / 2;
+    const int I = a.I;
+    float *gbuf = epi;
+    float *hbuf = epi + kTGuJ * kMaxTok;
+    float *wbuf = epi + 2 * kTGuJ * kMaxTok;
+    const int j0 = tile * kTGuJ;
+    if (warp < half) {
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const int s = 4 * nb + q;
+            if (s < ntok) {
+                gbuf[(16 * warp + pr) * kMaxTok + s] = acc[nb][0];
+                gbuf[(16 * warp + pr + 8) * kMaxTok + s] = acc[nb][1];
+            }
+        }
+    }
+    consumers_sync();
+    if (warp >= half) {
+        const int lr = 16 * (warp - half) + pr;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const int s = 4 * nb + q;
+            if (s < ntok) {
+                const float g0 = gbuf[lr * kMaxTok + s], g1 = gbuf[(lr + 8) * kMaxTok + s];
+                const float h0 = g0 / (1.0f + expf(-g0)) * acc[nb][0];
+                const float h1 = g1 / (1.0f + expf(-g1)) * acc[nb][1];
+                hbuf[lr * kMaxTok + s] = h0;
+                hbuf[(lr + 8) * kMaxTok + s] = h1;
+                float *hb = a.h + (size_t)sh.pairs[s] * I + j0;
+                if (j0 + lr < I) hb[lr] = h0;
+                if (j0 + lr + 8 < I) hb[lr + 8] = h1;
+            }
+        }
+    }
+    consumers_sync();
+    const int Gd = I / kGroup;
+    for (int idx = warp; idx < ntok * 2; idx += kTConsumers) {
+        const int s = idx >> 1, gg = idx & 1;
+        const int gd = tile * 2 + gg;
+        if (gd < Gd) {
+            const float v0 = hbuf[(gg * 64 + lane) * kMaxTok + s];
+            const float v1 = hbuf[(gg * 64 + 32 + lane) * kMaxTok + s];
+            const int e = split_exponent(warp_max(fmaxf(fabsf(v0), fabsf(v1))));
+            const float mul = ldexpf(1.0f, e);
+            wbuf[warp * 64 + lane] = v0 * mul;
+            wbuf[warp * 64 + 32 + lane] = v1 * mul;
+            __syncwarp();
+            const size_t cb = (size_t)sh.pairs[s] * Gd + gd;
+            if (lane < 16) a.hcells[cb * 16 + lane] = make_unit<false>(wbuf + warp * 64, lane);
+            if (lane == 0) a.hfac[cb] = ldexpf(1.0f, -e);
+            __syncwarp();
+        }
+    }
+    consumers_sync();
+}
+
+// The CTA whose range holds stage u (ub: first stage of each CTA, g + 1 entries).
+__device__ __forceinline__ int unit_owner(const long long *ub, int g, long long u) {
+    int l = 0, hgh = g - 1;
+    while (l < hgh) {
+        const int mid = (l + hgh + 1) >> 1;
+        if (ub[mid] <= u) l = mid; else hgh = mid - 1;
+    }
+    return l;
+}
+
+// An item whose stages are split between CTAs: this CTA stores its partial
+// sums (slot 0 if the item is the first of its range, else slot 1), and the
+// last contributor to arrive adds every contributor's partial in CTA order
+// (so the sum does not depend on which CTA finishes last), clears the
+// counter for the next launch and returns true: it then writes the item.
+// No CTA waits for another.
+template <int NB>
+__device__ __forceinline__ bool t_combine(const TmaArgs &a, TShared &sh, int ntok, int item,
+                                          bool head, int ns, float acc[NB][2]) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3;
+    const int g = gridDim.x;
+    const int r = 16 * warp + tile_row(lane >> 2);
+    float *mine = a.part + ((size_t)blockIdx.x * 2 + (head ? 0 : 1)) * (kTRows * kMaxTok);
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        const int s = 4 * nb + q;
+        if (s < ntok) {
+            mine[r * kMaxTok + s] = acc[nb][0];
+            mine[(r + 8) * kMaxTok + s] = acc[nb][1];
+        }
+    }
+    __threadfence();
+    consumers_sync();
+    const long long first = (long long)item * ns;
+    const int bf = unit_owner(sh.ub, g, first), bl = unit_owner(sh.ub, g, first + ns - 1);
+    if (threadIdx.x == 0) {
+        int n = 0;  // CTAs of [bf, bl] with a non-empty range all hold stages of this item
+        for (int c = bf; c <= bl; ++c) n += sh.ub[c + 1] > sh.ub[c];
+        sh.last = atomicAdd(&a.cnt[bf], 1) == n - 1;
+    }
+    consumers_sync();
+    if (!sh.last) return false;
+    __threadfence();
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = 0.f;
+    for (int c = bf; c <= bl; ++c) {
+        const long long c0 = sh.ub[c];
+        if (sh.ub[c + 1] <= c0) continue;
+        const float *pc =
+            a.part + ((size_t)c * 2 + (c0 >= first ? 0 : 1)) * (kTRows * kMaxTok);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const int s = 4 * nb + q;
+            if (s < ntok) {
+                acc[nb][0] += __ldcg(pc + r * kMaxTok + s);
+                acc[nb][1] += __ldcg(pc + (r + 8) * kMaxTok + s);
+            }
+        }
+    }
+    if (threadIdx.x == 0) a.cnt[bf] = 0;
+    return true;
+}
+
+__global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant__ TmaArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ TShared sh;
+    // 1024-byte alignment by an offset on the shared array itself, so the
+    // compiler keeps shared-window addressing (LDS) for every access.
+    uint8_t *ring = smem_raw + ((1024u - (tc05::smem_addr(smem_raw) & 1023u)) & 1023u);
+    float *epi = reinterpret_cast<float *>(ring + kTStages * kTStage);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTStages; ++s) {
+            tc05::mbar_init(&sh.full[s], 1);
+            tc05::mbar_init(&sh.empty[s], kTConsumers);
+        }
+        tc05::fence_mbar_init();
+    }
+    __syncthreads();
+
+    // gate+up needs the grouping (previous kernel) before its first load. The
+    // down kernel's grouping finished before the previous kernel started, so
+    // its producer waits only before its first copy of h units (below).
+    if (a.mode == 0 || warp < kTConsumers) pdl_wait();
+    pdl_trigger();
+
+    const int nu = *a.n_used;
+    const int tiles = a.mode == 0 ? (a.I + kTGuJ - 1) / kTGuJ : (a.H + kTDnRows - 1) / kTDnRows;
+    const int total_items = nu > 0 ? a.pass_ofs[nu] * tiles : 0;
+    const int ns = a.G / 4;
+    // Stage-level split: CTA b takes stages [U*b/g, U*(b+1)/g) of the item-major sequence.
+    const long long U = (long long)total_items * ns;
+    const int g = gridDim.x;
+    const long long u0 = (long long)blockIdx.x * U / g;
+    const long long u1 = (long long)(blockIdx.x + 1) * U / g;
+
+    if (warp == kTConsumers) {
+        // ---------------- producer (whole warp; lane 0 owns the barriers)
+        // Down: the weights of the first kTStages stages are requested before
+        // the previous kernel (which writes h) has finished; their activation
+        // copies only after it has.
+        const int total = (int)(u1 - u0);
+        const int pre = a.mode == 1 ? min(total, kTStages) : 0;
+        const int item0 = (int)(u0 / ns), kb_0 = (int)(u0 - (long long)item0 * ns);
+        PassCursor pc;
+        if (total > 0) pc.seek(a, nu, item0 / tiles);
+        auto weights = [&](int slot, int item, int kb, const PassCursor &c) {
+            const int pi = item / tiles, tile = item - pi * tiles;
+            const int rowA = a.mode == 0 ? tile * kTGuJ : tile * kTDnRows;
+            const int rowB = a.mode == 0 ? a.I + tile * kTGuJ : tile * kTDnRows + 128;
+            const uint32_t base = tc05::smem_addr(ring + slot * kTStage);
+            const uint32_t fb = tc05::smem_addr(&sh.full[slot]);
+            mbar_expect_tx(&sh.full[slot],
+                           (uint32_t)(kTStageW + kTStageS + c.ntok * (kTActTok + kTFacTok)));
+            tma_load3(base, &a.wmap, kb * 128, rowA, c.e, fb);
+            tma_load3(base + 128 * 128, &a.wmap, kb * 128, rowB, c.e, fb);
+            tma_load3(base + kTStageW, &a.smap, kb * 4, rowA, c.e, fb);
+            tma_load3(base + kTStageW + 128 * 16, &a.smap, kb * 4, rowB, c.e, fb);
+        };
+        if (pre > 0) {
+            int item = item0, kb = kb_0;
+            PassCursor c = pc;
+            for (int j = 0; j < pre; ++j) {
+                c.to(a, item / tiles);
+                if (lane == 0) weights(j, item, kb, c);
+                if (++kb == ns) {
+                    kb = 0;
+                    ++item;
+                }
+            }
+            pdl_wait();
+        }
+        int item = item0, kb = kb_0;
+        int myrow = 0, cur_pi = -1;
+        bool ok = true;
+        int issued = 0;
+        for (int j = 0; j < total; ++j) {
+            const int slot = j % kTStages;
+            if (j >= kTStages) {
+                int done = 1;
+                if (lane == 0)
+                    done = tc05::mbar_wait(&sh.empty[slot], (uint32_t)(((j / kTStages) - 1) & 1),
+                                           kTWait);
+                if (!__shfl_sync(0xffffffffu, done, 0)) {
+                    ok = false;
+                    break;
+                }
+            }
+            const int pi = item / tiles;
+            if (pi != cur_pi) {
+                pc.to(a, pi);
+                cur_pi = pi;
+                if (lane < pc.ntok) {
+                    const int p = a.list[pc.beg + lane];
+                    myrow = a.mode == 0 ? p / a.k : p;
+                }
+            }
+            if (j >= pre && lane == 0) weights(slot, item, kb, pc);
+            __syncwarp();
+            if (lane < pc.ntok) {
+                const uint32_t base = tc05::smem_addr(ring + slot * kTStage);
+                const uint32_t fb = tc05::smem_addr(&sh.full[slot]);
+                const size_t cg = (size_t)myrow * a.G + 4 * kb;
+                bulk_load(base + kTOffA + lane * kTActTok, a.cells + cg * 16, kTActTok, fb);
+                bulk_load(base + kTOffF + lane * kTFacTok, a.cfac + cg, kTFacTok, fb);
+            }
+            issued = j + 1;
+            if (++kb == ns) {
+                kb = 0;
+                ++item;
+            }
+        }
+        if (lane == 0) {
+            if (!ok) atomicOr(a.status, 2);
+            // Drain: every copy issued must land before the CTA may exit.
+            for (int j = (issued > kTStages ? issued - kTStages : 0); j < issued; ++j)
+                tc05::mbar_wait(&sh.full[j % kTStages], (uint32_t)((j / kTStages) & 1), kTWait);
+        }
+    } else {
+        // ---------------- consumers
+        for (int i = threadIdx.x; i <= g; i += 32 * kTConsumers)
+            sh.ub[i] = (long long)i * U / g;
+        int j = 0, cur_pi = -1;
+        bool failed = false;
+        PassCursor pc;
+        const int head_item = (int)(u0 / ns);
+        int left = (int)(u1 - u0);
+        int item = head_item, kb0 = (int)(u0 - (long long)head_item * ns);
+        if (left > 0) pc.seek(a, nu, head_item / tiles);
+        for (; left > 0; ++item, kb0 = 0) {
+            const int kb1 = min(ns, kb0 + left);
+            left -= kb1 - kb0;
+            const int pi = item / tiles, tile = item - pi * tiles;
+            const bool fresh = pi != cur_pi;
+            if (fresh) {
+                pc.to(a, pi);
+                consumers_sync();  // the previous epilogue is done with sh.pairs
+                if (threadIdx.x < pc.ntok) sh.pairs[threadIdx.x] = a.list[pc.beg + threadIdx.x];
+                cur_pi = pi;
+            }
+            const bool whole = kb0 == 0 && kb1 == ns;
+            if (pc.ntok <= 4) {
+                float acc[1][2];
+                t_consume<1>(sh, ring, pc.ntok, kb0, kb1, j, failed, acc);
+                if (fresh) consumers_sync();  // sh.pairs written before the epilogue reads it
+                if (whole || t_combine<1>(a, sh, pc.ntok, item, item == head_item, ns, acc))
+                    t_epilogue<1>(a, sh, epi, tile, pc.ntok, acc);
+            } else {
+                float acc[2][2];
+                t_consume<2>(sh, ring, pc.ntok, kb0, kb1, j, failed, acc);
+                if (fresh) consumers_sync();
+                if (whole || t_combine<2>(a, sh, pc.ntok, item, item == head_item, ns, acc))
+                    t_epilogue<2>(a, sh, epi, tile, pc.ntok, acc);
+            }
+        }
+        if (failed && (threadIdx.x & 31) == 0) atomicOr(a.status, 2);
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool make_maps(TmaArgs &a, const uint8_t *wq, const float *ws, int E, int rows, int K) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const int G = K / kGroup;
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)K / 2, (cuuint64_t)rows, (cuuint64_t)E};
+        cuuint64_t strides[2] = {(cuuint64_t)K / 2, (cuuint64_t)rows * (K / 2)};
+        cuuint32_t box[3] = {128, 128, 1};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(wq), dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)G, (cuuint64_t)rows, (cuuint64_t)E};
+        cuuint64_t strides[2] = {(cuuint64_t)G * 4, (cuuint64_t)rows * G * 4};
+        cuuint32_t box[3] = {4, 128, 1};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&a.smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ws), dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+bool tma_moe_supported(const MoeDims &m) {
+    // tensor maps need 16-byte aligned bases and 16-byte strides (scale rows of
+    // K/64 floats: K/64 a multiple of 4)
+    auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    return encode_fn() != nullptr && (m.H / kGroup) % 4 == 0 && (m.I / kGroup) % 4 == 0 &&
+           a16(m.gu_q) && a16(m.gu_s) && a16(m.dn_q) && a16(m.dn_s);
+}
+
+cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const float *cfac, int k,
+                           const int32_t *offsets, const int32_t *list, const int32_t *uexp,
+                           const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,
+                           float *hfac, float *y, int32_t *status, int32_t *cnt, float *part,
+                           cudaStream_t st) {
+    TmaArgs a;
+    memset(&a, 0, sizeof(a));
+    a.mode = mode;
+    a.I = m.I;
+    a.H = m.H;
+    a.k = k;
+    a.offsets = offsets; a.list = list; a.uexp = uexp; a.n_used = n_used; a.pass_ofs = pass_ofs;
+    a.cells = static_cast<const uint4 *>(cells);
+    a.cfac = cfac;
+    a.h = h;
+    a.hcells = static_cast<uint4 *>(hcells);
+    a.hfac = hfac;
+    a.y = y;
+    a.status = status;
+    a.cnt = cnt;
+    a.part = part;
+    bool ok;
+    if (mode == 0) {
+        a.G = m.H / kGroup;
+        ok = make_maps(a, m.gu_q, m.gu_s, m.E, 2 * m.I, m.H);
+    } else {
+        a.G = m.I / kGroup;
+        ok = make_maps(a, m.dn_q, m.dn_s, m.E, m.H, m.I);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    cudaError_t e = set_smem(k_moe_tma, kTSmem);
+    if (e != cudaSuccess) return e;
+    const int grid = std::min(kSkMaxCtas, sm_count() * max_ctas_per_sm(k_moe_tma, kTThreads, kTSmem));
+    return launch(k_moe_tma, dim3(grid), dim3(kTThreads), (size_t)kTSmem, st, true, a);
+}
+
+}  // namespace qmv

@@ -104,14 +104,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            | ((uint32_t)(M >> 4) << 24);    // M / 16
 }
 
-// Instruction descriptor: kind::f16, A and B fp16, D fp32, both K-major,
-// M = 128, N (multiple of 16, <= 256).
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
-    return (1u << 4)                        // D format: f32 (A, B format 0: f16)
-           | ((uint32_t)(N >> 3) << 17)     // N / 8
-           | ((uint32_t)(M >> 4) << 24);    // M / 16
-}
-
 // Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128
 // bytes (64 bf16), 8-row atoms 1024 bytes apart (atom base 1024-aligned).
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
