@@ -256,6 +256,29 @@ def run_profile_case(args):
     return 0
 
 
+def run_profile_dense(args):
+    """ncu case for the dense GEMV: int4-gs64 14336 x 4096, one token, over 4
+    rotating weight copies (132 MB, above L2), `--steps` launches each, no timing."""
+    import torch
+    import datagen
+    import int4_group_quantized_gs64_gb300 as q
+    q.build()
+    dev = torch.device("cuda")
+    N, K = 14336, 4096
+    wq, sc, x = datagen.dense_int4(N, K, 1)
+    ws_ = [torch.from_numpy(wq).to(dev) for _ in range(4)]
+    ss_ = [torch.from_numpy(sc).to(dev) for _ in range(4)]
+    xd = torch.from_numpy(x).to(dev)
+    y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    ws = torch.empty(q.qmv_gemv_workspace_bytes(K, 1), dtype=torch.uint8, device=dev)
+    for i in range(args.steps * 4):
+        q.qmv_int4_gs(ws_[i % 4], ss_[i % 4], xd, y=y, ws=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": f"int4-gs64 GEMV {N}x{K}, 1 token, 4 weight copies",
+                      "launches": args.steps * 4, "kernels_per_launch": 2}))
+    return 0
+
+
 # ------------------------------------------------------------------ ranks
 
 def max_over_ranks(t_step: float, device=None) -> float:
@@ -465,10 +488,12 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     xd = torch.from_numpy(x).to(dev)
     y = torch.empty((1, N), device=dev)
     wsd = torch.empty(q.qmv_gemv_workspace_bytes(K, 1), dtype=torch.uint8, device=dev)
-    gs = [graph_of(lambda i=i: q.qmv_int4_gs(wqs[i], scs[i], xd, y=y, ws=wsd, stream=stream), stream)
-          for i in range(C)]
-    time_graphs(gs, 32, stream)
-    t = time_graphs(gs, 256, stream)
+    # all C calls (rotating weight copies, 530 MB: above L2) in one graph, so
+    # host-side graph launches do not leave the GPU idle between calls
+    gs = [graph_of(lambda: [q.qmv_int4_gs(wqs[i], scs[i], xd, y=y, ws=wsd, stream=stream)
+                            for i in range(C)], stream)]
+    time_graphs(gs, 4, stream)
+    t = time_graphs(gs, 32, stream) / C
     Bq = wq.nbytes + sc.nbytes + x.nbytes + N * 4
     rows["int4_gemv_14336x4096"] = {"us": t * 1e6, "GBs": Bq / t / 1e9, "frac": Bq / t / 1e9 / peak,
                                     "bytes": Bq, "launches_per_call": 2}
@@ -477,10 +502,10 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     C8 = 8
     w8s = [torch.from_numpy(w8).to(dev) for _ in range(C8)]
     r8d = torch.from_numpy(r8).to(dev)
-    gs = [graph_of(lambda i=i: q.qmv_int8_row(w8s[i], r8d, xd, y=y, ws=wsd, stream=stream), stream)
-          for i in range(C8)]
-    time_graphs(gs, 32, stream)
-    t = time_graphs(gs, 256, stream)
+    gs = [graph_of(lambda: [q.qmv_int8_row(w8s[i], r8d, xd, y=y, ws=wsd, stream=stream)
+                            for i in range(C8)], stream)]
+    time_graphs(gs, 4, stream)
+    t = time_graphs(gs, 64, stream) / C8
     B8 = w8.nbytes + r8.nbytes + x.nbytes + N * 4
     rows["int8_gemv_14336x4096"] = {"us": t * 1e6, "GBs": B8 / t / 1e9, "frac": B8 / t / 1e9 / peak,
                                     "bytes": B8, "launches_per_call": 2}
@@ -502,9 +527,9 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
         return lambda: (q.moe_route_topk(l2[i], 8, ids=i2[i], w=w2[i], stream=stream),
                         q.moe_expert_ffn_int4(m2, x2[i], i2[i], w2[i], out=o2[i], ws=ws2[i],
                                               stream=stream))
-    gs = [graph_of(f2(i), stream) for i in range(ROTATE)]
-    time_graphs(gs, 32, stream)
-    t = time_graphs(gs, 256, stream)
+    gs = [graph_of(lambda: [f2(i)() for i in range(ROTATE)], stream)]
+    time_graphs(gs, 4, stream)
+    t = time_graphs(gs, 32, stream) / ROTATE
     B2 = statistics.mean(step_bytes(wl, b["U"]) for b in bs)
     rows["moe_decode_h2048_e256_i512_1tok"] = {"us": t * 1e6, "GBs": B2 / t / 1e9,
                                                "frac": B2 / t / 1e9 / peak, "bytes": B2,
@@ -522,9 +547,13 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--profile-experts", type=int, default=0,
                     help="run the small ncu case with this many experts instead of the bench")
+    ap.add_argument("--profile-dense", action="store_true",
+                    help="run the small ncu case of the dense GEMV instead of the bench")
     args = ap.parse_args()
     if args.profile_experts > 0:
         return run_profile_case(args)
+    if args.profile_dense:
+        return run_profile_dense(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -63,9 +63,12 @@ const char *qmv_status_str(int status);
 /* ---------------------------------------------------------------- GEMV */
 
 /* Scratch needed by qmv_int4_gs / qmv_int8_row for S tokens of length K, in
- * bytes (a multiple of 256; 0 for unsupported sizes). The activations are
- * converted there into fp16 hi/lo fragments with one power-of-two factor per
- * 64-wide group before the weights are streamed. */
+ * bytes (a multiple of 256; 0 for unsupported sizes). It holds a status word
+ * (the first int32, cleared by every call: bit 1 = a bounded device wait ran
+ * out and y is not valid), counters and partial sums for row tiles shared
+ * between thread blocks (about 4 MB, independent of K and S), and the
+ * activations, converted into fp16 hi/lo fragments with one power-of-two
+ * factor per 64-wide group before the weights are streamed. */
 size_t qmv_gemv_workspace_bytes(int K, int S);
 
 /* Dense int4 grouped-scale GEMV (colibri PR #418, commits "opt-in Vulkan
@@ -78,6 +81,10 @@ size_t qmv_gemv_workspace_bytes(int K, int S);
  *   ws      device scratch of at least qmv_gemv_workspace_bytes(K, S) bytes,
  *           256-byte aligned, not shared with a concurrent call
  *   gs must be 64; K a multiple of 64; 1 <= N, 1 <= S, K <= 65536.
+ * When N is a multiple of 256, K/64 a multiple of 4 and wq and scales are
+ * 16-byte aligned, the weights stream through tensor-map (TMA) copies with
+ * the row tiles' work shared evenly over all SMs; other shapes use per-warp
+ * cp.async rings. Both give the same results up to fp32 summation order.
  * Errors: QMV_EINVAL (null pointer, gs != 64, N or S < 1), QMV_ESHAPE (K),
  *         QMV_EALIGN, QMV_EWORKSPACE, QMV_ECUDA. */
 int qmv_int4_gs(const uint8_t *wq, const float *scales, int N, int K, int gs, const float *x,

@@ -80,7 +80,7 @@ const char *qmv_status_str(int status) {
 
 size_t qmv_gemv_workspace_bytes(int K, int S) {
     if (K < 64 || K % 64 || K > kMaxK || S < 1) return 0;
-    return (qmv::dense_scratch_bytes(K, S) + 255) & ~(size_t)255;
+    return qmv::gemv_ws_bytes(K, S);
 }
 
 int qmv_int4_gs(const uint8_t *wq, const float *scales, int N, int K, int gs, const float *x,
@@ -90,7 +90,7 @@ int qmv_int4_gs(const uint8_t *wq, const float *scales, int N, int K, int gs, co
     if (!aligned(wq, 16) || !aligned(scales, 4) || !aligned(x, 4) || !aligned(y, 4))
         return QMV_EALIGN;
     if (!ws || !aligned(ws, 256) || ws_bytes < qmv_gemv_workspace_bytes(K, S)) return QMV_EWORKSPACE;
-    return from_cuda(qmv::launch_dense_int4(wq, scales, N, K, x, y, S, ws, cs(stream)));
+    return from_cuda(qmv::launch_gemv_int4(wq, scales, N, K, x, y, S, ws, cs(stream)));
 }
 
 int qmv_int8_row(const int8_t *w, const float *row_scale, int N, int K, const float *x, float *y,
@@ -100,7 +100,7 @@ int qmv_int8_row(const int8_t *w, const float *row_scale, int N, int K, const fl
     if (!aligned(w, 16) || !aligned(row_scale, 4) || !aligned(x, 4) || !aligned(y, 4))
         return QMV_EALIGN;
     if (!ws || !aligned(ws, 256) || ws_bytes < qmv_gemv_workspace_bytes(K, S)) return QMV_EWORKSPACE;
-    return from_cuda(qmv::launch_dense_int8(w, row_scale, N, K, x, y, S, ws, cs(stream)));
+    return from_cuda(qmv::launch_gemv_int8(w, row_scale, N, K, x, y, S, ws, cs(stream)));
 }
 
 int moe_route_topk(const float *logits, int T, int E, int k, int32_t *ids, float *w,

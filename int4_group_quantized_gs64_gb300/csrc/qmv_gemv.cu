@@ -27,18 +27,25 @@ constexpr int kDenseBudget = 32 * 1024;
 
 // ------------------------------------------------------------------ split
 
-// One CTA per activation row; warp w converts groups w, w + nwarps, ...:
-// max |v| of the group -> exponent -> 16 fragment cells and the factor.
+// Grid (rows, ceil(G / 8)): warp w of CTA (r, c) converts group 8c + w of
+// activation row r (one group per warp, so the rows' groups convert in
+// parallel): max |v| of the group -> exponent -> 16 fragment cells and the
+// factor. CTA (0, 0) also clears zero[0 .. nzero) (the caller's status word
+// and split counters), which the next kernel reads only after waiting for
+// this one.
 template <bool kInt8>
 __global__ void __launch_bounds__(256)
     k_split(const float *__restrict__ v, int K, uint4 *__restrict__ cells,
-            float *__restrict__ fac) {
+            float *__restrict__ fac, int32_t *zero, int nzero) {
     __shared__ float buf[8][64];
     pdl_trigger();  // the consumer may start streaming its weights at once
     const int r = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (zero && r == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
     const int G = K / kGroup;
     const float *row = v + (size_t)r * K;
-    for (int g = warp; g < G; g += blockDim.x >> 5) {
+    const int g = blockIdx.y * (blockDim.x >> 5) + warp;
+    if (g < G) {
         const float a = row[g * kGroup + lane], b = row[g * kGroup + 32 + lane];
         const int e = split_exponent(warp_max(fmaxf(fabsf(a), fabsf(b))));
         const float mul = ldexpf(1.0f, e);
@@ -217,15 +224,16 @@ __global__ void __launch_bounds__(32 * kKsWarps)
 
 template <bool kInt8>
 cudaError_t launch_dense(const uint8_t *w, const float *scales, int N, int K, const float *x,
-                         float *y, int S, void *xcells, float *xfac, cudaStream_t st) {
+                         float *y, int S, void *xcells, float *xfac, cudaStream_t st,
+                         int32_t *zero = nullptr, int nzero = 0) {
     const size_t smem = engine_smem(kDenseWarps, kDenseStages, kDenseBudget, 0);
     cudaError_t e = set_smem(k_dense<kInt8>, smem);
     if (e != cudaSuccess) return e;
     const int nitems = (N + 16 * kDenseWarps - 1) / (16 * kDenseWarps);
     const int slots = sm_count() * max_ctas_per_sm(k_dense<kInt8>, 32 * kDenseWarps, smem);
     const int grid = nitems < slots ? nitems : slots;
-    e = launch(k_split<kInt8>, dim3(S), dim3(256), 0, st, false, x, K,
-               static_cast<uint4 *>(xcells), xfac);
+    e = launch(k_split<kInt8>, dim3(S, (K / kGroup + 7) / 8), dim3(256), 0, st, false, x, K,
+               static_cast<uint4 *>(xcells), xfac, zero, nzero);
     const int G = K / kGroup;
     if (S <= 4 && (size_t)G * S * 256 <= (size_t)kDenseBudget) {
         // one pass, K split over the warps of a CTA
@@ -253,8 +261,8 @@ cudaError_t launch_dense(const uint8_t *w, const float *scales, int N, int K, co
 
 cudaError_t launch_split(const float *v, int R, int K, void *cells, float *fac, cudaStream_t st) {
     if (R == 0) return cudaSuccess;
-    return launch(k_split<false>, dim3(R), dim3(256), 0, st, false, v, K,
-                  static_cast<uint4 *>(cells), fac);
+    return launch(k_split<false>, dim3(R, (K / kGroup + 7) / 8), dim3(256), 0, st, false, v, K,
+                  static_cast<uint4 *>(cells), fac, (int32_t *)nullptr, 0);
 }
 
 size_t dense_scratch_bytes(int K, int S) { return (size_t)S * K * 4 + (size_t)S * (K / kGroup) * 4; }
@@ -270,6 +278,49 @@ cudaError_t launch_dense_int8(const int8_t *w, const float *row_scale, int N, in
     float *fac = reinterpret_cast<float *>(static_cast<char *>(scratch) + (size_t)S * K * 4);
     return launch_dense<true>(reinterpret_cast<const uint8_t *>(w), row_scale, N, K, x, y, S,
                               scratch, fac, st);
+}
+
+// ------------------------------------------------------------------ workspace entry points
+//
+// Workspace of qmv_int4_gs / qmv_int8_row: the status word and the split
+// counters (cleared by the split kernel), the activation units and factors,
+// and the partial sums of row tiles split between CTAs.
+namespace {
+constexpr size_t kGemvHead = 1280;
+static_assert(kGemvHead >= 4 * (1 + (size_t)kSkMaxCtas) && kGemvHead % 256 == 0, "head layout");
+
+size_t gemv_part_offset(int K, int S) {
+    return (kGemvHead + dense_scratch_bytes(K, S) + 255) & ~(size_t)255;
+}
+}  // namespace
+
+size_t gemv_ws_bytes(int K, int S) {
+    return gemv_part_offset(K, S) + (size_t)kSkMaxCtas * kSkPartFloats * 4;
+}
+
+cudaError_t launch_gemv_int4(const uint8_t *wq, const float *scales, int N, int K, const float *x,
+                             float *y, int S, void *ws, cudaStream_t st) {
+    char *b = static_cast<char *>(ws);
+    int32_t *head = reinterpret_cast<int32_t *>(b);
+    void *cells = b + kGemvHead;
+    float *fac = reinterpret_cast<float *>(b + kGemvHead + (size_t)S * K * 4);
+    if (!tma_dense_supported(wq, scales, N, K))
+        return launch_dense<false>(wq, scales, N, K, x, y, S, cells, fac, st, head,
+                                   1 + kSkMaxCtas);
+    float *part = reinterpret_cast<float *>(b + gemv_part_offset(K, S));
+    cudaError_t e = launch(k_split<false>, dim3(S, (K / kGroup + 7) / 8), dim3(256), 0, st, false,
+                           x, K, static_cast<uint4 *>(cells), fac, head, 1 + kSkMaxCtas);
+    if (e != cudaSuccess) return e;
+    return launch_dense_tma(wq, scales, N, K, S, cells, fac, y, head, head + 1, part, st);
+}
+
+cudaError_t launch_gemv_int8(const int8_t *w, const float *row_scale, int N, int K,
+                             const float *x, float *y, int S, void *ws, cudaStream_t st) {
+    char *b = static_cast<char *>(ws);
+    float *fac = reinterpret_cast<float *>(b + kGemvHead + (size_t)S * K * 4);
+    return launch_dense<true>(reinterpret_cast<const uint8_t *>(w), row_scale, N, K, x, y, S,
+                              b + kGemvHead, fac, st, reinterpret_cast<int32_t *>(b),
+                              1 + kSkMaxCtas);
 }
 
 }  // namespace qmv

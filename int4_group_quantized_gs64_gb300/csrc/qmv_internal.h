@@ -2,6 +2,8 @@
 // the ABI layer checks every argument before calling these).
 #pragma once
 
+#include <cuda.h>
+
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -14,6 +16,15 @@ cudaError_t launch_dense_int4(const uint8_t *wq, const float *scales, int N, int
                               const float *x, float *y, int S, void *scratch, cudaStream_t st);
 cudaError_t launch_dense_int8(const int8_t *w, const float *row_scale, int N, int K,
                               const float *x, float *y, int S, void *scratch, cudaStream_t st);
+
+// The GEMV entry points' workspace (status word, split counters, activation
+// units, partial sums): gemv_ws_bytes(K, S) bytes. int4 runs on the
+// tensor-map kernel (qmv_moe_tma.cu, dense mode) when tma_dense_supported().
+size_t gemv_ws_bytes(int K, int S);
+cudaError_t launch_gemv_int4(const uint8_t *wq, const float *scales, int N, int K, const float *x,
+                             float *y, int S, void *ws, cudaStream_t st);
+cudaError_t launch_gemv_int8(const int8_t *w, const float *row_scale, int N, int K,
+                             const float *x, float *y, int S, void *ws, cudaStream_t st);
 
 struct MoeDims {
     const uint8_t *gu_q;
@@ -63,6 +74,14 @@ int prefill_pass_tokens();
 constexpr int kSkMaxCtas = 256;                 // CTAs of one launch, at most
 constexpr int kSkPartFloats = 2 * 256 * 8;      // per CTA: 2 slots x 256 rows x 8 tokens
 bool tma_moe_supported(const MoeDims &m);
+// 3-D tensor maps of a weight pool [E][rows][K/2] (box 128 B x 128 rows,
+// 128-byte swizzle) and of its scales [E][rows][K/64] (box 4 x 128 rows).
+bool encode_weight_maps(CUtensorMap *wmap, CUtensorMap *smap, const uint8_t *wq, const float *ws,
+                        int E, int rows, int K);
+bool tma_dense_supported(const uint8_t *wq, const float *scales, int N, int K);
+cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int K, int S,
+                             const void *cells, const float *cfac, float *y, int32_t *status,
+                             int32_t *cnt, float *part, cudaStream_t st);
 cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const float *cfac, int k,
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                            const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,

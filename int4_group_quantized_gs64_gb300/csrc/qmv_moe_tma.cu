@@ -13,7 +13,8 @@
 // no instructions on copies and never wait on a block barrier inside an item.
 // Consumer warp w owns stage rows 16w..16w+15: for gate+up warps 0-7 hold
 // gate rows and warps 8-15 the up rows of the same 128 hidden units; for
-// down, 256 consecutive rows.
+// down, 256 consecutive rows. The dense int4-gs64 GEMV (qmv_int4_gs) runs as
+// a third mode: one matrix, its S tokens in passes of 8, row tiles of 256.
 //
 // Work split: the stages of all items (item-major) are shared out evenly over
 // the CTAs, so every SM streams the same number of weight bytes. An item
@@ -64,8 +65,9 @@ static_assert(kSkPartFloats == 2 * kTRows * kMaxTok, "partial-sum slots must mat
 struct TmaArgs {
     CUtensorMap wmap;    // weights: uint8 [E][rows][K/2], box 128 B x 128 rows, 128B swizzle
     CUtensorMap smap;    // scales: f32 [E][rows][K/64], box 4 x 128 rows
-    int mode;            // 0: gate+up, 1: down
+    int mode;            // 0: gate+up, 1: down, 2: dense GEMV (one matrix, tokens 0..S-1)
     int G, I, H, k;
+    int S;               // dense: tokens
     const int32_t *offsets, *list, *uexp, *n_used, *pass_ofs;
     const uint4 *cells;  // activation units [row][G][16]
     const float *cfac;   // their factors [row][G]
@@ -123,6 +125,11 @@ struct PassCursor {
     int lo, pi, e, beg, ntok;
 
     __device__ __forceinline__ void seek(const TmaArgs &a, int nu, int p) {
+        pi = -1;
+        if (a.mode == 2) {
+            to(a, p);
+            return;
+        }
         int l = 0, hgh = nu - 1;
         while (l < hgh) {
             const int mid = (l + hgh + 1) >> 1;
@@ -135,6 +142,13 @@ struct PassCursor {
     // Moves forward to pass p (p >= the current pass).
     __device__ __forceinline__ void to(const TmaArgs &a, int p) {
         if (p == pi) return;
+        if (a.mode == 2) {  // dense: pass p is tokens 8p .. 8p + 7 of the one matrix
+            pi = p;
+            e = 0;
+            beg = p * kMaxTok;
+            ntok = min(kMaxTok, a.S - beg);
+            return;
+        }
         while (a.pass_ofs[lo + 1] <= p) ++lo;
         pi = p;
         e = a.uexp[lo];
@@ -263,7 +277,7 @@ __device__ __forceinline__ void t_epilogue(const TmaArgs &a, const TShared &sh, 
                                            int tile, int ntok, const float acc[NB][2]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3;
     const int pr = tile_row(lane >> 2);
-    if (a.mode == 1) {
+    if (a.mode != 0) {
         const int H = a.H;
         const int r0 = tile * kTDnRows + 16 * warp + pr;
 #pragma unroll
@@ -365,18 +379,24 @@ __device__ __forceinline__ bool t_combine(const TmaArgs &a, TShared &sh, int nto
             mine[(r + 8) * kMaxTok + s] = acc[nb][1];
         }
     }
-    __threadfence();
+    // The barrier orders every consumer's partial-sum stores before thread 0's
+    // fence, whose cumulativity makes them visible device-wide before its
+    // counter update; on the other side thread 0's fence after the update
+    // orders the other CTAs' partials before the barrier that the readers
+    // pass. One fence per side, by the thread that touches the counter.
     consumers_sync();
     const long long first = (long long)item * ns;
     const int bf = unit_owner(sh.ub, g, first), bl = unit_owner(sh.ub, g, first + ns - 1);
     if (threadIdx.x == 0) {
         int n = 0;  // CTAs of [bf, bl] with a non-empty range all hold stages of this item
         for (int c = bf; c <= bl; ++c) n += sh.ub[c + 1] > sh.ub[c];
-        sh.last = atomicAdd(&a.cnt[bf], 1) == n - 1;
+        __threadfence();
+        const bool last = atomicAdd(&a.cnt[bf], 1) == n - 1;
+        if (last) __threadfence();
+        sh.last = last;
     }
     consumers_sync();
     if (!sh.last) return false;
-    __threadfence();
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = 0.f;
     for (int c = bf; c <= bl; ++c) {
@@ -416,14 +436,16 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
     __syncthreads();
 
     // gate+up needs the grouping (previous kernel) before its first load. The
-    // down kernel's grouping finished before the previous kernel started, so
-    // its producer waits only before its first copy of h units (below).
+    // down kernel's grouping finished before the previous kernel started, and
+    // the dense GEMV has none, so their producers wait only before their first
+    // copy of activation units (below).
     if (a.mode == 0 || warp < kTConsumers) pdl_wait();
     pdl_trigger();
 
-    const int nu = *a.n_used;
+    const int nu = a.mode == 2 ? 1 : *a.n_used;
     const int tiles = a.mode == 0 ? (a.I + kTGuJ - 1) / kTGuJ : (a.H + kTDnRows - 1) / kTDnRows;
-    const int total_items = nu > 0 ? a.pass_ofs[nu] * tiles : 0;
+    const int passes = a.mode == 2 ? (a.S + kMaxTok - 1) / kMaxTok : (nu > 0 ? a.pass_ofs[nu] : 0);
+    const int total_items = passes * tiles;
     const int ns = a.G / 4;
     // Stage-level split: CTA b takes stages [U*b/g, U*(b+1)/g) of the item-major sequence.
     const long long U = (long long)total_items * ns;
@@ -433,11 +455,11 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
 
     if (warp == kTConsumers) {
         // ---------------- producer (whole warp; lane 0 owns the barriers)
-        // Down: the weights of the first kTStages stages are requested before
-        // the previous kernel (which writes h) has finished; their activation
-        // copies only after it has.
+        // Down and dense: the weights of the first kTStages stages are requested
+        // before the previous kernel (which writes the activation units) has
+        // finished; their activation copies only after it has.
         const int total = (int)(u1 - u0);
-        const int pre = a.mode == 1 ? min(total, kTStages) : 0;
+        const int pre = a.mode != 0 ? min(total, kTStages) : 0;
         const int item0 = (int)(u0 / ns), kb_0 = (int)(u0 - (long long)item0 * ns);
         PassCursor pc;
         if (total > 0) pc.seek(a, nu, item0 / tiles);
@@ -488,7 +510,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
                 pc.to(a, pi);
                 cur_pi = pi;
                 if (lane < pc.ntok) {
-                    const int p = a.list[pc.beg + lane];
+                    const int p = a.mode == 2 ? pc.beg + lane : a.list[pc.beg + lane];
                     myrow = a.mode == 0 ? p / a.k : p;
                 }
             }
@@ -532,7 +554,9 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
             if (fresh) {
                 pc.to(a, pi);
                 consumers_sync();  // the previous epilogue is done with sh.pairs
-                if (threadIdx.x < pc.ntok) sh.pairs[threadIdx.x] = a.list[pc.beg + threadIdx.x];
+                if (threadIdx.x < pc.ntok)
+                    sh.pairs[threadIdx.x] =
+                        a.mode == 2 ? pc.beg + threadIdx.x : a.list[pc.beg + threadIdx.x];
                 cur_pi = pi;
             }
             const bool whole = kb0 == 0 && kb1 == ns;
@@ -572,6 +596,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool make_maps(TmaArgs &a, const uint8_t *wq, const float *ws, int E, int rows, int K) {
+    return encode_weight_maps(&a.wmap, &a.smap, wq, ws, E, rows, K);
+}
+
+}  // namespace
+
+bool encode_weight_maps(CUtensorMap *wmap, CUtensorMap *smap, const uint8_t *wq, const float *ws,
+                        int E, int rows, int K) {
     auto enc = encode_fn();
     if (!enc) return false;
     const int G = K / kGroup;
@@ -580,7 +611,7 @@ bool make_maps(TmaArgs &a, const uint8_t *wq, const float *ws, int E, int rows, 
         cuuint64_t strides[2] = {(cuuint64_t)K / 2, (cuuint64_t)rows * (K / 2)};
         cuuint32_t box[3] = {128, 128, 1};
         cuuint32_t es[3] = {1, 1, 1};
-        if (enc(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(wq), dims, strides,
+        if (enc(wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(wq), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return false;
@@ -590,15 +621,13 @@ bool make_maps(TmaArgs &a, const uint8_t *wq, const float *ws, int E, int rows, 
         cuuint64_t strides[2] = {(cuuint64_t)G * 4, (cuuint64_t)rows * G * 4};
         cuuint32_t box[3] = {4, 128, 1};
         cuuint32_t es[3] = {1, 1, 1};
-        if (enc(&a.smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ws), dims, strides,
+        if (enc(smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ws), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return false;
     }
     return true;
 }
-
-}  // namespace
 
 bool tma_moe_supported(const MoeDims &m) {
     // tensor maps need 16-byte aligned bases and 16-byte strides (scale rows of
@@ -638,6 +667,34 @@ cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const 
         ok = make_maps(a, m.dn_q, m.dn_s, m.E, m.H, m.I);
     }
     if (!ok) return cudaErrorInvalidValue;
+    cudaError_t e = set_smem(k_moe_tma, kTSmem);
+    if (e != cudaSuccess) return e;
+    const int grid = std::min(kSkMaxCtas, sm_count() * max_ctas_per_sm(k_moe_tma, kTThreads, kTSmem));
+    return launch(k_moe_tma, dim3(grid), dim3(kTThreads), (size_t)kTSmem, st, true, a);
+}
+
+bool tma_dense_supported(const uint8_t *wq, const float *scales, int N, int K) {
+    auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    return encode_fn() != nullptr && N % kTDnRows == 0 && (K / kGroup) % 4 == 0 && a16(wq) &&
+           a16(scales);
+}
+
+cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int K, int S,
+                             const void *cells, const float *cfac, float *y, int32_t *status,
+                             int32_t *cnt, float *part, cudaStream_t st) {
+    TmaArgs a;
+    memset(&a, 0, sizeof(a));
+    a.mode = 2;
+    a.H = N;
+    a.S = S;
+    a.G = K / kGroup;
+    a.cells = static_cast<const uint4 *>(cells);
+    a.cfac = cfac;
+    a.y = y;
+    a.status = status;
+    a.cnt = cnt;
+    a.part = part;
+    if (!make_maps(a, wq, scales, 1, N, K)) return cudaErrorInvalidValue;
     cudaError_t e = set_smem(k_moe_tma, kTSmem);
     if (e != cudaSuccess) return e;
     const int grid = std::min(kSkMaxCtas, sm_count() * max_ctas_per_sm(k_moe_tma, kTThreads, kTSmem));

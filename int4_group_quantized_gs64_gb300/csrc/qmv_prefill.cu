@@ -36,6 +36,8 @@
 
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 namespace qmv {
 
 namespace {
@@ -352,12 +354,435 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(PfArgs a) {
     if (warp == 0) tc05::tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------------------ pipelined variant
+//
+// Shapes with H/64 and I/64 multiples of 4 and 16-byte aligned pools run a
+// warp-specialized version of the same computation. One CTA per SM, 10 warps,
+// a 3-slot ring of stages; a stage is 256 weight rows x 4 groups of one item:
+//   * producer warp: two 3-D tensor-map loads of the packed weights (128 rows
+//     x 128 bytes, 128-byte swizzle) and two of their scales, and the B tile
+//     of the 4 groups (the pass's token rows, bf16, 128-byte swizzled
+//     K-major, up to 64 rows per group) by cp.async; it marks a stage full
+//     after its own copies of it have landed and a proxy fence;
+//   * 8 dequant warps, thread = weight row = TMEM lane: per group, dequantize
+//     to bf16 with the scale folded in and store to that group's A slot in
+//     tensor memory, then signal the group; at the end of an item, read the
+//     accumulators back and write h (bf16) or y (fp32);
+//   * MMA warp: one thread issues per group 2 row tiles x 4 MMAs (M 128, N =
+//     tokens rounded up to 16, K 16) into one accumulator per tile that runs
+//     over the whole item, and commits them to the group's A-slot barrier;
+//     after a stage's last group it commits to the slot's empty barrier, and
+//     after an item's last stage to the accumulator barrier.
+// Tensor memory: A 4 groups x 2 tiles x 32 columns, D 2 tiles x 64 columns.
+// Every wait is bounded; a wait that runs out raises a CTA-wide abort flag,
+// after which nothing waits any more; copies and MMAs in flight are drained
+// (bounded) before the tensor memory is released, and bit 1 of the status
+// word is set.
+
+constexpr int kPqDq = 8;                             // dequant / epilogue warps
+constexpr int kPqProd = kPqDq;
+constexpr int kPqMma = kPqDq + 1;
+constexpr int kPqThreads = 32 * (kPqDq + 2);
+constexpr int kPqStages = 3;
+constexpr int kPqOffS = 256 * 128;                   // scales [256][4] f32
+constexpr int kPqOffB = kPqOffS + 256 * 16;          // B: 4 groups x 64 rows x 128 B
+constexpr int kPqBGroup = kPfMaxN * 128;
+constexpr int kPqStage = kPqOffB + 4 * kPqBGroup;    // 68 KB
+constexpr int kPqSmem = kPqStages * kPqStage + 1024;
+constexpr uint32_t kPqTmaBytes = 256 * 128 + 256 * 16;
+constexpr uint32_t kPqTmemCols = 512;
+constexpr uint32_t kPqD = 256;                       // first accumulator column
+constexpr uint32_t kPqWait = 1u << 24;
+
+static_assert(kPqStage % 1024 == 0, "stages must stay 1024-aligned for the 128B swizzle");
+static_assert(kPqBGroup % 1024 == 0, "B tiles must stay 1024-aligned");
+
+struct PqArgs {
+    CUtensorMap wmap, smap;
+    int mode;            // 0: gate_up, 1: down
+    int K, G, tiles, k, I, H;
+    const int32_t *offsets, *list, *uexp, *n_used, *pass_ofs;
+    const uint16_t *b;   // B rows, bf16: x [T][H] or h [P][I]
+    uint16_t *h;         // gate_up output [P][I] bf16
+    float *y;            // down output [P][H] fp32
+    int32_t *status;
+};
+
+struct PqShared {
+    uint64_t full[kPqStages], empty[kPqStages];
+    uint64_t afull[4], afree[4];
+    uint64_t dfull, dfree;
+    uint32_t tmem;
+    int abort;
+};
+
+__device__ __forceinline__ bool pq_try(uint64_t *mbar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(tc05::smem_addr(mbar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait that gives up at once when another role has aborted; running
+// out of polls raises the abort flag.
+__device__ __forceinline__ bool pq_wait(PqShared &sh, uint64_t *mbar, uint32_t parity) {
+    volatile int *ab = &sh.abort;
+    for (uint32_t i = 0; i < kPqWait; ++i) {
+        if (pq_try(mbar, parity)) return true;
+        if ((i & 15u) == 15u && *ab) return false;
+    }
+    *ab = 1;
+    return false;
+}
+
+// Bounded wait that ignores the abort flag (draining work in flight).
+__device__ __forceinline__ void pq_drain(uint64_t *mbar, uint32_t parity) {
+    for (uint32_t i = 0; i < kPqWait; ++i)
+        if (pq_try(mbar, parity)) return;
+}
+
+__device__ __forceinline__ void pq_expect_tx(uint64_t *mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     tc05::smem_addr(mbar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void pq_arrive(uint64_t *mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc05::smem_addr(mbar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void pq_tma3(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                        uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(mbar)
+        : "memory");
+}
+
+// Walks the passes (up to kPfMaxN pairs of one expert) in order.
+struct PqCursor {
+    int lo, pi, e, beg, ntok;
+    __device__ __forceinline__ void seek(const PqArgs &a, int nu, int p) {
+        int l = 0, hgh = nu - 1;
+        while (l < hgh) {
+            const int mid = (l + hgh + 1) >> 1;
+            if (a.pass_ofs[mid] <= p) l = mid; else hgh = mid - 1;
+        }
+        lo = l;
+        pi = -1;
+        to(a, p);
+    }
+    __device__ __forceinline__ void to(const PqArgs &a, int p) {
+        if (p == pi) return;
+        while (a.pass_ofs[lo + 1] <= p) ++lo;
+        pi = p;
+        e = a.uexp[lo];
+        const int pass = p - a.pass_ofs[lo];
+        const int b = a.offsets[e], cnt = a.offsets[e + 1] - b;
+        beg = b + pass * kPfMaxN;
+        ntok = min(kPfMaxN, cnt - pass * kPfMaxN);
+    }
+};
+
+__global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_constant__ PqArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ PqShared sh;
+    // 1024-byte alignment by an offset on the shared array itself (keeps LDS)
+    uint8_t *ring = smem_raw + ((1024u - (tc05::smem_addr(smem_raw) & 1023u)) & 1023u);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (warp == 0) tc05::tmem_alloc(&sh.tmem, kPqTmemCols);
+    if (threadIdx.x == 32) {
+        for (int s = 0; s < kPqStages; ++s) {
+            tc05::mbar_init(&sh.full[s], 2);
+            tc05::mbar_init(&sh.empty[s], 1);
+        }
+        for (int g = 0; g < 4; ++g) {
+            tc05::mbar_init(&sh.afull[g], kPqDq);
+            tc05::mbar_init(&sh.afree[g], 1);
+        }
+        tc05::mbar_init(&sh.dfull, 1);
+        tc05::mbar_init(&sh.dfree, kPqDq);
+        sh.abort = 0;
+        tc05::fence_mbar_init();
+    }
+    tc05::fence_before_sync();
+    __syncthreads();
+    tc05::fence_after_sync();
+    const uint32_t tmem = sh.tmem;
+
+    // gate_up reads the grouping and x after the previous kernel; down's
+    // grouping finished before the previous kernel started, so its producer
+    // requests the first weight stages before waiting for h (below).
+    if (a.mode == 0 || warp != kPqProd) pdl_wait();
+    pdl_trigger();
+
+    const int nu = *a.n_used;
+    const int total_items = nu > 0 ? a.pass_ofs[nu] * a.tiles : 0;
+    const int i0 = (int)((long long)blockIdx.x * total_items / gridDim.x);
+    const int i1 = (int)((long long)(blockIdx.x + 1) * total_items / gridDim.x);
+    const int ns = a.G / 4;
+    const int total = (i1 - i0) * ns;  // stages of this CTA
+
+    if (warp == kPqProd) {
+        // ---------------- producer
+        const int pre = a.mode == 1 ? min(total, kPqStages) : 0;
+        PqCursor pc;
+        if (total > 0) pc.seek(a, nu, i0 / a.tiles);
+        auto weights = [&](int slot, int item, int kb, int e) {
+            const int tile = item % a.tiles;
+            const int rowA = a.mode == 0 ? tile * 128 : tile * 256;
+            const int rowB = a.mode == 0 ? a.I + tile * 128 : tile * 256 + 128;
+            const uint32_t base = tc05::smem_addr(ring + slot * kPqStage);
+            const uint32_t fb = tc05::smem_addr(&sh.full[slot]);
+            pq_expect_tx(&sh.full[slot], kPqTmaBytes);
+            pq_tma3(base, &a.wmap, kb * 128, rowA, e, fb);
+            pq_tma3(base + 128 * 128, &a.wmap, kb * 128, rowB, e, fb);
+            pq_tma3(base + kPqOffS, &a.smap, kb * 4, rowA, e, fb);
+            pq_tma3(base + kPqOffS + 128 * 16, &a.smap, kb * 4, rowB, e, fb);
+        };
+        if (pre > 0) {
+            PqCursor c = pc;
+            for (int j = 0; j < pre; ++j) {
+                const int item = i0 + j / ns;
+                c.to(a, item / a.tiles);
+                if (lane == 0) weights(j, item, j % ns, c.e);
+            }
+            pdl_wait();  // h comes from the previous kernel
+        }
+        int cur_pi = -1, r_lo = 0, r_hi = 0, npad = 16;
+        int issued = 0, signaled = 0;  // stages copied / marked full
+        const uint32_t ring_s = tc05::smem_addr(ring);
+        for (int j = 0; j < total; ++j) {
+            const int slot = j % kPqStages;
+            const int item = i0 + j / ns, kb = j % ns;
+            const int pi = item / a.tiles;
+            if (pi != cur_pi) {
+                pc.to(a, pi);
+                cur_pi = pi;
+                npad = (pc.ntok + 15) & ~15;
+                const int t0 = min(lane, pc.ntok - 1), t1 = min(lane + 32, pc.ntok - 1);
+                const int p0 = a.list[pc.beg + t0], p1 = a.list[pc.beg + t1];
+                r_lo = a.mode == 0 ? p0 / a.k : p0;
+                r_hi = a.mode == 0 ? p1 / a.k : p1;
+            }
+            // the previous stage's B copies have landed: fence them into the
+            // async proxy (the MMA reads B) and mark that stage's B ready
+            if (j > 0) {
+                asm volatile("cp.async.wait_all;" ::: "memory");
+                tc05::fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) pq_arrive(&sh.full[(j - 1) % kPqStages]);
+                signaled = j;
+            }
+            if (j >= kPqStages) {
+                int done = 1;
+                if (lane == 0)
+                    done = pq_wait(sh, &sh.empty[slot], (uint32_t)(((j / kPqStages) - 1) & 1));
+                if (!__shfl_sync(0xffffffffu, done, 0)) break;
+            }
+            if (j >= pre && lane == 0) weights(slot, item, kb, pc.e);
+            // B: token t, group lane / 8, 16-byte column lane % 8
+            const int g = lane >> 3, ch = lane & 7;
+            const uint32_t dst0 = ring_s + slot * kPqStage + kPqOffB + g * kPqBGroup;
+            for (int t = 0; t < npad; ++t) {
+                const int row = __shfl_sync(0xffffffffu, t < 32 ? r_lo : r_hi, t & 31);
+                const uint16_t *src = a.b + (size_t)row * a.K + (size_t)(4 * kb + g) * 64 + ch * 8;
+                cp_async16_s(dst0 + t * 128 + ((ch ^ (t & 7)) << 4), src);
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            issued = j + 1;
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (signaled < issued) {
+            tc05::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) pq_arrive(&sh.full[(issued - 1) % kPqStages]);
+        }
+        if (lane == 0) {
+            // drain: every tensor copy issued must land before the CTA may exit
+            for (int j = (issued > kPqStages ? issued - kPqStages : 0); j < issued; ++j)
+                pq_drain(&sh.full[j % kPqStages], (uint32_t)((j / kPqStages) & 1));
+        }
+    } else if (warp == kPqMma) {
+        // ---------------- MMA issue (one thread)
+        if (lane == 0) {
+            PqCursor pc;
+            if (total > 0) pc.seek(a, nu, i0 / a.tiles);
+            int last_bar = -1;  // 0: afree, 1: empty, 2: dfull of the last commit
+            int last_j = -1, last_g = 0, items_done = 0;
+            bool ok = true;
+            for (int j = 0; j < total && ok; ++j) {
+                const int slot = j % kPqStages;
+                const int item = i0 + j / ns, kb = j % ns;
+                pc.to(a, item / a.tiles);
+                const uint32_t idesc = tc05::idesc_bf16_f32(128, (pc.ntok + 15) & ~15);
+                ok = pq_wait(sh, &sh.full[slot], (uint32_t)((j / kPqStages) & 1));
+                if (ok && kb == 0 && items_done > 0)
+                    ok = pq_wait(sh, &sh.dfree, (uint32_t)((items_done - 1) & 1));
+                const uint32_t sB = tc05::smem_addr(ring + slot * kPqStage + kPqOffB);
+                for (int g = 0; g < 4 && ok; ++g) {
+                    ok = pq_wait(sh, &sh.afull[g], (uint32_t)(j & 1));
+                    if (!ok) break;
+                    tc05::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+                        for (int tt = 0; tt < 2; ++tt) {
+                            tc05::mma_ts(tmem + kPqD + tt * 64, tmem + g * 64 + tt * 32 + kk * 8,
+                                         tc05::sdesc_sw128(sB + g * kPqBGroup + kk * 32), idesc,
+                                         (kb > 0 || g > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
+                    tc05::mma_commit(&sh.afree[g]);
+                    last_bar = 0; last_j = j; last_g = g;
+                }
+                if (!ok) break;
+                tc05::mma_commit(&sh.empty[slot]);
+                last_bar = 1;
+                if (kb == ns - 1) {
+                    tc05::mma_commit(&sh.dfull);
+                    last_bar = 2;
+                    ++items_done;
+                }
+            }
+            // the MMAs still in flight must finish before the tensor memory is freed
+            if (last_bar == 0) pq_drain(&sh.afree[last_g], (uint32_t)(last_j & 1));
+            else if (last_bar == 1) pq_drain(&sh.empty[last_j % kPqStages], (uint32_t)((last_j / kPqStages) & 1));
+            else if (last_bar == 2) pq_drain(&sh.dfull, (uint32_t)((items_done - 1) & 1));
+        }
+    } else {
+        // ---------------- dequant / epilogue warps
+        const int tt = warp >> 2, q = warp & 3;
+        const int r = tt * 128 + q * 32 + lane;     // stage row; TMEM lane q*32 + lane
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        PqCursor pc;
+        if (total > 0) pc.seek(a, nu, i0 / a.tiles);
+        int items_done = 0;
+        for (int j = 0; j < total; ++j) {
+            const int slot = j % kPqStages;
+            const int item = i0 + j / ns, kb = j % ns;
+            pq_wait(sh, &sh.full[slot], (uint32_t)((j / kPqStages) & 1));
+            const uint8_t *sp = ring + slot * kPqStage;
+            const uint8_t *wr = sp + r * 128;
+            const int x7 = r & 7;
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(wr + (((2 * g) ^ x7) << 4));
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(wr + (((2 * g + 1) ^ x7) << 4));
+                const float sc = *reinterpret_cast<const float *>(sp + kPqOffS + r * 16 + g * 4);
+                uint32_t A[32];
+                pf_dequant(w0, w1, sc, A);
+                if (j > 0) {
+                    // MMA(j - 1) of this group done: its A slot may be overwritten
+                    pq_wait(sh, &sh.afree[g], (uint32_t)((j - 1) & 1));
+                    tc05::fence_after_sync();
+                }
+                tc05::tmem_st32(tmem + lane_base + (uint32_t)(g * 64 + tt * 32), A);
+                tc05::tmem_wait_st();
+                tc05::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) pq_arrive(&sh.afull[g]);
+            }
+            if (kb == ns - 1) {
+                // item done: wait for its last MMAs, then read the accumulators
+                pq_wait(sh, &sh.dfull, (uint32_t)(items_done & 1));
+                tc05::fence_after_sync();
+                pc.to(a, item / a.tiles);
+                const int tile = item % a.tiles;
+                const int ntok = pc.ntok, nblk = ((ntok + 15) & ~15) / 16;
+                const int r128 = q * 32 + lane;
+                if (a.mode == 0) {
+                    // gate_up: tile tt takes column blocks tt, tt + 2, ...
+                    for (int blk = tt; blk < nblk; blk += 2) {
+                        uint32_t gv[16], uv[16];
+                        tc05::tmem_ld16(tmem + lane_base + kPqD + blk * 16, gv);
+                        tc05::tmem_ld16(tmem + lane_base + kPqD + 64 + blk * 16, uv);
+                        tc05::tmem_wait_ld();
+                        const int j0 = tile * 128 + r128;
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const int n = blk * 16 + c;
+                            if (n < ntok) {
+                                const float g0 = __uint_as_float(gv[c]), u0 = __uint_as_float(uv[c]);
+                                const float hv = g0 / (1.0f + expf(-g0)) * u0;
+                                const int p = a.list[pc.beg + n];
+                                const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                                a.h[(size_t)p * a.I + j0] = *reinterpret_cast<const uint16_t *>(&hb);
+                            }
+                        }
+                    }
+                } else {
+                    const int row = tile * 256 + tt * 128 + r128;
+                    for (int blk = 0; blk < nblk; ++blk) {
+                        uint32_t d[16];
+                        tc05::tmem_ld16(tmem + lane_base + kPqD + tt * 64 + blk * 16, d);
+                        tc05::tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const int n = blk * 16 + c;
+                            if (n < ntok) {
+                                const int p = a.list[pc.beg + n];
+                                a.y[(size_t)p * a.H + row] = __uint_as_float(d[c]);
+                            }
+                        }
+                    }
+                }
+                tc05::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) pq_arrive(&sh.dfree);
+                ++items_done;
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && sh.abort) atomicOr(a.status, 2);
+    tc05::fence_after_sync();
+    if (warp == 0) tc05::tmem_dealloc(tmem, kPqTmemCols);
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(const MoeDims &m, int mode, const uint16_t *b, int k,
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                            const int32_t *n_used, const int32_t *pass_ofs, uint16_t *h, float *y,
                            int32_t *status, cudaStream_t st) {
+    if (tma_moe_supported(m)) {
+        PqArgs q;
+        memset(&q, 0, sizeof(q));
+        q.mode = mode;
+        q.k = k;
+        q.I = m.I;
+        q.H = m.H;
+        q.offsets = offsets; q.list = list; q.uexp = uexp; q.n_used = n_used; q.pass_ofs = pass_ofs;
+        q.b = b;
+        q.h = h;
+        q.y = y;
+        q.status = status;
+        bool ok;
+        if (mode == 0) {
+            q.K = m.H;
+            q.tiles = m.I / 128;
+            ok = encode_weight_maps(&q.wmap, &q.smap, m.gu_q, m.gu_s, m.E, 2 * m.I, m.H);
+        } else {
+            q.K = m.I;
+            q.tiles = m.H / 256;
+            ok = encode_weight_maps(&q.wmap, &q.smap, m.dn_q, m.dn_s, m.E, m.H, m.I);
+        }
+        q.G = q.K / kGroup;
+        if (!ok) return cudaErrorInvalidValue;
+        cudaError_t e = set_smem(k_prefill_tma, kPqSmem);
+        if (e != cudaSuccess) return e;
+        const int grid = sm_count() * max_ctas_per_sm(k_prefill_tma, kPqThreads, kPqSmem);
+        return launch(k_prefill_tma, dim3(grid), dim3(kPqThreads), (size_t)kPqSmem, st, true, q);
+    }
     PfArgs a{};
     a.k = k;
     a.offsets = offsets; a.list = list; a.uexp = uexp; a.n_used = n_used; a.pass_ofs = pass_ofs;

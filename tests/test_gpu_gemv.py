@@ -64,6 +64,28 @@ def test_int4_shapes(N, K, S):
     assert norm_err(y, ref, den) <= TOL_FP32
 
 
+# Shapes of the tensor-map kernel (N a multiple of 256, K/64 a multiple of 4):
+# one tile and one stage, several passes of 8 tokens with a ragged last pass,
+# and long rows whose stages are split between CTAs.
+TMA_SHAPES = [(256, 256, 1), (512, 1024, 8), (768, 4096, 9), (2048, 2048, 17), (256, 16384, 2),
+              (14336, 4096, 8)]
+
+
+@pytest.mark.parametrize("N,K,S", TMA_SHAPES)
+def test_int4_tma_shapes(N, K, S):
+    rng = np.random.default_rng(N * 131 + K + S)
+    wq = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sc = (np.abs(rng.normal(0, 0.02, size=(N, K // 64))) + 1e-4).astype(np.float32)
+    x = rng.normal(size=(S, K)).astype(np.float32)
+    ws = torch.full((q.qmv_gemv_workspace_bytes(K, S),), 0xFF, dtype=torch.uint8, device="cuda")
+    for _ in range(2):  # the second call reuses the workspace left by the first
+        y = q.qmv_int4_gs(dev(wq), dev(sc), dev(x), ws=ws)
+        torch.cuda.synchronize()
+        assert int(ws[:4].view(torch.int32).cpu()[0]) == 0  # status word: no wait timed out
+        ref, den = oracle.qmv_int4_gs(wq, sc, x, 64, with_den=True)
+        assert norm_err(y.cpu().numpy(), ref, den) <= TOL_FP32
+
+
 @pytest.mark.parametrize("N,K,S", SHAPES)
 def test_int8_shapes(N, K, S):
     rng = np.random.default_rng(N * 31 + K + S)

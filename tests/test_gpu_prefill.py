@@ -44,7 +44,8 @@ def rand_experts(rng, E, H, I):
 
 @pytest.mark.parametrize("T,k,E,H,I", [(5, 2, 4, 256, 256), (40, 2, 4, 256, 256),
                                        (200, 2, 3, 128, 384), (70, 1, 1, 192, 128),
-                                       (64, 8, 16, 512, 256)])
+                                       (64, 8, 16, 512, 256), (300, 2, 4, 256, 512),
+                                       (33, 4, 8, 1024, 256)])
 def test_prefill_shapes(T, k, E, H, I):
     """Under 16 tokens per expert (padding), several passes of 64, one expert."""
     rng = np.random.default_rng(T * 7 + k * 3 + E)
