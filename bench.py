@@ -279,6 +279,29 @@ def run_profile_dense(args):
     return 0
 
 
+def run_profile_prefill(args):
+    """ncu case for the prefill kernels: 512 tokens (H 6144, I 2048, top-8) over
+    a pool of `--profile-prefill` experts, `--steps` calls, no timing."""
+    import torch
+    import datagen
+    import int4_group_quantized_gs64_gb300 as q
+    q.build()
+    dev = torch.device("cuda")
+    E, H, I, T, k = args.profile_prefill, W3["H"], W3["I"], 512, 8
+    m = q.MoeInt4Weights.from_numpy(datagen.moe_weights(E, H, I), dev)
+    xb, lg = datagen.moe_inputs(T, E, H, xdtype="bf16")
+    xbd = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    ids, w = q.moe_route_topk(torch.from_numpy(lg).to(dev), k)
+    ws = torch.empty(q.moe_prefill_workspace_bytes(m, T, k), dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    for _ in range(args.steps):
+        q.moe_expert_ffn_int4_prefill(m, xbd, ids, w, out=out, ws=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": f"MoE prefill H{H} I{I} top{k}, {T} tokens, {E}-expert pool",
+                      "steps": args.steps, "launches_per_step": 5}))
+    return 0
+
+
 # ------------------------------------------------------------------ ranks
 
 def max_over_ranks(t_step: float, device=None) -> float:
@@ -549,7 +572,11 @@ def main():
                     help="run the small ncu case with this many experts instead of the bench")
     ap.add_argument("--profile-dense", action="store_true",
                     help="run the small ncu case of the dense GEMV instead of the bench")
+    ap.add_argument("--profile-prefill", type=int, default=0,
+                    help="run the small ncu case of the prefill with this many experts")
     args = ap.parse_args()
+    if args.profile_prefill > 0:
+        return run_profile_prefill(args)
     if args.profile_experts > 0:
         return run_profile_case(args)
     if args.profile_dense:

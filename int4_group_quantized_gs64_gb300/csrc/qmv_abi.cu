@@ -322,12 +322,27 @@ int moe_expert_ffn_int4_prefill(const qmv_moe_int4 *m, const uint16_t *x_bf16, i
         e = qmv::launch_group_split(ids, T, k, m->E, offsets, list, uexp, n_used, pass_ofs, status,
                                     nullptr, m->H, nullptr, nullptr, st,
                                     qmv::prefill_pass_tokens());
-    if (e == cudaSuccess)
-        e = qmv::launch_prefill(d, 0, x_bf16, k, offsets, list, uexp, n_used, pass_ofs, h, y,
-                                status, st);
-    if (e == cudaSuccess)
-        e = qmv::launch_prefill(d, 1, h, k, offsets, list, uexp, n_used, pass_ofs, h, y, status,
-                                st);
+    if (qmv::tma_moe_supported(d)) {
+        // tensor-map path: B operands packed per pass (x by a packing kernel,
+        // h by the gate_up kernel itself)
+        uint16_t *xp = at<uint16_t>(ws, L.xp), *hp = at<uint16_t>(ws, L.hp);
+        if (e == cudaSuccess)
+            e = qmv::launch_pack_x(x_bf16, m->H, k, offsets, list, uexp, n_used, pass_ofs, xp,
+                                   L.pmax, st);
+        if (e == cudaSuccess)
+            e = qmv::launch_prefill(d, 0, xp, k, offsets, list, uexp, n_used, pass_ofs, hp, y,
+                                    status, st);
+        if (e == cudaSuccess)
+            e = qmv::launch_prefill(d, 1, hp, k, offsets, list, uexp, n_used, pass_ofs, hp, y,
+                                    status, st);
+    } else {
+        if (e == cudaSuccess)
+            e = qmv::launch_prefill(d, 0, x_bf16, k, offsets, list, uexp, n_used, pass_ofs, h, y,
+                                    status, st);
+        if (e == cudaSuccess)
+            e = qmv::launch_prefill(d, 1, h, k, offsets, list, uexp, n_used, pass_ofs, h, y,
+                                    status, st);
+    }
     if (e == cudaSuccess) e = qmv::launch_combine(y, ids, w, T, k, m->E, m->H, out, st, true);
     return from_cuda(e);
 }

@@ -64,6 +64,13 @@ cudaError_t launch_prefill(const MoeDims &m, int mode, const uint16_t *b, int k,
                            const int32_t *n_used, const int32_t *pass_ofs, uint16_t *h, float *y,
                            int32_t *status, cudaStream_t st);
 int prefill_pass_tokens();
+// Tensor-map prefill (tma_moe_supported shapes): B operands packed per pass,
+// [pass][K/64][64 rows][64 bf16], 128-byte swizzled, rows beyond the pass's
+// tokens zero. launch_pack_x packs x; the gate_up launch writes h packed
+// (argument h) and down reads it (argument b).
+cudaError_t launch_pack_x(const uint16_t *x, int H, int k, const int32_t *offsets,
+                          const int32_t *list, const int32_t *uexp, const int32_t *n_used,
+                          const int32_t *pass_ofs, uint16_t *xp, int pmax, cudaStream_t st);
 
 // TMA-fed decode kernels (qmv_moe_tma.cu): mode 0 = gate+up (cells = x units,
 // writes h, h units, h factors), mode 1 = down (cells = h units, writes y).
@@ -98,7 +105,8 @@ struct MoeWorkspace {
 MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k);
 
 struct PrefillWorkspace {
-    size_t status, offsets, list, uexp, n_used, pass_ofs, h, y, total;
+    size_t status, offsets, list, uexp, n_used, pass_ofs, h, y, xp, hp, total;
+    int pmax;  // passes, at most
 };
 PrefillWorkspace prefill_ws_layout(int E, int H, int I, int T, int k);
 

@@ -14,6 +14,8 @@
 #include <float.h>
 #include <limits.h>
 
+#include <algorithm>
+
 #include "qmv_internal.h"
 #include "qmv_launch.cuh"
 #include "qmv_rows.cuh"
@@ -620,6 +622,12 @@ PrefillWorkspace prefill_ws_layout(int E, int H, int I, int T, int k) {
     L.pass_ofs = o; o = align256(o + 4 * (size_t)(E + 1));
     L.h = o; o = align256(o + 2 * P * I);
     L.y = o; o = align256(o + 4 * P * H);
+    // packed B operands of the tensor-map path: a pass holds up to 64 pairs of
+    // one expert, so there are at most P / 64 + min(E, P) passes
+    const size_t pm = std::min(P, (P + 63) / 64 + std::min((size_t)E, P));
+    L.pmax = (int)pm;
+    L.xp = o; o = align256(o + pm * (size_t)(H / 64) * 8192);
+    L.hp = o; o = align256(o + pm * (size_t)(I / 64) * 8192);
     L.total = o;
     return L;
 }

@@ -358,43 +358,55 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(PfArgs a) {
 //
 // Shapes with H/64 and I/64 multiples of 4 and 16-byte aligned pools run a
 // warp-specialized version of the same computation. One CTA per SM, 10 warps,
-// a 3-slot ring of stages; a stage is 256 weight rows x 4 groups of one item:
-//   * producer warp: two 3-D tensor-map loads of the packed weights (128 rows
-//     x 128 bytes, 128-byte swizzle) and two of their scales, and the B tile
-//     of the 4 groups (the pass's token rows, bf16, 128-byte swizzled
-//     K-major, up to 64 rows per group) by cp.async; it marks a stage full
-//     after its own copies of it have landed and a proxy fence;
-//   * 8 dequant warps, thread = weight row = TMEM lane: per group, dequantize
-//     to bf16 with the scale folded in and store to that group's A slot in
-//     tensor memory, then signal the group; at the end of an item, read the
-//     accumulators back and write h (bf16) or y (fp32);
-//   * MMA warp: one thread issues per group 2 row tiles x 4 MMAs (M 128, N =
-//     tokens rounded up to 16, K 16) into one accumulator per tile that runs
-//     over the whole item, and commits them to the group's A-slot barrier;
-//     after a stage's last group it commits to the slot's empty barrier, and
-//     after an item's last stage to the accumulator barrier.
+// two rings of stages; a stage is 256 weight rows x 4 groups of one item:
+//   * weight producer warp: two 3-D tensor-map loads of the packed weights
+//     (128 rows x 128 bytes, 128-byte swizzle) and two of their scales per
+//     stage into a 4-slot ring that the dequant warps free as soon as they
+//     have read a stage, so weights stream up to 4 stages ahead;
+//   * B producer warp: the B tile of the 4 groups (the pass's token rows,
+//     bf16, 128-byte swizzled K-major, up to 64 rows per group) by cp.async
+//     into a 2-slot ring that the MMAs free; a stage's B is marked ready once
+//     its copies have landed, after a proxy fence;
+//   * 16 dequant warps, thread = weight row = TMEM lane, two warps per lane
+//     quarter: set 0 takes groups 0-1 of each stage, set 1 groups 2-3. Per
+//     group a thread dequantizes its row to bf16 with the scale folded in,
+//     stores it to that group's A slot in tensor memory and the warp signals
+//     the group; at the end of an item set 0 reads the accumulators back and
+//     writes h (bf16) or y (fp32);
+//   * 2 MMA warps, one per row tile: one thread of each issues 4 groups x 4
+//     MMAs (M 128, N = tokens rounded up to 16, K 16) per stage into its
+//     tile's accumulator, which runs over the whole item, and commits each
+//     group to that group's A-slot barrier of its tile; after a stage it
+//     commits to the slot's empty barrier, after an item to the accumulator
+//     barrier. (A thread that issues tcgen05.mma waits ~100 cycles per
+//     instruction for N up to 64, so one issuer per tile halves that time.)
 // Tensor memory: A 4 groups x 2 tiles x 32 columns, D 2 tiles x 64 columns.
 // Every wait is bounded; a wait that runs out raises a CTA-wide abort flag,
 // after which nothing waits any more; copies and MMAs in flight are drained
 // (bounded) before the tensor memory is released, and bit 1 of the status
 // word is set.
 
-constexpr int kPqDq = 8;                             // dequant / epilogue warps
-constexpr int kPqProd = kPqDq;
-constexpr int kPqMma = kPqDq + 1;
-constexpr int kPqThreads = 32 * (kPqDq + 2);
-constexpr int kPqStages = 3;
+constexpr int kPqDq = 16;                            // dequant warps (set 0: epilogue too)
+constexpr int kPqProdW = kPqDq;                      // weight producer warp
+constexpr int kPqProdB = kPqDq + 1;                  // B producer warp
+constexpr int kPqMma = kPqDq + 2;                    // first of 2 MMA warps
+constexpr int kPqMmaWarps = 2;
+constexpr int kPqThreads = 32 * (kPqDq + 2 + kPqMmaWarps);
+constexpr int kPqWStages = 4;                        // weight ring: freed after dequant
+constexpr int kPqBStages = 2;                        // B ring: freed by the MMAs
 constexpr int kPqOffS = 256 * 128;                   // scales [256][4] f32
-constexpr int kPqOffB = kPqOffS + 256 * 16;          // B: 4 groups x 64 rows x 128 B
-constexpr int kPqBGroup = kPfMaxN * 128;
-constexpr int kPqStage = kPqOffB + 4 * kPqBGroup;    // 68 KB
-constexpr int kPqSmem = kPqStages * kPqStage + 1024;
+constexpr int kPqWStage = kPqOffS + 256 * 16;        // 36 KB of weights and scales
+constexpr int kPqBGroup = kPfMaxN * 128;             // B: 64 rows x 128 B per group
+constexpr int kPqBStage = 4 * kPqBGroup;             // 32 KB
+constexpr int kPqOffBRing = kPqWStages * kPqWStage;
+constexpr int kPqSmem = kPqOffBRing + kPqBStages * kPqBStage + 1024;
 constexpr uint32_t kPqTmaBytes = 256 * 128 + 256 * 16;
 constexpr uint32_t kPqTmemCols = 512;
-constexpr uint32_t kPqD = 256;                       // first accumulator column
+constexpr uint32_t kPqD = 256;                       // accumulators: 2 tiles x 64 columns
 constexpr uint32_t kPqWait = 1u << 24;
 
-static_assert(kPqStage % 1024 == 0, "stages must stay 1024-aligned for the 128B swizzle");
+static_assert(kPqWStage % 1024 == 0 && kPqBStage % 1024 == 0,
+              "stages must stay 1024-aligned for the 128B swizzle");
 static_assert(kPqBGroup % 1024 == 0, "B tiles must stay 1024-aligned");
 
 struct PqArgs {
@@ -409,9 +421,11 @@ struct PqArgs {
 };
 
 struct PqShared {
-    uint64_t full[kPqStages], empty[kPqStages];
-    uint64_t afull[4], afree[4];
+    uint64_t wfull[kPqWStages], wempty[kPqWStages];
+    uint64_t bfull[kPqBStages], bempty[kPqBStages];
+    uint64_t afull[4], afree[4][2];
     uint64_t dfull, dfree;
+    uint64_t mdone[kPqMmaWarps];
     uint32_t tmem;
     int abort;
 };
@@ -466,6 +480,15 @@ __device__ __forceinline__ void pq_tma3(uint32_t dst, const CUtensorMap *map, in
         : "memory");
 }
 
+__device__ __forceinline__ void pq_bulk(uint32_t dst, const void *src, uint32_t bytes,
+                                        uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(mbar)
+        : "memory");
+}
+
 // Walks the passes (up to kPfMaxN pairs of one expert) in order.
 struct PqCursor {
     int lo, pi, e, beg, ntok;
@@ -500,16 +523,22 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
 
     if (warp == 0) tc05::tmem_alloc(&sh.tmem, kPqTmemCols);
     if (threadIdx.x == 32) {
-        for (int s = 0; s < kPqStages; ++s) {
-            tc05::mbar_init(&sh.full[s], 2);
-            tc05::mbar_init(&sh.empty[s], 1);
+        for (int s = 0; s < kPqWStages; ++s) {
+            tc05::mbar_init(&sh.wfull[s], 1);
+            tc05::mbar_init(&sh.wempty[s], kPqDq);
+        }
+        for (int s = 0; s < kPqBStages; ++s) {
+            tc05::mbar_init(&sh.bfull[s], 1);
+            tc05::mbar_init(&sh.bempty[s], kPqMmaWarps);
         }
         for (int g = 0; g < 4; ++g) {
-            tc05::mbar_init(&sh.afull[g], kPqDq);
-            tc05::mbar_init(&sh.afree[g], 1);
+            tc05::mbar_init(&sh.afull[g], kPqDq / 2);
+            tc05::mbar_init(&sh.afree[g][0], 1);
+            tc05::mbar_init(&sh.afree[g][1], 1);
         }
-        tc05::mbar_init(&sh.dfull, 1);
-        tc05::mbar_init(&sh.dfree, kPqDq);
+        tc05::mbar_init(&sh.dfull, kPqMmaWarps);
+        tc05::mbar_init(&sh.dfree, kPqDq / 2);
+        for (int m = 0; m < kPqMmaWarps; ++m) tc05::mbar_init(&sh.mdone[m], 1);
         sh.abort = 0;
         tc05::fence_mbar_init();
     }
@@ -518,10 +547,10 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
     tc05::fence_after_sync();
     const uint32_t tmem = sh.tmem;
 
-    // gate_up reads the grouping and x after the previous kernel; down's
-    // grouping finished before the previous kernel started, so its producer
-    // requests the first weight stages before waiting for h (below).
-    if (a.mode == 0 || warp != kPqProd) pdl_wait();
+    // The grouping finished before the previous kernel (the x packing, or
+    // gate_up) started, and the weights depend on no kernel, so the weight
+    // producer never waits; everything that reads packed B does.
+    if (warp != kPqProdW) pdl_wait();
     pdl_trigger();
 
     const int nu = *a.n_used;
@@ -531,150 +560,120 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
     const int ns = a.G / 4;
     const int total = (i1 - i0) * ns;  // stages of this CTA
 
-    if (warp == kPqProd) {
-        // ---------------- producer
-        const int pre = a.mode == 1 ? min(total, kPqStages) : 0;
-        PqCursor pc;
-        if (total > 0) pc.seek(a, nu, i0 / a.tiles);
-        auto weights = [&](int slot, int item, int kb, int e) {
-            const int tile = item % a.tiles;
-            const int rowA = a.mode == 0 ? tile * 128 : tile * 256;
-            const int rowB = a.mode == 0 ? a.I + tile * 128 : tile * 256 + 128;
-            const uint32_t base = tc05::smem_addr(ring + slot * kPqStage);
-            const uint32_t fb = tc05::smem_addr(&sh.full[slot]);
-            pq_expect_tx(&sh.full[slot], kPqTmaBytes);
-            pq_tma3(base, &a.wmap, kb * 128, rowA, e, fb);
-            pq_tma3(base + 128 * 128, &a.wmap, kb * 128, rowB, e, fb);
-            pq_tma3(base + kPqOffS, &a.smap, kb * 4, rowA, e, fb);
-            pq_tma3(base + kPqOffS + 128 * 16, &a.smap, kb * 4, rowB, e, fb);
-        };
-        if (pre > 0) {
-            PqCursor c = pc;
-            for (int j = 0; j < pre; ++j) {
-                const int item = i0 + j / ns;
-                c.to(a, item / a.tiles);
-                if (lane == 0) weights(j, item, j % ns, c.e);
-            }
-            pdl_wait();  // h comes from the previous kernel
-        }
-        int cur_pi = -1, r_lo = 0, r_hi = 0, npad = 16;
-        int issued = 0, signaled = 0;  // stages copied / marked full
-        const uint32_t ring_s = tc05::smem_addr(ring);
-        for (int j = 0; j < total; ++j) {
-            const int slot = j % kPqStages;
-            const int item = i0 + j / ns, kb = j % ns;
-            const int pi = item / a.tiles;
-            if (pi != cur_pi) {
-                pc.to(a, pi);
-                cur_pi = pi;
-                npad = (pc.ntok + 15) & ~15;
-                const int t0 = min(lane, pc.ntok - 1), t1 = min(lane + 32, pc.ntok - 1);
-                const int p0 = a.list[pc.beg + t0], p1 = a.list[pc.beg + t1];
-                r_lo = a.mode == 0 ? p0 / a.k : p0;
-                r_hi = a.mode == 0 ? p1 / a.k : p1;
-            }
-            // the previous stage's B copies have landed: fence them into the
-            // async proxy (the MMA reads B) and mark that stage's B ready
-            if (j > 0) {
-                asm volatile("cp.async.wait_all;" ::: "memory");
-                tc05::fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) pq_arrive(&sh.full[(j - 1) % kPqStages]);
-                signaled = j;
-            }
-            if (j >= kPqStages) {
-                int done = 1;
-                if (lane == 0)
-                    done = pq_wait(sh, &sh.empty[slot], (uint32_t)(((j / kPqStages) - 1) & 1));
-                if (!__shfl_sync(0xffffffffu, done, 0)) break;
-            }
-            if (j >= pre && lane == 0) weights(slot, item, kb, pc.e);
-            // B: token t, group lane / 8, 16-byte column lane % 8
-            const int g = lane >> 3, ch = lane & 7;
-            const uint32_t dst0 = ring_s + slot * kPqStage + kPqOffB + g * kPqBGroup;
-            for (int t = 0; t < npad; ++t) {
-                const int row = __shfl_sync(0xffffffffu, t < 32 ? r_lo : r_hi, t & 31);
-                const uint16_t *src = a.b + (size_t)row * a.K + (size_t)(4 * kb + g) * 64 + ch * 8;
-                cp_async16_s(dst0 + t * 128 + ((ch ^ (t & 7)) << 4), src);
-            }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-            issued = j + 1;
-        }
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        if (signaled < issued) {
-            tc05::fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) pq_arrive(&sh.full[(issued - 1) % kPqStages]);
-        }
-        if (lane == 0) {
-            // drain: every tensor copy issued must land before the CTA may exit
-            for (int j = (issued > kPqStages ? issued - kPqStages : 0); j < issued; ++j)
-                pq_drain(&sh.full[j % kPqStages], (uint32_t)((j / kPqStages) & 1));
-        }
-    } else if (warp == kPqMma) {
-        // ---------------- MMA issue (one thread)
+    if (warp == kPqProdW) {
+        // ---------------- weight producer (one thread)
         if (lane == 0) {
             PqCursor pc;
             if (total > 0) pc.seek(a, nu, i0 / a.tiles);
-            int last_bar = -1;  // 0: afree, 1: empty, 2: dfull of the last commit
-            int last_j = -1, last_g = 0, items_done = 0;
+            int issued = 0;
+            for (int j = 0; j < total; ++j) {
+                const int ws = j % kPqWStages;
+                if (j >= kPqWStages &&
+                    !pq_wait(sh, &sh.wempty[ws], (uint32_t)(((j / kPqWStages) - 1) & 1)))
+                    break;
+                const int item = i0 + j / ns, kb = j % ns;
+                pc.to(a, item / a.tiles);
+                const int tile = item % a.tiles;
+                const int rowA = a.mode == 0 ? tile * 128 : tile * 256;
+                const int rowB = a.mode == 0 ? a.I + tile * 128 : tile * 256 + 128;
+                const uint32_t base = tc05::smem_addr(ring + ws * kPqWStage);
+                const uint32_t fb = tc05::smem_addr(&sh.wfull[ws]);
+                pq_expect_tx(&sh.wfull[ws], kPqTmaBytes);
+                pq_tma3(base, &a.wmap, kb * 128, rowA, pc.e, fb);
+                pq_tma3(base + 128 * 128, &a.wmap, kb * 128, rowB, pc.e, fb);
+                pq_tma3(base + kPqOffS, &a.smap, kb * 4, rowA, pc.e, fb);
+                pq_tma3(base + kPqOffS + 128 * 16, &a.smap, kb * 4, rowB, pc.e, fb);
+                issued = j + 1;
+            }
+            // drain: every tensor copy issued must land before the CTA may exit
+            for (int j = (issued > kPqWStages ? issued - kPqWStages : 0); j < issued; ++j)
+                pq_drain(&sh.wfull[j % kPqWStages], (uint32_t)((j / kPqWStages) & 1));
+        }
+    } else if (warp == kPqProdB) {
+        // ---------------- B producer (one thread): per stage the 4 groups'
+        // packed B tiles of the pass, rows rounded up to 16, by bulk copy
+        if (lane == 0) {
+            PqCursor pc;
+            if (total > 0) pc.seek(a, nu, i0 / a.tiles);
+            int issued = 0;
+            for (int j = 0; j < total; ++j) {
+                const int bs = j % kPqBStages;
+                if (j >= kPqBStages &&
+                    !pq_wait(sh, &sh.bempty[bs], (uint32_t)(((j / kPqBStages) - 1) & 1)))
+                    break;
+                const int item = i0 + j / ns, kb = j % ns, pi = item / a.tiles;
+                pc.to(a, pi);
+                const uint32_t bytes = (uint32_t)(((pc.ntok + 15) & ~15) * 128);
+                const uint32_t dst = tc05::smem_addr(ring + kPqOffBRing + bs * kPqBStage);
+                const uint32_t fb = tc05::smem_addr(&sh.bfull[bs]);
+                pq_expect_tx(&sh.bfull[bs], 4 * bytes);
+                for (int g = 0; g < 4; ++g)
+                    pq_bulk(dst + g * kPqBGroup,
+                            a.b + ((size_t)pi * a.G + 4 * kb + g) * (kPqBGroup / 2), bytes, fb);
+                issued = j + 1;
+            }
+            // drain: every copy issued must land before the CTA may exit
+            for (int j = (issued > kPqBStages ? issued - kPqBStages : 0); j < issued; ++j)
+                pq_drain(&sh.bfull[j % kPqBStages], (uint32_t)((j / kPqBStages) & 1));
+        }
+    } else if (warp >= kPqMma) {
+        // ---------------- MMA issue: warp kPqMma + t issues row tile t
+        const int m = warp - kPqMma, t = m;
+        if (lane == 0) {
+            PqCursor pc;
+            if (total > 0) pc.seek(a, nu, i0 / a.tiles);
+            const uint32_t dacc = tmem + kPqD + (uint32_t)(t * 64);
+            int items_done = 0;
             bool ok = true;
             for (int j = 0; j < total && ok; ++j) {
-                const int slot = j % kPqStages;
+                const int bs = j % kPqBStages;
                 const int item = i0 + j / ns, kb = j % ns;
                 pc.to(a, item / a.tiles);
                 const uint32_t idesc = tc05::idesc_bf16_f32(128, (pc.ntok + 15) & ~15);
-                ok = pq_wait(sh, &sh.full[slot], (uint32_t)((j / kPqStages) & 1));
+                ok = pq_wait(sh, &sh.bfull[bs], (uint32_t)((j / kPqBStages) & 1));
                 if (ok && kb == 0 && items_done > 0)
                     ok = pq_wait(sh, &sh.dfree, (uint32_t)((items_done - 1) & 1));
-                const uint32_t sB = tc05::smem_addr(ring + slot * kPqStage + kPqOffB);
+                const uint32_t sB = tc05::smem_addr(ring + kPqOffBRing + bs * kPqBStage);
                 for (int g = 0; g < 4 && ok; ++g) {
                     ok = pq_wait(sh, &sh.afull[g], (uint32_t)(j & 1));
                     if (!ok) break;
                     tc05::fence_after_sync();
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-                        for (int tt = 0; tt < 2; ++tt) {
-                            tc05::mma_ts(tmem + kPqD + tt * 64, tmem + g * 64 + tt * 32 + kk * 8,
-                                         tc05::sdesc_sw128(sB + g * kPqBGroup + kk * 32), idesc,
-                                         (kb > 0 || g > 0 || kk > 0) ? 1u : 0u);
-                        }
-                    }
-                    tc05::mma_commit(&sh.afree[g]);
-                    last_bar = 0; last_j = j; last_g = g;
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc05::mma_ts(dacc, tmem + g * 64 + t * 32 + kk * 8,
+                                     tc05::sdesc_sw128(sB + g * kPqBGroup + kk * 32), idesc,
+                                     (kb > 0 || g > 0 || kk > 0) ? 1u : 0u);
+                    tc05::mma_commit(&sh.afree[g][t]);
                 }
                 if (!ok) break;
-                tc05::mma_commit(&sh.empty[slot]);
-                last_bar = 1;
+                tc05::mma_commit(&sh.bempty[bs]);
                 if (kb == ns - 1) {
                     tc05::mma_commit(&sh.dfull);
-                    last_bar = 2;
                     ++items_done;
                 }
             }
             // the MMAs still in flight must finish before the tensor memory is freed
-            if (last_bar == 0) pq_drain(&sh.afree[last_g], (uint32_t)(last_j & 1));
-            else if (last_bar == 1) pq_drain(&sh.empty[last_j % kPqStages], (uint32_t)((last_j / kPqStages) & 1));
-            else if (last_bar == 2) pq_drain(&sh.dfull, (uint32_t)((items_done - 1) & 1));
+            tc05::mma_commit(&sh.mdone[m]);
+            pq_drain(&sh.mdone[m], 0);
         }
     } else {
         // ---------------- dequant / epilogue warps
-        const int tt = warp >> 2, q = warp & 3;
+        const int set = warp >> 3, tt = (warp >> 2) & 1, q = warp & 3;
         const int r = tt * 128 + q * 32 + lane;     // stage row; TMEM lane q*32 + lane
+        const bool epi = set == 0;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         PqCursor pc;
         if (total > 0) pc.seek(a, nu, i0 / a.tiles);
         int items_done = 0;
         for (int j = 0; j < total; ++j) {
-            const int slot = j % kPqStages;
+            const int ws = j % kPqWStages;
             const int item = i0 + j / ns, kb = j % ns;
-            pq_wait(sh, &sh.full[slot], (uint32_t)((j / kPqStages) & 1));
-            const uint8_t *sp = ring + slot * kPqStage;
+            pq_wait(sh, &sh.wfull[ws], (uint32_t)((j / kPqWStages) & 1));
+            const uint8_t *sp = ring + ws * kPqWStage;
             const uint8_t *wr = sp + r * 128;
             const int x7 = r & 7;
 #pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
+            for (int g = 2 * set; g < 2 * set + 2; ++g) {
                 const uint4 w0 = *reinterpret_cast<const uint4 *>(wr + (((2 * g) ^ x7) << 4));
                 const uint4 w1 = *reinterpret_cast<const uint4 *>(wr + (((2 * g + 1) ^ x7) << 4));
                 const float sc = *reinterpret_cast<const float *>(sp + kPqOffS + r * 16 + g * 4);
@@ -682,7 +681,7 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                 pf_dequant(w0, w1, sc, A);
                 if (j > 0) {
                     // MMA(j - 1) of this group done: its A slot may be overwritten
-                    pq_wait(sh, &sh.afree[g], (uint32_t)((j - 1) & 1));
+                    pq_wait(sh, &sh.afree[g][tt], (uint32_t)((j - 1) & 1));
                     tc05::fence_after_sync();
                 }
                 tc05::tmem_st32(tmem + lane_base + (uint32_t)(g * 64 + tt * 32), A);
@@ -691,7 +690,9 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                 __syncwarp();
                 if (lane == 0) pq_arrive(&sh.afull[g]);
             }
-            if (kb == ns - 1) {
+            // this warp has read its rows of the stage: the weight slot may refill
+            if (lane == 0) pq_arrive(&sh.wempty[ws]);
+            if (kb == ns - 1 && epi) {
                 // item done: wait for its last MMAs, then read the accumulators
                 pq_wait(sh, &sh.dfull, (uint32_t)(items_done & 1));
                 tc05::fence_after_sync();
@@ -706,17 +707,22 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                         tc05::tmem_ld16(tmem + lane_base + kPqD + blk * 16, gv);
                         tc05::tmem_ld16(tmem + lane_base + kPqD + 64 + blk * 16, uv);
                         tc05::tmem_wait_ld();
+                        // h goes straight into down's packed B: pass pc.pi, group
+                        // j0 / 64, row n = token slot, column j0 % 64 (swizzled)
                         const int j0 = tile * 128 + r128;
+                        const int kq = j0 & 63;
+                        uint16_t *hp = a.h + ((size_t)pc.pi * (a.I / 64) + (j0 >> 6)) * (kPqBGroup / 2);
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
                             const int n = blk * 16 + c;
+                            float hv = 0.f;  // padded rows stay zero
                             if (n < ntok) {
                                 const float g0 = __uint_as_float(gv[c]), u0 = __uint_as_float(uv[c]);
-                                const float hv = g0 / (1.0f + expf(-g0)) * u0;
-                                const int p = a.list[pc.beg + n];
-                                const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-                                a.h[(size_t)p * a.I + j0] = *reinterpret_cast<const uint16_t *>(&hb);
+                                hv = g0 / (1.0f + expf(-g0)) * u0;
                             }
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                            hp[n * 64 + (((kq >> 3) ^ (n & 7)) << 3) + (kq & 7)] =
+                                *reinterpret_cast<const uint16_t *>(&hb);
                         }
                     }
                 } else {
@@ -746,6 +752,45 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
     if (threadIdx.x == 0 && sh.abort) atomicOr(a.status, 2);
     tc05::fence_after_sync();
     if (warp == 0) tc05::tmem_dealloc(tmem, kPqTmemCols);
+}
+
+// Packs the rows of x (bf16 [T][H]) that each pass uses into the MMA's B
+// layout: xp[pass][g][64 rows][64 bf16], row t = token slot t of the pass
+// (zero from its token count up to the next multiple of 16), 128-byte
+// swizzled. Grid (passes at most, ceil(G / 8)); warp w packs group
+// 8 * blockIdx.y + w of pass blockIdx.x.
+__global__ void __launch_bounds__(256)
+    k_pack_x(const uint16_t *__restrict__ x, int H, int k, const int32_t *offsets,
+             const int32_t *list, const int32_t *uexp, const int32_t *n_used,
+             const int32_t *pass_ofs, uint4 *xp) {
+    pdl_wait();  // the grouping comes from the previous kernel
+    pdl_trigger();
+    const int nu = *n_used;
+    const int pi = blockIdx.x;
+    if (nu == 0 || pi >= pass_ofs[nu]) return;
+    int lo = 0, hi = nu - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pass_ofs[mid] <= pi) lo = mid; else hi = mid - 1;
+    }
+    const int e = uexp[lo], pass = pi - pass_ofs[lo];
+    const int beg = offsets[e] + pass * kPfMaxN;
+    const int ntok = min(kPfMaxN, offsets[e + 1] - offsets[e] - pass * kPfMaxN);
+    const int npad = (ntok + 15) & ~15;
+    const int G = H / kGroup;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = blockIdx.y * 8 + warp;
+    if (g >= G) return;
+    uint4 *dst = xp + ((size_t)pi * G + g) * (kPfMaxN * 8);
+    for (int c = lane; c < npad * 8; c += 32) {
+        const int t = c >> 3, ch = c & 7;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (t < ntok) {
+            const int row = list[beg + t] / k;
+            v = *reinterpret_cast<const uint4 *>(x + (size_t)row * H + g * kGroup + ch * 8);
+        }
+        dst[t * 8 + (ch ^ (t & 7))] = v;
+    }
 }
 
 }  // namespace
@@ -808,5 +853,13 @@ cudaError_t launch_prefill(const MoeDims &m, int mode, const uint16_t *b, int k,
 }
 
 int prefill_pass_tokens() { return kPfMaxN; }
+
+cudaError_t launch_pack_x(const uint16_t *x, int H, int k, const int32_t *offsets,
+                          const int32_t *list, const int32_t *uexp, const int32_t *n_used,
+                          const int32_t *pass_ofs, uint16_t *xp, int pmax, cudaStream_t st) {
+    if (pmax < 1) return cudaSuccess;
+    return launch(k_pack_x, dim3(pmax, (H / kGroup + 7) / 8), dim3(256), 0, st, true, x, H, k,
+                  offsets, list, uexp, n_used, pass_ofs, reinterpret_cast<uint4 *>(xp));
+}
 
 }  // namespace qmv
