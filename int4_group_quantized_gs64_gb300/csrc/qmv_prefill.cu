@@ -373,14 +373,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(PfArgs a) {
 //     stores it to that group's A slot in tensor memory and the warp signals
 //     the group; at the end of an item set 0 reads the accumulators back and
 //     writes h (bf16) or y (fp32);
-//   * 2 MMA warps, one per row tile: one thread of each issues 4 groups x 4
-//     MMAs (M 128, N = tokens rounded up to 16, K 16) per stage into its
-//     tile's accumulator, which runs over the whole item, and commits each
-//     group to that group's A-slot barrier of its tile; after a stage it
-//     commits to the slot's empty barrier, after an item to the accumulator
-//     barrier. (A thread that issues tcgen05.mma waits ~100 cycles per
-//     instruction for N up to 64, so one issuer per tile halves that time.)
-// Tensor memory: A 4 groups x 2 tiles x 32 columns, D 2 tiles x 64 columns.
+//   * 4 MMA warps, one per (row tile, half of the stage's groups): one thread
+//     of each issues 2 groups x 4 MMAs (M 128, N = tokens rounded up to 16,
+//     K 16) per stage into its own accumulator, which runs over the whole
+//     item, and commits each group to that group's A-slot barrier of its
+//     tile; after a stage it commits to the B slot's empty barrier, after an
+//     item to the accumulator barrier. (A thread that issues tcgen05.mma
+//     waits ~100-200 cycles per instruction for N up to 64; four issuers
+//     share the stage's 32 MMAs.) The epilogue adds each tile's two halves.
+// Tensor memory: A 4 groups x 2 tiles x 32 columns, D 2 tiles x 2 halves x 64.
 // Every wait is bounded; a wait that runs out raises a CTA-wide abort flag,
 // after which nothing waits any more; copies and MMAs in flight are drained
 // (bounded) before the tensor memory is released, and bit 1 of the status
@@ -389,11 +390,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(PfArgs a) {
 constexpr int kPqDq = 16;                            // dequant warps (set 0: epilogue too)
 constexpr int kPqProdW = kPqDq;                      // weight producer warp
 constexpr int kPqProdB = kPqDq + 1;                  // B producer warp
-constexpr int kPqMma = kPqDq + 2;                    // first of 2 MMA warps
-constexpr int kPqMmaWarps = 2;
+constexpr int kPqMma = kPqDq + 2;                    // first of 4 MMA warps
+constexpr int kPqMmaWarps = 4;
 constexpr int kPqThreads = 32 * (kPqDq + 2 + kPqMmaWarps);
-constexpr int kPqWStages = 4;                        // weight ring: freed after dequant
-constexpr int kPqBStages = 2;                        // B ring: freed by the MMAs
+constexpr int kPqWStages = 3;                        // weight ring: freed after dequant
+constexpr int kPqBStages = 3;                        // B ring: freed by the MMAs
 constexpr int kPqOffS = 256 * 128;                   // scales [256][4] f32
 constexpr int kPqWStage = kPqOffS + 256 * 16;        // 36 KB of weights and scales
 constexpr int kPqBGroup = kPfMaxN * 128;             // B: 64 rows x 128 B per group
@@ -402,7 +403,7 @@ constexpr int kPqOffBRing = kPqWStages * kPqWStage;
 constexpr int kPqSmem = kPqOffBRing + kPqBStages * kPqBStage + 1024;
 constexpr uint32_t kPqTmaBytes = 256 * 128 + 256 * 16;
 constexpr uint32_t kPqTmemCols = 512;
-constexpr uint32_t kPqD = 256;                       // accumulators: 2 tiles x 64 columns
+constexpr uint32_t kPqD = 256;                       // accumulators: 2 tiles x 2 K halves x 64
 constexpr uint32_t kPqWait = 1u << 24;
 
 static_assert(kPqWStage % 1024 == 0 && kPqBStage % 1024 == 0,
@@ -617,12 +618,12 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                 pq_drain(&sh.bfull[j % kPqBStages], (uint32_t)((j / kPqBStages) & 1));
         }
     } else if (warp >= kPqMma) {
-        // ---------------- MMA issue: warp kPqMma + t issues row tile t
-        const int m = warp - kPqMma, t = m;
+        // ---------------- MMA issue: warp kPqMma + m: tile m / 2, groups 2(m % 2), +1
+        const int m = warp - kPqMma, t = m >> 1, hk = m & 1;
         if (lane == 0) {
             PqCursor pc;
             if (total > 0) pc.seek(a, nu, i0 / a.tiles);
-            const uint32_t dacc = tmem + kPqD + (uint32_t)(t * 64);
+            const uint32_t dacc = tmem + kPqD + (uint32_t)(m * 64);
             int items_done = 0;
             bool ok = true;
             for (int j = 0; j < total && ok; ++j) {
@@ -634,7 +635,7 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                 if (ok && kb == 0 && items_done > 0)
                     ok = pq_wait(sh, &sh.dfree, (uint32_t)((items_done - 1) & 1));
                 const uint32_t sB = tc05::smem_addr(ring + kPqOffBRing + bs * kPqBStage);
-                for (int g = 0; g < 4 && ok; ++g) {
+                for (int g = 2 * hk; g < 2 * hk + 2 && ok; ++g) {
                     ok = pq_wait(sh, &sh.afull[g], (uint32_t)(j & 1));
                     if (!ok) break;
                     tc05::fence_after_sync();
@@ -642,7 +643,7 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                     for (int kk = 0; kk < 4; ++kk)
                         tc05::mma_ts(dacc, tmem + g * 64 + t * 32 + kk * 8,
                                      tc05::sdesc_sw128(sB + g * kPqBGroup + kk * 32), idesc,
-                                     (kb > 0 || g > 0 || kk > 0) ? 1u : 0u);
+                                     (kb > 0 || g > 2 * hk || kk > 0) ? 1u : 0u);
                     tc05::mma_commit(&sh.afree[g][t]);
                 }
                 if (!ok) break;
@@ -703,9 +704,16 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                 if (a.mode == 0) {
                     // gate_up: tile tt takes column blocks tt, tt + 2, ...
                     for (int blk = tt; blk < nblk; blk += 2) {
-                        uint32_t gv[16], uv[16];
-                        tc05::tmem_ld16(tmem + lane_base + kPqD + blk * 16, gv);
-                        tc05::tmem_ld16(tmem + lane_base + kPqD + 64 + blk * 16, uv);
+                        // tile t, half h accumulates at kPqD + (2t + h) * 64
+                        float gs[16];
+                        uint32_t v0[16], v1[16];
+                        tc05::tmem_ld16(tmem + lane_base + kPqD + blk * 16, v0);
+                        tc05::tmem_ld16(tmem + lane_base + kPqD + 64 + blk * 16, v1);
+                        tc05::tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) gs[c] = __uint_as_float(v0[c]) + __uint_as_float(v1[c]);
+                        tc05::tmem_ld16(tmem + lane_base + kPqD + 128 + blk * 16, v0);
+                        tc05::tmem_ld16(tmem + lane_base + kPqD + 192 + blk * 16, v1);
                         tc05::tmem_wait_ld();
                         // h goes straight into down's packed B: pass pc.pi, group
                         // j0 / 64, row n = token slot, column j0 % 64 (swizzled)
@@ -717,7 +725,8 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                             const int n = blk * 16 + c;
                             float hv = 0.f;  // padded rows stay zero
                             if (n < ntok) {
-                                const float g0 = __uint_as_float(gv[c]), u0 = __uint_as_float(uv[c]);
+                                const float g0 = gs[c];
+                                const float u0 = __uint_as_float(v0[c]) + __uint_as_float(v1[c]);
                                 hv = g0 / (1.0f + expf(-g0)) * u0;
                             }
                             const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
@@ -728,15 +737,16 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                 } else {
                     const int row = tile * 256 + tt * 128 + r128;
                     for (int blk = 0; blk < nblk; ++blk) {
-                        uint32_t d[16];
-                        tc05::tmem_ld16(tmem + lane_base + kPqD + tt * 64 + blk * 16, d);
+                        uint32_t d[16], d2[16];
+                        tc05::tmem_ld16(tmem + lane_base + kPqD + tt * 128 + blk * 16, d);
+                        tc05::tmem_ld16(tmem + lane_base + kPqD + tt * 128 + 64 + blk * 16, d2);
                         tc05::tmem_wait_ld();
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
                             const int n = blk * 16 + c;
                             if (n < ntok) {
                                 const int p = a.list[pc.beg + n];
-                                a.y[(size_t)p * a.H + row] = __uint_as_float(d[c]);
+                                a.y[(size_t)p * a.H + row] = __uint_as_float(d[c]) + __uint_as_float(d2[c]);
                             }
                         }
                     }
