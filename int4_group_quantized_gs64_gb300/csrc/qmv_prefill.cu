@@ -556,10 +556,15 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
 
     const int nu = *a.n_used;
     const int total_items = nu > 0 ? a.pass_ofs[nu] * a.tiles : 0;
-    const int i0 = (int)((long long)blockIdx.x * total_items / gridDim.x);
-    const int i1 = (int)((long long)(blockIdx.x + 1) * total_items / gridDim.x);
+    // Items are dealt out round-robin (CTA c takes items c, c + grid, ...), so
+    // at any time the CTAs work on ~grid consecutive items: the tiles of a
+    // few passes, whose packed B and (passes of one expert) weights are then
+    // read from DRAM once and served from L2 to the other CTAs. Contiguous
+    // ranges would spread each pass's re-reads over the whole launch.
+    const int i0 = (int)blockIdx.x, istep = (int)gridDim.x;
+    const int n_items = i0 < total_items ? (total_items - i0 + istep - 1) / istep : 0;
     const int ns = a.G / 4;
-    const int total = (i1 - i0) * ns;  // stages of this CTA
+    const int total = n_items * ns;  // stages of this CTA
 
     if (warp == kPqProdW) {
         // ---------------- weight producer (one thread)
@@ -572,7 +577,7 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                 if (j >= kPqWStages &&
                     !pq_wait(sh, &sh.wempty[ws], (uint32_t)(((j / kPqWStages) - 1) & 1)))
                     break;
-                const int item = i0 + j / ns, kb = j % ns;
+                const int item = i0 + (j / ns) * istep, kb = j % ns;
                 pc.to(a, item / a.tiles);
                 const int tile = item % a.tiles;
                 const int rowA = a.mode == 0 ? tile * 128 : tile * 256;
@@ -602,7 +607,7 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                 if (j >= kPqBStages &&
                     !pq_wait(sh, &sh.bempty[bs], (uint32_t)(((j / kPqBStages) - 1) & 1)))
                     break;
-                const int item = i0 + j / ns, kb = j % ns, pi = item / a.tiles;
+                const int item = i0 + (j / ns) * istep, kb = j % ns, pi = item / a.tiles;
                 pc.to(a, pi);
                 const uint32_t bytes = (uint32_t)(((pc.ntok + 15) & ~15) * 128);
                 const uint32_t dst = tc05::smem_addr(ring + kPqOffBRing + bs * kPqBStage);
@@ -628,7 +633,7 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
             bool ok = true;
             for (int j = 0; j < total && ok; ++j) {
                 const int bs = j % kPqBStages;
-                const int item = i0 + j / ns, kb = j % ns;
+                const int item = i0 + (j / ns) * istep, kb = j % ns;
                 pc.to(a, item / a.tiles);
                 const uint32_t idesc = tc05::idesc_bf16_f32(128, (pc.ntok + 15) & ~15);
                 ok = pq_wait(sh, &sh.bfull[bs], (uint32_t)((j / kPqBStages) & 1));
@@ -668,7 +673,7 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
         int items_done = 0;
         for (int j = 0; j < total; ++j) {
             const int ws = j % kPqWStages;
-            const int item = i0 + j / ns, kb = j % ns;
+            const int item = i0 + (j / ns) * istep, kb = j % ns;
             pq_wait(sh, &sh.wfull[ws], (uint32_t)((j / kPqWStages) & 1));
             const uint8_t *sp = ring + ws * kPqWStage;
             const uint8_t *wr = sp + r * 128;
