@@ -198,7 +198,10 @@ size_t moe_workspace_bytes(const qmv_moe_int4 *m, int T, int k);
  *   256-byte aligned, owned by the caller, not shared between concurrent calls.
  *   The first int32 of ws is a device status word, cleared at the start of
  *   the call: bit 0 = an id outside [0, E) (that pair skipped, as moe_group),
- *   bit 1 = a bounded wait on the weight stream ran out (out not valid). */
+ *   bit 1 = a bounded wait on the weight stream ran out (out not valid).
+ *   One token (T == 1) with moe_one_token_path(m, k) == 1 runs as a single
+ *   cooperative kernel (all CTAs resident, one grid-wide barrier between
+ *   gate+up and down); the result is the same. */
 int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids,
                         const float *w, int k, float *out, void *ws, size_t ws_bytes,
                         qmv_stream_t stream);
@@ -232,6 +235,15 @@ int moe_ffn_combine(const qmv_moe_int4 *m, const int32_t *ids, const float *w, i
  * Errors: those of the descriptor check shared by every MoE call (QMV_EINVAL,
  * QMV_ESHAPE, QMV_EALIGN). */
 int moe_weight_path(const qmv_moe_int4 *m);
+
+/* Whether moe_expert_ffn_int4 with T == 1 and this k runs the single-launch
+ * kernel (1) or the grouped phases (0). The single launch is taken when the
+ * weight pools suit the tensor-map path (moe_weight_path == 1), H and I are
+ * multiples of 256, 1 <= k <= 32, and one CTA's share of the layer's weights
+ * fits in its shared memory. No counterpart on the pages; it names the kernel
+ * a profile shows. Host only, enqueues nothing.
+ * Errors: those of the descriptor check shared by every MoE call. */
+int moe_one_token_path(const qmv_moe_int4 *m, int k);
 
 /* Workspace of moe_expert_ffn_int4_prefill, in bytes (0 for unsupported sizes). */
 size_t moe_prefill_workspace_bytes(const qmv_moe_int4 *m, int T, int k);

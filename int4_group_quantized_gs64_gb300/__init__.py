@@ -74,6 +74,7 @@ def lib():
             "moe_ffn_down": ([P, i32, i32, vp, sz, vp], i32),
             "moe_ffn_combine": ([P, vp, vp, i32, i32, vp, vp, sz, vp], i32),
             "moe_weight_path": ([P], i32),
+            "moe_one_token_path": ([P, i32], i32),
             "moe_prefill_workspace_bytes": ([P, i32, i32], sz),
             "moe_expert_ffn_int4_prefill": ([P, vp, i32, vp, vp, i32, vp, vp, sz, vp], i32),
         }
@@ -304,6 +305,14 @@ def moe_weight_path(m: MoeInt4Weights) -> int:
     r = int(lib().moe_weight_path(m.desc))
     if r < 0:
         _check("moe_weight_path", r)
+    return r
+
+
+def moe_one_token_path(m: MoeInt4Weights, k: int) -> int:
+    """1: moe_expert_ffn_int4 with one token runs as a single cooperative kernel."""
+    r = int(lib().moe_one_token_path(m.desc, k))
+    if r < 0:
+        _check("moe_one_token_path", r)
     return r
 
 

@@ -54,6 +54,11 @@ int ffn_check(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
     return QMV_OK;
 }
 
+bool one_token(const qmv_moe_int4 *m, int k) {
+    const qmv::MoeDims d = dims(m);
+    return k >= 1 && k <= m->E && qmv::tma_moe_supported(d) && qmv::moe_one_supported(d, k);
+}
+
 template <class T>
 T *at(void *ws, size_t off) {
     return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
@@ -276,6 +281,12 @@ int moe_weight_path(const qmv_moe_int4 *m) {
     return qmv::tma_moe_supported(dims(m)) ? 1 : 0;
 }
 
+int moe_one_token_path(const qmv_moe_int4 *m, int k) {
+    const int r = check_moe(m);
+    if (r) return r;
+    return one_token(m, k) ? 1 : 0;
+}
+
 int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids,
                         const float *w, int k, float *out, void *ws, size_t ws_bytes,
                         qmv_stream_t stream) {
@@ -285,6 +296,17 @@ int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int3
     if (r) return r;
     if (!x || !ids || !w || !out) return QMV_EINVAL;
     if (!aligned(x, 4) || !aligned(ids, 4) || !aligned(w, 4) || !aligned(out, 4)) return QMV_EALIGN;
+    if (T == 1 && one_token(m, k)) {
+        // one token: a single cooperative launch after clearing the status
+        // word and the counters (the first counter is its grid barrier)
+        const cudaStream_t st = cs(stream);
+        cudaError_t e = cudaMemsetAsync(at<int32_t>(ws, L.status), 0, L.status_bytes, st);
+        if (e == cudaSuccess)
+            e = qmv::launch_moe_one(dims(m), x, ids, w, k, at<float>(ws, L.h), out,
+                                    at<int32_t>(ws, L.status),
+                                    reinterpret_cast<unsigned int *>(at<int32_t>(ws, L.sk_cnt)), st);
+        return from_cuda(e);
+    }
     if ((r = moe_ffn_prepare(m, x, T, ids, k, ws, ws_bytes, stream))) return r;
     if ((r = moe_ffn_gate_up(m, T, k, ws, ws_bytes, stream))) return r;
     if ((r = moe_ffn_down(m, T, k, ws, ws_bytes, stream))) return r;

@@ -95,6 +95,13 @@ cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const 
                            float *hfac, float *y, int32_t *status, int32_t *cnt, float *part,
                            cudaStream_t st);
 
+// Single-launch expert FFN of one token (cooperative grid, qmv_moe_one.cu).
+// bar: a zeroed word for the grid barrier.
+bool moe_one_supported(const MoeDims &m, int k);
+cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids, const float *w,
+                           int k, float *h, float *out, int32_t *status, unsigned int *bar,
+                           cudaStream_t st);
+
 // Workspace layout of the MoE entry points (256-byte aligned segments). The
 // status word and the split counters (kSkMaxCtas for gate+up, then kSkMaxCtas
 // for down) are adjacent, so one memset of status_bytes clears them all.

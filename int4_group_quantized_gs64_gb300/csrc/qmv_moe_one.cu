@@ -1,0 +1,405 @@
+// qmv_moe_one.cu - the expert FFN of one decode token in a single launch.
+//
+// Math (colibri PR #418, "qmatmul_gate_up.comp + coli_vk_gate_up",
+// "coli_vk_expert_group", "grouped scales in the Vulkan kernels"): for each
+// routed expert e_p with weight w_p, h_p = SiLU(G_p x) * (U_p x) and
+// out = sum_p w_p * D_p h_p; per 64-group the exact products (nibble - 8) * v
+// are summed and the group scale is applied in fp32 to that partial sum.
+// Operands are exact fp16 weights and fp16 hi + lo activations with one
+// power-of-two factor per 64-group (the fragment layout of qmv_device.cuh),
+// multiplied by warp MMAs with fp32 accumulation.
+//
+// With one token every expert is read once and the whole layer is only a
+// few MB, so the separate grouping, gate+up, down and combine launches cost
+// more than the bytes. Here one cooperative launch (one CTA per SM) does it:
+//   * at start, thread 0 requests the CTA's whole share of weights and scales
+//     by bulk copy: gate+up tiles t = CTA, CTA + grid, ... (a tile is 8 gate
+//     rows and the 8 up rows of the same hidden units) and down row tiles
+//     (16 output rows of every routed expert);
+//   * while they land, the CTA splits x into its activation units;
+//   * gate+up: the 8 warps split a tile's 64-groups, their partial sums are
+//     added in warp order and lane (gid, q = 0) writes h of unit gid;
+//   * one grid-wide barrier (every h written);
+//   * down: the CTA splits h into units, warp p computes expert p's 16-row
+//     tile and out = sum_p w_p y_p is added in expert order.
+// Every result is written by exactly one thread after a fixed-order sum, so
+// the output does not depend on timing.
+//
+// Waits are bounded: a copy or barrier wait that runs out sets bit 1 of the
+// status word (the outputs are then not valid) and the kernel goes on. An
+// expert id outside [0, E) sets bit 0 and contributes nothing.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "qmv_internal.h"
+#include "qmv_launch.cuh"
+#include "qmv_rows.cuh"
+#include "tc05.cuh"
+
+namespace qmv {
+
+namespace {
+
+constexpr int kOWarps = 8;
+constexpr int kOThreads = 32 * kOWarps;
+constexpr uint32_t kOWait = 1u << 24;
+constexpr int kOMaxK = 32;              // routed experts per token
+constexpr int kOSmemMax = 220 * 1024;   // dynamic shared memory budget
+
+struct OneArgs {
+    const uint8_t *gu_q;   // gate+up weights [E][2I][H/2]
+    const float *gu_s;     // their scales [E][2I][H/64]
+    const uint8_t *dn_q;   // down weights [E][H][I/2]
+    const float *dn_s;     // their scales [E][H][I/64]
+    int E, H, I, k;
+    const float *x;        // [H]
+    const int32_t *ids;    // [k]
+    const float *w;        // [k]
+    float *h;              // [k][I] (workspace)
+    float *out;            // [H]
+    int32_t *status;
+    unsigned int *bar;     // grid barrier count, zero at launch
+    // shared-memory layout (byte offsets from the aligned base)
+    int n1, n2;            // gate+up tiles, down row tiles per CTA (at most)
+    int o_xu, o_xf, o_w1, o_w2, o_hu, o_hf, o_red, o_scr;
+};
+
+struct OneShared {
+    uint64_t mb1, mb2;     // gate+up / down copies landed
+    int ids[kOMaxK];
+    float w[kOMaxK];
+};
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc05::smem_addr(mbar))
+        : "memory");
+}
+
+__device__ __forceinline__ void expect_tx(uint64_t *mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     tc05::smem_addr(mbar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned int *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// All CTAs of the (cooperative) grid: every write before it is visible to
+// every read after it. Bounded; returns false if it gave up.
+__device__ __forceinline__ bool grid_barrier(unsigned int *bar) {
+    __shared__ int ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ok = 1;
+        __threadfence();
+        atomicAdd(bar, 1u);
+        uint32_t i = 0;
+        while (ld_acquire(bar) < gridDim.x) {
+            if (++i == kOWait) {
+                ok = 0;
+                break;
+            }
+            __nanosleep(64);
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    return ok != 0;
+}
+
+// Groups c = w, w + nw, ... < n of a row-major source (64 floats per group
+// at src + 64 c, read through L2) -> activation units and factors in shared
+// memory; w / nw: this warp's index among the nw warps that share the work.
+// A warp takes up to 8 groups at once (loads, maxima and conversions of the 8
+// interleave), with 64 floats of scratch per group.
+__device__ __forceinline__ void split_groups(const float *src, int n, uint4 *units, float *fac,
+                                             float *scratch, int w, int nw) {
+    const int lane = threadIdx.x & 31;
+    for (int c0 = w; c0 < n; c0 += 8 * nw) {
+        float va[8], vb[8], m[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = c0 + i * nw;
+            va[i] = c < n ? __ldcg(src + (size_t)c * kGroup + lane) : 0.f;
+            vb[i] = c < n ? __ldcg(src + (size_t)c * kGroup + 32 + lane) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m[i] = fmaxf(fabsf(va[i]), fabsf(vb[i]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], o));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = c0 + i * nw;
+            const int e = split_exponent(m[i]);  // |e| <= 126: 2^e is a normal float
+            scratch[i * 64 + lane] = va[i] * __int_as_float((127 + e) << 23);
+            scratch[i * 64 + 32 + lane] = vb[i] * __int_as_float((127 + e) << 23);
+            if (lane == 0 && c < n) fac[c] = __int_as_float((127 - e) << 23);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = 2 * j + (lane >> 4), c = c0 + i * nw;
+            if (c < n) units[c * 16 + (lane & 15)] = make_unit<false>(scratch + i * 64, lane & 15);
+        }
+        __syncwarp();
+    }
+}
+
+// Lane (gid, q) of a warp: MMA over one 64-group of a 16-row tile in shared
+// memory (rows gid and gid + 8 at `rows` + row * rb, the group at byte 32 g)
+// against that group's activation units bu (one token: every B column is
+// token 0). Adds scale * factor * (hi + lo) of rows gid / gid + 8 to c0 / c8
+// (meaningful in lanes q == 0).
+__device__ __forceinline__ void tile_group_one(const uint8_t *rows, int rb, int g,
+                                               const uint4 (&bu)[1][2], float f, float s0,
+                                               float s8, float &c0, float &c8) {
+    const int lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
+    const uint8_t *r0 = rows + gid * rb + g * 32 + 8 * q;
+    const uint2 w0 = *reinterpret_cast<const uint2 *>(r0);
+    const uint2 w8 = *reinterpret_cast<const uint2 *>(r0 + 8 * rb);
+    float d[1][4];
+    tile_group_int4<1>(w0, w8, bu, d);
+    c0 = fmaf(s0 * f, d[0][0] + d[0][1], c0);
+    c8 = fmaf(s8 * f, d[0][2] + d[0][3], c8);
+}
+
+__device__ __forceinline__ void load_units(const uint4 *u, uint4 (&bu)[1][2]) {
+    const int lane = threadIdx.x & 31, q = lane & 3, part = (lane >> 2) & 1;
+    bu[0][0] = u[q * 2 + part];
+    bu[0][1] = u[(4 + q) * 2 + part];
+}
+
+__global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant__ OneArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ OneShared sh;
+    uint8_t *base = smem_raw + ((128u - (tc05::smem_addr(smem_raw) & 127u)) & 127u);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
+    const int H = a.H, I = a.I, k = a.k;
+    const int GH = H / kGroup, GI = I / kGroup;
+    const int tiles1 = k * (I / 8), tiles2 = H / 16;
+    const int b = blockIdx.x, grid = gridDim.x;
+    const int rb1 = H / 2, rb2 = I / 2;                        // row bytes
+    const uint32_t t1b = 16u * rb1 + 16u * GH * 4;            // gate+up tile: rows, scales
+    const uint32_t e2b = 16u * rb2 + 16u * GI * 4;            // down rows of one expert
+    const uint32_t t2b = (uint32_t)k * e2b;                   // down row tile
+    const int n1 = b < tiles1 ? (tiles1 - b + grid - 1) / grid : 0;
+    const int n2 = b < tiles2 ? (tiles2 - b + grid - 1) / grid : 0;
+
+    if (threadIdx.x < k) {
+        int e = a.ids[threadIdx.x];
+        if (e < 0 || e >= a.E) {
+            atomicOr(a.status, 1);
+            e = -1;
+        }
+        sh.ids[threadIdx.x] = e;
+        sh.w[threadIdx.x] = a.w[threadIdx.x];
+    }
+    if (threadIdx.x == 0) {
+        tc05::mbar_init(&sh.mb1, 1);
+        tc05::mbar_init(&sh.mb2, 1);
+        tc05::fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ---- every copy of the CTA's share, requested at once by thread 0 (a
+    // few large bulk copies: the copy engine takes commands one by one): per
+    // gate+up tile its 8 gate rows, its 8 up rows and their scales, per down
+    // row tile and expert 16 rows and their scales
+    if (threadIdx.x == 0) {
+        uint32_t bytes1 = 0, bytes2 = 0;
+        for (int i = 0; i < n1; ++i)
+            if (sh.ids[(b + i * grid) / (I / 8)] >= 0) bytes1 += t1b;
+        for (int p = 0; p < k; ++p)
+            if (sh.ids[p] >= 0) bytes2 += (uint32_t)n2 * e2b;
+        expect_tx(&sh.mb1, bytes1);
+        expect_tx(&sh.mb2, bytes2);
+        for (int i = 0; i < n1; ++i) {
+            const int t = b + i * grid, p = t / (I / 8), u0 = 8 * (t % (I / 8)), e = sh.ids[p];
+            if (e < 0) continue;
+            const uint32_t dw = tc05::smem_addr(base + a.o_w1 + i * t1b);
+            const uint32_t ds = dw + 16u * rb1;
+            const size_t rg = (size_t)e * 2 * I + u0, ru = rg + I;   // gate / up rows
+            bulk_g2s(dw, a.gu_q + rg * (H / 2), 8u * rb1, &sh.mb1);
+            bulk_g2s(dw + 8u * rb1, a.gu_q + ru * (H / 2), 8u * rb1, &sh.mb1);
+            bulk_g2s(ds, a.gu_s + rg * GH, 8u * GH * 4, &sh.mb1);
+            bulk_g2s(ds + 8u * GH * 4, a.gu_s + ru * GH, 8u * GH * 4, &sh.mb1);
+        }
+        for (int i = 0; i < n2; ++i)
+            for (int p = 0; p < k; ++p) {
+                const int e = sh.ids[p];
+                if (e < 0) continue;
+                const uint32_t dw = tc05::smem_addr(base + a.o_w2 + i * t2b) + (uint32_t)p * e2b;
+                const size_t r0 = (size_t)e * H + 16 * (b + i * grid);
+                bulk_g2s(dw, a.dn_q + r0 * (I / 2), 16u * rb2, &sh.mb2);
+                bulk_g2s(dw + 16u * rb2, a.dn_s + r0 * GI, 16u * GI * 4, &sh.mb2);
+            }
+    }
+
+    // ---- x -> activation units (each CTA its own copy)
+    uint4 *xu = reinterpret_cast<uint4 *>(base + a.o_xu);
+    float *xf = reinterpret_cast<float *>(base + a.o_xf);
+    float *red = reinterpret_cast<float *>(base + a.o_red);
+    float *scratch = reinterpret_cast<float *>(base + a.o_scr) + warp * 8 * 64;
+    if (warp > 0) split_groups(a.x, GH, xu, xf, scratch, warp - 1, kOWarps - 1);  // warp 0 copies
+    __syncthreads();
+
+    bool timed_out = false;
+    if (!tc05::mbar_wait(&sh.mb1, 0, kOWait)) timed_out = true;
+
+    // ---- gate+up: warp w takes groups w, w + 8, ... of every tile (four
+    // tiles at a time share the group's activation units); the partial sums
+    // red[tile][warp][16] are then added in warp order
+    for (int i0 = 0; i0 < n1; i0 += 4) {
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c8[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int g = warp; g < GH; g += kOWarps) {
+            uint4 bu[1][2];
+            load_units(xu + g * 16, bu);
+            const float f = xf[g];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j;
+                if (i < n1) {
+                    const uint8_t *rows = base + a.o_w1 + i * t1b;
+                    const float *sc = reinterpret_cast<const float *>(rows + 16 * rb1);
+                    tile_group_one(rows, rb1, g, bu, f, sc[gid * GH + g], sc[(gid + 8) * GH + g],
+                                   c0[j], c8[j]);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (q == 0 && i0 + j < n1) {
+                red[((i0 + j) * kOWarps + warp) * 16 + gid] = c0[j];
+                red[((i0 + j) * kOWarps + warp) * 16 + 8 + gid] = c8[j];
+            }
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < n1 * 8; c += kOThreads) {
+        const int i = c >> 3, u = c & 7, t = b + i * grid;
+        const int p = t / (I / 8), u0 = 8 * (t % (I / 8));
+        float gv = 0.f, uv = 0.f;
+        for (int w = 0; w < kOWarps; ++w) {
+            gv += red[(i * kOWarps + w) * 16 + u];
+            uv += red[(i * kOWarps + w) * 16 + 8 + u];
+        }
+        const float hv = sh.ids[p] >= 0 ? gv / (1.0f + expf(-gv)) * uv : 0.f;
+        a.h[(size_t)p * I + u0 + u] = hv;
+    }
+
+    if (!grid_barrier(a.bar)) timed_out = true;
+
+    // ---- h -> activation units (each CTA its own copy), then down + combine
+    uint4 *hu = reinterpret_cast<uint4 *>(base + a.o_hu);
+    float *hf = reinterpret_cast<float *>(base + a.o_hf);
+    split_groups(a.h, k * GI, hu, hf, scratch, warp, kOWarps);  // c: pair c / GI, group c % GI
+    __syncthreads();
+    if (!tc05::mbar_wait(&sh.mb2, 0, kOWait)) timed_out = true;
+    for (int i = 0; i < n2; ++i) {
+        for (int p = warp; p < k; p += kOWarps) {
+            float c0 = 0.f, c8 = 0.f;
+            if (sh.ids[p] >= 0) {
+                const uint8_t *rows = base + a.o_w2 + i * t2b + p * e2b;
+                const float *sc = reinterpret_cast<const float *>(rows + 16 * rb2);
+                for (int g = 0; g < GI; ++g) {
+                    uint4 bu[1][2];
+                    load_units(hu + (p * GI + g) * 16, bu);
+                    tile_group_one(rows, rb2, g, bu, hf[p * GI + g], sc[gid * GI + g],
+                                   sc[(gid + 8) * GI + g], c0, c8);
+                }
+            }
+            if (q == 0) {
+                red[p * 16 + gid] = c0;
+                red[p * 16 + 8 + gid] = c8;
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x < 16) {
+            float o = 0.f;
+            for (int p = 0; p < k; ++p)
+                if (sh.ids[p] >= 0) o = fmaf(sh.w[p], red[p * 16 + threadIdx.x], o);
+            a.out[16 * (b + i * grid) + threadIdx.x] = o;
+        }
+        __syncthreads();
+    }
+    if (timed_out && lane == 0) atomicOr(a.status, 2);
+    // copies still in flight (only after a wait ran out) land before exit
+    if (threadIdx.x == 0) {
+        tc05::mbar_wait(&sh.mb1, 0, kOWait);
+        tc05::mbar_wait(&sh.mb2, 0, kOWait);
+    }
+    __syncthreads();
+}
+
+inline size_t up16(size_t v) { return (v + 15) & ~(size_t)15; }
+
+// Shared-memory layout for (H, I, k) on a grid of `grid` CTAs; false if it
+// does not fit.
+bool one_layout(const MoeDims &m, int k, int grid, OneArgs &a, size_t &smem) {
+    const int GH = m.H / kGroup, GI = m.I / kGroup;
+    const int tiles1 = k * (m.I / 8), tiles2 = m.H / 16;
+    a.n1 = (tiles1 + grid - 1) / grid;
+    a.n2 = (tiles2 + grid - 1) / grid;
+    const size_t t1b = 16 * (size_t)(m.H / 2) + 16 * (size_t)GH * 4;
+    const size_t t2b = (size_t)k * (16 * (size_t)(m.I / 2) + 16 * (size_t)GI * 4);
+    size_t o = 0;
+    a.o_xu = (int)o; o = up16(o + (size_t)GH * 256);
+    a.o_xf = (int)o; o = up16(o + (size_t)GH * 4);
+    a.o_w1 = (int)o; o = up16(o + (size_t)a.n1 * t1b);
+    a.o_w2 = (int)o; o = up16(o + (size_t)a.n2 * t2b);
+    a.o_hu = (int)o; o = up16(o + (size_t)k * GI * 256);
+    a.o_hf = (int)o; o = up16(o + (size_t)k * GI * 4);
+    a.o_red = (int)o; o = up16(o + (size_t)std::max(a.n1 * kOWarps * 16, kOMaxK * 16) * 4);
+    a.o_scr = (int)o; o = up16(o + (size_t)kOWarps * 8 * 64 * 4);
+    smem = o + 128;
+    return smem <= (size_t)kOSmemMax;
+}
+
+}  // namespace
+
+bool moe_one_supported(const MoeDims &m, int k) {
+    if (k < 1 || k > kOMaxK || m.H % 256 || m.I % 256) return false;
+    OneArgs a;
+    size_t smem = 0;
+    return one_layout(m, k, sm_count(), a, smem);
+}
+
+cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids, const float *w,
+                           int k, float *h, float *out, int32_t *status, unsigned int *bar,
+                           cudaStream_t st) {
+    OneArgs a;
+    memset(&a, 0, sizeof(a));
+    size_t smem = 0;
+    const int grid = sm_count();
+    if (!one_layout(m, k, grid, a, smem)) return cudaErrorInvalidValue;
+    a.gu_q = m.gu_q; a.gu_s = m.gu_s; a.dn_q = m.dn_q; a.dn_s = m.dn_s;
+    a.E = m.E; a.H = m.H; a.I = m.I; a.k = k;
+    a.x = x; a.ids = ids; a.w = w; a.h = h; a.out = out; a.status = status; a.bar = bar;
+    cudaError_t e = set_smem(k_moe_one, smem);
+    if (e != cudaSuccess) return e;
+    if (max_ctas_per_sm(k_moe_one, kOThreads, smem) < 1) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kOThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_moe_one, a);
+}
+
+}  // namespace qmv

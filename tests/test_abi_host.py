@@ -123,6 +123,13 @@ def test_moe_validation(L):
     assert L.moe_weight_path(ctypes.byref(_desc(I=96))) == ESHAPE
     assert L.moe_weight_path(ctypes.byref(bad)) == EALIGN
     assert L.moe_weight_path(ctypes.byref(d)) in (0, 1)
+    # one-token path query: same descriptor rule
+    assert L.moe_one_token_path(None, 8) == EINVAL
+    assert L.moe_one_token_path(ctypes.byref(_desc(gs=32)), 8) == EINVAL
+    assert L.moe_one_token_path(ctypes.byref(_desc(I=96)), 8) == ESHAPE
+    assert L.moe_one_token_path(ctypes.byref(bad), 8) == EALIGN
+    assert L.moe_one_token_path(ctypes.byref(d), 8) in (0, 1)
+    assert L.moe_one_token_path(ctypes.byref(d), 0) == 0
 
 
 def test_workspace_grows_with_tokens(L):

@@ -111,10 +111,66 @@ def test_w2_full_layer():
     wts = datagen.moe_weights(wl["E"], wl["H"], wl["I"])
     m = q.MoeInt4Weights.from_numpy(wts)
     x, ids, w = _route_oracle(wl)
+    assert q.moe_one_token_path(m, wl["k"]) == 1  # one token: the single-launch kernel
     out = q.moe_expert_ffn_int4(m, dev(x), dev(ids), dev(w))
     torch.cuda.synchronize()
     ref = moe_oracle(wl["E"], wl["H"], wl["I"], x.astype(np.float64), ids, w, weights=wts)
     assert norm_err(out.cpu().numpy(), ref["out"], ref["den"]) <= TOL_FP32
+
+
+def _rand_pool(rng, E, H, I):
+    return dict(
+        gu_q=rng.integers(0, 256, size=(E, 2 * I, H // 2), dtype=np.uint8),
+        gu_s=(np.abs(rng.normal(0, 0.02, size=(E, 2 * I, H // 64))) + 1e-4).astype(np.float32),
+        dn_q=rng.integers(0, 256, size=(E, H, I // 2), dtype=np.uint8),
+        dn_s=(np.abs(rng.normal(0, 0.02, size=(E, H, I // 64))) + 1e-4).astype(np.float32),
+    )
+
+
+@pytest.mark.parametrize("E,H,I,k", [(8, 256, 256, 1), (8, 256, 256, 8), (40, 512, 768, 4),
+                                     (64, 1024, 256, 32), (300, 2048, 512, 8)])
+def test_one_token_shapes(E, H, I, k):
+    """One token on the single-launch kernel: one and many experts, k = E,
+    k = 32 (every warp takes several down tiles), several gate+up tiles per CTA."""
+    rng = np.random.default_rng(E * 7 + H + I + k)
+    wts = _rand_pool(rng, E, H, I)
+    m = q.MoeInt4Weights.from_numpy(wts)
+    assert q.moe_one_token_path(m, k) == 1
+    x = rng.normal(size=(1, H)).astype(np.float32)
+    ids, w = oracle.route_topk(rng.normal(size=(1, E)).astype(np.float32), k)
+    w = w.astype(np.float32)
+    ws = torch.full((q.moe_workspace_bytes(m, 1, k),), 0xFF, dtype=torch.uint8, device="cuda")
+    ref = oracle.moe_ffn(wts, x.astype(np.float64), ids, w)
+    first = None
+    for _ in range(3):  # the grid barrier's counter is cleared by every call
+        out = q.moe_expert_ffn_int4(m, dev(x), dev(ids), dev(w), ws=ws)
+        torch.cuda.synchronize()
+        assert int(ws[:4].view(torch.int32).cpu()[0]) == 0
+        o = out.cpu().numpy()
+        assert norm_err(o, ref["out"], ref["den"]) <= TOL_FP32
+        if first is None:
+            first = o
+        assert np.array_equal(o, first)
+
+
+def test_one_token_bad_ids_and_fallback():
+    rng = np.random.default_rng(78)
+    E, H, I, k = 4, 256, 256, 3
+    wts = _rand_pool(rng, E, H, I)
+    m = q.MoeInt4Weights.from_numpy(wts)
+    assert q.moe_one_token_path(m, k) == 1
+    x = rng.normal(size=(1, H)).astype(np.float32)
+    ids = np.array([[2, 9, 0]], np.int32)
+    w = np.array([[0.5, 0.25, 0.25]], np.float32)
+    ws = torch.empty(q.moe_workspace_bytes(m, 1, k), dtype=torch.uint8, device="cuda")
+    out = q.moe_expert_ffn_int4(m, dev(x), dev(ids), dev(w), ws=ws)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).cpu()[0]) == 1  # the bad id is flagged and skipped
+    ref = moe_oracle(E, H, I, x.astype(np.float64), ids, w, weights=wts)
+    assert norm_err(out.cpu().numpy(), ref["out"], ref["den"]) <= TOL_FP32
+    # too large for one CTA's shared memory: the grouped phases instead
+    big = q.MoeInt4Weights.from_numpy(_rand_pool(rng, 2, 6144, 2048))
+    assert q.moe_one_token_path(big, 2) == 0
 
 
 def test_w2_stages_hidden():
@@ -210,7 +266,7 @@ def test_ffn_phases_repeat_match_fused():
     wl = W2
     wts = datagen.moe_weights(wl["E"], wl["H"], wl["I"])
     m = q.MoeInt4Weights.from_numpy(wts)
-    x, ids, w = _route_oracle(wl)
+    x, ids, w = _route_oracle(wl, T=2)  # two tokens: the call runs the same phases
     dx, dids, dw = dev(x), dev(ids), dev(w)
     fused = q.moe_expert_ffn_int4(m, dx, dids, dw).cpu().numpy()
     T, k = ids.shape
