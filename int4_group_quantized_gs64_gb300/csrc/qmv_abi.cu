@@ -54,6 +54,13 @@ int ffn_check(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
     return QMV_OK;
 }
 
+// The phases keep the activation units pass-packed (two copies per stage in
+// the tensor-map kernel) when that kernel runs and a token's pairs fit the
+// grouping kernel's per-token slots.
+bool packed_units(const qmv_moe_int4 *m, int k) {
+    return qmv::tma_moe_supported(dims(m)) && k <= 32;
+}
+
 bool one_token(const qmv_moe_int4 *m, int k) {
     const qmv::MoeDims d = dims(m);
     return k >= 1 && k <= m->E && qmv::tma_moe_supported(d) && qmv::moe_one_supported(d, k);
@@ -217,13 +224,15 @@ int moe_ffn_prepare(const qmv_moe_int4 *m, const float *x, int T, const int32_t 
     if (!x || !ids) return QMV_EINVAL;
     if (!aligned(x, 4) || !aligned(ids, 4)) return QMV_EALIGN;
     const cudaStream_t st = cs(stream);
+    const bool pk = packed_units(m, k);
     cudaError_t e = cudaMemsetAsync(at<int32_t>(ws, L.status), 0, L.status_bytes, st);
     if (e == cudaSuccess)
         e = qmv::launch_group_split(ids, T, k, m->E, at<int32_t>(ws, L.offsets),
                                     at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
                                     at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs),
-                                    at<int32_t>(ws, L.status), x, m->H, at<void>(ws, L.xcells),
-                                    at<float>(ws, L.xfac), st);
+                                    at<int32_t>(ws, L.status), x, m->H,
+                                    at<void>(ws, pk ? L.xpk : L.xcells),
+                                    at<float>(ws, pk ? L.xpf : L.xfac), st, 8, pk);
     return from_cuda(e);
 }
 
@@ -232,13 +241,16 @@ int moe_ffn_gate_up(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_byt
     qmv::MoeWorkspace L;
     int r = ffn_check(m, T, k, ws, ws_bytes, L);
     if (r) return r;
-    if (qmv::tma_moe_supported(dims(m)))
+    if (qmv::tma_moe_supported(dims(m))) {
+        const bool pk = packed_units(m, k);
         return from_cuda(qmv::launch_moe_tma(
-            dims(m), 0, at<void>(ws, L.xcells), at<float>(ws, L.xfac), k,
+            dims(m), 0, at<void>(ws, pk ? L.xpk : L.xcells), at<float>(ws, pk ? L.xpf : L.xfac), k,
             at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
             at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs), at<float>(ws, L.h),
-            at<void>(ws, L.hcells), at<float>(ws, L.hfac), nullptr, at<int32_t>(ws, L.status),
-            at<int32_t>(ws, L.sk_cnt), at<float>(ws, L.sk_part), cs(stream)));
+            at<void>(ws, pk ? L.hpk : L.hcells), at<float>(ws, pk ? L.hpf : L.hfac), nullptr,
+            at<int32_t>(ws, L.status), at<int32_t>(ws, L.sk_cnt), at<float>(ws, L.sk_part),
+            cs(stream), pk));
+    }
     return from_cuda(qmv::launch_gate_up(
         dims(m), at<void>(ws, L.xcells), at<float>(ws, L.xfac), k, at<int32_t>(ws, L.offsets),
         at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp), at<int32_t>(ws, L.n_used),
@@ -251,13 +263,15 @@ int moe_ffn_down(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
     qmv::MoeWorkspace L;
     int r = ffn_check(m, T, k, ws, ws_bytes, L);
     if (r) return r;
-    if (qmv::tma_moe_supported(dims(m)))
+    if (qmv::tma_moe_supported(dims(m))) {
+        const bool pk = packed_units(m, k);
         return from_cuda(qmv::launch_moe_tma(
-            dims(m), 1, at<void>(ws, L.hcells), at<float>(ws, L.hfac), k,
+            dims(m), 1, at<void>(ws, pk ? L.hpk : L.hcells), at<float>(ws, pk ? L.hpf : L.hfac), k,
             at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
             at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs), nullptr, nullptr, nullptr,
             at<float>(ws, L.y), at<int32_t>(ws, L.status), at<int32_t>(ws, L.sk_cnt) + qmv::kSkMaxCtas,
-            at<float>(ws, L.sk_part), cs(stream)));
+            at<float>(ws, L.sk_part), cs(stream), pk));
+    }
     return from_cuda(qmv::launch_down(dims(m), at<void>(ws, L.hcells), at<float>(ws, L.hfac),
                                       at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list),
                                       at<int32_t>(ws, L.uexp), at<int32_t>(ws, L.n_used),

@@ -38,11 +38,13 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids,
                          cudaStream_t st);
 cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int32_t *list,
                          int32_t *uexp, int32_t *n_used, int32_t *status, cudaStream_t st);
-// Grouping plus the split of the T activation rows, in one launch.
+// Grouping plus the split of the T activation rows, in one launch. With
+// packed == true the units go to the pass-packed layout (see MoeWorkspace)
+// instead of per-row cells.
 cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
                                int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
-                               cudaStream_t st, int pass_tok = 8);
+                               cudaStream_t st, int pass_tok = 8, bool packed = false);
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
                           int32_t *pass_ofs, cudaStream_t st, bool pdl);
 // Activation rows [R][K] fp32 -> fragment cells [R][K/64][16] uint4 + factors [R][K/64].
@@ -89,11 +91,13 @@ bool tma_dense_supported(const uint8_t *wq, const float *scales, int N, int K);
 cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int K, int S,
                              const void *cells, const float *cfac, float *y, int32_t *status,
                              int32_t *cnt, float *part, cudaStream_t st);
+// packed: the activation units (cells, cfac) and, for gate+up, the units of
+// h it writes (hcells, hfac) are in the pass-packed layout; else per row.
 cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const float *cfac, int k,
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                            const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,
                            float *hfac, float *y, int32_t *status, int32_t *cnt, float *part,
-                           cudaStream_t st);
+                           cudaStream_t st, bool packed = false);
 
 // Single-launch expert FFN of one token (cooperative grid, qmv_moe_one.cu).
 // bar: a zeroed word for the grid barrier.
@@ -105,9 +109,15 @@ cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids,
 // Workspace layout of the MoE entry points (256-byte aligned segments). The
 // status word and the split counters (kSkMaxCtas for gate+up, then kSkMaxCtas
 // for down) are adjacent, so one memset of status_bytes clears them all.
+// Pass-packed activation units (tensor-map decode path): for pass pi and
+// stage s (4 groups), the units of the pass's token slots 0..7 follow each
+// other, [pi][s][slot][4 groups x 16 uint4] (8 KB per stage), with the
+// factors in [pi][s][slot][4]; a stage's operands are then one contiguous
+// copy per kind. xpk / xpf hold x for gate+up, hpk / hpf h for down.
 struct MoeWorkspace {
     size_t status, sk_cnt, status_bytes, offsets, list, uexp, n_used, pass_ofs, xcells, xfac, h,
-        hcells, hfac, y, sk_part, total;
+        hcells, hfac, y, sk_part, xpk, xpf, hpk, hpf, total;
+    int pmax;  // passes, at most
 };
 MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k);
 

@@ -191,14 +191,86 @@ __device__ void split_row_cta(const float *__restrict__ row, int K, uint4 *cells
     }
 }
 
-// CTA 0 groups the pairs; CTA 1 + t splits token row t of x.
+// Pass and slot of the pairs of token t (pairs tk .. tk + k - 1), as the
+// grouping of CTA 0 places them: the pass offset of each used expert comes
+// from the same counts and scan, the rank of a pair among the pairs of its
+// expert from counting the earlier pairs with that expert (the lists are in
+// pair order). pass[j] = -1 for an id outside [0, E).
+__device__ void pair_slots_cta(const int32_t *__restrict__ ids, int P, int E, int k, int t,
+                               int pass_tok, int *pass, int *slot) {
+    __shared__ int32_t cnt[1024], pofs[1024], tot[96], rank[32], eid[32];
+    const int tid = threadIdx.x;
+    cnt[tid] = 0;
+    if (tid < k) {
+        const int e = ids[(size_t)t * k + tid];
+        eid[tid] = (e >= 0 && e < E) ? e : -1;
+        rank[tid] = 0;
+    }
+    __syncthreads();
+    for (int p = tid; p < P; p += blockDim.x) {
+        const int e = ids[p];
+        if (e >= 0 && e < E) {
+            atomicAdd(&cnt[e], 1);
+            for (int j = 0; j < k; ++j)
+                if (e == eid[j] && p < t * k + j) atomicAdd(&rank[j], 1);
+        }
+    }
+    __syncthreads();
+    const int c = tid < E ? cnt[tid] : 0;
+    const int np = (c + pass_tok - 1) / pass_tok;
+    int ec, ef, ep;
+    block_scan3(c, c > 0 ? 1 : 0, np, ec, ef, ep, tot);
+    if (tid < E) pofs[tid] = ep;
+    __syncthreads();
+    if (tid < k) {
+        const int e = eid[tid];
+        pass[tid] = e < 0 ? -1 : pofs[e] + rank[tid] / pass_tok;
+        slot[tid] = e < 0 ? 0 : rank[tid] % pass_tok;
+    }
+    __syncthreads();
+}
+
+// Splits token row t into units once and writes them to each of its pairs'
+// (pass, slot) in the pass-packed layout: stage s = g / 4 of pass pi at
+// ((pi * ns + s) * kMaxTok + slot) * 64 + (g % 4) * 16 uint4, the factor at
+// ((pi * ns + s) * kMaxTok + slot) * 4 + g % 4.
+__device__ void split_row_packed_cta(const float *__restrict__ row, int K, int k,
+                                     const int *pass, const int *slot, uint4 *pk, float *pf) {
+    __shared__ float buf[32][64];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = K / kGroup, ns = G / 4;
+    for (int g = warp; g < G; g += blockDim.x >> 5) {
+        const float a = row[g * kGroup + lane], b = row[g * kGroup + 32 + lane];
+        const int e = split_exponent(warp_max(fmaxf(fabsf(a), fabsf(b))));
+        const float mul = ldexpf(1.0f, e);
+        buf[warp][lane] = a * mul;
+        buf[warp][32 + lane] = b * mul;
+        __syncwarp();
+        const uint4 u = make_unit<false>(buf[warp], lane & 15);
+        for (int j = lane >> 4; j < k; j += 2) {
+            if (pass[j] < 0) continue;
+            const size_t c = ((size_t)pass[j] * ns + g / 4) * kMaxTok + slot[j];
+            pk[c * 64 + (g % 4) * 16 + (lane & 15)] = u;
+            if ((lane & 15) == 0) pf[c * 4 + g % 4] = ldexpf(1.0f, -e);
+        }
+        __syncwarp();
+    }
+}
+
+// CTA 0 groups the pairs; CTA 1 + t splits token row t of x (per row, or
+// into the pass-packed layout when packed != 0).
 __global__ void __launch_bounds__(1024)
     k_group_split(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets, int32_t *list,
                   int32_t *uexp, int32_t *n_used, int32_t *pass_ofs, int32_t *status,
-                  const float *__restrict__ x, int H, uint4 *xcells, float *xfac, int pass_tok) {
+                  const float *__restrict__ x, int H, uint4 *xcells, float *xfac, int pass_tok,
+                  int k, int packed) {
     pdl_trigger();
     if (blockIdx.x == 0) {
         group_cta(ids, P, E, offsets, list, uexp, n_used, pass_ofs, status, pass_tok);
+    } else if (packed) {
+        __shared__ int pass[32], slot[32];
+        const int t = blockIdx.x - 1;
+        pair_slots_cta(ids, P, E, k, t, pass_tok, pass, slot);
+        split_row_packed_cta(x + (size_t)t * H, H, k, pass, slot, xcells, xfac);
     } else {
         const int t = blockIdx.x - 1;
         const int G = H / kGroup;
@@ -538,16 +610,16 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int
                          int32_t *uexp, int32_t *n_used, int32_t *status, cudaStream_t st) {
     return launch(k_group_split, dim3(1), dim3(1024), 0, st, false, ids, P, E, offsets, list, uexp,
                   n_used, (int32_t *)nullptr, status, (const float *)nullptr, 64,
-                  (uint4 *)nullptr, (float *)nullptr, (int)kMaxTok);
+                  (uint4 *)nullptr, (float *)nullptr, (int)kMaxTok, 1, 0);
 }
 
 cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
                                int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
-                               cudaStream_t st, int pass_tok) {
+                               cudaStream_t st, int pass_tok, bool packed) {
     return launch(k_group_split, dim3(x ? 1 + T : 1), dim3(1024), 0, st, false, ids, T * k, E,
                   offsets, list, uexp, n_used, pass_ofs, status, x, H, static_cast<uint4 *>(xcells),
-                  xfac, pass_tok);
+                  xfac, pass_tok, k, packed ? 1 : 0);
 }
 
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
@@ -606,6 +678,14 @@ MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k) {
     L.hfac = o; o = align256(o + 4 * P * (I / 64));
     L.y = o; o = align256(o + 4 * P * H);
     L.sk_part = o; o = align256(o + 4 * (size_t)kSkMaxCtas * kSkPartFloats);
+    // a pass holds up to kMaxTok pairs of one expert: at most P / kMaxTok + min(E, P) passes
+    const size_t pm = std::min(P, (P + kMaxTok - 1) / kMaxTok + std::min((size_t)E, P));
+    L.pmax = (int)pm;
+    const size_t sh = (size_t)H / (4 * kGroup), si = (size_t)I / (4 * kGroup);  // stages
+    L.xpk = o; o = align256(o + pm * sh * kMaxTok * 1024);
+    L.xpf = o; o = align256(o + pm * sh * kMaxTok * 16);
+    L.hpk = o; o = align256(o + pm * si * kMaxTok * 1024);
+    L.hpf = o; o = align256(o + pm * si * kMaxTok * 16);
     L.total = o;
     return L;
 }

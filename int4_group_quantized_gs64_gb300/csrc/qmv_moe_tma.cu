@@ -68,12 +68,14 @@ struct TmaArgs {
     int mode;            // 0: gate+up, 1: down, 2: dense GEMV (one matrix, tokens 0..S-1)
     int G, I, H, k;
     int S;               // dense: tokens
+    int packed;          // activation units pass-packed (else per row)
     const int32_t *offsets, *list, *uexp, *n_used, *pass_ofs;
-    const uint4 *cells;  // activation units [row][G][16]
-    const float *cfac;   // their factors [row][G]
+    const uint4 *cells;  // activation units: per row [row][G][16], or pass-packed
+                         // [pass][G/4][slot][64]
+    const float *cfac;   // their factors [row][G], or [pass][G/4][slot][4]
     float *h;            // gate+up: h fp32 [P][I]
-    uint4 *hcells;       // gate+up: units of h [P][I/64][16]
-    float *hfac;         // gate+up: factors of h [P][I/64]
+    uint4 *hcells;       // gate+up: units of h [P][I/64][16], or pass-packed
+    float *hfac;         // gate+up: factors of h [P][I/64], or pass-packed
     float *y;            // down: y [P][H]
     int32_t *status;
     int32_t *cnt;        // per CTA: contributors done on the split item that starts in it
@@ -274,7 +276,7 @@ __device__ __forceinline__ void t_consume(TShared &sh, const uint8_t *ring, int 
 
 template <int NB>
 __device__ __forceinline__ void t_epilogue(const TmaArgs &a, const TShared &sh, float *epi,
-                                           int tile, int ntok, const float acc[NB][2]) {
+                                           int tile, int ntok, int pi, const float acc[NB][2]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3;
     const int pr = tile_row(lane >> 2);
     if (a.mode != 0) {
@@ -339,9 +341,17 @@ __device__ __forceinline__ void t_epilogue(const TmaArgs &a, const TShared &sh, 
             wbuf[warp * 64 + lane] = v0 * mul;
             wbuf[warp * 64 + 32 + lane] = v1 * mul;
             __syncwarp();
-            const size_t cb = (size_t)sh.pairs[s] * Gd + gd;
-            if (lane < 16) a.hcells[cb * 16 + lane] = make_unit<false>(wbuf + warp * 64, lane);
-            if (lane == 0) a.hfac[cb] = ldexpf(1.0f, -e);
+            if (a.packed) {
+                // down's pass pi, slot s (down groups the pairs as gate+up does)
+                const size_t c = ((size_t)pi * (Gd / 4) + gd / 4) * kMaxTok + s;
+                if (lane < 16)
+                    a.hcells[c * 64 + (gd % 4) * 16 + lane] = make_unit<false>(wbuf + warp * 64, lane);
+                if (lane == 0) a.hfac[c * 4 + gd % 4] = ldexpf(1.0f, -e);
+            } else {
+                const size_t cb = (size_t)sh.pairs[s] * Gd + gd;
+                if (lane < 16) a.hcells[cb * 16 + lane] = make_unit<false>(wbuf + warp * 64, lane);
+                if (lane == 0) a.hfac[cb] = ldexpf(1.0f, -e);
+            }
             __syncwarp();
         }
     }
@@ -516,7 +526,16 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
             }
             if (j >= pre && lane == 0) weights(slot, item, kb, pc);
             __syncwarp();
-            if (lane < pc.ntok) {
+            if (a.packed) {
+                // the pass's token slots are contiguous: two copies per stage
+                if (lane == 0) {
+                    const uint32_t base = tc05::smem_addr(ring + slot * kTStage);
+                    const uint32_t fb = tc05::smem_addr(&sh.full[slot]);
+                    const size_t cs = ((size_t)pi * ns + kb) * kMaxTok;
+                    bulk_load(base + kTOffA, a.cells + cs * 64, pc.ntok * kTActTok, fb);
+                    bulk_load(base + kTOffF, a.cfac + cs * 4, pc.ntok * kTFacTok, fb);
+                }
+            } else if (lane < pc.ntok) {
                 const uint32_t base = tc05::smem_addr(ring + slot * kTStage);
                 const uint32_t fb = tc05::smem_addr(&sh.full[slot]);
                 const size_t cg = (size_t)myrow * a.G + 4 * kb;
@@ -565,13 +584,13 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
                 t_consume<1>(sh, ring, pc.ntok, kb0, kb1, j, failed, acc);
                 if (fresh) consumers_sync();  // sh.pairs written before the epilogue reads it
                 if (whole || t_combine<1>(a, sh, pc.ntok, item, item == head_item, ns, acc))
-                    t_epilogue<1>(a, sh, epi, tile, pc.ntok, acc);
+                    t_epilogue<1>(a, sh, epi, tile, pc.ntok, pi, acc);
             } else {
                 float acc[2][2];
                 t_consume<2>(sh, ring, pc.ntok, kb0, kb1, j, failed, acc);
                 if (fresh) consumers_sync();
                 if (whole || t_combine<2>(a, sh, pc.ntok, item, item == head_item, ns, acc))
-                    t_epilogue<2>(a, sh, epi, tile, pc.ntok, acc);
+                    t_epilogue<2>(a, sh, epi, tile, pc.ntok, pi, acc);
             }
         }
         if (failed && (threadIdx.x & 31) == 0) atomicOr(a.status, 2);
@@ -641,10 +660,11 @@ cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const 
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                            const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,
                            float *hfac, float *y, int32_t *status, int32_t *cnt, float *part,
-                           cudaStream_t st) {
+                           cudaStream_t st, bool packed) {
     TmaArgs a;
     memset(&a, 0, sizeof(a));
     a.mode = mode;
+    a.packed = packed ? 1 : 0;
     a.I = m.I;
     a.H = m.H;
     a.k = k;
