@@ -232,7 +232,7 @@ int moe_ffn_prepare(const qmv_moe_int4 *m, const float *x, int T, const int32_t 
                                     at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs),
                                     at<int32_t>(ws, L.status), x, m->H,
                                     at<void>(ws, pk ? L.xpk : L.xcells),
-                                    at<float>(ws, pk ? L.xpf : L.xfac), st, 8, pk);
+                                    (pk ? nullptr : at<float>(ws, L.xfac)), st, 8, pk);
     return from_cuda(e);
 }
 
@@ -244,10 +244,10 @@ int moe_ffn_gate_up(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_byt
     if (qmv::tma_moe_supported(dims(m))) {
         const bool pk = packed_units(m, k);
         return from_cuda(qmv::launch_moe_tma(
-            dims(m), 0, at<void>(ws, pk ? L.xpk : L.xcells), at<float>(ws, pk ? L.xpf : L.xfac), k,
+            dims(m), 0, at<void>(ws, pk ? L.xpk : L.xcells), (pk ? nullptr : at<float>(ws, L.xfac)), k,
             at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
             at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs), at<float>(ws, L.h),
-            at<void>(ws, pk ? L.hpk : L.hcells), at<float>(ws, pk ? L.hpf : L.hfac), nullptr,
+            at<void>(ws, pk ? L.hpk : L.hcells), (pk ? nullptr : at<float>(ws, L.hfac)), nullptr,
             at<int32_t>(ws, L.status), at<int32_t>(ws, L.sk_cnt), at<float>(ws, L.sk_part),
             cs(stream), pk));
     }
@@ -266,7 +266,7 @@ int moe_ffn_down(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
     if (qmv::tma_moe_supported(dims(m))) {
         const bool pk = packed_units(m, k);
         return from_cuda(qmv::launch_moe_tma(
-            dims(m), 1, at<void>(ws, pk ? L.hpk : L.hcells), at<float>(ws, pk ? L.hpf : L.hfac), k,
+            dims(m), 1, at<void>(ws, pk ? L.hpk : L.hcells), (pk ? nullptr : at<float>(ws, L.hfac)), k,
             at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
             at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs), nullptr, nullptr, nullptr,
             at<float>(ws, L.y), at<int32_t>(ws, L.status), at<int32_t>(ws, L.sk_cnt) + qmv::kSkMaxCtas,

@@ -83,10 +83,10 @@ cudaError_t launch_pack_x(const uint16_t *x, int H, int k, const int32_t *offset
 constexpr int kSkMaxCtas = 256;                 // CTAs of one launch, at most
 constexpr int kSkPartFloats = 2 * 256 * 8;      // per CTA: 2 slots x 256 rows x 8 tokens
 bool tma_moe_supported(const MoeDims &m);
-// 3-D tensor maps of a weight pool [E][rows][K/2] (box 128 B x 128 rows,
-// 128-byte swizzle) and of its scales [E][rows][K/64] (box 4 x 128 rows).
+// 3-D tensor maps of a weight pool [E][rows][K/2] (box 128 B x box_rows rows,
+// 128-byte swizzle) and of its scales [E][rows][K/64] (box 4 x box_rows rows).
 bool encode_weight_maps(CUtensorMap *wmap, CUtensorMap *smap, const uint8_t *wq, const float *ws,
-                        int E, int rows, int K);
+                        int E, int rows, int K, int box_rows = 128);
 bool tma_dense_supported(const uint8_t *wq, const float *scales, int N, int K);
 cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int K, int S,
                              const void *cells, const float *cfac, float *y, int32_t *status,
@@ -109,14 +109,16 @@ cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids,
 // Workspace layout of the MoE entry points (256-byte aligned segments). The
 // status word and the split counters (kSkMaxCtas for gate+up, then kSkMaxCtas
 // for down) are adjacent, so one memset of status_bytes clears them all.
-// Pass-packed activation units (tensor-map decode path): for pass pi and
-// stage s (4 groups), the units of the pass's token slots 0..7 follow each
-// other, [pi][s][slot][4 groups x 16 uint4] (8 KB per stage), with the
-// factors in [pi][s][slot][4]; a stage's operands are then one contiguous
-// copy per kind. xpk / xpf hold x for gate+up, hpk / hpf h for down.
+// Pass-packed activation units (tensor-map decode path): block (pi, s) of
+// kPackedStage bytes holds, for pass pi and stage s (4 groups), the factors
+// of the pass's token slots 0..7 ([slot][4] floats, 128 B) followed by their
+// units ([slot][4 groups x 16] uint4, 1 KB a slot), so a stage's activations
+// are one contiguous copy of 128 B + 1 KB per token. xpk holds x for
+// gate+up, hpk h for down.
+constexpr int kPackedStage = 128 + 8 * 1024;
 struct MoeWorkspace {
     size_t status, sk_cnt, status_bytes, offsets, list, uexp, n_used, pass_ofs, xcells, xfac, h,
-        hcells, hfac, y, sk_part, xpk, xpf, hpk, hpf, total;
+        hcells, hfac, y, sk_part, xpk, hpk, total;
     int pmax;  // passes, at most
 };
 MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k);

@@ -231,11 +231,11 @@ __device__ void pair_slots_cta(const int32_t *__restrict__ ids, int P, int E, in
 }
 
 // Splits token row t into units once and writes them to each of its pairs'
-// (pass, slot) in the pass-packed layout: stage s = g / 4 of pass pi at
-// ((pi * ns + s) * kMaxTok + slot) * 64 + (g % 4) * 16 uint4, the factor at
-// ((pi * ns + s) * kMaxTok + slot) * 4 + g % 4.
+// (pass, slot) in the pass-packed layout: in block (pi * ns + g / 4) of
+// kPackedStage bytes, the factor at float slot * 4 + g % 4 and the units at
+// byte 128 + slot * 1024 + (g % 4) * 256.
 __device__ void split_row_packed_cta(const float *__restrict__ row, int K, int k,
-                                     const int *pass, const int *slot, uint4 *pk, float *pf) {
+                                     const int *pass, const int *slot, uint8_t *pk) {
     __shared__ float buf[32][64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = K / kGroup, ns = G / 4;
     for (int g = warp; g < G; g += blockDim.x >> 5) {
@@ -248,9 +248,10 @@ __device__ void split_row_packed_cta(const float *__restrict__ row, int K, int k
         const uint4 u = make_unit<false>(buf[warp], lane & 15);
         for (int j = lane >> 4; j < k; j += 2) {
             if (pass[j] < 0) continue;
-            const size_t c = ((size_t)pass[j] * ns + g / 4) * kMaxTok + slot[j];
-            pk[c * 64 + (g % 4) * 16 + (lane & 15)] = u;
-            if ((lane & 15) == 0) pf[c * 4 + g % 4] = ldexpf(1.0f, -e);
+            uint8_t *blk = pk + ((size_t)pass[j] * ns + g / 4) * kPackedStage;
+            reinterpret_cast<uint4 *>(blk + 128 + slot[j] * 1024 + (g % 4) * 256)[lane & 15] = u;
+            if ((lane & 15) == 0)
+                reinterpret_cast<float *>(blk)[slot[j] * 4 + g % 4] = ldexpf(1.0f, -e);
         }
         __syncwarp();
     }
@@ -270,7 +271,8 @@ __global__ void __launch_bounds__(1024)
         __shared__ int pass[32], slot[32];
         const int t = blockIdx.x - 1;
         pair_slots_cta(ids, P, E, k, t, pass_tok, pass, slot);
-        split_row_packed_cta(x + (size_t)t * H, H, k, pass, slot, xcells, xfac);
+        split_row_packed_cta(x + (size_t)t * H, H, k, pass, slot,
+                             reinterpret_cast<uint8_t *>(xcells));
     } else {
         const int t = blockIdx.x - 1;
         const int G = H / kGroup;
@@ -682,10 +684,8 @@ MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k) {
     const size_t pm = std::min(P, (P + kMaxTok - 1) / kMaxTok + std::min((size_t)E, P));
     L.pmax = (int)pm;
     const size_t sh = (size_t)H / (4 * kGroup), si = (size_t)I / (4 * kGroup);  // stages
-    L.xpk = o; o = align256(o + pm * sh * kMaxTok * 1024);
-    L.xpf = o; o = align256(o + pm * sh * kMaxTok * 16);
-    L.hpk = o; o = align256(o + pm * si * kMaxTok * 1024);
-    L.hpf = o; o = align256(o + pm * si * kMaxTok * 16);
+    L.xpk = o; o = align256(o + pm * sh * kPackedStage);
+    L.hpk = o; o = align256(o + pm * si * kPackedStage);
     L.total = o;
     return L;
 }

@@ -50,9 +50,11 @@ constexpr int kTStageW = kTRows * 128;               // 32 KB of packed weights
 constexpr int kTStageS = kTRows * 16;                // 4 KB of scales
 constexpr int kTActTok = 4 * 16 * 16;                // units of 4 groups, one token: 1 KB
 constexpr int kTFacTok = 16;                         // factors of 4 groups, one token
-constexpr int kTOffA = kTStageW + kTStageS;
-constexpr int kTOffF = kTOffA + kMaxTok * kTActTok;
-constexpr int kTStage = (kTOffF + kMaxTok * kTFacTok + 1023) / 1024 * 1024;  // 45 KB
+// factors, then units: the order of a pass-packed block (one copy)
+constexpr int kTOffF = kTStageW + kTStageS;
+constexpr int kTOffA = kTOffF + kMaxTok * kTFacTok;
+constexpr int kTStage = (kTOffA + kMaxTok * kTActTok + 1023) / 1024 * 1024;  // 45 KB
+static_assert(kTOffA - kTOffF + kMaxTok * kTActTok == kPackedStage, "pass-packed block layout");
 constexpr int kTGuJ = 128;                           // hidden units per gate+up item
 constexpr int kTDnRows = 256;                        // output rows per down item
 constexpr int kTEpi = (2 * kTGuJ * kMaxTok + kTConsumers * 64) * 4;
@@ -71,11 +73,11 @@ struct TmaArgs {
     int packed;          // activation units pass-packed (else per row)
     const int32_t *offsets, *list, *uexp, *n_used, *pass_ofs;
     const uint4 *cells;  // activation units: per row [row][G][16], or pass-packed
-                         // [pass][G/4][slot][64]
-    const float *cfac;   // their factors [row][G], or [pass][G/4][slot][4]
+                         // blocks of kPackedStage bytes [pass][G/4]
+    const float *cfac;   // their factors [row][G] (per-row layout only)
     float *h;            // gate+up: h fp32 [P][I]
-    uint4 *hcells;       // gate+up: units of h [P][I/64][16], or pass-packed
-    float *hfac;         // gate+up: factors of h [P][I/64], or pass-packed
+    uint4 *hcells;       // gate+up: units of h [P][I/64][16], or pass-packed blocks
+    float *hfac;         // gate+up: factors of h [P][I/64] (per-row layout only)
     float *y;            // down: y [P][H]
     int32_t *status;
     int32_t *cnt;        // per CTA: contributors done on the split item that starts in it
@@ -343,10 +345,12 @@ __device__ __forceinline__ void t_epilogue(const TmaArgs &a, const TShared &sh, 
             __syncwarp();
             if (a.packed) {
                 // down's pass pi, slot s (down groups the pairs as gate+up does)
-                const size_t c = ((size_t)pi * (Gd / 4) + gd / 4) * kMaxTok + s;
+                uint8_t *blk = reinterpret_cast<uint8_t *>(a.hcells) +
+                               ((size_t)pi * (Gd / 4) + gd / 4) * kPackedStage;
                 if (lane < 16)
-                    a.hcells[c * 64 + (gd % 4) * 16 + lane] = make_unit<false>(wbuf + warp * 64, lane);
-                if (lane == 0) a.hfac[c * 4 + gd % 4] = ldexpf(1.0f, -e);
+                    reinterpret_cast<uint4 *>(blk + 128 + s * 1024 + (gd % 4) * 256)[lane] =
+                        make_unit<false>(wbuf + warp * 64, lane);
+                if (lane == 0) reinterpret_cast<float *>(blk)[s * 4 + gd % 4] = ldexpf(1.0f, -e);
             } else {
                 const size_t cb = (size_t)sh.pairs[s] * Gd + gd;
                 if (lane < 16) a.hcells[cb * 16 + lane] = make_unit<false>(wbuf + warp * 64, lane);
@@ -479,12 +483,18 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
             const int rowB = a.mode == 0 ? a.I + tile * kTGuJ : tile * kTDnRows + 128;
             const uint32_t base = tc05::smem_addr(ring + slot * kTStage);
             const uint32_t fb = tc05::smem_addr(&sh.full[slot]);
-            mbar_expect_tx(&sh.full[slot],
-                           (uint32_t)(kTStageW + kTStageS + c.ntok * (kTActTok + kTFacTok)));
-            tma_load3(base, &a.wmap, kb * 128, rowA, c.e, fb);
-            tma_load3(base + 128 * 128, &a.wmap, kb * 128, rowB, c.e, fb);
-            tma_load3(base + kTStageW, &a.smap, kb * 4, rowA, c.e, fb);
-            tma_load3(base + kTStageW + 128 * 16, &a.smap, kb * 4, rowB, c.e, fb);
+            const uint32_t act = a.packed ? (uint32_t)(kMaxTok * kTFacTok + c.ntok * kTActTok)
+                                          : (uint32_t)(c.ntok * (kTActTok + kTFacTok));
+            mbar_expect_tx(&sh.full[slot], (uint32_t)(kTStageW + kTStageS) + act);
+            if (a.mode == 0) {  // gate and up rows: two 128-row boxes each
+                tma_load3(base, &a.wmap, kb * 128, rowA, c.e, fb);
+                tma_load3(base + 128 * 128, &a.wmap, kb * 128, rowB, c.e, fb);
+                tma_load3(base + kTStageW, &a.smap, kb * 4, rowA, c.e, fb);
+                tma_load3(base + kTStageW + 128 * 16, &a.smap, kb * 4, rowB, c.e, fb);
+            } else {            // 256 consecutive rows: one box each
+                tma_load3(base, &a.wmap, kb * 128, rowA, c.e, fb);
+                tma_load3(base + kTStageW, &a.smap, kb * 4, rowA, c.e, fb);
+            }
         };
         if (pre > 0) {
             int item = item0, kb = kb_0;
@@ -527,13 +537,14 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
             if (j >= pre && lane == 0) weights(slot, item, kb, pc);
             __syncwarp();
             if (a.packed) {
-                // the pass's token slots are contiguous: two copies per stage
+                // the pass's factors and its token slots' units are one block
                 if (lane == 0) {
                     const uint32_t base = tc05::smem_addr(ring + slot * kTStage);
                     const uint32_t fb = tc05::smem_addr(&sh.full[slot]);
-                    const size_t cs = ((size_t)pi * ns + kb) * kMaxTok;
-                    bulk_load(base + kTOffA, a.cells + cs * 64, pc.ntok * kTActTok, fb);
-                    bulk_load(base + kTOffF, a.cfac + cs * 4, pc.ntok * kTFacTok, fb);
+                    const uint8_t *blk = reinterpret_cast<const uint8_t *>(a.cells) +
+                                         ((size_t)pi * ns + kb) * kPackedStage;
+                    bulk_load(base + kTOffF, blk,
+                              (uint32_t)(kMaxTok * kTFacTok + pc.ntok * kTActTok), fb);
                 }
             } else if (lane < pc.ntok) {
                 const uint32_t base = tc05::smem_addr(ring + slot * kTStage);
@@ -615,20 +626,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool make_maps(TmaArgs &a, const uint8_t *wq, const float *ws, int E, int rows, int K) {
-    return encode_weight_maps(&a.wmap, &a.smap, wq, ws, E, rows, K);
+    return encode_weight_maps(&a.wmap, &a.smap, wq, ws, E, rows, K, a.mode == 0 ? 128 : 256);
 }
 
 }  // namespace
 
 bool encode_weight_maps(CUtensorMap *wmap, CUtensorMap *smap, const uint8_t *wq, const float *ws,
-                        int E, int rows, int K) {
+                        int E, int rows, int K, int box_rows) {
     auto enc = encode_fn();
     if (!enc) return false;
     const int G = K / kGroup;
     {
         cuuint64_t dims[3] = {(cuuint64_t)K / 2, (cuuint64_t)rows, (cuuint64_t)E};
         cuuint64_t strides[2] = {(cuuint64_t)K / 2, (cuuint64_t)rows * (K / 2)};
-        cuuint32_t box[3] = {128, 128, 1};
+        cuuint32_t box[3] = {128, (cuuint32_t)box_rows, 1};
         cuuint32_t es[3] = {1, 1, 1};
         if (enc(wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(wq), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -638,7 +649,7 @@ bool encode_weight_maps(CUtensorMap *wmap, CUtensorMap *smap, const uint8_t *wq,
     {
         cuuint64_t dims[3] = {(cuuint64_t)G, (cuuint64_t)rows, (cuuint64_t)E};
         cuuint64_t strides[2] = {(cuuint64_t)G * 4, (cuuint64_t)rows * G * 4};
-        cuuint32_t box[3] = {4, 128, 1};
+        cuuint32_t box[3] = {4, (cuuint32_t)box_rows, 1};
         cuuint32_t es[3] = {1, 1, 1};
         if (enc(smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ws), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
