@@ -174,13 +174,11 @@ template <int NB>
 struct GroupFrag {
     uint2 w0, w8;
     uint4 bu[NB][2];
-    float f[NB];
 };
 
 template <int NB, int GL>
 __device__ __forceinline__ void group_load(const uint8_t *wa, int pr, int q,
-                                           const uint4 *const bp0[NB], const float *const fp0[NB],
-                                           GroupFrag<NB> &g) {
+                                           const uint4 *const bp0[NB], GroupFrag<NB> &g) {
     const int off = (((2 * GL + (q >> 1)) ^ pr) << 4) + ((q & 1) << 3);
     g.w0 = *reinterpret_cast<const uint2 *>(wa + off);
     g.w8 = *reinterpret_cast<const uint2 *>(wa + 1024 + off);
@@ -188,19 +186,18 @@ __device__ __forceinline__ void group_load(const uint8_t *wa, int pr, int q,
     for (int nb = 0; nb < NB; ++nb) {
         g.bu[nb][0] = bp0[nb][GL * 16];
         g.bu[nb][1] = bp0[nb][GL * 16 + 8];
-        g.f[nb] = fp0[nb][GL];
     }
 }
 
 template <int NB, int GL>
 __device__ __forceinline__ void group_math(const GroupFrag<NB> &g, float s0, float s8,
-                                           float c[2][NB][2]) {
+                                           const float (&f)[NB][4], float c[2][NB][2]) {
     float d[NB][4];
     tile_group_int4<NB>(g.w0, g.w8, g.bu, d);
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-        c[GL & 1][nb][0] = fmaf(s0 * g.f[nb], d[nb][0] + d[nb][1], c[GL & 1][nb][0]);
-        c[GL & 1][nb][1] = fmaf(s8 * g.f[nb], d[nb][2] + d[nb][3], c[GL & 1][nb][1]);
+        c[GL & 1][nb][0] = fmaf(s0 * f[nb][GL], d[nb][0] + d[nb][1], c[GL & 1][nb][0]);
+        c[GL & 1][nb][1] = fmaf(s8 * f[nb][GL], d[nb][2] + d[nb][3], c[GL & 1][nb][1]);
     }
 }
 
@@ -210,18 +207,26 @@ __device__ __forceinline__ void compute_stage(const uint8_t *slot, int r0,
                                               const uint4 *const bp[NB],
                                               const float *const fp[NB], float c[2][NB][2]) {
     const int lane = threadIdx.x & 31, q = lane & 3, pr = tile_row(lane >> 2);
-    const float *s0 = reinterpret_cast<const float *>(slot + kTStageW) + (r0 + pr) * 4;
-    const float *s8 = s0 + 32;
+    // the four groups' scales of rows pr and pr + 8, and the four factors of
+    // each token block, are 16-byte vectors
+    const float4 s0 = reinterpret_cast<const float4 *>(slot + kTStageW)[r0 + pr];
+    const float4 s8 = reinterpret_cast<const float4 *>(slot + kTStageW)[r0 + pr + 8];
+    float f[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        const float4 v = *reinterpret_cast<const float4 *>(fp[nb]);
+        f[nb][0] = v.x; f[nb][1] = v.y; f[nb][2] = v.z; f[nb][3] = v.w;
+    }
     const uint8_t *wa = slot + (r0 + pr) * 128;
     GroupFrag<NB> g;
-    group_load<NB, 0>(wa, pr, q, bp, fp, g);
-    group_math<NB, 0>(g, s0[0], s8[0], c);
-    group_load<NB, 1>(wa, pr, q, bp, fp, g);
-    group_math<NB, 1>(g, s0[1], s8[1], c);
-    group_load<NB, 2>(wa, pr, q, bp, fp, g);
-    group_math<NB, 2>(g, s0[2], s8[2], c);
-    group_load<NB, 3>(wa, pr, q, bp, fp, g);
-    group_math<NB, 3>(g, s0[3], s8[3], c);
+    group_load<NB, 0>(wa, pr, q, bp, g);
+    group_math<NB, 0>(g, s0.x, s8.x, f, c);
+    group_load<NB, 1>(wa, pr, q, bp, g);
+    group_math<NB, 1>(g, s0.y, s8.y, f, c);
+    group_load<NB, 2>(wa, pr, q, bp, g);
+    group_math<NB, 2>(g, s0.z, s8.z, f, c);
+    group_load<NB, 3>(wa, pr, q, bp, g);
+    group_math<NB, 3>(g, s0.w, s8.w, f, c);
 }
 
 struct TShared {
