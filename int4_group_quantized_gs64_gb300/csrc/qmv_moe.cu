@@ -173,12 +173,14 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
     if (tid == 0 && bad) atomicOr(status, 1);
 }
 
-// Splits activation row r (1024 threads): per 64-wide group, max |v| ->
-// power-of-two factor -> 16 fp16 hi/lo cells (int4 register order).
-__device__ void split_row_cta(const float *__restrict__ row, int K, uint4 *cells, float *fac) {
+// Splits groups g0 .. g0 + 31 of activation row r (1024 threads, one group
+// a warp): per 64-wide group, max |v| -> power-of-two factor -> 16 fp16 hi/lo
+// cells (int4 register order).
+__device__ void split_row_cta(const float *__restrict__ row, int K, int g0, uint4 *cells,
+                              float *fac) {
     __shared__ float buf[32][64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = K / kGroup;
-    for (int g = warp; g < G; g += blockDim.x >> 5) {
+    for (int g = g0 + warp; g < min(G, g0 + 32); g += blockDim.x >> 5) {
         const float a = row[g * kGroup + lane], b = row[g * kGroup + 32 + lane];
         const int e = split_exponent(warp_max(fmaxf(fabsf(a), fabsf(b))));
         const float mul = ldexpf(1.0f, e);
@@ -234,11 +236,11 @@ __device__ void pair_slots_cta(const int32_t *__restrict__ ids, int P, int E, in
 // (pass, slot) in the pass-packed layout: in block (pi * ns + g / 4) of
 // kPackedStage bytes, the factor at float slot * 4 + g % 4 and the units at
 // byte 128 + slot * 1024 + (g % 4) * 256.
-__device__ void split_row_packed_cta(const float *__restrict__ row, int K, int k,
+__device__ void split_row_packed_cta(const float *__restrict__ row, int K, int g0, int k,
                                      const int *pass, const int *slot, uint8_t *pk) {
     __shared__ float buf[32][64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = K / kGroup, ns = G / 4;
-    for (int g = warp; g < G; g += blockDim.x >> 5) {
+    for (int g = g0 + warp; g < min(G, g0 + 32); g += blockDim.x >> 5) {
         const float a = row[g * kGroup + lane], b = row[g * kGroup + 32 + lane];
         const int e = split_exponent(warp_max(fmaxf(fabsf(a), fabsf(b))));
         const float mul = ldexpf(1.0f, e);
@@ -257,8 +259,9 @@ __device__ void split_row_packed_cta(const float *__restrict__ row, int K, int k
     }
 }
 
-// CTA 0 groups the pairs; CTA 1 + t splits token row t of x (per row, or
-// into the pass-packed layout when packed != 0).
+// CTA 0 groups the pairs; CTA 1 + t * C + c splits groups 32c .. 32c + 31
+// of token row t of x (C = ceil(H / 2048): one group a warp), per row or into
+// the pass-packed layout when packed != 0.
 __global__ void __launch_bounds__(1024)
     k_group_split(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets, int32_t *list,
                   int32_t *uexp, int32_t *n_used, int32_t *pass_ofs, int32_t *status,
@@ -267,16 +270,18 @@ __global__ void __launch_bounds__(1024)
     pdl_trigger();
     if (blockIdx.x == 0) {
         group_cta(ids, P, E, offsets, list, uexp, n_used, pass_ofs, status, pass_tok);
-    } else if (packed) {
-        __shared__ int pass[32], slot[32];
-        const int t = blockIdx.x - 1;
-        pair_slots_cta(ids, P, E, k, t, pass_tok, pass, slot);
-        split_row_packed_cta(x + (size_t)t * H, H, k, pass, slot,
-                             reinterpret_cast<uint8_t *>(xcells));
     } else {
-        const int t = blockIdx.x - 1;
-        const int G = H / kGroup;
-        split_row_cta(x + (size_t)t * H, H, xcells + (size_t)t * G * 16, xfac + (size_t)t * G);
+        const int G = H / kGroup, C = (G + 31) / 32;
+        const int t = (blockIdx.x - 1) / C, g0 = 32 * ((blockIdx.x - 1) % C);
+        if (packed) {
+            __shared__ int pass[32], slot[32];
+            pair_slots_cta(ids, P, E, k, t, pass_tok, pass, slot);
+            split_row_packed_cta(x + (size_t)t * H, H, g0, k, pass, slot,
+                                 reinterpret_cast<uint8_t *>(xcells));
+        } else {
+            split_row_cta(x + (size_t)t * H, H, g0, xcells + (size_t)t * G * 16,
+                          xfac + (size_t)t * G);
+        }
     }
 }
 
@@ -619,7 +624,8 @@ cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t 
                                int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
                                cudaStream_t st, int pass_tok, bool packed) {
-    return launch(k_group_split, dim3(x ? 1 + T : 1), dim3(1024), 0, st, false, ids, T * k, E,
+    const int C = (H / kGroup + 31) / 32;  // CTAs per token row
+    return launch(k_group_split, dim3(x ? 1 + T * C : 1), dim3(1024), 0, st, false, ids, T * k, E,
                   offsets, list, uexp, n_used, pass_ofs, status, x, H, static_cast<uint4 *>(xcells),
                   xfac, pass_tok, k, packed ? 1 : 0);
 }
