@@ -223,17 +223,14 @@ int moe_ffn_prepare(const qmv_moe_int4 *m, const float *x, int T, const int32_t 
     if (r) return r;
     if (!x || !ids) return QMV_EINVAL;
     if (!aligned(x, 4) || !aligned(ids, 4)) return QMV_EALIGN;
-    const cudaStream_t st = cs(stream);
     const bool pk = packed_units(m, k);
-    cudaError_t e = cudaMemsetAsync(at<int32_t>(ws, L.status), 0, L.status_bytes, st);
-    if (e == cudaSuccess)
-        e = qmv::launch_group_split(ids, T, k, m->E, at<int32_t>(ws, L.offsets),
-                                    at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
-                                    at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs),
-                                    at<int32_t>(ws, L.status), x, m->H,
-                                    at<void>(ws, pk ? L.xpk : L.xcells),
-                                    (pk ? nullptr : at<float>(ws, L.xfac)), st, 8, pk);
-    return from_cuda(e);
+    // the grouping kernel clears the status word and the split counters itself
+    return from_cuda(qmv::launch_group_split(
+        ids, T, k, m->E, at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list),
+        at<int32_t>(ws, L.uexp), at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs),
+        at<int32_t>(ws, L.status), x, m->H, at<void>(ws, pk ? L.xpk : L.xcells),
+        (pk ? nullptr : at<float>(ws, L.xfac)), cs(stream), 8, pk, at<int32_t>(ws, L.status),
+        (int)(L.status_bytes / 4), true));
 }
 
 int moe_ffn_gate_up(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,

@@ -40,11 +40,13 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int
                          int32_t *uexp, int32_t *n_used, int32_t *status, cudaStream_t st);
 // Grouping plus the split of the T activation rows, in one launch. With
 // packed == true the units go to the pass-packed layout (see MoeWorkspace)
-// instead of per-row cells.
+// instead of per-row cells; zero[0 .. nzero) is cleared first; pdl: launched
+// with programmatic dependent launch.
 cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
                                int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
-                               cudaStream_t st, int pass_tok = 8, bool packed = false);
+                               cudaStream_t st, int pass_tok = 8, bool packed = false,
+                               int32_t *zero = nullptr, int nzero = 0, bool pdl = false);
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
                           int32_t *pass_ofs, cudaStream_t st, bool pdl);
 // Activation rows [R][K] fp32 -> fragment cells [R][K/64][16] uint4 + factors [R][K/64].

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(32 * kRouteWarps)
     k_route(const float *__restrict__ logits, int T, int E, int k, int32_t *__restrict__ ids,
             float *__restrict__ w) {
     __shared__ float sl[kRouteWarps][1024];
+    pdl_trigger();  // a dependent launched with PDL waits for this grid before reading ids
     const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
     const int t = blockIdx.x * kRouteWarps + wl;
     if (t >= T) return;
@@ -261,14 +262,22 @@ __device__ void split_row_packed_cta(const float *__restrict__ row, int K, int g
 
 // CTA 0 groups the pairs; CTA 1 + t * C + c splits groups 32c .. 32c + 31
 // of token row t of x (C = ceil(H / 2048): one group a warp), per row or into
-// the pass-packed layout when packed != 0.
+// the pass-packed layout when packed != 0. CTA 0 first clears zero[0 ..
+// nzero) (the call's status word and split counters), which later kernels
+// read only after waiting for this one. Launched with programmatic dependent
+// launch, every CTA waits for the previous kernel (routing writes ids).
 __global__ void __launch_bounds__(1024)
     k_group_split(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets, int32_t *list,
                   int32_t *uexp, int32_t *n_used, int32_t *pass_ofs, int32_t *status,
                   const float *__restrict__ x, int H, uint4 *xcells, float *xfac, int pass_tok,
-                  int k, int packed) {
+                  int k, int packed, int32_t *zero, int nzero) {
+    pdl_wait();
     pdl_trigger();
     if (blockIdx.x == 0) {
+        if (zero) {
+            for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
+            __syncthreads();
+        }
         group_cta(ids, P, E, offsets, list, uexp, n_used, pass_ofs, status, pass_tok);
     } else {
         const int G = H / kGroup, C = (G + 31) / 32;
@@ -617,17 +626,18 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int
                          int32_t *uexp, int32_t *n_used, int32_t *status, cudaStream_t st) {
     return launch(k_group_split, dim3(1), dim3(1024), 0, st, false, ids, P, E, offsets, list, uexp,
                   n_used, (int32_t *)nullptr, status, (const float *)nullptr, 64,
-                  (uint4 *)nullptr, (float *)nullptr, (int)kMaxTok, 1, 0);
+                  (uint4 *)nullptr, (float *)nullptr, (int)kMaxTok, 1, 0, (int32_t *)nullptr, 0);
 }
 
 cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
                                int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
-                               cudaStream_t st, int pass_tok, bool packed) {
+                               cudaStream_t st, int pass_tok, bool packed, int32_t *zero,
+                               int nzero, bool pdl) {
     const int C = (H / kGroup + 31) / 32;  // CTAs per token row
-    return launch(k_group_split, dim3(x ? 1 + T * C : 1), dim3(1024), 0, st, false, ids, T * k, E,
+    return launch(k_group_split, dim3(x ? 1 + T * C : 1), dim3(1024), 0, st, pdl, ids, T * k, E,
                   offsets, list, uexp, n_used, pass_ofs, status, x, H, static_cast<uint4 *>(xcells),
-                  xfac, pass_tok, k, packed ? 1 : 0);
+                  xfac, pass_tok, k, packed ? 1 : 0, zero, nzero);
 }
 
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
