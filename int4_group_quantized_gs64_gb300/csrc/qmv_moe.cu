@@ -40,7 +40,12 @@ __global__ void __launch_bounds__(32 * kRouteWarps)
     k_route(const float *__restrict__ logits, int T, int E, int k, int32_t *__restrict__ ids,
             float *__restrict__ w) {
     __shared__ float sl[kRouteWarps][1024];
-    pdl_trigger();  // a dependent launched with PDL waits for this grid before reading ids
+    // Launched with programmatic dependent launch: the logits may come from
+    // the previous kernel and it may still read ids / w of an earlier call,
+    // so wait for it before touching either; a dependent launched the same
+    // way waits for this grid before reading ids.
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
     const int t = blockIdx.x * kRouteWarps + wl;
     if (t >= T) return;
@@ -619,7 +624,7 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids,
                          cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     return launch(k_route, dim3((T + kRouteWarps - 1) / kRouteWarps), dim3(32 * kRouteWarps), 0,
-                  st, false, logits, T, E, k, ids, w);
+                  st, true, logits, T, E, k, ids, w);
 }
 
 cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int32_t *list,
