@@ -533,6 +533,36 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     rows["int8_gemv_14336x4096"] = {"us": t * 1e6, "GBs": B8 / t / 1e9, "frac": B8 / t / 1e9 / peak,
                                     "bytes": B8, "launches_per_call": 2}
     del w8s, gs
+    # pair of int4 GEMVs sharing x (q_a + kv_a shape 6144 -> (2048, 576)), one token;
+    # 24 rotating weight copies (218 MB, above L2)
+    K2, N0, N1, C2 = 6144, 2048, 576, 24
+    pq = []
+    for c in range(C2):
+        rng = np.random.default_rng(100 + c)
+        pm = []
+        for N in (N0, N1):
+            wq = rng.integers(0, 256, size=(N, K2 // 2), dtype=np.uint8)
+            sc = (np.abs(rng.normal(0, 0.02, size=(N, K2 // 64))) + 1e-4).astype(np.float32)
+            pm += [torch.from_numpy(wq).to(dev), torch.from_numpy(sc).to(dev)]
+        pq.append(pm)
+    xp = torch.from_numpy(np.random.default_rng(7).normal(size=(1, K2)).astype(np.float32)).to(dev)
+    yp0 = torch.empty((1, N0), device=dev)
+    yp1 = torch.empty((1, N1), device=dev)
+    wsp = torch.empty(q.qmv_gemv_workspace_bytes(K2, 1), dtype=torch.uint8, device=dev)
+    gs = [graph_of(lambda: [q.qmv_int4_gs_pair(*pq[i], xp, y0=yp0, y1=yp1, ws=wsp, stream=stream)
+                            for i in range(C2)], stream)]
+    time_graphs(gs, 4, stream)
+    t = time_graphs(gs, 32, stream) / C2
+    gs = [graph_of(lambda: [(q.qmv_int4_gs(pq[i][0], pq[i][1], xp, y=yp0, ws=wsp, stream=stream),
+                             q.qmv_int4_gs(pq[i][2], pq[i][3], xp, y=yp1, ws=wsp, stream=stream))
+                            for i in range(C2)], stream)]
+    time_graphs(gs, 4, stream)
+    t2 = time_graphs(gs, 32, stream) / C2
+    Bp = (N0 + N1) * (K2 // 2 + K2 // 64 * 4) + K2 * 4 + (N0 + N1) * 4
+    rows["int4_gemv_pair_6144_2048_576"] = {"us": t * 1e6, "GBs": Bp / t / 1e9,
+                                            "frac": Bp / t / 1e9 / peak, "bytes": Bp,
+                                            "two_calls_us": t2 * 1e6, "launches_per_call": 2}
+    del pq, gs
     # MoE decode, 1 token, H 2048 / E 256 / I 512 (pool 453 MB)
     wl = W2
     wts = datagen.moe_weights(wl["E"], wl["H"], wl["I"])

@@ -81,7 +81,7 @@ size_t qmv_gemv_workspace_bytes(int K, int S);
  *   ws      device scratch of at least qmv_gemv_workspace_bytes(K, S) bytes,
  *           256-byte aligned, not shared with a concurrent call
  *   gs must be 64; K a multiple of 64; 1 <= N, 1 <= S, K <= 65536.
- * When N is a multiple of 256, K/64 a multiple of 4 and wq and scales are
+ * When N is a multiple of 16, K/64 a multiple of 4 and wq and scales are
  * 16-byte aligned, the weights stream through tensor-map (TMA) copies with
  * the row tiles' work shared evenly over all SMs; other shapes use per-warp
  * cp.async rings. Both give the same results up to fp32 summation order.
@@ -89,6 +89,23 @@ size_t qmv_gemv_workspace_bytes(int K, int S);
  *         QMV_EALIGN, QMV_EWORKSPACE, QMV_ECUDA. */
 int qmv_int4_gs(const uint8_t *wq, const float *scales, int N, int K, int gs, const float *x,
                 float *y, int S, void *ws, size_t ws_bytes, qmv_stream_t stream);
+
+/* Two int4-gs64 GEMVs against the same activations (colibri PR #418, commit
+ * "qmatmul staged-x length fix": matmul_pair stages x once for the q_a and
+ * kv_a projections, 6144 -> (2048, 576), and records both in one submit):
+ *     y0 = W0 x and y1 = W1 x, each exactly as qmv_int4_gs computes it
+ *   wq0 [N0][K/2] and wq1 [N1][K/2] uint8, 16-byte aligned
+ *   s0 [N0][K/gs], s1 [N1][K/gs] fp32; x [S][K]; y0 [S][N0]; y1 [S][N1] fp32
+ *   ws      device scratch of at least qmv_gemv_workspace_bytes(K, S) bytes
+ *           (the same as one GEMV), 256-byte aligned
+ * x is converted into fp16 hi/lo fragments once. When both matrices qualify
+ * for the tensor-map path (see qmv_int4_gs), the row tiles of both are one
+ * work sequence of a single launch; otherwise the two GEMVs run one after
+ * the other (the status word then reports the second).
+ * Errors: as qmv_int4_gs. */
+int qmv_int4_gs_pair(const uint8_t *wq0, const float *s0, int N0, const uint8_t *wq1,
+                     const float *s1, int N1, int K, int gs, const float *x, float *y0, float *y1,
+                     int S, void *ws, size_t ws_bytes, qmv_stream_t stream);
 
 /* Dense int8 per-row-scale GEMV (same commit, fmt 1):
  *     y[s][i] = row_scale[i] * sum_k w[i][k] * x[s][k]

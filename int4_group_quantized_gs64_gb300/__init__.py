@@ -61,6 +61,8 @@ def lib():
             "qmv_status_str": ([i32], ctypes.c_char_p),
             "qmv_gemv_workspace_bytes": ([i32, i32], sz),
             "qmv_int4_gs": ([vp, vp, i32, i32, i32, vp, vp, i32, vp, sz, vp], i32),
+            "qmv_int4_gs_pair": ([vp, vp, i32, vp, vp, i32, i32, i32, vp, vp, vp, i32, vp, sz, vp],
+                                 i32),
             "qmv_int8_row": ([vp, vp, i32, i32, vp, vp, i32, vp, sz, vp], i32),
             "moe_route_topk": ([vp, i32, i32, i32, vp, vp, vp], i32),
             "moe_group": ([vp, i32, i32, i32, vp, vp, vp, vp, vp, vp], i32),
@@ -137,6 +139,32 @@ def qmv_int4_gs(wq, scales, x, y=None, gs: int = 64, ws=None, stream=None):
     _check("qmv_int4_gs", lib().qmv_int4_gs(_ptr(wq), _ptr(scales), N, K, gs, _ptr(x2), _ptr(y), S,
                                             _ptr(ws), ws.numel(), _stream(stream)))
     return y
+
+
+def qmv_int4_gs_pair(wq0, s0, wq1, s1, x, y0=None, y1=None, gs: int = 64, ws=None, stream=None):
+    """(y0, y1) = (W0 . x, W1 . x) for two int4-gs64 matrices sharing x [S][K]."""
+    import torch
+    for t, n in ((wq0, "wq0"), (wq1, "wq1")):
+        _need(t, torch.uint8, n)
+    for t, n in ((s0, "s0"), (s1, "s1"), (x, "x")):
+        _need(t, torch.float32, n)
+    N0, K = wq0.shape[0], wq0.shape[1] * 2
+    N1 = wq1.shape[0]
+    if wq1.shape[1] * 2 != K:
+        raise QmvError("qmv_int4_gs_pair: the two matrices need the same K")
+    x2 = x.view(-1, K)
+    S = x2.shape[0]
+    if y0 is None:
+        y0 = torch.empty((S, N0), dtype=torch.float32, device=x.device)
+    if y1 is None:
+        y1 = torch.empty((S, N1), dtype=torch.float32, device=x.device)
+    _need(y0, torch.float32, "y0"); _need(y1, torch.float32, "y1")
+    if ws is None:
+        ws = _workspace(qmv_gemv_workspace_bytes(K, S), x.device)
+    _check("qmv_int4_gs_pair",
+           lib().qmv_int4_gs_pair(_ptr(wq0), _ptr(s0), N0, _ptr(wq1), _ptr(s1), N1, K, gs, _ptr(x2),
+                                  _ptr(y0), _ptr(y1), S, _ptr(ws), ws.numel(), _stream(stream)))
+    return y0, y1
 
 
 def qmv_int8_row(w, row_scale, x, y=None, ws=None, stream=None):

@@ -105,6 +105,20 @@ int qmv_int4_gs(const uint8_t *wq, const float *scales, int N, int K, int gs, co
     return from_cuda(qmv::launch_gemv_int4(wq, scales, N, K, x, y, S, ws, cs(stream)));
 }
 
+int qmv_int4_gs_pair(const uint8_t *wq0, const float *s0, int N0, const uint8_t *wq1,
+                     const float *s1, int N1, int K, int gs, const float *x, float *y0, float *y1,
+                     int S, void *ws, size_t ws_bytes, qmv_stream_t stream) {
+    if (!wq0 || !s0 || !wq1 || !s1 || !x || !y0 || !y1 || N0 < 1 || N1 < 1 || S < 1 || gs != 64)
+        return QMV_EINVAL;
+    if (K < 64 || K % 64 || K > kMaxK) return QMV_ESHAPE;
+    if (!aligned(wq0, 16) || !aligned(wq1, 16) || !aligned(s0, 4) || !aligned(s1, 4) ||
+        !aligned(x, 4) || !aligned(y0, 4) || !aligned(y1, 4))
+        return QMV_EALIGN;
+    if (!ws || !aligned(ws, 256) || ws_bytes < qmv_gemv_workspace_bytes(K, S)) return QMV_EWORKSPACE;
+    return from_cuda(
+        qmv::launch_gemv_int4_pair(wq0, s0, N0, wq1, s1, N1, K, x, y0, y1, S, ws, cs(stream)));
+}
+
 int qmv_int8_row(const int8_t *w, const float *row_scale, int N, int K, const float *x, float *y,
                  int S, void *ws, size_t ws_bytes, qmv_stream_t stream) {
     if (!w || !row_scale || !x || !y || N < 1 || S < 1) return QMV_EINVAL;

@@ -314,6 +314,25 @@ cudaError_t launch_gemv_int4(const uint8_t *wq, const float *scales, int N, int 
     return launch_dense_tma(wq, scales, N, K, S, cells, fac, y, head, head + 1, part, st);
 }
 
+cudaError_t launch_gemv_int4_pair(const uint8_t *wq0, const float *s0, int N0, const uint8_t *wq1,
+                                  const float *s1, int N1, int K, const float *x, float *y0,
+                                  float *y1, int S, void *ws, cudaStream_t st) {
+    if (!tma_dense_supported(wq0, s0, N0, K) || !tma_dense_supported(wq1, s1, N1, K)) {
+        cudaError_t e = launch_gemv_int4(wq0, s0, N0, K, x, y0, S, ws, st);
+        return e == cudaSuccess ? launch_gemv_int4(wq1, s1, N1, K, x, y1, S, ws, st) : e;
+    }
+    char *b = static_cast<char *>(ws);
+    int32_t *head = reinterpret_cast<int32_t *>(b);
+    void *cells = b + kGemvHead;
+    float *fac = reinterpret_cast<float *>(b + kGemvHead + (size_t)S * K * 4);
+    float *part = reinterpret_cast<float *>(b + gemv_part_offset(K, S));
+    cudaError_t e = launch(k_split<false>, dim3(S, (K / kGroup + 7) / 8), dim3(256), 0, st, false,
+                           x, K, static_cast<uint4 *>(cells), fac, head, 1 + kSkMaxCtas);
+    if (e != cudaSuccess) return e;
+    return launch_dense_tma(wq0, s0, N0, K, S, cells, fac, y0, head, head + 1, part, st, wq1, s1,
+                            N1, y1);
+}
+
 cudaError_t launch_gemv_int8(const int8_t *w, const float *row_scale, int N, int K,
                              const float *x, float *y, int S, void *ws, cudaStream_t st) {
     char *b = static_cast<char *>(ws);

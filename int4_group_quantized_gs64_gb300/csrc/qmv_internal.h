@@ -25,6 +25,11 @@ cudaError_t launch_gemv_int4(const uint8_t *wq, const float *scales, int N, int 
                              float *y, int S, void *ws, cudaStream_t st);
 cudaError_t launch_gemv_int8(const int8_t *w, const float *row_scale, int N, int K,
                              const float *x, float *y, int S, void *ws, cudaStream_t st);
+// Two int4 GEMVs against the same x: one activation split; one launch when
+// both matrices take the tensor-map kernel, else two.
+cudaError_t launch_gemv_int4_pair(const uint8_t *wq0, const float *s0, int N0, const uint8_t *wq1,
+                                  const float *s1, int N1, int K, const float *x, float *y0,
+                                  float *y1, int S, void *ws, cudaStream_t st);
 
 struct MoeDims {
     const uint8_t *gu_q;
@@ -90,9 +95,13 @@ bool tma_moe_supported(const MoeDims &m);
 bool encode_weight_maps(CUtensorMap *wmap, CUtensorMap *smap, const uint8_t *wq, const float *ws,
                         int E, int rows, int K, int box_rows = 128);
 bool tma_dense_supported(const uint8_t *wq, const float *scales, int N, int K);
+// wq2 != null: a second matrix [N2][K/2] against the same activations, its
+// row tiles after the first's in the same launch, output y2 [S][N2].
 cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int K, int S,
                              const void *cells, const float *cfac, float *y, int32_t *status,
-                             int32_t *cnt, float *part, cudaStream_t st);
+                             int32_t *cnt, float *part, cudaStream_t st,
+                             const uint8_t *wq2 = nullptr, const float *scales2 = nullptr,
+                             int N2 = 0, float *y2 = nullptr);
 // packed: the activation units (cells, cfac) and, for gate+up, the units of
 // h it writes (hcells, hfac) are in the pass-packed layout; else per row.
 cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const float *cfac, int k,

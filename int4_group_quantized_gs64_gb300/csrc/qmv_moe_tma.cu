@@ -67,6 +67,10 @@ static_assert(kSkPartFloats == 2 * kTRows * kMaxTok, "partial-sum slots must mat
 struct TmaArgs {
     CUtensorMap wmap;    // weights: uint8 [E][rows][K/2], box 128 B x 128 rows, 128B swizzle
     CUtensorMap smap;    // scales: f32 [E][rows][K/64], box 4 x 128 rows
+    CUtensorMap wmap2;   // dense pair: the second matrix's maps (row tiles tiles0 ..)
+    CUtensorMap smap2;
+    int H2, tiles0;      // dense pair: rows of the second matrix, row tiles of the first
+    float *y2;           // dense pair: its output [S][H2]
     int mode;            // 0: gate+up, 1: down, 2: dense GEMV (one matrix, tokens 0..S-1)
     int G, I, H, k;
     int S;               // dense: tokens
@@ -287,13 +291,14 @@ __device__ __forceinline__ void t_epilogue(const TmaArgs &a, const TShared &sh, 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3;
     const int pr = tile_row(lane >> 2);
     if (a.mode != 0) {
-        const int H = a.H;
-        const int r0 = tile * kTDnRows + 16 * warp + pr;
+        const bool second = tile >= a.tiles0;  // dense pair: the second matrix
+        const int H = second ? a.H2 : a.H;
+        const int r0 = (second ? tile - a.tiles0 : tile) * kTDnRows + 16 * warp + pr;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
             const int s = 4 * nb + q;
             if (s < ntok) {
-                float *yb = a.y + (size_t)sh.pairs[s] * H;
+                float *yb = (second ? a.y2 : a.y) + (size_t)sh.pairs[s] * H;
                 if (r0 < H) yb[r0] = acc[nb][0];
                 if (r0 + 8 < H) yb[r0 + 8] = acc[nb][1];
             }
@@ -462,7 +467,8 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
     pdl_trigger();
 
     const int nu = a.mode == 2 ? 1 : *a.n_used;
-    const int tiles = a.mode == 0 ? (a.I + kTGuJ - 1) / kTGuJ : (a.H + kTDnRows - 1) / kTDnRows;
+    const int tiles = a.mode == 0 ? (a.I + kTGuJ - 1) / kTGuJ
+                                  : a.tiles0 + (a.H2 + kTDnRows - 1) / kTDnRows;
     const int passes = a.mode == 2 ? (a.S + kMaxTok - 1) / kMaxTok : (nu > 0 ? a.pass_ofs[nu] : 0);
     const int total_items = passes * tiles;
     const int ns = a.G / 4;
@@ -496,9 +502,13 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
                 tma_load3(base + 128 * 128, &a.wmap, kb * 128, rowB, c.e, fb);
                 tma_load3(base + kTStageW, &a.smap, kb * 4, rowA, c.e, fb);
                 tma_load3(base + kTStageW + 128 * 16, &a.smap, kb * 4, rowB, c.e, fb);
-            } else {            // 256 consecutive rows: one box each
+            } else if (tile < a.tiles0) {  // 256 consecutive rows: one box each
                 tma_load3(base, &a.wmap, kb * 128, rowA, c.e, fb);
                 tma_load3(base + kTStageW, &a.smap, kb * 4, rowA, c.e, fb);
+            } else {                       // the second matrix of a dense pair
+                const int r2 = (tile - a.tiles0) * kTDnRows;
+                tma_load3(base, &a.wmap2, kb * 128, r2, 0, fb);
+                tma_load3(base + kTStageW, &a.smap2, kb * 4, r2, 0, fb);
             }
         };
         if (pre > 0) {
@@ -694,6 +704,7 @@ cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const 
     a.status = status;
     a.cnt = cnt;
     a.part = part;
+    a.tiles0 = (m.H + kTDnRows - 1) / kTDnRows;  // down: every row tile is the first matrix's
     bool ok;
     if (mode == 0) {
         a.G = m.H / kGroup;
@@ -711,19 +722,24 @@ cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const 
 
 bool tma_dense_supported(const uint8_t *wq, const float *scales, int N, int K) {
     auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-    return encode_fn() != nullptr && N % kTDnRows == 0 && (K / kGroup) % 4 == 0 && a16(wq) &&
+    // a partial last row tile reads zeros past row N and writes nothing there
+    return encode_fn() != nullptr && N % 16 == 0 && (K / kGroup) % 4 == 0 && a16(wq) &&
            a16(scales);
 }
 
+// Dense mode over one matrix, or a pair sharing the activations (wq2 != null):
+// the row tiles of both form one item sequence.
 cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int K, int S,
                              const void *cells, const float *cfac, float *y, int32_t *status,
-                             int32_t *cnt, float *part, cudaStream_t st) {
+                             int32_t *cnt, float *part, cudaStream_t st, const uint8_t *wq2,
+                             const float *scales2, int N2, float *y2) {
     TmaArgs a;
     memset(&a, 0, sizeof(a));
     a.mode = 2;
     a.H = N;
     a.S = S;
     a.G = K / kGroup;
+    a.tiles0 = (N + kTDnRows - 1) / kTDnRows;
     a.cells = static_cast<const uint4 *>(cells);
     a.cfac = cfac;
     a.y = y;
@@ -731,6 +747,12 @@ cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int 
     a.cnt = cnt;
     a.part = part;
     if (!make_maps(a, wq, scales, 1, N, K)) return cudaErrorInvalidValue;
+    if (wq2) {
+        a.H2 = N2;
+        a.y2 = y2;
+        if (!encode_weight_maps(&a.wmap2, &a.smap2, wq2, scales2, 1, N2, K, 256))
+            return cudaErrorInvalidValue;
+    }
     cudaError_t e = set_smem(k_moe_tma, kTSmem);
     if (e != cudaSuccess) return e;
     const int grid = std::min(kSkMaxCtas, sm_count() * max_ctas_per_sm(k_moe_tma, kTThreads, kTSmem));

@@ -86,6 +86,33 @@ def test_int4_tma_shapes(N, K, S):
         assert norm_err(y.cpu().numpy(), ref, den) <= TOL_FP32
 
 
+# Pairs of matrices against one x: the pages' q_a + kv_a shape 6144 -> (2048, 576),
+# ragged last row tiles (N not a multiple of 256), several token passes, and
+# a pair that does not qualify for the tensor-map kernel (two GEMVs).
+PAIR_SHAPES = [(2048, 576, 6144, 1), (256, 256, 256, 1), (512, 48, 1024, 3), (1024, 1040, 2048, 9),
+               (100, 36, 192, 2)]
+
+
+@pytest.mark.parametrize("N0,N1,K,S", PAIR_SHAPES)
+def test_int4_pair(N0, N1, K, S):
+    rng = np.random.default_rng(N0 + 3 * N1 + K + S)
+    mats = []
+    for N in (N0, N1):
+        wq = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+        sc = (np.abs(rng.normal(0, 0.02, size=(N, K // 64))) + 1e-4).astype(np.float32)
+        mats.append((wq, sc))
+    x = rng.normal(size=(S, K)).astype(np.float32)
+    ws = torch.full((q.qmv_gemv_workspace_bytes(K, S),), 0xFF, dtype=torch.uint8, device="cuda")
+    for _ in range(2):  # the second call reuses the workspace left by the first
+        y0, y1 = q.qmv_int4_gs_pair(dev(mats[0][0]), dev(mats[0][1]), dev(mats[1][0]),
+                                    dev(mats[1][1]), dev(x), ws=ws)
+        torch.cuda.synchronize()
+        assert int(ws[:4].view(torch.int32).cpu()[0]) == 0
+        for y, (wq, sc) in zip((y0, y1), mats):
+            ref, den = oracle.qmv_int4_gs(wq, sc, x, 64, with_den=True)
+            assert norm_err(y.cpu().numpy(), ref, den) <= TOL_FP32
+
+
 @pytest.mark.parametrize("N,K,S", SHAPES)
 def test_int8_shapes(N, K, S):
     rng = np.random.default_rng(N * 31 + K + S)
