@@ -223,6 +223,24 @@ int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int3
                         const float *w, int k, float *out, void *ws, size_t ws_bytes,
                         qmv_stream_t stream);
 
+/* moe_expert_ffn_int4 over the resident experts only (colibri PR #418,
+ * "Vulkan expert tier ... overlapped with CPU rows": the GPU computes the
+ * experts of its registry while the CPU computes the rest; PR #1338,
+ * "Validation": a miss returns no mask bit):
+ *     out[t] = sum over served slots j of w[t][j] * down_e(SiLU(gate_e x[t]) * up_e x[t])
+ *     served[t][j] = 1 if e = ids[t][j] is in [0, E) and bit e % 32 of
+ *                    resident[e / 32] is set, else 0
+ *   resident  device bitmap [ceil(E / 32)] uint32, 4-byte aligned
+ *   served    device [T][k] uint8, written
+ *   others and the workspace as moe_expert_ffn_int4. A token with no served
+ *   slot gets out[t] = 0. The caller adds the unserved slots' terms itself.
+ *   A non-resident id is not an error; status bit 0 still flags ids outside
+ *   [0, E). Errors: those of moe_expert_ffn_int4, plus QMV_EINVAL for a null
+ *   resident or served and QMV_EALIGN for a misaligned resident. */
+int moe_expert_ffn_int4_resident(const qmv_moe_int4 *m, const uint32_t *resident, const float *x,
+                                 int T, const int32_t *ids, const float *w, int k, float *out,
+                                 uint8_t *served, void *ws, size_t ws_bytes, qmv_stream_t stream);
+
 /* The four phases of moe_expert_ffn_int4, for callers that interleave other
  * work or time the phases (the pages split their expert group the same way
  * into issue and take). All four take the same workspace; each phase reads

@@ -77,6 +77,7 @@ def lib():
             "moe_ffn_combine": ([P, vp, vp, i32, i32, vp, vp, sz, vp], i32),
             "moe_weight_path": ([P], i32),
             "moe_one_token_path": ([P, i32], i32),
+            "moe_expert_ffn_int4_resident": ([P, vp, vp, i32, vp, vp, i32, vp, vp, vp, sz, vp], i32),
             "moe_prefill_workspace_bytes": ([P, i32, i32], sz),
             "moe_expert_ffn_int4_prefill": ([P, vp, i32, vp, vp, i32, vp, vp, sz, vp], i32),
         }
@@ -304,6 +305,29 @@ def moe_expert_ffn_int4(m: MoeInt4Weights, x, ids, w, out=None, ws=None, stream=
         m.desc, _ptr(x), T, _ptr(ids), _ptr(w), k, _ptr(out), _ptr(ws), ws.numel(),
         _stream(stream)))
     return out
+
+
+def moe_expert_ffn_int4_resident(m: MoeInt4Weights, resident, x, ids, w, out=None, served=None,
+                                 ws=None, stream=None):
+    """As moe_expert_ffn_int4 over the experts set in the bitmap ``resident``
+    (int32 [ceil(E/32)], bit e%32 of word e/32); returns (out, served uint8 [T][k])."""
+    import torch
+    _need(x, torch.float32, "x"); _need(ids, torch.int32, "ids"); _need(w, torch.float32, "w")
+    _need(resident, torch.int32, "resident")
+    if resident.numel() * 32 < m.E:
+        raise QmvError("moe_expert_ffn_int4_resident: the bitmap needs ceil(E/32) words")
+    T, k = ids.shape
+    if out is None:
+        out = torch.empty((T, m.H), dtype=torch.float32, device=x.device)
+    if served is None:
+        served = torch.empty((T, k), dtype=torch.uint8, device=x.device)
+    _need(served, torch.uint8, "served")
+    if ws is None:
+        ws = _workspace(moe_workspace_bytes(m, T, k), x.device)
+    _check("moe_expert_ffn_int4_resident", lib().moe_expert_ffn_int4_resident(
+        m.desc, _ptr(resident), _ptr(x), T, _ptr(ids), _ptr(w), k, _ptr(out), _ptr(served),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return out, served
 
 
 def moe_ffn_prepare(m: MoeInt4Weights, x, ids, ws, stream=None):

@@ -230,8 +230,14 @@ int moe_combine(const float *y, const int32_t *ids, const float *w, int T, int k
     return from_cuda(qmv::launch_combine(y, ids, w, T, k, E, H, out, cs(stream), false));
 }
 
-int moe_ffn_prepare(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids, int k,
-                    void *ws, size_t ws_bytes, qmv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The prepare phase with an optional residency bitmap and served mask.
+int prepare_impl(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids, int k,
+                 void *ws, size_t ws_bytes, qmv_stream_t stream, const uint32_t *res,
+                 uint8_t *served) {
     qmv::MoeWorkspace L;
     int r = ffn_check(m, T, k, ws, ws_bytes, L);
     if (r) return r;
@@ -244,7 +250,21 @@ int moe_ffn_prepare(const qmv_moe_int4 *m, const float *x, int T, const int32_t 
         at<int32_t>(ws, L.uexp), at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs),
         at<int32_t>(ws, L.status), x, m->H, at<void>(ws, pk ? L.xpk : L.xcells),
         (pk ? nullptr : at<float>(ws, L.xfac)), cs(stream), 8, pk, at<int32_t>(ws, L.status),
-        (int)(L.status_bytes / 4), true));
+        (int)(L.status_bytes / 4), true, res, served));
+}
+
+// Whole FFN (moe_expert_ffn_int4 with res == served == null).
+int ffn_impl(const qmv_moe_int4 *m, const uint32_t *res, const float *x, int T,
+             const int32_t *ids, const float *w, int k, float *out, uint8_t *served, void *ws,
+             size_t ws_bytes, qmv_stream_t stream);
+
+}  // namespace
+
+extern "C" {
+
+int moe_ffn_prepare(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids, int k,
+                    void *ws, size_t ws_bytes, qmv_stream_t stream) {
+    return prepare_impl(m, x, T, ids, k, ws, ws_bytes, stream, nullptr, nullptr);
 }
 
 int moe_ffn_gate_up(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
@@ -315,28 +335,52 @@ int moe_one_token_path(const qmv_moe_int4 *m, int k) {
 int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids,
                         const float *w, int k, float *out, void *ws, size_t ws_bytes,
                         qmv_stream_t stream) {
+    return ffn_impl(m, nullptr, x, T, ids, w, k, out, nullptr, ws, ws_bytes, stream);
+}
+
+int moe_expert_ffn_int4_resident(const qmv_moe_int4 *m, const uint32_t *resident, const float *x,
+                                 int T, const int32_t *ids, const float *w, int k, float *out,
+                                 uint8_t *served, void *ws, size_t ws_bytes, qmv_stream_t stream) {
+    if (!resident || !served) return QMV_EINVAL;
+    if (!aligned(resident, 4)) return QMV_EALIGN;
+    return ffn_impl(m, resident, x, T, ids, w, k, out, served, ws, ws_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int ffn_impl(const qmv_moe_int4 *m, const uint32_t *res, const float *x, int T,
+             const int32_t *ids, const float *w, int k, float *out, uint8_t *served, void *ws,
+             size_t ws_bytes, qmv_stream_t stream) {
     if (T == 0 && !check_moe(m) && k >= 1 && k <= m->E) return QMV_OK;
     qmv::MoeWorkspace L;
     int r = ffn_check(m, T, k, ws, ws_bytes, L);
     if (r) return r;
     if (!x || !ids || !w || !out) return QMV_EINVAL;
     if (!aligned(x, 4) || !aligned(ids, 4) || !aligned(w, 4) || !aligned(out, 4)) return QMV_EALIGN;
+    const cudaStream_t st = cs(stream);
     if (T == 1 && one_token(m, k)) {
         // one token: a single cooperative launch after clearing the status
         // word and the counters (the first counter is its grid barrier)
-        const cudaStream_t st = cs(stream);
         cudaError_t e = cudaMemsetAsync(at<int32_t>(ws, L.status), 0, L.status_bytes, st);
         if (e == cudaSuccess)
             e = qmv::launch_moe_one(dims(m), x, ids, w, k, at<float>(ws, L.h), out,
                                     at<int32_t>(ws, L.status),
-                                    reinterpret_cast<unsigned int *>(at<int32_t>(ws, L.sk_cnt)), st);
+                                    reinterpret_cast<unsigned int *>(at<int32_t>(ws, L.sk_cnt)), st,
+                                    res, served);
         return from_cuda(e);
     }
-    if ((r = moe_ffn_prepare(m, x, T, ids, k, ws, ws_bytes, stream))) return r;
+    if ((r = prepare_impl(m, x, T, ids, k, ws, ws_bytes, stream, res, served))) return r;
     if ((r = moe_ffn_gate_up(m, T, k, ws, ws_bytes, stream))) return r;
     if ((r = moe_ffn_down(m, T, k, ws, ws_bytes, stream))) return r;
-    return moe_ffn_combine(m, ids, w, T, k, out, ws, ws_bytes, stream);
+    return from_cuda(qmv::launch_combine(at<float>(ws, L.y), ids, w, T, k, m->E, m->H, out, st,
+                                         true, res));
 }
+
+}  // namespace
+
+extern "C" {
 
 size_t moe_prefill_workspace_bytes(const qmv_moe_int4 *m, int T, int k) {
     if (check_moe(m) || m->I % 128 || T < 0 || k < 1 || (int64_t)T * k > kMaxPairs) return 0;

@@ -51,7 +51,8 @@ cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t 
                                int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
                                cudaStream_t st, int pass_tok = 8, bool packed = false,
-                               int32_t *zero = nullptr, int nzero = 0, bool pdl = false);
+                               int32_t *zero = nullptr, int nzero = 0, bool pdl = false,
+                               const uint32_t *res = nullptr, uint8_t *served = nullptr);
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
                           int32_t *pass_ofs, cudaStream_t st, bool pdl);
 // Activation rows [R][K] fp32 -> fragment cells [R][K/64][16] uint4 + factors [R][K/64].
@@ -64,7 +65,8 @@ cudaError_t launch_down(const MoeDims &m, const void *hcells, const float *hfac,
                         const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                         const int32_t *n_used, const int32_t *pass_ofs, float *y, cudaStream_t st);
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int T, int k, int E,
-                           int H, float *out, cudaStream_t st, bool pdl);
+                           int H, float *out, cudaStream_t st, bool pdl,
+                           const uint32_t *res = nullptr);
 
 // Prefill (tcgen05): mode 0 = gate+up+SiLU (B = x bf16 rows, writes h bf16),
 // mode 1 = down (B = h bf16 rows, writes y fp32). Passes of prefill_pass_tokens().
@@ -115,7 +117,8 @@ cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const 
 bool moe_one_supported(const MoeDims &m, int k);
 cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids, const float *w,
                            int k, float *h, float *out, int32_t *status, unsigned int *bar,
-                           cudaStream_t st);
+                           cudaStream_t st, const uint32_t *res = nullptr,
+                           uint8_t *served = nullptr);
 
 // Workspace layout of the MoE entry points (256-byte aligned segments). The
 // status word and the split counters (kSkMaxCtas for gate+up, then kSkMaxCtas

@@ -127,9 +127,13 @@ __device__ __forceinline__ void block_scan3(int a, int b, int c, int &ea, int &e
 // give the offsets, the slots of the used experts and the pass offsets (one
 // pass = up to kMaxTok pairs of one expert); a single warp then fills the
 // lists in pair order (ranks from __match_any_sync), keeping them ascending.
+// res: bitmap of the experts this call serves (bit e % 32 of word e / 32), or
+// null for all; pairs of other experts are left out of the lists without
+// error. served (if not null): 1 for each pair that is grouped, else 0.
 __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets,
                           int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
-                          int32_t *status, int pass_tok) {
+                          int32_t *status, int pass_tok, const uint32_t *res = nullptr,
+                          uint8_t *served = nullptr) {
     __shared__ int32_t cnt[1024], run[1024], tot[96];
     __shared__ int bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -138,8 +142,10 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
     __syncthreads();
     for (int p = tid; p < P; p += blockDim.x) {
         const int e = ids[p];
-        if (e < 0 || e >= E) bad = 1;
-        else atomicAdd(&cnt[e], 1);
+        const bool in = e >= 0 && e < E;
+        if (!in) bad = 1;
+        else if (expert_served(res, e)) atomicAdd(&cnt[e], 1);
+        if (served) served[p] = in && expert_served(res, e) ? 1 : 0;
     }
     __syncthreads();
     const int c = tid < E ? cnt[tid] : 0;
@@ -166,7 +172,7 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
         for (int base = 0; base < P; base += 32) {
             const int p = base + lane;
             int e = p < P ? ids[p] : -1;
-            const bool valid = p < P && e >= 0 && e < E;
+            const bool valid = p < P && e >= 0 && e < E && expert_served(res, e);
             if (!valid) e = -1 - lane;  // unique key: never matches another lane
             const unsigned mask = __match_any_sync(0xFFFFFFFFu, e);
             const int rank = __popc(mask & lt);
@@ -205,19 +211,19 @@ __device__ void split_row_cta(const float *__restrict__ row, int K, int g0, uint
 // expert from counting the earlier pairs with that expert (the lists are in
 // pair order). pass[j] = -1 for an id outside [0, E).
 __device__ void pair_slots_cta(const int32_t *__restrict__ ids, int P, int E, int k, int t,
-                               int pass_tok, int *pass, int *slot) {
+                               int pass_tok, int *pass, int *slot, const uint32_t *res) {
     __shared__ int32_t cnt[1024], pofs[1024], tot[96], rank[32], eid[32];
     const int tid = threadIdx.x;
     cnt[tid] = 0;
     if (tid < k) {
         const int e = ids[(size_t)t * k + tid];
-        eid[tid] = (e >= 0 && e < E) ? e : -1;
+        eid[tid] = (e >= 0 && e < E && expert_served(res, e)) ? e : -1;
         rank[tid] = 0;
     }
     __syncthreads();
     for (int p = tid; p < P; p += blockDim.x) {
         const int e = ids[p];
-        if (e >= 0 && e < E) {
+        if (e >= 0 && e < E && expert_served(res, e)) {
             atomicAdd(&cnt[e], 1);
             for (int j = 0; j < k; ++j)
                 if (e == eid[j] && p < t * k + j) atomicAdd(&rank[j], 1);
@@ -275,7 +281,8 @@ __global__ void __launch_bounds__(1024)
     k_group_split(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets, int32_t *list,
                   int32_t *uexp, int32_t *n_used, int32_t *pass_ofs, int32_t *status,
                   const float *__restrict__ x, int H, uint4 *xcells, float *xfac, int pass_tok,
-                  int k, int packed, int32_t *zero, int nzero) {
+                  int k, int packed, int32_t *zero, int nzero, const uint32_t *res,
+                  uint8_t *served) {
     pdl_wait();
     pdl_trigger();
     if (blockIdx.x == 0) {
@@ -283,13 +290,13 @@ __global__ void __launch_bounds__(1024)
             for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
             __syncthreads();
         }
-        group_cta(ids, P, E, offsets, list, uexp, n_used, pass_ofs, status, pass_tok);
+        group_cta(ids, P, E, offsets, list, uexp, n_used, pass_ofs, status, pass_tok, res, served);
     } else {
         const int G = H / kGroup, C = (G + 31) / 32;
         const int t = (blockIdx.x - 1) / C, g0 = 32 * ((blockIdx.x - 1) % C);
         if (packed) {
             __shared__ int pass[32], slot[32];
-            pair_slots_cta(ids, P, E, k, t, pass_tok, pass, slot);
+            pair_slots_cta(ids, P, E, k, t, pass_tok, pass, slot, res);
             split_row_packed_cta(x + (size_t)t * H, H, g0, k, pass, slot,
                                  reinterpret_cast<uint8_t *>(xcells));
         } else {
@@ -591,7 +598,8 @@ __global__ void __launch_bounds__(32 * kMoeWarps, 1)
 
 __global__ void __launch_bounds__(256)
     k_combine(const float *__restrict__ y, const int32_t *__restrict__ ids,
-              const float *__restrict__ w, int k, int E, int H, float *__restrict__ out) {
+              const float *__restrict__ w, int k, int E, int H, float *__restrict__ out,
+              const uint32_t *res) {
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.y;
@@ -601,7 +609,7 @@ __global__ void __launch_bounds__(256)
     for (int j = 0; j < k; ++j) {
         const int p = t * k + j;
         const int e = ids[p];
-        if (e >= 0 && e < E) o = fmaf(w[p], y[(size_t)p * H + i], o);
+        if (e >= 0 && e < E && expert_served(res, e)) o = fmaf(w[p], y[(size_t)p * H + i], o);
     }
     out[(size_t)t * H + i] = o;
 }
@@ -631,18 +639,19 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int
                          int32_t *uexp, int32_t *n_used, int32_t *status, cudaStream_t st) {
     return launch(k_group_split, dim3(1), dim3(1024), 0, st, false, ids, P, E, offsets, list, uexp,
                   n_used, (int32_t *)nullptr, status, (const float *)nullptr, 64,
-                  (uint4 *)nullptr, (float *)nullptr, (int)kMaxTok, 1, 0, (int32_t *)nullptr, 0);
+                  (uint4 *)nullptr, (float *)nullptr, (int)kMaxTok, 1, 0, (int32_t *)nullptr, 0,
+                  (const uint32_t *)nullptr, (uint8_t *)nullptr);
 }
 
 cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
                                int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
                                cudaStream_t st, int pass_tok, bool packed, int32_t *zero,
-                               int nzero, bool pdl) {
+                               int nzero, bool pdl, const uint32_t *res, uint8_t *served) {
     const int C = (H / kGroup + 31) / 32;  // CTAs per token row
     return launch(k_group_split, dim3(x ? 1 + T * C : 1), dim3(1024), 0, st, pdl, ids, T * k, E,
                   offsets, list, uexp, n_used, pass_ofs, status, x, H, static_cast<uint4 *>(xcells),
-                  xfac, pass_tok, k, packed ? 1 : 0, zero, nzero);
+                  xfac, pass_tok, k, packed ? 1 : 0, zero, nzero, res, served);
 }
 
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
@@ -675,10 +684,10 @@ cudaError_t launch_down(const MoeDims &m, const void *hcells, const float *hfac,
 }
 
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int T, int k, int E,
-                           int H, float *out, cudaStream_t st, bool pdl) {
+                           int H, float *out, cudaStream_t st, bool pdl, const uint32_t *res) {
     if (T == 0) return cudaSuccess;
     return launch(k_combine, dim3((H + 255) / 256, T), dim3(256), 0, st, pdl, y, ids, w, k, E, H,
-                  out);
+                  out, res);
 }
 
 MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k) {

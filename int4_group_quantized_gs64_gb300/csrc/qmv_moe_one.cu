@@ -27,7 +27,8 @@
 //
 // Waits are bounded: a copy or barrier wait that runs out sets bit 1 of the
 // status word (the outputs are then not valid) and the kernel goes on. An
-// expert id outside [0, E) sets bit 0 and contributes nothing.
+// expert id outside [0, E) sets bit 0 and contributes nothing; so does, with
+// no error, an expert outside the call's residency bitmap.
 #include <cuda.h>
 
 #include <algorithm>
@@ -61,6 +62,8 @@ struct OneArgs {
     float *out;            // [H]
     int32_t *status;
     unsigned int *bar;     // grid barrier count, zero at launch
+    const uint32_t *res;   // served experts' bitmap, or null for all
+    uint8_t *served;       // [k]: 1 = pair computed (CTA 0 writes it), or null
     // shared-memory layout (byte offsets from the aligned base)
     int n1, n2;            // gate+up tiles, down row tiles per CTA (at most)
     int o_xu, o_xf, o_w1, o_w2, o_hu, o_hf, o_red, o_scr;
@@ -200,11 +203,14 @@ __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant_
     if (threadIdx.x < k) {
         int e = a.ids[threadIdx.x];
         if (e < 0 || e >= a.E) {
-            atomicOr(a.status, 1);
+            if (b == 0) atomicOr(a.status, 1);
             e = -1;
+        } else if (!expert_served(a.res, e)) {
+            e = -1;  // not resident: left to the caller, no error
         }
         sh.ids[threadIdx.x] = e;
         sh.w[threadIdx.x] = a.w[threadIdx.x];
+        if (b == 0 && a.served) a.served[threadIdx.x] = e >= 0 ? 1 : 0;
     }
     if (threadIdx.x == 0) {
         tc05::mbar_init(&sh.mb1, 1);
@@ -377,7 +383,7 @@ bool moe_one_supported(const MoeDims &m, int k) {
 
 cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids, const float *w,
                            int k, float *h, float *out, int32_t *status, unsigned int *bar,
-                           cudaStream_t st) {
+                           cudaStream_t st, const uint32_t *res, uint8_t *served) {
     OneArgs a;
     memset(&a, 0, sizeof(a));
     size_t smem = 0;
@@ -386,6 +392,7 @@ cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids,
     a.gu_q = m.gu_q; a.gu_s = m.gu_s; a.dn_q = m.dn_q; a.dn_s = m.dn_s;
     a.E = m.E; a.H = m.H; a.I = m.I; a.k = k;
     a.x = x; a.ids = ids; a.w = w; a.h = h; a.out = out; a.status = status; a.bar = bar;
+    a.res = res; a.served = served;
     cudaError_t e = set_smem(k_moe_one, smem);
     if (e != cudaSuccess) return e;
     if (max_ctas_per_sm(k_moe_one, kOThreads, smem) < 1) return cudaErrorInvalidConfiguration;

@@ -65,6 +65,12 @@ __device__ __forceinline__ void cp_async_wait() {
 // Programmatic dependent launch: wait for the previous kernel's results /
 // let the next kernel's CTAs start. Both are no-ops without the launch attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Whether expert e is served by the call: bit e % 32 of word e / 32 of the
+// residency bitmap, or every expert when there is none.
+__device__ __forceinline__ bool expert_served(const uint32_t *res, int e) {
+    return res == nullptr || ((res[e >> 5] >> (e & 31)) & 1u) != 0;
+}
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

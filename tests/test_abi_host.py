@@ -132,6 +132,16 @@ def test_moe_validation(L):
     assert L.moe_weight_path(ctypes.byref(_desc(I=96))) == ESHAPE
     assert L.moe_weight_path(ctypes.byref(bad)) == EALIGN
     assert L.moe_weight_path(ctypes.byref(d)) in (0, 1)
+    # resident variant: bitmap and served mask required, bitmap 4-byte aligned
+    # (m, resident, x, T, ids, w, k, out, served, ws, bytes, stream)
+    assert L.moe_expert_ffn_int4_resident(ctypes.byref(d), None, p, 3, p, p, 2, p, p, ws,
+                                          need, None) == EINVAL
+    assert L.moe_expert_ffn_int4_resident(ctypes.byref(d), p, p, 3, p, p, 2, p, None, ws,
+                                          need, None) == EINVAL
+    assert L.moe_expert_ffn_int4_resident(ctypes.byref(d), ctypes.c_void_p(FAKE + 2), p, 3, p, p,
+                                          2, p, p, ws, need, None) == EALIGN
+    assert L.moe_expert_ffn_int4_resident(ctypes.byref(d), p, p, 3, p, p, 2, p, p, ws,
+                                          need - 1, None) == EWORKSPACE
     # one-token path query: same descriptor rule
     assert L.moe_one_token_path(None, 8) == EINVAL
     assert L.moe_one_token_path(ctypes.byref(_desc(gs=32)), 8) == EINVAL

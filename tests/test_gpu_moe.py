@@ -173,6 +173,60 @@ def test_one_token_bad_ids_and_fallback():
     assert q.moe_one_token_path(big, 2) == 0
 
 
+def _bitmap(mask):
+    """bool [E] -> int32 words [ceil(E/32)], bit e % 32 of word e / 32."""
+    E = len(mask)
+    words = np.zeros((E + 31) // 32, np.uint32)
+    for e in np.flatnonzero(mask):
+        words[e // 32] |= np.uint32(1) << np.uint32(e % 32)
+    return words.view(np.int32)
+
+
+@pytest.mark.parametrize("T,k,E,H,I,frac", [(1, 8, 64, 256, 256, 0.5), (8, 8, 40, 512, 256, 0.3),
+                                            (5, 3, 6, 128, 192, 0.5), (8, 4, 16, 256, 256, 0.0),
+                                            (3, 2, 7, 256, 256, 1.0), (1, 8, 300, 2048, 512, 0.7)])
+def test_resident_subset(T, k, E, H, I, frac):
+    """Only resident experts are computed: out is the oracle over the served
+    slots (the others weighted zero), served marks exactly those slots, and a
+    non-resident id is no error. Covers the single-launch one-token kernel,
+    the tensor-map phases (packed), the cp.async phases and no resident expert."""
+    rng = np.random.default_rng(T * 1000 + k * 10 + E)
+    wts = _rand_pool(rng, E, H, I)
+    m = q.MoeInt4Weights.from_numpy(wts)
+    x = rng.normal(size=(T, H)).astype(np.float32)
+    ids, w = oracle.route_topk(rng.normal(size=(T, E)).astype(np.float32), k)
+    w = w.astype(np.float32)
+    res = rng.random(E) < frac
+    ws = torch.empty(q.moe_workspace_bytes(m, T, k), dtype=torch.uint8, device="cuda")
+    out, served = q.moe_expert_ffn_int4_resident(m, dev(_bitmap(res)), dev(x), dev(ids), dev(w),
+                                                 ws=ws)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).cpu()[0]) == 0
+    want = res[ids]
+    assert np.array_equal(served.cpu().numpy(), want.astype(np.uint8))
+    ref = oracle.moe_ffn(wts, x.astype(np.float64), ids, np.where(want, w, 0).astype(np.float32))
+    o = out.cpu().numpy()
+    assert np.all(o[~want.any(axis=1)] == 0)
+    den = np.maximum(ref["den"], 1e-30)
+    assert norm_err(o, ref["out"], den) <= TOL_FP32
+
+
+def test_resident_all_matches_plain_call():
+    """Every expert resident: the same result as moe_expert_ffn_int4, bit for bit."""
+    rng = np.random.default_rng(91)
+    E, H, I, T, k = 12, 256, 256, 8, 4
+    wts = _rand_pool(rng, E, H, I)
+    m = q.MoeInt4Weights.from_numpy(wts)
+    x = rng.normal(size=(T, H)).astype(np.float32)
+    ids, w = oracle.route_topk(rng.normal(size=(T, E)).astype(np.float32), k)
+    w = w.astype(np.float32)
+    a = q.moe_expert_ffn_int4(m, dev(x), dev(ids), dev(w)).cpu().numpy()
+    b, served = q.moe_expert_ffn_int4_resident(m, dev(_bitmap(np.ones(E, bool))), dev(x),
+                                               dev(ids), dev(w))
+    assert np.array_equal(a, b.cpu().numpy())
+    assert np.all(served.cpu().numpy() == 1)
+
+
 def test_w2_stages_hidden():
     wl = W2
     wts = datagen.moe_weights(wl["E"], wl["H"], wl["I"])
