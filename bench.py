@@ -533,6 +533,21 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     rows["int8_gemv_14336x4096"] = {"us": t * 1e6, "GBs": B8 / t / 1e9, "frac": B8 / t / 1e9 / peak,
                                     "bytes": B8, "launches_per_call": 2}
     del w8s, gs
+    # small-S dense decode: 4 tokens against the 14336 x 4096 int4 matrix (weights read once)
+    wqs = [torch.from_numpy(wq).to(dev) for _ in range(C)]
+    x4 = torch.from_numpy(np.random.default_rng(11).normal(size=(4, K)).astype(np.float32)).to(dev)
+    y4 = torch.empty((4, N), device=dev)
+    ws4d = torch.empty(q.qmv_gemv_workspace_bytes(K, 4), dtype=torch.uint8, device=dev)
+    scs = [torch.from_numpy(sc).to(dev) for _ in range(C)]
+    gs = [graph_of(lambda: [q.qmv_int4_gs(wqs[i], scs[i], x4, y=y4, ws=ws4d, stream=stream)
+                            for i in range(C)], stream)]
+    time_graphs(gs, 4, stream)
+    t = time_graphs(gs, 32, stream) / C
+    Bq4 = wq.nbytes + sc.nbytes + x4.numel() * 4 + 4 * N * 4
+    rows["int4_gemv_14336x4096_s4"] = {"us": t * 1e6, "GBs": Bq4 / t / 1e9,
+                                       "frac": Bq4 / t / 1e9 / peak, "bytes": Bq4,
+                                       "token_eq_per_s": 4 / t, "launches_per_call": 2}
+    del wqs, scs, gs
     # pair of int4 GEMVs sharing x (q_a + kv_a shape 6144 -> (2048, 576)), one token;
     # 24 rotating weight copies (218 MB, above L2)
     K2, N0, N1, C2 = 6144, 2048, 576, 24
@@ -563,6 +578,42 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
                                             "frac": Bp / t / 1e9 / peak, "bytes": Bp,
                                             "two_calls_us": t2 * 1e6, "launches_per_call": 2}
     del pq, gs
+    # the 8-token layer with half of the 160 experts resident (served mask);
+    # bytes: the served experts only
+    wl = W3
+    rmask = np.zeros(wl["E"], bool)
+    rmask[np.random.default_rng(5).permutation(wl["E"])[: wl["E"] // 2]] = True
+    words = np.zeros((wl["E"] + 31) // 32, np.uint32)
+    for e in np.flatnonzero(rmask):
+        words[e // 32] |= np.uint32(1) << np.uint32(e % 32)
+    resd = torch.from_numpy(words.view(np.int32)).to(dev)
+    bs3 = w3_batches(wl, ROTATE)
+    T3, k3 = wl["T"], wl["k"]
+    x3 = [torch.from_numpy(b["x"]).to(dev) for b in bs3]
+    l3 = [torch.from_numpy(b["logits"]).to(dev) for b in bs3]
+    i3 = [torch.empty((T3, k3), dtype=torch.int32, device=dev) for _ in bs3]
+    w3 = [torch.empty((T3, k3), dtype=torch.float32, device=dev) for _ in bs3]
+    o3 = [torch.empty((T3, wl["H"]), device=dev) for _ in bs3]
+    sv3 = [torch.empty((T3, k3), dtype=torch.uint8, device=dev) for _ in bs3]
+    ws3 = [torch.empty(q.moe_workspace_bytes(pool, T3, k3), dtype=torch.uint8, device=dev)
+           for _ in bs3]
+
+    def f3(i):
+        return lambda: (q.moe_route_topk(l3[i], k3, ids=i3[i], w=w3[i], stream=stream),
+                        q.moe_expert_ffn_int4_resident(pool, resd, x3[i], i3[i], w3[i], out=o3[i],
+                                                       served=sv3[i], ws=ws3[i], stream=stream))
+    gs = [graph_of(lambda: [f3(i)() for i in range(len(bs3))], stream)]
+    time_graphs(gs, 4, stream)
+    t = time_graphs(gs, 16, stream) / len(bs3)
+    U3 = []
+    for b in bs3:
+        top = np.argsort(-b["logits"], axis=1, kind="stable")[:, :k3]
+        U3.append(int(rmask[np.unique(top)].sum()))
+    B3 = statistics.mean(step_bytes(wl, u) for u in U3)
+    rows["moe_decode_h6144_e160_i2048_8tok_resident_half"] = {
+        "us": t * 1e6, "GBs": B3 / t / 1e9, "frac": B3 / t / 1e9 / peak, "bytes": B3,
+        "served_experts_mean": statistics.mean(U3), "launches_per_call": 5}
+    del ws3, gs
     # MoE decode, 1 token, H 2048 / E 256 / I 512 (pool 453 MB)
     wl = W2
     wts = datagen.moe_weights(wl["E"], wl["H"], wl["I"])
