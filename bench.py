@@ -628,10 +628,9 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     o2 = [torch.empty((1, wl["H"]), device=dev) for _ in bs]
     ws2 = [torch.empty(q.moe_workspace_bytes(m2, 1, 8), dtype=torch.uint8, device=dev) for _ in bs]
 
-    def f2(i):
-        return lambda: (q.moe_route_topk(l2[i], 8, ids=i2[i], w=w2[i], stream=stream),
-                        q.moe_expert_ffn_int4(m2, x2[i], i2[i], w2[i], out=o2[i], ws=ws2[i],
-                                              stream=stream))
+    def f2(i):  # routing + FFN through the one-call entry point
+        return lambda: q.moe_route_expert_ffn_int4(m2, l2[i], x2[i], 8, ids=i2[i], w=w2[i],
+                                                   out=o2[i], ws=ws2[i], stream=stream)
     gs = [graph_of(lambda: [f2(i)() for i in range(len(bs))], stream)]
     time_graphs(gs, 4, stream)
     t = time_graphs(gs, 16, stream) / len(bs)
@@ -639,9 +638,9 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     one = q.moe_one_token_path(m2, 8) == 1
     rows["moe_decode_h2048_e256_i512_1tok"] = {
         "us": t * 1e6, "GBs": B2 / t / 1e9, "frac": B2 / t / 1e9 / peak, "bytes": B2,
-        "launches_per_call": 2 if one else 5,
-        "path": "routing + single cooperative FFN kernel (k_moe_one)" if one
-                else "routing + grouped phases (k_moe_tma)"}
+        "launches_per_call": 1 if one else 5,
+        "path": "one cooperative kernel routing the token and running the FFN (k_moe_one)"
+                if one else "routing + grouped phases (k_moe_tma)"}
     return rows
 
 

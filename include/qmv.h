@@ -223,6 +223,18 @@ int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int3
                         const float *w, int k, float *out, void *ws, size_t ws_bytes,
                         qmv_stream_t stream);
 
+/* Routing and expert FFN of a decode micro-batch in one call: moe_route_topk
+ * on logits [T][E] (ids [T][k] and w [T][k] are written, as that call writes
+ * them), then moe_expert_ffn_int4 with those ids and weights; same
+ * workspace, limits and status word (1 <= k <= min(E, 32)). With one token
+ * and moe_one_token_path(m, k) == 1 the routing runs inside the
+ * single-launch FFN kernel (every thread block routes the token itself; the
+ * first writes ids and w), so the call is one kernel after the status clear.
+ * Errors: those of moe_route_topk and moe_expert_ffn_int4. */
+int moe_route_expert_ffn_int4(const qmv_moe_int4 *m, const float *logits, const float *x, int T,
+                              int k, int32_t *ids, float *w, float *out, void *ws, size_t ws_bytes,
+                              qmv_stream_t stream);
+
 /* moe_expert_ffn_int4 over the resident experts only (colibri PR #418,
  * "Vulkan expert tier ... overlapped with CPU rows": the GPU computes the
  * experts of its registry while the CPU computes the rest; PR #1338,

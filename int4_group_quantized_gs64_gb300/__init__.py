@@ -77,6 +77,7 @@ def lib():
             "moe_ffn_combine": ([P, vp, vp, i32, i32, vp, vp, sz, vp], i32),
             "moe_weight_path": ([P], i32),
             "moe_one_token_path": ([P, i32], i32),
+            "moe_route_expert_ffn_int4": ([P, vp, vp, i32, i32, vp, vp, vp, vp, sz, vp], i32),
             "moe_expert_ffn_int4_resident": ([P, vp, vp, i32, vp, vp, i32, vp, vp, vp, sz, vp], i32),
             "moe_prefill_workspace_bytes": ([P, i32, i32], sz),
             "moe_expert_ffn_int4_prefill": ([P, vp, i32, vp, vp, i32, vp, vp, sz, vp], i32),
@@ -305,6 +306,27 @@ def moe_expert_ffn_int4(m: MoeInt4Weights, x, ids, w, out=None, ws=None, stream=
         m.desc, _ptr(x), T, _ptr(ids), _ptr(w), k, _ptr(out), _ptr(ws), ws.numel(),
         _stream(stream)))
     return out
+
+
+def moe_route_expert_ffn_int4(m: MoeInt4Weights, logits, x, k: int, ids=None, w=None, out=None,
+                              ws=None, stream=None):
+    """Routing plus expert FFN in one call; returns (out [T][H], ids [T][k], w [T][k])."""
+    import torch
+    _need(logits, torch.float32, "logits"); _need(x, torch.float32, "x")
+    T = logits.shape[0]
+    if ids is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    if w is None:
+        w = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    if out is None:
+        out = torch.empty((T, m.H), dtype=torch.float32, device=x.device)
+    _need(ids, torch.int32, "ids"); _need(w, torch.float32, "w")
+    if ws is None:
+        ws = _workspace(moe_workspace_bytes(m, T, k), x.device)
+    _check("moe_route_expert_ffn_int4", lib().moe_route_expert_ffn_int4(
+        m.desc, _ptr(logits), _ptr(x), T, k, _ptr(ids), _ptr(w), _ptr(out), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out, ids, w
 
 
 def moe_expert_ffn_int4_resident(m: MoeInt4Weights, resident, x, ids, w, out=None, served=None,

@@ -338,6 +338,34 @@ int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int3
     return ffn_impl(m, nullptr, x, T, ids, w, k, out, nullptr, ws, ws_bytes, stream);
 }
 
+int moe_route_expert_ffn_int4(const qmv_moe_int4 *m, const float *logits, const float *x, int T,
+                              int k, int32_t *ids, float *w, float *out, void *ws, size_t ws_bytes,
+                              qmv_stream_t stream) {
+    int r = check_moe(m);
+    if (r) return r;
+    if (T < 0 || k < 1 || k > m->E || k > 32 || (int64_t)T * k > kMaxPairs) return QMV_EINVAL;
+    if (T == 0) return QMV_OK;
+    if (!logits || !ids || !w) return QMV_EINVAL;
+    if (!aligned(logits, 4) || !aligned(ids, 4) || !aligned(w, 4)) return QMV_EALIGN;
+    if (T == 1 && one_token(m, k)) {
+        qmv::MoeWorkspace L;
+        if ((r = ffn_check(m, T, k, ws, ws_bytes, L))) return r;
+        if (!x || !out) return QMV_EINVAL;
+        if (!aligned(x, 4) || !aligned(out, 4)) return QMV_EALIGN;
+        // one token: routing inside the single cooperative launch
+        const cudaStream_t st = cs(stream);
+        cudaError_t e = cudaMemsetAsync(at<int32_t>(ws, L.status), 0, L.status_bytes, st);
+        if (e == cudaSuccess)
+            e = qmv::launch_moe_one(dims(m), x, nullptr, nullptr, k, at<float>(ws, L.h), out,
+                                    at<int32_t>(ws, L.status),
+                                    reinterpret_cast<unsigned int *>(at<int32_t>(ws, L.sk_cnt)), st,
+                                    nullptr, nullptr, logits, ids, w);
+        return from_cuda(e);
+    }
+    if ((r = moe_route_topk(logits, T, m->E, k, ids, w, stream))) return r;
+    return moe_expert_ffn_int4(m, x, T, ids, w, k, out, ws, ws_bytes, stream);
+}
+
 int moe_expert_ffn_int4_resident(const qmv_moe_int4 *m, const uint32_t *resident, const float *x,
                                  int T, const int32_t *ids, const float *w, int k, float *out,
                                  uint8_t *served, void *ws, size_t ws_bytes, qmv_stream_t stream) {

@@ -118,7 +118,8 @@ bool moe_one_supported(const MoeDims &m, int k);
 cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids, const float *w,
                            int k, float *h, float *out, int32_t *status, unsigned int *bar,
                            cudaStream_t st, const uint32_t *res = nullptr,
-                           uint8_t *served = nullptr);
+                           uint8_t *served = nullptr, const float *logits = nullptr,
+                           int32_t *ids_out = nullptr, float *w_out = nullptr);
 
 // Workspace layout of the MoE entry points (256-byte aligned segments). The
 // status word and the split counters (kSkMaxCtas for gate+up, then kSkMaxCtas

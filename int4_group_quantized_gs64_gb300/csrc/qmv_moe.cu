@@ -18,17 +18,12 @@
 
 #include "qmv_internal.h"
 #include "qmv_launch.cuh"
+#include "qmv_route.cuh"
 #include "qmv_rows.cuh"
 
 namespace qmv {
 
 namespace {
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    return v;
-}
 
 // ------------------------------------------------------------------ routing
 
@@ -49,41 +44,12 @@ __global__ void __launch_bounds__(32 * kRouteWarps)
     const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
     const int t = blockIdx.x * kRouteWarps + wl;
     if (t >= T) return;
-    const float *l = logits + (size_t)t * E;
-    float *row = sl[wl];
-    for (int e = lane; e < E; e += 32) {
-        const float v = l[e];
-        row[e] = (v != v) ? -INFINITY : v;  // NaN never ahead of a finite logit
-    }
-    __syncwarp();
-    uint32_t taken = 0u;
-    int my_id = 0;
-    float my_l = -INFINITY;
-    for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = INT_MAX;
-        for (int i = 0; lane + 32 * i < E; ++i) {
-            if ((taken >> i) & 1u) continue;
-            const int e = lane + 32 * i;
-            const float v = row[e];
-            if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == j) { my_id = bi; my_l = bv; }
-    }
-    const float mx = __shfl_sync(0xFFFFFFFFu, my_l, 0);
-    float ev = 0.0f;
-    if (lane < k) ev = (mx == -INFINITY) ? 1.0f : expf(my_l - mx);
-    const float z = warp_sum(ev);
+    int my_id;
+    float my_w;
+    route_warp(logits + (size_t)t * E, E, k, sl[wl], my_id, my_w);
     if (lane < k) {
         ids[(size_t)t * k + lane] = my_id;
-        w[(size_t)t * k + lane] = ev / z;
+        w[(size_t)t * k + lane] = my_w;
     }
 }
 

@@ -36,6 +36,7 @@
 
 #include "qmv_internal.h"
 #include "qmv_launch.cuh"
+#include "qmv_route.cuh"
 #include "qmv_rows.cuh"
 #include "tc05.cuh"
 
@@ -64,9 +65,12 @@ struct OneArgs {
     unsigned int *bar;     // grid barrier count, zero at launch
     const uint32_t *res;   // served experts' bitmap, or null for all
     uint8_t *served;       // [k]: 1 = pair computed (CTA 0 writes it), or null
+    const float *logits;   // [E]: route in-kernel (ids / w then outputs), or null
+    int32_t *ids_out;      // routed ids [k] (CTA 0 writes them) when logits != null
+    float *w_out;          // their weights [k]
     // shared-memory layout (byte offsets from the aligned base)
     int n1, n2;            // gate+up tiles, down row tiles per CTA (at most)
-    int o_xu, o_xf, o_w1, o_w2, o_hu, o_hf, o_red, o_scr;
+    int o_xu, o_xf, o_w1, o_w2, o_hu, o_hf, o_red, o_scr, o_lg;
 };
 
 struct OneShared {
@@ -200,8 +204,23 @@ __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant_
     const int n1 = b < tiles1 ? (tiles1 - b + grid - 1) / grid : 0;
     const int n2 = b < tiles2 ? (tiles2 - b + grid - 1) / grid : 0;
 
+    if (a.logits && warp == 0) {
+        // every CTA routes the token itself (the same top-k as moe_route_topk)
+        int my_id;
+        float my_w;
+        route_warp(a.logits, a.E, k, reinterpret_cast<float *>(base + a.o_lg), my_id, my_w);
+        if (lane < k) {
+            sh.ids[lane] = my_id;
+            sh.w[lane] = my_w;
+            if (b == 0) {
+                a.ids_out[lane] = my_id;
+                a.w_out[lane] = my_w;
+            }
+        }
+    }
+    __syncthreads();
     if (threadIdx.x < k) {
-        int e = a.ids[threadIdx.x];
+        int e = a.logits ? sh.ids[threadIdx.x] : a.ids[threadIdx.x];
         if (e < 0 || e >= a.E) {
             if (b == 0) atomicOr(a.status, 1);
             e = -1;
@@ -209,7 +228,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant_
             e = -1;  // not resident: left to the caller, no error
         }
         sh.ids[threadIdx.x] = e;
-        sh.w[threadIdx.x] = a.w[threadIdx.x];
+        if (!a.logits) sh.w[threadIdx.x] = a.w[threadIdx.x];
         if (b == 0 && a.served) a.served[threadIdx.x] = e >= 0 ? 1 : 0;
     }
     if (threadIdx.x == 0) {
@@ -368,6 +387,7 @@ bool one_layout(const MoeDims &m, int k, int grid, OneArgs &a, size_t &smem) {
     a.o_hf = (int)o; o = up16(o + (size_t)k * GI * 4);
     a.o_red = (int)o; o = up16(o + (size_t)std::max(a.n1 * kOWarps * 16, kOMaxK * 16) * 4);
     a.o_scr = (int)o; o = up16(o + (size_t)kOWarps * 8 * 64 * 4);
+    a.o_lg = (int)o; o = up16(o + (size_t)1024 * 4);  // one routing row (E <= 1024)
     smem = o + 128;
     return smem <= (size_t)kOSmemMax;
 }
@@ -383,7 +403,8 @@ bool moe_one_supported(const MoeDims &m, int k) {
 
 cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids, const float *w,
                            int k, float *h, float *out, int32_t *status, unsigned int *bar,
-                           cudaStream_t st, const uint32_t *res, uint8_t *served) {
+                           cudaStream_t st, const uint32_t *res, uint8_t *served,
+                           const float *logits, int32_t *ids_out, float *w_out) {
     OneArgs a;
     memset(&a, 0, sizeof(a));
     size_t smem = 0;
@@ -393,6 +414,7 @@ cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids,
     a.E = m.E; a.H = m.H; a.I = m.I; a.k = k;
     a.x = x; a.ids = ids; a.w = w; a.h = h; a.out = out; a.status = status; a.bar = bar;
     a.res = res; a.served = served;
+    a.logits = logits; a.ids_out = ids_out; a.w_out = w_out;
     cudaError_t e = set_smem(k_moe_one, smem);
     if (e != cudaSuccess) return e;
     if (max_ctas_per_sm(k_moe_one, kOThreads, smem) < 1) return cudaErrorInvalidConfiguration;

@@ -132,6 +132,15 @@ def test_moe_validation(L):
     assert L.moe_weight_path(ctypes.byref(_desc(I=96))) == ESHAPE
     assert L.moe_weight_path(ctypes.byref(bad)) == EALIGN
     assert L.moe_weight_path(ctypes.byref(d)) in (0, 1)
+    # fused routing + FFN: (m, logits, x, T, k, ids, w, out, ws, bytes, stream)
+    assert L.moe_route_expert_ffn_int4(ctypes.byref(d), None, p, 3, 2, p, p, p, ws, need,
+                                       None) == EINVAL
+    assert L.moe_route_expert_ffn_int4(ctypes.byref(d), p, p, 3, 33, p, p, p, ws, need,
+                                       None) == EINVAL                     # k > 32
+    assert L.moe_route_expert_ffn_int4(ctypes.byref(d), p, p, 3, 2, ctypes.c_void_p(FAKE + 2), p,
+                                       p, ws, need, None) == EALIGN
+    assert L.moe_route_expert_ffn_int4(ctypes.byref(d), p, p, 0, 2, p, p, p, ws, need,
+                                       None) == 0
     # resident variant: bitmap and served mask required, bitmap 4-byte aligned
     # (m, resident, x, T, ids, w, k, out, served, ws, bytes, stream)
     assert L.moe_expert_ffn_int4_resident(ctypes.byref(d), None, p, 3, p, p, 2, p, p, ws,

@@ -173,6 +173,31 @@ def test_one_token_bad_ids_and_fallback():
     assert q.moe_one_token_path(big, 2) == 0
 
 
+@pytest.mark.parametrize("T,k,E,H,I", [(1, 8, 256, 2048, 512), (1, 3, 40, 256, 256),
+                                       (8, 8, 160, 512, 256), (2, 32, 64, 256, 256)])
+def test_route_ffn_fused(T, k, E, H, I):
+    """Routing inside the one-token kernel, and routing then the phases for
+    more tokens: ids bit-exact and w as moe_route_topk, out within 2e-5."""
+    rng = np.random.default_rng(T + 10 * k + E)
+    wts = _rand_pool(rng, E, H, I)
+    m = q.MoeInt4Weights.from_numpy(wts)
+    x = rng.normal(size=(T, H)).astype(np.float32)
+    logits = rng.normal(size=(T, E)).astype(np.float32)
+    if T == 1:
+        assert q.moe_one_token_path(m, k) == 1
+    ws = torch.empty(q.moe_workspace_bytes(m, T, k), dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        out, ids, w = q.moe_route_expert_ffn_int4(m, dev(logits), dev(x), k, ws=ws)
+        torch.cuda.synchronize()
+        assert int(ws[:4].view(torch.int32).cpu()[0]) == 0
+        rid, rw = oracle.route_topk(logits, k)
+        assert np.array_equal(ids.cpu().numpy(), rid)
+        gi, gw = q.moe_route_topk(dev(logits), k)
+        assert np.array_equal(w.cpu().numpy(), gw.cpu().numpy())  # the same routing code
+        ref = oracle.moe_ffn(wts, x.astype(np.float64), rid, rw.astype(np.float32))
+        assert norm_err(out.cpu().numpy(), ref["out"], ref["den"]) <= TOL_FP32
+
+
 def _bitmap(mask):
     """bool [E] -> int32 words [ceil(E/32)], bit e % 32 of word e / 32."""
     E = len(mask)
