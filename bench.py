@@ -212,7 +212,8 @@ def time_graphs(graphs, iters, stream):
 
 
 def load_traffic(kernel: str):
-    """dram bytes per launch from the committed ncu summary, if it still matches the source."""
+    """dram bytes per launch from the committed ncu summary, if it still matches the source:
+    the kernel's file and the headers holding its device code and sizes, hashed."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:

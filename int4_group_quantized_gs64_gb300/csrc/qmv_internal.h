@@ -8,6 +8,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "qmv_layout.h"
+
 namespace qmv {
 
 // Dense GEMV, any S (passes of up to 16 tokens). scratch: dense_scratch_bytes(K, S).
@@ -89,8 +91,6 @@ cudaError_t launch_pack_x(const uint16_t *x, int H, int k, const int32_t *offset
 // split between CTAs leaves partial sums in `part` and the last CTA to finish
 // it (counted in cnt, which must be zero at launch and is zero again after
 // the kernel) adds them and writes the item.
-constexpr int kSkMaxCtas = 256;                 // CTAs of one launch, at most
-constexpr int kSkPartFloats = 2 * 256 * 8;      // per CTA: 2 slots x 256 rows x 8 tokens
 bool tma_moe_supported(const MoeDims &m);
 // 3-D tensor maps of a weight pool [E][rows][K/2] (box 128 B x box_rows rows,
 // 128-byte swizzle) and of its scales [E][rows][K/64] (box 4 x box_rows rows).
@@ -124,13 +124,8 @@ cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids,
 // Workspace layout of the MoE entry points (256-byte aligned segments). The
 // status word and the split counters (kSkMaxCtas for gate+up, then kSkMaxCtas
 // for down) are adjacent, so one memset of status_bytes clears them all.
-// Pass-packed activation units (tensor-map decode path): block (pi, s) of
-// kPackedStage bytes holds, for pass pi and stage s (4 groups), the factors
-// of the pass's token slots 0..7 ([slot][4] floats, 128 B) followed by their
-// units ([slot][4 groups x 16] uint4, 1 KB a slot), so a stage's activations
-// are one contiguous copy of 128 B + 1 KB per token. xpk holds x for
-// gate+up, hpk h for down.
-constexpr int kPackedStage = 128 + 8 * 1024;
+// Pass-packed activation units (kPackedStage blocks, qmv_layout.h): xpk
+// holds x for gate+up, hpk h for down.
 struct MoeWorkspace {
     size_t status, sk_cnt, status_bytes, offsets, list, uexp, n_used, pass_ofs, xcells, xfac, h,
         hcells, hfac, y, sk_part, xpk, hpk, total;
