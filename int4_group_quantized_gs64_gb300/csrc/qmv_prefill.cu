@@ -196,6 +196,34 @@ __device__ __forceinline__ void pf_dequant(const uint4 &w0, const uint4 &w1, flo
     }
 }
 
+// The same values in the MMA K order of the tensor-map kernel's B tiles:
+// column 4i + m holds the elements (8i + m, 8i + m + 4) of the group, which
+// are nibbles m and m + 4 of word i. Masking the word, or the word shifted
+// by 4, 8 or 12 bits, with 0x000F000F puts such a pair in the two halves'
+// mantissa bits 0..3 directly, with no byte permute (15 instructions a word
+// instead of 17). The B operands are stored in the same K order (kperm).
+__device__ __forceinline__ void pf_dequant_perm(const uint4 &w0, const uint4 &w1, float scale,
+                                                uint32_t (&r)[32]) {
+    const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const uint32_t kBias = 0x43004300u;   // (128, 128) in bf16
+    const uint32_t kSub = 0xC308C308u;    // (-136, -136)
+    const __nv_bfloat162 s2 = __float2bfloat162_rn(scale);
+    const uint32_t s = *reinterpret_cast<const uint32_t *>(&s2);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t w = words[i], w4 = w >> 4, w8 = w >> 8, w12 = w4 >> 8;
+        r[4 * i + 0] = bmul2(badd2(lop3_andor_(w, 0x000F000Fu, kBias), kSub), s);
+        r[4 * i + 1] = bmul2(badd2(lop3_andor_(w4, 0x000F000Fu, kBias), kSub), s);
+        r[4 * i + 2] = bmul2(badd2(lop3_andor_(w8, 0x000F000Fu, kBias), kSub), s);
+        r[4 * i + 3] = bmul2(badd2(lop3_andor_(w12, 0x000F000Fu, kBias), kSub), s);
+    }
+}
+
+// Position of group element kq (0..63) in the MMA K order of pf_dequant_perm.
+__host__ __device__ __forceinline__ int kperm_pos(int kq) {
+    return 8 * (kq >> 3) + 2 * (kq & 3) + ((kq >> 2) & 1);
+}
+
 __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(PfArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t mbar[2];
@@ -684,7 +712,7 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                 const uint4 w1 = *reinterpret_cast<const uint4 *>(wr + (((2 * g + 1) ^ x7) << 4));
                 const float sc = *reinterpret_cast<const float *>(sp + kPqOffS + r * 16 + g * 4);
                 uint32_t A[32];
-                pf_dequant(w0, w1, sc, A);
+                pf_dequant_perm(w0, w1, sc, A);
                 if (j > 0) {
                     // MMA(j - 1) of this group done: its A slot may be overwritten
                     pq_wait(sh, &sh.afree[g][tt], (uint32_t)((j - 1) & 1));
@@ -735,7 +763,8 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                                 hv = g0 / (1.0f + expf(-g0)) * u0;
                             }
                             const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-                            hp[n * 64 + (((kq >> 3) ^ (n & 7)) << 3) + (kq & 7)] =
+                            const int kp = kperm_pos(kq);  // down's B in the dequant's K order
+                            hp[n * 64 + (((kp >> 3) ^ (n & 7)) << 3) + (kp & 7)] =
                                 *reinterpret_cast<const uint16_t *>(&hb);
                         }
                     }
@@ -770,7 +799,8 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
 }
 
 // Packs the rows of x (bf16 [T][H]) that each pass uses into the MMA's B
-// layout: xp[pass][g][64 rows][64 bf16], row t = token slot t of the pass
+// layout, each group's 64 values in the dequant's K order (kperm_pos):
+// xp[pass][g][64 rows][64 bf16], row t = token slot t of the pass
 // (zero from its token count up to the next multiple of 16), 128-byte
 // swizzled. Grid (passes at most, ceil(G / 8)); warp w packs group
 // 8 * blockIdx.y + w of pass blockIdx.x.
@@ -802,7 +832,10 @@ __global__ void __launch_bounds__(256)
         uint4 v = make_uint4(0, 0, 0, 0);
         if (t < ntok) {
             const int row = list[beg + t] / k;
-            v = *reinterpret_cast<const uint4 *>(x + (size_t)row * H + g * kGroup + ch * 8);
+            const uint4 u = *reinterpret_cast<const uint4 *>(x + (size_t)row * H + g * kGroup + ch * 8);
+            // the dequant's K order (kperm_pos): elements (0,4,1,5,2,6,3,7) of the chunk
+            v = make_uint4(prmt(u.x, u.z, 0x5410), prmt(u.x, u.z, 0x7632), prmt(u.y, u.w, 0x5410),
+                           prmt(u.y, u.w, 0x7632));
         }
         dst[t * 8 + (ch ^ (t & 7))] = v;
     }
