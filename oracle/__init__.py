@@ -63,6 +63,10 @@ def _bind(lib):
     lib.orc_qmv_int4_gs_absden.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp]
     lib.orc_matvec_f64.argtypes = [vp, i32, i32, vp, i32, vp]
     lib.orc_qmv_int8_row.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp]
+    lib.orc_unpack_int3.argtypes = [vp, i64, vp]
+    lib.orc_pack_int3.argtypes = [vp, i64, vp]
+    lib.orc_pack_int3.restype = i32
+    lib.orc_qmv_int3_gs.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp]
     lib.orc_route_topk.argtypes = [vp, i32, i32, i32, vp, vp]
     lib.orc_route_topk.restype = i32
     lib.orc_group.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp]
@@ -162,6 +166,38 @@ def qmv_int8_row(w, r, x, lib=None):
     y = np.empty((S, N), np.float64)
     den = np.empty((S, N), np.float64)
     lib.orc_qmv_int8_row(_p(w), _p(r), N, K, _p(x), S, _p(y), _p(den))
+    return y, den
+
+
+# ------------------------------------------------------------------ f2: int3-g64
+
+def unpack_int3(packed_row, n_vals: int, lib=None) -> np.ndarray:
+    """Values code - 4 of one two-plane row (reading R6 in qmv_oracle.c)."""
+    lib = lib or load()
+    packed_row = _c(packed_row, np.uint8)
+    vals = np.empty(n_vals, np.int8)
+    lib.orc_unpack_int3(_p(packed_row), n_vals, _p(vals))
+    return vals
+
+
+def pack_int3(values, lib=None) -> np.ndarray:
+    """int8 values in [-4, 3], length a multiple of 64 -> two-plane bytes."""
+    lib = lib or load()
+    values = _c(values, np.int8)
+    out = np.empty(values.size // 64 * 24, np.uint8)
+    if lib.orc_pack_int3(_p(values), values.size, _p(out)) != 0:
+        raise ValueError("int3 values must lie in [-4, 3], in whole 64-groups")
+    return out
+
+
+def qmv_int3_gs(wq, scales, x, lib=None):
+    """(y [S][N], den [S][N]) float64 for two-plane int3-g64 rows wq [N][K/64*24]."""
+    lib = lib or load()
+    wq, scales, x = _c(wq, np.uint8), _c(scales, np.float32), _c(np.atleast_2d(x), np.float32)
+    N, K, S = wq.shape[0], wq.shape[1] // 24 * 64, x.shape[0]
+    y = np.empty((S, N), np.float64)
+    den = np.empty((S, N), np.float64)
+    lib.orc_qmv_int3_gs(_p(wq), _p(scales), N, K, _p(x), S, _p(y), _p(den))
     return y, den
 
 

@@ -33,6 +33,16 @@
  *     compare, the lower expert index wins a tie), renormalise the selected
  *     probabilities to sum to one.
  *  R5 SiLU(g) = g * sigma(g), sigma(g) = 1 / (1 + exp(-g)).
+ *  R6 int3-g64 two-plane rows ([PR418] "fmt 5", the 24-byte-per-64-group
+ *     layout whose lanes stride 16-value low-plane words and whose
+ *     high-plane word is pre-shifted to bit 0): a row is K/64 groups of 24
+ *     bytes; bytes 0..15 of a group are the low plane, 2 bits per element
+ *     (element e in bits 2(e%4), 2(e%4)+1 of byte e/4: 16 elements to a
+ *     little-endian 32-bit word), bytes 16..23 the high plane, 1 bit per
+ *     element (element e in bit e%8 of byte 16 + e/8). code = low | high << 2
+ *     and the value is code - 4 (offset binary, as int4's nibble - 8); one
+ *     fp32 scale per group, row-major [rows][K/64]. The pages print no byte
+ *     of this layout; this is the plainest reading of the words they name.
  *
  * Every accumulation is in double. No blocking, fusion or reordering beyond
  * the definitions: parallel loops only split independent outputs.
@@ -146,6 +156,64 @@ void orc_matvec_f64(const double *W, int N, int K, const float *x, int S, double
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k) acc += W[i * K + k] * (double)x[t * (int64_t)K + k];
             y[t * N + i] = acc;
+        }
+}
+
+/* --------------------------- f2: int3-g64 two-plane GEMV [PR418 fmt 5, R6] */
+
+/* 3-bit code (0..7) of element k of a packed row (reading R6). */
+static inline int orc_code3(const uint8_t *row, int64_t k) {
+    const uint8_t *g = row + (k / 64) * 24;
+    const int e = (int)(k % 64);
+    const int lo = (g[e / 4] >> (2 * (e % 4))) & 3;
+    const int hi = (g[16 + e / 8] >> (e % 8)) & 1;
+    return lo | (hi << 2);
+}
+
+/* vals[k] = code(k) - 4, in [-4, 3]; n_vals a multiple of 64 (one row). */
+void orc_unpack_int3(const uint8_t *bytes, int64_t n_vals, int8_t *vals) {
+    for (int64_t k = 0; k < n_vals; ++k) vals[k] = (int8_t)(orc_code3(bytes, k) - 4);
+}
+
+/* Inverse of orc_unpack_int3 for vals in [-4, 3]; n_vals a multiple of 64.
+ * Returns -1 on a bad count or value. */
+int orc_pack_int3(const int8_t *vals, int64_t n_vals, uint8_t *bytes) {
+    if (n_vals % 64) return -1;
+    memset(bytes, 0, (size_t)(n_vals / 64) * 24);
+    for (int64_t k = 0; k < n_vals; ++k) {
+        const int v = vals[k];
+        if (v < -4 || v > 3) return -1;
+        const int c = v + 4, e = (int)(k % 64);
+        uint8_t *g = bytes + (k / 64) * 24;
+        g[e / 4] |= (uint8_t)((c & 3) << (2 * (e % 4)));
+        g[16 + e / 8] |= (uint8_t)(((c >> 2) & 1) << (e % 8));
+    }
+    return 0;
+}
+
+/* y[t][i] = sum_g s[i][g] * sum_{k in g} (code(i,k) - 4) * x[t][k] (form (i),
+ * as for int4), and den[t][i] = sum_k |(code - 4) * s * x|. */
+void orc_qmv_int3_gs(const uint8_t *wq, const float *s, int N, int K, const float *x, int S,
+                     double *y, double *den) {
+    const int G = K / 64;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t t = 0; t < S; ++t)
+        for (int64_t i = 0; i < N; ++i) {
+            const uint8_t *row = wq + i * (int64_t)G * 24;
+            const float *xt = x + t * (int64_t)K;
+            double acc = 0.0, a = 0.0;
+            for (int g = 0; g < G; ++g) {
+                double part = 0.0;
+                const double sc = (double)s[i * G + g];
+                for (int64_t k = (int64_t)g * 64; k < (int64_t)(g + 1) * 64; ++k) {
+                    const double v = (double)(orc_code3(row, k) - 4);
+                    part += v * (double)xt[k];
+                    a += fabs(v * sc * (double)xt[k]);
+                }
+                acc += sc * part;
+            }
+            y[t * N + i] = acc;
+            den[t * N + i] = a;
         }
 }
 

@@ -345,10 +345,79 @@ def pin_ffn_hidden_bound(lib):
     assert np.all(worst >= eps * res["hden"][0] * (1 - 1e-4))
 
 
+# ----------------------------------------------------------------- f2 int3-g64
+
+def np_unpack3(wq3: np.ndarray, K: int) -> np.ndarray:
+    """Reading R6 by explicit bit slicing: [N][K/64*24] bytes -> [N][K] values."""
+    N = wq3.shape[0]
+    g = wq3.reshape(N, K // 64, 24)
+    low = np.unpackbits(g[:, :, :16], axis=2, bitorder="little").reshape(N, K // 64, 64, 2)
+    lo = low[..., 0].astype(np.int16) + 2 * low[..., 1].astype(np.int16)
+    hi = np.unpackbits(g[:, :, 16:], axis=2, bitorder="little").astype(np.int16)
+    return (lo + 4 * hi - 4).reshape(N, K)
+
+
+def pin_int3_pack_roundtrip(lib):
+    rng = _rng(20)
+    vals = rng.integers(-4, 4, size=64 * 20).astype(np.int8)
+    b = oracle.pack_int3(vals, lib=lib)
+    assert b.size == 20 * 24
+    assert np.array_equal(oracle.unpack_int3(b, vals.size, lib=lib), vals)
+    assert np.array_equal(np_unpack3(b[None], vals.size)[0], vals), "oracle != numpy bit slicing"
+    raw = rng.integers(0, 256, size=24 * 7, dtype=np.uint8)  # every byte pattern decodes
+    v = oracle.unpack_int3(raw, 7 * 64, lib=lib)
+    assert v.min() >= -4 and v.max() <= 3
+    assert np.array_equal(oracle.pack_int3(v, lib=lib), raw)
+
+
+def pin_int3_as_int4(lib):
+    """An int3 matrix re-encoded as int4 nibbles (value + 8) gives the same y,
+    bit for bit: both forms sum the same products in the same order."""
+    rng = _rng(21)
+    for (N, K, S) in [(5, 64, 1), (9, 256, 3), (17, 1024, 2)]:
+        vals = rng.integers(-4, 4, size=(N, K)).astype(np.int8)
+        wq3 = np.stack([oracle.pack_int3(vals[i], lib=lib) for i in range(N)])
+        wq4 = np.stack([oracle.pack_int4(vals[i], lib=lib) for i in range(N)])
+        s = (np.abs(rng.normal(0, 0.02, size=(N, K // 64))) + 1e-4).astype(np.float32)
+        x = rng.normal(size=(S, K)).astype(np.float32)
+        y3, d3 = oracle.qmv_int3_gs(wq3, s, x, lib=lib)
+        y4 = oracle.qmv_int4_gs(wq4, s, x, 64, lib=lib)
+        assert np.array_equal(y3, y4)
+        assert np.all(d3 >= np.abs(y3) * (1 - 1e-12))
+
+
+def pin_int3_exact_bruteforce(lib):
+    rng = _rng(22)
+    for (N, K, S) in [(2, 64, 1), (3, 128, 2)]:
+        vals = rng.integers(-4, 4, size=(N, K)).astype(np.int8)
+        wq3 = np.stack([oracle.pack_int3(vals[i], lib=lib) for i in range(N)])
+        s = (np.abs(rng.normal(0, 0.02, size=(N, K // 64))) + 1e-4).astype(np.float32)
+        x = rng.normal(size=(S, K)).astype(np.float32)
+        y, _ = oracle.qmv_int3_gs(wq3, s, x, lib=lib)
+        for t in range(S):
+            for i in range(N):
+                exact = sum(int(vals[i, k]) * Fraction(float(s[i, k // 64])) * Fraction(float(x[t, k]))
+                            for k in range(K))
+                mag = sum(abs(int(vals[i, k]) * Fraction(float(s[i, k // 64])) * Fraction(float(x[t, k])))
+                          for k in range(K))
+                assert abs(Fraction(float(y[t, i])) - exact) <= mag * Fraction(1, 2 ** 45)
+
+
+def pin_golden_int3_planes(lib):
+    d = json.load(open(os.path.join(GOLDEN, "int3_g64_two_plane.json")))
+    row = np.array([d["low_byte"]] * 16 + [d["high_byte"]] * 8, np.uint8)
+    v = oracle.unpack_int3(row, 64, lib=lib)
+    assert v[:8].tolist() == d["expected_values_first8"]
+    x = np.where(np.arange(64) % 4 == 3, 3.0, 1.0).astype(np.float32)[None]
+    y, _ = oracle.qmv_int3_gs(row[None], np.array([[d["scale"]]], np.float32), x, lib=lib)
+    assert y[0, 0] == d["expected_y"]
+
+
 ALL_PINS = [
     pin_pack_roundtrip, pin_golden_nibble_order, pin_int4_exact_bruteforce,
     pin_int4_library_identity, pin_int4_linearity, pin_int4_all_equal_closed_form,
     pin_gs_equals_k_is_row_scale, pin_int8_exact, pin_route_stable_sort, pin_route_exhaustive,
     pin_golden_route, pin_group_bruteforce, pin_ffn_textbook_swiglu, pin_ffn_zero_gate,
-    pin_golden_swiglu, pin_ffn_hidden_bound,
+    pin_golden_swiglu, pin_ffn_hidden_bound, pin_int3_pack_roundtrip, pin_int3_as_int4,
+    pin_int3_exact_bruteforce, pin_golden_int3_planes,
 ]

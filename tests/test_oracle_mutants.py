@@ -27,6 +27,10 @@ MUTANTS = [
     ("group_order_reversed", "for (int64_t p = 0; p < P; ++p) list[fill[ids[p]]++] = (int32_t)p;",
      "for (int64_t p = P - 1; p >= 0; --p) list[fill[ids[p]]++] = (int32_t)p;"),
     ("int8_row_scale_dropped", "y[t * N + i] = (double)r[i] * acc;", "y[t * N + i] = acc;"),
+    ("int3_high_bit_msb_first", "const int hi = (g[16 + e / 8] >> (e % 8)) & 1;",
+     "const int hi = (g[16 + e / 8] >> (7 - e % 8)) & 1;"),
+    ("int3_offset_3_not_4", "const double v = (double)(orc_code3(row, k) - 4);",
+     "const double v = (double)(orc_code3(row, k) - 3);"),
     ("hden_term_dropped", "hden[p * I + c] = fabs(dsilu * u) * dg + fabs(silu) * du;",
      "hden[p * I + c] = fabs(dsilu * u) * dg;"),
 ]
