@@ -534,6 +534,20 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     rows["int8_gemv_14336x4096"] = {"us": t * 1e6, "GBs": B8 / t / 1e9, "frac": B8 / t / 1e9 / peak,
                                     "bytes": B8, "launches_per_call": 2}
     del w8s, gs
+    # int3-g64 two-plane GEMV, 14336 x 4096, one token (16 rotating copies, 410 MB)
+    rng3 = np.random.default_rng(3)
+    w3q = [torch.from_numpy(rng3.integers(0, 256, size=(N, K // 64 * 24), dtype=np.uint8)).to(dev)
+           for _ in range(C)]
+    s3 = torch.from_numpy(sc).to(dev)
+    gs = [graph_of(lambda: [q.qmv_int3_gs(w3q[i], s3, xd, y=y, stream=stream) for i in range(C)],
+                   stream)]
+    time_graphs(gs, 4, stream)
+    t = time_graphs(gs, 32, stream) / C
+    B3q = N * K // 64 * 24 + sc.nbytes + x.nbytes + N * 4
+    rows["int3_gemv_14336x4096"] = {"us": t * 1e6, "GBs": B3q / t / 1e9,
+                                    "frac": B3q / t / 1e9 / peak, "bytes": B3q,
+                                    "launches_per_call": 1, "path": "CUDA cores, warp per row"}
+    del w3q, gs
     # small-S dense decode: 4 tokens against the 14336 x 4096 int4 matrix (weights read once)
     wqs = [torch.from_numpy(wq).to(dev) for _ in range(C)]
     x4 = torch.from_numpy(np.random.default_rng(11).normal(size=(4, K)).astype(np.float32)).to(dev)

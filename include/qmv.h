@@ -107,6 +107,25 @@ int qmv_int4_gs_pair(const uint8_t *wq0, const float *s0, int N0, const uint8_t 
                      const float *s1, int N1, int K, int gs, const float *x, float *y0, float *y1,
                      int S, void *ws, size_t ws_bytes, qmv_stream_t stream);
 
+/* Dense int3-g64 GEMV over two-plane rows (colibri PR #418, the fmt-5
+ * commit: 24 bytes per 64-group, lanes striding the 16-value low-plane words,
+ * the high-plane word pre-shifted to bit 0, group scales applied to the word
+ * partials). The pages name the planes but print no byte; the layout read
+ * here: in each 24-byte group, bytes 0..15 hold 2 low bits per element
+ * (element e at bits 2(e%4) of byte e/4) and bytes 16..23 one high bit per
+ * element (bit e%8 of byte 16 + e/8); code = low | high << 2, value = code - 4.
+ *     y[s][i] = sum_g scales[i][g] * sum_{k in group g} (code(i,k) - 4) * x[s][k]
+ *   wq3     [N][K/64 * 24] uint8, 4-byte aligned
+ *   scales  [N][K/gs] fp32, 4-byte aligned
+ *   x       [S][K] fp32, 16-byte aligned
+ *   y       [S][N] fp32 (written, fp32-accumulated)
+ *   gs must be 64; K a multiple of 64; 1 <= N, 1 <= S, K <= 65536. No
+ *   workspace: one warp a row decodes each 32-bit low-plane word once for all
+ *   tokens, on the CUDA cores.
+ * Errors: QMV_EINVAL, QMV_ESHAPE (K), QMV_EALIGN, QMV_ECUDA. */
+int qmv_int3_gs(const uint8_t *wq3, const float *scales, int N, int K, int gs, const float *x,
+                float *y, int S, qmv_stream_t stream);
+
 /* Dense int8 per-row-scale GEMV (same commit, fmt 1):
  *     y[s][i] = row_scale[i] * sum_k w[i][k] * x[s][k]
  *   w [N][K] int8 (16-byte aligned), row_scale [N] fp32, x [S][K] fp32, y [S][N] fp32,

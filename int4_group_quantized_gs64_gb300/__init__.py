@@ -63,6 +63,7 @@ def lib():
             "qmv_int4_gs": ([vp, vp, i32, i32, i32, vp, vp, i32, vp, sz, vp], i32),
             "qmv_int4_gs_pair": ([vp, vp, i32, vp, vp, i32, i32, i32, vp, vp, vp, i32, vp, sz, vp],
                                  i32),
+            "qmv_int3_gs": ([vp, vp, i32, i32, i32, vp, vp, i32, vp], i32),
             "qmv_int8_row": ([vp, vp, i32, i32, vp, vp, i32, vp, sz, vp], i32),
             "moe_route_topk": ([vp, i32, i32, i32, vp, vp, vp], i32),
             "moe_group": ([vp, i32, i32, i32, vp, vp, vp, vp, vp, vp], i32),
@@ -167,6 +168,24 @@ def qmv_int4_gs_pair(wq0, s0, wq1, s1, x, y0=None, y1=None, gs: int = 64, ws=Non
            lib().qmv_int4_gs_pair(_ptr(wq0), _ptr(s0), N0, _ptr(wq1), _ptr(s1), N1, K, gs, _ptr(x2),
                                   _ptr(y0), _ptr(y1), S, _ptr(ws), ws.numel(), _stream(stream)))
     return y0, y1
+
+
+def qmv_int3_gs(wq3, scales, x, y=None, gs: int = 64, stream=None):
+    """y[S][N] = int3-g64 two-plane W . x  (wq3 uint8 [N][K/64*24], scales fp32 [N][K/64])."""
+    import torch
+    _need(wq3, torch.uint8, "wq3"); _need(scales, torch.float32, "scales")
+    _need(x, torch.float32, "x")
+    N, K = wq3.shape[0], wq3.shape[1] // 24 * 64
+    if wq3.shape[1] % 24:
+        raise QmvError("qmv_int3_gs: rows must be whole 24-byte groups")
+    x2 = x.view(-1, K)
+    S = x2.shape[0]
+    if y is None:
+        y = torch.empty((S, N), dtype=torch.float32, device=x.device)
+    _need(y, torch.float32, "y")
+    _check("qmv_int3_gs", lib().qmv_int3_gs(_ptr(wq3), _ptr(scales), N, K, gs, _ptr(x2), _ptr(y),
+                                            S, _stream(stream)))
+    return y
 
 
 def qmv_int8_row(w, row_scale, x, y=None, ws=None, stream=None):

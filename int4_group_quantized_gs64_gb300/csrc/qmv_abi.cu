@@ -119,6 +119,15 @@ int qmv_int4_gs_pair(const uint8_t *wq0, const float *s0, int N0, const uint8_t 
         qmv::launch_gemv_int4_pair(wq0, s0, N0, wq1, s1, N1, K, x, y0, y1, S, ws, cs(stream)));
 }
 
+int qmv_int3_gs(const uint8_t *wq3, const float *scales, int N, int K, int gs, const float *x,
+                float *y, int S, qmv_stream_t stream) {
+    if (!wq3 || !scales || !x || !y || N < 1 || S < 1 || gs != 64) return QMV_EINVAL;
+    if (K < 64 || K % 64 || K > kMaxK) return QMV_ESHAPE;
+    if (!aligned(wq3, 4) || !aligned(scales, 4) || !aligned(x, 16) || !aligned(y, 4))
+        return QMV_EALIGN;
+    return from_cuda(qmv::launch_gemv_int3(wq3, scales, N, K, x, y, S, cs(stream)));
+}
+
 int qmv_int8_row(const int8_t *w, const float *row_scale, int N, int K, const float *x, float *y,
                  int S, void *ws, size_t ws_bytes, qmv_stream_t stream) {
     if (!w || !row_scale || !x || !y || N < 1 || S < 1) return QMV_EINVAL;

@@ -37,7 +37,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("qmv_gemv_workspace_bytes", "qmv_int4_gs", "qmv_int4_gs_pair", "qmv_int8_row",
+    for n in ("qmv_gemv_workspace_bytes", "qmv_int4_gs", "qmv_int4_gs_pair", "qmv_int3_gs",
+              "qmv_int8_row",
               "moe_route_topk", "moe_group", "moe_gate_up_silu",
               "moe_down", "moe_combine", "moe_workspace_bytes", "moe_expert_ffn_int4"):
         assert n in names
@@ -82,6 +83,12 @@ def test_dense_validation(L):
     assert L.qmv_int4_gs_pair(p, p, 8, ctypes.c_void_p(FAKE + 8), p, 8, 64, 64, p, p, p, 1,
                               *ok) == EALIGN
     assert L.qmv_int4_gs_pair(p, p, 8, p, p, 8, 64, 64, p, p, p, 1, p, need - 1, None) == EWORKSPACE
+    # int3: (wq3, scales, N, K, gs, x, y, S, stream), no workspace
+    assert L.qmv_int3_gs(None, p, 8, 64, 64, p, p, 1, None) == EINVAL
+    assert L.qmv_int3_gs(p, p, 8, 64, 32, p, p, 1, None) == EINVAL
+    assert L.qmv_int3_gs(p, p, 8, 96, 64, p, p, 1, None) == ESHAPE
+    assert L.qmv_int3_gs(ctypes.c_void_p(FAKE + 2), p, 8, 64, 64, p, p, 1, None) == EALIGN
+    assert L.qmv_int3_gs(p, p, 8, 64, 64, ctypes.c_void_p(FAKE + 8), p, 1, None) == EALIGN
     assert L.qmv_int8_row(p, None, 8, 64, p, p, 1, *ok) == EINVAL
     assert L.qmv_int8_row(p, p, 8, 100, p, p, 1, *ok) == ESHAPE
     assert L.qmv_int8_row(ctypes.c_void_p(FAKE + 4), p, 8, 64, p, p, 1, *ok) == EALIGN

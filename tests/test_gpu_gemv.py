@@ -113,6 +113,38 @@ def test_int4_pair(N0, N1, K, S):
             assert norm_err(y.cpu().numpy(), ref, den) <= TOL_FP32
 
 
+# int3-g64 two-plane rows: one and many groups, ragged row counts, several
+# token passes (4 a pass), the 14336 x 4096 shape and K = 16384.
+INT3_SHAPES = [(1, 64, 1), (17, 192, 3), (100, 1024, 5), (256, 4096, 8), (14336, 4096, 1),
+               (64, 16384, 2)]
+
+
+@pytest.mark.parametrize("N,K,S", INT3_SHAPES)
+def test_int3_shapes(N, K, S):
+    rng = np.random.default_rng(N * 17 + K + S)
+    wq3 = rng.integers(0, 256, size=(N, K // 64 * 24), dtype=np.uint8)
+    sc = (np.abs(rng.normal(0, 0.02, size=(N, K // 64))) + 1e-4).astype(np.float32)
+    x = rng.normal(size=(S, K)).astype(np.float32)
+    y = q.qmv_int3_gs(dev(wq3), dev(sc), dev(x))
+    torch.cuda.synchronize()
+    ref, den = oracle.qmv_int3_gs(wq3, sc, x)
+    assert norm_err(y.cpu().numpy(), ref, den) <= TOL_FP32
+
+
+def test_int3_all_codes_bit_exact():
+    """Every code at every position, dyadic scales, small-integer x: exact in fp32 too."""
+    rng = np.random.default_rng(13)
+    N, K = 40, 512
+    vals = rng.integers(-4, 4, size=(N, K)).astype(np.int8)
+    wq3 = np.stack([oracle.pack_int3(vals[i]) for i in range(N)])
+    s = (2.0 ** rng.integers(-6, 2, size=(N, K // 64))).astype(np.float32)
+    x = rng.integers(-20, 21, size=(3, K)).astype(np.float32)
+    y = q.qmv_int3_gs(dev(wq3), dev(s), dev(x))
+    torch.cuda.synchronize()
+    ref, _ = oracle.qmv_int3_gs(wq3, s, x)
+    assert np.array_equal(y.cpu().numpy().astype(np.float64), ref)
+
+
 @pytest.mark.parametrize("N,K,S", SHAPES)
 def test_int8_shapes(N, K, S):
     rng = np.random.default_rng(N * 31 + K + S)
