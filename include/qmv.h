@@ -249,6 +249,8 @@ int moe_expert_ffn_int4(const qmv_moe_int4 *m, const float *x, int T, const int3
  * and moe_one_token_path(m, k) == 1 the routing runs inside the
  * single-launch FFN kernel (every thread block routes the token itself; the
  * first writes ids and w), so the call is one kernel after the status clear.
+ * With 2..32 tokens on the tensor-map path the grouping kernel routes the
+ * tokens itself the same way, which saves the routing launch.
  * Errors: those of moe_route_topk and moe_expert_ffn_int4. */
 int moe_route_expert_ffn_int4(const qmv_moe_int4 *m, const float *logits, const float *x, int T,
                               int k, int32_t *ids, float *w, float *out, void *ws, size_t ws_bytes,

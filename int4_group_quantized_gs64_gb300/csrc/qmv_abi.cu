@@ -246,7 +246,8 @@ namespace {
 // The prepare phase with an optional residency bitmap and served mask.
 int prepare_impl(const qmv_moe_int4 *m, const float *x, int T, const int32_t *ids, int k,
                  void *ws, size_t ws_bytes, qmv_stream_t stream, const uint32_t *res,
-                 uint8_t *served) {
+                 uint8_t *served, const float *logits = nullptr, int32_t *ids_out = nullptr,
+                 float *w_out = nullptr) {
     qmv::MoeWorkspace L;
     int r = ffn_check(m, T, k, ws, ws_bytes, L);
     if (r) return r;
@@ -259,7 +260,7 @@ int prepare_impl(const qmv_moe_int4 *m, const float *x, int T, const int32_t *id
         at<int32_t>(ws, L.uexp), at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs),
         at<int32_t>(ws, L.status), x, m->H, at<void>(ws, pk ? L.xpk : L.xcells),
         (pk ? nullptr : at<float>(ws, L.xfac)), cs(stream), 8, pk, at<int32_t>(ws, L.status),
-        (int)(L.status_bytes / 4), true, res, served));
+        (int)(L.status_bytes / 4), true, res, served, logits, ids_out, w_out));
 }
 
 // Whole FFN (moe_expert_ffn_int4 with res == served == null).
@@ -370,6 +371,20 @@ int moe_route_expert_ffn_int4(const qmv_moe_int4 *m, const float *logits, const 
                                     reinterpret_cast<unsigned int *>(at<int32_t>(ws, L.sk_cnt)), st,
                                     nullptr, nullptr, logits, ids, w);
         return from_cuda(e);
+    }
+    if (T <= 32 && packed_units(m, k)) {
+        // a decode micro-batch: the grouping kernel routes the tokens itself
+        qmv::MoeWorkspace L;
+        if ((r = ffn_check(m, T, k, ws, ws_bytes, L))) return r;
+        if (!x || !out) return QMV_EINVAL;
+        if (!aligned(x, 4) || !aligned(out, 4)) return QMV_EALIGN;
+        if ((r = prepare_impl(m, x, T, ids, k, ws, ws_bytes, stream, nullptr, nullptr, logits,
+                              ids, w)))
+            return r;
+        if ((r = moe_ffn_gate_up(m, T, k, ws, ws_bytes, stream))) return r;
+        if ((r = moe_ffn_down(m, T, k, ws, ws_bytes, stream))) return r;
+        return from_cuda(qmv::launch_combine(at<float>(ws, L.y), ids, w, T, k, m->E, m->H, out,
+                                             cs(stream), true));
     }
     if ((r = moe_route_topk(logits, T, m->E, k, ids, w, stream))) return r;
     return moe_expert_ffn_int4(m, x, T, ids, w, k, out, ws, ws_bytes, stream);

@@ -48,7 +48,8 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids,
                          cudaStream_t st);
 cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int32_t *list,
                          int32_t *uexp, int32_t *n_used, int32_t *status, cudaStream_t st);
-// Grouping plus the split of the T activation rows, in one launch. With
+// Grouping plus the split of the T activation rows, in one launch (with
+// logits: routing too, ids / w then written to ids_out / w_out). With
 // packed == true the units go to the pass-packed layout (see MoeWorkspace)
 // instead of per-row cells; zero[0 .. nzero) is cleared first; pdl: launched
 // with programmatic dependent launch.
@@ -57,7 +58,12 @@ cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t 
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
                                cudaStream_t st, int pass_tok = 8, bool packed = false,
                                int32_t *zero = nullptr, int nzero = 0, bool pdl = false,
-                               const uint32_t *res = nullptr, uint8_t *served = nullptr);
+                               const uint32_t *res = nullptr, uint8_t *served = nullptr,
+                               const float *logits = nullptr, int32_t *ids_out = nullptr,
+                               float *w_out = nullptr);
+// Shared memory of the grouping kernel when it also routes (logits != null):
+// every CTA routes the T tokens itself, so T * k pairs and E logits a warp.
+size_t route_smem_bytes(int T, int E, int k);
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
                           int32_t *pass_ofs, cudaStream_t st, bool pdl);
 // Activation rows [R][K] fp32 -> fragment cells [R][K/64][16] uint4 + factors [R][K/64].

@@ -248,9 +248,32 @@ __global__ void __launch_bounds__(1024)
                   int32_t *uexp, int32_t *n_used, int32_t *pass_ofs, int32_t *status,
                   const float *__restrict__ x, int H, uint4 *xcells, float *xfac, int pass_tok,
                   int k, int packed, int32_t *zero, int nzero, const uint32_t *res,
-                  uint8_t *served) {
+                  uint8_t *served, const float *__restrict__ logits, int32_t *ids_out,
+                  float *w_out) {
     pdl_wait();
     pdl_trigger();
+    if (logits) {
+        // routing folded in: every CTA routes all T = P / k tokens itself (a
+        // warp a token, the moe_route_topk code) into shared memory, so no
+        // CTA waits for another; CTA 0 writes ids and w out
+        extern __shared__ float route_smem[];  // [32 warps][E] rows, then ids
+        const int T = P / k, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        int32_t *rids = reinterpret_cast<int32_t *>(route_smem + 32 * E);
+        for (int t = warp; t < T; t += 32) {
+            int my_id;
+            float my_w;
+            route_warp(logits + (size_t)t * E, E, k, route_smem + warp * E, my_id, my_w);
+            if (lane < k) {
+                rids[t * k + lane] = my_id;
+                if (blockIdx.x == 0) {
+                    ids_out[t * k + lane] = my_id;
+                    w_out[t * k + lane] = my_w;
+                }
+            }
+        }
+        __syncthreads();
+        ids = rids;
+    }
     if (blockIdx.x == 0) {
         if (zero) {
             for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
@@ -606,18 +629,32 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int
     return launch(k_group_split, dim3(1), dim3(1024), 0, st, false, ids, P, E, offsets, list, uexp,
                   n_used, (int32_t *)nullptr, status, (const float *)nullptr, 64,
                   (uint4 *)nullptr, (float *)nullptr, (int)kMaxTok, 1, 0, (int32_t *)nullptr, 0,
-                  (const uint32_t *)nullptr, (uint8_t *)nullptr);
+                  (const uint32_t *)nullptr, (uint8_t *)nullptr, (const float *)nullptr,
+                  (int32_t *)nullptr, (float *)nullptr);
 }
 
 cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
                                int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
                                cudaStream_t st, int pass_tok, bool packed, int32_t *zero,
-                               int nzero, bool pdl, const uint32_t *res, uint8_t *served) {
+                               int nzero, bool pdl, const uint32_t *res, uint8_t *served,
+                               const float *logits, int32_t *ids_out, float *w_out) {
     const int C = (H / kGroup + 31) / 32;  // CTAs per token row
-    return launch(k_group_split, dim3(x ? 1 + T * C : 1), dim3(1024), 0, st, pdl, ids, T * k, E,
-                  offsets, list, uexp, n_used, pass_ofs, status, x, H, static_cast<uint4 *>(xcells),
-                  xfac, pass_tok, k, packed ? 1 : 0, zero, nzero, res, served);
+    const size_t smem = logits ? route_smem_bytes(T, E, k) : 0;
+    if (smem) {
+        // with ~33 KB of static shared memory, even a small dynamic part
+        // needs the opt-in (set_smem only opts in above 48 KB)
+        cudaError_t e = set_smem(k_group_split, std::max(smem, (size_t)49 * 1024));
+        if (e != cudaSuccess) return e;
+    }
+    return launch(k_group_split, dim3(x ? 1 + T * C : 1), dim3(1024), smem, st, pdl, ids, T * k,
+                  E, offsets, list, uexp, n_used, pass_ofs, status, x, H,
+                  static_cast<uint4 *>(xcells), xfac, pass_tok, k, packed ? 1 : 0, zero, nzero, res,
+                  served, logits, ids_out, w_out);
+}
+
+size_t route_smem_bytes(int T, int E, int k) {
+    return (size_t)32 * E * sizeof(float) + (size_t)T * k * sizeof(int32_t);
 }
 
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
