@@ -424,16 +424,39 @@ def run_ours(args):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n_e2e = max(args.steps, 10)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for s in range(n_e2e):
-            i = s % ROTATE
+    # Copies run on their own streams so that step s+1's inputs travel while
+    # step s computes; buffer i (of ROTATE) is reused only after the compute
+    # and the read-back that used it before have finished. Every step's H2D
+    # and D2H copies lie inside the timed region.
+    st_h, st_d = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_h = [torch.cuda.Event() for _ in range(ROTATE)]
+    ev_c = [torch.cuda.Event() for _ in range(ROTATE)]
+    ev_d = [torch.cuda.Event() for _ in range(ROTATE)]
+    e0.record(stream)
+    st_h.wait_event(e0)
+    st_d.wait_event(e0)
+    for s in range(n_e2e):
+        i = s % ROTATE
+        if s >= ROTATE:
+            st_h.wait_event(ev_c[i])  # the compute that read xs[i], ls[i] is done
+        with torch.cuda.stream(st_h):
             xs[i].copy_(hx[i], non_blocking=True)
             ls[i].copy_(hl[i], non_blocking=True)
+            ev_h[i].record(st_h)
+        stream.wait_event(ev_h[i])
+        if s >= ROTATE:
+            stream.wait_event(ev_d[i])  # the read-back of outs[i] is done
+        with torch.cuda.stream(stream):
             q.moe_route_expert_ffn_int4(m, ls[i], xs[i], k, ids=ids[i], w=wv[i], out=outs[i],
                                         ws=wss[i], stream=stream)
+            ev_c[i].record(stream)
+        st_d.wait_event(ev_c[i])
+        with torch.cuda.stream(st_d):
             ho[i].copy_(outs[i], non_blocking=True)
-        e1.record(stream)
+            ev_d[i].record(st_d)
+    for i in range(ROTATE):
+        stream.wait_event(ev_d[i])
+    e1.record(stream)
     e1.synchronize()
     t_e2e = e0.elapsed_time(e1) * 1e-3 / n_e2e
     if ws_n > 1:
