@@ -281,6 +281,29 @@ def run_profile_dense(args):
     return 0
 
 
+def run_profile_int3(args):
+    """ncu case for the int3-g64 GEMV: 14336 x 4096, one token, over 8 rotating
+    weight and scale copies (206 MB, above L2), `--steps` launches each, no timing."""
+    import torch
+    import int4_group_quantized_gs64_gb300 as q
+    q.build()
+    dev = torch.device("cuda")
+    N, K, C = 14336, 4096, 8
+    rng = np.random.default_rng(3)
+    w3 = [torch.from_numpy(rng.integers(0, 256, size=(N, K // 64 * 24), dtype=np.uint8)).to(dev)
+          for _ in range(C)]
+    s3 = [torch.from_numpy((np.abs(rng.normal(0, 0.02, size=(N, K // 64))) + 1e-4)
+                           .astype(np.float32)).to(dev) for _ in range(C)]
+    xd = torch.from_numpy(rng.normal(size=(1, K)).astype(np.float32)).to(dev)
+    y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    for i in range(args.steps * C):
+        q.qmv_int3_gs(w3[i % C], s3[i % C], xd, y=y)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": f"int3-g64 GEMV {N}x{K}, 1 token, {C} weight copies",
+                      "launches": args.steps * C, "kernels_per_launch": 1}))
+    return 0
+
+
 def run_profile_prefill(args):
     """ncu case for the prefill kernels: 512 tokens (H 6144, I 2048, top-8) over
     a pool of `--profile-prefill` experts, `--steps` calls, no timing."""
@@ -562,16 +585,17 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     rng3 = np.random.default_rng(3)
     w3q = [torch.from_numpy(rng3.integers(0, 256, size=(N, K // 64 * 24), dtype=np.uint8)).to(dev)
            for _ in range(C)]
-    s3 = torch.from_numpy(sc).to(dev)
-    gs = [graph_of(lambda: [q.qmv_int3_gs(w3q[i], s3, xd, y=y, stream=stream) for i in range(C)],
-                   stream)]
+    s3 = [torch.from_numpy(sc).to(dev) for _ in range(C)]
+    gs = [graph_of(lambda: [q.qmv_int3_gs(w3q[i], s3[i], xd, y=y, stream=stream)
+                            for i in range(C)], stream)]
     time_graphs(gs, 4, stream)
     t = time_graphs(gs, 32, stream) / C
     B3q = N * K // 64 * 24 + sc.nbytes + x.nbytes + N * 4
     rows["int3_gemv_14336x4096"] = {"us": t * 1e6, "GBs": B3q / t / 1e9,
                                     "frac": B3q / t / 1e9 / peak, "bytes": B3q,
-                                    "launches_per_call": 1, "path": "CUDA cores, warp per row"}
-    del w3q, gs
+                                    "launches_per_call": 1,
+                                    "path": "CUDA cores, warps walking rows, x staged in shared memory"}
+    del w3q, s3, gs
     # small-S dense decode: 4 tokens against the 14336 x 4096 int4 matrix (weights read once)
     wqs = [torch.from_numpy(wq).to(dev) for _ in range(C)]
     x4 = torch.from_numpy(np.random.default_rng(11).normal(size=(4, K)).astype(np.float32)).to(dev)
@@ -695,6 +719,8 @@ def main():
                     help="run the small ncu case with this many experts instead of the bench")
     ap.add_argument("--profile-dense", action="store_true",
                     help="run the small ncu case of the dense GEMV instead of the bench")
+    ap.add_argument("--profile-int3", action="store_true",
+                    help="run the small ncu case of the int3 GEMV instead of the bench")
     ap.add_argument("--profile-prefill", type=int, default=0,
                     help="run the small ncu case of the prefill with this many experts")
     args = ap.parse_args()
@@ -704,6 +730,8 @@ def main():
         return run_profile_case(args)
     if args.profile_dense:
         return run_profile_dense(args)
+    if args.profile_int3:
+        return run_profile_int3(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -120,8 +120,9 @@ int qmv_int4_gs_pair(const uint8_t *wq0, const float *s0, int N0, const uint8_t 
  *   x       [S][K] fp32, 16-byte aligned
  *   y       [S][N] fp32 (written, fp32-accumulated)
  *   gs must be 64; K a multiple of 64; 1 <= N, 1 <= S, K <= 65536. No
- *   workspace: one warp a row decodes each 32-bit low-plane word once for all
- *   tokens, on the CUDA cores.
+ *   workspace: on the CUDA cores, each warp walks its rows and decodes each
+ *   32-bit low-plane word once for up to 4 tokens; x is staged per CTA in up
+ *   to 96 KB of shared memory (read from global memory when K > 24576).
  * Errors: QMV_EINVAL, QMV_ESHAPE (K), QMV_EALIGN, QMV_ECUDA. */
 int qmv_int3_gs(const uint8_t *wq3, const float *scales, int N, int K, int gs, const float *x,
                 float *y, int S, qmv_stream_t stream);

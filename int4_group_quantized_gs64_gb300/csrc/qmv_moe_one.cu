@@ -12,13 +12,15 @@
 // With one token every expert is read once and the whole layer is only a
 // few MB, so the separate grouping, gate+up, down and combine launches cost
 // more than the bytes. Here one cooperative launch (one CTA per SM) does it:
-//   * at start, thread 0 requests the CTA's whole share of weights and scales
-//     by bulk copy: gate+up tiles t = CTA, CTA + grid, ... (a tile is 8 gate
-//     rows and the 8 up rows of the same hidden units) and down row tiles
-//     (16 output rows of every routed expert);
-//   * while they land, the CTA splits x into its activation units;
-//   * gate+up: the 8 warps split a tile's 64-groups, their partial sums are
-//     added in warp order and lane (gid, q = 0) writes h of unit gid;
+//   * at start, a producer warp requests the CTA's whole share of weights
+//     and scales by bulk copy: gate+up tiles t = CTA, CTA + grid, ... (a tile
+//     is 8 gate rows and the 8 up rows of the same hidden units; one
+//     transaction barrier each) and down row tiles (16 output rows of every
+//     routed expert);
+//   * while they land, the 8 compute warps split x into activation units;
+//   * gate+up, tile by tile as each lands: the 8 warps split the tile's
+//     64-groups, their partial sums are added in warp order and one thread
+//     per hidden unit writes h;
 //   * one grid-wide barrier (every h written);
 //   * down: the CTA splits h into units, warp p computes expert p's 16-row
 //     tile and out = sum_p w_p y_p is added in expert order.
@@ -44,8 +46,9 @@ namespace qmv {
 
 namespace {
 
-constexpr int kOWarps = 8;
-constexpr int kOThreads = 32 * kOWarps;
+constexpr int kOWarps = 8;                  // compute warps; warp kOWarps issues the copies
+constexpr int kOThreads = 32 * (kOWarps + 1);
+constexpr int kOMaxT1 = 64;                 // gate+up tiles per CTA (one barrier each)
 constexpr uint32_t kOWait = 1u << 24;
 constexpr int kOMaxK = 32;              // routed experts per token
 constexpr int kOSmemMax = 220 * 1024;   // dynamic shared memory budget
@@ -74,7 +77,8 @@ struct OneArgs {
 };
 
 struct OneShared {
-    uint64_t mb1, mb2;     // gate+up / down copies landed
+    uint64_t mb1[kOMaxT1]; // gate+up tile i landed
+    uint64_t mb2;          // down copies landed
     int ids[kOMaxK];
     float w[kOMaxK];
 };
@@ -99,6 +103,11 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned int *p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// The compute warps only (the producer warp does not take part).
+__device__ __forceinline__ void compute_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kOWarps) : "memory");
 }
 
 // All CTAs of the (cooperative) grid: every write before it is visible to
@@ -232,136 +241,132 @@ __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant_
         if (b == 0 && a.served) a.served[threadIdx.x] = e >= 0 ? 1 : 0;
     }
     if (threadIdx.x == 0) {
-        tc05::mbar_init(&sh.mb1, 1);
+        for (int i = 0; i < n1; ++i) tc05::mbar_init(&sh.mb1[i], 1);
         tc05::mbar_init(&sh.mb2, 1);
         tc05::fence_mbar_init();
     }
     __syncthreads();
 
-    // ---- every copy of the CTA's share, requested at once by thread 0 (a
-    // few large bulk copies: the copy engine takes commands one by one): per
-    // gate+up tile its 8 gate rows, its 8 up rows and their scales, per down
-    // row tile and expert 16 rows and their scales
-    if (threadIdx.x == 0) {
-        uint32_t bytes1 = 0, bytes2 = 0;
-        for (int i = 0; i < n1; ++i)
-            if (sh.ids[(b + i * grid) / (I / 8)] >= 0) bytes1 += t1b;
-        for (int p = 0; p < k; ++p)
-            if (sh.ids[p] >= 0) bytes2 += (uint32_t)n2 * e2b;
-        expect_tx(&sh.mb1, bytes1);
-        expect_tx(&sh.mb2, bytes2);
-        for (int i = 0; i < n1; ++i) {
-            const int t = b + i * grid, p = t / (I / 8), u0 = 8 * (t % (I / 8)), e = sh.ids[p];
-            if (e < 0) continue;
-            const uint32_t dw = tc05::smem_addr(base + a.o_w1 + i * t1b);
-            const uint32_t ds = dw + 16u * rb1;
-            const size_t rg = (size_t)e * 2 * I + u0, ru = rg + I;   // gate / up rows
-            bulk_g2s(dw, a.gu_q + rg * (H / 2), 8u * rb1, &sh.mb1);
-            bulk_g2s(dw + 8u * rb1, a.gu_q + ru * (H / 2), 8u * rb1, &sh.mb1);
-            bulk_g2s(ds, a.gu_s + rg * GH, 8u * GH * 4, &sh.mb1);
-            bulk_g2s(ds + 8u * GH * 4, a.gu_s + ru * GH, 8u * GH * 4, &sh.mb1);
-        }
-        for (int i = 0; i < n2; ++i)
-            for (int p = 0; p < k; ++p) {
-                const int e = sh.ids[p];
-                if (e < 0) continue;
-                const uint32_t dw = tc05::smem_addr(base + a.o_w2 + i * t2b) + (uint32_t)p * e2b;
-                const size_t r0 = (size_t)e * H + 16 * (b + i * grid);
-                bulk_g2s(dw, a.dn_q + r0 * (I / 2), 16u * rb2, &sh.mb2);
-                bulk_g2s(dw + 16u * rb2, a.dn_s + r0 * GI, 16u * GI * 4, &sh.mb2);
-            }
-    }
-
-    // ---- x -> activation units (each CTA its own copy)
-    uint4 *xu = reinterpret_cast<uint4 *>(base + a.o_xu);
-    float *xf = reinterpret_cast<float *>(base + a.o_xf);
-    float *red = reinterpret_cast<float *>(base + a.o_red);
-    float *scratch = reinterpret_cast<float *>(base + a.o_scr) + warp * 8 * 64;
-    if (warp > 0) split_groups(a.x, GH, xu, xf, scratch, warp - 1, kOWarps - 1);  // warp 0 copies
-    __syncthreads();
-
     bool timed_out = false;
-    if (!tc05::mbar_wait(&sh.mb1, 0, kOWait)) timed_out = true;
-
-    // ---- gate+up: warp w takes groups w, w + 8, ... of every tile (four
-    // tiles at a time share the group's activation units); the partial sums
-    // red[tile][warp][16] are then added in warp order
-    for (int i0 = 0; i0 < n1; i0 += 4) {
-        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c8[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int g = warp; g < GH; g += kOWarps) {
-            uint4 bu[1][2];
-            load_units(xu + g * 16, bu);
-            const float f = xf[g];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i = i0 + j;
-                if (i < n1) {
-                    const uint8_t *rows = base + a.o_w1 + i * t1b;
-                    const float *sc = reinterpret_cast<const float *>(rows + 16 * rb1);
-                    tile_group_one(rows, rb1, g, bu, f, sc[gid * GH + g], sc[(gid + 8) * GH + g],
-                                   c0[j], c8[j]);
+    if (warp == kOWarps) {
+        // ---- producer: every copy of the CTA's share, requested at once (a
+        // few large bulk copies: the copy engine takes commands one by one):
+        // per gate+up tile its 8 gate rows, its 8 up rows and their scales,
+        // then per down row tile and expert 16 rows and their scales
+        if (lane == 0) {
+            uint32_t bytes2 = 0;
+            for (int p = 0; p < k; ++p)
+                if (sh.ids[p] >= 0) bytes2 += (uint32_t)n2 * e2b;
+            expect_tx(&sh.mb2, bytes2);
+            for (int i = 0; i < n1; ++i) {
+                const int t = b + i * grid, p = t / (I / 8), u0 = 8 * (t % (I / 8)), e = sh.ids[p];
+                expect_tx(&sh.mb1[i], e >= 0 ? t1b : 0u);
+                if (e < 0) continue;
+                const uint32_t dw = tc05::smem_addr(base + a.o_w1 + i * t1b);
+                const uint32_t ds = dw + 16u * rb1;
+                const size_t rg = (size_t)e * 2 * I + u0, ru = rg + I;   // gate / up rows
+                bulk_g2s(dw, a.gu_q + rg * (H / 2), 8u * rb1, &sh.mb1[i]);
+                bulk_g2s(dw + 8u * rb1, a.gu_q + ru * (H / 2), 8u * rb1, &sh.mb1[i]);
+                bulk_g2s(ds, a.gu_s + rg * GH, 8u * GH * 4, &sh.mb1[i]);
+                bulk_g2s(ds + 8u * GH * 4, a.gu_s + ru * GH, 8u * GH * 4, &sh.mb1[i]);
+            }
+            for (int i = 0; i < n2; ++i)
+                for (int p = 0; p < k; ++p) {
+                    const int e = sh.ids[p];
+                    if (e < 0) continue;
+                    const uint32_t dw =
+                        tc05::smem_addr(base + a.o_w2 + i * t2b) + (uint32_t)p * e2b;
+                    const size_t r0 = (size_t)e * H + 16 * (b + i * grid);
+                    bulk_g2s(dw, a.dn_q + r0 * (I / 2), 16u * rb2, &sh.mb2);
+                    bulk_g2s(dw + 16u * rb2, a.dn_s + r0 * GI, 16u * GI * 4, &sh.mb2);
                 }
+        }
+        __syncwarp();
+    } else {
+        // ---- x -> activation units (each CTA its own copy)
+        uint4 *xu = reinterpret_cast<uint4 *>(base + a.o_xu);
+        float *xf = reinterpret_cast<float *>(base + a.o_xf);
+        float *red = reinterpret_cast<float *>(base + a.o_red);
+        float *scratch = reinterpret_cast<float *>(base + a.o_scr) + warp * 8 * 64;
+        split_groups(a.x, GH, xu, xf, scratch, warp, kOWarps);
+        compute_sync();
+
+        // ---- gate+up, tile by tile as each lands: warp w takes groups w,
+        // w + 8, ... of the tile; the partial sums red[tile][warp][16] are then
+        // added in warp order
+        for (int i = 0; i < n1; ++i) {
+            if (!tc05::mbar_wait(&sh.mb1[i], 0, kOWait)) timed_out = true;
+            const uint8_t *rows = base + a.o_w1 + i * t1b;
+            const float *sc = reinterpret_cast<const float *>(rows + 16 * rb1);
+            float c0 = 0.f, c8 = 0.f;
+            for (int g = warp; g < GH; g += kOWarps) {
+                uint4 bu[1][2];
+                load_units(xu + g * 16, bu);
+                tile_group_one(rows, rb1, g, bu, xf[g], sc[gid * GH + g], sc[(gid + 8) * GH + g],
+                               c0, c8);
+            }
+            if (q == 0) {
+                red[(i * kOWarps + warp) * 16 + gid] = c0;
+                red[(i * kOWarps + warp) * 16 + 8 + gid] = c8;
             }
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (q == 0 && i0 + j < n1) {
-                red[((i0 + j) * kOWarps + warp) * 16 + gid] = c0[j];
-                red[((i0 + j) * kOWarps + warp) * 16 + 8 + gid] = c8[j];
+        compute_sync();
+        for (int c = threadIdx.x; c < n1 * 8; c += 32 * kOWarps) {
+            const int i = c >> 3, u = c & 7, t = b + i * grid;
+            const int p = t / (I / 8), u0 = 8 * (t % (I / 8));
+            float gv = 0.f, uv = 0.f;
+            for (int w = 0; w < kOWarps; ++w) {
+                gv += red[(i * kOWarps + w) * 16 + u];
+                uv += red[(i * kOWarps + w) * 16 + 8 + u];
             }
-    }
-    __syncthreads();
-    for (int c = threadIdx.x; c < n1 * 8; c += kOThreads) {
-        const int i = c >> 3, u = c & 7, t = b + i * grid;
-        const int p = t / (I / 8), u0 = 8 * (t % (I / 8));
-        float gv = 0.f, uv = 0.f;
-        for (int w = 0; w < kOWarps; ++w) {
-            gv += red[(i * kOWarps + w) * 16 + u];
-            uv += red[(i * kOWarps + w) * 16 + 8 + u];
+            const float hv = sh.ids[p] >= 0 ? gv / (1.0f + expf(-gv)) * uv : 0.f;
+            a.h[(size_t)p * I + u0 + u] = hv;
         }
-        const float hv = sh.ids[p] >= 0 ? gv / (1.0f + expf(-gv)) * uv : 0.f;
-        a.h[(size_t)p * I + u0 + u] = hv;
     }
 
     if (!grid_barrier(a.bar)) timed_out = true;
 
-    // ---- h -> activation units (each CTA its own copy), then down + combine
-    uint4 *hu = reinterpret_cast<uint4 *>(base + a.o_hu);
-    float *hf = reinterpret_cast<float *>(base + a.o_hf);
-    split_groups(a.h, k * GI, hu, hf, scratch, warp, kOWarps);  // c: pair c / GI, group c % GI
-    __syncthreads();
-    if (!tc05::mbar_wait(&sh.mb2, 0, kOWait)) timed_out = true;
-    for (int i = 0; i < n2; ++i) {
-        for (int p = warp; p < k; p += kOWarps) {
-            float c0 = 0.f, c8 = 0.f;
-            if (sh.ids[p] >= 0) {
-                const uint8_t *rows = base + a.o_w2 + i * t2b + p * e2b;
-                const float *sc = reinterpret_cast<const float *>(rows + 16 * rb2);
-                for (int g = 0; g < GI; ++g) {
-                    uint4 bu[1][2];
-                    load_units(hu + (p * GI + g) * 16, bu);
-                    tile_group_one(rows, rb2, g, bu, hf[p * GI + g], sc[gid * GI + g],
-                                   sc[(gid + 8) * GI + g], c0, c8);
+    if (warp < kOWarps) {
+        // ---- h -> activation units (each CTA its own copy), then down + combine
+        uint4 *hu = reinterpret_cast<uint4 *>(base + a.o_hu);
+        float *hf = reinterpret_cast<float *>(base + a.o_hf);
+        float *red = reinterpret_cast<float *>(base + a.o_red);
+        float *scratch = reinterpret_cast<float *>(base + a.o_scr) + warp * 8 * 64;
+        split_groups(a.h, k * GI, hu, hf, scratch, warp, kOWarps);  // c: pair c / GI, group c % GI
+        compute_sync();
+        if (!tc05::mbar_wait(&sh.mb2, 0, kOWait)) timed_out = true;
+        for (int i = 0; i < n2; ++i) {
+            for (int p = warp; p < k; p += kOWarps) {
+                float c0 = 0.f, c8 = 0.f;
+                if (sh.ids[p] >= 0) {
+                    const uint8_t *rows = base + a.o_w2 + i * t2b + p * e2b;
+                    const float *sc = reinterpret_cast<const float *>(rows + 16 * rb2);
+                    for (int g = 0; g < GI; ++g) {
+                        uint4 bu[1][2];
+                        load_units(hu + (p * GI + g) * 16, bu);
+                        tile_group_one(rows, rb2, g, bu, hf[p * GI + g], sc[gid * GI + g],
+                                       sc[(gid + 8) * GI + g], c0, c8);
+                    }
+                }
+                if (q == 0) {
+                    red[p * 16 + gid] = c0;
+                    red[p * 16 + 8 + gid] = c8;
                 }
             }
-            if (q == 0) {
-                red[p * 16 + gid] = c0;
-                red[p * 16 + 8 + gid] = c8;
+            compute_sync();
+            if (threadIdx.x < 16) {
+                float o = 0.f;
+                for (int p = 0; p < k; ++p)
+                    if (sh.ids[p] >= 0) o = fmaf(sh.w[p], red[p * 16 + threadIdx.x], o);
+                a.out[16 * (b + i * grid) + threadIdx.x] = o;
             }
+            compute_sync();
         }
-        __syncthreads();
-        if (threadIdx.x < 16) {
-            float o = 0.f;
-            for (int p = 0; p < k; ++p)
-                if (sh.ids[p] >= 0) o = fmaf(sh.w[p], red[p * 16 + threadIdx.x], o);
-            a.out[16 * (b + i * grid) + threadIdx.x] = o;
-        }
-        __syncthreads();
     }
     if (timed_out && lane == 0) atomicOr(a.status, 2);
     // copies still in flight (only after a wait ran out) land before exit
-    if (threadIdx.x == 0) {
-        tc05::mbar_wait(&sh.mb1, 0, kOWait);
+    if (warp == kOWarps && lane == 0) {
+        for (int i = 0; i < n1; ++i) tc05::mbar_wait(&sh.mb1[i], 0, kOWait);
         tc05::mbar_wait(&sh.mb2, 0, kOWait);
     }
     __syncthreads();
@@ -389,7 +394,7 @@ bool one_layout(const MoeDims &m, int k, int grid, OneArgs &a, size_t &smem) {
     a.o_scr = (int)o; o = up16(o + (size_t)kOWarps * 8 * 64 * 4);
     a.o_lg = (int)o; o = up16(o + (size_t)1024 * 4);  // one routing row (E <= 1024)
     smem = o + 128;
-    return smem <= (size_t)kOSmemMax;
+    return smem <= (size_t)kOSmemMax && a.n1 <= kOMaxT1;
 }
 
 }  // namespace

@@ -114,8 +114,11 @@ def test_int4_pair(N0, N1, K, S):
 
 
 # int3-g64 two-plane rows: one and many groups, ragged row counts, several
-# token passes (4 a pass), the 14336 x 4096 shape and K = 16384.
+# token passes (4 a pass), the 14336 x 4096 shape, K = 16384 and 24576 (x staged
+# in shared memory, fewer tokens a pass) and K = 32768 and 65536 (x read from
+# global memory).
 INT3_SHAPES = [(1, 64, 1), (17, 192, 3), (100, 1024, 5), (256, 4096, 8), (14336, 4096, 1),
+               (9, 32768, 3), (5, 65536, 1), (40, 24576, 2),
                (64, 16384, 2)]
 
 
