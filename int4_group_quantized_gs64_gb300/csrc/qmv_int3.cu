@@ -16,19 +16,21 @@
 // as exact fp32, and used for every token of the pass. The words and scales
 // of the warp's next block of 8 steps (the rest of this row or the start of
 // its next row) are requested before the current block is computed, so a
-// warp always has one row's loads in flight. The partials of a group's four
-// lanes are added with two shuffles and scaled once; the lanes' sums are
-// reduced when the row is done. All arithmetic is fp32 (products of a small
-// integer and an fp32 x are exact). Tokens go in passes of NT = min(S, 4).
+// warp always has one row's loads in flight. Each lane multiplies its
+// word's partial sum by the group scale and keeps its own sum; the lanes'
+// sums are reduced when the row is done. All arithmetic is fp32 (products of
+// a small integer and an fp32 x are exact). Tokens go in passes of
+// NT = min(S, 4).
 //
 // A lane's 16 elements are x[16 l .. 16 l + 15] (relative to the step's 512),
 // so each of its four 16-byte x reads has lanes 64 bytes apart: read from L1
 // that is 16 cache lines per instruction. The CTA therefore first copies the
-// pass's x rows into shared memory with 16-byte chunk c stored at
-// c ^ ((c >> 3) & 3), which puts lanes 0..7 of every read on eight different
-// bank quads (4 wavefronts, the minimum for 512 bytes). When one token's x
-// does not fit the shared-memory budget (K > 24576) x is read from global
-// memory instead.
+// pass's x rows into shared memory, transposed within each block of 128
+// 16-byte chunks (one step): chunk 4 l + q of a block is stored at 32 q + l.
+// A lane's four reads are then 512 bytes apart from one base, and the lanes
+// of each read are consecutive (4 wavefronts, the minimum for 512 bytes).
+// When one token's x does not fit the shared-memory budget (K > 24576) x is
+// read from global memory instead.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -44,8 +46,12 @@ constexpr int kI3Warps = 8;
 constexpr int kI3Steps = 8;  // steps (8 groups each) whose words are requested at once
 constexpr int kI3SmemX = 96 * 1024;  // shared-memory budget for the staged x rows
 
-// Shared-memory slot of 16-byte x chunk c (see above).
-__device__ __forceinline__ int i3_swz(int c) { return c ^ ((c >> 3) & 3); }
+// Shared-memory slot of 16-byte x chunk c (see above), and the chunks a
+// token takes there (a whole number of 128-chunk blocks).
+__device__ __forceinline__ int i3_slot(int c) {
+    return (c & ~127) | ((c & 3) << 5) | ((c & 127) >> 2);
+}
+__host__ __device__ __forceinline__ int i3_chunks(int K) { return ((K / 4 + 127) / 128) * 128; }
 
 // A block of one row: kI3Steps steps of this lane's words and group scales.
 struct I3Block {
@@ -97,10 +103,10 @@ __device__ __forceinline__ void i3_load(const uint8_t *__restrict__ wq,
     }
 }
 
-// Adds the block's scaled group sums for tokens 0 .. nt - 1 of xt (rows of
-// K floats) to acc (meaningful in lanes l % 4 == 0).
-// xt: the pass's x rows (K floats each), in shared memory (chunks swizzled)
-// when STAGED, else in global memory.
+// Adds the lane's scaled word partials of the block for tokens 0 .. nt - 1
+// to acc.
+// xt: the pass's x rows, in shared memory (i3_chunks(K) chunks a token, laid
+// out as above) when STAGED, else in global memory (K floats a token).
 template <int NT, bool STAGED>
 __device__ __forceinline__ void i3_compute(const I3Block &u, int G, int gb,
                                            const float *__restrict__ xt, int K, int nt,
@@ -115,14 +121,17 @@ __device__ __forceinline__ void i3_compute(const I3Block &u, int G, int gb,
         if (g < G) {
             float v[16];
             decode16(u.lo[st], u.hi[st] >> (16 * (w & 1)), v);
-            const int c0 = 16 * g + 4 * w;  // the lane's first x chunk
+            // the lane's first x chunk: 16 g + 4 w, global; 32 q + lane in the
+            // step's shared block (gb is a multiple of 64, so block gb / 8 + st)
+            const int c0 = STAGED ? (((gb >> 3) + st) << 7) + lane : 16 * g + 4 * w;
+            const int ct = STAGED ? i3_chunks(K) : K / 4;  // chunks a token
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
                 if (t < nt) {
-                    const float4 *xp = reinterpret_cast<const float4 *>(xt + (size_t)t * K);
+                    const float4 *xp = reinterpret_cast<const float4 *>(xt) + (size_t)t * ct + c0;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const float4 xv = STAGED ? xp[i3_swz(c0 + q)] : __ldg(xp + c0 + q);
+                        const float4 xv = STAGED ? xp[32 * q] : __ldg(xp + q);
                         part[t] = fmaf(v[4 * q + 0], xv.x, part[t]);
                         part[t] = fmaf(v[4 * q + 1], xv.y, part[t]);
                         part[t] = fmaf(v[4 * q + 2], xv.z, part[t]);
@@ -132,12 +141,7 @@ __device__ __forceinline__ void i3_compute(const I3Block &u, int G, int gb,
             }
         }
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            // the group's four word partials, then its scale (one lane adds it)
-            float p = part[t] + __shfl_xor_sync(0xffffffffu, part[t], 1);
-            p += __shfl_xor_sync(0xffffffffu, p, 2);
-            if (w == 0) acc[t] = fmaf(u.sc[st], p, acc[t]);
-        }
+        for (int t = 0; t < NT; ++t) acc[t] = fmaf(u.sc[st], part[t], acc[t]);
     }
 }
 
@@ -149,7 +153,7 @@ __global__ void __launch_bounds__(32 * kI3Warps)
     const int lane = threadIdx.x & 31;
     const int i0 = blockIdx.x * kI3Warps + (threadIdx.x >> 5), nw = gridDim.x * kI3Warps;
     const int G = K / 64, span = 8 * kI3Steps, nb = (G + span - 1) / span;  // blocks per row
-    const int kc = K / 4;                                                    // x chunks per token
+    const int kc = K / 4, kcs = i3_chunks(K);  // x chunks a token: in x, staged
     for (int t0 = 0; t0 < S; t0 += NT) {
         const int nt = min(NT, S - t0);
         I3Block cur, nxt;
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(32 * kI3Warps)
             const float4 *src = reinterpret_cast<const float4 *>(xt);
             for (int c = threadIdx.x; c < nt * kc; c += blockDim.x) {
                 const int t = c / kc, cc = c - t * kc;
-                xs4[t * kc + i3_swz(cc)] = __ldg(src + c);
+                xs4[t * kcs + i3_slot(cc)] = __ldg(src + c);
             }
             __syncthreads();
             xt = reinterpret_cast<const float *>(xs4);
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(32 * kI3Warps)
 template <int NT, bool STAGED>
 cudaError_t launch_int3_nt(const uint8_t *wq, const float *scales, int N, int K, const float *x,
                            float *y, int S, cudaStream_t st) {
-    const size_t smem = STAGED ? (size_t)NT * K * 4 : 0;
+    const size_t smem = STAGED ? (size_t)NT * i3_chunks(K) * 16 : 0;
     cudaError_t e = set_smem(k_int3_gemv<NT, STAGED>, smem);
     if (e != cudaSuccess) return e;
     const int rows_blocks = (N + kI3Warps - 1) / kI3Warps;
@@ -215,7 +219,7 @@ cudaError_t launch_int3_nt(const uint8_t *wq, const float *scales, int N, int K,
 cudaError_t launch_gemv_int3(const uint8_t *wq, const float *scales, int N, int K, const float *x,
                              float *y, int S, cudaStream_t st) {
     // tokens per pass: up to 4, as many as the staged x rows allow
-    const int fit = kI3SmemX / (K * 4);
+    const int fit = kI3SmemX / (i3_chunks(K) * 16);
     if (fit < 1) {
         switch (std::min(S, 4)) {
             case 1: return launch_int3_nt<1, false>(wq, scales, N, K, x, y, S, st);

@@ -72,6 +72,58 @@ def test_route_many_experts_and_k32():
     assert np.allclose(w.cpu().numpy(), rw, rtol=TOL_W, atol=0)
 
 
+def _lane_heavy(rng, T, E):
+    """Logits whose largest values all sit on experts 3, 35, 67, ...: one lane
+    of the routing warp holds the top, so it wins round after round (and has
+    to rescan its experts every other round)."""
+    logits = rng.normal(size=(T, E)).astype(np.float32)
+    logits[:, 3::32] += 10.0
+    return logits
+
+
+@pytest.mark.parametrize("T,k,E", [(2, 32, 1024), (5, 8, 256), (3, 16, 40), (4, 8, 160)])
+def test_route_one_lane_holds_the_top(T, k, E):
+    rng = np.random.default_rng(7 * T + k + E)
+    logits = _lane_heavy(rng, T, E)
+    ids, w = q.moe_route_topk(dev(logits), k)
+    torch.cuda.synchronize()
+    rid, rw = oracle.route_topk(logits, k)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.allclose(w.cpu().numpy(), rw, rtol=TOL_W, atol=0)
+
+
+def test_route_signed_zero_inf_and_nan_ties():
+    """+0 and -0 tie (the lower index first), -inf ties with -inf and NaN
+    counts as -inf: ids bit-exact against the oracle on the logits with NaN
+    replaced by -inf."""
+    rng = np.random.default_rng(29)
+    vals = np.array([0.0, -0.0, -np.inf, np.nan, 1.0, -1.0], np.float32)
+    for E, k in ((64, 16), (200, 32), (33, 32)):
+        logits = rng.choice(vals, size=(6, E)).astype(np.float32)
+        ids, _ = q.moe_route_topk(dev(logits), k)
+        torch.cuda.synchronize()
+        rid, _ = oracle.route_topk(np.where(np.isnan(logits), -np.inf, logits).astype(np.float32), k)
+        assert np.array_equal(ids.cpu().numpy(), rid), (E, k)
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_route_ffn_fused_lane_heavy_logits(T):
+    """The in-kernel routing of the one-token kernel (T = 1) and of the
+    grouping kernel (T = 3) on logits that make one lane win repeatedly."""
+    E, H, I, k = 256, 256, 256, 8
+    rng = np.random.default_rng(40 + T)
+    wts = _rand_pool(rng, E, H, I)
+    m = q.MoeInt4Weights.from_numpy(wts)
+    x = rng.normal(size=(T, H)).astype(np.float32)
+    logits = _lane_heavy(rng, T, E)
+    out, ids, w = q.moe_route_expert_ffn_int4(m, dev(logits), dev(x), k)
+    torch.cuda.synchronize()
+    rid, rw = oracle.route_topk(logits, k)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    ref = oracle.moe_ffn(wts, x.astype(np.float64), rid, rw.astype(np.float32))
+    assert norm_err(out.cpu().numpy(), ref["out"], ref["den"]) <= TOL_FP32
+
+
 @pytest.mark.parametrize("T,k,E", [(1, 8, 256), (8, 8, 160), (512, 8, 160), (33, 2, 7),
                                    (3000, 4, 1024), (5, 3, 6)])
 def test_group_matches_oracle(T, k, E):
