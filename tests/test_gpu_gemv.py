@@ -134,10 +134,12 @@ def test_int3_shapes(N, K, S):
     assert norm_err(y.cpu().numpy(), ref, den) <= TOL_FP32
 
 
-def test_int3_all_codes_bit_exact():
-    """Every code at every position, dyadic scales, small-integer x: exact in fp32 too."""
-    rng = np.random.default_rng(13)
-    N, K = 40, 512
+@pytest.mark.parametrize("K", [512, 2048])
+def test_int3_all_codes_bit_exact(K):
+    """Every code at every position, dyadic scales, small-integer x: exact in
+    fp32 too (one x block a row at K = 512, several at 2048)."""
+    rng = np.random.default_rng(13 + K)
+    N = 40
     vals = rng.integers(-4, 4, size=(N, K)).astype(np.int8)
     wq3 = np.stack([oracle.pack_int3(vals[i]) for i in range(N)])
     s = (2.0 ** rng.integers(-6, 2, size=(N, K // 64))).astype(np.float32)
@@ -146,6 +148,39 @@ def test_int3_all_codes_bit_exact():
     torch.cuda.synchronize()
     ref, _ = oracle.qmv_int3_gs(wq3, s, x)
     assert np.array_equal(y.cpu().numpy().astype(np.float64), ref)
+
+
+def test_int3_weights_not_16_byte_aligned():
+    """Weights 4 bytes past a 16-byte boundary (the entry point asks for 4)."""
+    rng = np.random.default_rng(23)
+    N, K, S = 96, 4096, 2
+    rb = K // 64 * 24
+    flat = torch.from_numpy(rng.integers(0, 256, size=N * rb + 16, dtype=np.uint8)).cuda()
+    wq3 = flat[4:4 + N * rb].view(N, rb)
+    assert wq3.data_ptr() % 16 == 4
+    sc = (np.abs(rng.normal(0, 0.02, size=(N, K // 64))) + 1e-4).astype(np.float32)
+    x = rng.normal(size=(S, K)).astype(np.float32)
+    y = q.qmv_int3_gs(wq3, dev(sc), dev(x))
+    torch.cuda.synchronize()
+    ref, den = oracle.qmv_int3_gs(wq3.cpu().numpy(), sc, x)
+    assert norm_err(y.cpu().numpy(), ref, den) <= TOL_FP32
+
+
+def test_int3_extreme_activations():
+    """Activations from 1e-30 to 1e30 (one magnitude a group) and an all-zero
+    group: each group gets its own power-of-two factor before the fp16 split."""
+    rng = np.random.default_rng(17)
+    N, K, S = 48, 1024, 3
+    wq3 = rng.integers(0, 256, size=(N, K // 64 * 24), dtype=np.uint8)
+    sc = (np.abs(rng.normal(0, 0.02, size=(N, K // 64))) + 1e-4).astype(np.float32)
+    mag = 10.0 ** rng.integers(-30, 31, size=(S, K // 64))
+    x = (rng.normal(size=(S, K // 64, 64)) * mag[:, :, None]).reshape(S, K).astype(np.float32)
+    x[:, 64:128] = 0.0
+    y = q.qmv_int3_gs(dev(wq3), dev(sc), dev(x))
+    torch.cuda.synchronize()
+    ref, den = oracle.qmv_int3_gs(wq3, sc, x)
+    assert np.all(np.isfinite(y.cpu().numpy()))
+    assert norm_err(y.cpu().numpy(), ref, den) <= TOL_FP32
 
 
 @pytest.mark.parametrize("N,K,S", SHAPES)
