@@ -213,13 +213,16 @@ __device__ void pair_slots_cta(const int32_t *__restrict__ ids, int P, int E, in
 // Splits token row t into units once and writes them to each of its pairs'
 // (pass, slot) in the pass-packed layout: in block (pi * ns + g / 4) of
 // kPackedStage bytes, the factor at float slot * 4 + g % 4 and the units at
-// byte 128 + slot * 1024 + (g % 4) * 256.
-__device__ void split_row_packed_cta(const float *__restrict__ row, int K, int g0, int k,
-                                     const int *pass, const int *slot, uint8_t *pk) {
+// byte 128 + slot * 1024 + (g % 4) * 256. With 32 warps each warp has one
+// group, g0 + warp: xa / xb are its values lane and 32 + lane, loaded by the
+// caller (0 past the row's last group).
+__device__ void split_row_packed_cta(int K, int g0, int k, const int *pass, const int *slot,
+                                     uint8_t *pk, float xa, float xb) {
     __shared__ float buf[32][64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = K / kGroup, ns = G / 4;
-    for (int g = g0 + warp; g < min(G, g0 + 32); g += blockDim.x >> 5) {
-        const float a = row[g * kGroup + lane], b = row[g * kGroup + 32 + lane];
+    const int g = g0 + warp;
+    if (g < G) {
+        const float a = xa, b = xb;
         const int e = split_exponent(warp_max(fmaxf(fabsf(a), fabsf(b))));
         const float mul = ldexpf(1.0f, e);
         buf[warp][lane] = a * mul;
@@ -233,7 +236,6 @@ __device__ void split_row_packed_cta(const float *__restrict__ row, int K, int g
             if ((lane & 15) == 0)
                 reinterpret_cast<float *>(blk)[slot[j] * 4 + g % 4] = ldexpf(1.0f, -e);
         }
-        __syncwarp();
     }
 }
 
@@ -252,6 +254,18 @@ __global__ void __launch_bounds__(1024)
                   float *w_out) {
     pdl_wait();
     pdl_trigger();
+    // a packed-split CTA (32 warps, one group each) requests its x values
+    // first, so that their latency overlaps routing and the slot scan
+    float xa = 0.f, xb = 0.f;
+    if (packed && blockIdx.x > 0) {
+        const int G = H / kGroup, C = (G + 31) / 32;
+        const int t = (blockIdx.x - 1) / C, g = 32 * ((blockIdx.x - 1) % C) + (threadIdx.x >> 5);
+        if (g < G) {
+            const float *src = x + (size_t)t * H + g * kGroup + (threadIdx.x & 31);
+            xa = src[0];
+            xb = src[32];
+        }
+    }
     if (logits) {
         // routing folded in: every CTA routes all T = P / k tokens itself (a
         // warp a token, the moe_route_topk code) into shared memory, so no
@@ -286,8 +300,7 @@ __global__ void __launch_bounds__(1024)
         if (packed) {
             __shared__ int pass[32], slot[32];
             pair_slots_cta(ids, P, E, k, t, pass_tok, pass, slot, res);
-            split_row_packed_cta(x + (size_t)t * H, H, g0, k, pass, slot,
-                                 reinterpret_cast<uint8_t *>(xcells));
+            split_row_packed_cta(H, g0, k, pass, slot, reinterpret_cast<uint8_t *>(xcells), xa, xb);
         } else {
             split_row_cta(x + (size_t)t * H, H, g0, xcells + (size_t)t * G * 16,
                           xfac + (size_t)t * G);

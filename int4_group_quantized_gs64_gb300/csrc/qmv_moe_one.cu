@@ -22,8 +22,8 @@
 //     64-groups, their partial sums are added in warp order and one thread
 //     per hidden unit writes h;
 //   * one grid-wide barrier (every h written);
-//   * down: the CTA splits h into units, warp p computes expert p's 16-row
-//     tile and out = sum_p w_p y_p is added in expert order.
+//   * down: warp p splits expert p's h into units and computes its 16-row
+//     tile; out = sum_p w_p y_p is added in expert order.
 // Every result is written by exactly one thread after a fixed-order sum, so
 // the output does not depend on timing.
 //
@@ -332,8 +332,10 @@ __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant_
         float *hf = reinterpret_cast<float *>(base + a.o_hf);
         float *red = reinterpret_cast<float *>(base + a.o_red);
         float *scratch = reinterpret_cast<float *>(base + a.o_scr) + warp * 8 * 64;
-        split_groups(a.h, k * GI, hu, hf, scratch, warp, kOWarps);  // c: pair c / GI, group c % GI
-        compute_sync();
+        // warp w splits the h rows of the experts it computes (p = w, w + 8,
+        // ...), so it needs no other warp's units
+        for (int p = warp; p < k; p += kOWarps)
+            split_groups(a.h + (size_t)p * I, GI, hu + p * GI * 16, hf + p * GI, scratch, 0, 1);
         if (!tc05::mbar_wait(&sh.mb2, 0, kOWait)) timed_out = true;
         for (int i = 0; i < n2; ++i) {
             for (int p = warp; p < k; p += kOWarps) {
