@@ -304,6 +304,29 @@ def run_profile_int3(args):
     return 0
 
 
+def run_profile_one(args):
+    """ncu case for the one-token layer (H 2048, E 256, I 512, top-8; k_moe_one):
+    8 seeded tokens in turn, `--steps` rounds, routing in-kernel, no timing."""
+    import torch
+    import datagen
+    import int4_group_quantized_gs64_gb300 as q
+    q.build()
+    dev = torch.device("cuda")
+    wl = W2
+    m = q.MoeInt4Weights.from_numpy(datagen.moe_weights(wl["E"], wl["H"], wl["I"]), dev)
+    bs = w3_batches(wl, 8)
+    xs = [torch.from_numpy(b["x"]).to(dev) for b in bs]
+    ls = [torch.from_numpy(b["logits"]).to(dev) for b in bs]
+    ws = torch.empty(q.moe_workspace_bytes(m, 1, 8), dtype=torch.uint8, device=dev)
+    out = torch.empty((1, wl["H"]), dtype=torch.float32, device=dev)
+    for i in range(args.steps * len(bs)):
+        q.moe_route_expert_ffn_int4(m, ls[i % len(bs)], xs[i % len(bs)], 8, out=out, ws=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": "one-token MoE layer H2048 E256 I512 top8",
+                      "calls": args.steps * len(bs), "one_kernel": q.moe_one_token_path(m, 8) == 1}))
+    return 0
+
+
 def run_profile_prefill(args):
     """ncu case for the prefill kernels: 512 tokens (H 6144, I 2048, top-8) over
     a pool of `--profile-prefill` experts, `--steps` calls, no timing."""
@@ -719,6 +742,8 @@ def main():
                     help="run the small ncu case with this many experts instead of the bench")
     ap.add_argument("--profile-dense", action="store_true",
                     help="run the small ncu case of the dense GEMV instead of the bench")
+    ap.add_argument("--profile-one", action="store_true",
+                    help="run the small ncu case of the one-token layer instead of the bench")
     ap.add_argument("--profile-int3", action="store_true",
                     help="run the small ncu case of the int3 GEMV instead of the bench")
     ap.add_argument("--profile-prefill", type=int, default=0,
@@ -732,6 +757,8 @@ def main():
         return run_profile_dense(args)
     if args.profile_int3:
         return run_profile_int3(args)
+    if args.profile_one:
+        return run_profile_one(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
