@@ -24,14 +24,17 @@
  *           arrives as fmt 4 / grp 64 at half a byte per element; the
  *           weighted accumulation of expert outputs is checked lane by lane).
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *  R1 nibble order: element 2j of a row is the LOW nibble of byte j,
  *     element 2j+1 the HIGH nibble; bytes run in K order.
  *  R2 scales are fp32, row-major [rows][K/gs].
  *  R3 the stacked gate+up tensor holds gate rows 0..I-1, then up rows I..2I-1.
  *  R4 routing: softmax over all experts, select the k largest logits (fp32
  *     compare, the lower expert index wins a tie), renormalise the selected
- *     probabilities to sum to one.
+ *     probabilities to sum to one. A NaN logit counts as -inf: it is never
+ *     chosen ahead of a finite logit and, when chosen, weighs exp(-inf) = 0.
+ *     If every logit of a token is -inf or NaN they are all equal, so the k
+ *     lowest indices are chosen with weight 1/k each.
  *  R5 SiLU(g) = g * sigma(g), sigma(g) = 1 / (1 + exp(-g)).
  *  R6 int3-g64 two-plane rows ([PR418] "fmt 5", the 24-byte-per-64-group
  *     layout whose lanes stride 16-value low-plane words and whose
@@ -238,6 +241,9 @@ void orc_qmv_int8_row(const int8_t *w, const float *r, int N, int K, const float
 
 /* ------------------------------------------------- a4: top-k routing (R4) */
 
+/* The value routing compares: the logit, except that NaN counts as -inf. */
+static inline double orc_route_val(float v) { return v != v ? -INFINITY : (double)v; }
+
 /* ids[t][j], j = 0..k-1, in descending logit order; w[t][j] the selected
  * softmax probabilities renormalised over the k selected experts.
  * Returns 0, or -1 on bad sizes. */
@@ -248,11 +254,15 @@ int orc_route_topk(const float *logits, int T, int E, int k, int32_t *ids, doubl
     if (!taken || !p) { free(taken); free(p); return -1; }
     for (int t = 0; t < T; ++t) {
         const float *l = logits + (int64_t)t * E;
-        /* softmax over all experts, in double */
-        double m = (double)l[0];
-        for (int e = 1; e < E; ++e) if ((double)l[e] > m) m = (double)l[e];
+        /* softmax over all experts, in double; with every logit at -inf they
+         * are all equal, and so are their probabilities */
+        double m = orc_route_val(l[0]);
+        for (int e = 1; e < E; ++e) if (orc_route_val(l[e]) > m) m = orc_route_val(l[e]);
         double z = 0.0;
-        for (int e = 0; e < E; ++e) { p[e] = exp((double)l[e] - m); z += p[e]; }
+        for (int e = 0; e < E; ++e) {
+            p[e] = (m == -INFINITY) ? 1.0 : exp(orc_route_val(l[e]) - m);
+            z += p[e];
+        }
         for (int e = 0; e < E; ++e) p[e] /= z;
         /* selection on the fp32 logits; a strict '>' keeps the lower index on ties */
         memset(taken, 0, (size_t)E);
@@ -261,7 +271,7 @@ int orc_route_topk(const float *logits, int T, int E, int k, int32_t *ids, doubl
             int best = -1;
             for (int e = 0; e < E; ++e) {
                 if (taken[e]) continue;
-                if (best < 0 || l[e] > l[best]) best = e;
+                if (best < 0 || orc_route_val(l[e]) > orc_route_val(l[best])) best = e;
             }
             taken[best] = 1;
             ids[(int64_t)t * k + j] = best;

@@ -236,6 +236,18 @@ def pin_golden_route(lib):
     assert np.allclose(w[0], d["expected_w"], rtol=1e-15, atol=0)
 
 
+def pin_golden_route_nan(lib):
+    """NaN logits count as -inf (never ahead of a finite logit, weight 0); a
+    token whose logits are all -inf or NaN takes the k lowest indices at 1/k;
+    -0 ties with +0. Hand-derived fixture."""
+    d = json.load(open(os.path.join(GOLDEN, "route_nan_as_minus_inf.json")))
+    logits = np.array([[float(v) for v in row] for row in d["logits"]], np.float32)
+    ids, w = oracle.route_topk(logits, d["k"], lib=lib)
+    assert ids.tolist() == d["expected_ids"], ids
+    assert np.all(np.isfinite(w))
+    assert np.allclose(w, d["expected_w"], rtol=1e-15, atol=0), w
+
+
 # ----------------------------------------------------------------- a5 grouping
 
 def pin_group_bruteforce(lib):
@@ -291,6 +303,8 @@ def pin_ffn_textbook_swiglu(lib):
                 den += abs(float(w[t, j])) * d
                 assert np.allclose(res["h"][t * k + j], h, rtol=1e-12, atol=1e-300)
             assert np.all(np.abs(res["out"][t] - ref) <= 1e-12 * den)
+            # the tolerance denominator sum_j |w_j| sum_c |D_ij h_c|, from numpy
+            assert np.allclose(res["den"][t], den, rtol=1e-12, atol=0)
 
 
 def pin_ffn_zero_gate(lib):
@@ -403,6 +417,21 @@ def pin_int3_exact_bruteforce(lib):
                 assert abs(Fraction(float(y[t, i])) - exact) <= mag * Fraction(1, 2 ** 45)
 
 
+def pin_int3_den(lib):
+    """den = |W3| @ |x| over a numpy bit-sliced matrix times its group scales."""
+    rng = _rng(23)
+    for (N, K, S) in [(7, 128, 2), (12, 512, 3)]:
+        vals = rng.integers(-4, 4, size=(N, K)).astype(np.int8)
+        wq3 = np.stack([oracle.pack_int3(vals[i], lib=lib) for i in range(N)])
+        s = (np.abs(rng.normal(0, 0.02, size=(N, K // 64))) + 1e-4).astype(np.float32)
+        x = rng.normal(size=(S, K)).astype(np.float32)
+        W3 = np_unpack3(wq3, K).astype(np.float64) * np.repeat(s.astype(np.float64), 64, axis=-1)
+        y, den = oracle.qmv_int3_gs(wq3, s, x, lib=lib)
+        ref_den = np.abs(x.astype(np.float64)) @ np.abs(W3).T
+        assert np.allclose(den, ref_den, rtol=1e-12, atol=0)
+        assert np.all(np.abs(y - x.astype(np.float64) @ W3.T) <= 1e-13 * ref_den)
+
+
 def pin_golden_int3_planes(lib):
     d = json.load(open(os.path.join(GOLDEN, "int3_g64_two_plane.json")))
     row = np.array([d["low_byte"]] * 16 + [d["high_byte"]] * 8, np.uint8)
@@ -417,7 +446,7 @@ ALL_PINS = [
     pin_pack_roundtrip, pin_golden_nibble_order, pin_int4_exact_bruteforce,
     pin_int4_library_identity, pin_int4_linearity, pin_int4_all_equal_closed_form,
     pin_gs_equals_k_is_row_scale, pin_int8_exact, pin_route_stable_sort, pin_route_exhaustive,
-    pin_golden_route, pin_group_bruteforce, pin_ffn_textbook_swiglu, pin_ffn_zero_gate,
+    pin_golden_route, pin_golden_route_nan, pin_group_bruteforce, pin_ffn_textbook_swiglu, pin_ffn_zero_gate,
     pin_golden_swiglu, pin_ffn_hidden_bound, pin_int3_pack_roundtrip, pin_int3_as_int4,
-    pin_int3_exact_bruteforce, pin_golden_int3_planes,
+    pin_int3_exact_bruteforce, pin_int3_den, pin_golden_int3_planes,
 ]

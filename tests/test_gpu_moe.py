@@ -56,10 +56,22 @@ def test_route_ties_and_nan():
     ids = ids.cpu().numpy()
     assert ids[0].tolist() == [1, 2, 5, 4]
     assert ids[1].tolist() == [1, 2, 3, 4]
-    rid, rw = oracle.route_topk(logits[:1], 4)
-    assert np.array_equal(ids[:1], rid)
-    assert np.allclose(w.cpu().numpy()[0], rw[0], rtol=TOL_W, atol=0)
-    assert np.allclose(w.cpu().numpy()[1], 0.25, rtol=TOL_W)
+    rid, rw = oracle.route_topk(logits, 4)  # the oracle reads NaN as -inf
+    assert np.array_equal(ids, rid)
+    assert np.allclose(w.cpu().numpy(), rw, rtol=TOL_W, atol=0)
+
+
+def test_route_nan_golden():
+    """The hand-derived NaN / all -inf / signed-zero fixture, on the GPU."""
+    import json
+    import os
+    d = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                    "route_nan_as_minus_inf.json")))
+    logits = np.array([[float(v) for v in row] for row in d["logits"]], np.float32)
+    ids, w = q.moe_route_topk(dev(logits), d["k"])
+    torch.cuda.synchronize()
+    assert ids.cpu().numpy().tolist() == d["expected_ids"]
+    assert np.allclose(w.cpu().numpy(), d["expected_w"], rtol=TOL_W, atol=0)
 
 
 def test_route_many_experts_and_k32():
@@ -94,15 +106,15 @@ def test_route_one_lane_holds_the_top(T, k, E):
 
 def test_route_signed_zero_inf_and_nan_ties():
     """+0 and -0 tie (the lower index first), -inf ties with -inf and NaN
-    counts as -inf: ids bit-exact against the oracle on the logits with NaN
-    replaced by -inf."""
+    counts as -inf: ids bit-exact against the oracle, which reads NaN the
+    same way."""
     rng = np.random.default_rng(29)
     vals = np.array([0.0, -0.0, -np.inf, np.nan, 1.0, -1.0], np.float32)
     for E, k in ((64, 16), (200, 32), (33, 32)):
         logits = rng.choice(vals, size=(6, E)).astype(np.float32)
         ids, _ = q.moe_route_topk(dev(logits), k)
         torch.cuda.synchronize()
-        rid, _ = oracle.route_topk(np.where(np.isnan(logits), -np.inf, logits).astype(np.float32), k)
+        rid, _ = oracle.route_topk(logits, k)
         assert np.array_equal(ids.cpu().numpy(), rid), (E, k)
 
 

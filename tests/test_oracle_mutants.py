@@ -17,7 +17,9 @@ MUTANTS = [
     ("first_group_scale_only", "acc += (double)s[i * G + g] * part;", "acc += (double)s[i * G] * part;"),
     ("scale_index_transposed", "return (double)(orc_nibble(row, k) - 8) * (double)s[i * (int64_t)(K / gs) + k / gs];",
      "return (double)(orc_nibble(row, k) - 8) * (double)s[(k / gs) * (int64_t)(K / gs) + i % (K / gs)];"),
-    ("tie_goes_to_higher_index", "if (best < 0 || l[e] > l[best]) best = e;", "if (best < 0 || l[e] >= l[best]) best = e;"),
+    ("tie_goes_to_higher_index", "if (best < 0 || orc_route_val(l[e]) > orc_route_val(l[best])) best = e;",
+     "if (best < 0 || orc_route_val(l[e]) >= orc_route_val(l[best])) best = e;"),
+    ("nan_not_minus_inf", "{ return v != v ? -INFINITY : (double)v; }", "{ return (double)v; }"),
     ("no_renormalisation", "w[(int64_t)t * k + j] = p[ids[(int64_t)t * k + j]] / psum;",
      "w[(int64_t)t * k + j] = p[ids[(int64_t)t * k + j]];"),
     ("silu_sign", "double sg = 1.0 / (1.0 + exp(-g));", "double sg = 1.0 / (1.0 + exp(g));"),
@@ -31,6 +33,8 @@ MUTANTS = [
      "const int hi = (g[16 + e / 8] >> (7 - e % 8)) & 1;"),
     ("int3_offset_3_not_4", "const double v = (double)(orc_code3(row, k) - 4);",
      "const double v = (double)(orc_code3(row, k) - 3);"),
+    ("moe_den_weight_dropped", "a += fabs((double)w[p]) * ad;", "a += ad;"),
+    ("int3_den_scale_dropped", "a += fabs(v * sc * (double)xt[k]);", "a += fabs(v * (double)xt[k]);"),
     ("hden_term_dropped", "hden[p * I + c] = fabs(dsilu * u) * dg + fabs(silu) * du;",
      "hden[p * I + c] = fabs(dsilu * u) * dg;"),
 ]
