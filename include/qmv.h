@@ -138,21 +138,28 @@ int qmv_int8_row(const int8_t *w, const float *row_scale, int N, int K, const fl
 /* The dense int4-gs64 GEMV of qmv_int4_gs for callers that cannot allocate
  * device memory: code that must never make the device synchronise (cudaMalloc
  * and cudaFree can), hosts that forbid device allocation after start-up, and
- * C callers with nowhere to keep a workspace between calls. Same arguments
- * and results as qmv_int4_gs, minus the workspace; the pages have no
- * counterpart of this entry point.
+ * C callers with nowhere to keep a workspace between calls. Same arguments as
+ * qmv_int4_gs, minus the workspace, and the same results up to the order of
+ * the fp32 additions: it always runs the per-warp cp.async kernel, never the
+ * tensor-map kernel that qmv_int4_gs takes when N % 16 == 0, so results are
+ * not bit-identical to qmv_int4_gs and its speed differs on such shapes. The
+ * pages have no counterpart of this entry point.
  *   Scratch: one file-scope device array inside the library (266,240 bytes,
  *   held by every GPU that loads the library until the process exits), so
  *   S * K must be at most 65536; larger calls return QMV_EWORKSPACE and
  *   enqueue nothing.
- *   The first call on a device looks up the array's device address (a host
- *   call, cudaGetSymbolAddress); make that first call before any stream
- *   capture.
+ *   Every call looks up the array's device address in the current context (a
+ *   host call, cudaGetSymbolAddress), so a device reset does not leave a stale
+ *   address behind. The first call on a device may load the library's module
+ *   there, which allocates the array and can synchronise: make one call per
+ *   device at start-up, before any stream capture and before any code that
+ *   must not synchronise.
  *   Every call uses the same array and overwrites all of it that it reads, so
  *   nothing carries over between calls, but calls whose work overlaps on the
  *   GPU (different streams, or different host threads on one device) race on
  *   it: order them on one stream.
- *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+ *   Allocates nothing itself: no cudaMalloc, cudaFree or allocating library
+ *   call. */
 int qmv_int4_gs_noalloc(const uint8_t *wq, const float *scales, int N, int K, int gs,
                         const float *x, float *y, int S, qmv_stream_t stream);
 

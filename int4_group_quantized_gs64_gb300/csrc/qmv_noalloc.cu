@@ -8,8 +8,6 @@
 // a caller workspace goes into one file-scope device array instead. The array
 // is part of the library image: every GPU that loads the library holds it
 // until the process exits.
-#include <mutex>
-
 #include "../../include/qmv.h"
 #include "qmv_internal.h"
 
@@ -22,21 +20,16 @@ constexpr size_t kNoAllocBytes = kNoAllocMaxValues * 4 + (kNoAllocMaxValues / 64
 // factor per 64 values: 266,240 bytes.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
-// Device address of the array for the current device, looked up once per
-// device. Host code must not pass the symbol itself to a kernel: on the host
-// it is only a stand-in for the device array.
+// Device address of the array in the current device's context. Host code
+// must not pass the symbol itself to a kernel: on the host it is only a
+// stand-in for the device array. The lookup runs on every call rather than
+// being cached, so a device reset or another context on the same device never
+// leaves a stale address behind; once the library's module is loaded on the
+// device it is a host-side lookup that allocates nothing.
 void *noalloc_scratch() {
-    static std::mutex mu;
-    static void *addr[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> g(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = p;
-    }
-    return addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    return p;
 }
 
 }  // namespace

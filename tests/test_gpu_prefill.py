@@ -12,6 +12,8 @@ q = pytest.importorskip("int4_group_quantized_gs64_gb300")
 
 pytestmark = pytest.mark.gpu
 
+PASS_PAIRS = 64  # the prefill kernels run an expert's pairs in passes of up to 64
+
 
 @pytest.fixture(scope="module", autouse=True)
 def _built():
@@ -61,12 +63,50 @@ def test_prefill_shapes(T, k, E, H, I):
     assert norm_err(out, ref["out"], ref["den"]) <= TOL_BF16
 
 
+def pass_cells(ids, E, pass_tok):
+    """Per token, the cells its pairs fall in: (expert, pass) for every pair,
+    plus (expert, pass, "last") for the pair in a pass's last column. An
+    expert's pairs run in ascending pair id, as the grouping lists them, in
+    passes of pass_tok."""
+    T, k = ids.shape
+    flat = ids.reshape(-1)
+    cells = [set() for _ in range(T)]
+    for e in range(E):
+        pairs = np.nonzero(flat == e)[0]
+        for j, p in enumerate(pairs):
+            ps = j // pass_tok
+            cells[p // k].add((e, ps))
+            if j == min(len(pairs), (ps + 1) * pass_tok) - 1:
+                cells[p // k].add((e, ps, "last"))
+    return cells
+
+
+def covering_sample(ids, E, pass_tok):
+    """Greedy token sample whose pairs touch every used expert, every pass of
+    each expert and the last column of every pass, so that every weight tile
+    the kernel streams, every pass it runs and the widest MMA column of each
+    pass meet a checked output. Returns the sorted tokens and all cells."""
+    cells = pass_cells(ids, E, pass_tok)
+    todo = set().union(*cells)
+    every = set(todo)
+    chosen = []
+    while todo:
+        t = max(range(len(cells)), key=lambda t: (len(cells[t] & todo), -t))
+        chosen.append(t)
+        todo -= cells[t]
+    return np.array(sorted(chosen)), every
+
+
 def test_prefill_workload_512_tokens_sampled():
     """512 tokens, H 6144, E 160, I 2048, top-8: every output computed on the
-    GPU, a seeded sample of tokens checked against the oracle."""
+    GPU; a greedy sample of tokens that touches every expert and every pass
+    of 64 pairs and the last column of every pass (hence every weight row
+    tile of both projections) is checked against the oracle, element by
+    element."""
     wl = datagen.WORKLOADS[4]
     E, H, I, k, T = wl["E"], wl["H"], wl["I"], wl["k"], wl["T"]
-    m = q.MoeInt4Weights.from_numpy(datagen.moe_weights(E, H, I))
+    wts = datagen.moe_weights(E, H, I)
+    m = q.MoeInt4Weights.from_numpy(wts)
     xbits, logits = datagen.moe_inputs(T, E, H, xdtype="bf16")
     ids_d, w_d = q.moe_route_topk(torch.from_numpy(logits).cuda(), k)
     ids, w = oracle.route_topk(logits, k)
@@ -74,8 +114,14 @@ def test_prefill_workload_512_tokens_sampled():
     w = w.astype(np.float32)
     out, status = run_prefill(m, xbits, ids, w)
     assert status == 0
-    sample = np.sort(np.random.default_rng(4).choice(T, size=6, replace=False))
-    x64 = datagen.bf16_bits_to_f32(xbits[sample]).astype(np.float64)
-    ref = moe_oracle(E, H, I, x64, ids[sample], w[sample])
-    assert norm_err(out[sample], ref["out"], ref["den"]) <= TOL_BF16
     assert np.all(np.isfinite(out))
+    sample, cells = covering_sample(ids, E, PASS_PAIRS)
+    per_tok = pass_cells(ids, E, PASS_PAIRS)
+    assert set().union(*(per_tok[t] for t in sample)) == cells, "sample misses a cell"
+    assert set(np.unique(ids[sample]).tolist()) == set(np.unique(ids).tolist())
+    x64 = datagen.bf16_bits_to_f32(xbits[sample]).astype(np.float64)
+    ref = moe_oracle(E, H, I, x64, ids[sample], w[sample], weights=wts)
+    err = norm_err(out[sample], ref["out"], ref["den"])
+    print(f"prefill 512 tokens: {len(sample)} tokens checked, {len(cells)} cells, "
+          f"normalised error {err:.3e} (bound {TOL_BF16:.0e})")
+    assert err <= TOL_BF16, err

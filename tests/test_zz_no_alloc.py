@@ -61,6 +61,27 @@ def test_matches_workspace_entry_point_on_two_calls(L):
         assert norm_err(yn, exact, den) <= TOL_FP32
 
 
+def test_exact_scratch_limit_multi_pass(L):
+    """S * K == 65536 exactly (the factor block ends at the array's last byte)
+    with S > 4, so the kernel walks the tokens in several passes."""
+    N, K, S = 1000, 4096, 16
+    wq, sc, x = datagen.dense_int4(N, K, S, seed=5)
+    dwq, dsc, dx = (torch.from_numpy(a).cuda() for a in (wq, sc, x))
+    ys = []
+    for _ in range(2):
+        y = torch.full((S, N), float("nan"), device="cuda")
+        assert _call_noalloc(L, dwq, dsc, dx, y) == 0
+        ys.append(y)
+    ref = q.qmv_int4_gs(dwq, dsc, dx)
+    torch.cuda.synchronize()
+    exact, den = oracle.qmv_int4_gs(wq, sc, x, 64, with_den=True)
+    for y in ys:
+        yn = y.cpu().numpy()
+        assert norm_err(yn, ref.cpu().numpy(), den) <= TOL_FP32
+        assert norm_err(yn, exact, den) <= TOL_FP32
+    assert torch.equal(ys[0], ys[1])
+
+
 def test_rejects_sizes_beyond_the_static_scratch(L):
     N, K, S = 64, 4096, 17  # S * K = 69632 > 65536
     dwq = torch.zeros((N, K // 2), dtype=torch.uint8, device="cuda")
