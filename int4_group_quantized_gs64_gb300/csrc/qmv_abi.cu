@@ -183,7 +183,8 @@ int moe_gate_up_silu(const qmv_moe_int4 *m, const float *x, int T, int k, const 
     float *part = reinterpret_cast<float *>(b + L.sk_part);
     cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * qmv::kSkMaxCtas, st);
     if (e == cudaSuccess) e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
-    if (e == cudaSuccess) e = qmv::launch_split(x, T, m->H, b + L.xcells, xfac, st);
+    if (e == cudaSuccess)
+        e = qmv::launch_split(x, T, m->H, b + L.xcells, xfac, st, qmv::tma_moe_supported(dims(m)));
     if (e == cudaSuccess) {
         float *hfac = reinterpret_cast<float *>(b + L.hfac);
         if (qmv::tma_moe_supported(dims(m)))
@@ -217,7 +218,9 @@ int moe_down(const qmv_moe_int4 *m, const float *h, int T, int k, const int32_t 
     float *part = reinterpret_cast<float *>(b + L.sk_part);
     cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * qmv::kSkMaxCtas, st);
     if (e == cudaSuccess) e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
-    if (e == cudaSuccess) e = qmv::launch_split(h, T * k, m->I, b + L.hcells, hfac, st);
+    if (e == cudaSuccess)
+        e = qmv::launch_split(h, T * k, m->I, b + L.hcells, hfac, st,
+                              qmv::tma_moe_supported(dims(m)));
     if (e == cudaSuccess) {
         if (qmv::tma_moe_supported(dims(m)))
             e = qmv::launch_moe_tma(dims(m), 1, b + L.hcells, hfac, k, offsets, list, uexp, n_used,
@@ -260,7 +263,8 @@ int prepare_impl(const qmv_moe_int4 *m, const float *x, int T, const int32_t *id
         at<int32_t>(ws, L.uexp), at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs),
         at<int32_t>(ws, L.status), x, m->H, at<void>(ws, pk ? L.xpk : L.xcells),
         (pk ? nullptr : at<float>(ws, L.xfac)), cs(stream), 8, pk, at<int32_t>(ws, L.status),
-        (int)(L.status_bytes / 4), true, res, served, logits, ids_out, w_out));
+        (int)(L.status_bytes / 4), true, res, served, logits, ids_out, w_out,
+        qmv::tma_moe_supported(dims(m))));
 }
 
 // Whole FFN (moe_expert_ffn_int4 with res == served == null).

@@ -108,6 +108,24 @@ __device__ __forceinline__ void dequant_int4_word(uint32_t w, uint32_t p[4]) {
     p[3] = hfma2_u32(lop3_and_or(w8, 0x00F000F0u, kBias), kSixteenth, kMinus72);
 }
 
+// The tensor-map decode kernel's int4 form: no fp16 arithmetic at all. A
+// nibble masked into the low bits of an fp16 word is the subnormal n * 2^-24,
+// and a nibble four bits up is (16 n) * 2^-24, both exact:
+//   p[0] = (e0, e4) * 2^-24, p[1] = (e1, e5) * 16 * 2^-24,
+//   p[2] = (e2, e6) * 2^-24, p[3] = (e3, e7) * 16 * 2^-24.
+// The activations that meet p[1] and p[3] are stored divided by 16 (exact,
+// see make_unit_s), so the MMA sums 2^-24 * n * v, and the offset -8 enters
+// as the accumulator's initial value -8 * 2^-24 * sum(v) of each token
+// (tile_group_int4s). Five integer instructions for eight weights instead of
+// nine with fp16 adds.
+__device__ __forceinline__ void dequant_int4_word_s(uint32_t w, uint32_t p[4]) {
+    const uint32_t w8 = w >> 8;
+    p[0] = w & 0x000F000Fu;
+    p[1] = w & 0x00F000F0u;
+    p[2] = w8 & 0x000F000Fu;
+    p[3] = w8 & 0x00F000F0u;
+}
+
 // One 32-bit word of int8 weights (bytes b0..b3, signed). Returns exact half2
 //   pa = (b0, b2), pb = (b1, b3).
 // Flipping the sign bit maps b to b + 128 in 0..255; placing that byte under
@@ -171,6 +189,34 @@ __device__ __forceinline__ uint4 make_unit(const float *v, int u) {
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+// Unit u of a group in the tensor-map kernel's int4 form: as make_unit<false>
+// with the values at k2, k3 (the ones multiplied by the high nibbles' 16 n)
+// divided by 16 before the hi/lo split.
+__device__ __forceinline__ uint4 make_unit_s(const float *v, int u) {
+    const int part = u & 1, q = (u >> 1) & 3, mh = u >> 3;
+    uint32_t r[4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        int k0, k1, k2, k3;
+        frag_ks<false>(2 * mh + i, q, k0, k1, k2, k3);
+        r[2 * i] = pack_half2(split_part(v[k0], part), split_part(v[k1], part));
+        r[2 * i + 1] = pack_half2(split_part(v[k2] * 0.0625f, part),
+                                  split_part(v[k3] * 0.0625f, part));
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// Initial accumulator of a group in that form: -8 * 2^-24 * sum of the
+// group's 64 scaled values (the offset of nibble - 8, folded out of the
+// weights). `sum` is the fp32 sum of the scaled values.
+__device__ __forceinline__ float offset_init(float sum) { return sum * -0x1p-21f; }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
 // Power-of-two exponent that maps max|v| into [2^13, 2^14); 0 for an all-zero group.
 __device__ __forceinline__ int split_exponent(float amax) {
     if (!(amax > 0.0f) || !isfinite(amax)) return 0;
@@ -207,6 +253,38 @@ __device__ __forceinline__ void tile_group_int4(uint2 w0, uint2 w8, const uint4 
         for (int nb = 0; nb < NB; ++nb) b[nb] = bu[nb][mh];
         dequant_int4_word(mh ? w0.y : w0.x, p0);
         dequant_int4_word(mh ? w8.y : w8.x, p8);
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm) {
+            a[0] = p0[2 * mm];
+            a[1] = p8[2 * mm];
+            a[2] = p0[2 * mm + 1];
+            a[3] = p8[2 * mm + 1];
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+                mma_16816(d[nb], a, mm ? b[nb].z : b[nb].x, mm ? b[nb].w : b[nb].y);
+        }
+    }
+}
+
+// The same tile in the tensor-map kernel's int4 form (dequant_int4_word_s):
+// the token columns (hi) start from cinit[nb] (offset_init of the lane's
+// token 4nb+q), so d[nb] ends as 2^-24 * sum (nibble - 8) * v.
+template <int NB>
+__device__ __forceinline__ void tile_group_int4s(uint2 w0, uint2 w8, const uint4 (&bu)[NB][2],
+                                                 const float (&cinit)[NB], float d[NB][4]) {
+    uint32_t p0[4], p8[4], a[4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        d[nb][0] = d[nb][2] = cinit[nb];
+        d[nb][1] = d[nb][3] = 0.0f;
+    }
+#pragma unroll
+    for (int mh = 0; mh < 2; ++mh) {
+        uint4 b[NB];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) b[nb] = bu[nb][mh];
+        dequant_int4_word_s(mh ? w0.y : w0.x, p0);
+        dequant_int4_word_s(mh ? w8.y : w8.x, p8);
 #pragma unroll
         for (int mm = 0; mm < 2; ++mm) {
             a[0] = p0[2 * mm];

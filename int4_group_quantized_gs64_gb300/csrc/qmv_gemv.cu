@@ -28,12 +28,14 @@ constexpr int kDenseBudget = 32 * 1024;
 // ------------------------------------------------------------------ split
 
 // Grid (rows, ceil(G / 8)): warp w of CTA (r, c) converts group 8c + w of
-// activation row r (one group per warp, so the rows' groups convert in
+// activation row r (one group a warp, so the rows' groups convert in
 // parallel): max |v| of the group -> exponent -> 16 fragment cells and the
-// factor. CTA (0, 0) also clears zero[0 .. nzero) (the caller's status word
-// and split counters), which the next kernel reads only after waiting for
-// this one.
-template <bool kInt8>
+// factor. kSub: the tensor-map kernel's int4 form (make_unit_s), with a
+// record (factor, offset_init) per group, fac [rows][G][2]; else fac
+// [rows][G]. CTA (0, 0) also clears zero[0 .. nzero) (the caller's status
+// word and split counters), which the next kernel reads only after waiting
+// for this one.
+template <bool kInt8, bool kSub = false>
 __global__ void __launch_bounds__(256)
     k_split(const float *__restrict__ v, int K, uint4 *__restrict__ cells,
             float *__restrict__ fac, int32_t *zero, int nzero) {
@@ -52,8 +54,17 @@ __global__ void __launch_bounds__(256)
         buf[warp][lane] = a * mul;
         buf[warp][32 + lane] = b * mul;
         __syncwarp();
-        if (lane < 16) cells[((size_t)r * G + g) * 16 + lane] = make_unit<kInt8>(buf[warp], lane);
-        if (lane == 0) fac[(size_t)r * G + g] = ldexpf(1.0f, -e);
+        if constexpr (kSub) {
+            const float sum = warp_sum(a * mul + b * mul);
+            if (lane < 16) cells[((size_t)r * G + g) * 16 + lane] = make_unit_s(buf[warp], lane);
+            if (lane == 0)
+                reinterpret_cast<float2 *>(fac)[(size_t)r * G + g] =
+                    make_float2(ldexpf(1.0f, -e), offset_init(sum));
+        } else {
+            if (lane < 16)
+                cells[((size_t)r * G + g) * 16 + lane] = make_unit<kInt8>(buf[warp], lane);
+            if (lane == 0) fac[(size_t)r * G + g] = ldexpf(1.0f, -e);
+        }
         __syncwarp();
     }
 }
@@ -259,13 +270,18 @@ cudaError_t launch_dense(const uint8_t *w, const float *scales, int N, int K, co
 
 }  // namespace
 
-cudaError_t launch_split(const float *v, int R, int K, void *cells, float *fac, cudaStream_t st) {
+cudaError_t launch_split(const float *v, int R, int K, void *cells, float *fac, cudaStream_t st,
+                         bool sub) {
     if (R == 0) return cudaSuccess;
+    if (sub)
+        return launch(k_split<false, true>, dim3(R, (K / kGroup + 7) / 8), dim3(256), 0, st, false,
+                      v, K, static_cast<uint4 *>(cells), fac, (int32_t *)nullptr, 0);
     return launch(k_split<false>, dim3(R, (K / kGroup + 7) / 8), dim3(256), 0, st, false, v, K,
                   static_cast<uint4 *>(cells), fac, (int32_t *)nullptr, 0);
 }
 
-size_t dense_scratch_bytes(int K, int S) { return (size_t)S * K * 4 + (size_t)S * (K / kGroup) * 4; }
+// activation units (4 bytes a value) and a factor record of up to 8 bytes a group
+size_t dense_scratch_bytes(int K, int S) { return (size_t)S * K * 4 + (size_t)S * (K / kGroup) * 8; }
 
 cudaError_t launch_dense_int4(const uint8_t *wq, const float *scales, int N, int K,
                               const float *x, float *y, int S, void *scratch, cudaStream_t st) {
@@ -308,8 +324,8 @@ cudaError_t launch_gemv_int4(const uint8_t *wq, const float *scales, int N, int 
         return launch_dense<false>(wq, scales, N, K, x, y, S, cells, fac, st, head,
                                    1 + kSkMaxCtas);
     float *part = reinterpret_cast<float *>(b + gemv_part_offset(K, S));
-    cudaError_t e = launch(k_split<false>, dim3(S, (K / kGroup + 7) / 8), dim3(256), 0, st, false,
-                           x, K, static_cast<uint4 *>(cells), fac, head, 1 + kSkMaxCtas);
+    cudaError_t e = launch(k_split<false, true>, dim3(S, (K / kGroup + 7) / 8), dim3(256), 0, st,
+                           false, x, K, static_cast<uint4 *>(cells), fac, head, 1 + kSkMaxCtas);
     if (e != cudaSuccess) return e;
     return launch_dense_tma(wq, scales, N, K, S, cells, fac, y, head, head + 1, part, st);
 }
@@ -326,8 +342,8 @@ cudaError_t launch_gemv_int4_pair(const uint8_t *wq0, const float *s0, int N0, c
     void *cells = b + kGemvHead;
     float *fac = reinterpret_cast<float *>(b + kGemvHead + (size_t)S * K * 4);
     float *part = reinterpret_cast<float *>(b + gemv_part_offset(K, S));
-    cudaError_t e = launch(k_split<false>, dim3(S, (K / kGroup + 7) / 8), dim3(256), 0, st, false,
-                           x, K, static_cast<uint4 *>(cells), fac, head, 1 + kSkMaxCtas);
+    cudaError_t e = launch(k_split<false, true>, dim3(S, (K / kGroup + 7) / 8), dim3(256), 0, st,
+                           false, x, K, static_cast<uint4 *>(cells), fac, head, 1 + kSkMaxCtas);
     if (e != cudaSuccess) return e;
     return launch_dense_tma(wq0, s0, N0, K, S, cells, fac, y0, head, head + 1, part, st, wq1, s1,
                             N1, y1);

@@ -52,7 +52,8 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int
 // logits: routing too, ids / w then written to ids_out / w_out). With
 // packed == true the units go to the pass-packed layout (see MoeWorkspace)
 // instead of per-row cells; zero[0 .. nzero) is cleared first; pdl: launched
-// with programmatic dependent launch.
+// with programmatic dependent launch. Per-row cells are in the tensor-map
+// kernel's int4 form when sub == true (see launch_split); packed units always are.
 cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
                                int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
@@ -60,14 +61,17 @@ cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t 
                                int32_t *zero = nullptr, int nzero = 0, bool pdl = false,
                                const uint32_t *res = nullptr, uint8_t *served = nullptr,
                                const float *logits = nullptr, int32_t *ids_out = nullptr,
-                               float *w_out = nullptr);
+                               float *w_out = nullptr, bool sub = false);
 // Shared memory of the grouping kernel when it also routes (logits != null):
 // every CTA routes the T tokens itself, so T * k pairs and E logits a warp.
 size_t route_smem_bytes(int T, int E, int k);
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
                           int32_t *pass_ofs, cudaStream_t st, bool pdl);
-// Activation rows [R][K] fp32 -> fragment cells [R][K/64][16] uint4 + factors [R][K/64].
-cudaError_t launch_split(const float *v, int R, int K, void *cells, float *fac, cudaStream_t st);
+// Activation rows [R][K] fp32 -> fragment cells [R][K/64][16] uint4 + factors [R][K/64],
+// or, with sub == true, the tensor-map kernel's int4 form: cells with the
+// high-nibble values divided by 16 and records (factor, offset_init) [R][K/64][2].
+cudaError_t launch_split(const float *v, int R, int K, void *cells, float *fac, cudaStream_t st,
+                         bool sub = false);
 cudaError_t launch_gate_up(const MoeDims &m, const void *xcells, const float *xfac, int k,
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                            const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,

@@ -11,11 +11,13 @@ namespace qmv {
 constexpr int kSkMaxCtas = 256;
 constexpr int kSkPartFloats = 2 * 256 * 8;
 
-// Pass-packed activation units (tensor-map decode path): block (pi, s) of
-// kPackedStage bytes holds, for pass pi and stage s (4 groups), the factors
-// of the pass's token slots 0..7 ([slot][4] floats, 128 B) followed by their
-// units ([slot][4 groups x 16] uint4, 1 KB a slot), so a stage's activations
-// are one contiguous copy of 128 B + 1 KB per token.
-constexpr int kPackedStage = 128 + 8 * 1024;
+// Pass-packed activation units (tensor-map decode path, in that kernel's
+// int4 form): block (pi, s) of kPackedStage bytes holds, for pass pi and
+// stage s (4 groups), the records (power-of-two factor, offset_init) of the
+// pass's token slots 0..7 ([slot][4] float2, 256 B) followed by their units
+// ([slot][4 groups x 16] uint4, 1 KB a slot), so a stage's activations are
+// one contiguous copy of 256 B + 1 KB per token.
+constexpr int kPackedHead = 8 * 4 * 8;
+constexpr int kPackedStage = kPackedHead + 8 * 1024;
 
 }  // namespace qmv

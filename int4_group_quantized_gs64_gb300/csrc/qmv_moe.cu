@@ -153,9 +153,10 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
 
 // Splits groups g0 .. g0 + 31 of activation row r (1024 threads, one group
 // a warp): per 64-wide group, max |v| -> power-of-two factor -> 16 fp16 hi/lo
-// cells (int4 register order).
+// cells (int4 register order). sub: the tensor-map kernel's int4 form, with a
+// (factor, offset_init) record per group (fac [G][2]); else fac [G].
 __device__ void split_row_cta(const float *__restrict__ row, int K, int g0, uint4 *cells,
-                              float *fac) {
+                              float *fac, bool sub) {
     __shared__ float buf[32][64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = K / kGroup;
     for (int g = g0 + warp; g < min(G, g0 + 32); g += blockDim.x >> 5) {
@@ -165,8 +166,15 @@ __device__ void split_row_cta(const float *__restrict__ row, int K, int g0, uint
         buf[warp][lane] = a * mul;
         buf[warp][32 + lane] = b * mul;
         __syncwarp();
-        if (lane < 16) cells[(size_t)g * 16 + lane] = make_unit<false>(buf[warp], lane);
-        if (lane == 0) fac[g] = ldexpf(1.0f, -e);
+        if (sub) {
+            const float sum = warp_sum(a * mul + b * mul);
+            if (lane < 16) cells[(size_t)g * 16 + lane] = make_unit_s(buf[warp], lane);
+            if (lane == 0)
+                reinterpret_cast<float2 *>(fac)[g] = make_float2(ldexpf(1.0f, -e), offset_init(sum));
+        } else {
+            if (lane < 16) cells[(size_t)g * 16 + lane] = make_unit<false>(buf[warp], lane);
+            if (lane == 0) fac[g] = ldexpf(1.0f, -e);
+        }
         __syncwarp();
     }
 }
@@ -210,10 +218,11 @@ __device__ void pair_slots_cta(const int32_t *__restrict__ ids, int P, int E, in
     __syncthreads();
 }
 
-// Splits token row t into units once and writes them to each of its pairs'
-// (pass, slot) in the pass-packed layout: in block (pi * ns + g / 4) of
-// kPackedStage bytes, the factor at float slot * 4 + g % 4 and the units at
-// byte 128 + slot * 1024 + (g % 4) * 256. With 32 warps each warp has one
+// Splits token row t into units once (the tensor-map kernel's int4 form) and
+// writes them to each of its pairs' (pass, slot) in the pass-packed layout:
+// in block (pi * ns + g / 4) of kPackedStage bytes, the record (factor,
+// offset_init) at float2 slot * 4 + g % 4 and the units at byte
+// kPackedHead + slot * 1024 + (g % 4) * 256. With 32 warps each warp has one
 // group, g0 + warp: xa / xb are its values lane and 32 + lane, loaded by the
 // caller (0 past the row's last group).
 __device__ void split_row_packed_cta(int K, int g0, int k, const int *pass, const int *slot,
@@ -227,21 +236,23 @@ __device__ void split_row_packed_cta(int K, int g0, int k, const int *pass, cons
         const float mul = ldexpf(1.0f, e);
         buf[warp][lane] = a * mul;
         buf[warp][32 + lane] = b * mul;
+        const float2 rec = make_float2(ldexpf(1.0f, -e), offset_init(warp_sum(a * mul + b * mul)));
         __syncwarp();
-        const uint4 u = make_unit<false>(buf[warp], lane & 15);
+        const uint4 u = make_unit_s(buf[warp], lane & 15);
         for (int j = lane >> 4; j < k; j += 2) {
             if (pass[j] < 0) continue;
             uint8_t *blk = pk + ((size_t)pass[j] * ns + g / 4) * kPackedStage;
-            reinterpret_cast<uint4 *>(blk + 128 + slot[j] * 1024 + (g % 4) * 256)[lane & 15] = u;
-            if ((lane & 15) == 0)
-                reinterpret_cast<float *>(blk)[slot[j] * 4 + g % 4] = ldexpf(1.0f, -e);
+            reinterpret_cast<uint4 *>(blk + kPackedHead + slot[j] * 1024 + (g % 4) * 256)[lane & 15] = u;
+            if ((lane & 15) == 0) reinterpret_cast<float2 *>(blk)[slot[j] * 4 + g % 4] = rec;
         }
     }
 }
 
 // CTA 0 groups the pairs; CTA 1 + t * C + c splits groups 32c .. 32c + 31
 // of token row t of x (C = ceil(H / 2048): one group a warp), per row or into
-// the pass-packed layout when packed != 0. CTA 0 first clears zero[0 ..
+// the pass-packed layout when bit 0 of `form` is set; bit 1 selects the
+// tensor-map kernel's int4 form for the per-row split (the packed layout is
+// always in that form). CTA 0 first clears zero[0 ..
 // nzero) (the call's status word and split counters), which later kernels
 // read only after waiting for this one. Launched with programmatic dependent
 // launch, every CTA waits for the previous kernel (routing writes ids).
@@ -249,11 +260,12 @@ __global__ void __launch_bounds__(1024)
     k_group_split(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets, int32_t *list,
                   int32_t *uexp, int32_t *n_used, int32_t *pass_ofs, int32_t *status,
                   const float *__restrict__ x, int H, uint4 *xcells, float *xfac, int pass_tok,
-                  int k, int packed, int32_t *zero, int nzero, const uint32_t *res,
+                  int k, int form, int32_t *zero, int nzero, const uint32_t *res,
                   uint8_t *served, const float *__restrict__ logits, int32_t *ids_out,
                   float *w_out) {
     pdl_wait();
     pdl_trigger();
+    const bool packed = form & 1;
     // a packed-split CTA (32 warps, one group each) requests its x values
     // first, so that their latency overlaps routing and the slot scan
     float xa = 0.f, xb = 0.f;
@@ -303,7 +315,7 @@ __global__ void __launch_bounds__(1024)
             split_row_packed_cta(H, g0, k, pass, slot, reinterpret_cast<uint8_t *>(xcells), xa, xb);
         } else {
             split_row_cta(x + (size_t)t * H, H, g0, xcells + (size_t)t * G * 16,
-                          xfac + (size_t)t * G);
+                          xfac + (size_t)t * G * ((form & 2) ? 2 : 1), (form & 2) != 0);
         }
     }
 }
@@ -651,7 +663,7 @@ cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t 
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
                                cudaStream_t st, int pass_tok, bool packed, int32_t *zero,
                                int nzero, bool pdl, const uint32_t *res, uint8_t *served,
-                               const float *logits, int32_t *ids_out, float *w_out) {
+                               const float *logits, int32_t *ids_out, float *w_out, bool sub) {
     const int C = (H / kGroup + 31) / 32;  // CTAs per token row
     const size_t smem = logits ? route_smem_bytes(T, E, k) : 0;
     if (smem) {
@@ -662,8 +674,9 @@ cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t 
     }
     return launch(k_group_split, dim3(x ? 1 + T * C : 1), dim3(1024), smem, st, pdl, ids, T * k,
                   E, offsets, list, uexp, n_used, pass_ofs, status, x, H,
-                  static_cast<uint4 *>(xcells), xfac, pass_tok, k, packed ? 1 : 0, zero, nzero, res,
-                  served, logits, ids_out, w_out);
+                  static_cast<uint4 *>(xcells), xfac, pass_tok, k,
+                  (packed ? 1 : 0) | ((packed || sub) ? 2 : 0), zero, nzero, res, served, logits,
+                  ids_out, w_out);
 }
 
 size_t route_smem_bytes(int T, int E, int k) {
@@ -720,10 +733,10 @@ MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k) {
     L.n_used = o; o = align256(o + 4);
     L.pass_ofs = o; o = align256(o + 4 * (size_t)(E + 1));
     L.xcells = o; o = align256(o + 4 * (size_t)T * H);
-    L.xfac = o; o = align256(o + 4 * (size_t)T * (H / 64));
+    L.xfac = o; o = align256(o + 8 * (size_t)T * (H / 64));  // up to 8 bytes a group
     L.h = o; o = align256(o + 4 * P * I);
     L.hcells = o; o = align256(o + 4 * P * I);
-    L.hfac = o; o = align256(o + 4 * P * (I / 64));
+    L.hfac = o; o = align256(o + 8 * P * (I / 64));
     L.y = o; o = align256(o + 4 * P * H);
     L.sk_part = o; o = align256(o + 4 * (size_t)kSkMaxCtas * kSkPartFloats);
     // a pass holds up to kMaxTok pairs of one expert: at most P / kMaxTok + min(E, P) passes

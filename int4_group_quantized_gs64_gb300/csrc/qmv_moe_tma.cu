@@ -49,8 +49,8 @@ constexpr int kTRows = 256;                          // weight rows per stage
 constexpr int kTStageW = kTRows * 128;               // 32 KB of packed weights
 constexpr int kTStageS = kTRows * 16;                // 4 KB of scales
 constexpr int kTActTok = 4 * 16 * 16;                // units of 4 groups, one token: 1 KB
-constexpr int kTFacTok = 16;                         // factors of 4 groups, one token
-// factors, then units: the order of a pass-packed block (one copy)
+constexpr int kTFacTok = 32;                         // (factor, offset_init) of 4 groups, one token
+// records, then units: the order of a pass-packed block (one copy)
 constexpr int kTOffF = kTStageW + kTStageS;
 constexpr int kTOffA = kTOffF + kMaxTok * kTFacTok;
 constexpr int kTStage = (kTOffA + kMaxTok * kTActTok + 1023) / 1024 * 1024;  // 45 KB
@@ -76,12 +76,14 @@ struct TmaArgs {
     int S;               // dense: tokens
     int packed;          // activation units pass-packed (else per row)
     const int32_t *offsets, *list, *uexp, *n_used, *pass_ofs;
-    const uint4 *cells;  // activation units: per row [row][G][16], or pass-packed
-                         // blocks of kPackedStage bytes [pass][G/4]
-    const float *cfac;   // their factors [row][G] (per-row layout only)
+    const uint4 *cells;  // activation units (int4 form of make_unit_s): per row
+                         // [row][G][16], or pass-packed blocks of kPackedStage
+                         // bytes [pass][G/4]
+    const float *cfac;   // their (factor, offset_init) records [row][G][2] (per-row
+                         // layout only)
     float *h;            // gate+up: h fp32 [P][I]
     uint4 *hcells;       // gate+up: units of h [P][I/64][16], or pass-packed blocks
-    float *hfac;         // gate+up: factors of h [P][I/64] (per-row layout only)
+    float *hfac;         // gate+up: records of h [P][I/64][2] (per-row layout only)
     float *y;            // down: y [P][H]
     int32_t *status;
     int32_t *cnt;        // per CTA: contributors done on the split item that starts in it
@@ -193,15 +195,25 @@ __device__ __forceinline__ void group_load(const uint8_t *wa, int pr, int q,
     }
 }
 
+// d = 2^-24 * sum (nibble - 8) * v over the group (tile_group_int4s); the
+// exact 2^24 comes back before the group scale and the activation factor.
+// fp[nb]: the (factor, offset_init) records of the four groups of token
+// block nb, read per group (fewer live registers than all four at once).
 template <int NB, int GL>
 __device__ __forceinline__ void group_math(const GroupFrag<NB> &g, float s0, float s8,
-                                           const float (&f)[NB][4], float c[2][NB][2]) {
-    float d[NB][4];
-    tile_group_int4<NB>(g.w0, g.w8, g.bu, d);
+                                           const float *const fp[NB], float c[2][NB][2]) {
+    float d[NB][4], ci[NB], f[NB];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-        c[GL & 1][nb][0] = fmaf(s0 * f[nb][GL], d[nb][0] + d[nb][1], c[GL & 1][nb][0]);
-        c[GL & 1][nb][1] = fmaf(s8 * f[nb][GL], d[nb][2] + d[nb][3], c[GL & 1][nb][1]);
+        const float2 r = reinterpret_cast<const float2 *>(fp[nb])[GL];
+        f[nb] = r.x;
+        ci[nb] = r.y;
+    }
+    tile_group_int4s<NB>(g.w0, g.w8, g.bu, ci, d);
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        c[GL & 1][nb][0] = fmaf(s0 * f[nb], (d[nb][0] + d[nb][1]) * 0x1p24f, c[GL & 1][nb][0]);
+        c[GL & 1][nb][1] = fmaf(s8 * f[nb], (d[nb][2] + d[nb][3]) * 0x1p24f, c[GL & 1][nb][1]);
     }
 }
 
@@ -211,26 +223,19 @@ __device__ __forceinline__ void compute_stage(const uint8_t *slot, int r0,
                                               const uint4 *const bp[NB],
                                               const float *const fp[NB], float c[2][NB][2]) {
     const int lane = threadIdx.x & 31, q = lane & 3, pr = tile_row(lane >> 2);
-    // the four groups' scales of rows pr and pr + 8, and the four factors of
-    // each token block, are 16-byte vectors
+    // the four groups' scales of rows pr and pr + 8 are a 16-byte vector
     const float4 s0 = reinterpret_cast<const float4 *>(slot + kTStageW)[r0 + pr];
     const float4 s8 = reinterpret_cast<const float4 *>(slot + kTStageW)[r0 + pr + 8];
-    float f[NB][4];
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-        const float4 v = *reinterpret_cast<const float4 *>(fp[nb]);
-        f[nb][0] = v.x; f[nb][1] = v.y; f[nb][2] = v.z; f[nb][3] = v.w;
-    }
     const uint8_t *wa = slot + (r0 + pr) * 128;
     GroupFrag<NB> g;
     group_load<NB, 0>(wa, pr, q, bp, g);
-    group_math<NB, 0>(g, s0.x, s8.x, f, c);
+    group_math<NB, 0>(g, s0.x, s8.x, fp, c);
     group_load<NB, 1>(wa, pr, q, bp, g);
-    group_math<NB, 1>(g, s0.y, s8.y, f, c);
+    group_math<NB, 1>(g, s0.y, s8.y, fp, c);
     group_load<NB, 2>(wa, pr, q, bp, g);
-    group_math<NB, 2>(g, s0.z, s8.z, f, c);
+    group_math<NB, 2>(g, s0.z, s8.z, fp, c);
     group_load<NB, 3>(wa, pr, q, bp, g);
-    group_math<NB, 3>(g, s0.w, s8.w, f, c);
+    group_math<NB, 3>(g, s0.w, s8.w, fp, c);
 }
 
 struct TShared {
@@ -352,19 +357,21 @@ __device__ __forceinline__ void t_epilogue(const TmaArgs &a, const TShared &sh, 
             const float mul = ldexpf(1.0f, e);
             wbuf[warp * 64 + lane] = v0 * mul;
             wbuf[warp * 64 + 32 + lane] = v1 * mul;
+            const float2 rec =
+                make_float2(ldexpf(1.0f, -e), offset_init(warp_sum(v0 * mul + v1 * mul)));
             __syncwarp();
             if (a.packed) {
                 // down's pass pi, slot s (down groups the pairs as gate+up does)
                 uint8_t *blk = reinterpret_cast<uint8_t *>(a.hcells) +
                                ((size_t)pi * (Gd / 4) + gd / 4) * kPackedStage;
                 if (lane < 16)
-                    reinterpret_cast<uint4 *>(blk + 128 + s * 1024 + (gd % 4) * 256)[lane] =
-                        make_unit<false>(wbuf + warp * 64, lane);
-                if (lane == 0) reinterpret_cast<float *>(blk)[s * 4 + gd % 4] = ldexpf(1.0f, -e);
+                    reinterpret_cast<uint4 *>(blk + kPackedHead + s * 1024 + (gd % 4) * 256)[lane] =
+                        make_unit_s(wbuf + warp * 64, lane);
+                if (lane == 0) reinterpret_cast<float2 *>(blk)[s * 4 + gd % 4] = rec;
             } else {
                 const size_t cb = (size_t)sh.pairs[s] * Gd + gd;
-                if (lane < 16) a.hcells[cb * 16 + lane] = make_unit<false>(wbuf + warp * 64, lane);
-                if (lane == 0) a.hfac[cb] = ldexpf(1.0f, -e);
+                if (lane < 16) a.hcells[cb * 16 + lane] = make_unit_s(wbuf + warp * 64, lane);
+                if (lane == 0) reinterpret_cast<float2 *>(a.hfac)[cb] = rec;
             }
             __syncwarp();
         }
@@ -566,7 +573,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
                 const uint32_t fb = tc05::smem_addr(&sh.full[slot]);
                 const size_t cg = (size_t)myrow * a.G + 4 * kb;
                 bulk_load(base + kTOffA + lane * kTActTok, a.cells + cg * 16, kTActTok, fb);
-                bulk_load(base + kTOffF + lane * kTFacTok, a.cfac + cg, kTFacTok, fb);
+                bulk_load(base + kTOffF + lane * kTFacTok, a.cfac + 2 * cg, kTFacTok, fb);
             }
             issued = j + 1;
             if (++kb == ns) {
