@@ -257,6 +257,16 @@ int prepare_impl(const qmv_moe_int4 *m, const float *x, int T, const int32_t *id
     if (!x || !ids) return QMV_EINVAL;
     if (!aligned(x, 4) || !aligned(ids, 4)) return QMV_EALIGN;
     const bool pk = packed_units(m, k);
+    // the packed path also gets the work plan of the gate+up and down kernels
+    qmv::PlanArgs plan{};
+    if (pk) {
+        plan.ptab = at<int4>(ws, L.ptab);
+        plan.plan_gu = at<int32_t>(ws, L.plan);
+        plan.plan_dn = at<int32_t>(ws, L.plan) + qmv::kSkMaxCtas + 1;
+        plan.s_gu = ((m->I + 127) / 128) * (m->H / 256);
+        plan.s_dn = ((m->H + 255) / 256) * (m->I / 256);
+        plan.g = qmv::tma_grid();
+    }
     // the grouping kernel clears the status word and the split counters itself
     return from_cuda(qmv::launch_group_split(
         ids, T, k, m->E, at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list),
@@ -264,7 +274,7 @@ int prepare_impl(const qmv_moe_int4 *m, const float *x, int T, const int32_t *id
         at<int32_t>(ws, L.status), x, m->H, at<void>(ws, pk ? L.xpk : L.xcells),
         (pk ? nullptr : at<float>(ws, L.xfac)), cs(stream), 8, pk, at<int32_t>(ws, L.status),
         (int)(L.status_bytes / 4), true, res, served, logits, ids_out, w_out,
-        qmv::tma_moe_supported(dims(m))));
+        qmv::tma_moe_supported(dims(m)), pk ? &plan : nullptr));
 }
 
 // Whole FFN (moe_expert_ffn_int4 with res == served == null).
@@ -294,7 +304,8 @@ int moe_ffn_gate_up(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_byt
             at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs), at<float>(ws, L.h),
             at<void>(ws, pk ? L.hpk : L.hcells), (pk ? nullptr : at<float>(ws, L.hfac)), nullptr,
             at<int32_t>(ws, L.status), at<int32_t>(ws, L.sk_cnt), at<float>(ws, L.sk_part),
-            cs(stream), pk));
+            cs(stream), pk, pk ? at<int4>(ws, L.ptab) : nullptr,
+            pk ? at<int32_t>(ws, L.plan) : nullptr));
     }
     return from_cuda(qmv::launch_gate_up(
         dims(m), at<void>(ws, L.xcells), at<float>(ws, L.xfac), k, at<int32_t>(ws, L.offsets),
@@ -315,7 +326,8 @@ int moe_ffn_down(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
             at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
             at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs), nullptr, nullptr, nullptr,
             at<float>(ws, L.y), at<int32_t>(ws, L.status), at<int32_t>(ws, L.sk_cnt) + qmv::kSkMaxCtas,
-            at<float>(ws, L.sk_part), cs(stream), pk));
+            at<float>(ws, L.sk_part), cs(stream), pk, pk ? at<int4>(ws, L.ptab) : nullptr,
+            pk ? at<int32_t>(ws, L.plan) + qmv::kSkMaxCtas + 1 : nullptr));
     }
     return from_cuda(qmv::launch_down(dims(m), at<void>(ws, L.hcells), at<float>(ws, L.hfac),
                                       at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list),

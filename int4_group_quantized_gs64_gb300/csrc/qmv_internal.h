@@ -48,6 +48,22 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids,
                          cudaStream_t st);
 cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int32_t *list,
                          int32_t *uexp, int32_t *n_used, int32_t *status, cudaStream_t st);
+// Work plan of the tensor-map FFN kernels, written by the grouping kernel
+// (ptab == null: none). A pass is up to kMaxTok pairs of one expert; the CTAs
+// of gate+up (and of down) split the passes' stages so that every CTA gets
+// the same cost, a stage with more than 4 tokens counting kPlanW2 / kPlanW1
+// of one with at most 4 (its MMAs cover two token blocks).
+constexpr int kPlanW1 = 3, kPlanW2 = 4;
+struct PlanArgs {
+    int4 *ptab;        // [passes]: (expert, first list index, tokens, 0)
+    int32_t *plan_gu;  // [g + 1]: first stage of each gate+up CTA, then the total
+    int32_t *plan_dn;  // [g + 1]: the same for down
+    int s_gu, s_dn;    // stages per pass: row tiles x stages per tile
+    int g;             // CTAs of the tensor-map kernel
+};
+// CTAs of a tensor-map decode launch.
+int tma_grid();
+
 // Grouping plus the split of the T activation rows, in one launch (with
 // logits: routing too, ids / w then written to ids_out / w_out). With
 // packed == true the units go to the pass-packed layout (see MoeWorkspace)
@@ -61,7 +77,8 @@ cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t 
                                int32_t *zero = nullptr, int nzero = 0, bool pdl = false,
                                const uint32_t *res = nullptr, uint8_t *served = nullptr,
                                const float *logits = nullptr, int32_t *ids_out = nullptr,
-                               float *w_out = nullptr, bool sub = false);
+                               float *w_out = nullptr, bool sub = false,
+                               const PlanArgs *plan = nullptr);
 // Shared memory of the grouping kernel when it also routes (logits != null):
 // every CTA routes the T tokens itself, so T * k pairs and E logits a warp.
 size_t route_smem_bytes(int T, int E, int k);
@@ -119,11 +136,15 @@ cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int 
                              int N2 = 0, float *y2 = nullptr);
 // packed: the activation units (cells, cfac) and, for gate+up, the units of
 // h it writes (hcells, hfac) are in the pass-packed layout; else per row.
+// ptab / plan (optional): the grouping kernel's pass table and this mode's
+// CTA stage boundaries (PlanArgs); without them the kernel splits the stages
+// evenly and walks the passes through pass_ofs.
 cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const float *cfac, int k,
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                            const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,
                            float *hfac, float *y, int32_t *status, int32_t *cnt, float *part,
-                           cudaStream_t st, bool packed = false);
+                           cudaStream_t st, bool packed = false, const int4 *ptab = nullptr,
+                           const int32_t *plan = nullptr);
 
 // Single-launch expert FFN of one token (cooperative grid, qmv_moe_one.cu).
 // bar: a zeroed word for the grid barrier.
@@ -141,7 +162,7 @@ cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids,
 // holds x for gate+up, hpk h for down.
 struct MoeWorkspace {
     size_t status, sk_cnt, status_bytes, offsets, list, uexp, n_used, pass_ofs, xcells, xfac, h,
-        hcells, hfac, y, sk_part, xpk, hpk, total;
+        hcells, hfac, y, sk_part, xpk, hpk, ptab, plan, total;
     int pmax;  // passes, at most
 };
 MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k);

@@ -96,10 +96,17 @@ __device__ __forceinline__ void block_scan3(int a, int b, int c, int &ea, int &e
 // res: bitmap of the experts this call serves (bit e % 32 of word e / 32), or
 // null for all; pairs of other experts are left out of the lists without
 // error. served (if not null): 1 for each pair that is grouped, else 0.
+//
+// With a work plan (pl && pl->ptab): the pass table and, for gate+up and for
+// down, the first stage of every CTA, so that each CTA's stages carry the
+// same cost (PlanArgs). Cost units: the stages of used expert u start at
+// S * wpre[u] (wpre: exclusive scan of the experts' pass weights); CTA b
+// starts at cost C * b / g of the total C, inside the pass that cost falls
+// in, at the first stage whose start is not below it.
 __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets,
                           int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                           int32_t *status, int pass_tok, const uint32_t *res = nullptr,
-                          uint8_t *served = nullptr) {
+                          uint8_t *served = nullptr, const PlanArgs *pl = nullptr) {
     __shared__ int32_t cnt[1024], run[1024], tot[96];
     __shared__ int bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -131,6 +138,58 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
         offsets[E] = ec + c;
         *n_used = ef + f;
         if (pass_ofs) pass_ofs[ef + f] = ep + np;
+    }
+    if (pl && pl->ptab) {
+        // pass table, and each used expert's pass weight (full passes weigh
+        // kPlanW2, the last one by its token count)
+        __shared__ int32_t nu_s;
+        __shared__ long long wtot_s;
+        int wexp = 0;
+        if (f) {
+            for (int i = 0; i < np; ++i)
+                pl->ptab[ep + i] = make_int4(tid, ec + i * pass_tok, min(pass_tok, c - i * pass_tok), 0);
+            const int last = c - (np - 1) * pass_tok;
+            wexp = (np - 1) * kPlanW2 + (last > 4 ? kPlanW2 : kPlanW1);
+        }
+        int ew, d1, d2;
+        __syncthreads();  // cnt[] (c) has been read: reuse it for wpre
+        block_scan3(wexp, 0, 0, ew, d1, d2, tot);
+        if (f) cnt[ef] = ew;
+        if (tid == E - 1) {
+            nu_s = ef + f;
+            wtot_s = (long long)ew + wexp;
+        }
+        __syncthreads();
+        const int nu = nu_s;
+        for (int b = tid; b <= pl->g; b += blockDim.x) {
+            for (int m = 0; m < 2; ++m) {
+                const long long S = m ? pl->s_dn : pl->s_gu;
+                int32_t ub;
+                if (nu == 0) {
+                    ub = 0;
+                } else if (b == pl->g) {
+                    ub = (int32_t)(S * pass_ofs[nu]);
+                } else {
+                    const long long cb = S * wtot_s * b / pl->g;
+                    int lo = 0, hi = nu - 1;  // last used expert whose stages start at or below cb
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (S * cnt[mid] <= cb) lo = mid; else hi = mid - 1;
+                    }
+                    const int e = uexp[lo];
+                    const int ce = offsets[e + 1] - offsets[e];
+                    const int npe = (ce + pass_tok - 1) / pass_tok;
+                    const int wl = ce - (npe - 1) * pass_tok > 4 ? kPlanW2 : kPlanW1;
+                    const long long r = cb - S * cnt[lo];
+                    const int i = (int)min((long long)(npe - 1), r / (kPlanW2 * S));
+                    const long long r2 = r - (long long)i * kPlanW2 * S;
+                    const int wi = i < npe - 1 ? kPlanW2 : wl;
+                    const long long st = min(S, (r2 + wi - 1) / wi);
+                    ub = (int32_t)(S * (pass_ofs[lo] + i) + st);
+                }
+                (m ? pl->plan_dn : pl->plan_gu)[b] = ub;
+            }
+        }
     }
     __syncthreads();
     if (warp == 0) {
@@ -262,7 +321,7 @@ __global__ void __launch_bounds__(1024)
                   const float *__restrict__ x, int H, uint4 *xcells, float *xfac, int pass_tok,
                   int k, int form, int32_t *zero, int nzero, const uint32_t *res,
                   uint8_t *served, const float *__restrict__ logits, int32_t *ids_out,
-                  float *w_out) {
+                  float *w_out, PlanArgs plan) {
     pdl_wait();
     pdl_trigger();
     const bool packed = form & 1;
@@ -305,7 +364,8 @@ __global__ void __launch_bounds__(1024)
             for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
             __syncthreads();
         }
-        group_cta(ids, P, E, offsets, list, uexp, n_used, pass_ofs, status, pass_tok, res, served);
+        group_cta(ids, P, E, offsets, list, uexp, n_used, pass_ofs, status, pass_tok, res, served,
+                  &plan);
     } else {
         const int G = H / kGroup, C = (G + 31) / 32;
         const int t = (blockIdx.x - 1) / C, g0 = 32 * ((blockIdx.x - 1) % C);
@@ -655,7 +715,7 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int
                   n_used, (int32_t *)nullptr, status, (const float *)nullptr, 64,
                   (uint4 *)nullptr, (float *)nullptr, (int)kMaxTok, 1, 0, (int32_t *)nullptr, 0,
                   (const uint32_t *)nullptr, (uint8_t *)nullptr, (const float *)nullptr,
-                  (int32_t *)nullptr, (float *)nullptr);
+                  (int32_t *)nullptr, (float *)nullptr, PlanArgs{});
 }
 
 cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t *offsets,
@@ -663,7 +723,8 @@ cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t 
                                int32_t *status, const float *x, int H, void *xcells, float *xfac,
                                cudaStream_t st, int pass_tok, bool packed, int32_t *zero,
                                int nzero, bool pdl, const uint32_t *res, uint8_t *served,
-                               const float *logits, int32_t *ids_out, float *w_out, bool sub) {
+                               const float *logits, int32_t *ids_out, float *w_out, bool sub,
+                               const PlanArgs *plan) {
     const int C = (H / kGroup + 31) / 32;  // CTAs per token row
     const size_t smem = logits ? route_smem_bytes(T, E, k) : 0;
     if (smem) {
@@ -676,7 +737,7 @@ cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t 
                   E, offsets, list, uexp, n_used, pass_ofs, status, x, H,
                   static_cast<uint4 *>(xcells), xfac, pass_tok, k,
                   (packed ? 1 : 0) | ((packed || sub) ? 2 : 0), zero, nzero, res, served, logits,
-                  ids_out, w_out);
+                  ids_out, w_out, plan ? *plan : PlanArgs{});
 }
 
 size_t route_smem_bytes(int T, int E, int k) {
@@ -745,6 +806,8 @@ MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k) {
     const size_t sh = (size_t)H / (4 * kGroup), si = (size_t)I / (4 * kGroup);  // stages
     L.xpk = o; o = align256(o + pm * sh * kPackedStage);
     L.hpk = o; o = align256(o + pm * si * kPackedStage);
+    L.ptab = o; o = align256(o + 16 * pm);
+    L.plan = o; o = align256(o + 4 * 2 * ((size_t)kSkMaxCtas + 1));
     L.total = o;
     return L;
 }

@@ -85,6 +85,8 @@ struct TmaArgs {
     uint4 *hcells;       // gate+up: units of h [P][I/64][16], or pass-packed blocks
     float *hfac;         // gate+up: records of h [P][I/64][2] (per-row layout only)
     float *y;            // down: y [P][H]
+    const int4 *ptab;    // the grouping kernel's pass table, or null (PlanArgs)
+    const int32_t *plan; // this mode's CTA stage boundaries [g + 1], or null
     int32_t *status;
     int32_t *cnt;        // per CTA: contributors done on the split item that starts in it
     float *part;         // per CTA: partial sums [2][kTRows][kMaxTok] (head / tail item)
@@ -136,7 +138,7 @@ struct PassCursor {
 
     __device__ __forceinline__ void seek(const TmaArgs &a, int nu, int p) {
         pi = -1;
-        if (a.mode == 2) {
+        if (a.mode == 2 || a.ptab) {
             to(a, p);
             return;
         }
@@ -157,6 +159,14 @@ struct PassCursor {
             e = 0;
             beg = p * kMaxTok;
             ntok = min(kMaxTok, a.S - beg);
+            return;
+        }
+        if (a.ptab) {  // one load instead of a walk over pass_ofs, uexp and offsets
+            const int4 t = a.ptab[p];
+            pi = p;
+            e = t.x;
+            beg = t.y;
+            ntok = t.z;
             return;
         }
         while (a.pass_ofs[lo + 1] <= p) ++lo;
@@ -473,17 +483,27 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
     if (a.mode == 0 || warp < kTConsumers) pdl_wait();
     pdl_trigger();
 
-    const int nu = a.mode == 2 ? 1 : *a.n_used;
     const int tiles = a.mode == 0 ? (a.I + kTGuJ - 1) / kTGuJ
                                   : a.tiles0 + (a.H2 + kTDnRows - 1) / kTDnRows;
-    const int passes = a.mode == 2 ? (a.S + kMaxTok - 1) / kMaxTok : (nu > 0 ? a.pass_ofs[nu] : 0);
-    const int total_items = passes * tiles;
     const int ns = a.G / 4;
-    // Stage-level split: CTA b takes stages [U*b/g, U*(b+1)/g) of the item-major sequence.
-    const long long U = (long long)total_items * ns;
     const int g = gridDim.x;
-    const long long u0 = (long long)blockIdx.x * U / g;
-    const long long u1 = (long long)(blockIdx.x + 1) * U / g;
+    // Stage-level split: CTA b takes stages [u0, u1) of the item-major sequence
+    // (items pass-major): the grouping kernel's cost-balanced plan, or else an
+    // even split [U*b/g, U*(b+1)/g).
+    int nu = 1;
+    long long U, u0, u1;
+    if (a.plan) {
+        U = a.plan[g];
+        u0 = a.plan[blockIdx.x];
+        u1 = a.plan[blockIdx.x + 1];
+    } else {
+        nu = a.mode == 2 ? 1 : *a.n_used;
+        const int passes =
+            a.mode == 2 ? (a.S + kMaxTok - 1) / kMaxTok : (nu > 0 ? a.pass_ofs[nu] : 0);
+        U = (long long)passes * tiles * ns;
+        u0 = (long long)blockIdx.x * U / g;
+        u1 = (long long)(blockIdx.x + 1) * U / g;
+    }
 
     if (warp == kTConsumers) {
         // ---------------- producer (whole warp; lane 0 owns the barriers)
@@ -590,7 +610,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
     } else {
         // ---------------- consumers
         for (int i = threadIdx.x; i <= g; i += 32 * kTConsumers)
-            sh.ub[i] = (long long)i * U / g;
+            sh.ub[i] = a.plan ? (long long)a.plan[i] : (long long)i * U / g;
         int j = 0, cur_pi = -1;
         bool failed = false;
         PassCursor pc;
@@ -693,11 +713,13 @@ cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const 
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                            const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,
                            float *hfac, float *y, int32_t *status, int32_t *cnt, float *part,
-                           cudaStream_t st, bool packed) {
+                           cudaStream_t st, bool packed, const int4 *ptab, const int32_t *plan) {
     TmaArgs a;
     memset(&a, 0, sizeof(a));
     a.mode = mode;
     a.packed = packed ? 1 : 0;
+    a.ptab = ptab;
+    a.plan = plan;
     a.I = m.I;
     a.H = m.H;
     a.k = k;
@@ -723,8 +745,12 @@ cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const 
     if (!ok) return cudaErrorInvalidValue;
     cudaError_t e = set_smem(k_moe_tma, kTSmem);
     if (e != cudaSuccess) return e;
-    const int grid = std::min(kSkMaxCtas, sm_count() * max_ctas_per_sm(k_moe_tma, kTThreads, kTSmem));
-    return launch(k_moe_tma, dim3(grid), dim3(kTThreads), (size_t)kTSmem, st, true, a);
+    return launch(k_moe_tma, dim3(tma_grid()), dim3(kTThreads), (size_t)kTSmem, st, true, a);
+}
+
+int tma_grid() {
+    set_smem(k_moe_tma, kTSmem);
+    return std::min(kSkMaxCtas, sm_count() * max_ctas_per_sm(k_moe_tma, kTThreads, kTSmem));
 }
 
 bool tma_dense_supported(const uint8_t *wq, const float *scales, int N, int K) {
