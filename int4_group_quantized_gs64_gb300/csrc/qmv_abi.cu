@@ -57,8 +57,14 @@ int ffn_check(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
 // The phases keep the activation units pass-packed (two copies per stage in
 // the tensor-map kernel) when that kernel runs and a token's pairs fit the
 // grouping kernel's per-token slots.
-bool packed_units(const qmv_moe_int4 *m, int k) {
-    return qmv::tma_moe_supported(dims(m)) && k <= 32;
+bool packed_units(const qmv_moe_int4 *m, int T, int k) {
+    return qmv::tma_moe_supported(dims(m), (long long)T * k) && k <= 32;
+}
+
+// The tensor-map kernels run this call (shape, alignment, and a stage count
+// that their 32-bit stage numbers hold).
+bool tma_path(const qmv_moe_int4 *m, int T, int k) {
+    return qmv::tma_moe_supported(dims(m), (long long)T * k);
 }
 
 bool one_token(const qmv_moe_int4 *m, int k) {
@@ -184,10 +190,10 @@ int moe_gate_up_silu(const qmv_moe_int4 *m, const float *x, int T, int k, const 
     cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * qmv::kSkMaxCtas, st);
     if (e == cudaSuccess) e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
     if (e == cudaSuccess)
-        e = qmv::launch_split(x, T, m->H, b + L.xcells, xfac, st, qmv::tma_moe_supported(dims(m)));
+        e = qmv::launch_split(x, T, m->H, b + L.xcells, xfac, st, tma_path(m, T, k));
     if (e == cudaSuccess) {
         float *hfac = reinterpret_cast<float *>(b + L.hfac);
-        if (qmv::tma_moe_supported(dims(m)))
+        if (tma_path(m, T, k))
             e = qmv::launch_moe_tma(dims(m), 0, b + L.xcells, xfac, k, offsets, list, uexp, n_used,
                                     pass_ofs, h, b + L.hcells, hfac, nullptr,
                                     reinterpret_cast<int32_t *>(b + L.status), cnt, part, st);
@@ -219,10 +225,9 @@ int moe_down(const qmv_moe_int4 *m, const float *h, int T, int k, const int32_t 
     cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * qmv::kSkMaxCtas, st);
     if (e == cudaSuccess) e = qmv::launch_passes(offsets, uexp, n_used, pass_ofs, st, false);
     if (e == cudaSuccess)
-        e = qmv::launch_split(h, T * k, m->I, b + L.hcells, hfac, st,
-                              qmv::tma_moe_supported(dims(m)));
+        e = qmv::launch_split(h, T * k, m->I, b + L.hcells, hfac, st, tma_path(m, T, k));
     if (e == cudaSuccess) {
-        if (qmv::tma_moe_supported(dims(m)))
+        if (tma_path(m, T, k))
             e = qmv::launch_moe_tma(dims(m), 1, b + L.hcells, hfac, k, offsets, list, uexp, n_used,
                                     pass_ofs, nullptr, nullptr, nullptr, y,
                                     reinterpret_cast<int32_t *>(b + L.status), cnt, part, st);
@@ -256,7 +261,7 @@ int prepare_impl(const qmv_moe_int4 *m, const float *x, int T, const int32_t *id
     if (r) return r;
     if (!x || !ids) return QMV_EINVAL;
     if (!aligned(x, 4) || !aligned(ids, 4)) return QMV_EALIGN;
-    const bool pk = packed_units(m, k);
+    const bool pk = packed_units(m, T, k);
     // the packed path also gets the work plan of the gate+up and down kernels
     qmv::PlanArgs plan{};
     if (pk) {
@@ -274,7 +279,7 @@ int prepare_impl(const qmv_moe_int4 *m, const float *x, int T, const int32_t *id
         at<int32_t>(ws, L.status), x, m->H, at<void>(ws, pk ? L.xpk : L.xcells),
         (pk ? nullptr : at<float>(ws, L.xfac)), cs(stream), 8, pk, at<int32_t>(ws, L.status),
         (int)(L.status_bytes / 4), true, res, served, logits, ids_out, w_out,
-        qmv::tma_moe_supported(dims(m)), pk ? &plan : nullptr));
+        tma_path(m, T, k), pk ? &plan : nullptr));
 }
 
 // Whole FFN (moe_expert_ffn_int4 with res == served == null).
@@ -296,8 +301,8 @@ int moe_ffn_gate_up(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_byt
     qmv::MoeWorkspace L;
     int r = ffn_check(m, T, k, ws, ws_bytes, L);
     if (r) return r;
-    if (qmv::tma_moe_supported(dims(m))) {
-        const bool pk = packed_units(m, k);
+    if (tma_path(m, T, k)) {
+        const bool pk = packed_units(m, T, k);
         return from_cuda(qmv::launch_moe_tma(
             dims(m), 0, at<void>(ws, pk ? L.xpk : L.xcells), (pk ? nullptr : at<float>(ws, L.xfac)), k,
             at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
@@ -319,8 +324,8 @@ int moe_ffn_down(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
     qmv::MoeWorkspace L;
     int r = ffn_check(m, T, k, ws, ws_bytes, L);
     if (r) return r;
-    if (qmv::tma_moe_supported(dims(m))) {
-        const bool pk = packed_units(m, k);
+    if (tma_path(m, T, k)) {
+        const bool pk = packed_units(m, T, k);
         return from_cuda(qmv::launch_moe_tma(
             dims(m), 1, at<void>(ws, pk ? L.hpk : L.hcells), (pk ? nullptr : at<float>(ws, L.hfac)), k,
             at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list), at<int32_t>(ws, L.uexp),
@@ -388,7 +393,7 @@ int moe_route_expert_ffn_int4(const qmv_moe_int4 *m, const float *logits, const 
                                     nullptr, nullptr, logits, ids, w);
         return from_cuda(e);
     }
-    if (T <= 32 && packed_units(m, k)) {
+    if (T <= 32 && packed_units(m, T, k)) {
         // a decode micro-batch: the grouping kernel routes the tokens itself
         qmv::MoeWorkspace L;
         if ((r = ffn_check(m, T, k, ws, ws_bytes, L))) return r;

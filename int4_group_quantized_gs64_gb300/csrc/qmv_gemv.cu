@@ -320,7 +320,7 @@ cudaError_t launch_gemv_int4(const uint8_t *wq, const float *scales, int N, int 
     int32_t *head = reinterpret_cast<int32_t *>(b);
     void *cells = b + kGemvHead;
     float *fac = reinterpret_cast<float *>(b + kGemvHead + (size_t)S * K * 4);
-    if (!tma_dense_supported(wq, scales, N, K))
+    if (!tma_dense_supported(wq, scales, N, K, S))
         return launch_dense<false>(wq, scales, N, K, x, y, S, cells, fac, st, head,
                                    1 + kSkMaxCtas);
     float *part = reinterpret_cast<float *>(b + gemv_part_offset(K, S));
@@ -333,7 +333,7 @@ cudaError_t launch_gemv_int4(const uint8_t *wq, const float *scales, int N, int 
 cudaError_t launch_gemv_int4_pair(const uint8_t *wq0, const float *s0, int N0, const uint8_t *wq1,
                                   const float *s1, int N1, int K, const float *x, float *y0,
                                   float *y1, int S, void *ws, cudaStream_t st) {
-    if (!tma_dense_supported(wq0, s0, N0, K) || !tma_dense_supported(wq1, s1, N1, K)) {
+    if (!tma_dense_supported(wq0, s0, N0, K, S) || !tma_dense_supported(wq1, s1, N1, K, S)) {
         cudaError_t e = launch_gemv_int4(wq0, s0, N0, K, x, y0, S, ws, st);
         return e == cudaSuccess ? launch_gemv_int4(wq1, s1, N1, K, x, y1, S, ws, st) : e;
     }

@@ -121,12 +121,13 @@ cudaError_t launch_pack_x(const uint16_t *x, int H, int k, const int32_t *offset
 // split between CTAs leaves partial sums in `part` and the last CTA to finish
 // it (counted in cnt, which must be zero at launch and is zero again after
 // the kernel) adds them and writes the item.
-bool tma_moe_supported(const MoeDims &m);
+// P: the call's token-expert pairs (0: shape and alignment only).
+bool tma_moe_supported(const MoeDims &m, long long P = 0);
 // 3-D tensor maps of a weight pool [E][rows][K/2] (box 128 B x box_rows rows,
 // 128-byte swizzle) and of its scales [E][rows][K/64] (box 4 x box_rows rows).
 bool encode_weight_maps(CUtensorMap *wmap, CUtensorMap *smap, const uint8_t *wq, const float *ws,
                         int E, int rows, int K, int box_rows = 128);
-bool tma_dense_supported(const uint8_t *wq, const float *scales, int N, int K);
+bool tma_dense_supported(const uint8_t *wq, const float *scales, int N, int K, int S);
 // wq2 != null: a second matrix [N2][K/2] against the same activations, its
 // row tiles after the first's in the same launch, output y2 [S][N2].
 cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int K, int S,

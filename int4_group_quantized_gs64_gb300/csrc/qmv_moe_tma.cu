@@ -421,20 +421,18 @@ __device__ __forceinline__ bool t_combine(const TmaArgs &a, TShared &sh, int nto
         }
     }
     // The barrier orders every consumer's partial-sum stores before thread 0's
-    // fence, whose cumulativity makes them visible device-wide before its
-    // counter update; on the other side thread 0's fence after the update
-    // orders the other CTAs' partials before the barrier that the readers
-    // pass. One fence per side, by the thread that touches the counter.
+    // counter update, a release whose cumulativity makes them visible
+    // device-wide first; the same atomic is an acquire, which orders the
+    // other CTAs' partials before the barrier that the readers pass.
     consumers_sync();
     const long long first = (long long)item * ns;
     const int bf = unit_owner(sh.ub, g, first), bl = unit_owner(sh.ub, g, first + ns - 1);
     if (threadIdx.x == 0) {
         int n = 0;  // CTAs of [bf, bl] with a non-empty range all hold stages of this item
         for (int c = bf; c <= bl; ++c) n += sh.ub[c + 1] > sh.ub[c];
-        __threadfence();
-        const bool last = atomicAdd(&a.cnt[bf], 1) == n - 1;
-        if (last) __threadfence();
-        sh.last = last;
+        int old;  // acquire-release at gpu scope: the partials above, then the others'
+        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(&a.cnt[bf]) : "memory");
+        sh.last = old == n - 1;
     }
     consumers_sync();
     if (!sh.last) return false;
@@ -701,12 +699,19 @@ bool encode_weight_maps(CUtensorMap *wmap, CUtensorMap *smap, const uint8_t *wq,
     return true;
 }
 
-bool tma_moe_supported(const MoeDims &m) {
+bool tma_moe_supported(const MoeDims &m, long long P) {
     // tensor maps need 16-byte aligned bases and 16-byte strides (scale rows of
     // K/64 floats: K/64 a multiple of 4)
     auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-    return encode_fn() != nullptr && (m.H / kGroup) % 4 == 0 && (m.I / kGroup) % 4 == 0 &&
-           a16(m.gu_q) && a16(m.gu_s) && a16(m.dn_q) && a16(m.dn_s);
+    if (!(encode_fn() != nullptr && (m.H / kGroup) % 4 == 0 && (m.I / kGroup) % 4 == 0 &&
+          a16(m.gu_q) && a16(m.gu_s) && a16(m.dn_q) && a16(m.dn_s)))
+        return false;
+    // the kernel numbers items and stage boundaries with 32-bit ints: passes x
+    // stages per pass must fit
+    const long long passes = std::min(P, (P + kMaxTok - 1) / kMaxTok + std::min((long long)m.E, P));
+    const long long s_gu = (long long)((m.I + kTGuJ - 1) / kTGuJ) * (m.H / 256);
+    const long long s_dn = (long long)((m.H + kTDnRows - 1) / kTDnRows) * (m.I / 256);
+    return passes * std::max(s_gu, s_dn) < (1LL << 31) - 1;
 }
 
 cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const float *cfac, int k,
@@ -753,11 +758,14 @@ int tma_grid() {
     return std::min(kSkMaxCtas, sm_count() * max_ctas_per_sm(k_moe_tma, kTThreads, kTSmem));
 }
 
-bool tma_dense_supported(const uint8_t *wq, const float *scales, int N, int K) {
+bool tma_dense_supported(const uint8_t *wq, const float *scales, int N, int K, int S) {
     auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-    // a partial last row tile reads zeros past row N and writes nothing there
+    // a partial last row tile reads zeros past row N and writes nothing there;
+    // the kernel numbers its items with 32-bit ints
+    const long long stages =
+        (long long)((S + kMaxTok - 1) / kMaxTok) * ((N + kTDnRows - 1) / kTDnRows) * (K / 256);
     return encode_fn() != nullptr && N % 16 == 0 && (K / kGroup) % 4 == 0 && a16(wq) &&
-           a16(scales);
+           a16(scales) && stages < (1LL << 31) - 1;
 }
 
 // Dense mode over one matrix, or a pair sharing the activations (wq2 != null):
