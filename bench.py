@@ -591,6 +591,16 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     Bq = wq.nbytes + sc.nbytes + x.nbytes + N * 4
     rows["int4_gemv_14336x4096"] = {"us": t * 1e6, "GBs": Bq / t / 1e9, "frac": Bq / t / 1e9 / peak,
                                     "bytes": Bq, "launches_per_call": 2}
+    # the same with the output rounded to bf16 (qmv_int4_gs_bf16)
+    ybf = torch.empty((1, N), dtype=torch.bfloat16, device=dev)
+    gs = [graph_of(lambda: [q.qmv_int4_gs_bf16(wqs[i], scs[i], xd, y=ybf, ws=wsd, stream=stream)
+                            for i in range(C)], stream)]
+    time_graphs(gs, 4, stream)
+    t = time_graphs(gs, 32, stream) / C
+    Bqh = wq.nbytes + sc.nbytes + x.nbytes + N * 2
+    rows["int4_gemv_14336x4096_bf16out"] = {"us": t * 1e6, "GBs": Bqh / t / 1e9,
+                                            "frac": Bqh / t / 1e9 / peak, "bytes": Bqh,
+                                            "launches_per_call": 2}
     del wqs, scs, gs
     w8, r8, x8 = datagen.dense_int8(N, K, 1)
     C8 = 8
@@ -603,6 +613,14 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     B8 = w8.nbytes + r8.nbytes + x.nbytes + N * 4
     rows["int8_gemv_14336x4096"] = {"us": t * 1e6, "GBs": B8 / t / 1e9, "frac": B8 / t / 1e9 / peak,
                                     "bytes": B8, "launches_per_call": 2}
+    gs = [graph_of(lambda: [q.qmv_int8_row_bf16(w8s[i], r8d, xd, y=ybf, ws=wsd, stream=stream)
+                            for i in range(C8)], stream)]
+    time_graphs(gs, 4, stream)
+    t = time_graphs(gs, 64, stream) / C8
+    B8h = w8.nbytes + r8.nbytes + x.nbytes + N * 2
+    rows["int8_gemv_14336x4096_bf16out"] = {"us": t * 1e6, "GBs": B8h / t / 1e9,
+                                            "frac": B8h / t / 1e9 / peak, "bytes": B8h,
+                                            "launches_per_call": 2}
     del w8s, gs
     # int3-g64 two-plane GEMV, 14336 x 4096, one token (16 rotating copies, 410 MB)
     rng3 = np.random.default_rng(3)

@@ -90,6 +90,20 @@ size_t qmv_gemv_workspace_bytes(int K, int S);
 int qmv_int4_gs(const uint8_t *wq, const float *scales, int N, int K, int gs, const float *x,
                 float *y, int S, void *ws, size_t ws_bytes, qmv_stream_t stream);
 
+/* qmv_int4_gs with a bf16 output (colibri PR #418: the commit "vk_matmul_qt
+ * routes a resident int4/int8 matmul_qt through coli_vk_matmul", whose dense
+ * projections feed the next layer, and the rmsnorm / coli_vk_attn_qprep
+ * chain that consumes them on the device; bf16 is the reading of the
+ * activation type that chain passes on). The sum is formed exactly as in
+ * qmv_int4_gs, in fp32, and each output is then rounded to the nearest bf16
+ * value, ties to even:
+ *   y_bf16  [S][N] bf16 bit patterns (uint16_t, 2-byte aligned; written)
+ *   every other argument, the workspace and the errors as qmv_int4_gs.
+ * For the same inputs and workspace size the result is the fp32 output of
+ * qmv_int4_gs rounded to bf16, bit for bit. */
+int qmv_int4_gs_bf16(const uint8_t *wq, const float *scales, int N, int K, int gs, const float *x,
+                     uint16_t *y_bf16, int S, void *ws, size_t ws_bytes, qmv_stream_t stream);
+
 /* Two int4-gs64 GEMVs against the same activations (colibri PR #418, commit
  * "qmatmul staged-x length fix": matmul_pair stages x once for the q_a and
  * kv_a projections, 6144 -> (2048, 576), and records both in one submit):
@@ -134,6 +148,13 @@ int qmv_int3_gs(const uint8_t *wq3, const float *scales, int N, int K, int gs, c
  *   Errors as qmv_int4_gs. */
 int qmv_int8_row(const int8_t *w, const float *row_scale, int N, int K, const float *x,
                  float *y, int S, void *ws, size_t ws_bytes, qmv_stream_t stream);
+
+/* qmv_int8_row with a bf16 output (as qmv_int4_gs_bf16): the fp32 result of
+ * qmv_int8_row rounded to the nearest bf16, ties to even, into
+ *   y_bf16  [S][N] bf16 bit patterns (uint16_t, 2-byte aligned; written);
+ *   every other argument, the workspace and the errors as qmv_int8_row. */
+int qmv_int8_row_bf16(const int8_t *w, const float *row_scale, int N, int K, const float *x,
+                      uint16_t *y_bf16, int S, void *ws, size_t ws_bytes, qmv_stream_t stream);
 
 /* The dense int4-gs64 GEMV of qmv_int4_gs for callers that cannot allocate
  * device memory: code that must never make the device synchronise (cudaMalloc

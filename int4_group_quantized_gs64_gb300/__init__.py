@@ -6,7 +6,8 @@ provides device memory and streams); outputs are allocated with torch when the
 caller passes none. There is no CPU fallback: if the library cannot be loaded,
 every call raises.
 
-Functions carry the C names: ``qmv_int4_gs``, ``qmv_int8_row``,
+Functions carry the C names: ``qmv_int4_gs``, ``qmv_int8_row``, their bf16-output
+forms ``qmv_int4_gs_bf16`` and ``qmv_int8_row_bf16``,
 ``moe_route_topk``, ``moe_group``, ``moe_gate_up_silu``, ``moe_down``,
 ``moe_combine``, ``moe_workspace_bytes``, ``moe_expert_ffn_int4`` and
 ``moe_expert_ffn_int4_prefill``.
@@ -65,6 +66,8 @@ def lib():
                                  i32),
             "qmv_int3_gs": ([vp, vp, i32, i32, i32, vp, vp, i32, vp], i32),
             "qmv_int8_row": ([vp, vp, i32, i32, vp, vp, i32, vp, sz, vp], i32),
+            "qmv_int4_gs_bf16": ([vp, vp, i32, i32, i32, vp, vp, i32, vp, sz, vp], i32),
+            "qmv_int8_row_bf16": ([vp, vp, i32, i32, vp, vp, i32, vp, sz, vp], i32),
             "moe_route_topk": ([vp, i32, i32, i32, vp, vp, vp], i32),
             "moe_group": ([vp, i32, i32, i32, vp, vp, vp, vp, vp, vp], i32),
             "moe_gate_up_silu": ([P, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp], i32),
@@ -144,6 +147,24 @@ def qmv_int4_gs(wq, scales, x, y=None, gs: int = 64, ws=None, stream=None):
     return y
 
 
+def qmv_int4_gs_bf16(wq, scales, x, y=None, gs: int = 64, ws=None, stream=None):
+    """qmv_int4_gs with the fp32 result rounded to bf16 (ties to even): y bf16 [S][N]."""
+    import torch
+    _need(wq, torch.uint8, "wq"); _need(scales, torch.float32, "scales"); _need(x, torch.float32, "x")
+    N, K = wq.shape[0], wq.shape[1] * 2
+    x2 = x.view(-1, K)
+    S = x2.shape[0]
+    if y is None:
+        y = torch.empty((S, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, "y")
+    if ws is None:
+        ws = _workspace(qmv_gemv_workspace_bytes(K, S), x.device)
+    _check("qmv_int4_gs_bf16", lib().qmv_int4_gs_bf16(_ptr(wq), _ptr(scales), N, K, gs, _ptr(x2),
+                                                      _ptr(y), S, _ptr(ws), ws.numel(),
+                                                      _stream(stream)))
+    return y
+
+
 def qmv_int4_gs_pair(wq0, s0, wq1, s1, x, y0=None, y1=None, gs: int = 64, ws=None, stream=None):
     """(y0, y1) = (W0 . x, W1 . x) for two int4-gs64 matrices sharing x [S][K]."""
     import torch
@@ -202,6 +223,24 @@ def qmv_int8_row(w, row_scale, x, y=None, ws=None, stream=None):
         ws = _workspace(qmv_gemv_workspace_bytes(K, S), x.device)
     _check("qmv_int8_row", lib().qmv_int8_row(_ptr(w), _ptr(row_scale), N, K, _ptr(x2), _ptr(y), S,
                                               _ptr(ws), ws.numel(), _stream(stream)))
+    return y
+
+
+def qmv_int8_row_bf16(w, row_scale, x, y=None, ws=None, stream=None):
+    """qmv_int8_row with the fp32 result rounded to bf16 (ties to even): y bf16 [S][N]."""
+    import torch
+    _need(w, torch.int8, "w"); _need(row_scale, torch.float32, "row_scale"); _need(x, torch.float32, "x")
+    N, K = w.shape
+    x2 = x.view(-1, K)
+    S = x2.shape[0]
+    if y is None:
+        y = torch.empty((S, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, "y")
+    if ws is None:
+        ws = _workspace(qmv_gemv_workspace_bytes(K, S), x.device)
+    _check("qmv_int8_row_bf16", lib().qmv_int8_row_bf16(_ptr(w), _ptr(row_scale), N, K, _ptr(x2),
+                                                        _ptr(y), S, _ptr(ws), ws.numel(),
+                                                        _stream(stream)))
     return y
 
 

@@ -111,6 +111,17 @@ int qmv_int4_gs(const uint8_t *wq, const float *scales, int N, int K, int gs, co
     return from_cuda(qmv::launch_gemv_int4(wq, scales, N, K, x, y, S, ws, cs(stream)));
 }
 
+int qmv_int4_gs_bf16(const uint8_t *wq, const float *scales, int N, int K, int gs, const float *x,
+                     uint16_t *y_bf16, int S, void *ws, size_t ws_bytes, qmv_stream_t stream) {
+    if (!wq || !scales || !x || !y_bf16 || N < 1 || S < 1 || gs != 64) return QMV_EINVAL;
+    if (K < 64 || K % 64 || K > kMaxK) return QMV_ESHAPE;
+    if (!aligned(wq, 16) || !aligned(scales, 4) || !aligned(x, 4) || !aligned(y_bf16, 2))
+        return QMV_EALIGN;
+    if (!ws || !aligned(ws, 256) || ws_bytes < qmv_gemv_workspace_bytes(K, S)) return QMV_EWORKSPACE;
+    return from_cuda(
+        qmv::launch_gemv_int4(wq, scales, N, K, x, nullptr, S, ws, cs(stream), y_bf16));
+}
+
 int qmv_int4_gs_pair(const uint8_t *wq0, const float *s0, int N0, const uint8_t *wq1,
                      const float *s1, int N1, int K, int gs, const float *x, float *y0, float *y1,
                      int S, void *ws, size_t ws_bytes, qmv_stream_t stream) {
@@ -142,6 +153,17 @@ int qmv_int8_row(const int8_t *w, const float *row_scale, int N, int K, const fl
         return QMV_EALIGN;
     if (!ws || !aligned(ws, 256) || ws_bytes < qmv_gemv_workspace_bytes(K, S)) return QMV_EWORKSPACE;
     return from_cuda(qmv::launch_gemv_int8(w, row_scale, N, K, x, y, S, ws, cs(stream)));
+}
+
+int qmv_int8_row_bf16(const int8_t *w, const float *row_scale, int N, int K, const float *x,
+                      uint16_t *y_bf16, int S, void *ws, size_t ws_bytes, qmv_stream_t stream) {
+    if (!w || !row_scale || !x || !y_bf16 || N < 1 || S < 1) return QMV_EINVAL;
+    if (K < 64 || K % 64 || K > kMaxK) return QMV_ESHAPE;
+    if (!aligned(w, 16) || !aligned(row_scale, 4) || !aligned(x, 4) || !aligned(y_bf16, 2))
+        return QMV_EALIGN;
+    if (!ws || !aligned(ws, 256) || ws_bytes < qmv_gemv_workspace_bytes(K, S)) return QMV_EWORKSPACE;
+    return from_cuda(
+        qmv::launch_gemv_int8(w, row_scale, N, K, x, nullptr, S, ws, cs(stream), y_bf16));
 }
 
 int moe_route_topk(const float *logits, int T, int E, int k, int32_t *ids, float *w,

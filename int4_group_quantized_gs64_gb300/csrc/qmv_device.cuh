@@ -22,6 +22,7 @@
 // depend on the order of its terms).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -85,6 +86,13 @@ __device__ __forceinline__ void mma_16816(float d[4], const uint32_t a[4], uint3
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Output element i of a GEMV: fp32 into y, or, when ybf is set, the fp32
+// result rounded to the nearest bf16 (ties to even) into ybf.
+__device__ __forceinline__ void store_y(float *y, uint16_t *ybf, size_t i, float v) {
+    if (ybf) ybf[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    else y[i] = v;
 }
 
 // ------------------------------------------------------------------ dequant

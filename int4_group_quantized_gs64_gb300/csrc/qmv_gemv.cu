@@ -73,8 +73,8 @@ __global__ void __launch_bounds__(256)
 
 template <int NB, bool kInt8, class WS>
 __device__ __forceinline__ void dense_item(WS &ws, int &cslot, int row0, int N, const float *scales,
-                                           float *y, uint4 *cells, float *fac, int ntok, bool reuse,
-                                           const StageCells &stage) {
+                                           float *y, uint16_t *ybf, uint4 *cells, float *fac,
+                                           int ntok, bool reuse, const StageCells &stage) {
     const int lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
     float acc[NB][2];
     run_item<NB, kInt8>(ws, cslot, cells, fac, kDenseBudget, ntok, reuse, stage, acc);
@@ -88,8 +88,8 @@ __device__ __forceinline__ void dense_item(WS &ws, int &cslot, int row0, int N, 
     for (int nb = 0; nb < NB; ++nb) {
         const int t = 4 * nb + q;
         if (t < ntok) {
-            if (rA < N) y[(size_t)t * N + rA] = acc[nb][0] * ra;
-            if (rB < N) y[(size_t)t * N + rB] = acc[nb][1] * rb;
+            if (rA < N) store_y(y, ybf, (size_t)t * N + rA, acc[nb][0] * ra);
+            if (rB < N) store_y(y, ybf, (size_t)t * N + rB, acc[nb][1] * rb);
         }
     }
 }
@@ -130,7 +130,7 @@ template <bool kInt8>
 __global__ void __launch_bounds__(32 * kDenseWarps)
     k_dense(const uint8_t *__restrict__ w, const float *__restrict__ scales, int N, int K,
             const uint4 *__restrict__ xcells, const float *__restrict__ xfac,
-            float *__restrict__ y, int ntok) {
+            float *__restrict__ y, uint16_t *__restrict__ ybf, int ntok) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ int s_rows[kMaxTok];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -157,9 +157,11 @@ __global__ void __launch_bounds__(32 * kDenseWarps)
         const int row0 = (i0 + it) * 16 * kDenseWarps + 16 * warp;
         const bool reuse = it > 0;
         if (ntok <= 4)
-            dense_item<1, kInt8>(ws, cslot, row0, N, scales, y, cells, fac, ntok, reuse, stage);
+            dense_item<1, kInt8>(ws, cslot, row0, N, scales, y, ybf, cells, fac, ntok, reuse,
+                                 stage);
         else
-            dense_item<2, kInt8>(ws, cslot, row0, N, scales, y, cells, fac, ntok, reuse, stage);
+            dense_item<2, kInt8>(ws, cslot, row0, N, scales, y, ybf, cells, fac, ntok, reuse,
+                                 stage);
     }
     cp_async_wait<0>();
 }
@@ -176,7 +178,7 @@ template <bool kInt8>
 __global__ void __launch_bounds__(32 * kKsWarps)
     k_dense_ks(const uint8_t *__restrict__ w, const float *__restrict__ scales, int N, int K,
                const uint4 *__restrict__ xcells, const float *__restrict__ xfac,
-               float *__restrict__ y, int ntok) {
+               float *__restrict__ y, uint16_t *__restrict__ ybf, int ntok) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ float red[kKsWarps][16][4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
@@ -225,8 +227,8 @@ __global__ void __launch_bounds__(32 * kKsWarps)
                 if (rA < N) a0 *= scales[rA];
                 if (rB < N) a1 *= scales[rB];
             }
-            if (rA < N) y[(size_t)q * N + rA] = a0;
-            if (rB < N) y[(size_t)q * N + rB] = a1;
+            if (rA < N) store_y(y, ybf, (size_t)q * N + rA, a0);
+            if (rB < N) store_y(y, ybf, (size_t)q * N + rB, a1);
         }
         __syncthreads();
     }
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(32 * kKsWarps)
 template <bool kInt8>
 cudaError_t launch_dense(const uint8_t *w, const float *scales, int N, int K, const float *x,
                          float *y, int S, void *xcells, float *xfac, cudaStream_t st,
-                         int32_t *zero = nullptr, int nzero = 0) {
+                         int32_t *zero = nullptr, int nzero = 0, uint16_t *ybf = nullptr) {
     const size_t smem = engine_smem(kDenseWarps, kDenseStages, kDenseBudget, 0);
     cudaError_t e = set_smem(k_dense<kInt8>, smem);
     if (e != cudaSuccess) return e;
@@ -256,14 +258,15 @@ cudaError_t launch_dense(const uint8_t *w, const float *scales, int N, int K, co
         if (e == cudaSuccess)
             e = launch(k_dense_ks<kInt8>, dim3(items < slots_ks ? items : slots_ks),
                        dim3(32 * kKsWarps), smem_ks, st, true, w, scales, N, K,
-                       static_cast<const uint4 *>(xcells), (const float *)xfac, y, S);
+                       static_cast<const uint4 *>(xcells), (const float *)xfac, y, ybf, S);
         return e;
     }
     for (int s0 = 0; s0 < S && e == cudaSuccess; s0 += kMaxTok) {
         const int ntok = S - s0 < kMaxTok ? S - s0 : kMaxTok;
         e = launch(k_dense<kInt8>, dim3(grid), dim3(32 * kDenseWarps), smem, st, true, w, scales, N,
                    K, static_cast<const uint4 *>(xcells) + (size_t)s0 * (K / kGroup) * 16,
-                   xfac + (size_t)s0 * (K / kGroup), y + (size_t)s0 * N, ntok);
+                   xfac + (size_t)s0 * (K / kGroup), y ? y + (size_t)s0 * N : nullptr,
+                   ybf ? ybf + (size_t)s0 * N : nullptr, ntok);
     }
     return e;
 }
@@ -315,19 +318,20 @@ size_t gemv_ws_bytes(int K, int S) {
 }
 
 cudaError_t launch_gemv_int4(const uint8_t *wq, const float *scales, int N, int K, const float *x,
-                             float *y, int S, void *ws, cudaStream_t st) {
+                             float *y, int S, void *ws, cudaStream_t st, uint16_t *ybf) {
     char *b = static_cast<char *>(ws);
     int32_t *head = reinterpret_cast<int32_t *>(b);
     void *cells = b + kGemvHead;
     float *fac = reinterpret_cast<float *>(b + kGemvHead + (size_t)S * K * 4);
     if (!tma_dense_supported(wq, scales, N, K, S))
         return launch_dense<false>(wq, scales, N, K, x, y, S, cells, fac, st, head,
-                                   1 + kSkMaxCtas);
+                                   1 + kSkMaxCtas, ybf);
     float *part = reinterpret_cast<float *>(b + gemv_part_offset(K, S));
     cudaError_t e = launch(k_split<false, true>, dim3(S, (K / kGroup + 7) / 8), dim3(256), 0, st,
                            false, x, K, static_cast<uint4 *>(cells), fac, head, 1 + kSkMaxCtas);
     if (e != cudaSuccess) return e;
-    return launch_dense_tma(wq, scales, N, K, S, cells, fac, y, head, head + 1, part, st);
+    return launch_dense_tma(wq, scales, N, K, S, cells, fac, y, head, head + 1, part, st, nullptr,
+                            nullptr, 0, nullptr, ybf);
 }
 
 cudaError_t launch_gemv_int4_pair(const uint8_t *wq0, const float *s0, int N0, const uint8_t *wq1,
@@ -350,12 +354,13 @@ cudaError_t launch_gemv_int4_pair(const uint8_t *wq0, const float *s0, int N0, c
 }
 
 cudaError_t launch_gemv_int8(const int8_t *w, const float *row_scale, int N, int K,
-                             const float *x, float *y, int S, void *ws, cudaStream_t st) {
+                             const float *x, float *y, int S, void *ws, cudaStream_t st,
+                             uint16_t *ybf) {
     char *b = static_cast<char *>(ws);
     float *fac = reinterpret_cast<float *>(b + kGemvHead + (size_t)S * K * 4);
     return launch_dense<true>(reinterpret_cast<const uint8_t *>(w), row_scale, N, K, x, y, S,
                               b + kGemvHead, fac, st, reinterpret_cast<int32_t *>(b),
-                              1 + kSkMaxCtas);
+                              1 + kSkMaxCtas, ybf);
 }
 
 }  // namespace qmv

@@ -23,10 +23,12 @@ cudaError_t launch_dense_int8(const int8_t *w, const float *row_scale, int N, in
 // units, partial sums): gemv_ws_bytes(K, S) bytes. int4 runs on the
 // tensor-map kernel (qmv_moe_tma.cu, dense mode) when tma_dense_supported().
 size_t gemv_ws_bytes(int K, int S);
+// ybf (optional): write y rounded to bf16 there instead of fp32 into y.
 cudaError_t launch_gemv_int4(const uint8_t *wq, const float *scales, int N, int K, const float *x,
-                             float *y, int S, void *ws, cudaStream_t st);
+                             float *y, int S, void *ws, cudaStream_t st, uint16_t *ybf = nullptr);
 cudaError_t launch_gemv_int8(const int8_t *w, const float *row_scale, int N, int K,
-                             const float *x, float *y, int S, void *ws, cudaStream_t st);
+                             const float *x, float *y, int S, void *ws, cudaStream_t st,
+                             uint16_t *ybf = nullptr);
 // int3-g64 two-plane rows [N][K/64 * 24 bytes], fp32 x [S][K] (16-byte aligned).
 cudaError_t launch_gemv_int3(const uint8_t *wq, const float *scales, int N, int K, const float *x,
                              float *y, int S, cudaStream_t st);
@@ -134,7 +136,7 @@ cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int 
                              const void *cells, const float *cfac, float *y, int32_t *status,
                              int32_t *cnt, float *part, cudaStream_t st,
                              const uint8_t *wq2 = nullptr, const float *scales2 = nullptr,
-                             int N2 = 0, float *y2 = nullptr);
+                             int N2 = 0, float *y2 = nullptr, uint16_t *ybf = nullptr);
 // packed: the activation units (cells, cfac) and, for gate+up, the units of
 // h it writes (hcells, hfac) are in the pass-packed layout; else per row.
 // ptab / plan (optional): the grouping kernel's pass table and this mode's

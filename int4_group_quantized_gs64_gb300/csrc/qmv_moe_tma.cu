@@ -84,7 +84,8 @@ struct TmaArgs {
     float *h;            // gate+up: h fp32 [P][I]
     uint4 *hcells;       // gate+up: units of h [P][I/64][16], or pass-packed blocks
     float *hfac;         // gate+up: records of h [P][I/64][2] (per-row layout only)
-    float *y;            // down: y [P][H]
+    float *y;            // down: y [P][H]; dense: y [S][H]
+    uint16_t *ybf;       // dense, first matrix: y rounded to bf16 [S][H] instead of y
     const int4 *ptab;    // the grouping kernel's pass table, or null (PlanArgs)
     const int32_t *plan; // this mode's CTA stage boundaries [g + 1], or null
     int32_t *status;
@@ -313,9 +314,11 @@ __device__ __forceinline__ void t_epilogue(const TmaArgs &a, const TShared &sh, 
         for (int nb = 0; nb < NB; ++nb) {
             const int s = 4 * nb + q;
             if (s < ntok) {
-                float *yb = (second ? a.y2 : a.y) + (size_t)sh.pairs[s] * H;
-                if (r0 < H) yb[r0] = acc[nb][0];
-                if (r0 + 8 < H) yb[r0 + 8] = acc[nb][1];
+                float *yb = second ? a.y2 : a.y;
+                uint16_t *hb = second ? nullptr : a.ybf;
+                const size_t o = (size_t)sh.pairs[s] * H + r0;
+                if (r0 < H) store_y(yb, hb, o, acc[nb][0]);
+                if (r0 + 8 < H) store_y(yb, hb, o + 8, acc[nb][1]);
             }
         }
         return;
@@ -773,7 +776,7 @@ bool tma_dense_supported(const uint8_t *wq, const float *scales, int N, int K, i
 cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int K, int S,
                              const void *cells, const float *cfac, float *y, int32_t *status,
                              int32_t *cnt, float *part, cudaStream_t st, const uint8_t *wq2,
-                             const float *scales2, int N2, float *y2) {
+                             const float *scales2, int N2, float *y2, uint16_t *ybf) {
     TmaArgs a;
     memset(&a, 0, sizeof(a));
     a.mode = 2;
@@ -784,6 +787,7 @@ cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int 
     a.cells = static_cast<const uint4 *>(cells);
     a.cfac = cfac;
     a.y = y;
+    a.ybf = ybf;
     a.status = status;
     a.cnt = cnt;
     a.part = part;

@@ -38,7 +38,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("qmv_gemv_workspace_bytes", "qmv_int4_gs", "qmv_int4_gs_pair", "qmv_int3_gs",
-              "qmv_int8_row",
+              "qmv_int8_row", "qmv_int4_gs_bf16", "qmv_int8_row_bf16",
               "moe_route_topk", "moe_group", "moe_gate_up_silu",
               "moe_down", "moe_combine", "moe_workspace_bytes", "moe_expert_ffn_int4"):
         assert n in names
@@ -93,6 +93,17 @@ def test_dense_validation(L):
     assert L.qmv_int8_row(p, p, 8, 100, p, p, 1, *ok) == ESHAPE
     assert L.qmv_int8_row(ctypes.c_void_p(FAKE + 4), p, 8, 64, p, p, 1, *ok) == EALIGN
     assert L.qmv_int8_row(p, p, 8, 64, p, p, 1, p, 0, None) == EWORKSPACE
+    # bf16 outputs: same arguments, y is bf16 (2-byte aligned)
+    odd = ctypes.c_void_p(FAKE + 1)
+    assert L.qmv_int4_gs_bf16(p, p, 8, 64, 64, p, None, 1, *ok) == EINVAL
+    assert L.qmv_int4_gs_bf16(p, p, 8, 64, 32, p, p, 1, *ok) == EINVAL
+    assert L.qmv_int4_gs_bf16(p, p, 8, 96, 64, p, p, 1, *ok) == ESHAPE
+    assert L.qmv_int4_gs_bf16(p, p, 8, 64, 64, p, odd, 1, *ok) == EALIGN
+    assert L.qmv_int4_gs_bf16(p, p, 8, 64, 64, p, ctypes.c_void_p(FAKE + 2), 1, p, 0, None) == EWORKSPACE
+    assert L.qmv_int8_row_bf16(p, None, 8, 64, p, p, 1, *ok) == EINVAL
+    assert L.qmv_int8_row_bf16(p, p, 8, 100, p, p, 1, *ok) == ESHAPE
+    assert L.qmv_int8_row_bf16(p, p, 8, 64, p, odd, 1, *ok) == EALIGN
+    assert L.qmv_int8_row_bf16(p, p, 8, 64, p, p, 1, p, 0, None) == EWORKSPACE
 
 
 def test_route_and_group_validation(L):

@@ -243,3 +243,58 @@ def test_bad_arguments_leave_output_untouched():
         q.qmv_int4_gs(wq, sc, x, y=y)
     torch.cuda.synchronize()
     assert torch.all(y == 7.0)
+
+
+# ------------------------------------------------------------------ bf16 outputs
+
+def bf16_rne(y32):
+    """fp32 -> bf16 bit patterns, round to nearest, ties to even (finite inputs)."""
+    b = np.ascontiguousarray(y32, np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def bf16_to_f64(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def half_ulp_bf16(v):
+    """Half the spacing of bf16 values at |v| (8 significand bits)."""
+    e = np.floor(np.log2(np.maximum(np.abs(v), np.finfo(np.float32).tiny)))
+    return np.ldexp(1.0, (e - 8).astype(int))
+
+
+def check_bf16(ybf, y32, ref, den):
+    bits = ybf.view(torch.int16).cpu().numpy().view(np.uint16)
+    # the fp32 result of the same kernel, rounded here: equal bit for bit
+    assert np.array_equal(bits, bf16_rne(y32))
+    # and within the fp32 tolerance plus half a bf16 ulp of the exact result
+    g = bf16_to_f64(bits)
+    bound = TOL_FP32 * den + half_ulp_bf16(np.maximum(np.abs(g), np.abs(ref)))
+    assert np.all(np.abs(g - ref) <= bound)
+
+
+@pytest.mark.parametrize("N,K,S", [(14336, 4096, 1), (1024, 1024, 1), (512, 1024, 9),
+                                   (1000, 2048, 3), (63, 1088, 4), (40, 256, 17)])
+def test_int4_bf16_output(N, K, S):
+    """qmv_int4_gs_bf16 on the tensor-map path (N % 16 == 0) and the cp.async
+    path (other N), one and several token passes."""
+    wq, sc, x = datagen.dense_int4(N, K, S, seed=N + K + S)
+    ws = torch.empty(q.qmv_gemv_workspace_bytes(K, S), dtype=torch.uint8, device="cuda")
+    dwq, dsc, dx = dev(wq), dev(sc), dev(x)
+    y32 = q.qmv_int4_gs(dwq, dsc, dx, ws=ws)
+    ybf = q.qmv_int4_gs_bf16(dwq, dsc, dx, ws=ws)
+    torch.cuda.synchronize()
+    ref, den = oracle.qmv_int4_gs(wq, sc, x, 64, with_den=True)
+    check_bf16(ybf, y32.cpu().numpy(), ref, den)
+
+
+@pytest.mark.parametrize("N,K,S", [(14336, 4096, 1), (100, 192, 5), (33, 640, 16)])
+def test_int8_bf16_output(N, K, S):
+    w, r, x = datagen.dense_int8(N, K, S, seed=N + K + S)
+    ws = torch.empty(q.qmv_gemv_workspace_bytes(K, S), dtype=torch.uint8, device="cuda")
+    dw, dr, dx = dev(w), dev(r), dev(x)
+    y32 = q.qmv_int8_row(dw, dr, dx, ws=ws)
+    ybf = q.qmv_int8_row_bf16(dw, dr, dx, ws=ws)
+    torch.cuda.synchronize()
+    ref, den = oracle.qmv_int8_row(w, r, x)
+    check_bf16(ybf, y32.cpu().numpy(), ref, den)
