@@ -590,7 +590,7 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     t = time_graphs(gs, 32, stream) / C
     Bq = wq.nbytes + sc.nbytes + x.nbytes + N * 4
     rows["int4_gemv_14336x4096"] = {"us": t * 1e6, "GBs": Bq / t / 1e9, "frac": Bq / t / 1e9 / peak,
-                                    "bytes": Bq, "launches_per_call": 2}
+                                    "bytes": Bq, "launches_per_call": 1}
     # the same with the output rounded to bf16 (qmv_int4_gs_bf16)
     ybf = torch.empty((1, N), dtype=torch.bfloat16, device=dev)
     gs = [graph_of(lambda: [q.qmv_int4_gs_bf16(wqs[i], scs[i], xd, y=ybf, ws=wsd, stream=stream)
@@ -600,7 +600,7 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     Bqh = wq.nbytes + sc.nbytes + x.nbytes + N * 2
     rows["int4_gemv_14336x4096_bf16out"] = {"us": t * 1e6, "GBs": Bqh / t / 1e9,
                                             "frac": Bqh / t / 1e9 / peak, "bytes": Bqh,
-                                            "launches_per_call": 2}
+                                            "launches_per_call": 1}
     del wqs, scs, gs
     w8, r8, x8 = datagen.dense_int8(N, K, 1)
     C8 = 8
@@ -612,7 +612,7 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     t = time_graphs(gs, 64, stream) / C8
     B8 = w8.nbytes + r8.nbytes + x.nbytes + N * 4
     rows["int8_gemv_14336x4096"] = {"us": t * 1e6, "GBs": B8 / t / 1e9, "frac": B8 / t / 1e9 / peak,
-                                    "bytes": B8, "launches_per_call": 2}
+                                    "bytes": B8, "launches_per_call": 1}
     gs = [graph_of(lambda: [q.qmv_int8_row_bf16(w8s[i], r8d, xd, y=ybf, ws=wsd, stream=stream)
                             for i in range(C8)], stream)]
     time_graphs(gs, 4, stream)
@@ -620,7 +620,7 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     B8h = w8.nbytes + r8.nbytes + x.nbytes + N * 2
     rows["int8_gemv_14336x4096_bf16out"] = {"us": t * 1e6, "GBs": B8h / t / 1e9,
                                             "frac": B8h / t / 1e9 / peak, "bytes": B8h,
-                                            "launches_per_call": 2}
+                                            "launches_per_call": 1}
     del w8s, gs
     # int3-g64 two-plane GEMV, 14336 x 4096, one token (16 rotating copies, 410 MB)
     rng3 = np.random.default_rng(3)
@@ -650,7 +650,7 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     Bq4 = wq.nbytes + sc.nbytes + x4.numel() * 4 + 4 * N * 4
     rows["int4_gemv_14336x4096_s4"] = {"us": t * 1e6, "GBs": Bq4 / t / 1e9,
                                        "frac": Bq4 / t / 1e9 / peak, "bytes": Bq4,
-                                       "token_eq_per_s": 4 / t, "launches_per_call": 2}
+                                       "token_eq_per_s": 4 / t, "launches_per_call": 1}
     del wqs, scs, gs
     # pair of int4 GEMVs sharing x (q_a + kv_a shape 6144 -> (2048, 576)), one token;
     # 24 rotating weight copies (218 MB, above L2)
@@ -680,7 +680,7 @@ def measure_rows(q, datagen, dev, stream, peak, pool):
     Bp = (N0 + N1) * (K2 // 2 + K2 // 64 * 4) + K2 * 4 + (N0 + N1) * 4
     rows["int4_gemv_pair_6144_2048_576"] = {"us": t * 1e6, "GBs": Bp / t / 1e9,
                                             "frac": Bp / t / 1e9 / peak, "bytes": Bp,
-                                            "two_calls_us": t2 * 1e6, "launches_per_call": 2}
+                                            "two_calls_us": t2 * 1e6, "launches_per_call": 1}
     del pq, gs
     # the 8-token layer with half of the 160 experts resident (served mask);
     # bytes: the served experts only

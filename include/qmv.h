@@ -81,10 +81,14 @@ size_t qmv_gemv_workspace_bytes(int K, int S);
  *   ws      device scratch of at least qmv_gemv_workspace_bytes(K, S) bytes,
  *           256-byte aligned, not shared with a concurrent call
  *   gs must be 64; K a multiple of 64; 1 <= N, 1 <= S, K <= 65536.
- * When N is a multiple of 16, K/64 a multiple of 4 and wq and scales are
- * 16-byte aligned, the weights stream through tensor-map (TMA) copies with
- * the row tiles' work shared evenly over all SMs; other shapes use per-warp
- * cp.async rings. Both give the same results up to fp32 summation order.
+ * Up to 4 tokens whose activations fit 64 KB of fragments (S * K <= 16384)
+ * run as one launch: every thread block converts x itself and streams its
+ * 16-row tiles through per-warp cp.async rings, K split over the warps.
+ * Otherwise, when N is a multiple of 16, K/64 a multiple of 4 and wq and
+ * scales are 16-byte aligned, the weights stream through tensor-map (TMA)
+ * copies with the row tiles' work shared evenly over all SMs; other shapes
+ * use per-warp cp.async rings. All give the same results up to fp32
+ * summation order.
  * Errors: QMV_EINVAL (null pointer, gs != 64, N or S < 1), QMV_ESHAPE (K),
  *         QMV_EALIGN, QMV_EWORKSPACE, QMV_ECUDA. */
 int qmv_int4_gs(const uint8_t *wq, const float *scales, int N, int K, int gs, const float *x,
@@ -112,10 +116,11 @@ int qmv_int4_gs_bf16(const uint8_t *wq, const float *scales, int N, int K, int g
  *   s0 [N0][K/gs], s1 [N1][K/gs] fp32; x [S][K]; y0 [S][N0]; y1 [S][N1] fp32
  *   ws      device scratch of at least qmv_gemv_workspace_bytes(K, S) bytes
  *           (the same as one GEMV), 256-byte aligned
- * x is converted into fp16 hi/lo fragments once. When both matrices qualify
- * for the tensor-map path (see qmv_int4_gs), the row tiles of both are one
- * work sequence of a single launch; otherwise the two GEMVs run one after
- * the other (the status word then reports the second).
+ * x is converted into fp16 hi/lo fragments once. For up to 4 tokens with
+ * S * K <= 16384 (see qmv_int4_gs) the row tiles of both matrices are one
+ * work sequence of the single-launch kernel; otherwise, when both matrices
+ * qualify for the tensor-map path, of one tensor-map launch; otherwise the
+ * two GEMVs run one after the other (the status word then reports the second).
  * Errors: as qmv_int4_gs. */
 int qmv_int4_gs_pair(const uint8_t *wq0, const float *s0, int N0, const uint8_t *wq1,
                      const float *s1, int N1, int K, int gs, const float *x, float *y0, float *y1,

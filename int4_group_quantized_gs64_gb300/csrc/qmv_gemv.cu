@@ -126,6 +126,28 @@ struct DenseSplitTile {
     }
 };
 
+// The items of k_dense_ks_x: 16-row tiles of the first matrix, then (for a
+// pair sharing x) of the second; warp ks streams groups [ga, gb) of them.
+template <bool kInt8>
+struct PairSplitTile {
+    const uint8_t *w0, *w1;
+    const float *s0, *s1;
+    size_t rowBytes;
+    int N0, N1, items0, G, i0, ga;
+    __device__ __forceinline__ TileSrc operator()(int item, int) const {
+        const int gi = i0 + item;
+        const bool sec = gi >= items0;
+        const int N = sec ? N1 : N0;
+        int row0 = (sec ? gi - items0 : gi) * 16;
+        int nrows = N - row0;
+        if (nrows <= 0) { row0 = N - 1; nrows = 1; }
+        const uint8_t *w = sec ? w1 : w0;
+        const float *sc = sec ? s1 : s0;
+        return TileSrc{w + (size_t)row0 * rowBytes + (size_t)ga * Fmt<kInt8>::kGroupBytes,
+                       kInt8 ? nullptr : sc + (size_t)row0 * G + ga, rowBytes, nrows, G};
+    }
+};
+
 template <bool kInt8>
 __global__ void __launch_bounds__(32 * kDenseWarps)
     k_dense(const uint8_t *__restrict__ w, const float *__restrict__ scales, int N, int K,
@@ -235,6 +257,176 @@ __global__ void __launch_bounds__(32 * kKsWarps)
     cp_async_wait<0>();
 }
 
+// Activation rows x[s][K] (s < ntok) -> the unit table cells[s][g][16] and
+// factors fac[s][g] in shared memory, four threads per 64-group. Thread
+// quarter q of a group holds values 16q .. 16q+15, which are exactly the
+// values of the group's units (mh, q, part) (frag_ks: the quad's k's lie in
+// [16q, 16q + 16)), so each thread builds its four units from its own values;
+// the group's max |v| takes two shuffles between the four threads. Same
+// arithmetic as k_split.
+template <bool kInt8>
+__device__ void split_rows_smem(const float *__restrict__ x, int K, int ntok, uint4 *cells,
+                                float *fac) {
+    const int G = K / kGroup, nq = ntok * G * 4;
+    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    for (int base = 0; base < nq; base += blockDim.x) {  // uniform trip count: shuffles below
+        const int idx = base + threadIdx.x;
+        const bool valid = idx < nq;
+        const int s = valid ? idx / (G * 4) : 0, g = valid ? (idx >> 2) % G : 0, q = idx & 3;
+        const float *src = x + (size_t)s * K + g * kGroup + 16 * q;
+        float v[16];
+        if (valid && vec) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 t = reinterpret_cast<const float4 *>(src)[i];
+                v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = valid ? src[i] : 0.f;
+        }
+        float am = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(v[i]));
+        am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+        const int e = split_exponent(am);
+        const float mul = ldexpf(1.0f, e);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] *= mul;
+        if (valid) {
+            uint4 *dst = cells + ((size_t)s * G + g) * 16;
+#pragma unroll
+            for (int mh = 0; mh < 2; ++mh)
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    uint32_t r[4];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        int k0, k1, k2, k3;
+                        frag_ks<kInt8>(2 * mh + i, 0, k0, k1, k2, k3);  // local to the quad
+                        r[2 * i] = pack_half2(split_part(v[k0], part), split_part(v[k1], part));
+                        r[2 * i + 1] = pack_half2(split_part(v[k2], part), split_part(v[k3], part));
+                    }
+                    dst[(mh * 4 + q) * 2 + part] = make_uint4(r[0], r[1], r[2], r[3]);
+                }
+            if (q == 0) fac[s * G + g] = ldexpf(1.0f, -e);
+        }
+    }
+}
+
+// k_dense_ks for activations given as fp32 rows: every CTA converts x into
+// its shared-memory unit table itself (split_rows_smem) while its first
+// weight stages are in flight, so the GEMV is one launch. With a second
+// matrix (w2 != null: a pair sharing x) its row tiles follow the first's in
+// the same item sequence. CTA 0 clears zero[0 .. nzero) (the caller's status
+// word and counters).
+template <bool kInt8, int kBudget>
+__global__ void __launch_bounds__(32 * kKsWarps)
+    k_dense_ks_x(const uint8_t *__restrict__ w, const float *__restrict__ scales, int N, int K,
+                 const float *__restrict__ x, float *__restrict__ y, uint16_t *__restrict__ ybf,
+                 int ntok, int32_t *zero, int nzero, const uint8_t *__restrict__ w2,
+                 const float *__restrict__ scales2, int N2, float *__restrict__ y2) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float red[kKsWarps][16][4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
+    const int G = K / kGroup;
+    const int gq = (G + kKsWarps - 1) / kKsWarps;
+    const int ga = min(G, warp * gq), gb = min(G, ga + gq);
+    const int items0 = (N + 15) / 16;
+    const int nitems = items0 + (w2 ? (N2 + 15) / 16 : 0);
+    const int i0 = (int)((long long)blockIdx.x * nitems / gridDim.x);
+    const int i1 = (int)((long long)(blockIdx.x + 1) * nitems / gridDim.x);
+    const size_t rowBytes = kInt8 ? (size_t)K : (size_t)K / 2;
+
+    PairSplitTile<kInt8> tile{w, w2, scales, scales2, rowBytes, N, N2, items0, G, i0, ga};
+    WarpStream<kInt8, kKsStages, PairSplitTile<kInt8>> ws;
+    ws.init(smem + warp * kKsRing, tile, gb - ga, gb > ga ? i1 - i0 : 0, warp, lane);
+    ws.prologue();  // weights are call inputs: safe to read before the wait
+
+    pdl_wait();     // x may come from the previous kernel
+    pdl_trigger();
+    if (zero && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
+    uint4 *cells = reinterpret_cast<uint4 *>(smem + kKsWarps * kKsRing);
+    float *fac = reinterpret_cast<float *>(smem + kKsWarps * kKsRing + kBudget);
+    split_rows_smem<kInt8>(x, K, ntok, cells, fac);
+    __syncthreads();
+    int cslot = 0;
+    const int sb = min(gid >> 1, ntok - 1), sd = min(q, ntok - 1);
+    const uint4 *bp0 = cells + (sb * G + ga) * 16 + q * 2 + (gid & 1);
+    const float *fp0 = fac + sd * G + ga;
+
+    for (int it = 0; it < i1 - i0; ++it) {
+        float acc[1][2] = {{0.f, 0.f}};
+        if (gb > ga) run_staged<kInt8>(ws, cslot, bp0, fp0, acc);
+        red[warp][gid][q] = acc[0][0];
+        red[warp][gid + 8][q] = acc[0][1];
+        __syncthreads();
+        if (warp == 0 && q < ntok) {
+            const int gi = i0 + it;
+            const bool sec = gi >= items0;
+            const int Nm = sec ? N2 : N;
+            const int row0 = (sec ? gi - items0 : gi) * 16;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < kKsWarps; ++k) {
+                a0 += red[k][gid][q];
+                a1 += red[k][gid + 8][q];
+            }
+            const int rA = row0 + gid, rB = row0 + gid + 8;
+            if constexpr (kInt8) {
+                const float *rs = sec ? scales2 : scales;
+                if (rA < Nm) a0 *= rs[rA];
+                if (rB < Nm) a1 *= rs[rB];
+            }
+            float *yo = sec ? y2 : y;
+            uint16_t *ho = sec ? nullptr : ybf;
+            if (rA < Nm) store_y(yo, ho, (size_t)q * Nm + rA, a0);
+            if (rB < Nm) store_y(yo, ho, (size_t)q * Nm + rB, a1);
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+}
+
+// Whether a GEMV of S tokens of length K runs as the single-launch
+// k_dense_ks_x: up to 4 tokens whose units fit 64 KB of shared memory (the
+// 32 KB form keeps two thread blocks per SM).
+constexpr int kXBudgetSmall = 32 * 1024, kXBudgetLarge = 64 * 1024;
+inline bool dense_one_launch(int K, int S) {
+    return S <= 4 && (size_t)(K / kGroup) * S * 256 <= (size_t)kXBudgetLarge;
+}
+
+// The single-launch GEMV (k_dense_ks_x) of one matrix, or of a pair sharing x.
+template <bool kInt8, int kBudget>
+cudaError_t launch_ks_x_b(const uint8_t *w, const float *scales, int N, int K, const float *x,
+                          float *y, uint16_t *ybf, int S, int32_t *zero, int nzero,
+                          cudaStream_t st, const uint8_t *w2, const float *scales2, int N2,
+                          float *y2) {
+    const size_t smem_ks = (size_t)kKsWarps * kKsRing + kBudget + kBudget / 64;
+    cudaError_t e = set_smem(k_dense_ks_x<kInt8, kBudget>, smem_ks);
+    if (e != cudaSuccess) return e;
+    const int items = (N + 15) / 16 + (w2 ? (N2 + 15) / 16 : 0);
+    const int slots =
+        sm_count() * max_ctas_per_sm(k_dense_ks_x<kInt8, kBudget>, 32 * kKsWarps, smem_ks);
+    return launch(k_dense_ks_x<kInt8, kBudget>, dim3(items < slots ? items : slots),
+                  dim3(32 * kKsWarps), smem_ks, st, true, w, scales, N, K, x, y, ybf, S, zero,
+                  nzero, w2, scales2, N2, y2);
+}
+
+template <bool kInt8>
+cudaError_t launch_ks_x(const uint8_t *w, const float *scales, int N, int K, const float *x,
+                        float *y, uint16_t *ybf, int S, int32_t *zero, int nzero, cudaStream_t st,
+                        const uint8_t *w2 = nullptr, const float *scales2 = nullptr, int N2 = 0,
+                        float *y2 = nullptr) {
+    if ((size_t)(K / kGroup) * S * 256 <= (size_t)kXBudgetSmall)
+        return launch_ks_x_b<kInt8, kXBudgetSmall>(w, scales, N, K, x, y, ybf, S, zero, nzero, st,
+                                                   w2, scales2, N2, y2);
+    return launch_ks_x_b<kInt8, kXBudgetLarge>(w, scales, N, K, x, y, ybf, S, zero, nzero, st, w2,
+                                               scales2, N2, y2);
+}
+
 template <bool kInt8>
 cudaError_t launch_dense(const uint8_t *w, const float *scales, int N, int K, const float *x,
                          float *y, int S, void *xcells, float *xfac, cudaStream_t st,
@@ -245,22 +437,10 @@ cudaError_t launch_dense(const uint8_t *w, const float *scales, int N, int K, co
     const int nitems = (N + 16 * kDenseWarps - 1) / (16 * kDenseWarps);
     const int slots = sm_count() * max_ctas_per_sm(k_dense<kInt8>, 32 * kDenseWarps, smem);
     const int grid = nitems < slots ? nitems : slots;
+    if (dense_one_launch(K, S))  // one launch: every CTA splits x itself
+        return launch_ks_x<kInt8>(w, scales, N, K, x, y, ybf, S, zero, nzero, st);
     e = launch(k_split<kInt8>, dim3(S, (K / kGroup + 7) / 8), dim3(256), 0, st, false, x, K,
                static_cast<uint4 *>(xcells), xfac, zero, nzero);
-    const int G = K / kGroup;
-    if (S <= 4 && (size_t)G * S * 256 <= (size_t)kDenseBudget) {
-        // one pass, K split over the warps of a CTA
-        const size_t smem_ks = (size_t)kKsWarps * kKsRing + kDenseBudget + kDenseBudget / 64;
-        e = (e == cudaSuccess) ? set_smem(k_dense_ks<kInt8>, smem_ks) : e;
-        const int items = (N + 15) / 16;
-        const int slots_ks =
-            sm_count() * max_ctas_per_sm(k_dense_ks<kInt8>, 32 * kKsWarps, smem_ks);
-        if (e == cudaSuccess)
-            e = launch(k_dense_ks<kInt8>, dim3(items < slots_ks ? items : slots_ks),
-                       dim3(32 * kKsWarps), smem_ks, st, true, w, scales, N, K,
-                       static_cast<const uint4 *>(xcells), (const float *)xfac, y, ybf, S);
-        return e;
-    }
     for (int s0 = 0; s0 < S && e == cudaSuccess; s0 += kMaxTok) {
         const int ntok = S - s0 < kMaxTok ? S - s0 : kMaxTok;
         e = launch(k_dense<kInt8>, dim3(grid), dim3(32 * kDenseWarps), smem, st, true, w, scales, N,
@@ -323,7 +503,11 @@ cudaError_t launch_gemv_int4(const uint8_t *wq, const float *scales, int N, int 
     int32_t *head = reinterpret_cast<int32_t *>(b);
     void *cells = b + kGemvHead;
     float *fac = reinterpret_cast<float *>(b + kGemvHead + (size_t)S * K * 4);
-    if (!tma_dense_supported(wq, scales, N, K, S))
+    // one or a few tokens with x fitting shared memory: the single-launch
+    // cp.async kernel (no activation split ahead of it) is faster than the
+    // tensor-map kernel, whose split, pipeline fill and stream-K fix-up cost
+    // more than a few stages of streaming
+    if (!tma_dense_supported(wq, scales, N, K, S) || dense_one_launch(K, S))
         return launch_dense<false>(wq, scales, N, K, x, y, S, cells, fac, st, head,
                                    1 + kSkMaxCtas, ybf);
     float *part = reinterpret_cast<float *>(b + gemv_part_offset(K, S));
@@ -337,6 +521,9 @@ cudaError_t launch_gemv_int4(const uint8_t *wq, const float *scales, int N, int 
 cudaError_t launch_gemv_int4_pair(const uint8_t *wq0, const float *s0, int N0, const uint8_t *wq1,
                                   const float *s1, int N1, int K, const float *x, float *y0,
                                   float *y1, int S, void *ws, cudaStream_t st) {
+    if (dense_one_launch(K, S))  // both matrices' row tiles in one single-launch GEMV
+        return launch_ks_x<false>(wq0, s0, N0, K, x, y0, nullptr, S,
+                                  static_cast<int32_t *>(ws), 1 + kSkMaxCtas, st, wq1, s1, N1, y1);
     if (!tma_dense_supported(wq0, s0, N0, K, S) || !tma_dense_supported(wq1, s1, N1, K, S)) {
         cudaError_t e = launch_gemv_int4(wq0, s0, N0, K, x, y0, S, ws, st);
         return e == cudaSuccess ? launch_gemv_int4(wq1, s1, N1, K, x, y1, S, ws, st) : e;

@@ -49,8 +49,11 @@ def test_int8_workload():
     assert norm_err(y, ref, den) <= TOL_FP32
 
 
+# (the single-launch kernel takes S <= 4 with S * K <= 16384: both its 32 KB
+# and 64 KB activation tables appear below, and larger S * K take the others)
 SHAPES = [(1, 64, 1), (17, 64, 3), (100, 192, 5), (63, 1088, 4), (65, 4096, 8), (33, 640, 16),
-          (40, 256, 17), (16, 16384, 2), (128, 2048, 33)]
+          (40, 256, 17), (16, 16384, 2), (128, 2048, 33), (1000, 4096, 4), (2048, 4096, 3),
+          (48, 16384, 1)]
 
 
 @pytest.mark.parametrize("N,K,S", SHAPES)
@@ -288,7 +291,7 @@ def test_int4_bf16_output(N, K, S):
     check_bf16(ybf, y32.cpu().numpy(), ref, den)
 
 
-@pytest.mark.parametrize("N,K,S", [(14336, 4096, 1), (100, 192, 5), (33, 640, 16)])
+@pytest.mark.parametrize("N,K,S", [(14336, 4096, 1), (100, 192, 5), (33, 640, 16), (300, 4096, 4)])
 def test_int8_bf16_output(N, K, S):
     w, r, x = datagen.dense_int8(N, K, S, seed=N + K + S)
     ws = torch.empty(q.qmv_gemv_workspace_bytes(K, S), dtype=torch.uint8, device="cuda")
