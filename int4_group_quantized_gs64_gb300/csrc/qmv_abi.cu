@@ -405,15 +405,11 @@ int moe_route_expert_ffn_int4(const qmv_moe_int4 *m, const float *logits, const 
         if ((r = ffn_check(m, T, k, ws, ws_bytes, L))) return r;
         if (!x || !out) return QMV_EINVAL;
         if (!aligned(x, 4) || !aligned(out, 4)) return QMV_EALIGN;
-        // one token: routing inside the single cooperative launch
-        const cudaStream_t st = cs(stream);
-        cudaError_t e = cudaMemsetAsync(at<int32_t>(ws, L.status), 0, L.status_bytes, st);
-        if (e == cudaSuccess)
-            e = qmv::launch_moe_one(dims(m), x, nullptr, nullptr, k, at<float>(ws, L.h), out,
-                                    at<int32_t>(ws, L.status),
-                                    reinterpret_cast<unsigned int *>(at<int32_t>(ws, L.sk_cnt)), st,
-                                    nullptr, nullptr, logits, ids, w);
-        return from_cuda(e);
+        // one token: routing inside the single cooperative launch, which
+        // clears the status word itself
+        return from_cuda(qmv::launch_moe_one(dims(m), x, nullptr, nullptr, k, at<float>(ws, L.h),
+                                             out, at<int32_t>(ws, L.status), cs(stream), nullptr,
+                                             nullptr, logits, ids, w));
     }
     if (T <= 32 && packed_units(m, T, k)) {
         // a decode micro-batch: the grouping kernel routes the tokens itself
@@ -456,15 +452,9 @@ int ffn_impl(const qmv_moe_int4 *m, const uint32_t *res, const float *x, int T,
     if (!aligned(x, 4) || !aligned(ids, 4) || !aligned(w, 4) || !aligned(out, 4)) return QMV_EALIGN;
     const cudaStream_t st = cs(stream);
     if (T == 1 && one_token(m, k)) {
-        // one token: a single cooperative launch after clearing the status
-        // word and the counters (the first counter is its grid barrier)
-        cudaError_t e = cudaMemsetAsync(at<int32_t>(ws, L.status), 0, L.status_bytes, st);
-        if (e == cudaSuccess)
-            e = qmv::launch_moe_one(dims(m), x, ids, w, k, at<float>(ws, L.h), out,
-                                    at<int32_t>(ws, L.status),
-                                    reinterpret_cast<unsigned int *>(at<int32_t>(ws, L.sk_cnt)), st,
-                                    res, served);
-        return from_cuda(e);
+        // one token: a single cooperative launch (it clears the status word)
+        return from_cuda(qmv::launch_moe_one(dims(m), x, ids, w, k, at<float>(ws, L.h), out,
+                                             at<int32_t>(ws, L.status), st, res, served));
     }
     if ((r = prepare_impl(m, x, T, ids, k, ws, ws_bytes, stream, res, served))) return r;
     if ((r = moe_ffn_gate_up(m, T, k, ws, ws_bytes, stream))) return r;

@@ -149,11 +149,11 @@ cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const 
                            cudaStream_t st, bool packed = false, const int4 *ptab = nullptr,
                            const int32_t *plan = nullptr);
 
-// Single-launch expert FFN of one token (cooperative grid, qmv_moe_one.cu).
-// bar: a zeroed word for the grid barrier.
+// Single-launch expert FFN of one token (cooperative grid, qmv_moe_one.cu);
+// it clears the status word itself.
 bool moe_one_supported(const MoeDims &m, int k);
 cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids, const float *w,
-                           int k, float *h, float *out, int32_t *status, unsigned int *bar,
+                           int k, float *h, float *out, int32_t *status,
                            cudaStream_t st, const uint32_t *res = nullptr,
                            uint8_t *served = nullptr, const float *logits = nullptr,
                            int32_t *ids_out = nullptr, float *w_out = nullptr);

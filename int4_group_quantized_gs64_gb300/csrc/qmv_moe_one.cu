@@ -28,7 +28,8 @@
 // the output does not depend on timing.
 //
 // Waits are bounded: a copy or barrier wait that runs out sets bit 1 of the
-// status word (the outputs are then not valid) and the kernel goes on. An
+// status word (the outputs are then not valid) and the kernel goes on. CTA 0
+// clears the status word at the start, so a call needs no memset first. An
 // expert id outside [0, E) sets bit 0 and contributes nothing; so does, with
 // no error, an expert outside the call's residency bitmap.
 #include <cuda.h>
@@ -64,8 +65,7 @@ struct OneArgs {
     const float *w;        // [k]
     float *h;              // [k][I] (workspace)
     float *out;            // [H]
-    int32_t *status;
-    unsigned int *bar;     // grid barrier count, zero at launch
+    int32_t *status;       // cleared by CTA 0 at the start
     const uint32_t *res;   // served experts' bitmap, or null for all
     uint8_t *served;       // [k]: 1 = pair computed (CTA 0 writes it), or null
     const float *logits;   // [E]: route in-kernel (ids / w then outputs), or null
@@ -99,35 +99,44 @@ __device__ __forceinline__ void expect_tx(uint64_t *mbar, uint32_t bytes) {
                  : "memory");
 }
 
-__device__ __forceinline__ unsigned ld_acquire(const unsigned int *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 // The compute warps only (the producer warp does not take part).
 __device__ __forceinline__ void compute_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kOWarps) : "memory");
 }
 
+// Grid barrier count of this kernel on this device: zero when the library
+// is loaded and never reset. Launches are cooperative, of one CTA per SM,
+// and a launch takes no ticket before every CTA of the launch before it
+// has taken its own (a CTA of the next launch starts only where one of this
+// launch has exited, after the barrier), so launch n holds tickets
+// [n * grid, (n + 1) * grid) and its CTAs wait for the count to reach
+// (n + 1) * grid. No clearing between calls: no memset node in the graph.
+__device__ unsigned long long g_one_bar;
+
+__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // All CTAs of the (cooperative) grid: every write before it is visible to
 // every read after it. Bounded; returns false if it gave up.
-__device__ __forceinline__ bool grid_barrier(unsigned int *bar) {
+__device__ __forceinline__ bool grid_barrier() {
     __shared__ int ok;
     __syncthreads();
     if (threadIdx.x == 0) {
         ok = 1;
-        __threadfence();
-        atomicAdd(bar, 1u);
+        unsigned long long t;  // release: this CTA's writes before the barrier
+        asm volatile("atom.add.release.gpu.u64 %0, [%1], 1;" : "=l"(t) : "l"(&g_one_bar) : "memory");
+        const unsigned long long target = (t / gridDim.x + 1) * gridDim.x;
         uint32_t i = 0;
-        while (ld_acquire(bar) < gridDim.x) {
+        while (ld_acquire64(&g_one_bar) < target) {
             if (++i == kOWait) {
                 ok = 0;
                 break;
             }
             __nanosleep(64);
         }
-        __threadfence();
     }
     __syncthreads();
     return ok != 0;
@@ -213,6 +222,9 @@ __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant_
     const int n1 = b < tiles1 ? (tiles1 - b + grid - 1) / grid : 0;
     const int n2 = b < tiles2 ? (tiles2 - b + grid - 1) / grid : 0;
 
+    // the call's status word: cleared here, before any bit of this call is set
+    // (bit 0 by CTA 0 below, bit 1 only after the grid barrier)
+    if (b == 0 && threadIdx.x == 0) *a.status = 0;
     if (a.logits && warp == 0) {
         // every CTA routes the token itself (the same top-k as moe_route_topk)
         int my_id;
@@ -324,7 +336,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant_
         }
     }
 
-    if (!grid_barrier(a.bar)) timed_out = true;
+    if (!grid_barrier()) timed_out = true;
 
     if (warp < kOWarps) {
         // ---- h -> activation units (each CTA its own copy), then down + combine
@@ -409,9 +421,9 @@ bool moe_one_supported(const MoeDims &m, int k) {
 }
 
 cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids, const float *w,
-                           int k, float *h, float *out, int32_t *status, unsigned int *bar,
-                           cudaStream_t st, const uint32_t *res, uint8_t *served,
-                           const float *logits, int32_t *ids_out, float *w_out) {
+                           int k, float *h, float *out, int32_t *status, cudaStream_t st,
+                           const uint32_t *res, uint8_t *served, const float *logits,
+                           int32_t *ids_out, float *w_out) {
     OneArgs a;
     memset(&a, 0, sizeof(a));
     size_t smem = 0;
@@ -419,7 +431,7 @@ cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids,
     if (!one_layout(m, k, grid, a, smem)) return cudaErrorInvalidValue;
     a.gu_q = m.gu_q; a.gu_s = m.gu_s; a.dn_q = m.dn_q; a.dn_s = m.dn_s;
     a.E = m.E; a.H = m.H; a.I = m.I; a.k = k;
-    a.x = x; a.ids = ids; a.w = w; a.h = h; a.out = out; a.status = status; a.bar = bar;
+    a.x = x; a.ids = ids; a.w = w; a.h = h; a.out = out; a.status = status;
     a.res = res; a.served = served;
     a.logits = logits; a.ids_out = ids_out; a.w_out = w_out;
     cudaError_t e = set_smem(k_moe_one, smem);
