@@ -130,6 +130,12 @@ bool tma_moe_supported(const MoeDims &m, long long P = 0);
 bool encode_weight_maps(CUtensorMap *wmap, CUtensorMap *smap, const uint8_t *wq, const float *ws,
                         int E, int rows, int K, int box_rows = 128);
 bool tma_dense_supported(const uint8_t *wq, const float *scales, int N, int K, int S);
+// A row-major byte matrix [rows][row_bytes] as a 3-D tensor map (128 bytes,
+// row, 128-byte chunk), boxes of box_rows whole rows with the 128-byte
+// swizzle (in shared memory: [chunk][row][128 B], 16-byte units XOR-ed with
+// the row mod 8). row_bytes a multiple of 128, at most 32768.
+bool encode_rows_swizzled(CUtensorMap *map, const uint8_t *base, long long rows, int row_bytes,
+                          int box_rows);
 // wq2 != null: a second matrix [N2][K/2] against the same activations, its
 // row tiles after the first's in the same launch, output y2 [S][N2].
 cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int K, int S,

@@ -55,6 +55,12 @@ constexpr int kOMaxK = 32;              // routed experts per token
 constexpr int kOSmemMax = 220 * 1024;   // dynamic shared memory budget
 
 struct OneArgs {
+    // the weight pools as 3-D tensor maps (128 bytes, row, 128-byte chunk of
+    // the row), boxes of 8 (gate+up) / 16 (down) whole rows, 128-byte
+    // swizzle: one copy per box, and a row's 16-byte chunks land XOR-ed with
+    // the row index, so a warp's 8-byte loads of 8 rows hit distinct banks
+    CUtensorMap map_gu;
+    CUtensorMap map_dn;
     const uint8_t *gu_q;   // gate+up weights [E][2I][H/2]
     const float *gu_s;     // their scales [E][2I][H/64]
     const uint8_t *dn_q;   // down weights [E][H][I/2]
@@ -73,7 +79,7 @@ struct OneArgs {
     float *w_out;          // their weights [k]
     // shared-memory layout (byte offsets from the aligned base)
     int n1, n2;            // gate+up tiles, down row tiles per CTA (at most)
-    int o_xu, o_xf, o_w1, o_w2, o_hu, o_hf, o_red, o_scr, o_lg;
+    int o_xu, o_xf, o_w1, o_s1, o_w2, o_s2, o_hu, o_hf, o_red, o_scr, o_lg;
 };
 
 struct OneShared {
@@ -90,6 +96,22 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
             "r"(dst),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc05::smem_addr(mbar))
         : "memory");
+}
+
+__device__ __forceinline__ void tma_g2s3(uint32_t dst, const CUtensorMap *map, int c1,
+                                         uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(c1), "r"(0), "r"(tc05::smem_addr(mbar))
+        : "memory");
+}
+
+// Byte o of row r of a box of R rows loaded through a swizzled map (R a
+// multiple of 8, box base 1024-byte aligned): the box is [chunk][row][128 B]
+// with the 16-byte units of each 128-byte line XOR-ed with the row mod 8.
+__device__ __forceinline__ const uint8_t *swz(const uint8_t *box, int R, int r, int o) {
+    return box + (((o >> 7) * R + r) << 7) + ((((o >> 4) & 7) ^ (r & 7)) << 4) + (o & 15);
 }
 
 __device__ __forceinline__ void expect_tx(uint64_t *mbar, uint32_t bytes) {
@@ -183,17 +205,18 @@ __device__ __forceinline__ void split_groups(const float *src, int n, uint4 *uni
 }
 
 // Lane (gid, q) of a warp: MMA over one 64-group of a 16-row tile in shared
-// memory (rows gid and gid + 8 at `rows` + row * rb, the group at byte 32 g)
-// against that group's activation units bu (one token: every B column is
-// token 0). Adds scale * factor * (hi + lo) of rows gid / gid + 8 to c0 / c8
-// (meaningful in lanes q == 0).
-__device__ __forceinline__ void tile_group_one(const uint8_t *rows, int rb, int g,
-                                               const uint4 (&bu)[1][2], float f, float s0,
-                                               float s8, float &c0, float &c8) {
-    const int lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
-    const uint8_t *r0 = rows + gid * rb + g * 32 + 8 * q;
-    const uint2 w0 = *reinterpret_cast<const uint2 *>(r0);
-    const uint2 w8 = *reinterpret_cast<const uint2 *>(r0 + 8 * rb);
+// memory (row gid: row r0 of box b0 with R0 rows; row gid + 8: row r8 of box
+// b8 with R8 rows; the group at byte 32 g of a row) against that group's
+// activation units bu (one token: every B column is token 0). Adds
+// scale * factor * (hi + lo) of rows gid / gid + 8 to c0 / c8 (meaningful in
+// lanes q == 0).
+__device__ __forceinline__ void tile_group_one(const uint8_t *b0, int R0, int r0, const uint8_t *b8,
+                                               int R8, int r8, int g, const uint4 (&bu)[1][2],
+                                               float f, float s0, float s8, float &c0, float &c8) {
+    const int lane = threadIdx.x & 31, q = lane & 3;
+    const int o = g * 32 + 8 * q;
+    const uint2 w0 = *reinterpret_cast<const uint2 *>(swz(b0, R0, r0, o));
+    const uint2 w8 = *reinterpret_cast<const uint2 *>(swz(b8, R8, r8, o));
     float d[1][4];
     tile_group_int4<1>(w0, w8, bu, d);
     c0 = fmaf(s0 * f, d[0][0] + d[0][1], c0);
@@ -209,16 +232,15 @@ __device__ __forceinline__ void load_units(const uint4 *u, uint4 (&bu)[1][2]) {
 __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant__ OneArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ OneShared sh;
-    uint8_t *base = smem_raw + ((128u - (tc05::smem_addr(smem_raw) & 127u)) & 127u);
+    uint8_t *base = smem_raw + ((1024u - (tc05::smem_addr(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
     const int H = a.H, I = a.I, k = a.k;
     const int GH = H / kGroup, GI = I / kGroup;
     const int tiles1 = k * (I / 8), tiles2 = H / 16;
     const int b = blockIdx.x, grid = gridDim.x;
     const int rb1 = H / 2, rb2 = I / 2;                        // row bytes
-    const uint32_t t1b = 16u * rb1 + 16u * GH * 4;            // gate+up tile: rows, scales
-    const uint32_t e2b = 16u * rb2 + 16u * GI * 4;            // down rows of one expert
-    const uint32_t t2b = (uint32_t)k * e2b;                   // down row tile
+    const uint32_t t1w = 16u * rb1, t1s = 16u * GH * 4;       // gate+up tile: rows, scales
+    const uint32_t e2w = 16u * rb2, e2s = 16u * GI * 4;       // down rows of one expert
     const int n1 = b < tiles1 ? (tiles1 - b + grid - 1) / grid : 0;
     const int n2 = b < tiles2 ? (tiles2 - b + grid - 1) / grid : 0;
 
@@ -268,17 +290,17 @@ __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant_
         if (lane == 0) {
             uint32_t bytes2 = 0;
             for (int p = 0; p < k; ++p)
-                if (sh.ids[p] >= 0) bytes2 += (uint32_t)n2 * e2b;
+                if (sh.ids[p] >= 0) bytes2 += (uint32_t)n2 * (e2w + e2s);
             expect_tx(&sh.mb2, bytes2);
             for (int i = 0; i < n1; ++i) {
                 const int t = b + i * grid, p = t / (I / 8), u0 = 8 * (t % (I / 8)), e = sh.ids[p];
-                expect_tx(&sh.mb1[i], e >= 0 ? t1b : 0u);
+                expect_tx(&sh.mb1[i], e >= 0 ? t1w + t1s : 0u);
                 if (e < 0) continue;
-                const uint32_t dw = tc05::smem_addr(base + a.o_w1 + i * t1b);
-                const uint32_t ds = dw + 16u * rb1;
+                const uint32_t dw = tc05::smem_addr(base + a.o_w1 + i * t1w);
+                const uint32_t ds = tc05::smem_addr(base + a.o_s1 + i * t1s);
                 const size_t rg = (size_t)e * 2 * I + u0, ru = rg + I;   // gate / up rows
-                bulk_g2s(dw, a.gu_q + rg * (H / 2), 8u * rb1, &sh.mb1[i]);
-                bulk_g2s(dw + 8u * rb1, a.gu_q + ru * (H / 2), 8u * rb1, &sh.mb1[i]);
+                tma_g2s3(dw, &a.map_gu, (int)rg, &sh.mb1[i]);
+                tma_g2s3(dw + 8u * rb1, &a.map_gu, (int)ru, &sh.mb1[i]);
                 bulk_g2s(ds, a.gu_s + rg * GH, 8u * GH * 4, &sh.mb1[i]);
                 bulk_g2s(ds + 8u * GH * 4, a.gu_s + ru * GH, 8u * GH * 4, &sh.mb1[i]);
             }
@@ -286,11 +308,12 @@ __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant_
                 for (int p = 0; p < k; ++p) {
                     const int e = sh.ids[p];
                     if (e < 0) continue;
-                    const uint32_t dw =
-                        tc05::smem_addr(base + a.o_w2 + i * t2b) + (uint32_t)p * e2b;
+                    const int slot = i * k + p;
                     const size_t r0 = (size_t)e * H + 16 * (b + i * grid);
-                    bulk_g2s(dw, a.dn_q + r0 * (I / 2), 16u * rb2, &sh.mb2);
-                    bulk_g2s(dw + 16u * rb2, a.dn_s + r0 * GI, 16u * GI * 4, &sh.mb2);
+                    tma_g2s3(tc05::smem_addr(base + a.o_w2 + slot * e2w), &a.map_dn, (int)r0,
+                             &sh.mb2);
+                    bulk_g2s(tc05::smem_addr(base + a.o_s2 + slot * e2s), a.dn_s + r0 * GI,
+                             16u * GI * 4, &sh.mb2);
                 }
         }
         __syncwarp();
@@ -308,14 +331,14 @@ __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant_
         // added in warp order
         for (int i = 0; i < n1; ++i) {
             if (!tc05::mbar_wait(&sh.mb1[i], 0, kOWait)) timed_out = true;
-            const uint8_t *rows = base + a.o_w1 + i * t1b;
-            const float *sc = reinterpret_cast<const float *>(rows + 16 * rb1);
+            const uint8_t *rows = base + a.o_w1 + i * t1w;   // gate box, then up box
+            const float *sc = reinterpret_cast<const float *>(base + a.o_s1 + i * t1s);
             float c0 = 0.f, c8 = 0.f;
             for (int g = warp; g < GH; g += kOWarps) {
                 uint4 bu[1][2];
                 load_units(xu + g * 16, bu);
-                tile_group_one(rows, rb1, g, bu, xf[g], sc[gid * GH + g], sc[(gid + 8) * GH + g],
-                               c0, c8);
+                tile_group_one(rows, 8, gid, rows + 8 * rb1, 8, gid, g, bu, xf[g],
+                               sc[gid * GH + g], sc[(gid + 8) * GH + g], c0, c8);
             }
             if (q == 0) {
                 red[(i * kOWarps + warp) * 16 + gid] = c0;
@@ -353,13 +376,14 @@ __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant_
             for (int p = warp; p < k; p += kOWarps) {
                 float c0 = 0.f, c8 = 0.f;
                 if (sh.ids[p] >= 0) {
-                    const uint8_t *rows = base + a.o_w2 + i * t2b + p * e2b;
-                    const float *sc = reinterpret_cast<const float *>(rows + 16 * rb2);
+                    const uint8_t *rows = base + a.o_w2 + (i * k + p) * e2w;  // one 16-row box
+                    const float *sc =
+                        reinterpret_cast<const float *>(base + a.o_s2 + (i * k + p) * e2s);
                     for (int g = 0; g < GI; ++g) {
                         uint4 bu[1][2];
                         load_units(hu + (p * GI + g) * 16, bu);
-                        tile_group_one(rows, rb2, g, bu, hf[p * GI + g], sc[gid * GI + g],
-                                       sc[(gid + 8) * GI + g], c0, c8);
+                        tile_group_one(rows, 16, gid, rows, 16, gid + 8, g, bu, hf[p * GI + g],
+                                       sc[gid * GI + g], sc[(gid + 8) * GI + g], c0, c8);
                     }
                 }
                 if (q == 0) {
@@ -387,6 +411,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant_
 }
 
 inline size_t up16(size_t v) { return (v + 15) & ~(size_t)15; }
+inline size_t up1k(size_t v) { return (v + 1023) & ~(size_t)1023; }
 
 // Shared-memory layout for (H, I, k) on a grid of `grid` CTAs; false if it
 // does not fit.
@@ -395,26 +420,30 @@ bool one_layout(const MoeDims &m, int k, int grid, OneArgs &a, size_t &smem) {
     const int tiles1 = k * (m.I / 8), tiles2 = m.H / 16;
     a.n1 = (tiles1 + grid - 1) / grid;
     a.n2 = (tiles2 + grid - 1) / grid;
-    const size_t t1b = 16 * (size_t)(m.H / 2) + 16 * (size_t)GH * 4;
-    const size_t t2b = (size_t)k * (16 * (size_t)(m.I / 2) + 16 * (size_t)GI * 4);
+    // weight boxes at 1024-byte aligned offsets (the 128-byte swizzle's atom)
+    const size_t t1w = 16 * (size_t)(m.H / 2), t1s = 16 * (size_t)GH * 4;
+    const size_t e2w = 16 * (size_t)(m.I / 2), e2s = 16 * (size_t)GI * 4;
     size_t o = 0;
+    a.o_w1 = (int)o; o = up1k(o + (size_t)a.n1 * t1w);
+    a.o_w2 = (int)o; o = up1k(o + (size_t)a.n2 * k * e2w);
+    a.o_s1 = (int)o; o = up16(o + (size_t)a.n1 * t1s);
+    a.o_s2 = (int)o; o = up16(o + (size_t)a.n2 * k * e2s);
     a.o_xu = (int)o; o = up16(o + (size_t)GH * 256);
     a.o_xf = (int)o; o = up16(o + (size_t)GH * 4);
-    a.o_w1 = (int)o; o = up16(o + (size_t)a.n1 * t1b);
-    a.o_w2 = (int)o; o = up16(o + (size_t)a.n2 * t2b);
     a.o_hu = (int)o; o = up16(o + (size_t)k * GI * 256);
     a.o_hf = (int)o; o = up16(o + (size_t)k * GI * 4);
     a.o_red = (int)o; o = up16(o + (size_t)std::max(a.n1 * kOWarps * 16, kOMaxK * 16) * 4);
     a.o_scr = (int)o; o = up16(o + (size_t)kOWarps * 8 * 64 * 4);
     a.o_lg = (int)o; o = up16(o + (size_t)1024 * 4);  // one routing row (E <= 1024)
-    smem = o + 128;
+    smem = o + 1024;
     return smem <= (size_t)kOSmemMax && a.n1 <= kOMaxT1;
 }
 
 }  // namespace
 
 bool moe_one_supported(const MoeDims &m, int k) {
-    if (k < 1 || k > kOMaxK || m.H % 256 || m.I % 256) return false;
+    // whole rows per box: row bytes (H / 2, I / 2) a multiple of 128, at most 32 KB
+    if (k < 1 || k > kOMaxK || m.H % 256 || m.I % 256 || m.H > 65536 || m.I > 65536) return false;
     OneArgs a;
     size_t smem = 0;
     return one_layout(m, k, sm_count(), a, smem);
@@ -434,6 +463,9 @@ cudaError_t launch_moe_one(const MoeDims &m, const float *x, const int32_t *ids,
     a.x = x; a.ids = ids; a.w = w; a.h = h; a.out = out; a.status = status;
     a.res = res; a.served = served;
     a.logits = logits; a.ids_out = ids_out; a.w_out = w_out;
+    if (!encode_rows_swizzled(&a.map_gu, m.gu_q, (long long)m.E * 2 * m.I, m.H / 2, 8) ||
+        !encode_rows_swizzled(&a.map_dn, m.dn_q, (long long)m.E * m.H, m.I / 2, 16))
+        return cudaErrorInvalidValue;
     cudaError_t e = set_smem(k_moe_one, smem);
     if (e != cudaSuccess) return e;
     if (max_ctas_per_sm(k_moe_one, kOThreads, smem) < 1) return cudaErrorInvalidConfiguration;

@@ -702,6 +702,19 @@ bool encode_weight_maps(CUtensorMap *wmap, CUtensorMap *smap, const uint8_t *wq,
     return true;
 }
 
+bool encode_rows_swizzled(CUtensorMap *map, const uint8_t *base, long long rows, int row_bytes,
+                          int box_rows) {
+    auto enc = encode_fn();
+    if (!enc || row_bytes % 128 || row_bytes / 128 > 256 || box_rows > 256) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)(row_bytes / 128)};
+    cuuint64_t strides[2] = {(cuuint64_t)row_bytes, 128};
+    cuuint32_t box[3] = {128, (cuuint32_t)box_rows, (cuuint32_t)(row_bytes / 128)};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(base), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tma_moe_supported(const MoeDims &m, long long P) {
     // tensor maps need 16-byte aligned bases and 16-byte strides (scale rows of
     // K/64 floats: K/64 a multiple of 4)
