@@ -204,6 +204,55 @@ __device__ __forceinline__ void split_groups(const float *src, int n, uint4 *uni
     }
 }
 
+// Rows src[p][n * 64] (p < rows_n, read through L2: other CTAs wrote them)
+// -> units[p][g][16] and factors fac[p][g] in shared memory, by the nt
+// threads t < nt, four threads per 64-group. Thread quarter q of a group
+// holds values 16q .. 16q+15, exactly the values of the group's units
+// (mh, q, part), so each thread builds its four units from its own values;
+// the group's max |v| takes two shuffles. Same arithmetic as split_groups.
+__device__ __forceinline__ void split_rows_quad(const float *src, int rows_n, int n, uint4 *units,
+                                                float *fac, int t, int nt) {
+    const int nq = rows_n * n * 4;
+    for (int base = 0; base < nq; base += nt) {  // uniform trip count: shuffles below
+        const int idx = base + t;
+        const bool valid = idx < nq;
+        const int c = valid ? idx >> 2 : 0, q = idx & 3;  // c = p * n + g
+        float v[16];
+        const float4 *s4 = reinterpret_cast<const float4 *>(src + (size_t)c * kGroup + 16 * q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 f = valid ? __ldcg(s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+        }
+        float am = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(v[i]));
+        am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+        const int e = split_exponent(am);  // |e| <= 126: 2^e is a normal float
+        const float mul = __int_as_float((127 + e) << 23);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] *= mul;
+        if (valid) {
+#pragma unroll
+            for (int mh = 0; mh < 2; ++mh)
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    uint32_t r[4];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        int k0, k1, k2, k3;
+                        frag_ks<false>(2 * mh + i, 0, k0, k1, k2, k3);  // local to the quad
+                        r[2 * i] = pack_half2(split_part(v[k0], part), split_part(v[k1], part));
+                        r[2 * i + 1] = pack_half2(split_part(v[k2], part), split_part(v[k3], part));
+                    }
+                    units[c * 16 + (mh * 4 + q) * 2 + part] = make_uint4(r[0], r[1], r[2], r[3]);
+                }
+            if (q == 0) fac[c] = __int_as_float((127 - e) << 23);
+        }
+    }
+}
+
 // Lane (gid, q) of a warp: MMA over one 64-group of a 16-row tile in shared
 // memory (row gid: row r0 of box b0 with R0 rows; row gid + 8: row r8 of box
 // b8 with R8 rows; the group at byte 32 g of a row) against that group's
@@ -366,11 +415,9 @@ __global__ void __launch_bounds__(kOThreads, 1) k_moe_one(const __grid_constant_
         uint4 *hu = reinterpret_cast<uint4 *>(base + a.o_hu);
         float *hf = reinterpret_cast<float *>(base + a.o_hf);
         float *red = reinterpret_cast<float *>(base + a.o_red);
-        float *scratch = reinterpret_cast<float *>(base + a.o_scr) + warp * 8 * 64;
-        // warp w splits the h rows of the experts it computes (p = w, w + 8,
-        // ...), so it needs no other warp's units
-        for (int p = warp; p < k; p += kOWarps)
-            split_groups(a.h + (size_t)p * I, GI, hu + p * GI * 16, hf + p * GI, scratch, 0, 1);
+        // all compute threads split h (k rows of I), four threads a group
+        split_rows_quad(a.h, k, GI, hu, hf, threadIdx.x, 32 * kOWarps);
+        compute_sync();
         if (!tc05::mbar_wait(&sh.mb2, 0, kOWait)) timed_out = true;
         for (int i = 0; i < n2; ++i) {
             for (int p = warp; p < k; p += kOWarps) {
