@@ -177,8 +177,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded datagen)",
-        "config": {"workload": "MoE decode H6144 E160 I2048 top8, 8 tokens, 16 hot experts",
-                   "global_batch": wl["T"], "parallelism": "none (host oracle)"},
+        "config": bench_config(1, wl["T"]),
+        "timing": "host wall clock of the fp64 oracle on the host cores (no GPU)",
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": per[0]["cores"],
                          "kind": "oracle", "sample": per[0]["sample"]},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -210,6 +210,36 @@ def time_graphs(graphs, iters, stream):
         e.record(stream)
     e.synchronize()
     return s.elapsed_time(e) * 1e-3 / iters
+
+
+def time_graphs_steps(graphs, iters, stream):
+    """Like time_graphs, with an event after every replay: (mean seconds per
+    replay over the whole region, per-replay seconds)."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(iters):
+            graphs[i % len(graphs)].replay()
+            ev[i + 1].record(stream)
+    ev[-1].synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) * 1e-3 for i in range(iters)]
+    return ev[0].elapsed_time(ev[-1]) * 1e-3 / iters, per
+
+
+def spread(xs, scale=1.0):
+    """min / p10 / median / p90 / max of a list, times scale."""
+    v = sorted(x * scale for x in xs)
+    pick = lambda f: v[min(len(v) - 1, int(round(f * (len(v) - 1))))]  # noqa: E731
+    return {"min": v[0], "p10": pick(0.1), "median": pick(0.5), "p90": pick(0.9), "max": v[-1]}
+
+
+def bench_config(ws_n: int, T: int) -> dict:
+    """The workload, as both arms print it."""
+    return {"workload": "MoE decode H6144 E160 I2048 top8, 8 tokens, 16 hot experts",
+            "global_batch": T * ws_n, "seq_len": 1, "parallelism": f"replicas x{ws_n}",
+            "l2": "inputs larger than L2 (~0.6 GB of expert weights per step vs 129 MB L2); "
+                  "8 rotating seeded micro-batches"}
 
 
 def load_traffic(kernel: str):
@@ -277,7 +307,7 @@ def run_profile_dense(args):
         q.qmv_int4_gs(ws_[i % 4], ss_[i % 4], xd, y=y, ws=ws)
     torch.cuda.synchronize()
     print(json.dumps({"profile_case": f"int4-gs64 GEMV {N}x{K}, 1 token, 4 weight copies",
-                      "launches": args.steps * 4, "kernels_per_launch": 2}))
+                      "launches": args.steps * 4, "kernels_per_launch": 1}))
     return 0
 
 
@@ -423,40 +453,54 @@ def run_ours(args):
     if ws_n > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    t_step = time_graphs(graphs, args.steps, stream)
+    t_step, step_times = time_graphs_steps(graphs, args.steps, stream)
     torch.cuda.synchronize()
     if ws_n > 1:
         t_step = max_over_ranks(t_step, dev)
         dist.barrier()
     clk = clocks.stop()
 
-    # ---- dominant kernel (gate+up) alone, CUDA events on the launching stream
-    ws0 = wss[0]
-    with torch.cuda.stream(stream):
-        q.moe_route_topk(ls[0], k, ids=ids[0], w=wv[0], stream=stream)
-        q.moe_ffn_prepare(m, xs[0], ids[0], ws0, stream=stream)
-    kt = []
-    for r in range(20):
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---- the two FFN kernels alone (gate+up, the dominant one, and down), CUDA
+    # events on the launching stream, over the 8 rotating micro-batches
+    for i in range(ROTATE):
         with torch.cuda.stream(stream):
-            ev0.record(stream)
-            q.moe_ffn_gate_up(m, T, k, ws0, stream=stream)
-            ev1.record(stream)
-            q.moe_ffn_down(m, T, k, ws0, stream=stream)  # keeps L2 honest between repeats
-        ev1.synchronize()
-        if r >= 3:
-            kt.append(ev0.elapsed_time(ev1) * 1e-3)
-    t_gu = statistics.mean(kt)
-    gu_bytes = batches[0]["U"] * (2 * wl["I"] * wl["H"] // 2 + 2 * wl["I"] * wl["H"] // 64 * 4) \
-        + T * wl["H"] * 4 + T * k * wl["I"] * 4
+            q.moe_route_topk(ls[i], k, ids=ids[i], w=wv[i], stream=stream)
+            q.moe_ffn_prepare(m, xs[i], ids[i], wss[i], stream=stream)
+    gu_t, dn_t, gu_b, dn_b = [], [], [], []
+    E_gu = 2 * wl["I"] * wl["H"] // 2 + 2 * wl["I"] * wl["H"] // 64 * 4
+    E_dn = wl["H"] * wl["I"] // 2 + wl["H"] * wl["I"] // 64 * 4
+    for rep in range(4):
+        for i in range(ROTATE):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            with torch.cuda.stream(stream):
+                ev[0].record(stream)
+                q.moe_ffn_gate_up(m, T, k, wss[i], stream=stream)
+                ev[1].record(stream)
+                q.moe_ffn_down(m, T, k, wss[i], stream=stream)
+                ev[2].record(stream)
+            ev[2].synchronize()
+            if rep >= 1:
+                gu_t.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+                dn_t.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+                U = batches[i]["U"]
+                gu_b.append(U * E_gu + T * wl["H"] * 4 + T * k * wl["I"] * 4)
+                dn_b.append(U * E_dn + T * k * wl["I"] * 4 + T * k * wl["H"] * 4)
     peak, peak_kind = peaks()
     gu_kernel = "k_moe_tma" if q.moe_weight_path(m) == 1 else "k_gate_up"
-    roofline = {"bound": "hbm", "kernel": gu_kernel, "achieved": gu_bytes / t_gu / 1e9,
-                "peak": peak, "unit": "GB/s", "frac": gu_bytes / t_gu / 1e9 / peak,
+    gu_ach = sum(gu_b) / sum(gu_t) / 1e9
+    dn_ach = sum(dn_b) / sum(dn_t) / 1e9
+    roofline = {"bound": "hbm", "kernel": gu_kernel, "achieved": gu_ach,
+                "peak": peak, "unit": "GB/s", "frac": gu_ach / peak,
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
                 "traffic": load_traffic(gu_kernel + " gate+up"),
-                "bytes_per_launch": gu_bytes, "us_per_launch": t_gu * 1e6}
+                "bytes_per_launch": statistics.mean(gu_b),
+                "us_per_launch": statistics.mean(gu_t) * 1e6,
+                "us_per_launch_spread": spread(gu_t, 1e6), "launches_timed": len(gu_t),
+                "down": {"kernel": gu_kernel, "achieved": dn_ach, "frac": dn_ach / peak,
+                         "bytes_per_launch": statistics.mean(dn_b),
+                         "us_per_launch": statistics.mean(dn_t) * 1e6,
+                         "us_per_launch_spread": spread(dn_t, 1e6)}}
 
     # ---- end to end through the public API with pinned host buffers
     hx = [torch.from_numpy(b["x"]).pin_memory() for b in batches]
@@ -523,12 +567,10 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp16x2-split MMA, fp32 accumulate",
         "data": "synthetic (seeded datagen, no trained weights)",
-        "config": {"workload": "MoE decode H6144 E160 I2048 top8, 8 tokens, 16 hot experts",
-                   "global_batch": T * ws_n, "seq_len": 1, "parallelism": f"replicas x{ws_n}",
-                   "experts_touched_mean": U_mean, "bytes_per_step_mean": B_mean,
-                   "l2": "inputs larger than L2 (~0.6 GB of weights per step vs 129 MB L2); "
-                         "8 rotating micro-batches",
-                   "timing": "CUDA graph replay of K steps between CUDA events"},
+        "config": bench_config(ws_n, T),
+        "experts_touched_mean": U_mean, "bytes_per_step_mean": B_mean,
+        "timing": "CUDA graph replay of K steps between CUDA events, an event after every step",
+        "ms_per_step_spread": spread(step_times, 1e3),
         "pct_of_8TBs": value / ws_n / NOMINAL_HBM_GBS * 100,
         "us_per_layer": t_step * 1e6, "us_per_decode_token_layer": t_step * 1e6 / T,
         "token_eq_per_s": ws_n * T / t_step,
