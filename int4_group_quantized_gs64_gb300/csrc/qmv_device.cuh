@@ -306,6 +306,42 @@ __device__ __forceinline__ void tile_group_int4s(uint2 w0, uint2 w8, const uint4
     }
 }
 
+// Two tiles of the same 16 rows' shape (A: w0, w8; B: v0, v8) against the
+// same activation fragments, in the tensor-map kernel's int4 form: the two
+// tiles' MMA chains interleave, and each B fragment serves both.
+template <int NB>
+__device__ __forceinline__ void tile2_group_int4s(uint2 w0, uint2 w8, uint2 v0, uint2 v8,
+                                                  const uint4 (&bu)[NB][2],
+                                                  const float (&cinit)[NB], float dA[NB][4],
+                                                  float dB[NB][4]) {
+    uint32_t p0[4], p8[4], q0[4], q8[4], a[4], b[4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        dA[nb][0] = dA[nb][2] = dB[nb][0] = dB[nb][2] = cinit[nb];
+        dA[nb][1] = dA[nb][3] = dB[nb][1] = dB[nb][3] = 0.0f;
+    }
+#pragma unroll
+    for (int mh = 0; mh < 2; ++mh) {
+        uint4 bv[NB];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) bv[nb] = bu[nb][mh];
+        dequant_int4_word_s(mh ? w0.y : w0.x, p0);
+        dequant_int4_word_s(mh ? w8.y : w8.x, p8);
+        dequant_int4_word_s(mh ? v0.y : v0.x, q0);
+        dequant_int4_word_s(mh ? v8.y : v8.x, q8);
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm) {
+            a[0] = p0[2 * mm]; a[1] = p8[2 * mm]; a[2] = p0[2 * mm + 1]; a[3] = p8[2 * mm + 1];
+            b[0] = q0[2 * mm]; b[1] = q8[2 * mm]; b[2] = q0[2 * mm + 1]; b[3] = q8[2 * mm + 1];
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                mma_16816(dA[nb], a, mm ? bv[nb].z : bv[nb].x, mm ? bv[nb].w : bv[nb].y);
+                mma_16816(dB[nb], b, mm ? bv[nb].z : bv[nb].x, mm ? bv[nb].w : bv[nb].y);
+            }
+        }
+    }
+}
+
 // int8: 16 bytes of row gid (w0) and of row gid+8 (w8); MMA step m uses word m.
 template <int NB>
 __device__ __forceinline__ void tile_group_int8(uint4 w0, uint4 w8, const uint4 (&bu)[NB][2],

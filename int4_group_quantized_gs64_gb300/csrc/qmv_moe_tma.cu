@@ -42,8 +42,11 @@ namespace qmv {
 
 namespace {
 
-constexpr int kTConsumers = 16;
+constexpr int kTConsumers = 8;                       // consumer warps, two 16-row tiles each
 constexpr int kTThreads = 32 * (kTConsumers + 1);
+// Registers: warps are spread round-robin over the 4 SM sub-partitions, so
+// one holds 3 of the 9 warps; 3 x 32 x 168 fits its 16,384 registers.
+constexpr int kTRegBound = 3 * 4 * 32;               // launch bound giving 168 registers
 constexpr int kTStages = 4;
 constexpr int kTRows = 256;                          // weight rows per stage
 constexpr int kTStageW = kTRows * 128;               // 32 KB of packed weights
@@ -57,7 +60,7 @@ constexpr int kTStage = (kTOffA + kMaxTok * kTActTok + 1023) / 1024 * 1024;  // 
 static_assert(kTOffA - kTOffF + kMaxTok * kTActTok == kPackedStage, "pass-packed block layout");
 constexpr int kTGuJ = 128;                           // hidden units per gate+up item
 constexpr int kTDnRows = 256;                        // output rows per down item
-constexpr int kTEpi = (2 * kTGuJ * kMaxTok + kTConsumers * 64) * 4;
+constexpr int kTEpi = (kTGuJ * kMaxTok + kTConsumers * 64) * 4;  // h of an item, split scratch
 constexpr int kTSmem = kTStages * kTStage + kTEpi + 1024;
 constexpr uint32_t kTWait = 1u << 24;
 
@@ -186,19 +189,28 @@ struct PassCursor {
 // half-warp are conflict-free.
 __device__ __forceinline__ int tile_row(int gid) { return 2 * (gid & 3) + (gid >> 2); }
 
-// Fragments of one group of this warp's 16-row tile (smem rows r0..r0+15).
+// Consumer warp w owns two 16-row tiles of a stage: A = stage rows
+// 16w..16w+15 and B = rows 128+16w..128+16w+15. For gate+up that is the gate
+// and the up rows of the same 16 hidden units (pairs of the fused SiLU live in
+// one warp); for down and dense, two independent row tiles. Both tiles take
+// the same activation fragments, loaded once.
+constexpr int kTRowB = 128;
+
+// Fragments of one group of this warp's two tiles.
 template <int NB>
 struct GroupFrag {
-    uint2 w0, w8;
+    uint2 a0, a8, b0, b8;
     uint4 bu[NB][2];
 };
 
 template <int NB, int GL>
-__device__ __forceinline__ void group_load(const uint8_t *wa, int pr, int q,
+__device__ __forceinline__ void group_load(const uint8_t *waA, const uint8_t *waB, int pr, int q,
                                            const uint4 *const bp0[NB], GroupFrag<NB> &g) {
     const int off = (((2 * GL + (q >> 1)) ^ pr) << 4) + ((q & 1) << 3);
-    g.w0 = *reinterpret_cast<const uint2 *>(wa + off);
-    g.w8 = *reinterpret_cast<const uint2 *>(wa + 1024 + off);
+    g.a0 = *reinterpret_cast<const uint2 *>(waA + off);
+    g.a8 = *reinterpret_cast<const uint2 *>(waA + 1024 + off);
+    g.b0 = *reinterpret_cast<const uint2 *>(waB + off);
+    g.b8 = *reinterpret_cast<const uint2 *>(waB + 1024 + off);
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
         g.bu[nb][0] = bp0[nb][GL * 16];
@@ -206,47 +218,52 @@ __device__ __forceinline__ void group_load(const uint8_t *wa, int pr, int q,
     }
 }
 
-// d = 2^-24 * sum (nibble - 8) * v over the group (tile_group_int4s); the
+// d = 2^-24 * sum (nibble - 8) * v over the group (tile2_group_int4s); the
 // exact 2^24 comes back before the group scale and the activation factor.
 // fp[nb]: the (factor, offset_init) records of the four groups of token
-// block nb, read per group (fewer live registers than all four at once).
+// block nb. c[tile][GL & 1][nb][row gid, gid + 8].
 template <int NB, int GL>
-__device__ __forceinline__ void group_math(const GroupFrag<NB> &g, float s0, float s8,
-                                           const float *const fp[NB], float c[2][NB][2]) {
-    float d[NB][4], ci[NB], f[NB];
+__device__ __forceinline__ void group_math(const GroupFrag<NB> &g, float sA0, float sA8, float sB0,
+                                           float sB8, const float *const fp[NB],
+                                           float c[2][2][NB][2]) {
+    float dA[NB][4], dB[NB][4], ci[NB], f[NB];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
         const float2 r = reinterpret_cast<const float2 *>(fp[nb])[GL];
         f[nb] = r.x;
         ci[nb] = r.y;
     }
-    tile_group_int4s<NB>(g.w0, g.w8, g.bu, ci, d);
+    tile2_group_int4s<NB>(g.a0, g.a8, g.b0, g.b8, g.bu, ci, dA, dB);
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-        c[GL & 1][nb][0] = fmaf(s0 * f[nb], (d[nb][0] + d[nb][1]) * 0x1p24f, c[GL & 1][nb][0]);
-        c[GL & 1][nb][1] = fmaf(s8 * f[nb], (d[nb][2] + d[nb][3]) * 0x1p24f, c[GL & 1][nb][1]);
+        c[0][GL & 1][nb][0] = fmaf(sA0 * f[nb], (dA[nb][0] + dA[nb][1]) * 0x1p24f, c[0][GL & 1][nb][0]);
+        c[0][GL & 1][nb][1] = fmaf(sA8 * f[nb], (dA[nb][2] + dA[nb][3]) * 0x1p24f, c[0][GL & 1][nb][1]);
+        c[1][GL & 1][nb][0] = fmaf(sB0 * f[nb], (dB[nb][0] + dB[nb][1]) * 0x1p24f, c[1][GL & 1][nb][0]);
+        c[1][GL & 1][nb][1] = fmaf(sB8 * f[nb], (dB[nb][2] + dB[nb][3]) * 0x1p24f, c[1][GL & 1][nb][1]);
     }
 }
 
-// One stage of this warp's tile: four groups, each loaded then used.
+// One stage of this warp's two tiles: four groups, the next group's
+// fragments loaded before the current one's arithmetic.
 template <int NB>
-__device__ __forceinline__ void compute_stage(const uint8_t *slot, int r0,
+__device__ __forceinline__ void compute_stage(const uint8_t *slot, int warp,
                                               const uint4 *const bp[NB],
-                                              const float *const fp[NB], float c[2][NB][2]) {
+                                              const float *const fp[NB], float c[2][2][NB][2]) {
     const int lane = threadIdx.x & 31, q = lane & 3, pr = tile_row(lane >> 2);
-    // the four groups' scales of rows pr and pr + 8 are a 16-byte vector
-    const float4 s0 = reinterpret_cast<const float4 *>(slot + kTStageW)[r0 + pr];
-    const float4 s8 = reinterpret_cast<const float4 *>(slot + kTStageW)[r0 + pr + 8];
-    const uint8_t *wa = slot + (r0 + pr) * 128;
-    GroupFrag<NB> g;
-    group_load<NB, 0>(wa, pr, q, bp, g);
-    group_math<NB, 0>(g, s0.x, s8.x, fp, c);
-    group_load<NB, 1>(wa, pr, q, bp, g);
-    group_math<NB, 1>(g, s0.y, s8.y, fp, c);
-    group_load<NB, 2>(wa, pr, q, bp, g);
-    group_math<NB, 2>(g, s0.z, s8.z, fp, c);
-    group_load<NB, 3>(wa, pr, q, bp, g);
-    group_math<NB, 3>(g, s0.w, s8.w, fp, c);
+    const int rA = 16 * warp + pr, rB = kTRowB + 16 * warp + pr;
+    // the four groups' scales of a row are a 16-byte vector
+    const float4 *sv = reinterpret_cast<const float4 *>(slot + kTStageW);
+    const float4 sA0 = sv[rA], sA8 = sv[rA + 8], sB0 = sv[rB], sB8 = sv[rB + 8];
+    const uint8_t *waA = slot + rA * 128, *waB = slot + rB * 128;
+    GroupFrag<NB> g0, g1;
+    group_load<NB, 0>(waA, waB, pr, q, bp, g0);
+    group_load<NB, 1>(waA, waB, pr, q, bp, g1);
+    group_math<NB, 0>(g0, sA0.x, sA8.x, sB0.x, sB8.x, fp, c);
+    group_load<NB, 2>(waA, waB, pr, q, bp, g0);
+    group_math<NB, 1>(g1, sA0.y, sA8.y, sB0.y, sB8.y, fp, c);
+    group_load<NB, 3>(waA, waB, pr, q, bp, g1);
+    group_math<NB, 2>(g0, sA0.z, sA8.z, sB0.z, sB8.z, fp, c);
+    group_math<NB, 3>(g1, sA0.w, sA8.w, sB0.w, sB8.w, fp, c);
 }
 
 struct TShared {
@@ -259,24 +276,25 @@ struct TShared {
 
 // Consumer side of stages [kb0, kb1) of one item. A wait that runs out sets
 // `failed`; from then on the warp stops waiting but keeps the same sequence
-// of barriers, so every warp reaches the end. acc: rows tile_row(gid) and +8 of this
-// warp's tile, token 4nb+q.
+// of barriers, so every warp reaches the end. acc[tile][nb]: rows
+// tile_row(gid) and +8 of the warp's tile A / B, token 4nb+q.
 template <int NB>
 __device__ __forceinline__ void t_consume(TShared &sh, const uint8_t *ring, int ntok, int kb0,
-                                          int kb1, int &j, bool &failed, float acc[NB][2]) {
+                                          int kb1, int &j, bool &failed, float acc[2][NB][2]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
-    const int r0 = 16 * warp;
     int ob[NB], of[NB];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
         ob[nb] = min(4 * nb + (gid >> 1), ntok - 1) * (kTActTok / 16) + q * 2 + (gid & 1);
         of[nb] = min(4 * nb + q, ntok - 1) * (kTFacTok / 4);
     }
-    float c[2][NB][2];
+    float c[2][2][NB][2];
 #pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2)
+    for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) c[h2][nb][0] = c[h2][nb][1] = 0.f;
+        for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) c[t][h2][nb][0] = c[t][h2][nb][1] = 0.f;
     for (int kb = kb0; kb < kb1; ++kb, ++j) {
         const int slot = j % kTStages;
         if (!failed &&
@@ -290,72 +308,63 @@ __device__ __forceinline__ void t_consume(TShared &sh, const uint8_t *ring, int 
             bp[nb] = reinterpret_cast<const uint4 *>(sp + kTOffA) + ob[nb];
             fp[nb] = reinterpret_cast<const float *>(sp + kTOffF) + of[nb];
         }
-        compute_stage<NB>(sp, r0, bp, fp, c);
+        compute_stage<NB>(sp, warp, bp, fp, c);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.empty[slot]);
     }
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-        acc[nb][0] = c[0][nb][0] + c[1][nb][0];
-        acc[nb][1] = c[0][nb][1] + c[1][nb][1];
-    }
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            acc[t][nb][0] = c[t][0][nb][0] + c[t][1][nb][0];
+            acc[t][nb][1] = c[t][0][nb][1] + c[t][1][nb][1];
+        }
 }
 
 template <int NB>
 __device__ __forceinline__ void t_epilogue(const TmaArgs &a, const TShared &sh, float *epi,
-                                           int tile, int ntok, int pi, const float acc[NB][2]) {
+                                           int tile, int ntok, int pi, const float acc[2][NB][2]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3;
     const int pr = tile_row(lane >> 2);
     if (a.mode != 0) {
         const bool second = tile >= a.tiles0;  // dense pair: the second matrix
         const int H = second ? a.H2 : a.H;
-        const int r0 = (second ? tile - a.tiles0 : tile) * kTDnRows + 16 * warp + pr;
+        const int base = (second ? tile - a.tiles0 : tile) * kTDnRows + 16 * warp + pr;
+        float *yb = second ? a.y2 : a.y;
+        uint16_t *hb = second ? nullptr : a.ybf;
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-            const int s = 4 * nb + q;
-            if (s < ntok) {
-                float *yb = second ? a.y2 : a.y;
-                uint16_t *hb = second ? nullptr : a.ybf;
-                const size_t o = (size_t)sh.pairs[s] * H + r0;
-                if (r0 < H) store_y(yb, hb, o, acc[nb][0]);
-                if (r0 + 8 < H) store_y(yb, hb, o + 8, acc[nb][1]);
+        for (int t = 0; t < 2; ++t) {
+            const int r0 = base + t * kTRowB;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                const int s = 4 * nb + q;
+                if (s < ntok) {
+                    const size_t o = (size_t)sh.pairs[s] * H + r0;
+                    if (r0 < H) store_y(yb, hb, o, acc[t][nb][0]);
+                    if (r0 + 8 < H) store_y(yb, hb, o + 8, acc[t][nb][1]);
+                }
             }
         }
         return;
     }
-    // gate+up: warps 0-7 hold gate rows, warps 8-15 the up rows of the same units
-    constexpr int half = kTConsumers / 2;
+    // gate+up: tile A holds the gate rows, tile B the up rows of the same units
     const int I = a.I;
-    float *gbuf = epi;
-    float *hbuf = epi + kTGuJ * kMaxTok;
-    float *wbuf = epi + 2 * kTGuJ * kMaxTok;
+    float *hbuf = epi;
+    float *wbuf = epi + kTGuJ * kMaxTok;
     const int j0 = tile * kTGuJ;
-    if (warp < half) {
+    const int lr = 16 * warp + pr;
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-            const int s = 4 * nb + q;
-            if (s < ntok) {
-                gbuf[(16 * warp + pr) * kMaxTok + s] = acc[nb][0];
-                gbuf[(16 * warp + pr + 8) * kMaxTok + s] = acc[nb][1];
-            }
-        }
-    }
-    consumers_sync();
-    if (warp >= half) {
-        const int lr = 16 * (warp - half) + pr;
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-            const int s = 4 * nb + q;
-            if (s < ntok) {
-                const float g0 = gbuf[lr * kMaxTok + s], g1 = gbuf[(lr + 8) * kMaxTok + s];
-                const float h0 = g0 / (1.0f + expf(-g0)) * acc[nb][0];
-                const float h1 = g1 / (1.0f + expf(-g1)) * acc[nb][1];
-                hbuf[lr * kMaxTok + s] = h0;
-                hbuf[(lr + 8) * kMaxTok + s] = h1;
-                float *hb = a.h + (size_t)sh.pairs[s] * I + j0;
-                if (j0 + lr < I) hb[lr] = h0;
-                if (j0 + lr + 8 < I) hb[lr + 8] = h1;
-            }
+    for (int nb = 0; nb < NB; ++nb) {
+        const int s = 4 * nb + q;
+        if (s < ntok) {
+            const float g0 = acc[0][nb][0], g1 = acc[0][nb][1];
+            const float h0 = g0 / (1.0f + expf(-g0)) * acc[1][nb][0];
+            const float h1 = g1 / (1.0f + expf(-g1)) * acc[1][nb][1];
+            hbuf[lr * kMaxTok + s] = h0;
+            hbuf[(lr + 8) * kMaxTok + s] = h1;
+            float *hg = a.h + (size_t)sh.pairs[s] * I + j0;
+            if (j0 + lr < I) hg[lr] = h0;
+            if (j0 + lr + 8 < I) hg[lr + 8] = h1;
         }
     }
     consumers_sync();
@@ -410,19 +419,21 @@ __device__ __forceinline__ int unit_owner(const long long *ub, int g, long long 
 // No CTA waits for another.
 template <int NB>
 __device__ __forceinline__ bool t_combine(const TmaArgs &a, TShared &sh, int ntok, int item,
-                                          bool head, int ns, float acc[NB][2]) {
+                                          bool head, int ns, float acc[2][NB][2]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3;
     const int g = gridDim.x;
     const int r = 16 * warp + tile_row(lane >> 2);
     float *mine = a.part + ((size_t)blockIdx.x * 2 + (head ? 0 : 1)) * (kTRows * kMaxTok);
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-        const int s = 4 * nb + q;
-        if (s < ntok) {
-            mine[r * kMaxTok + s] = acc[nb][0];
-            mine[(r + 8) * kMaxTok + s] = acc[nb][1];
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const int s = 4 * nb + q, rt = r + t * kTRowB;
+            if (s < ntok) {
+                mine[rt * kMaxTok + s] = acc[t][nb][0];
+                mine[(rt + 8) * kMaxTok + s] = acc[t][nb][1];
+            }
         }
-    }
     // The barrier orders every consumer's partial-sum stores before thread 0's
     // counter update, a release whose cumulativity makes them visible
     // device-wide first; the same atomic is an acquire, which orders the
@@ -440,26 +451,30 @@ __device__ __forceinline__ bool t_combine(const TmaArgs &a, TShared &sh, int nto
     consumers_sync();
     if (!sh.last) return false;
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = 0.f;
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) acc[t][nb][0] = acc[t][nb][1] = 0.f;
     for (int c = bf; c <= bl; ++c) {
         const long long c0 = sh.ub[c];
         if (sh.ub[c + 1] <= c0) continue;
         const float *pc =
             a.part + ((size_t)c * 2 + (c0 >= first ? 0 : 1)) * (kTRows * kMaxTok);
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-            const int s = 4 * nb + q;
-            if (s < ntok) {
-                acc[nb][0] += __ldcg(pc + r * kMaxTok + s);
-                acc[nb][1] += __ldcg(pc + (r + 8) * kMaxTok + s);
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                const int s = 4 * nb + q, rt = r + t * kTRowB;
+                if (s < ntok) {
+                    acc[t][nb][0] += __ldcg(pc + rt * kMaxTok + s);
+                    acc[t][nb][1] += __ldcg(pc + (rt + 8) * kMaxTok + s);
+                }
             }
-        }
     }
     if (threadIdx.x == 0) a.cnt[bf] = 0;
     return true;
 }
 
-__global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant__ TmaArgs a) {
+__global__ void __launch_bounds__(kTRegBound, 1) k_moe_tma(const __grid_constant__ TmaArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ TShared sh;
     // 1024-byte alignment by an offset on the shared array itself, so the
@@ -634,13 +649,13 @@ __global__ void __launch_bounds__(kTThreads, 1) k_moe_tma(const __grid_constant_
             }
             const bool whole = kb0 == 0 && kb1 == ns;
             if (pc.ntok <= 4) {
-                float acc[1][2];
+                float acc[2][1][2];
                 t_consume<1>(sh, ring, pc.ntok, kb0, kb1, j, failed, acc);
                 if (fresh) consumers_sync();  // sh.pairs written before the epilogue reads it
                 if (whole || t_combine<1>(a, sh, pc.ntok, item, item == head_item, ns, acc))
                     t_epilogue<1>(a, sh, epi, tile, pc.ntok, pi, acc);
             } else {
-                float acc[2][2];
+                float acc[2][2][2];
                 t_consume<2>(sh, ring, pc.ntok, kb0, kb1, j, failed, acc);
                 if (fresh) consumers_sync();
                 if (whole || t_combine<2>(a, sh, pc.ntok, item, item == head_item, ns, acc))
