@@ -469,6 +469,9 @@ def run_ours(args):
     gu_t, dn_t, gu_b, dn_b = [], [], [], []
     E_gu = 2 * wl["I"] * wl["H"] // 2 + 2 * wl["I"] * wl["H"] // 64 * 4
     E_dn = wl["H"] * wl["I"] // 2 + wl["H"] * wl["I"] // 64 * 4
+    # every launch enqueued back to back and one synchronize at the end, so
+    # the events measure the kernels, not the host's launch latency
+    evs = []
     for rep in range(4):
         for i in range(ROTATE):
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
@@ -478,13 +481,15 @@ def run_ours(args):
                 ev[1].record(stream)
                 q.moe_ffn_down(m, T, k, wss[i], stream=stream)
                 ev[2].record(stream)
-            ev[2].synchronize()
-            if rep >= 1:
-                gu_t.append(ev[0].elapsed_time(ev[1]) * 1e-3)
-                dn_t.append(ev[1].elapsed_time(ev[2]) * 1e-3)
-                U = batches[i]["U"]
-                gu_b.append(U * E_gu + T * wl["H"] * 4 + T * k * wl["I"] * 4)
-                dn_b.append(U * E_dn + T * k * wl["I"] * 4 + T * k * wl["H"] * 4)
+            evs.append((rep, i, ev))
+    torch.cuda.synchronize()
+    for rep, i, ev in evs:
+        if rep >= 1:
+            gu_t.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+            dn_t.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+            U = batches[i]["U"]
+            gu_b.append(U * E_gu + T * wl["H"] * 4 + T * k * wl["I"] * 4)
+            dn_b.append(U * E_dn + T * k * wl["I"] * 4 + T * k * wl["H"] * 4)
     peak, peak_kind = peaks()
     gu_kernel = "k_moe_tma" if q.moe_weight_path(m) == 1 else "k_gate_up"
     gu_ach = sum(gu_b) / sum(gu_t) / 1e9
