@@ -288,8 +288,8 @@ int prepare_impl(const qmv_moe_int4 *m, const float *x, int T, const int32_t *id
     qmv::PlanArgs plan{};
     if (pk) {
         plan.ptab = at<int4>(ws, L.ptab);
-        plan.plan_gu = at<int32_t>(ws, L.plan);
-        plan.plan_dn = at<int32_t>(ws, L.plan) + qmv::kSkMaxCtas + 1;
+        plan.plan_gu = at<int4>(ws, L.plan);
+        plan.plan_dn = at<int4>(ws, L.plan) + qmv::kSkMaxCtas + 1;
         plan.s_gu = ((m->I + 127) / 128) * (m->H / 256);
         plan.s_dn = ((m->H + 255) / 256) * (m->I / 256);
         plan.g = qmv::tma_grid();
@@ -332,7 +332,7 @@ int moe_ffn_gate_up(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_byt
             at<void>(ws, pk ? L.hpk : L.hcells), (pk ? nullptr : at<float>(ws, L.hfac)), nullptr,
             at<int32_t>(ws, L.status), at<int32_t>(ws, L.sk_cnt), at<float>(ws, L.sk_part),
             cs(stream), pk, pk ? at<int4>(ws, L.ptab) : nullptr,
-            pk ? at<int32_t>(ws, L.plan) : nullptr));
+            pk ? at<int4>(ws, L.plan) : nullptr));
     }
     return from_cuda(qmv::launch_gate_up(
         dims(m), at<void>(ws, L.xcells), at<float>(ws, L.xfac), k, at<int32_t>(ws, L.offsets),
@@ -354,7 +354,7 @@ int moe_ffn_down(const qmv_moe_int4 *m, int T, int k, void *ws, size_t ws_bytes,
             at<int32_t>(ws, L.n_used), at<int32_t>(ws, L.pass_ofs), nullptr, nullptr, nullptr,
             at<float>(ws, L.y), at<int32_t>(ws, L.status), at<int32_t>(ws, L.sk_cnt) + qmv::kSkMaxCtas,
             at<float>(ws, L.sk_part), cs(stream), pk, pk ? at<int4>(ws, L.ptab) : nullptr,
-            pk ? at<int32_t>(ws, L.plan) + qmv::kSkMaxCtas + 1 : nullptr));
+            pk ? at<int4>(ws, L.plan) + qmv::kSkMaxCtas + 1 : nullptr));
     }
     return from_cuda(qmv::launch_down(dims(m), at<void>(ws, L.hcells), at<float>(ws, L.hfac),
                                       at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.list),

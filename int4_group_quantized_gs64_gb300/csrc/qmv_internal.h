@@ -58,8 +58,10 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int
 constexpr int kPlanW1 = 3, kPlanW2 = 4;
 struct PlanArgs {
     int4 *ptab;        // [passes]: (expert, first list index, tokens, 0)
-    int32_t *plan_gu;  // [g + 1]: first stage of each gate+up CTA, then the total
-    int32_t *plan_dn;  // [g + 1]: the same for down
+    int4 *plan_gu;     // [g + 1]: (first stage of each gate+up CTA, then the total;
+                       //  and the expert, first list index and tokens of the pass
+                       //  holding that stage), so a CTA starts with one load
+    int4 *plan_dn;     // [g + 1]: the same for down
     int s_gu, s_dn;    // stages per pass: row tiles x stages per tile
     int g;             // CTAs of the tensor-map kernel
 };
@@ -153,7 +155,7 @@ cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const 
                            const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,
                            float *hfac, float *y, int32_t *status, int32_t *cnt, float *part,
                            cudaStream_t st, bool packed = false, const int4 *ptab = nullptr,
-                           const int32_t *plan = nullptr);
+                           const int4 *plan = nullptr);
 
 // Single-launch expert FFN of one token (cooperative grid, qmv_moe_one.cu);
 // it clears the status word itself.

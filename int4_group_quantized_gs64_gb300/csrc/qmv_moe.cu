@@ -161,6 +161,7 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
         }
         __syncthreads();
         const int nu = nu_s;
+        const int npass = nu > 0 ? pass_ofs[nu] : 0;
         for (int b = tid; b <= pl->g; b += blockDim.x) {
             for (int m = 0; m < 2; ++m) {
                 const long long S = m ? pl->s_dn : pl->s_gu;
@@ -187,7 +188,9 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
                     const long long st = min(S, (r2 + wi - 1) / wi);
                     ub = (int32_t)(S * (pass_ofs[lo] + i) + st);
                 }
-                (m ? pl->plan_dn : pl->plan_gu)[b] = ub;
+                const int p = (int)(ub / S);  // the pass holding stage ub, if any
+                const int4 t = p < npass ? pl->ptab[p] : make_int4(0, 0, 0, 0);
+                (m ? pl->plan_dn : pl->plan_gu)[b] = make_int4(ub, t.x, t.y, t.z);
             }
         }
     }
@@ -807,7 +810,7 @@ MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k) {
     L.xpk = o; o = align256(o + pm * sh * kPackedStage);
     L.hpk = o; o = align256(o + pm * si * kPackedStage);
     L.ptab = o; o = align256(o + 16 * pm);
-    L.plan = o; o = align256(o + 4 * 2 * ((size_t)kSkMaxCtas + 1));
+    L.plan = o; o = align256(o + 16 * 2 * ((size_t)kSkMaxCtas + 1));
     L.total = o;
     return L;
 }

@@ -90,7 +90,7 @@ struct TmaArgs {
     float *y;            // down: y [P][H]; dense: y [S][H]
     uint16_t *ybf;       // dense, first matrix: y rounded to bf16 [S][H] instead of y
     const int4 *ptab;    // the grouping kernel's pass table, or null (PlanArgs)
-    const int32_t *plan; // this mode's CTA stage boundaries [g + 1], or null
+    const int4 *plan;    // this mode's CTA plan [g + 1] (PlanArgs), or null
     int32_t *status;
     int32_t *cnt;        // per CTA: contributors done on the split item that starts in it
     float *part;         // per CTA: partial sums [2][kTRows][kMaxTok] (head / tail item)
@@ -182,6 +182,24 @@ struct PassCursor {
         ntok = min(kMaxTok, cnt - pass * kMaxTok);
     }
 };
+
+// Places a cursor on pass p, the first pass of this CTA: from the plan's
+// entry (no load) when there is a plan, else by seek.
+__device__ __forceinline__ void start_cursor(PassCursor &c, const TmaArgs &a, int nu, int p,
+                                             int4 pl0) {
+    if (a.plan) {
+        c.pi = p;
+        c.e = pl0.y;
+        c.beg = pl0.z;
+        c.ntok = pl0.w;
+    } else {
+        c.seek(a, nu, p);
+    }
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
 
 // Shared-memory row (within a 16-row tile) that holds MMA row gid (and gid + 8
 // at +8). With the 128-byte swizzle, rows {0,2,4,6} and {1,3,5,7} each spread
@@ -483,6 +501,14 @@ __global__ void __launch_bounds__(kTRegBound, 1) k_moe_tma(const __grid_constant
     float *epi = reinterpret_cast<float *>(ring + kTStages * kTStage);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    if (warp == kTConsumers && lane == 0) {  // the tensor-map descriptors, early
+        prefetch_tmap(&a.wmap);
+        prefetch_tmap(&a.smap);
+        if (a.H2 > 0) {
+            prefetch_tmap(&a.wmap2);
+            prefetch_tmap(&a.smap2);
+        }
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTStages; ++s) {
             tc05::mbar_init(&sh.full[s], 1);
@@ -508,10 +534,12 @@ __global__ void __launch_bounds__(kTRegBound, 1) k_moe_tma(const __grid_constant
     // even split [U*b/g, U*(b+1)/g).
     int nu = 1;
     long long U, u0, u1;
+    int4 pl0 = make_int4(0, 0, 0, 0);  // the plan's first pass of this CTA
     if (a.plan) {
-        U = a.plan[g];
-        u0 = a.plan[blockIdx.x];
-        u1 = a.plan[blockIdx.x + 1];
+        pl0 = a.plan[blockIdx.x];
+        U = a.plan[g].x;
+        u0 = pl0.x;
+        u1 = a.plan[blockIdx.x + 1].x;
     } else {
         nu = a.mode == 2 ? 1 : *a.n_used;
         const int passes =
@@ -530,7 +558,7 @@ __global__ void __launch_bounds__(kTRegBound, 1) k_moe_tma(const __grid_constant
         const int pre = a.mode != 0 ? min(total, kTStages) : 0;
         const int item0 = (int)(u0 / ns), kb_0 = (int)(u0 - (long long)item0 * ns);
         PassCursor pc;
-        if (total > 0) pc.seek(a, nu, item0 / tiles);
+        if (total > 0) start_cursor(pc, a, nu, item0 / tiles, pl0);
         auto weights = [&](int slot, int item, int kb, const PassCursor &c) {
             const int pi = item / tiles, tile = item - pi * tiles;
             const int rowA = a.mode == 0 ? tile * kTGuJ : tile * kTDnRows;
@@ -626,14 +654,14 @@ __global__ void __launch_bounds__(kTRegBound, 1) k_moe_tma(const __grid_constant
     } else {
         // ---------------- consumers
         for (int i = threadIdx.x; i <= g; i += 32 * kTConsumers)
-            sh.ub[i] = a.plan ? (long long)a.plan[i] : (long long)i * U / g;
+            sh.ub[i] = a.plan ? (long long)a.plan[i].x : (long long)i * U / g;
         int j = 0, cur_pi = -1;
         bool failed = false;
         PassCursor pc;
         const int head_item = (int)(u0 / ns);
         int left = (int)(u1 - u0);
         int item = head_item, kb0 = (int)(u0 - (long long)head_item * ns);
-        if (left > 0) pc.seek(a, nu, head_item / tiles);
+        if (left > 0) start_cursor(pc, a, nu, head_item / tiles, pl0);
         for (; left > 0; ++item, kb0 = 0) {
             const int kb1 = min(ns, kb0 + left);
             left -= kb1 - kb0;
@@ -749,7 +777,7 @@ cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const 
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                            const int32_t *n_used, const int32_t *pass_ofs, float *h, void *hcells,
                            float *hfac, float *y, int32_t *status, int32_t *cnt, float *part,
-                           cudaStream_t st, bool packed, const int4 *ptab, const int32_t *plan) {
+                           cudaStream_t st, bool packed, const int4 *ptab, const int4 *plan) {
     TmaArgs a;
     memset(&a, 0, sizeof(a));
     a.mode = mode;
