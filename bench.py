@@ -242,9 +242,12 @@ def bench_config(ws_n: int, T: int) -> dict:
                   "8 rotating seeded micro-batches"}
 
 
-def load_traffic(kernel: str):
-    """dram bytes per launch from the committed ncu summary, if it still matches the source:
-    the kernel's file and the headers holding its device code and sizes, hashed."""
+def load_traffic(kernel: str, alg_bytes: float):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches the
+    source (the kernel's file and the headers holding its device code and sizes,
+    hashed): the captured launch's dram read + write bytes, scaled to a launch of
+    `alg_bytes` algorithmic bytes by the ratio of algorithmic bytes (the capture runs
+    a smaller expert pool; traffic grows with the experts touched)."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
@@ -257,7 +260,9 @@ def load_traffic(kernel: str):
             h.update(open(os.path.join(ROOT, f), "rb").read())
     except OSError:
         return None  # a source it was measured on is gone: stale
-    return d["bytes_per_launch"] if h.hexdigest() == d.get("sha256") else None
+    if h.hexdigest() != d.get("sha256"):
+        return None
+    return d["measured_bytes"] * alg_bytes / d["measured_algorithmic_bytes"]
 
 
 # ------------------------------------------------------------------ profiling case
@@ -498,11 +503,12 @@ def run_ours(args):
                 "peak": peak, "unit": "GB/s", "frac": gu_ach / peak,
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
-                "traffic": load_traffic(gu_kernel + " gate+up"),
+                "traffic": load_traffic(gu_kernel + " gate+up", statistics.mean(gu_b)),
                 "bytes_per_launch": statistics.mean(gu_b),
                 "us_per_launch": statistics.mean(gu_t) * 1e6,
                 "us_per_launch_spread": spread(gu_t, 1e6), "launches_timed": len(gu_t),
                 "down": {"kernel": gu_kernel, "achieved": dn_ach, "frac": dn_ach / peak,
+                         "traffic": load_traffic(gu_kernel + " down", statistics.mean(dn_b)),
                          "bytes_per_launch": statistics.mean(dn_b),
                          "us_per_launch": statistics.mean(dn_t) * 1e6,
                          "us_per_launch_spread": spread(dn_t, 1e6)}}

@@ -2,7 +2,9 @@
 
 The bench runs one replica per GPU (the path has no exchange step); its
 reported value is the bytes of all ranks over the slowest rank's step time.
-These tests run that host logic with two gloo ranks on 127.0.0.1.
+These tests run that host logic with two gloo ranks on 127.0.0.1. The last
+test checks that the committed ncu traffic record still matches the decode
+kernel's sources.
 """
 import os
 import socket
@@ -57,3 +59,15 @@ def test_single_process_passthrough():
     import bench
     assert bench.max_over_ranks(0.25) == 0.25
     assert bench.whole_job_value(1, 2e9, 0.5) == pytest.approx(4.0)
+
+
+@pytest.mark.parametrize("launch", ["gate+up", "down"])
+def test_traffic_record_matches_kernel_sources(launch):
+    """The committed ncu traffic record still hashes to the decode kernel's
+    sources (a changed kernel needs a new capture) and reads close to the
+    algorithmic bytes."""
+    sys.path.insert(0, ROOT)
+    import bench
+    t = bench.load_traffic("k_moe_tma " + launch, 1e8)
+    assert t is not None, "profiles/traffic.json is stale for the decode kernel"
+    assert 1.0 <= t / 1e8 < 1.2
