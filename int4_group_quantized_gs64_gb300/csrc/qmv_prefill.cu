@@ -224,6 +224,51 @@ __host__ __device__ __forceinline__ int kperm_pos(int kq) {
     return 8 * (kq >> 3) + 2 * (kq & 3) + ((kq >> 2) & 1);
 }
 
+__device__ __forceinline__ uint32_t bfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_splat(float v) {
+    const __nv_bfloat162 b = __float2bfloat162_rn(v);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+// The same values and K order as pf_dequant_perm in 11 instructions a word
+// instead of 15. Each nibble is moved to bits 4..7 of its 16-bit half with
+// nothing else set: as a bf16 bit pattern below 0x100 (exponent field 0 or 1,
+// where consecutive patterns are 2^-133 apart) that reads exactly n * 2^-129.
+// One fused multiply-add per pair, n * 2^-129 * (s * 2^129) - 8 s, is then
+// (n - 8) * s with a single bf16 rounding: the product is exact and -8 s is
+// exact in bf16, so the result is bit for bit the two-step form's. Valid
+// while s * 2^129 and 8 s stay normal bf16 numbers: 2^-120 <= |s| < 2^-2
+// (or s = 0); pf_dequant_fast checks that per warp.
+__device__ __forceinline__ void pf_dequant_sub(const uint4 &w0, const uint4 &w1, float scale,
+                                               uint32_t (&r)[32]) {
+    const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const uint32_t s = bf16x2_splat(scale * 0x1p64f * 0x1p65f);  // two exact steps
+    const uint32_t c = bf16x2_splat(-8.0f * scale);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t w = words[i];
+        r[4 * i + 0] = bfma2((w << 4) & 0x00F000F0u, s, c);  // nibbles 0 and 4
+        r[4 * i + 1] = bfma2(w & 0x00F000F0u, s, c);         // 1 and 5
+        r[4 * i + 2] = bfma2((w >> 4) & 0x00F000F0u, s, c);  // 2 and 6
+        r[4 * i + 3] = bfma2((w >> 8) & 0x00F000F0u, s, c);  // 3 and 7
+    }
+}
+
+// pf_dequant_sub when every lane's scale is in its range, else
+// pf_dequant_perm (same bits either way). Whole warp.
+__device__ __forceinline__ void pf_dequant_fast(const uint4 &w0, const uint4 &w1, float scale,
+                                                uint32_t (&r)[32]) {
+    const float m = fabsf(scale);
+    if (__all_sync(0xffffffffu, (m < 0.25f && m >= 0x1p-120f) || scale == 0.0f))
+        pf_dequant_sub(w0, w1, scale, r);
+    else
+        pf_dequant_perm(w0, w1, scale, r);
+}
+
 __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(PfArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t mbar[2];
@@ -385,42 +430,48 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(PfArgs a) {
 // ------------------------------------------------------------------ pipelined variant
 //
 // Shapes with H/64 and I/64 multiples of 4 and 16-byte aligned pools run a
-// warp-specialized version of the same computation. One CTA per SM, 10 warps,
-// two rings of stages; a stage is 256 weight rows x 4 groups of one item:
+// warp-specialized version of the same computation. One CTA per SM, 26 warps,
+// two rings of stages in shared memory; a stage is 256 weight rows x 4 groups
+// of one item:
 //   * weight producer warp: two 3-D tensor-map loads of the packed weights
 //     (128 rows x 128 bytes, 128-byte swizzle) and two of their scales per
-//     stage into a 4-slot ring that the dequant warps free as soon as they
-//     have read a stage, so weights stream up to 4 stages ahead;
-//   * B producer warp: the B tile of the 4 groups (the pass's token rows,
-//     bf16, 128-byte swizzled K-major, up to 64 rows per group) by cp.async
-//     into a 2-slot ring that the MMAs free; a stage's B is marked ready once
-//     its copies have landed, after a proxy fence;
+//     stage into a 3-slot ring that the dequant warps free as soon as they
+//     have read a stage;
+//   * B producer warp: the B tiles of the stage's 4 groups (the pass's token
+//     rows, bf16, 128-byte swizzled K-major, rows rounded up to 16) by bulk
+//     copy into a 3-slot ring that the MMAs free;
 //   * 16 dequant warps, thread = weight row = TMEM lane, two warps per lane
-//     quarter: set 0 takes groups 0-1 of each stage, set 1 groups 2-3. Per
-//     group a thread dequantizes its row to bf16 with the scale folded in,
-//     stores it to that group's A slot in tensor memory and the warp signals
-//     the group; at the end of an item set 0 reads the accumulators back and
-//     writes h (bf16) or y (fp32);
-//   * 4 MMA warps, one per (row tile, half of the stage's groups): one thread
-//     of each issues 2 groups x 4 MMAs (M 128, N = tokens rounded up to 16,
+//     quarter and tile: set 0 takes groups 0-1 of each stage, set 1 groups
+//     2-3. Per group a thread dequantizes its row to bf16 with the scale
+//     folded in and stores it to the group's A slot of its tile in tensor
+//     memory; the first group's store drains while the second group is
+//     dequantized;
+//   * 4 MMA warps, one per (tile, half of the stage's groups): one thread of
+//     each issues 2 groups x 4 MMAs (M 128, N = tokens rounded up to 16,
 //     K 16) per stage into its own accumulator, which runs over the whole
-//     item, and commits each group to that group's A-slot barrier of its
-//     tile; after a stage it commits to the B slot's empty barrier, after an
-//     item to the accumulator barrier. (A thread that issues tcgen05.mma
-//     waits ~100-200 cycles per instruction for N up to 64; four issuers
-//     share the stage's 32 MMAs.) The epilogue adds each tile's two halves.
-// Tensor memory: A 4 groups x 2 tiles x 32 columns, D 2 tiles x 2 halves x 64.
-// Every wait is bounded; a wait that runs out raises a CTA-wide abort flag,
-// after which nothing waits any more; copies and MMAs in flight are drained
-// (bounded) before the tensor memory is released, and bit 1 of the status
-// word is set.
+//     item, and commits each group to the A slot's barrier of its tile, each
+//     stage to the B slot's, each item to the accumulator barrier. A thread
+//     issues about one tcgen05.mma per ~120 cycles whatever N, so the
+//     stage's 32 MMAs need the four issuers (and four accumulators, to keep
+//     each accumulation order fixed);
+//   * 4 epilogue warps, one per lane quarter: they look up the next item's
+//     pass (and, for down, its token rows) while the item runs, then read
+//     the accumulators back with tcgen05.ld, add each tile's two halves and
+//     write h = SiLU(gate) * up (bf16, straight into down's B layout) or y
+//     (fp32); the MMA warps wait for them before the next item's first MMA.
+// Tensor memory: D 2 tiles x 2 halves x 64 columns, A 4 groups x 2 tiles x
+// 32 columns. Every wait is bounded; a wait that runs out raises a CTA-wide
+// abort flag, after which nothing waits any more; copies and MMAs in flight
+// are drained (bounded) before the tensor memory is released, and bit 1 of
+// the status word is set.
 
-constexpr int kPqDq = 16;                            // dequant warps (set 0: epilogue too)
-constexpr int kPqProdW = kPqDq;                      // weight producer warp
-constexpr int kPqProdB = kPqDq + 1;                  // B producer warp
-constexpr int kPqMma = kPqDq + 2;                    // first of 4 MMA warps
+constexpr int kPqDq = 16;                            // dequant warps
+constexpr int kPqEpi = kPqDq;                        // first of 4 epilogue warps (quarters 0-3)
+constexpr int kPqProdW = kPqDq + 4;                  // weight producer warp
+constexpr int kPqProdB = kPqDq + 5;                  // B producer warp
+constexpr int kPqMma = kPqDq + 6;                    // first of 4 MMA warps
 constexpr int kPqMmaWarps = 4;
-constexpr int kPqThreads = 32 * (kPqDq + 2 + kPqMmaWarps);
+constexpr int kPqThreads = 32 * (kPqDq + 6 + kPqMmaWarps);
 constexpr int kPqWStages = 3;                        // weight ring: freed after dequant
 constexpr int kPqBStages = 3;                        // B ring: freed by the MMAs
 constexpr int kPqOffS = 256 * 128;                   // scales [256][4] f32
@@ -431,12 +482,16 @@ constexpr int kPqOffBRing = kPqWStages * kPqWStage;
 constexpr int kPqSmem = kPqOffBRing + kPqBStages * kPqBStage + 1024;
 constexpr uint32_t kPqTmaBytes = 256 * 128 + 256 * 16;
 constexpr uint32_t kPqTmemCols = 512;
-constexpr uint32_t kPqD = 256;                       // accumulators: 2 tiles x 2 K halves x 64
+constexpr uint32_t kPqD = 0;                         // accumulators: (tile, half) at (2 tile + half) x 64
+constexpr uint32_t kPqA = 256;                       // A: group g, tile t at g x 64 + t x 32
 constexpr uint32_t kPqWait = 1u << 24;
 
 static_assert(kPqWStage % 1024 == 0 && kPqBStage % 1024 == 0,
               "stages must stay 1024-aligned for the 128B swizzle");
 static_assert(kPqBGroup % 1024 == 0, "B tiles must stay 1024-aligned");
+static_assert(kPqD + 4 * kPfMaxN <= kPqA && kPqA + 4 * 64 <= kPqTmemCols,
+              "tensor memory: accumulators and A slots must fit the allocation");
+static_assert(kPqEpi % 4 == 0, "epilogue warp q must sit in lane quarter q");
 
 struct PqArgs {
     CUtensorMap wmap, smap;
@@ -451,13 +506,14 @@ struct PqArgs {
 
 struct PqShared {
     uint64_t wfull[kPqWStages], wempty[kPqWStages];
-    uint64_t bfull[kPqBStages], bempty[kPqBStages];
-    uint64_t afull[4], afree[4][2];
-    uint64_t dfull, dfree;
-    uint64_t mdone[kPqMmaWarps];
+    uint64_t bfull[kPqBStages];
+    uint64_t afull[2][2];                      // [set][tile]: the stage's two A groups stored
+    uint64_t sdone[kPqMmaWarps][kPqBStages];   // issuer m's MMAs of the stage in B slot s done
+    uint64_t dfull, dfree, mdone[kPqMmaWarps];
     uint32_t tmem;
     int abort;
 };
+
 
 __device__ __forceinline__ bool pq_try(uint64_t *mbar, uint32_t parity) {
     uint32_t done;
@@ -480,6 +536,12 @@ __device__ __forceinline__ bool pq_wait(PqShared &sh, uint64_t *mbar, uint32_t p
     }
     *ab = 1;
     return false;
+}
+
+// pq_wait by every lane of a warp, with one answer for all of them, so the
+// warp leaves its loop together (its .sync.aligned instructions need that).
+__device__ __forceinline__ bool pq_wait_warp(PqShared &sh, uint64_t *mbar, uint32_t parity) {
+    return __all_sync(0xffffffffu, pq_wait(sh, mbar, parity));
 }
 
 // Bounded wait that ignores the abort flag (draining work in flight).
@@ -558,15 +620,12 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
         }
         for (int s = 0; s < kPqBStages; ++s) {
             tc05::mbar_init(&sh.bfull[s], 1);
-            tc05::mbar_init(&sh.bempty[s], kPqMmaWarps);
+            for (int m = 0; m < kPqMmaWarps; ++m) tc05::mbar_init(&sh.sdone[m][s], 1);
         }
-        for (int g = 0; g < 4; ++g) {
-            tc05::mbar_init(&sh.afull[g], kPqDq / 2);
-            tc05::mbar_init(&sh.afree[g][0], 1);
-            tc05::mbar_init(&sh.afree[g][1], 1);
-        }
+        for (int g = 0; g < 2; ++g)
+            for (int t = 0; t < 2; ++t) tc05::mbar_init(&sh.afull[g][t], 4);  // 4 lane quarters
         tc05::mbar_init(&sh.dfull, kPqMmaWarps);
-        tc05::mbar_init(&sh.dfree, kPqDq / 2);
+        tc05::mbar_init(&sh.dfree, 4);
         for (int m = 0; m < kPqMmaWarps; ++m) tc05::mbar_init(&sh.mdone[m], 1);
         sh.abort = 0;
         tc05::fence_mbar_init();
@@ -578,7 +637,7 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
 
     // The grouping finished before the previous kernel (the x packing, or
     // gate_up) started, and the weights depend on no kernel, so the weight
-    // producer never waits; everything that reads packed B does.
+    // producer never waits; everything that reads packed B or writes h / y does.
     if (warp != kPqProdW) pdl_wait();
     pdl_trigger();
 
@@ -632,9 +691,11 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
             int issued = 0;
             for (int j = 0; j < total; ++j) {
                 const int bs = j % kPqBStages;
-                if (j >= kPqBStages &&
-                    !pq_wait(sh, &sh.bempty[bs], (uint32_t)(((j / kPqBStages) - 1) & 1)))
-                    break;
+                // the slot is free once every issuer's MMAs of stage j - kPqBStages are done
+                bool free = true;
+                for (int m = 0; m < kPqMmaWarps && j >= kPqBStages && free; ++m)
+                    free = pq_wait(sh, &sh.sdone[m][bs], (uint32_t)(((j / kPqBStages) - 1) & 1));
+                if (!free) break;
                 const int item = i0 + (j / ns) * istep, kb = j % ns, pi = item / a.tiles;
                 pc.to(a, pi);
                 const uint32_t bytes = (uint32_t)(((pc.ntok + 15) & ~15) * 128);
@@ -651,145 +712,161 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                 pq_drain(&sh.bfull[j % kPqBStages], (uint32_t)((j / kPqBStages) & 1));
         }
     } else if (warp >= kPqMma) {
-        // ---------------- MMA issue: warp kPqMma + m: tile m / 2, groups 2(m % 2), +1
+        // ---------------- MMA issue: warp kPqMma + m: tile m / 2, groups 2(m % 2), +1.
+        // Every mbarrier operation of the issuing thread after an MMA costs a
+        // few hundred cycles (it waits for the MMAs issued so far to be taken
+        // up), so a stage has one wait for its A groups and one commit.
         const int m = warp - kPqMma, t = m >> 1, hk = m & 1;
         if (lane == 0) {
             PqCursor pc;
             if (total > 0) pc.seek(a, nu, i0 / a.tiles);
             const uint32_t dacc = tmem + kPqD + (uint32_t)(m * 64);
-            int items_done = 0;
+            const uint32_t a0 = tmem + kPqA + (uint32_t)(2 * hk * 64 + t * 32);
+            // B descriptor of slot 0, group 2 hk; +1 in the address field = 16 bytes
+            const uint64_t b0 = tc05::sdesc_sw128(
+                tc05::smem_addr(ring + kPqOffBRing + 2 * hk * kPqBGroup));
             bool ok = true;
             for (int j = 0; j < total && ok; ++j) {
                 const int bs = j % kPqBStages;
-                const int item = i0 + (j / ns) * istep, kb = j % ns;
-                pc.to(a, item / a.tiles);
+                const int it = j / ns, kb = j % ns;
+                pc.to(a, (i0 + it * istep) / a.tiles);
                 const uint32_t idesc = tc05::idesc_bf16_f32(128, (pc.ntok + 15) & ~15);
                 ok = pq_wait(sh, &sh.bfull[bs], (uint32_t)((j / kPqBStages) & 1));
-                if (ok && kb == 0 && items_done > 0)
-                    ok = pq_wait(sh, &sh.dfree, (uint32_t)((items_done - 1) & 1));
-                const uint32_t sB = tc05::smem_addr(ring + kPqOffBRing + bs * kPqBStage);
-                for (int g = 2 * hk; g < 2 * hk + 2 && ok; ++g) {
-                    ok = pq_wait(sh, &sh.afull[g], (uint32_t)(j & 1));
-                    if (!ok) break;
-                    tc05::fence_after_sync();
+                // the accumulators are free once the epilogue has read the last item
+                if (ok && kb == 0 && it > 0) ok = pq_wait(sh, &sh.dfree, (uint32_t)((it - 1) & 1));
+                if (ok) ok = pq_wait(sh, &sh.afull[hk][t], (uint32_t)(j & 1));
+                if (!ok) break;
+                tc05::fence_after_sync();
+                const uint64_t bd = b0 + (uint64_t)((bs * kPqBStage) >> 4);
+#pragma unroll
+                for (int gg = 0; gg < 2; ++gg)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc05::mma_ts(dacc, tmem + g * 64 + t * 32 + kk * 8,
-                                     tc05::sdesc_sw128(sB + g * kPqBGroup + kk * 32), idesc,
-                                     (kb > 0 || g > 2 * hk || kk > 0) ? 1u : 0u);
-                    tc05::mma_commit(&sh.afree[g][t]);
-                }
-                if (!ok) break;
-                tc05::mma_commit(&sh.bempty[bs]);
-                if (kb == ns - 1) {
-                    tc05::mma_commit(&sh.dfull);
-                    ++items_done;
-                }
+                        tc05::mma_ts(dacc, a0 + (uint32_t)(gg * 64 + kk * 8),
+                                     bd + (uint64_t)((gg * kPqBGroup + kk * 32) >> 4), idesc,
+                                     (kb > 0 || gg > 0 || kk > 0) ? 1u : 0u);
+                // frees this issuer's A slots and its use of the B slot
+                tc05::mma_commit(&sh.sdone[m][bs]);
+                if (kb == ns - 1) tc05::mma_commit(&sh.dfull);
             }
             // the MMAs still in flight must finish before the tensor memory is freed
             tc05::mma_commit(&sh.mdone[m]);
             pq_drain(&sh.mdone[m], 0);
         }
-    } else {
-        // ---------------- dequant / epilogue warps
-        const int set = warp >> 3, tt = (warp >> 2) & 1, q = warp & 3;
-        const int r = tt * 128 + q * 32 + lane;     // stage row; TMEM lane q*32 + lane
-        const bool epi = set == 0;
+    } else if (warp >= kPqEpi && warp < kPqEpi + 4) {
+        // ---------------- epilogue: lane quarter q of both tiles
+        const int q = warp & 3, r128 = q * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         PqCursor pc;
         if (total > 0) pc.seek(a, nu, i0 / a.tiles);
-        int items_done = 0;
-        for (int j = 0; j < total; ++j) {
+        for (int it = 0; it < n_items; ++it) {
+            const int item = i0 + it * istep, tile = item % a.tiles;
+            pc.to(a, item / a.tiles);
+            const int ntok = pc.ntok, nblk = ((ntok + 15) & ~15) / 16;
+            // down scatters to the pairs' rows: lane l holds pairs l and 32 + l
+            int p0 = 0, p1 = 0;
+            if (a.mode == 1) {
+                if (lane < ntok) p0 = a.list[pc.beg + lane];
+                if (lane + 32 < ntok) p1 = a.list[pc.beg + 32 + lane];
+            }
+            if (!pq_wait_warp(sh, &sh.dfull, (uint32_t)(it & 1))) break;
+            tc05::fence_after_sync();
+            if (a.mode == 0) {
+                // h goes straight into down's packed B: pass pc.pi, group j0 / 64,
+                // row n = token slot, column j0 % 64 in the dequant's K order (swizzled)
+                const int j0 = tile * 128 + r128;
+                const int kp = kperm_pos(j0 & 63);
+                uint16_t *hp = a.h + ((size_t)pc.pi * (a.I / 64) + (j0 >> 6)) * (kPqBGroup / 2);
+                // tile t, half h accumulates at kPqD + (2t + h) * 64: gate is tile 0,
+                // up tile 1; 8 token columns at a time
+                for (int c0 = 0; c0 < nblk * 16; c0 += 8) {
+                    float gs[8];
+                    uint32_t v0[8], v1[8];
+                    tc05::tmem_ld8(tmem + lane_base + kPqD + c0, v0);
+                    tc05::tmem_ld8(tmem + lane_base + kPqD + 64 + c0, v1);
+                    tc05::tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) gs[c] = __uint_as_float(v0[c]) + __uint_as_float(v1[c]);
+                    tc05::tmem_ld8(tmem + lane_base + kPqD + 128 + c0, v0);
+                    tc05::tmem_ld8(tmem + lane_base + kPqD + 192 + c0, v1);
+                    tc05::tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int n = c0 + c;
+                        float hv = 0.f;  // padded rows stay zero
+                        if (n < ntok) {
+                            const float g0 = gs[c];
+                            hv = g0 / (1.0f + expf(-g0)) *
+                                 (__uint_as_float(v0[c]) + __uint_as_float(v1[c]));
+                        }
+                        const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                        hp[n * 64 + (((kp >> 3) ^ (n & 7)) << 3) + (kp & 7)] =
+                            *reinterpret_cast<const uint16_t *>(&hb);
+                    }
+                }
+            } else {
+                const int row = tile * 256 + r128;
+#pragma unroll 1
+                for (int t = 0; t < 2; ++t)  // rows t * 128 + r128 of the tile
+                    for (int c0 = 0; c0 < nblk * 16; c0 += 8) {
+                        uint32_t d0[8], d1[8];
+                        tc05::tmem_ld8(tmem + lane_base + kPqD + t * 128 + c0, d0);
+                        tc05::tmem_ld8(tmem + lane_base + kPqD + t * 128 + 64 + c0, d1);
+                        tc05::tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const int n = c0 + c;
+                            const int p = __shfl_sync(0xffffffffu, n < 32 ? p0 : p1, n & 31);
+                            if (n < ntok)
+                                a.y[(size_t)p * a.H + row + t * 128] =
+                                    __uint_as_float(d0[c]) + __uint_as_float(d1[c]);
+                        }
+                    }
+            }
+            tc05::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) pq_arrive(&sh.dfree);
+        }
+    } else {
+        // ---------------- dequant warps
+        const int set = warp >> 3, tt = (warp >> 2) & 1, q = warp & 3;
+        const int r = tt * 128 + q * 32 + lane;     // stage row; TMEM lane q*32 + lane
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const uint32_t a_col = tmem + lane_base + kPqA + (uint32_t)(tt * 32);
+        const int x7 = r & 7, ga = 2 * set;
+        bool ok = true;
+        for (int j = 0; j < total && ok; ++j) {
             const int ws = j % kPqWStages;
-            const int item = i0 + (j / ns) * istep, kb = j % ns;
-            pq_wait(sh, &sh.wfull[ws], (uint32_t)((j / kPqWStages) & 1));
+            ok = pq_wait_warp(sh, &sh.wfull[ws], (uint32_t)((j / kPqWStages) & 1));
+            if (!ok) break;
             const uint8_t *sp = ring + ws * kPqWStage;
             const uint8_t *wr = sp + r * 128;
-            const int x7 = r & 7;
-#pragma unroll 1
-            for (int g = 2 * set; g < 2 * set + 2; ++g) {
-                const uint4 w0 = *reinterpret_cast<const uint4 *>(wr + (((2 * g) ^ x7) << 4));
-                const uint4 w1 = *reinterpret_cast<const uint4 *>(wr + (((2 * g + 1) ^ x7) << 4));
-                const float sc = *reinterpret_cast<const float *>(sp + kPqOffS + r * 16 + g * 4);
-                uint32_t A[32];
-                pf_dequant_perm(w0, w1, sc, A);
-                if (j > 0) {
-                    // MMA(j - 1) of this group done: its A slot may be overwritten
-                    pq_wait(sh, &sh.afree[g][tt], (uint32_t)((j - 1) & 1));
-                    tc05::fence_after_sync();
-                }
-                tc05::tmem_st32(tmem + lane_base + (uint32_t)(g * 64 + tt * 32), A);
-                tc05::tmem_wait_st();
-                tc05::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) pq_arrive(&sh.afull[g]);
+            const float2 sc = *reinterpret_cast<const float2 *>(sp + kPqOffS + r * 16 + ga * 4);
+            const uint4 wa0 = *reinterpret_cast<const uint4 *>(wr + (((2 * ga) ^ x7) << 4));
+            const uint4 wa1 = *reinterpret_cast<const uint4 *>(wr + (((2 * ga + 1) ^ x7) << 4));
+            uint32_t A[32];
+            pf_dequant_fast(wa0, wa1, sc.x, A);
+            if (j > 0) {
+                // the MMAs of the previous stage that read this warp's A slots are done
+                ok = pq_wait_warp(sh, &sh.sdone[2 * tt + set][(j - 1) % kPqBStages],
+                                  (uint32_t)(((j - 1) / kPqBStages) & 1));
+                tc05::fence_after_sync();
+            }
+            if (!ok) break;
+            tc05::tmem_st32(a_col + (uint32_t)(ga * 64), A);
+            // the second group is dequantized while the first one's store drains
+            {
+                const uint4 wb0 = *reinterpret_cast<const uint4 *>(wr + (((2 * ga + 2) ^ x7) << 4));
+                const uint4 wb1 = *reinterpret_cast<const uint4 *>(wr + (((2 * ga + 3) ^ x7) << 4));
+                pf_dequant_fast(wb0, wb1, sc.y, A);
             }
             // this warp has read its rows of the stage: the weight slot may refill
             if (lane == 0) pq_arrive(&sh.wempty[ws]);
-            if (kb == ns - 1 && epi) {
-                // item done: wait for its last MMAs, then read the accumulators
-                pq_wait(sh, &sh.dfull, (uint32_t)(items_done & 1));
-                tc05::fence_after_sync();
-                pc.to(a, item / a.tiles);
-                const int tile = item % a.tiles;
-                const int ntok = pc.ntok, nblk = ((ntok + 15) & ~15) / 16;
-                const int r128 = q * 32 + lane;
-                if (a.mode == 0) {
-                    // gate_up: tile tt takes column blocks tt, tt + 2, ...
-                    for (int blk = tt; blk < nblk; blk += 2) {
-                        // tile t, half h accumulates at kPqD + (2t + h) * 64
-                        float gs[16];
-                        uint32_t v0[16], v1[16];
-                        tc05::tmem_ld16(tmem + lane_base + kPqD + blk * 16, v0);
-                        tc05::tmem_ld16(tmem + lane_base + kPqD + 64 + blk * 16, v1);
-                        tc05::tmem_wait_ld();
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) gs[c] = __uint_as_float(v0[c]) + __uint_as_float(v1[c]);
-                        tc05::tmem_ld16(tmem + lane_base + kPqD + 128 + blk * 16, v0);
-                        tc05::tmem_ld16(tmem + lane_base + kPqD + 192 + blk * 16, v1);
-                        tc05::tmem_wait_ld();
-                        // h goes straight into down's packed B: pass pc.pi, group
-                        // j0 / 64, row n = token slot, column j0 % 64 (swizzled)
-                        const int j0 = tile * 128 + r128;
-                        const int kq = j0 & 63;
-                        uint16_t *hp = a.h + ((size_t)pc.pi * (a.I / 64) + (j0 >> 6)) * (kPqBGroup / 2);
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const int n = blk * 16 + c;
-                            float hv = 0.f;  // padded rows stay zero
-                            if (n < ntok) {
-                                const float g0 = gs[c];
-                                const float u0 = __uint_as_float(v0[c]) + __uint_as_float(v1[c]);
-                                hv = g0 / (1.0f + expf(-g0)) * u0;
-                            }
-                            const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-                            const int kp = kperm_pos(kq);  // down's B in the dequant's K order
-                            hp[n * 64 + (((kp >> 3) ^ (n & 7)) << 3) + (kp & 7)] =
-                                *reinterpret_cast<const uint16_t *>(&hb);
-                        }
-                    }
-                } else {
-                    const int row = tile * 256 + tt * 128 + r128;
-                    for (int blk = 0; blk < nblk; ++blk) {
-                        uint32_t d[16], d2[16];
-                        tc05::tmem_ld16(tmem + lane_base + kPqD + tt * 128 + blk * 16, d);
-                        tc05::tmem_ld16(tmem + lane_base + kPqD + tt * 128 + 64 + blk * 16, d2);
-                        tc05::tmem_wait_ld();
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const int n = blk * 16 + c;
-                            if (n < ntok) {
-                                const int p = a.list[pc.beg + n];
-                                a.y[(size_t)p * a.H + row] = __uint_as_float(d[c]) + __uint_as_float(d2[c]);
-                            }
-                        }
-                    }
-                }
-                tc05::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) pq_arrive(&sh.dfree);
-                ++items_done;
-            }
+            tc05::tmem_st32(a_col + (uint32_t)((ga + 1) * 64), A);
+            tc05::tmem_wait_st();
+            tc05::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) pq_arrive(&sh.afull[set][tt]);
         }
     }
     __syncthreads();
