@@ -449,11 +449,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(PfArgs a) {
 //   * 4 MMA warps, one per (tile, half of the stage's groups): one thread of
 //     each issues 2 groups x 4 MMAs (M 128, N = tokens rounded up to 16,
 //     K 16) per stage into its own accumulator, which runs over the whole
-//     item, and commits each group to the A slot's barrier of its tile, each
-//     stage to the B slot's, each item to the accumulator barrier. A thread
-//     issues about one tcgen05.mma per ~120 cycles whatever N, so the
-//     stage's 32 MMAs need the four issuers (and four accumulators, to keep
-//     each accumulation order fixed);
+//     item. Per stage it waits once (the A groups of its tile and set
+//     stored, which the dequant warps signal only after the stage's B tiles
+//     have landed) and commits once (freeing its A slots and its use of the
+//     B slot); after an item it commits to the accumulator barrier. An
+//     mbarrier operation of the issuing thread waits for its MMAs in flight,
+//     so the fewer per MMA the better; four issuers (four accumulators, so
+//     that each accumulation order stays fixed) keep the tensor pipe fed;
 //   * 4 epilogue warps, one per lane quarter: they look up the next item's
 //     pass (and, for down, its token rows) while the item runs, then read
 //     the accumulators back with tcgen05.ld, add each tile's two halves and
@@ -731,9 +733,9 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
                 const int it = j / ns, kb = j % ns;
                 pc.to(a, (i0 + it * istep) / a.tiles);
                 const uint32_t idesc = tc05::idesc_bf16_f32(128, (pc.ntok + 15) & ~15);
-                ok = pq_wait(sh, &sh.bfull[bs], (uint32_t)((j / kPqBStages) & 1));
                 // the accumulators are free once the epilogue has read the last item
-                if (ok && kb == 0 && it > 0) ok = pq_wait(sh, &sh.dfree, (uint32_t)((it - 1) & 1));
+                if (kb == 0 && it > 0) ok = pq_wait(sh, &sh.dfree, (uint32_t)((it - 1) & 1));
+                // A of this stage stored, and its B landed (the dequant warps check that)
                 if (ok) ok = pq_wait(sh, &sh.afull[hk][t], (uint32_t)(j & 1));
                 if (!ok) break;
                 tc05::fence_after_sync();
@@ -863,9 +865,13 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
             // this warp has read its rows of the stage: the weight slot may refill
             if (lane == 0) pq_arrive(&sh.wempty[ws]);
             tc05::tmem_st32(a_col + (uint32_t)((ga + 1) * 64), A);
+            // the MMA warps wait on one barrier a stage: the first lane quarter
+            // also checks that the stage's B tiles have landed
+            if (q == 0) ok = pq_wait_warp(sh, &sh.bfull[j % kPqBStages], (uint32_t)((j / kPqBStages) & 1));
             tc05::tmem_wait_st();
             tc05::fence_before_sync();
             __syncwarp();
+            if (!ok) break;
             if (lane == 0) pq_arrive(&sh.afull[set][tt]);
         }
     }
