@@ -6,21 +6,22 @@
 // fp32 (colibri PR #418, "qmatmul_gate_up.comp + coli_vk_gate_up",
 // "coli_vk_expert_group", "grouped scales in the Vulkan kernels"). What
 // changes is how the operands arrive: one producer warp fills a 4-stage ring
-// guarded by mbarriers. A stage holds 256 weight rows x 4 groups (two 3-D
-// tensor-map loads of 128 rows x 128 bytes, 128-byte swizzle), their scales,
-// and the activation units and factors of the same 4 groups for every token
-// of the pass (one bulk copy each per token), so the 16 consumer warps spend
-// no instructions on copies and never wait on a block barrier inside an item.
-// Consumer warp w owns stage rows 16w..16w+15: for gate+up warps 0-7 hold
-// gate rows and warps 8-15 the up rows of the same 128 hidden units; for
-// down, 256 consecutive rows. The dense int4-gs64 GEMV (qmv_int4_gs) runs as
-// a third mode: one matrix, its S tokens in passes of 8, row tiles of 256.
+// guarded by mbarriers. A stage holds 256 weight rows x 4 groups (tensor-map
+// loads of 128 or 256 rows x 128 bytes, 128-byte swizzle), their scales, and
+// the activation units and factors of the same 4 groups for every token of
+// the pass (one bulk copy of the pass-packed block, or one per token), so
+// the 8 consumer warps spend no instructions on copies and never wait on a
+// block barrier inside an item. Consumer warp w owns two 16-row tiles, stage
+// rows 16w..16w+15 and 128+16w..128+16w+15: for gate+up the gate rows and
+// the up rows of the same 16 hidden units; for down and dense, two row tiles.
+// The dense int4-gs64 GEMV (qmv_int4_gs) runs as a third mode: one matrix (or
+// a pair sharing x), its S tokens in passes of 8, row tiles of 256.
 //
-// Work split: the stages of all items (item-major) are shared out evenly over
-// the CTAs, so every SM streams the same number of weight bytes. An item
-// whose stages fall to several CTAs is finished by the last of them to
-// arrive (an atomic counter; nobody waits for anybody), which adds the
-// partial sums in CTA order and writes the item.
+// Work split: the stages of all items (item-major) are shared out over the
+// CTAs, by the grouping kernel's cost-balanced plan when there is one, else
+// evenly. An item whose stages fall to several CTAs is finished by the last
+// of them to arrive (an acquire-release counter; nobody waits for anybody),
+// which adds the partial sums in CTA order and writes the item.
 //
 // Every mbarrier wait is bounded. A consumer warp whose wait runs out stops
 // waiting but keeps computing (on whatever the slot holds) and keeps every
