@@ -103,6 +103,8 @@ __device__ __forceinline__ void block_scan3(int a, int b, int c, int &ea, int &e
 // S * wpre[u] (wpre: exclusive scan of the experts' pass weights); CTA b
 // starts at cost C * b / g of the total C, inside the pass that cost falls
 // in, at the first stage whose start is not below it.
+constexpr int kGroupTile = 2048;  // ids staged in shared memory per round of the list fill
+
 __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets,
                           int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                           int32_t *status, int pass_tok, const uint32_t *res = nullptr,
@@ -194,20 +196,29 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
             }
         }
     }
-    __syncthreads();
-    if (warp == 0) {
-        const unsigned lt = (1u << lane) - 1u;
-        for (int base = 0; base < P; base += 32) {
-            const int p = base + lane;
-            int e = p < P ? ids[p] : -1;
-            const bool valid = p < P && e >= 0 && e < E && expert_served(res, e);
-            if (!valid) e = -1 - lane;  // unique key: never matches another lane
-            const unsigned mask = __match_any_sync(0xFFFFFFFFu, e);
-            const int rank = __popc(mask & lt);
-            if (valid) list[run[e] + rank] = p;
-            __syncwarp();
-            if (valid && rank == 0) run[e] += __popc(mask);
-            __syncwarp();
+    // The list, in pair order within each expert: the CTA stages the ids in
+    // shared memory a tile at a time, and warp 0 places them 32 at a time
+    // (the global loads no longer sit on warp 0's serial path).
+    __shared__ int32_t tile_ids[kGroupTile];
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base0 = 0; base0 < P; base0 += kGroupTile) {
+        const int n = min(kGroupTile, P - base0);
+        __syncthreads();  // warp 0 is done with the previous tile (and run[] is set)
+        for (int i = tid; i < n; i += blockDim.x) tile_ids[i] = ids[base0 + i];
+        __syncthreads();
+        if (warp == 0) {
+            for (int base = 0; base < n; base += 32) {
+                const int i = base + lane, p = base0 + i;
+                int e = i < n ? tile_ids[i] : -1;
+                const bool valid = i < n && e >= 0 && e < E && expert_served(res, e);
+                if (!valid) e = -1 - lane;  // unique key: never matches another lane
+                const unsigned mask = __match_any_sync(0xFFFFFFFFu, e);
+                const int rank = __popc(mask & lt);
+                if (valid) list[run[e] + rank] = p;
+                __syncwarp();
+                if (valid && rank == 0) run[e] += __popc(mask);
+                __syncwarp();
+            }
         }
     }
     if (tid == 0 && bad) atomicOr(status, 1);
@@ -673,6 +684,11 @@ __global__ void __launch_bounds__(32 * kMoeWarps, 1)
 
 // ------------------------------------------------------------------ combine
 
+// out[t] = sum_j w[t][j] * y[t*k + j] over the served slots, j in order (one
+// fused multiply-add each). V = 4: four consecutive outputs a thread with
+// 16-byte loads (H a multiple of 4, out 16-byte aligned), so the k loads of
+// a thread are in flight together.
+template <int V>
 __global__ void __launch_bounds__(256)
     k_combine(const float *__restrict__ y, const int32_t *__restrict__ ids,
               const float *__restrict__ w, int k, int E, int H, float *__restrict__ out,
@@ -680,15 +696,32 @@ __global__ void __launch_bounds__(256)
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.y;
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int i = (blockIdx.x * blockDim.x + threadIdx.x) * V;
     if (i >= H) return;
-    float o = 0.0f;
+    float o[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) o[v] = 0.0f;
     for (int j = 0; j < k; ++j) {
         const int p = t * k + j;
         const int e = ids[p];
-        if (e >= 0 && e < E && expert_served(res, e)) o = fmaf(w[p], y[(size_t)p * H + i], o);
+        if (e >= 0 && e < E && expert_served(res, e)) {
+            const float wp = w[p];
+            const float *yr = y + (size_t)p * H + i;
+            if (V == 4) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(yr);
+                o[0] = fmaf(wp, v4.x, o[0]);
+                o[1] = fmaf(wp, v4.y, o[1]);
+                o[2] = fmaf(wp, v4.z, o[2]);
+                o[3] = fmaf(wp, v4.w, o[3]);
+            } else {
+                o[0] = fmaf(wp, yr[0], o[0]);
+            }
+        }
     }
-    out[(size_t)t * H + i] = o;
+    if (V == 4)
+        *reinterpret_cast<float4 *>(out + (size_t)t * H + i) = make_float4(o[0], o[1], o[2], o[3]);
+    else
+        out[(size_t)t * H + i] = o[0];
 }
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -779,7 +812,10 @@ cudaError_t launch_down(const MoeDims &m, const void *hcells, const float *hfac,
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int T, int k, int E,
                            int H, float *out, cudaStream_t st, bool pdl, const uint32_t *res) {
     if (T == 0) return cudaSuccess;
-    return launch(k_combine, dim3((H + 255) / 256, T), dim3(256), 0, st, pdl, y, ids, w, k, E, H,
+    if (H % 4 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0)
+        return launch(k_combine<4>, dim3((H / 4 + 255) / 256, T), dim3(256), 0, st, pdl, y, ids, w,
+                      k, E, H, out, res);
+    return launch(k_combine<1>, dim3((H + 255) / 256, T), dim3(256), 0, st, pdl, y, ids, w, k, E, H,
                   out, res);
 }
 
