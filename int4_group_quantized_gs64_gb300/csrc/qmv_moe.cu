@@ -91,8 +91,9 @@ __device__ __forceinline__ void block_scan3(int a, int b, int c, int &ea, int &e
 
 // Grouping on one CTA of 1024 threads: counts by shared atomics; block scans
 // give the offsets, the slots of the used experts and the pass offsets (one
-// pass = up to kMaxTok pairs of one expert); a single warp then fills the
-// lists in pair order (ranks from __match_any_sync), keeping them ascending.
+// pass = up to kMaxTok pairs of one expert); then warp w fills the lists of
+// the experts e with e % 32 == w in pair order (ids staged in shared memory,
+// ranks by lane shuffles), keeping them ascending.
 // res: bitmap of the experts this call serves (bit e % 32 of word e / 32), or
 // null for all; pairs of other experts are left out of the lists without
 // error. served (if not null): 1 for each pair that is grouped, else 0.
@@ -196,29 +197,36 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
             }
         }
     }
-    // The list, in pair order within each expert: the CTA stages the ids in
-    // shared memory a tile at a time, and warp 0 places them 32 at a time
-    // (the global loads no longer sit on warp 0's serial path).
+    // The list, in pair order within each expert. The CTA stages the ids in
+    // shared memory a tile at a time; warp w places the pairs of the experts
+    // e with e % 32 == w, walking the tile 32 pairs at a time, so each run[e]
+    // has one writer and the lists stay in pair order.
     __shared__ int32_t tile_ids[kGroupTile];
-    const unsigned lt = (1u << lane) - 1u;
     for (int base0 = 0; base0 < P; base0 += kGroupTile) {
         const int n = min(kGroupTile, P - base0);
-        __syncthreads();  // warp 0 is done with the previous tile (and run[] is set)
+        __syncthreads();  // the previous tile is placed (and run[] is set)
         for (int i = tid; i < n; i += blockDim.x) tile_ids[i] = ids[base0 + i];
         __syncthreads();
-        if (warp == 0) {
-            for (int base = 0; base < n; base += 32) {
-                const int i = base + lane, p = base0 + i;
-                int e = i < n ? tile_ids[i] : -1;
-                const bool valid = i < n && e >= 0 && e < E && expert_served(res, e);
-                if (!valid) e = -1 - lane;  // unique key: never matches another lane
-                const unsigned mask = __match_any_sync(0xFFFFFFFFu, e);
-                const int rank = __popc(mask & lt);
-                if (valid) list[run[e] + rank] = p;
-                __syncwarp();
-                if (valid && rank == 0) run[e] += __popc(mask);
-                __syncwarp();
+        for (int base = 0; base < n; base += 32) {
+            const int i = base + lane, p = base0 + i;
+            const int e = i < n ? tile_ids[i] : -1;
+            const bool mine = i < n && e >= 0 && e < E && (e & 31) == warp && expert_served(res, e);
+            unsigned m = __ballot_sync(0xFFFFFFFFu, mine);
+            if (m == 0) continue;
+            // rank among the lower lanes with the same expert, and whether
+            // this lane is the expert's last in the chunk
+            int rank = 0, after = 0;
+            while (m) {
+                const int l = __ffs(m) - 1;
+                m &= m - 1;
+                const int el = __shfl_sync(0xFFFFFFFFu, e, l);
+                rank += (l < lane && el == e) ? 1 : 0;
+                after += (l > lane && el == e) ? 1 : 0;
             }
+            if (mine) list[run[e] + rank] = p;
+            __syncwarp();
+            if (mine && after == 0) run[e] += rank + 1;
+            __syncwarp();
         }
     }
     if (tid == 0 && bad) atomicOr(status, 1);
