@@ -63,6 +63,30 @@ def test_prefill_shapes(T, k, E, H, I):
     assert norm_err(out, ref["out"], ref["den"]) <= TOL_BF16
 
 
+@pytest.mark.parametrize("lo,hi", [(-4.0, -0.55), (-3.0, -0.7), (-1.0, 0.5), (-0.58, -0.5)])
+def test_prefill_scale_ranges(lo, hi):
+    """Group scales 10^U(lo, hi): the tensor-map kernel's dequant takes its
+    one-multiply-add form for a warp only while all 32 rows' scales lie in
+    [2^-120, 1/4), else the two-step form; both must give the oracle's result:
+    mixed warps, all warps in the first form, all in the second (large
+    scales, scales just above 1/4)."""
+    rng = np.random.default_rng(int(100 * (hi - lo)))
+    E, H, I, T, k = 4, 256, 256, 48, 2
+    wts = rand_experts(rng, E, H, I)
+    for key in ("gu_s", "dn_s"):
+        wts[key] = (10.0 ** rng.uniform(lo, hi, size=wts[key].shape)).astype(np.float32)
+    m = q.MoeInt4Weights.from_numpy(wts)
+    assert q.moe_weight_path(m) == 1
+    xbits = datagen.normal_bf16_bits(7, (T, H), start=3)
+    logits = rng.normal(size=(T, E)).astype(np.float32)
+    ids, w = oracle.route_topk(logits, k)
+    w = w.astype(np.float32)
+    out, status = run_prefill(m, xbits, ids, w)
+    assert status == 0
+    ref = oracle.moe_ffn(wts, datagen.bf16_bits_to_f32(xbits).astype(np.float64), ids, w)
+    assert norm_err(out, ref["out"], ref["den"]) <= TOL_BF16
+
+
 def pass_cells(ids, E, pass_tok):
     """Per token, the cells its pairs fall in: (expert, pass) for every pair,
     plus (expert, pass, "last") for the pair in a pass's last column. An
