@@ -321,6 +321,10 @@ __device__ void split_rows_smem(const float *__restrict__ x, int K, int ntok, ui
 // matrix (w2 != null: a pair sharing x) its row tiles follow the first's in
 // the same item sequence. CTA 0 clears zero[0 .. nzero) (the caller's status
 // word and counters).
+// Weight stages per warp ring: with the 64 KB unit table, 2 stages keep the
+// block under half the SM's shared memory, so two blocks stay resident.
+constexpr int ks_x_stages(int budget) { return budget > 32 * 1024 ? 2 : 4; }
+
 template <bool kInt8, int kBudget>
 __global__ void __launch_bounds__(32 * kKsWarps)
     k_dense_ks_x(const uint8_t *__restrict__ w, const float *__restrict__ scales, int N, int K,
@@ -340,16 +344,17 @@ __global__ void __launch_bounds__(32 * kKsWarps)
     const size_t rowBytes = kInt8 ? (size_t)K : (size_t)K / 2;
 
     PairSplitTile<kInt8> tile{w, w2, scales, scales2, rowBytes, N, N2, items0, G, i0, ga};
-    WarpStream<kInt8, kKsStages, PairSplitTile<kInt8>> ws;
-    ws.init(smem + warp * kKsRing, tile, gb - ga, gb > ga ? i1 - i0 : 0, warp, lane);
+    constexpr int kNS = ks_x_stages(kBudget), kRing = kNS * kStageBytes;
+    WarpStream<kInt8, kNS, PairSplitTile<kInt8>> ws;
+    ws.init(smem + warp * kRing, tile, gb - ga, gb > ga ? i1 - i0 : 0, warp, lane);
     ws.prologue();  // weights are call inputs: safe to read before the wait
 
     pdl_wait();     // x may come from the previous kernel
     pdl_trigger();
     if (zero && blockIdx.x == 0)
         for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
-    uint4 *cells = reinterpret_cast<uint4 *>(smem + kKsWarps * kKsRing);
-    float *fac = reinterpret_cast<float *>(smem + kKsWarps * kKsRing + kBudget);
+    uint4 *cells = reinterpret_cast<uint4 *>(smem + kKsWarps * kRing);
+    float *fac = reinterpret_cast<float *>(smem + kKsWarps * kRing + kBudget);
     split_rows_smem<kInt8>(x, K, ntok, cells, fac);
     __syncthreads();
     int cslot = 0;
@@ -404,7 +409,7 @@ cudaError_t launch_ks_x_b(const uint8_t *w, const float *scales, int N, int K, c
                           float *y, uint16_t *ybf, int S, int32_t *zero, int nzero,
                           cudaStream_t st, const uint8_t *w2, const float *scales2, int N2,
                           float *y2) {
-    const size_t smem_ks = (size_t)kKsWarps * kKsRing + kBudget + kBudget / 64;
+    const size_t smem_ks = (size_t)kKsWarps * ks_x_stages(kBudget) * kStageBytes + kBudget + kBudget / 64;
     cudaError_t e = set_smem(k_dense_ks_x<kInt8, kBudget>, smem_ks);
     if (e != cudaSuccess) return e;
     const int items = (N + 15) / 16 + (w2 ? (N2 + 15) / 16 : 0);
