@@ -86,6 +86,7 @@ cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t 
 // Shared memory of the grouping kernel when it also routes (logits != null):
 // every CTA routes the T tokens itself, so T * k pairs and E logits a warp.
 size_t route_smem_bytes(int T, int E, int k);
+size_t group_smem_bytes(int E);  // the grouping's per-warp expert counts, 32 x E ints
 cudaError_t launch_passes(const int32_t *offsets, const int32_t *uexp, const int32_t *n_used,
                           int32_t *pass_ofs, cudaStream_t st, bool pdl);
 // Activation rows [R][K] fp32 -> fragment cells [R][K/64][16] uint4 + factors [R][K/64],

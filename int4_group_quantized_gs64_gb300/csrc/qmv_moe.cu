@@ -91,9 +91,8 @@ __device__ __forceinline__ void block_scan3(int a, int b, int c, int &ea, int &e
 
 // Grouping on one CTA of 1024 threads: counts by shared atomics; block scans
 // give the offsets, the slots of the used experts and the pass offsets (one
-// pass = up to kMaxTok pairs of one expert); then warp w fills the lists of
-// the experts e with e % 32 == w in pair order (ids staged in shared memory,
-// ranks by lane shuffles), keeping them ascending.
+// pass = up to kMaxTok pairs of one expert); then the warps place the pairs
+// in parallel (below), keeping the lists ascending.
 // res: bitmap of the experts this call serves (bit e % 32 of word e / 32), or
 // null for all; pairs of other experts are left out of the lists without
 // error. served (if not null): 1 for each pair that is grouped, else 0.
@@ -104,13 +103,11 @@ __device__ __forceinline__ void block_scan3(int a, int b, int c, int &ea, int &e
 // S * wpre[u] (wpre: exclusive scan of the experts' pass weights); CTA b
 // starts at cost C * b / g of the total C, inside the pass that cost falls
 // in, at the first stage whose start is not below it.
-constexpr int kGroupTile = 2048;  // ids staged in shared memory per round of the list fill
-
 __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets,
                           int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                           int32_t *status, int pass_tok, const uint32_t *res = nullptr,
                           uint8_t *served = nullptr, const PlanArgs *pl = nullptr) {
-    __shared__ int32_t cnt[1024], run[1024], tot[96];
+    __shared__ int32_t cnt[1024], tot[96];
     __shared__ int bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) bad = 0;
@@ -131,7 +128,6 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
     block_scan3(c, f, np, ec, ef, ep, tot);
     if (tid < E) {
         offsets[tid] = ec;
-        run[tid] = ec;
         if (f) {
             uexp[ef] = tid;
             if (pass_ofs) pass_ofs[ef] = ep;
@@ -197,24 +193,26 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
             }
         }
     }
-    // The list, in pair order within each expert. The CTA stages the ids in
-    // shared memory a tile at a time; warp w places the pairs of the experts
-    // e with e % 32 == w, walking the tile 32 pairs at a time, so each run[e]
-    // has one writer and the lists stay in pair order.
-    __shared__ int32_t tile_ids[kGroupTile];
-    for (int base0 = 0; base0 < P; base0 += kGroupTile) {
-        const int n = min(kGroupTile, P - base0);
-        __syncthreads();  // the previous tile is placed (and run[] is set)
-        for (int i = tid; i < n; i += blockDim.x) tile_ids[i] = ids[base0 + i];
+    // The list, in pair order within each expert. Up to 1024 pairs (a decode
+    // micro-batch), warp w places the pairs of the experts e with e % 32 == w,
+    // walking all pairs 32 at a time, so each expert's running position has one
+    // writer. More pairs: warp w takes the w-th 32nd of the pairs; hist[w][e]
+    // counts its pairs of expert e, a scan over w turns the counts into each
+    // segment's first list position for e, and the warp places its pairs in
+    // order, 32 at a time. Ranks among the lanes come from shuffles. The
+    // positions live in the dynamic shared memory (32 x E ints).
+    extern __shared__ int32_t group_smem[];
+    __syncthreads();  // the scan's reads of tot[] are done; routing's shared rows too
+    if (P <= 1024) {
+        int32_t *run = group_smem;
+        if (tid < E) run[tid] = ec;
         __syncthreads();
-        for (int base = 0; base < n; base += 32) {
-            const int i = base + lane, p = base0 + i;
-            const int e = i < n ? tile_ids[i] : -1;
-            const bool mine = i < n && e >= 0 && e < E && (e & 31) == warp && expert_served(res, e);
+        for (int base = 0; base < P; base += 32) {
+            const int p = base + lane;
+            const int e = p < P ? ids[p] : -1;
+            const bool mine = p < P && e >= 0 && e < E && (e & 31) == warp && expert_served(res, e);
             unsigned m = __ballot_sync(0xFFFFFFFFu, mine);
             if (m == 0) continue;
-            // rank among the lower lanes with the same expert, and whether
-            // this lane is the expert's last in the chunk
             int rank = 0, after = 0;
             while (m) {
                 const int l = __ffs(m) - 1;
@@ -226,6 +224,42 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
             if (mine) list[run[e] + rank] = p;
             __syncwarp();
             if (mine && after == 0) run[e] += rank + 1;
+            __syncwarp();
+        }
+    } else {
+        int32_t *hist = group_smem, *hw = group_smem + warp * E;
+        const int seg = (P + 31) / 32, s0 = min(P, warp * seg), s1 = min(P, s0 + seg);
+        for (int i = tid; i < 32 * E; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+        for (int p = s0 + lane; p < s1; p += 32) {
+            const int e = ids[p];
+            if (e >= 0 && e < E && expert_served(res, e)) atomicAdd(&hw[e], 1);
+        }
+        __syncthreads();
+        if (tid < E) {
+            int at = ec;
+            for (int w = 0; w < 32; ++w) {
+                const int h = hist[w * E + tid];
+                hist[w * E + tid] = at;
+                at += h;
+            }
+        }
+        __syncthreads();
+        for (int base = s0; base < s1; base += 32) {
+            const int p = base + lane;
+            int e = p < s1 ? ids[p] : -1;
+            const bool valid = p < s1 && e >= 0 && e < E && expert_served(res, e);
+            if (!valid) e = -1 - lane;  // unique key: never matches another lane
+            int rank = 0, after = 0;
+#pragma unroll
+            for (int l = 0; l < 32; ++l) {
+                const int el = __shfl_sync(0xFFFFFFFFu, e, l);
+                rank += (l < lane && el == e) ? 1 : 0;
+                after += (l > lane && el == e) ? 1 : 0;
+            }
+            if (valid) list[hw[e] + rank] = p;
+            __syncwarp();
+            if (valid && after == 0) hw[e] += rank + 1;
             __syncwarp();
         }
     }
@@ -755,7 +789,10 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids,
 
 cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int32_t *list,
                          int32_t *uexp, int32_t *n_used, int32_t *status, cudaStream_t st) {
-    return launch(k_group_split, dim3(1), dim3(1024), 0, st, false, ids, P, E, offsets, list, uexp,
+    const size_t smem = group_smem_bytes(E);
+    cudaError_t e = set_smem(k_group_split, std::max(smem, (size_t)49 * 1024));
+    if (e != cudaSuccess) return e;
+    return launch(k_group_split, dim3(1), dim3(1024), smem, st, false, ids, P, E, offsets, list, uexp,
                   n_used, (int32_t *)nullptr, status, (const float *)nullptr, 64,
                   (uint4 *)nullptr, (float *)nullptr, (int)kMaxTok, 1, 0, (int32_t *)nullptr, 0,
                   (const uint32_t *)nullptr, (uint8_t *)nullptr, (const float *)nullptr,
@@ -770,10 +807,13 @@ cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t 
                                const float *logits, int32_t *ids_out, float *w_out, bool sub,
                                const PlanArgs *plan) {
     const int C = (H / kGroup + 31) / 32;  // CTAs per token row
-    const size_t smem = logits ? route_smem_bytes(T, E, k) : 0;
-    if (smem) {
-        // with ~33 KB of static shared memory, even a small dynamic part
-        // needs the opt-in (set_smem only opts in above 48 KB)
+    // dynamic shared memory: the routing rows and ids, or the grouping's
+    // per-warp expert counts, whichever is larger (the counts reuse the
+    // routing rows after routing)
+    const size_t smem = std::max(logits ? route_smem_bytes(T, E, k) : 0, group_smem_bytes(E));
+    {
+        // with the static shared memory, even a small dynamic part needs the
+        // opt-in (set_smem only opts in above 48 KB)
         cudaError_t e = set_smem(k_group_split, std::max(smem, (size_t)49 * 1024));
         if (e != cudaSuccess) return e;
     }
@@ -783,6 +823,8 @@ cudaError_t launch_group_split(const int32_t *ids, int T, int k, int E, int32_t 
                   (packed ? 1 : 0) | ((packed || sub) ? 2 : 0), zero, nzero, res, served, logits,
                   ids_out, w_out, plan ? *plan : PlanArgs{});
 }
+
+size_t group_smem_bytes(int E) { return (size_t)32 * E * sizeof(int32_t); }
 
 size_t route_smem_bytes(int T, int E, int k) {
     return (size_t)32 * E * sizeof(float) + (size_t)T * k * sizeof(int32_t);
