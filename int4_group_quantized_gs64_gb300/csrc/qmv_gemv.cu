@@ -265,14 +265,16 @@ __global__ void __launch_bounds__(32 * kKsWarps)
 // the group's max |v| takes two shuffles between the four threads. Same
 // arithmetic as k_split.
 template <bool kInt8>
+// Groups [ga, gb) of the ntok rows, split by the threads [t0, t0 + nthr) (a
+// multiple of 4 threads: quad q of a group takes its values 16 q .. 16 q + 15).
 __device__ void split_rows_smem(const float *__restrict__ x, int K, int ntok, uint4 *cells,
-                                float *fac) {
-    const int G = K / kGroup, nq = ntok * G * 4;
+                                float *fac, int ga, int gb, int t0, int nthr) {
+    const int G = K / kGroup, ng = gb - ga, nq = ntok * ng * 4;
     const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-    for (int base = 0; base < nq; base += blockDim.x) {  // uniform trip count: shuffles below
-        const int idx = base + threadIdx.x;
+    for (int base = 0; base < nq; base += nthr) {  // uniform trip count: shuffles below
+        const int idx = base + (int)threadIdx.x - t0;
         const bool valid = idx < nq;
-        const int s = valid ? idx / (G * 4) : 0, g = valid ? (idx >> 2) % G : 0, q = idx & 3;
+        const int s = valid ? idx / (ng * 4) : 0, g = valid ? ga + (idx >> 2) % ng : 0, q = idx & 3;
         const float *src = x + (size_t)s * K + g * kGroup + 16 * q;
         float v[16];
         if (valid && vec) {
@@ -355,8 +357,9 @@ __global__ void __launch_bounds__(32 * kKsWarps)
         for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
     uint4 *cells = reinterpret_cast<uint4 *>(smem + kKsWarps * kRing);
     float *fac = reinterpret_cast<float *>(smem + kKsWarps * kRing + kBudget);
-    split_rows_smem<kInt8>(x, K, ntok, cells, fac);
-    __syncthreads();
+    // each warp converts the groups of its own K share: no block barrier
+    split_rows_smem<kInt8>(x, K, ntok, cells, fac, ga, gb, warp * 32, 32);
+    __syncwarp();
     int cslot = 0;
     const int sb = min(gid >> 1, ntok - 1), sd = min(q, ntok - 1);
     const uint4 *bp0 = cells + (sb * G + ga) * 16 + q * 2 + (gid & 1);
