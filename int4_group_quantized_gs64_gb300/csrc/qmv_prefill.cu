@@ -446,8 +446,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(PfArgs a) {
 //     folded in and stores it to the group's A slot of its tile in tensor
 //     memory; the first group's store drains while the second group is
 //     dequantized;
-//   * 4 MMA warps, one per (tile, half of the stage's groups): one thread of
-//     each issues 2 groups x 4 MMAs (M 128, N = tokens rounded up to 16,
+//   * 4 MMA warps, one per (tile, half of the stage's groups): one elected
+//     lane of each issues 2 groups x 4 MMAs (M 128, N = tokens rounded up to 16,
 //     K 16) per stage into its own accumulator, which runs over the whole
 //     item. Per stage it waits once (the A groups of its tile and set
 //     stored, which the dequant warps signal only after the stage's B tiles
@@ -579,6 +579,30 @@ __device__ __forceinline__ void pq_bulk(uint32_t dst, const void *src, uint32_t 
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
             "r"(dst),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(mbar)
+        : "memory");
+}
+
+// tcgen05.mma (A in tensor memory) from a warp-uniform branch: every lane of
+// the warp runs the instruction stream and elect.sync picks the lane that
+// issues, so the operands the whole warp computes stay warp-uniform. A probe
+// issued ~34 cycles per MMA this way against ~66 from a loop that a single
+// lane runs (and ~16 cycles per MMA of tensor pipe at N 32 with two issuers).
+__device__ __forceinline__ void pq_mma_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Commit of the MMAs issued by pq_mma_elect: with all 32 lanes active the
+// same lane is elected, the one whose MMAs the commit tracks.
+__device__ __forceinline__ void pq_commit_elect(uint64_t *mbar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            tc05::smem_addr(mbar))
         : "memory");
 }
 
@@ -715,46 +739,46 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
         }
     } else if (warp >= kPqMma) {
         // ---------------- MMA issue: warp kPqMma + m: tile m / 2, groups 2(m % 2), +1.
-        // Every mbarrier operation of the issuing thread after an MMA costs a
-        // few hundred cycles (it waits for the MMAs issued so far to be taken
-        // up), so a stage has one wait for its A groups and one commit.
+        // The whole warp runs the loop (warp-uniform operands); one elected
+        // lane issues the MMAs and the commits. Every mbarrier operation of
+        // the issuing lane after an MMA costs a few hundred cycles (it waits
+        // for the MMAs issued so far to be taken up), so a stage has one wait
+        // for its A groups and one commit.
         const int m = warp - kPqMma, t = m >> 1, hk = m & 1;
-        if (lane == 0) {
-            PqCursor pc;
-            if (total > 0) pc.seek(a, nu, i0 / a.tiles);
-            const uint32_t dacc = tmem + kPqD + (uint32_t)(m * 64);
-            const uint32_t a0 = tmem + kPqA + (uint32_t)(2 * hk * 64 + t * 32);
-            // B descriptor of slot 0, group 2 hk; +1 in the address field = 16 bytes
-            const uint64_t b0 = tc05::sdesc_sw128(
-                tc05::smem_addr(ring + kPqOffBRing + 2 * hk * kPqBGroup));
-            bool ok = true;
-            for (int j = 0; j < total && ok; ++j) {
-                const int bs = j % kPqBStages;
-                const int it = j / ns, kb = j % ns;
-                pc.to(a, (i0 + it * istep) / a.tiles);
-                const uint32_t idesc = tc05::idesc_bf16_f32(128, (pc.ntok + 15) & ~15);
-                // the accumulators are free once the epilogue has read the last item
-                if (kb == 0 && it > 0) ok = pq_wait(sh, &sh.dfree, (uint32_t)((it - 1) & 1));
-                // A of this stage stored, and its B landed (the dequant warps check that)
-                if (ok) ok = pq_wait(sh, &sh.afull[hk][t], (uint32_t)(j & 1));
-                if (!ok) break;
-                tc05::fence_after_sync();
-                const uint64_t bd = b0 + (uint64_t)((bs * kPqBStage) >> 4);
+        PqCursor pc;
+        if (total > 0) pc.seek(a, nu, i0 / a.tiles);
+        const uint32_t dacc = tmem + kPqD + (uint32_t)(m * 64);
+        const uint32_t a0 = tmem + kPqA + (uint32_t)(2 * hk * 64 + t * 32);
+        // B descriptor of slot 0, group 2 hk; +1 in the address field = 16 bytes
+        const uint64_t b0 = tc05::sdesc_sw128(
+            tc05::smem_addr(ring + kPqOffBRing + 2 * hk * kPqBGroup));
+        bool ok = true;
+        for (int j = 0; j < total && ok; ++j) {
+            const int bs = j % kPqBStages;
+            const int it = j / ns, kb = j % ns;
+            pc.to(a, (i0 + it * istep) / a.tiles);
+            const uint32_t idesc = tc05::idesc_bf16_f32(128, (pc.ntok + 15) & ~15);
+            // the accumulators are free once the epilogue has read the last item
+            if (kb == 0 && it > 0) ok = pq_wait_warp(sh, &sh.dfree, (uint32_t)((it - 1) & 1));
+            // A of this stage stored, and its B landed (the dequant warps check that)
+            if (ok) ok = pq_wait_warp(sh, &sh.afull[hk][t], (uint32_t)(j & 1));
+            if (!ok) break;
+            tc05::fence_after_sync();
+            const uint64_t bd = b0 + (uint64_t)((bs * kPqBStage) >> 4);
 #pragma unroll
-                for (int gg = 0; gg < 2; ++gg)
+            for (int gg = 0; gg < 2; ++gg)
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc05::mma_ts(dacc, a0 + (uint32_t)(gg * 64 + kk * 8),
-                                     bd + (uint64_t)((gg * kPqBGroup + kk * 32) >> 4), idesc,
-                                     (kb > 0 || gg > 0 || kk > 0) ? 1u : 0u);
-                // frees this issuer's A slots and its use of the B slot
-                tc05::mma_commit(&sh.sdone[m][bs]);
-                if (kb == ns - 1) tc05::mma_commit(&sh.dfull);
-            }
-            // the MMAs still in flight must finish before the tensor memory is freed
-            tc05::mma_commit(&sh.mdone[m]);
-            pq_drain(&sh.mdone[m], 0);
+                for (int kk = 0; kk < 4; ++kk)
+                    pq_mma_elect(dacc, a0 + (uint32_t)(gg * 64 + kk * 8),
+                                 bd + (uint64_t)((gg * kPqBGroup + kk * 32) >> 4), idesc,
+                                 (kb > 0 || gg > 0 || kk > 0) ? 1u : 0u);
+            // frees this issuer's A slots and its use of the B slot
+            pq_commit_elect(&sh.sdone[m][bs]);
+            if (kb == ns - 1) pq_commit_elect(&sh.dfull);
         }
+        // the MMAs still in flight must finish before the tensor memory is freed
+        pq_commit_elect(&sh.mdone[m]);
+        pq_drain(&sh.mdone[m], 0);
     } else if (warp >= kPqEpi && warp < kPqEpi + 4) {
         // ---------------- epilogue: lane quarter q of both tiles
         const int q = warp & 3, r128 = q * 32 + lane;
