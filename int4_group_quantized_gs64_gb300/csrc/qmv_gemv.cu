@@ -435,6 +435,256 @@ cudaError_t launch_ks_x(const uint8_t *w, const float *scales, int N, int K, con
                                                scales2, N2, y2);
 }
 
+// ------------------------------------------------------------------ int3-g64 on the warp MMA
+//
+// The int3-g64 two-plane rows (24 bytes a group: a 16-byte low plane with
+// element j of word w at bits 2j, then 8 bytes of high bits, element e at bit
+// e % 8 of byte e / 8) through the same single-launch structure as
+// k_dense_ks_x: 8 warps share each 16-row item, warp ks streams an eighth of
+// its groups through a cp.async ring, every block splits x into its own unit
+// table, and the 16 elements a lane quad takes of each group are decoded into
+// exact fp16 (code - 4) in int4's register order, so the int4 activation
+// units and MMA steps serve unchanged.
+
+// A stage: 16 rows x 4 groups (96 bytes a row), rows 112 bytes apart so that
+// a fragment load of the 8 row pairs (28 words apart) touches 8 distinct
+// 4-bank windows; then the 16 x 4 group scales.
+constexpr int kI3Row = 112;
+constexpr int kI3StageW = 16 * kI3Row;
+constexpr int kI3Stage = kI3StageW + 16 * 4 * 4;
+
+// Exact (code - 4) of the 16 elements of one row that a lane quad takes from
+// a group, in int4's register order (dequant_int4_word): p[j] = (e_j, e_j+4)
+// and p[4 + j] = (e_8+j, e_12+j), j = 0..3, first element in the low half.
+// lo: their low-plane word (e_j at bits 2j); hs: their 16 high bits (e_j at
+// bit j). The low bits of pair j are left at bits 2j (a byte spread puts
+// e_j+4 16 bits above e_j) and the high bit is moved to 2j + 2, so OR-ing
+// both into fp16 1024.0 gives 1024 + 4^j code exactly; one fma by 4^-j with
+// -(1024 * 4^-j + 4) leaves code - 4.
+__device__ __forceinline__ void dequant_int3_16(uint32_t lo, uint32_t hs, uint32_t p[8]) {
+    const uint32_t kBias = 0x64006400u;
+    const uint32_t x[2] = {prmt_u32(lo, 0u, 0x4140u), prmt_u32(lo, 0u, 0x4342u)};
+    // high bits of (e_j, e_j+4) at (j + 2, j + 18); of (e_8+j, e_12+j) likewise
+    const uint32_t h[2] = {((hs << 2) | (hs << 14)) & 0x003C003Cu,
+                           ((hs >> 6) | (hs << 6)) & 0x003C003Cu};
+    const uint32_t kScale[4] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u};  // 4^-j
+    const uint32_t kAdd[4] = {0xE404E404u, 0xDC10DC10u, 0xD440D440u, 0xCD00CD00u};    // -(1024 * 4^-j + 4)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t t = lop3_and_or(x[hh], 0x00030003u << (2 * j), kBias);
+            const uint32_t r = lop3_and_or(h[hh] << j, 0x00040004u << (2 * j), t);
+            p[4 * hh + j] = hfma2_u32(r, kScale[j], kAdd[j]);
+        }
+}
+
+// One warp's 16-row tile of one group, up to 4 tokens (see tile_group_int4):
+// lo / hs of rows gid and gid + 8.
+__device__ __forceinline__ void tile_group_int3(uint32_t lo0, uint32_t hs0, uint32_t lo8,
+                                                uint32_t hs8, const uint4 (&bu)[2], float d[4]) {
+    uint32_t p0[8], p8[8], a[4];
+    dequant_int3_16(lo0, hs0, p0);
+    dequant_int3_16(lo8, hs8, p8);
+    d[0] = d[1] = d[2] = d[3] = 0.0f;
+#pragma unroll
+    for (int mh = 0; mh < 2; ++mh)
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm) {
+            a[0] = p0[4 * mh + 2 * mm];
+            a[1] = p8[4 * mh + 2 * mm];
+            a[2] = p0[4 * mh + 2 * mm + 1];
+            a[3] = p8[4 * mh + 2 * mm + 1];
+            mma_16816(d, a, mm ? bu[mh].z : bu[mh].x, mm ? bu[mh].w : bu[mh].y);
+        }
+}
+
+// Per-warp cp.async stream of 4-group stages over the CTA's items (16-row
+// tiles), groups [ga, ga + 4 nst) of each row. Lane l copies the 16-byte
+// pieces l, l + 32, l + 64 of a stage's 96 (row = piece / 6) and two scales.
+template <int NS>
+struct I3Stream {
+    uint32_t ring_s;
+    const uint8_t *w;
+    const float *sc;
+    size_t rowBytes;
+    int N, G, ga, nst, i0, nitems;
+    int it_item, it_s, slot, lane;
+    const uint8_t *wsrc[3];
+    const float *ssrc[2];
+    uint32_t wdst[3], sdst[2];
+
+    __device__ __forceinline__ void init(uint8_t *ring, const uint8_t *w_, const float *sc_,
+                                         int N_, int G_, int ga_, int nst_, int i0_, int nitems_,
+                                         int lane_) {
+        ring_s = smem_u32(ring);
+        w = w_;
+        sc = sc_;
+        N = N_;
+        G = G_;
+        rowBytes = (size_t)G_ * 24;
+        ga = ga_;
+        nst = nst_;
+        i0 = i0_;
+        nitems = nst_ > 0 ? nitems_ : 0;
+        it_item = it_s = slot = 0;
+        lane = lane_;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const int c = lane + 32 * k;
+            wdst[k] = (c / 6) * kI3Row + (c % 6) * 16;
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) sdst[k] = kI3StageW + (((lane >> 2) + 8 * k) * 4 + (lane & 3)) * 4;
+        if (nitems > 0) set_item(0);
+    }
+    __device__ __forceinline__ void set_item(int item) {
+        const int row0 = (i0 + item) * 16;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const int c = lane + 32 * k;
+            const int row = min(row0 + c / 6, N - 1);  // rows past N: read, never stored
+            wsrc[k] = w + (size_t)row * rowBytes + (size_t)ga * 24 + (c % 6) * 16;
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int row = min(row0 + (lane >> 2) + 8 * k, N - 1);
+            ssrc[k] = sc + (size_t)row * G + ga + (lane & 3);
+        }
+    }
+    __device__ __forceinline__ void issue_next() {
+        if (it_item < nitems) {
+            const uint32_t base = ring_s + slot * kI3Stage;
+#pragma unroll
+            for (int k = 0; k < 3; ++k) cp_async16_s(base + wdst[k], wsrc[k] + it_s * 96);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) cp_async4_s(base + sdst[k], ssrc[k] + 4 * it_s);
+            if (++it_s == nst) {
+                it_s = 0;
+                if (++it_item < nitems) set_item(it_item);
+            }
+        }
+        cp_async_commit();  // possibly empty: keeps the group count uniform
+        slot = (slot + 1 == NS) ? 0 : slot + 1;
+    }
+    __device__ __forceinline__ void prologue() {
+        for (int i = 0; i < NS - 1; ++i) issue_next();
+    }
+    __device__ __forceinline__ void acquire() {
+        cp_async_wait<NS - 2>();
+        __syncwarp();
+        issue_next();
+    }
+};
+
+// One stage of 4 groups: the lane's unit / factor pointers at the stage's
+// first group; c2[i]: rows gid / gid + 8 of token q, groups of parity i.
+__device__ __forceinline__ void compute_stage_int3(const uint8_t *slotp, const uint4 *bp,
+                                                   const float *fp, float c2[2][2]) {
+    const int lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
+    const float *ss = reinterpret_cast<const float *>(slotp + kI3StageW);
+    const float4 SA = *reinterpret_cast<const float4 *>(ss + gid * 4);
+    const float4 SB = *reinterpret_cast<const float4 *>(ss + (gid + 8) * 4);
+    const float sa[4] = {SA.x, SA.y, SA.z, SA.w}, sb[4] = {SB.x, SB.y, SB.z, SB.w};
+    const uint8_t *r0 = slotp + gid * kI3Row, *r8 = r0 + 8 * kI3Row;
+#pragma unroll
+    for (int h = 0; h < 4; h += 2) {
+        uint32_t lo0[2], lo8[2], hs0[2], hs8[2];
+        uint4 bu[2][2];
+        float f[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int gl = h + i;
+            lo0[i] = *reinterpret_cast<const uint32_t *>(r0 + gl * 24 + 4 * q);
+            lo8[i] = *reinterpret_cast<const uint32_t *>(r8 + gl * 24 + 4 * q);
+            hs0[i] = *reinterpret_cast<const uint16_t *>(r0 + gl * 24 + 16 + 2 * q);
+            hs8[i] = *reinterpret_cast<const uint16_t *>(r8 + gl * 24 + 16 + 2 * q);
+            bu[i][0] = bp[gl * 16];
+            bu[i][1] = bp[gl * 16 + 8];
+            f[i] = fp[gl];
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int gl = h + i;
+            float dd[4];
+            tile_group_int3(lo0[i], hs0[i], lo8[i], hs8[i], bu[i], dd);
+            c2[i][0] = fmaf(sa[gl] * f[i], dd[0] + dd[1], c2[i][0]);
+            c2[i][1] = fmaf(sb[gl] * f[i], dd[2] + dd[3], c2[i][1]);
+        }
+    }
+}
+
+template <int kBudget>
+__global__ void __launch_bounds__(32 * kKsWarps)
+    k_int3_ks_x(const uint8_t *__restrict__ w, const float *__restrict__ scales, int N, int K,
+                const float *__restrict__ x, float *__restrict__ y, int ntok) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float red[kKsWarps][16][4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
+    const int G = K / kGroup;
+    // groups per warp: an eighth of G rounded up to whole 4-group stages
+    const int gq = (G / 4 + kKsWarps - 1) / kKsWarps * 4;
+    const int ga = min(G, warp * gq), gb = min(G, ga + gq);
+    const int nitems = (N + 15) / 16;
+    const int i0 = (int)((long long)blockIdx.x * nitems / gridDim.x);
+    const int i1 = (int)((long long)(blockIdx.x + 1) * nitems / gridDim.x);
+
+    constexpr int kNS = ks_x_stages(kBudget), kRing = kNS * kI3Stage;
+    I3Stream<kNS> ws;
+    ws.init(smem + warp * kRing, w, scales, N, G, ga, (gb - ga) / 4, i0, i1 - i0, lane);
+    ws.prologue();  // weights are call inputs: safe to read before the wait
+
+    pdl_wait();     // x may come from the previous kernel
+    pdl_trigger();
+    uint4 *cells = reinterpret_cast<uint4 *>(smem + kKsWarps * kRing);
+    float *fac = reinterpret_cast<float *>(smem + kKsWarps * kRing + kBudget);
+    // each warp converts the groups of its own K share: no block barrier
+    split_rows_smem<false>(x, K, ntok, cells, fac, ga, gb, warp * 32, 32);
+    __syncwarp();
+    int cslot = 0;
+    const int sb = min(gid >> 1, ntok - 1), sd = min(q, ntok - 1);
+    const uint4 *bp0 = cells + (sb * G + ga) * 16 + q * 2 + (gid & 1);
+    const float *fp0 = fac + sd * G + ga;
+
+    for (int it = 0; it < i1 - i0; ++it) {
+        float c2[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        for (int s = 0; s < (gb - ga) / 4; ++s) {
+            ws.acquire();
+            compute_stage_int3(smem + warp * kRing + cslot * kI3Stage, bp0 + s * 64, fp0 + 4 * s, c2);
+            cslot = (cslot + 1 == kNS) ? 0 : cslot + 1;
+        }
+        red[warp][gid][q] = c2[0][0] + c2[1][0];
+        red[warp][gid + 8][q] = c2[0][1] + c2[1][1];
+        __syncthreads();
+        if (warp == 0 && q < ntok) {
+            const int row0 = (i0 + it) * 16;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < kKsWarps; ++k) {
+                a0 += red[k][gid][q];
+                a1 += red[k][gid + 8][q];
+            }
+            const int rA = row0 + gid, rB = row0 + gid + 8;
+            if (rA < N) y[(size_t)q * N + rA] = a0;
+            if (rB < N) y[(size_t)q * N + rB] = a1;
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+}
+
+template <int kBudget>
+cudaError_t launch_i3_ks_b(const uint8_t *w, const float *scales, int N, int K, const float *x,
+                           float *y, int S, cudaStream_t st) {
+    const size_t smem = (size_t)kKsWarps * ks_x_stages(kBudget) * kI3Stage + kBudget + kBudget / 64;
+    cudaError_t e = set_smem(k_int3_ks_x<kBudget>, smem);
+    if (e != cudaSuccess) return e;
+    const int items = (N + 15) / 16;
+    const int slots = sm_count() * max_ctas_per_sm(k_int3_ks_x<kBudget>, 32 * kKsWarps, smem);
+    return launch(k_int3_ks_x<kBudget>, dim3(items < slots ? items : slots), dim3(32 * kKsWarps),
+                  smem, st, true, w, scales, N, K, x, y, S);
+}
+
 template <bool kInt8>
 cudaError_t launch_dense(const uint8_t *w, const float *scales, int N, int K, const float *x,
                          float *y, int S, void *xcells, float *xfac, cudaStream_t st,
@@ -469,6 +719,18 @@ cudaError_t launch_split(const float *v, int R, int K, void *cells, float *fac, 
                       v, K, static_cast<uint4 *>(cells), fac, (int32_t *)nullptr, 0);
     return launch(k_split<false>, dim3(R, (K / kGroup + 7) / 8), dim3(256), 0, st, false, v, K,
                   static_cast<uint4 *>(cells), fac, (int32_t *)nullptr, 0);
+}
+
+bool int3_one_launch(const uint8_t *wq, int K, int S) {
+    return S >= 1 && S <= 4 && K % 256 == 0 && (reinterpret_cast<uintptr_t>(wq) & 15) == 0 &&
+           (size_t)(K / kGroup) * S * 256 <= (size_t)kXBudgetLarge;
+}
+
+cudaError_t launch_gemv_int3_mma(const uint8_t *wq, const float *scales, int N, int K,
+                                 const float *x, float *y, int S, cudaStream_t st) {
+    if ((size_t)(K / kGroup) * S * 256 <= (size_t)kXBudgetSmall)
+        return launch_i3_ks_b<kXBudgetSmall>(wq, scales, N, K, x, y, S, st);
+    return launch_i3_ks_b<kXBudgetLarge>(wq, scales, N, K, x, y, S, st);
 }
 
 // activation units (4 bytes a value) and a factor record of up to 8 bytes a group

@@ -218,6 +218,8 @@ cudaError_t launch_int3_nt(const uint8_t *wq, const float *scales, int N, int K,
 
 cudaError_t launch_gemv_int3(const uint8_t *wq, const float *scales, int N, int K, const float *x,
                              float *y, int S, cudaStream_t st) {
+    if (int3_one_launch(wq, K, S))  // a few tokens: the warp-MMA single launch
+        return launch_gemv_int3_mma(wq, scales, N, K, x, y, S, st);
     // tokens per pass: up to 4, as many as the staged x rows allow
     const int fit = kI3SmemX / (i3_chunks(K) * 16);
     if (fit < 1) {

@@ -32,6 +32,11 @@ cudaError_t launch_gemv_int8(const int8_t *w, const float *row_scale, int N, int
 // int3-g64 two-plane rows [N][K/64 * 24 bytes], fp32 x [S][K] (16-byte aligned).
 cudaError_t launch_gemv_int3(const uint8_t *wq, const float *scales, int N, int K, const float *x,
                              float *y, int S, cudaStream_t st);
+// The same on the warp MMA in one launch (k_int3_ks_x), for up to 4 tokens,
+// K a multiple of 256, 16-byte aligned rows and x's units within 64 KB.
+bool int3_one_launch(const uint8_t *wq, int K, int S);
+cudaError_t launch_gemv_int3_mma(const uint8_t *wq, const float *scales, int N, int K,
+                                 const float *x, float *y, int S, cudaStream_t st);
 // Two int4 GEMVs against the same x: one activation split; one launch when
 // both matrices take the tensor-map kernel, else two.
 cudaError_t launch_gemv_int4_pair(const uint8_t *wq0, const float *s0, int N0, const uint8_t *wq1,

@@ -119,10 +119,15 @@ def test_int4_pair(N0, N1, K, S):
 # int3-g64 two-plane rows: one and many groups, ragged row counts, several
 # token passes (4 a pass), the 14336 x 4096 shape, K = 16384 and 24576 (x staged
 # in shared memory, fewer tokens a pass) and K = 32768 and 65536 (x read from
-# global memory).
+# global memory). Up to 4 tokens with K a multiple of 256 and x's units within
+# 64 KB take the warp-MMA single launch: 14336 x 4096, a ragged last row tile
+# (1000, 33 rows), one 4-group stage for one warp only (K 256), warps with no
+# groups (K 4352: 68 groups as 12 a warp; K 7168), and the 64 KB unit table
+# (K x tokens = 16384: 4096 x 4 and 8192 x 2; K 16384 x 2 is past it).
 INT3_SHAPES = [(1, 64, 1), (17, 192, 3), (100, 1024, 5), (256, 4096, 8), (14336, 4096, 1),
                (9, 32768, 3), (5, 65536, 1), (40, 24576, 2),
-               (64, 16384, 2)]
+               (64, 16384, 2), (1000, 1024, 4), (33, 256, 2), (300, 4352, 3), (2048, 7168, 1),
+               (80, 4096, 4), (64, 8192, 2)]
 
 
 @pytest.mark.parametrize("N,K,S", INT3_SHAPES)
