@@ -457,25 +457,29 @@ constexpr int kI3Stage = kI3StageW + 16 * 4 * 4;
 // a group, in int4's register order (dequant_int4_word): p[j] = (e_j, e_j+4)
 // and p[4 + j] = (e_8+j, e_12+j), j = 0..3, first element in the low half.
 // lo: their low-plane word (e_j at bits 2j); hs: their 16 high bits (e_j at
-// bit j). The low bits of pair j are left at bits 2j (a byte spread puts
-// e_j+4 16 bits above e_j) and the high bit is moved to 2j + 2, so OR-ing
-// both into fp16 1024.0 gives 1024 + 4^j code exactly; one fma by 4^-j with
-// -(1024 * 4^-j + 4) leaves code - 4.
+// bit j). A byte spread of lo leaves pair j's low bits at bits 2j and 2j + 16,
+// so OR-ing them into fp16 1024.0 gives t = 1024 + 4^j low; the high bits,
+// placed at j + 2 and j + 18, give u = 1024 + 2^(j+2) high. Then
+//   t * 4^-j - (4 + 1024 * 2^-j + 1024 * 4^-j) = low - 4 - 1024 * 2^-j
+//   u * 2^-j + that                              = low + 4 high - 4
+// are two fp16 fmas whose results are exact (small integers, and the
+// intermediate within fp16's integer spacing at its magnitude).
 __device__ __forceinline__ void dequant_int3_16(uint32_t lo, uint32_t hs, uint32_t p[8]) {
     const uint32_t kBias = 0x64006400u;
     const uint32_t x[2] = {prmt_u32(lo, 0u, 0x4140u), prmt_u32(lo, 0u, 0x4342u)};
     // high bits of (e_j, e_j+4) at (j + 2, j + 18); of (e_8+j, e_12+j) likewise
     const uint32_t h[2] = {((hs << 2) | (hs << 14)) & 0x003C003Cu,
                            ((hs >> 6) | (hs << 6)) & 0x003C003Cu};
-    const uint32_t kScale[4] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u};  // 4^-j
-    const uint32_t kAdd[4] = {0xE404E404u, 0xDC10DC10u, 0xD440D440u, 0xCD00CD00u};    // -(1024 * 4^-j + 4)
+    const uint32_t kLoScale[4] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u};  // 4^-j
+    const uint32_t kLoAdd[4] = {0xE802E802u, 0xE208E208u, 0xDD10DD10u, 0xD8A0D8A0u};    // -2052, -772, -324, -148
+    const uint32_t kHiScale[4] = {0x3C003C00u, 0x38003800u, 0x34003400u, 0x30003000u};  // 2^-j
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint32_t t = lop3_and_or(x[hh], 0x00030003u << (2 * j), kBias);
-            const uint32_t r = lop3_and_or(h[hh] << j, 0x00040004u << (2 * j), t);
-            p[4 * hh + j] = hfma2_u32(r, kScale[j], kAdd[j]);
+            const uint32_t u = lop3_and_or(h[hh], 0x00040004u << j, kBias);
+            p[4 * hh + j] = hfma2_u32(u, kHiScale[j], hfma2_u32(t, kLoScale[j], kLoAdd[j]));
         }
 }
 
