@@ -264,9 +264,17 @@ __global__ void __launch_bounds__(32 * kKsWarps)
 // [16q, 16q + 16)), so each thread builds its four units from its own values;
 // the group's max |v| takes two shuffles between the four threads. Same
 // arithmetic as k_split.
-template <bool kInt8>
+// The int3 decode's register order (dequant_int3_16: pairs (e_j, e_j+8) of a
+// quad's 16 values, MMA step m taking pairs 2m and 2m + 1): the k's of the
+// B operands of step m, relative to the quad's first value.
+__device__ __forceinline__ void frag_ks_i3(int m, int &k0, int &k1, int &k2, int &k3) {
+    k0 = 2 * m; k1 = 2 * m + 8; k2 = 2 * m + 1; k3 = 2 * m + 9;
+}
+
+template <bool kInt8, bool kI3 = false>
 // Groups [ga, gb) of the ntok rows, split by the threads [t0, t0 + nthr) (a
 // multiple of 4 threads: quad q of a group takes its values 16 q .. 16 q + 15).
+// kI3: units in the int3 decode's order (frag_ks_i3) instead of int4's.
 __device__ void split_rows_smem(const float *__restrict__ x, int K, int ntok, uint4 *cells,
                                 float *fac, int ga, int gb, int t0, int nthr) {
     const int G = K / kGroup, ng = gb - ga, nq = ntok * ng * 4;
@@ -306,7 +314,10 @@ __device__ void split_rows_smem(const float *__restrict__ x, int K, int ntok, ui
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
                         int k0, k1, k2, k3;
-                        frag_ks<kInt8>(2 * mh + i, 0, k0, k1, k2, k3);  // local to the quad
+                        if constexpr (kI3)
+                            frag_ks_i3(2 * mh + i, k0, k1, k2, k3);
+                        else
+                            frag_ks<kInt8>(2 * mh + i, 0, k0, k1, k2, k3);  // local to the quad
                         r[2 * i] = pack_half2(split_part(v[k0], part), split_part(v[k1], part));
                         r[2 * i + 1] = pack_half2(split_part(v[k2], part), split_part(v[k3], part));
                     }
@@ -453,38 +464,38 @@ constexpr int kI3Row = 112;
 constexpr int kI3StageW = 16 * kI3Row;
 constexpr int kI3Stage = kI3StageW + 16 * 4 * 4;
 
-// Exact (code - 4) of the 16 elements of one row that a lane quad takes from
-// a group, in int4's register order (dequant_int4_word): p[j] = (e_j, e_j+4)
-// and p[4 + j] = (e_8+j, e_12+j), j = 0..3, first element in the low half.
-// lo: their low-plane word (e_j at bits 2j); hs: their 16 high bits (e_j at
-// bit j). A byte spread of lo leaves pair j's low bits at bits 2j and 2j + 16,
-// so OR-ing them into fp16 1024.0 gives t = 1024 + 4^j low; the high bits,
-// placed at j + 2 and j + 18, give u = 1024 + 2^(j+2) high. Then
-//   t * 4^-j - (4 + 1024 * 2^-j + 1024 * 4^-j) = low - 4 - 1024 * 2^-j
-//   u * 2^-j + that                              = low + 4 high - 4
-// are two fp16 fmas whose results are exact (small integers, and the
-// intermediate within fp16's integer spacing at its magnitude).
+// Exact (code - 4) of the 16 elements e_0 .. e_15 of one row that a lane
+// quad takes from a group, as p[j] = (e_j, e_j+8), j = 0..7, first element in
+// the low half (the units follow: frag_ks_i3). lo: their low-plane word (e_j
+// at bits 2j); hs: their 16 high bits (e_j at bit j). Pair j's low bits sit
+// at bits 2j' and 2j' + 16 of lo (j' = j) or of lo >> 8 (j' = j - 4), so
+// OR-ing them into fp16 1024.0 gives t = 1024 + 4^j' low; its high bits,
+// moved to j + 2 and j + 18, give u = 1024 + 2^(j+2) high. Then
+//   t * 4^-j' - (4 + 1024 * 2^-j + 1024 * 4^-j') = low - 4 - 1024 * 2^-j
+//   u * 2^-j + that                               = low + 4 high - 4
+// are two fp16 fmas with exact results (small integers, and the intermediate
+// within fp16's integer spacing at its magnitude).
 __device__ __forceinline__ void dequant_int3_16(uint32_t lo, uint32_t hs, uint32_t p[8]) {
     const uint32_t kBias = 0x64006400u;
-    const uint32_t x[2] = {prmt_u32(lo, 0u, 0x4140u), prmt_u32(lo, 0u, 0x4342u)};
-    // high bits of (e_j, e_j+4) at (j + 2, j + 18); of (e_8+j, e_12+j) likewise
-    const uint32_t h[2] = {((hs << 2) | (hs << 14)) & 0x003C003Cu,
-                           ((hs >> 6) | (hs << 6)) & 0x003C003Cu};
-    const uint32_t kLoScale[4] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u};  // 4^-j
-    const uint32_t kLoAdd[4] = {0xE802E802u, 0xE208E208u, 0xDD10DD10u, 0xD8A0D8A0u};    // -2052, -772, -324, -148
-    const uint32_t kHiScale[4] = {0x3C003C00u, 0x38003800u, 0x34003400u, 0x30003000u};  // 2^-j
+    const uint32_t x[2] = {lo, lo >> 8};
+    const uint32_t h = prmt_u32(hs, 0u, 0x4140u) << 2;  // e_j at j + 2, e_j+8 at j + 18
+    const uint32_t kLoScale[4] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u};  // 4^-j'
+    // -(4 + 1024 * 2^-j + 1024 * 4^-j'): -2052, -772, -324, -148, -1092, -292, -84, -28
+    const uint32_t kLoAdd[8] = {0xE802E802u, 0xE208E208u, 0xDD10DD10u, 0xD8A0D8A0u,
+                                0xE444E444u, 0xDC90DC90u, 0xD540D540u, 0xCF00CF00u};
+    // 2^-j
+    const uint32_t kHiScale[8] = {0x3C003C00u, 0x38003800u, 0x34003400u, 0x30003000u,
+                                  0x2C002C00u, 0x28002800u, 0x24002400u, 0x20002000u};
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t t = lop3_and_or(x[hh], 0x00030003u << (2 * j), kBias);
-            const uint32_t u = lop3_and_or(h[hh], 0x00040004u << j, kBias);
-            p[4 * hh + j] = hfma2_u32(u, kHiScale[j], hfma2_u32(t, kLoScale[j], kLoAdd[j]));
-        }
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t t = lop3_and_or(x[j >> 2], 0x00030003u << (2 * (j & 3)), kBias);
+        const uint32_t u = lop3_and_or(h, 0x00040004u << j, kBias);
+        p[j] = hfma2_u32(u, kHiScale[j], hfma2_u32(t, kLoScale[j & 3], kLoAdd[j]));
+    }
 }
 
-// One warp's 16-row tile of one group, up to 4 tokens (see tile_group_int4):
-// lo / hs of rows gid and gid + 8.
+// One warp's 16-row tile of one group, up to 4 tokens (see tile_group_int4;
+// MMA step m takes pairs 2m, 2m + 1): lo / hs of rows gid and gid + 8.
 __device__ __forceinline__ void tile_group_int3(uint32_t lo0, uint32_t hs0, uint32_t lo8,
                                                 uint32_t hs8, const uint4 (&bu)[2], float d[4]) {
     uint32_t p0[8], p8[8], a[4];
@@ -492,15 +503,14 @@ __device__ __forceinline__ void tile_group_int3(uint32_t lo0, uint32_t hs0, uint
     dequant_int3_16(lo8, hs8, p8);
     d[0] = d[1] = d[2] = d[3] = 0.0f;
 #pragma unroll
-    for (int mh = 0; mh < 2; ++mh)
-#pragma unroll
-        for (int mm = 0; mm < 2; ++mm) {
-            a[0] = p0[4 * mh + 2 * mm];
-            a[1] = p8[4 * mh + 2 * mm];
-            a[2] = p0[4 * mh + 2 * mm + 1];
-            a[3] = p8[4 * mh + 2 * mm + 1];
-            mma_16816(d, a, mm ? bu[mh].z : bu[mh].x, mm ? bu[mh].w : bu[mh].y);
-        }
+    for (int m = 0; m < 4; ++m) {
+        a[0] = p0[2 * m];
+        a[1] = p8[2 * m];
+        a[2] = p0[2 * m + 1];
+        a[3] = p8[2 * m + 1];
+        const uint4 &b = bu[m >> 1];
+        mma_16816(d, a, (m & 1) ? b.z : b.x, (m & 1) ? b.w : b.y);
+    }
 }
 
 // Per-warp cp.async stream of 4-group stages over the CTA's items (16-row
@@ -643,7 +653,7 @@ __global__ void __launch_bounds__(32 * kKsWarps)
     uint4 *cells = reinterpret_cast<uint4 *>(smem + kKsWarps * kRing);
     float *fac = reinterpret_cast<float *>(smem + kKsWarps * kRing + kBudget);
     // each warp converts the groups of its own K share: no block barrier
-    split_rows_smem<false>(x, K, ntok, cells, fac, ga, gb, warp * 32, 32);
+    split_rows_smem<false, true>(x, K, ntok, cells, fac, ga, gb, warp * 32, 32);
     __syncwarp();
     int cslot = 0;
     const int sb = min(gid >> 1, ntok - 1), sd = min(q, ntok - 1);
