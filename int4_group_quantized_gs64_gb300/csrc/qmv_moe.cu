@@ -55,7 +55,10 @@ __global__ void __launch_bounds__(32 * kRouteWarps)
 
 // ------------------------------------------------------------------ grouping
 
-// Exclusive block scan of three per-thread values (blockDim.x == 1024).
+// Exclusive block scan of three per-thread values (blockDim.x == 1024): warp
+// scans, the warp totals through shared memory, and each warp adds the
+// totals of the warps before it with one warp reduction per value (one
+// barrier). The caller synchronises before it writes `tot` again.
 __device__ __forceinline__ void block_scan3(int a, int b, int c, int &ea, int &eb, int &ec,
                                             int *tot) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -69,24 +72,18 @@ __device__ __forceinline__ void block_scan3(int a, int b, int c, int &ea, int &e
     }
     if (lane == 31) { tot[warp] = ia; tot[32 + warp] = ib; tot[64 + warp] = ic; }
     __syncthreads();
-    if (warp == 0) {
-        int va = tot[lane], vb = tot[32 + lane], vc = tot[64 + lane];
-        int sa = va, sb = vb, sc = vc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int x = __shfl_up_sync(0xFFFFFFFFu, sa, o);
-            const int y = __shfl_up_sync(0xFFFFFFFFu, sb, o);
-            const int z = __shfl_up_sync(0xFFFFFFFFu, sc, o);
-            if (lane >= o) { sa += x; sb += y; sc += z; }
-        }
-        tot[lane] = sa - va;
-        tot[32 + lane] = sb - vb;
-        tot[64 + lane] = sc - vc;
-    }
-    __syncthreads();
-    ea = tot[warp] + ia - a;
-    eb = tot[32 + warp] + ib - b;
-    ec = tot[64 + warp] + ic - c;
+    const bool before = lane < warp;
+    ea = (int)__reduce_add_sync(0xFFFFFFFFu, before ? (unsigned)tot[lane] : 0u) + ia - a;
+    eb = (int)__reduce_add_sync(0xFFFFFFFFu, before ? (unsigned)tot[32 + lane] : 0u) + ib - b;
+    ec = (int)__reduce_add_sync(0xFFFFFFFFu, before ? (unsigned)tot[64 + lane] : 0u) + ic - c;
+}
+
+// a / b for non-negative a, b: one 32-bit division when both fit in 32 bits
+// (the plan's stage and cost numbers nearly always do), else the 64-bit one.
+__device__ __forceinline__ long long div_nn(long long a, long long b) {
+    if ((((unsigned long long)a | (unsigned long long)b) >> 32) == 0)
+        return (long long)((uint32_t)a / (uint32_t)b);
+    return a / b;
 }
 
 // Grouping on one CTA of 1024 threads: counts by shared atomics; block scans
@@ -126,16 +123,27 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
     const int np = (c + pass_tok - 1) / pass_tok;
     int ec, ef, ep;
     block_scan3(c, f, np, ec, ef, ep, tot);
+    // shared copies for the plan below (reading back the global ones would
+    // cost a round trip to L2 for every dependent step): the expert offsets,
+    // the used experts and their first passes, in the dynamic shared memory
+    // (at least 32 E words; the routing's ids, if any, lie beyond 32 E)
+    extern __shared__ int32_t group_smem[];
+    int32_t *s_off = group_smem, *s_uexp = group_smem + (E + 1), *s_pofs = group_smem + 2 * (E + 1);
     if (tid < E) {
         offsets[tid] = ec;
+        s_off[tid] = ec;
         if (f) {
             uexp[ef] = tid;
+            s_uexp[ef] = tid;
+            s_pofs[ef] = ep;
             if (pass_ofs) pass_ofs[ef] = ep;
         }
     }
     if (tid == E - 1) {
         offsets[E] = ec + c;
+        s_off[E] = ec + c;
         *n_used = ef + f;
+        s_pofs[ef + f] = ep + np;
         if (pass_ofs) pass_ofs[ef + f] = ep + np;
     }
     if (pl && pl->ptab) {
@@ -160,37 +168,46 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
         }
         __syncthreads();
         const int nu = nu_s;
-        const int npass = nu > 0 ? pass_ofs[nu] : 0;
-        for (int b = tid; b <= pl->g; b += blockDim.x) {
-            for (int m = 0; m < 2; ++m) {
-                const long long S = m ? pl->s_dn : pl->s_gu;
-                int32_t ub;
-                if (nu == 0) {
-                    ub = 0;
-                } else if (b == pl->g) {
-                    ub = (int32_t)(S * pass_ofs[nu]);
-                } else {
-                    const long long cb = S * wtot_s * b / pl->g;
-                    int lo = 0, hi = nu - 1;  // last used expert whose stages start at or below cb
-                    while (lo < hi) {
-                        const int mid = (lo + hi + 1) >> 1;
-                        if (S * cnt[mid] <= cb) lo = mid; else hi = mid - 1;
-                    }
-                    const int e = uexp[lo];
-                    const int ce = offsets[e + 1] - offsets[e];
-                    const int npe = (ce + pass_tok - 1) / pass_tok;
-                    const int wl = ce - (npe - 1) * pass_tok > 4 ? kPlanW2 : kPlanW1;
-                    const long long r = cb - S * cnt[lo];
-                    const int i = (int)min((long long)(npe - 1), r / (kPlanW2 * S));
-                    const long long r2 = r - (long long)i * kPlanW2 * S;
-                    const int wi = i < npe - 1 ? kPlanW2 : wl;
-                    const long long st = min(S, (r2 + wi - 1) / wi);
-                    ub = (int32_t)(S * (pass_ofs[lo] + i) + st);
+        const int npass = nu > 0 ? s_pofs[nu] : 0;
+        // (expert, first list index, tokens) of pass p, which is a pass of
+        // used expert lo or the first pass of the next one (as in ptab)
+        auto pass_at = [&](int p, int lo) -> int4 {
+            if (p >= npass) return make_int4(0, 0, 0, 0);
+            const int l = p >= s_pofs[lo + 1] ? lo + 1 : lo;
+            const int e = s_uexp[l], i = p - s_pofs[l];
+            const int ce = s_off[e + 1] - s_off[e];
+            return make_int4(e, s_off[e] + i * pass_tok, min(pass_tok, ce - i * pass_tok), 0);
+        };
+        // one thread per (mode, CTA boundary b): both modes at once
+        for (int idx = tid; idx < 2 * (pl->g + 1); idx += blockDim.x) {
+            const int m = idx / (pl->g + 1), b = idx - m * (pl->g + 1);
+            const long long S = m ? pl->s_dn : pl->s_gu;
+            int32_t ub;
+            int lo = 0;
+            if (nu == 0) {
+                ub = 0;
+            } else if (b == pl->g) {
+                ub = (int32_t)(S * npass);
+            } else {
+                const long long cb = div_nn(S * wtot_s * b, pl->g);
+                int hi = nu - 1;  // last used expert whose stages start at or below cb
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (S * cnt[mid] <= cb) lo = mid; else hi = mid - 1;
                 }
-                const int p = (int)(ub / S);  // the pass holding stage ub, if any
-                const int4 t = p < npass ? pl->ptab[p] : make_int4(0, 0, 0, 0);
-                (m ? pl->plan_dn : pl->plan_gu)[b] = make_int4(ub, t.x, t.y, t.z);
+                const int e = s_uexp[lo];
+                const int ce = s_off[e + 1] - s_off[e];
+                const int npe = (ce + pass_tok - 1) / pass_tok;
+                const int wl = ce - (npe - 1) * pass_tok > 4 ? kPlanW2 : kPlanW1;
+                const long long r = cb - S * cnt[lo];
+                const int i = (int)min((long long)(npe - 1), div_nn(r, kPlanW2 * S));
+                const long long r2 = r - (long long)i * kPlanW2 * S;
+                const int wi = i < npe - 1 ? kPlanW2 : wl;
+                const long long st = min(S, div_nn(r2 + wi - 1, wi));
+                ub = (int32_t)(S * (s_pofs[lo] + i) + st);
             }
+            const int4 t = pass_at((int)div_nn(ub, S), lo);  // the pass holding stage ub, if any
+            (m ? pl->plan_dn : pl->plan_gu)[b] = make_int4(ub, t.x, t.y, t.z);
         }
     }
     // The list, in pair order within each expert. Up to 1024 pairs (a decode
@@ -201,8 +218,7 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
     // segment's first list position for e, and the warp places its pairs in
     // order, 32 at a time. Ranks among the lanes come from shuffles. The
     // positions live in the dynamic shared memory (32 x E ints).
-    extern __shared__ int32_t group_smem[];
-    __syncthreads();  // the scan's reads of tot[] are done; routing's shared rows too
+    __syncthreads();  // the scan's reads of tot[] and the plan's of group_smem are done
     if (P <= 1024) {
         int32_t *run = group_smem;
         if (tid < E) run[tid] = ec;
