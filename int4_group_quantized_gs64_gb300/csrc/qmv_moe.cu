@@ -146,7 +146,10 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
         s_pofs[ef + f] = ep + np;
         if (pass_ofs) pass_ofs[ef + f] = ep + np;
     }
-    if (pl && pl->ptab) {
+    // the plan's arguments in registers (pl points at a kernel parameter:
+    // every access through it would be a memory load)
+    const PlanArgs pa = pl ? *pl : PlanArgs{};
+    if (pa.ptab) {
         // pass table, and each used expert's pass weight (full passes weigh
         // kPlanW2, the last one by its token count)
         __shared__ int32_t nu_s;
@@ -154,7 +157,7 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
         int wexp = 0;
         if (f) {
             for (int i = 0; i < np; ++i)
-                pl->ptab[ep + i] = make_int4(tid, ec + i * pass_tok, min(pass_tok, c - i * pass_tok), 0);
+                pa.ptab[ep + i] = make_int4(tid, ec + i * pass_tok, min(pass_tok, c - i * pass_tok), 0);
             const int last = c - (np - 1) * pass_tok;
             wexp = (np - 1) * kPlanW2 + (last > 4 ? kPlanW2 : kPlanW1);
         }
@@ -179,17 +182,18 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
             return make_int4(e, s_off[e] + i * pass_tok, min(pass_tok, ce - i * pass_tok), 0);
         };
         // one thread per (mode, CTA boundary b): both modes at once
-        for (int idx = tid; idx < 2 * (pl->g + 1); idx += blockDim.x) {
-            const int m = idx / (pl->g + 1), b = idx - m * (pl->g + 1);
-            const long long S = m ? pl->s_dn : pl->s_gu;
+        const int g = pa.g;
+        for (int idx = tid; idx < 2 * (g + 1); idx += blockDim.x) {
+            const int m = idx / (g + 1), b = idx - m * (g + 1);
+            const long long S = m ? pa.s_dn : pa.s_gu;
             int32_t ub;
             int lo = 0;
             if (nu == 0) {
                 ub = 0;
-            } else if (b == pl->g) {
+            } else if (b == g) {
                 ub = (int32_t)(S * npass);
             } else {
-                const long long cb = div_nn(S * wtot_s * b, pl->g);
+                const long long cb = div_nn(S * wtot_s * b, g);
                 int hi = nu - 1;  // last used expert whose stages start at or below cb
                 while (lo < hi) {
                     const int mid = (lo + hi + 1) >> 1;
@@ -207,7 +211,7 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
                 ub = (int32_t)(S * (s_pofs[lo] + i) + st);
             }
             const int4 t = pass_at((int)div_nn(ub, S), lo);  // the pass holding stage ub, if any
-            (m ? pl->plan_dn : pl->plan_gu)[b] = make_int4(ub, t.x, t.y, t.z);
+            (m ? pa.plan_dn : pa.plan_gu)[b] = make_int4(ub, t.x, t.y, t.z);
         }
     }
     // The list, in pair order within each expert. Up to 1024 pairs (a decode
@@ -311,14 +315,16 @@ __device__ void split_row_cta(const float *__restrict__ row, int K, int g0, uint
 }
 
 // Pass and slot of the pairs of token t (pairs tk .. tk + k - 1), as the
-// grouping of CTA 0 places them: the pass offset of each used expert comes
-// from the same counts and scan, the rank of a pair among the pairs of its
+// grouping of CTA 0 places them: the rank of a pair among the pairs of its
 // expert from counting the earlier pairs with that expert (the lists are in
-// pair order). pass[j] = -1 for an id outside [0, E).
+// pair order); then warp j takes pair j: its pass is the passes of all
+// experts below its expert (from the shared counts, one warp reduction) plus
+// rank / pass_tok, its slot the remainder. pass[j] = -1 for an id outside
+// [0, E) or an expert not served.
 __device__ void pair_slots_cta(const int32_t *__restrict__ ids, int P, int E, int k, int t,
                                int pass_tok, int *pass, int *slot, const uint32_t *res) {
-    __shared__ int32_t cnt[1024], pofs[1024], tot[96], rank[32], eid[32];
-    const int tid = threadIdx.x;
+    __shared__ int32_t cnt[1024], rank[32], eid[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     cnt[tid] = 0;
     if (tid < k) {
         const int e = ids[(size_t)t * k + tid];
@@ -335,16 +341,15 @@ __device__ void pair_slots_cta(const int32_t *__restrict__ ids, int P, int E, in
         }
     }
     __syncthreads();
-    const int c = tid < E ? cnt[tid] : 0;
-    const int np = (c + pass_tok - 1) / pass_tok;
-    int ec, ef, ep;
-    block_scan3(c, c > 0 ? 1 : 0, np, ec, ef, ep, tot);
-    if (tid < E) pofs[tid] = ep;
-    __syncthreads();
-    if (tid < k) {
-        const int e = eid[tid];
-        pass[tid] = e < 0 ? -1 : pofs[e] + rank[tid] / pass_tok;
-        slot[tid] = e < 0 ? 0 : rank[tid] % pass_tok;
+    if (warp < k) {
+        const int e = eid[warp];
+        int before = 0;
+        for (int u = lane; u < e; u += 32) before += (cnt[u] + pass_tok - 1) / pass_tok;
+        before = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)before);
+        if (lane == 0) {
+            pass[warp] = e < 0 ? -1 : before + rank[warp] / pass_tok;
+            slot[warp] = e < 0 ? 0 : rank[warp] % pass_tok;
+        }
     }
     __syncthreads();
 }
