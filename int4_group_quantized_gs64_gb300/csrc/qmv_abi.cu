@@ -422,8 +422,9 @@ int moe_route_expert_ffn_int4(const qmv_moe_int4 *m, const float *logits, const 
             return r;
         if ((r = moe_ffn_gate_up(m, T, k, ws, ws_bytes, stream))) return r;
         if ((r = moe_ffn_down(m, T, k, ws, ws_bytes, stream))) return r;
+        // ids and w come from the grouping kernel, three launches back
         return from_cuda(qmv::launch_combine(at<float>(ws, L.y), ids, w, T, k, m->E, m->H, out,
-                                             cs(stream), true));
+                                             cs(stream), true, nullptr, true));
     }
     if ((r = moe_route_topk(logits, T, m->E, k, ids, w, stream))) return r;
     return moe_expert_ffn_int4(m, x, T, ids, w, k, out, ws, ws_bytes, stream);
@@ -459,8 +460,9 @@ int ffn_impl(const qmv_moe_int4 *m, const uint32_t *res, const float *x, int T,
     if ((r = prepare_impl(m, x, T, ids, k, ws, ws_bytes, stream, res, served))) return r;
     if ((r = moe_ffn_gate_up(m, T, k, ws, ws_bytes, stream))) return r;
     if ((r = moe_ffn_down(m, T, k, ws, ws_bytes, stream))) return r;
+    // ids, w and res are call inputs, older than this call's first kernel
     return from_cuda(qmv::launch_combine(at<float>(ws, L.y), ids, w, T, k, m->E, m->H, out, st,
-                                         true, res));
+                                         true, res, true));
 }
 
 }  // namespace
@@ -519,7 +521,8 @@ int moe_expert_ffn_int4_prefill(const qmv_moe_int4 *m, const uint16_t *x_bf16, i
             e = qmv::launch_prefill(d, 1, h, k, offsets, list, uexp, n_used, pass_ofs, h, y,
                                     status, st);
     }
-    if (e == cudaSuccess) e = qmv::launch_combine(y, ids, w, T, k, m->E, m->H, out, st, true);
+    if (e == cudaSuccess)  // ids and w are call inputs
+        e = qmv::launch_combine(y, ids, w, T, k, m->E, m->H, out, st, true, nullptr, true);
     return from_cuda(e);
 }
 

@@ -106,9 +106,12 @@ cudaError_t launch_gate_up(const MoeDims &m, const void *xcells, const float *xf
 cudaError_t launch_down(const MoeDims &m, const void *hcells, const float *hfac,
                         const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                         const int32_t *n_used, const int32_t *pass_ofs, float *y, cudaStream_t st);
+// early (with pdl): ids, w and res were written before the previous kernel
+// started (call inputs, or written by a kernel at least two launches back),
+// so the combine reads them before it waits for y.
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int T, int k, int E,
                            int H, float *out, cudaStream_t st, bool pdl,
-                           const uint32_t *res = nullptr);
+                           const uint32_t *res = nullptr, bool early = false);
 
 // Prefill (tcgen05): mode 0 = gate+up+SiLU (B = x bf16 rows, writes h bf16),
 // mode 1 = down (B = h bf16 rows, writes y fp32). Passes of prefill_pass_tokens().

@@ -755,30 +755,50 @@ template <int V>
 __global__ void __launch_bounds__(256)
     k_combine(const float *__restrict__ y, const int32_t *__restrict__ ids,
               const float *__restrict__ w, int k, int E, int H, float *__restrict__ out,
-              const uint32_t *res) {
+              const uint32_t *res, int early) {
+    // the token's pairs: weight, and whether the pair is combined (k <= 1024)
+    __shared__ float s_w[1024];
+    __shared__ unsigned char s_on[1024];
+    const int t = blockIdx.y;
+    auto stage = [&]() {
+        for (int j = threadIdx.x; j < k; j += blockDim.x) {
+            const int p = t * k + j;
+            const int e = ids[p];
+            const bool on = e >= 0 && e < E && expert_served(res, e);
+            s_on[j] = on ? 1 : 0;
+            s_w[j] = on ? w[p] : 0.0f;
+        }
+    };
+    // ids, w and res are read before the wait when they predate the previous
+    // kernel (early), so that only y's loads follow it
+    if (early) stage();
     pdl_wait();
     pdl_trigger();
-    const int t = blockIdx.y;
+    if (!early) stage();
+    __syncthreads();
     const int i = (blockIdx.x * blockDim.x + threadIdx.x) * V;
     if (i >= H) return;
     float o[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) o[v] = 0.0f;
+    // the y rows of all pairs are in bounds: load them independently (the
+    // skipped pairs' values are never used), add in pair order
+#pragma unroll 8
     for (int j = 0; j < k; ++j) {
-        const int p = t * k + j;
-        const int e = ids[p];
-        if (e >= 0 && e < E && expert_served(res, e)) {
-            const float wp = w[p];
-            const float *yr = y + (size_t)p * H + i;
-            if (V == 4) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(yr);
+        const float *yr = y + (size_t)(t * k + j) * H + i;
+        const float wp = s_w[j];
+        const bool on = s_on[j] != 0;
+        if (V == 4) {
+            const float4 v4 = *reinterpret_cast<const float4 *>(yr);
+            if (on) {
                 o[0] = fmaf(wp, v4.x, o[0]);
                 o[1] = fmaf(wp, v4.y, o[1]);
                 o[2] = fmaf(wp, v4.z, o[2]);
                 o[3] = fmaf(wp, v4.w, o[3]);
-            } else {
-                o[0] = fmaf(wp, yr[0], o[0]);
             }
+        } else {
+            const float v1 = yr[0];
+            if (on) o[0] = fmaf(wp, v1, o[0]);
         }
     }
     if (V == 4)
@@ -881,13 +901,16 @@ cudaError_t launch_down(const MoeDims &m, const void *hcells, const float *hfac,
 }
 
 cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, int T, int k, int E,
-                           int H, float *out, cudaStream_t st, bool pdl, const uint32_t *res) {
+                           int H, float *out, cudaStream_t st, bool pdl, const uint32_t *res,
+                           bool early) {
     if (T == 0) return cudaSuccess;
-    if (H % 4 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0)
+    const int ea = early && pdl ? 1 : 0;
+    if (H % 4 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0 &&
+        (reinterpret_cast<uintptr_t>(y) & 15) == 0)
         return launch(k_combine<4>, dim3((H / 4 + 255) / 256, T), dim3(256), 0, st, pdl, y, ids, w,
-                      k, E, H, out, res);
+                      k, E, H, out, res, ea);
     return launch(k_combine<1>, dim3((H + 255) / 256, T), dim3(256), 0, st, pdl, y, ids, w, k, E, H,
-                  out, res);
+                  out, res, ea);
 }
 
 MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k) {
