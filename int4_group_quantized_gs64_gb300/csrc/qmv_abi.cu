@@ -496,17 +496,23 @@ int moe_expert_ffn_int4_prefill(const qmv_moe_int4 *m, const uint16_t *x_bf16, i
     uint16_t *h = at<uint16_t>(ws, L.h);
     float *y = at<float>(ws, L.y);
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
-    if (e == cudaSuccess)
-        e = qmv::launch_group_split(ids, T, k, m->E, offsets, list, uexp, n_used, pass_ofs, status,
-                                    nullptr, m->H, nullptr, nullptr, st,
-                                    qmv::prefill_pass_tokens());
+    {
+        // the grouping also writes the pass table, which the x packing reads
+        qmv::PlanArgs pt{};
+        pt.ptab = at<int4>(ws, L.ptab);
+        if (e == cudaSuccess)
+            e = qmv::launch_group_split(ids, T, k, m->E, offsets, list, uexp, n_used, pass_ofs,
+                                        status, nullptr, m->H, nullptr, nullptr, st,
+                                        qmv::prefill_pass_tokens(), false, nullptr, 0, false,
+                                        nullptr, nullptr, nullptr, nullptr, nullptr, false, &pt);
+    }
     if (qmv::tma_moe_supported(d)) {
         // tensor-map path: B operands packed per pass (x by a packing kernel,
         // h by the gate_up kernel itself)
         uint16_t *xp = at<uint16_t>(ws, L.xp), *hp = at<uint16_t>(ws, L.hp);
         if (e == cudaSuccess)
-            e = qmv::launch_pack_x(x_bf16, m->H, k, offsets, list, uexp, n_used, pass_ofs, xp,
-                                   L.pmax, st);
+            e = qmv::launch_pack_x(x_bf16, m->H, k, offsets, list, uexp, n_used, pass_ofs,
+                                   at<int4>(ws, L.ptab), xp, L.pmax, st);
         if (e == cudaSuccess)
             e = qmv::launch_prefill(d, 0, xp, k, offsets, list, uexp, n_used, pass_ofs, hp, y,
                                     status, st);

@@ -126,7 +126,7 @@ int prefill_pass_tokens();
 // (argument h) and down reads it (argument b).
 cudaError_t launch_pack_x(const uint16_t *x, int H, int k, const int32_t *offsets,
                           const int32_t *list, const int32_t *uexp, const int32_t *n_used,
-                          const int32_t *pass_ofs, uint16_t *xp, int pmax, cudaStream_t st);
+                          const int32_t *pass_ofs, const int4 *ptab, uint16_t *xp, int pmax, cudaStream_t st);
 
 // TMA-fed decode kernels (qmv_moe_tma.cu): mode 0 = gate+up (cells = x units,
 // writes h, h units, h factors), mode 1 = down (cells = h units, writes y).
@@ -188,7 +188,7 @@ struct MoeWorkspace {
 MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k);
 
 struct PrefillWorkspace {
-    size_t status, offsets, list, uexp, n_used, pass_ofs, h, y, xp, hp, total;
+    size_t status, offsets, list, uexp, n_used, pass_ofs, ptab, h, y, xp, hp, total;
     int pmax;  // passes, at most
 };
 PrefillWorkspace prefill_ws_layout(int E, int H, int I, int T, int k);

@@ -149,15 +149,17 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
     // the plan's arguments in registers (pl points at a kernel parameter:
     // every access through it would be a memory load)
     const PlanArgs pa = pl ? *pl : PlanArgs{};
-    if (pa.ptab) {
-        // pass table, and each used expert's pass weight (full passes weigh
-        // kPlanW2, the last one by its token count)
+    // the pass table (expert, first list index, tokens of every pass)
+    if (pa.ptab && f)
+        for (int i = 0; i < np; ++i)
+            pa.ptab[ep + i] = make_int4(tid, ec + i * pass_tok, min(pass_tok, c - i * pass_tok), 0);
+    if (pa.ptab && pa.plan_gu) {
+        // each used expert's pass weight (full passes weigh kPlanW2, the last
+        // one by its token count)
         __shared__ int32_t nu_s;
         __shared__ long long wtot_s;
         int wexp = 0;
         if (f) {
-            for (int i = 0; i < np; ++i)
-                pa.ptab[ep + i] = make_int4(tid, ec + i * pass_tok, min(pass_tok, c - i * pass_tok), 0);
             const int last = c - (np - 1) * pass_tok;
             wexp = (np - 1) * kPlanW2 + (last > 4 ? kPlanW2 : kPlanW1);
         }
@@ -961,6 +963,7 @@ PrefillWorkspace prefill_ws_layout(int E, int H, int I, int T, int k) {
     // one expert, so there are at most P / 64 + min(E, P) passes
     const size_t pm = std::min(P, (P + 63) / 64 + std::min((size_t)E, P));
     L.pmax = (int)pm;
+    L.ptab = o; o = align256(o + 16 * pm);
     L.xp = o; o = align256(o + pm * (size_t)(H / 64) * 8192);
     L.hp = o; o = align256(o + pm * (size_t)(I / 64) * 8192);
     L.total = o;

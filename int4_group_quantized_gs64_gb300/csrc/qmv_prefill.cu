@@ -914,20 +914,15 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
 __global__ void __launch_bounds__(256)
     k_pack_x(const uint16_t *__restrict__ x, int H, int k, const int32_t *offsets,
              const int32_t *list, const int32_t *uexp, const int32_t *n_used,
-             const int32_t *pass_ofs, uint4 *xp) {
+             const int32_t *pass_ofs, const int4 *ptab, uint4 *xp) {
     pdl_wait();  // the grouping comes from the previous kernel
     pdl_trigger();
-    const int nu = *n_used;
     const int pi = blockIdx.x;
+    // the pass table entry is loaded alongside the pass count (two loads)
+    const int4 pt = ptab[pi];
+    const int nu = *n_used;
     if (nu == 0 || pi >= pass_ofs[nu]) return;
-    int lo = 0, hi = nu - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (pass_ofs[mid] <= pi) lo = mid; else hi = mid - 1;
-    }
-    const int e = uexp[lo], pass = pi - pass_ofs[lo];
-    const int beg = offsets[e] + pass * kPfMaxN;
-    const int ntok = min(kPfMaxN, offsets[e + 1] - offsets[e] - pass * kPfMaxN);
+    const int beg = pt.y, ntok = pt.z;
     const int npad = (ntok + 15) & ~15;
     const int G = H / kGroup;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1011,10 +1006,11 @@ int prefill_pass_tokens() { return kPfMaxN; }
 
 cudaError_t launch_pack_x(const uint16_t *x, int H, int k, const int32_t *offsets,
                           const int32_t *list, const int32_t *uexp, const int32_t *n_used,
-                          const int32_t *pass_ofs, uint16_t *xp, int pmax, cudaStream_t st) {
+                          const int32_t *pass_ofs, const int4 *ptab, uint16_t *xp, int pmax,
+                          cudaStream_t st) {
     if (pmax < 1) return cudaSuccess;
     return launch(k_pack_x, dim3(pmax, (H / kGroup + 7) / 8), dim3(256), 0, st, true, x, H, k,
-                  offsets, list, uexp, n_used, pass_ofs, reinterpret_cast<uint4 *>(xp));
+                  offsets, list, uexp, n_used, pass_ofs, ptab, reinterpret_cast<uint4 *>(xp));
 }
 
 }  // namespace qmv
