@@ -515,10 +515,10 @@ int moe_expert_ffn_int4_prefill(const qmv_moe_int4 *m, const uint16_t *x_bf16, i
                                    at<int4>(ws, L.ptab), xp, L.pmax, st);
         if (e == cudaSuccess)
             e = qmv::launch_prefill(d, 0, xp, k, offsets, list, uexp, n_used, pass_ofs, hp, y,
-                                    status, st);
+                                    status, st, at<int4>(ws, L.ptab));
         if (e == cudaSuccess)
             e = qmv::launch_prefill(d, 1, hp, k, offsets, list, uexp, n_used, pass_ofs, hp, y,
-                                    status, st);
+                                    status, st, at<int4>(ws, L.ptab));
     } else {
         if (e == cudaSuccess)
             e = qmv::launch_prefill(d, 0, x_bf16, k, offsets, list, uexp, n_used, pass_ofs, h, y,

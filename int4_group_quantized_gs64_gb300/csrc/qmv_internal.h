@@ -115,10 +115,12 @@ cudaError_t launch_combine(const float *y, const int32_t *ids, const float *w, i
 
 // Prefill (tcgen05): mode 0 = gate+up+SiLU (B = x bf16 rows, writes h bf16),
 // mode 1 = down (B = h bf16 rows, writes y fp32). Passes of prefill_pass_tokens().
+// ptab: the grouping kernel's pass table, or null (then the passes are found
+// through pass_ofs, uexp and offsets).
 cudaError_t launch_prefill(const MoeDims &m, int mode, const uint16_t *b, int k,
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                            const int32_t *n_used, const int32_t *pass_ofs, uint16_t *h, float *y,
-                           int32_t *status, cudaStream_t st);
+                           int32_t *status, cudaStream_t st, const int4 *ptab = nullptr);
 int prefill_pass_tokens();
 // Tensor-map prefill (tma_moe_supported shapes): B operands packed per pass,
 // [pass][K/64][64 rows][64 bf16], 128-byte swizzled, rows beyond the pass's

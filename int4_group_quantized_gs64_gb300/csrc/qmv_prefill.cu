@@ -500,6 +500,7 @@ struct PqArgs {
     int mode;            // 0: gate_up, 1: down
     int K, G, tiles, k, I, H;
     const int32_t *offsets, *list, *uexp, *n_used, *pass_ofs;
+    const int4 *ptab;    // pass table (expert, first list index, tokens), or null
     const uint16_t *b;   // B rows, bf16: x [T][H] or h [P][I]
     uint16_t *h;         // gate_up output [P][I] bf16
     float *y;            // down output [P][H] fp32
@@ -610,6 +611,11 @@ __device__ __forceinline__ void pq_commit_elect(uint64_t *mbar) {
 struct PqCursor {
     int lo, pi, e, beg, ntok;
     __device__ __forceinline__ void seek(const PqArgs &a, int nu, int p) {
+        if (a.ptab) {  // one load a pass instead of a search and walk
+            pi = -1;
+            to(a, p);
+            return;
+        }
         int l = 0, hgh = nu - 1;
         while (l < hgh) {
             const int mid = (l + hgh + 1) >> 1;
@@ -621,6 +627,14 @@ struct PqCursor {
     }
     __device__ __forceinline__ void to(const PqArgs &a, int p) {
         if (p == pi) return;
+        if (a.ptab) {
+            const int4 t = a.ptab[p];
+            pi = p;
+            e = t.x;
+            beg = t.y;
+            ntok = t.z;
+            return;
+        }
         while (a.pass_ofs[lo + 1] <= p) ++lo;
         pi = p;
         e = a.uexp[lo];
@@ -948,7 +962,7 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_prefill(const MoeDims &m, int mode, const uint16_t *b, int k,
                            const int32_t *offsets, const int32_t *list, const int32_t *uexp,
                            const int32_t *n_used, const int32_t *pass_ofs, uint16_t *h, float *y,
-                           int32_t *status, cudaStream_t st) {
+                           int32_t *status, cudaStream_t st, const int4 *ptab) {
     if (tma_moe_supported(m)) {
         PqArgs q;
         memset(&q, 0, sizeof(q));
@@ -957,6 +971,7 @@ cudaError_t launch_prefill(const MoeDims &m, int mode, const uint16_t *b, int k,
         q.I = m.I;
         q.H = m.H;
         q.offsets = offsets; q.list = list; q.uexp = uexp; q.n_used = n_used; q.pass_ofs = pass_ofs;
+        q.ptab = ptab;
         q.b = b;
         q.h = h;
         q.y = y;
