@@ -143,6 +143,9 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
         offsets[E] = ec + c;
         s_off[E] = ec + c;
         *n_used = ef + f;
+        // with a pass table (the library's own workspaces, whose n_used slot
+        // has room) the pass count too, so that a reader needs one load
+        if (pl && pl->ptab) n_used[1] = ep + np;
         s_pofs[ef + f] = ep + np;
         if (pass_ofs) pass_ofs[ef + f] = ep + np;
     }

@@ -681,8 +681,16 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
     if (warp != kPqProdW) pdl_wait();
     pdl_trigger();
 
-    const int nu = *a.n_used;
-    const int total_items = nu > 0 ? a.pass_ofs[nu] * a.tiles : 0;
+    // with the pass table the grouping kernel also wrote the pass count
+    // next to n_used (one load); else it is pass_ofs[n_used]
+    int nu = 0, npass;
+    if (a.ptab) {
+        npass = a.n_used[1];
+    } else {
+        nu = *a.n_used;
+        npass = nu > 0 ? a.pass_ofs[nu] : 0;
+    }
+    const int total_items = npass * a.tiles;
     // Items are dealt out round-robin (CTA c takes items c, c + grid, ...), so
     // at any time the CTAs work on ~grid consecutive items: the tiles of a
     // few passes, whose packed B and (passes of one expert) weights are then
@@ -932,10 +940,9 @@ __global__ void __launch_bounds__(256)
     pdl_wait();  // the grouping comes from the previous kernel
     pdl_trigger();
     const int pi = blockIdx.x;
-    // the pass table entry is loaded alongside the pass count (two loads)
+    // the pass table entry and the pass count (next to n_used), one load each
     const int4 pt = ptab[pi];
-    const int nu = *n_used;
-    if (nu == 0 || pi >= pass_ofs[nu]) return;
+    if (pi >= n_used[1]) return;
     const int beg = pt.y, ntok = pt.z;
     const int npad = (ntok + 15) & ~15;
     const int G = H / kGroup;
