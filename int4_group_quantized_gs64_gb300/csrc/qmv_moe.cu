@@ -225,7 +225,7 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
     // writer. More pairs: warp w takes the w-th 32nd of the pairs; hist[w][e]
     // counts its pairs of expert e, a scan over w turns the counts into each
     // segment's first list position for e, and the warp places its pairs in
-    // order, 32 at a time. Ranks among the lanes come from shuffles. The
+    // order, 32 at a time. Ranks among the lanes come from __match_any_sync. The
     // positions live in the dynamic shared memory (32 x E ints).
     __syncthreads();  // the scan's reads of tot[] and the plan's of group_smem are done
     if (P <= 1024) {
@@ -236,16 +236,11 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
             const int p = base + lane;
             const int e = p < P ? ids[p] : -1;
             const bool mine = p < P && e >= 0 && e < E && (e & 31) == warp && expert_served(res, e);
-            unsigned m = __ballot_sync(0xFFFFFFFFu, mine);
-            if (m == 0) continue;
-            int rank = 0, after = 0;
-            while (m) {
-                const int l = __ffs(m) - 1;
-                m &= m - 1;
-                const int el = __shfl_sync(0xFFFFFFFFu, e, l);
-                rank += (l < lane && el == e) ? 1 : 0;
-                after += (l > lane && el == e) ? 1 : 0;
-            }
+            if (__ballot_sync(0xFFFFFFFFu, mine) == 0) continue;
+            // the lanes holding the same expert (other lanes get unique keys)
+            const unsigned same = __match_any_sync(0xFFFFFFFFu, mine ? e : -1 - lane);
+            const int rank = __popc(same & ((1u << lane) - 1u));
+            const int after = __popc(same & ~((2u << lane) - 1u));
             if (mine) list[run[e] + rank] = p;
             __syncwarp();
             if (mine && after == 0) run[e] += rank + 1;
@@ -275,13 +270,9 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
             int e = p < s1 ? ids[p] : -1;
             const bool valid = p < s1 && e >= 0 && e < E && expert_served(res, e);
             if (!valid) e = -1 - lane;  // unique key: never matches another lane
-            int rank = 0, after = 0;
-#pragma unroll
-            for (int l = 0; l < 32; ++l) {
-                const int el = __shfl_sync(0xFFFFFFFFu, e, l);
-                rank += (l < lane && el == e) ? 1 : 0;
-                after += (l > lane && el == e) ? 1 : 0;
-            }
+            const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+            const int rank = __popc(same & ((1u << lane) - 1u));
+            const int after = __popc(same & ~((2u << lane) - 1u));
             if (valid) list[hw[e] + rank] = p;
             __syncwarp();
             if (valid && after == 0) hw[e] += rank + 1;
