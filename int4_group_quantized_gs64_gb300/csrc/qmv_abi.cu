@@ -511,8 +511,8 @@ int moe_expert_ffn_int4_prefill(const qmv_moe_int4 *m, const uint16_t *x_bf16, i
         // h by the gate_up kernel itself)
         uint16_t *xp = at<uint16_t>(ws, L.xp), *hp = at<uint16_t>(ws, L.hp);
         if (e == cudaSuccess)
-            e = qmv::launch_pack_x(x_bf16, m->H, k, offsets, list, uexp, n_used, pass_ofs,
-                                   at<int4>(ws, L.ptab), xp, L.pmax, st);
+            e = qmv::launch_pack_x(x_bf16, m->H, k, list, n_used, at<int4>(ws, L.ptab), xp,
+                                   L.pmax, st);
         if (e == cudaSuccess)
             e = qmv::launch_prefill(d, 0, xp, k, offsets, list, uexp, n_used, pass_ofs, hp, y,
                                     status, st, at<int4>(ws, L.ptab));

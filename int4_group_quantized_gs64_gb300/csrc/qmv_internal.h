@@ -126,9 +126,9 @@ int prefill_pass_tokens();
 // [pass][K/64][64 rows][64 bf16], 128-byte swizzled, rows beyond the pass's
 // tokens zero. launch_pack_x packs x; the gate_up launch writes h packed
 // (argument h) and down reads it (argument b).
-cudaError_t launch_pack_x(const uint16_t *x, int H, int k, const int32_t *offsets,
-                          const int32_t *list, const int32_t *uexp, const int32_t *n_used,
-                          const int32_t *pass_ofs, const int4 *ptab, uint16_t *xp, int pmax, cudaStream_t st);
+cudaError_t launch_pack_x(const uint16_t *x, int H, int k, const int32_t *list,
+                          const int32_t *n_used, const int4 *ptab, uint16_t *xp, int pmax,
+                          cudaStream_t st);
 
 // TMA-fed decode kernels (qmv_moe_tma.cu): mode 0 = gate+up (cells = x units,
 // writes h, h units, h factors), mode 1 = down (cells = h units, writes y).

@@ -932,11 +932,11 @@ __global__ void __launch_bounds__(kPqThreads, 1) k_prefill_tma(const __grid_cons
 // xp[pass][g][64 rows][64 bf16], row t = token slot t of the pass
 // (zero from its token count up to the next multiple of 16), 128-byte
 // swizzled. Grid (passes at most, ceil(G / 8)); warp w packs group
-// 8 * blockIdx.y + w of pass blockIdx.x.
+// 8 * blockIdx.y + w of pass blockIdx.x. The passes come from the grouping
+// kernel's pass table, their count from the word after n_used.
 __global__ void __launch_bounds__(256)
-    k_pack_x(const uint16_t *__restrict__ x, int H, int k, const int32_t *offsets,
-             const int32_t *list, const int32_t *uexp, const int32_t *n_used,
-             const int32_t *pass_ofs, const int4 *ptab, uint4 *xp) {
+    k_pack_x(const uint16_t *__restrict__ x, int H, int k, const int32_t *list,
+             const int32_t *n_used, const int4 *ptab, uint4 *xp) {
     pdl_wait();  // the grouping comes from the previous kernel
     pdl_trigger();
     const int pi = blockIdx.x;
@@ -1026,13 +1026,12 @@ cudaError_t launch_prefill(const MoeDims &m, int mode, const uint16_t *b, int k,
 
 int prefill_pass_tokens() { return kPfMaxN; }
 
-cudaError_t launch_pack_x(const uint16_t *x, int H, int k, const int32_t *offsets,
-                          const int32_t *list, const int32_t *uexp, const int32_t *n_used,
-                          const int32_t *pass_ofs, const int4 *ptab, uint16_t *xp, int pmax,
+cudaError_t launch_pack_x(const uint16_t *x, int H, int k, const int32_t *list,
+                          const int32_t *n_used, const int4 *ptab, uint16_t *xp, int pmax,
                           cudaStream_t st) {
     if (pmax < 1) return cudaSuccess;
     return launch(k_pack_x, dim3(pmax, (H / kGroup + 7) / 8), dim3(256), 0, st, true, x, H, k,
-                  offsets, list, uexp, n_used, pass_ofs, ptab, reinterpret_cast<uint4 *>(xp));
+                  list, n_used, ptab, reinterpret_cast<uint4 *>(xp));
 }
 
 }  // namespace qmv
