@@ -454,8 +454,8 @@ cudaError_t launch_ks_x(const uint8_t *w, const float *scales, int N, int K, con
 // k_dense_ks_x: 8 warps share each 16-row item, warp ks streams an eighth of
 // its groups through a cp.async ring, every block splits x into its own unit
 // table, and the 16 elements a lane quad takes of each group are decoded into
-// exact fp16 (code - 4) in int4's register order, so the int4 activation
-// units and MMA steps serve unchanged.
+// exact fp16 (code - 4) as pairs (e_j, e_j+8), the order the activation units
+// of this path are built in (frag_ks_i3); the MMA steps are int4's.
 
 // A stage: 16 rows x 4 groups (96 bytes a row), rows 112 bytes apart so that
 // a fragment load of the 8 row pairs (28 words apart) touches 8 distinct

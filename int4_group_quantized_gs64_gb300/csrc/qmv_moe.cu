@@ -149,8 +149,7 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
         s_pofs[ef + f] = ep + np;
         if (pass_ofs) pass_ofs[ef + f] = ep + np;
     }
-    // the plan's arguments in registers (pl points at a kernel parameter:
-    // every access through it would be a memory load)
+    // the plan's arguments, read once
     const PlanArgs pa = pl ? *pl : PlanArgs{};
     // the pass table (expert, first list index, tokens of every pass)
     if (pa.ptab && f)
@@ -920,7 +919,7 @@ MoeWorkspace moe_ws_layout(int E, int H, int I, int T, int k) {
     L.offsets = o; o = align256(o + 4 * (size_t)(E + 1));
     L.list = o; o = align256(o + 4 * P);
     L.uexp = o; o = align256(o + 4 * (size_t)E);
-    L.n_used = o; o = align256(o + 4);
+    L.n_used = o; o = align256(o + 8);  // n_used, then the pass count
     L.pass_ofs = o; o = align256(o + 4 * (size_t)(E + 1));
     L.xcells = o; o = align256(o + 4 * (size_t)T * H);
     L.xfac = o; o = align256(o + 8 * (size_t)T * (H / 64));  // up to 8 bytes a group
@@ -949,7 +948,7 @@ PrefillWorkspace prefill_ws_layout(int E, int H, int I, int T, int k) {
     L.offsets = o; o = align256(o + 4 * (size_t)(E + 1));
     L.list = o; o = align256(o + 4 * P);
     L.uexp = o; o = align256(o + 4 * (size_t)E);
-    L.n_used = o; o = align256(o + 4);
+    L.n_used = o; o = align256(o + 8);  // n_used, then the pass count
     L.pass_ofs = o; o = align256(o + 4 * (size_t)(E + 1));
     L.h = o; o = align256(o + 2 * P * I);
     L.y = o; o = align256(o + 4 * P * H);
