@@ -20,8 +20,11 @@
 // Work split: the stages of all items (item-major) are shared out over the
 // CTAs, by the grouping kernel's cost-balanced plan when there is one, else
 // evenly. An item whose stages fall to several CTAs is finished by the last
-// of them to arrive (an acquire-release counter; nobody waits for anybody),
-// which adds the partial sums in CTA order and writes the item.
+// of them to publish its partial sums (an acquire-release counter; nobody
+// waits for anybody), which adds the partial sums in CTA order and writes
+// the item. A tenth warp keeps that off the consumers' path: it publishes
+// the item a CTA starts in while the consumers go on, and fetches the next
+// CTA's partial sums of the item a CTA ends in while the range still runs.
 //
 // Every mbarrier wait is bounded. A consumer warp whose wait runs out stops
 // waiting but keeps computing (on whatever the slot holds) and keeps every
@@ -44,9 +47,10 @@ namespace qmv {
 namespace {
 
 constexpr int kTConsumers = 8;                       // consumer warps, two 16-row tiles each
-constexpr int kTThreads = 32 * (kTConsumers + 1);
+constexpr int kTSync = kTConsumers + 1;              // warp of the split items' counters
+constexpr int kTThreads = 32 * (kTConsumers + 2);    // consumers, producer, sync warp
 // Registers: warps are spread round-robin over the 4 SM sub-partitions, so
-// one holds 3 of the 9 warps; 3 x 32 x 168 fits its 16,384 registers.
+// one holds 3 of the 10 warps; 3 x 32 x 168 fits its 16,384 registers.
 constexpr int kTRegBound = 3 * 4 * 32;               // launch bound giving 168 registers
 constexpr int kTStages = 4;
 constexpr int kTRows = 256;                          // weight rows per stage
@@ -62,8 +66,10 @@ static_assert(kTOffA - kTOffF + kMaxTok * kTActTok == kPackedStage, "pass-packed
 constexpr int kTGuJ = 128;                           // hidden units per gate+up item
 constexpr int kTDnRows = 256;                        // output rows per down item
 constexpr int kTEpi = (kTGuJ * kMaxTok + kTConsumers * 64) * 4;  // h of an item, split scratch
-constexpr int kTSmem = kTStages * kTStage + kTEpi + 1024;
+constexpr int kTTail = kTRows * kMaxTok * 4;        // the next CTA's partial sums of the last item
+constexpr int kTSmem = kTStages * kTStage + kTEpi + kTTail + 1024;
 constexpr uint32_t kTWait = 1u << 24;
+constexpr uint32_t kTPoll = 1u << 16;                // sync warp: polls of a counter (~0.5 us apart)
 
 static_assert(kTStage % 1024 == 0, "stages must stay 1024-aligned for the 128B swizzle");
 static_assert(kSkPartFloats == 2 * kTRows * kMaxTok, "partial-sum slots must match the stage");
@@ -288,9 +294,16 @@ __device__ __forceinline__ void compute_stage(const uint8_t *slot, int warp,
 struct TShared {
     uint64_t full[kTStages];
     uint64_t empty[kTStages];
+    uint64_t hp;   // the head item's partial sums are stored (each consumer warp arrives)
+    uint64_t hd;   // the sync warp has counted the head item (defer is valid)
+    uint64_t tp;   // the sync warp's verdict on the last item (ready is valid)
     long long ub[kSkMaxCtas + 1];  // first stage of each CTA's range (consumers' copy)
     int pairs[kMaxTok];
     int last;
+    int h_bf, h_n;        // the head item's first contributor and contributor count
+    volatile int stop;    // consumers are at the last item's end: stop polling
+    volatile int ready;   // the next CTA's partial sums of the last item are in shared memory
+    volatile int defer;   // this CTA was the head item's last contributor: it writes the item
 };
 
 // Consumer side of stages [kb0, kb1) of one item. A wait that runs out sets
@@ -430,17 +443,31 @@ __device__ __forceinline__ int unit_owner(const long long *ub, int g, long long 
     return l;
 }
 
-// An item whose stages are split between CTAs: this CTA stores its partial
-// sums (slot 0 if the item is the first of its range, else slot 1), and the
-// last contributor to arrive adds every contributor's partial in CTA order
-// (so the sum does not depend on which CTA finishes last), clears the
-// counter for the next launch and returns true: it then writes the item.
-// No CTA waits for another.
+// Split items. An item whose stages fall to several CTAs (contributors
+// bf .. bl, those with non-empty ranges) is written by one of them with the
+// sum of every contributor's partial sums, added in CTA order from zero (so
+// the result does not depend on who writes it). Counter cnt[bf] counts the
+// contributors that have published (stored their partial sums, then a
+// release at gpu scope); a contributor that finds all the others published
+// writes the item and clears the counter for the next launch. No CTA waits
+// for another: whoever publishes last writes.
+//
+// The item a CTA starts in (begun by an earlier CTA) comes at the start of
+// its range, where a block barrier and a counter round trip would stall the
+// consumers while the ring is full; its publication goes to the sync warp
+// (the consumers store and move on; should the count show this CTA last,
+// it writes the item after its range). The item a CTA ends in comes at the
+// end of its range: when exactly one later CTA holds the rest of it, the
+// sync warp watches that CTA's publication during the range and copies its
+// partial sums into shared memory, so the item ends without a round trip to
+// L2; if they are not there by the end, the CTA publishes instead.
+
+// This CTA's partial sums of an item: slot 0 if the item is the first of its
+// range, else slot 1.
 template <int NB>
-__device__ __forceinline__ bool t_combine(const TmaArgs &a, TShared &sh, int ntok, int item,
-                                          bool head, int ns, float acc[2][NB][2]) {
+__device__ __forceinline__ void t_store_part(const TmaArgs &a, int ntok, bool head,
+                                             const float acc[2][NB][2]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3;
-    const int g = gridDim.x;
     const int r = 16 * warp + tile_row(lane >> 2);
     float *mine = a.part + ((size_t)blockIdx.x * 2 + (head ? 0 : 1)) * (kTRows * kMaxTok);
 #pragma unroll
@@ -453,22 +480,36 @@ __device__ __forceinline__ bool t_combine(const TmaArgs &a, TShared &sh, int nto
                 mine[(rt + 8) * kMaxTok + s] = acc[t][nb][1];
             }
         }
-    // The barrier orders every consumer's partial-sum stores before thread 0's
-    // counter update, a release whose cumulativity makes them visible
-    // device-wide first; the same atomic is an acquire, which orders the
-    // other CTAs' partials before the barrier that the readers pass.
-    consumers_sync();
+}
+
+// Contributors of the item whose stages begin at `first`: the first one and
+// how many (CTAs of [bf, bl] with a non-empty range all hold its stages).
+__device__ __forceinline__ void t_contributors(const long long *ub, int g, long long first,
+                                               int ns, int &bf, int &n) {
+    bf = unit_owner(ub, g, first);
+    const int bl = unit_owner(ub, g, first + ns - 1);
+    n = 0;
+    for (int c = bf; c <= bl; ++c) n += ub[c + 1] > ub[c];
+}
+
+// Publishes (acquire-release at gpu scope: this CTA's partials, then the
+// others'); true if every other contributor had published before.
+__device__ __forceinline__ bool t_publish(const TmaArgs &a, int bf, int n) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(&a.cnt[bf]) : "memory");
+    return old == n - 1;
+}
+
+// Every contributor's partial sums of the item, added in CTA order from zero;
+// clears the counter for the next launch.
+template <int NB>
+__device__ __forceinline__ void t_gather(const TmaArgs &a, const TShared &sh, int ntok, int item,
+                                         int ns, float acc[2][NB][2]) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3;
+    const int g = gridDim.x;
+    const int r = 16 * warp + tile_row(lane >> 2);
     const long long first = (long long)item * ns;
     const int bf = unit_owner(sh.ub, g, first), bl = unit_owner(sh.ub, g, first + ns - 1);
-    if (threadIdx.x == 0) {
-        int n = 0;  // CTAs of [bf, bl] with a non-empty range all hold stages of this item
-        for (int c = bf; c <= bl; ++c) n += sh.ub[c + 1] > sh.ub[c];
-        int old;  // acquire-release at gpu scope: the partials above, then the others'
-        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(&a.cnt[bf]) : "memory");
-        sh.last = old == n - 1;
-    }
-    consumers_sync();
-    if (!sh.last) return false;
 #pragma unroll
     for (int t = 0; t < 2; ++t)
 #pragma unroll
@@ -490,7 +531,121 @@ __device__ __forceinline__ bool t_combine(const TmaArgs &a, TShared &sh, int nto
             }
     }
     if (threadIdx.x == 0) a.cnt[bf] = 0;
+}
+
+// The item at hand, synchronously: store, publish (thread 0, between two
+// barriers: the barrier orders every consumer's stores before the release;
+// the acquire orders the others' partials before the readers' barrier),
+// and gather if this CTA published last. True: the caller writes the item.
+template <int NB>
+__device__ __forceinline__ bool t_combine(const TmaArgs &a, TShared &sh, int ntok, int item,
+                                          bool head, int ns, float acc[2][NB][2]) {
+    t_store_part<NB>(a, ntok, head, acc);
+    consumers_sync();
+    if (threadIdx.x == 0) {
+        int bf, n;
+        t_contributors(sh.ub, gridDim.x, (long long)item * ns, ns, bf, n);
+        sh.last = t_publish(a, bf, n);
+    }
+    consumers_sync();
+    if (!sh.last) return false;
+    t_gather<NB>(a, sh, ntok, item, ns, acc);
     return true;
+}
+
+// The last item, finished with the next CTA's partial sums that the sync
+// warp copied into shared memory (tail: [kTRows][kMaxTok]): (0 + own) +
+// next, the order t_gather adds them in.
+template <int NB>
+__device__ __forceinline__ void t_add_tail(const float *tail, int ntok, float acc[2][NB][2]) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3;
+    const int r = 16 * warp + tile_row(lane >> 2);
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const int s = 4 * nb + q, rt = r + t * kTRowB;
+            if (s < ntok) {
+                acc[t][nb][0] = (0.f + acc[t][nb][0]) + tail[rt * kMaxTok + s];
+                acc[t][nb][1] = (0.f + acc[t][nb][1]) + tail[(rt + 8) * kMaxTok + s];
+            }
+        }
+}
+
+// The split-item roles of a CTA's range [u0, u1) of stages (ns an item; u2:
+// where the next CTA's range ends). head_async: its first item began in an
+// earlier CTA and the range goes on past it (published by the sync warp).
+// tail_next: its last item began inside the range and the next CTA holds all
+// the rest of it (the sync warp fetches that CTA's partial sums).
+struct TRoles {
+    bool head_async, tail_next;
+};
+__device__ __forceinline__ TRoles t_roles(long long u0, long long u1, long long u2, int ns, int g) {
+    TRoles r{false, false};
+    if (u1 <= u0) return r;
+    const long long hi = u0 / ns, ti = (u1 - 1) / ns;
+    r.head_async = u0 % ns != 0 && ti != hi;
+    r.tail_next = ti != hi && u1 % ns != 0 && (int)blockIdx.x + 1 < g && u2 >= (ti + 1) * ns;
+    return r;
+}
+
+// Consumers, after the stages of an item: write it, or publish it and write
+// it if this CTA is its last contributor (see t_store_part).
+template <int NB>
+__device__ __forceinline__ void t_finish(const TmaArgs &a, TShared &sh, float *epi, int tile,
+                                         int ntok, int pi, int item, bool head, int ns, bool whole,
+                                         bool head_pub, bool tail_fin, float acc[2][NB][2]) {
+    bool write = whole;
+    if (head_pub) {  // store and move on; the sync warp publishes
+        t_store_part<NB>(a, ntok, true, acc);
+        if (threadIdx.x == 0) {
+            int bf, n;
+            t_contributors(sh.ub, gridDim.x, (long long)item * ns, ns, bf, n);
+            sh.h_bf = bf;
+            sh.h_n = n;
+        }
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.hp);
+    } else if (!whole) {
+        bool fetched = false;
+        if (tail_fin) {  // the next CTA's partial sums, if the sync warp has them
+            if ((threadIdx.x & 31) == 0) sh.stop = 1;
+            const bool ok = tc05::mbar_wait(&sh.tp, 0u, kTWait);
+            if (!ok && (threadIdx.x & 31) == 0) atomicOr(a.status, 2);
+            fetched = ok && sh.ready;
+        }
+        if (fetched) {
+            t_add_tail<NB>(epi + kTEpi / 4, ntok, acc);
+            if (threadIdx.x == 0) a.cnt[blockIdx.x] = 0;  // every other contributor is done
+            write = true;
+        } else {
+            write = t_combine<NB>(a, sh, ntok, item, head, ns, acc);
+        }
+    }
+    if (write) t_epilogue<NB>(a, sh, epi, tile, ntok, pi, acc);
+}
+
+// Consumers, after their range: the first item, which this CTA published
+// last (rare: its first contributor finishes its part at the end of its own
+// range). Out of line, so it costs the item loop no registers.
+__device__ __noinline__ void t_write_deferred(const TmaArgs &a, TShared &sh, float *epi, int nu,
+                                              int item, int tiles, int ns) {
+    const int pi = item / tiles, tile = item - pi * tiles;
+    PassCursor hc;
+    hc.seek(a, nu, pi);
+    consumers_sync();  // the last epilogue is done with sh.pairs
+    if (threadIdx.x < hc.ntok)
+        sh.pairs[threadIdx.x] = a.mode == 2 ? hc.beg + threadIdx.x : a.list[hc.beg + threadIdx.x];
+    consumers_sync();
+    if (hc.ntok <= 4) {
+        float acc[2][1][2];
+        t_gather<1>(a, sh, hc.ntok, item, ns, acc);
+        t_epilogue<1>(a, sh, epi, tile, hc.ntok, pi, acc);
+    } else {
+        float acc[2][2][2];
+        t_gather<2>(a, sh, hc.ntok, item, ns, acc);
+        t_epilogue<2>(a, sh, epi, tile, hc.ntok, pi, acc);
+    }
 }
 
 __global__ void __launch_bounds__(kTRegBound, 1) k_moe_tma(const __grid_constant__ TmaArgs a) {
@@ -500,6 +655,7 @@ __global__ void __launch_bounds__(kTRegBound, 1) k_moe_tma(const __grid_constant
     // compiler keeps shared-window addressing (LDS) for every access.
     uint8_t *ring = smem_raw + ((1024u - (tc05::smem_addr(smem_raw) & 1023u)) & 1023u);
     float *epi = reinterpret_cast<float *>(ring + kTStages * kTStage);
+    float *tail = reinterpret_cast<float *>(ring + kTStages * kTStage + kTEpi);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (warp == kTConsumers && lane == 0) {  // the tensor-map descriptors, early
@@ -515,6 +671,12 @@ __global__ void __launch_bounds__(kTRegBound, 1) k_moe_tma(const __grid_constant
             tc05::mbar_init(&sh.full[s], 1);
             tc05::mbar_init(&sh.empty[s], kTConsumers);
         }
+        tc05::mbar_init(&sh.hp, kTConsumers);
+        tc05::mbar_init(&sh.hd, 1);
+        tc05::mbar_init(&sh.tp, 1);
+        sh.stop = 0;
+        sh.ready = 0;
+        sh.defer = 0;
         tc05::fence_mbar_init();
     }
     __syncthreads();
@@ -523,7 +685,7 @@ __global__ void __launch_bounds__(kTRegBound, 1) k_moe_tma(const __grid_constant
     // down kernel's grouping finished before the previous kernel started, and
     // the dense GEMV has none, so their producers wait only before their first
     // copy of activation units (below).
-    if (a.mode == 0 || warp < kTConsumers) pdl_wait();
+    if (a.mode == 0 || warp != kTConsumers) pdl_wait();
     pdl_trigger();
 
     const int tiles = a.mode == 0 ? (a.I + kTGuJ - 1) / kTGuJ
@@ -549,6 +711,10 @@ __global__ void __launch_bounds__(kTRegBound, 1) k_moe_tma(const __grid_constant
         u0 = (long long)blockIdx.x * U / g;
         u1 = (long long)(blockIdx.x + 1) * U / g;
     }
+    // first stage of CTA i's range
+    auto ub_at = [&](int i) -> long long {
+        return a.plan ? (long long)a.plan[i].x : (long long)i * U / g;
+    };
 
     if (warp == kTConsumers) {
         // ---------------- producer (whole warp; lane 0 owns the barriers)
@@ -652,10 +818,50 @@ __global__ void __launch_bounds__(kTRegBound, 1) k_moe_tma(const __grid_constant
             for (int j = (issued > kTStages ? issued - kTStages : 0); j < issued; ++j)
                 tc05::mbar_wait(&sh.full[j % kTStages], (uint32_t)((j / kTStages) & 1), kTWait);
         }
+    } else if (warp == kTSync) {
+        // ---------------- split-item counters (lane 0) and the last item's fetch
+        const TRoles ro = t_roles(u0, u1, (int)blockIdx.x + 1 < g ? ub_at(blockIdx.x + 2) : u1, ns, g);
+        if (ro.head_async && lane == 0) {
+            int d = 0;
+            if (tc05::mbar_wait(&sh.hp, 0u, kTWait))
+                d = t_publish(a, sh.h_bf, sh.h_n) ? 1 : 0;
+            else
+                atomicOr(a.status, 2);
+            sh.defer = d;
+            mbar_arrive(&sh.hd);
+        }
+        __syncwarp();
+        if (ro.tail_next) {
+            // this CTA is the item's first contributor: its counter reaches 1
+            // when the next CTA has published
+            const int32_t *c = a.cnt + blockIdx.x;
+            bool got = false;
+            for (uint32_t it = 0; it < kTPoll; ++it) {
+                int v;
+                asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+                if (__all_sync(0xFFFFFFFFu, v == 1)) {
+                    got = true;
+                    break;
+                }
+                if (__any_sync(0xFFFFFFFFu, sh.stop != 0)) break;
+                __nanosleep(256);
+            }
+            if (got) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    a.part + (size_t)(blockIdx.x + 1) * 2 * (kTRows * kMaxTok));
+                float4 *dst = reinterpret_cast<float4 *>(tail);
+                for (int i = lane; i < kTRows * kMaxTok / 4; i += 32) dst[i] = __ldcg(src + i);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                sh.ready = got ? 1 : 0;
+                mbar_arrive(&sh.tp);
+            }
+        }
     } else {
         // ---------------- consumers
-        for (int i = threadIdx.x; i <= g; i += 32 * kTConsumers)
-            sh.ub[i] = a.plan ? (long long)a.plan[i].x : (long long)i * U / g;
+        for (int i = threadIdx.x; i <= g; i += 32 * kTConsumers) sh.ub[i] = ub_at(i);
+        const TRoles ro = t_roles(u0, u1, (int)blockIdx.x + 1 < g ? ub_at(blockIdx.x + 2) : u1, ns, g);
         int j = 0, cur_pi = -1;
         bool failed = false;
         PassCursor pc;
@@ -677,19 +883,27 @@ __global__ void __launch_bounds__(kTRegBound, 1) k_moe_tma(const __grid_constant
                 cur_pi = pi;
             }
             const bool whole = kb0 == 0 && kb1 == ns;
+            const bool head = item == head_item;
             if (pc.ntok <= 4) {
                 float acc[2][1][2];
                 t_consume<1>(sh, ring, pc.ntok, kb0, kb1, j, failed, acc);
                 if (fresh) consumers_sync();  // sh.pairs written before the epilogue reads it
-                if (whole || t_combine<1>(a, sh, pc.ntok, item, item == head_item, ns, acc))
-                    t_epilogue<1>(a, sh, epi, tile, pc.ntok, pi, acc);
+                t_finish<1>(a, sh, epi, tile, pc.ntok, pi, item, head, ns, whole,
+                            ro.head_async && head, ro.tail_next && left == 0, acc);
             } else {
                 float acc[2][2][2];
                 t_consume<2>(sh, ring, pc.ntok, kb0, kb1, j, failed, acc);
                 if (fresh) consumers_sync();
-                if (whole || t_combine<2>(a, sh, pc.ntok, item, item == head_item, ns, acc))
-                    t_epilogue<2>(a, sh, epi, tile, pc.ntok, pi, acc);
+                t_finish<2>(a, sh, epi, tile, pc.ntok, pi, item, head, ns, whole,
+                            ro.head_async && head, ro.tail_next && left == 0, acc);
             }
+        }
+        if (ro.head_async) {
+            // the sync warp's count of the first item: if this CTA published
+            // it last, it writes the item now
+            const bool ok = tc05::mbar_wait(&sh.hd, 0u, kTWait);
+            if (!ok) failed = true;
+            if (ok && sh.defer) t_write_deferred(a, sh, epi, nu, head_item, tiles, ns);
         }
         if (failed && (threadIdx.x & 31) == 0) atomicOr(a.status, 2);
     }
