@@ -292,6 +292,8 @@ int prepare_impl(const qmv_moe_int4 *m, const float *x, int T, const int32_t *id
         plan.plan_dn = at<int4>(ws, L.plan) + qmv::kSkMaxCtas + 1;
         plan.s_gu = ((m->I + 127) / 128) * (m->H / 256);
         plan.s_dn = ((m->H + 255) / 256) * (m->I / 256);
+        plan.ns_gu = m->H / 256;
+        plan.ns_dn = m->I / 256;
         plan.g = qmv::tma_grid();
     }
     // the grouping kernel clears the status word and the split counters itself

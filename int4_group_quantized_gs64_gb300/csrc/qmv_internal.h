@@ -58,9 +58,10 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, int32_t *offsets, int
 // Work plan of the tensor-map FFN kernels, written by the grouping kernel
 // (ptab == null: none). A pass is up to kMaxTok pairs of one expert; the CTAs
 // of gate+up (and of down) split the passes' stages so that every CTA gets
-// the same cost, a stage with more than 4 tokens counting kPlanW2 / kPlanW1
-// of one with at most 4 (its MMAs cover two token blocks).
-constexpr int kPlanW1 = 3, kPlanW2 = 4;
+// the same cost: a stage with at most 4 tokens costs kPlanW1, one with more
+// kPlanW2 (its MMAs cover two token blocks), and the end of every item (a
+// row tile's last stage: its epilogue) kPlanItem more.
+constexpr int kPlanW1 = 3, kPlanW2 = 4, kPlanItem = 4;
 struct PlanArgs {
     int4 *ptab;        // [passes]: (expert, first list index, tokens, 0)
     int4 *plan_gu;     // [g + 1]: (first stage of each gate+up CTA, then the total;
@@ -68,6 +69,7 @@ struct PlanArgs {
                        //  holding that stage), so a CTA starts with one load
     int4 *plan_dn;     // [g + 1]: the same for down
     int s_gu, s_dn;    // stages per pass: row tiles x stages per tile
+    int ns_gu, ns_dn;  // stages per row tile (an item)
     int g;             // CTAs of the tensor-map kernel
 };
 // CTAs of a tensor-map decode launch.

@@ -96,10 +96,11 @@ __device__ __forceinline__ long long div_nn(long long a, long long b) {
 //
 // With a work plan (pl && pl->ptab): the pass table and, for gate+up and for
 // down, the first stage of every CTA, so that each CTA's stages carry the
-// same cost (PlanArgs). Cost units: the stages of used expert u start at
-// S * wpre[u] (wpre: exclusive scan of the experts' pass weights); CTA b
-// starts at cost C * b / g of the total C, inside the pass that cost falls
-// in, at the first stage whose start is not below it.
+// same cost (PlanArgs: weighted stages plus a cost per row tile's end). The
+// stages of used expert u start at cost wpre[u] (exclusive scan of the
+// experts' costs); CTA b starts at cost C * b / g of the total C, inside the
+// pass and row tile that cost falls in, at the first stage whose start is
+// not below it.
 __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t *offsets,
                           int32_t *list, int32_t *uexp, int32_t *n_used, int32_t *pass_ofs,
                           int32_t *status, int pass_tok, const uint32_t *res = nullptr,
@@ -156,22 +157,35 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
         for (int i = 0; i < np; ++i)
             pa.ptab[ep + i] = make_int4(tid, ec + i * pass_tok, min(pass_tok, c - i * pass_tok), 0);
     if (pa.ptab && pa.plan_gu) {
-        // each used expert's pass weight (full passes weigh kPlanW2, the last
-        // one by its token count)
+        // Cost of a pass of mode m: its T row tiles of N stages each, a stage
+        // weighing w (kPlanW2, or for an expert's last pass by its token
+        // count), plus kPlanItem at the end of each tile. Each used expert's
+        // cost in both modes, scanned at once: the prefix of gate+up in
+        // cnt[], that of down in s_wdn[].
         __shared__ int32_t nu_s;
-        __shared__ long long wtot_s;
-        int wexp = 0;
+        __shared__ long long wtot_s[2];
+        int32_t *s_wdn = group_smem + 3 * (E + 1);
+        auto pass_cost = [&](int m, int w) -> int {
+            const int N = m ? pa.ns_dn : pa.ns_gu, T = (m ? pa.s_dn : pa.s_gu) / N;
+            return T * (N * w + kPlanItem);
+        };
+        int wgu = 0, wdn = 0;
         if (f) {
-            const int last = c - (np - 1) * pass_tok;
-            wexp = (np - 1) * kPlanW2 + (last > 4 ? kPlanW2 : kPlanW1);
+            const int wl = c - (np - 1) * pass_tok > 4 ? kPlanW2 : kPlanW1;
+            wgu = (np - 1) * pass_cost(0, kPlanW2) + pass_cost(0, wl);
+            wdn = (np - 1) * pass_cost(1, kPlanW2) + pass_cost(1, wl);
         }
-        int ew, d1, d2;
-        __syncthreads();  // cnt[] (c) has been read: reuse it for wpre
-        block_scan3(wexp, 0, 0, ew, d1, d2, tot);
-        if (f) cnt[ef] = ew;
+        int egu, edn, d2;
+        __syncthreads();  // cnt[] (c) has been read: reuse it
+        block_scan3(wgu, wdn, 0, egu, edn, d2, tot);
+        if (f) {
+            cnt[ef] = egu;
+            s_wdn[ef] = edn;
+        }
         if (tid == E - 1) {
             nu_s = ef + f;
-            wtot_s = (long long)ew + wexp;
+            wtot_s[0] = (long long)egu + wgu;
+            wtot_s[1] = (long long)edn + wdn;
         }
         __syncthreads();
         const int nu = nu_s;
@@ -185,11 +199,15 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
             const int ce = s_off[e + 1] - s_off[e];
             return make_int4(e, s_off[e] + i * pass_tok, min(pass_tok, ce - i * pass_tok), 0);
         };
-        // one thread per (mode, CTA boundary b): both modes at once
+        // one thread per (mode, CTA boundary b): both modes at once. CTA b
+        // starts at cost C * b / g: in the pass, row tile and stage that cost
+        // falls in, at the first stage whose start is not below it.
         const int g = pa.g;
         for (int idx = tid; idx < 2 * (g + 1); idx += blockDim.x) {
             const int m = idx / (g + 1), b = idx - m * (g + 1);
             const long long S = m ? pa.s_dn : pa.s_gu;
+            const int N = m ? pa.ns_dn : pa.ns_gu, T = (int)(S / N);
+            const int32_t *wp = m ? s_wdn : cnt;
             int32_t ub;
             int lo = 0;
             if (nu == 0) {
@@ -197,22 +215,25 @@ __device__ void group_cta(const int32_t *__restrict__ ids, int P, int E, int32_t
             } else if (b == g) {
                 ub = (int32_t)(S * npass);
             } else {
-                const long long cb = div_nn(S * wtot_s * b, g);
-                int hi = nu - 1;  // last used expert whose stages start at or below cb
+                const long long cb = div_nn(wtot_s[m] * b, g);
+                int hi = nu - 1;  // last used expert whose cost starts at or below cb
                 while (lo < hi) {
                     const int mid = (lo + hi + 1) >> 1;
-                    if (S * cnt[mid] <= cb) lo = mid; else hi = mid - 1;
+                    if (wp[mid] <= cb) lo = mid; else hi = mid - 1;
                 }
                 const int e = s_uexp[lo];
                 const int ce = s_off[e + 1] - s_off[e];
                 const int npe = (ce + pass_tok - 1) / pass_tok;
                 const int wl = ce - (npe - 1) * pass_tok > 4 ? kPlanW2 : kPlanW1;
-                const long long r = cb - S * cnt[lo];
-                const int i = (int)min((long long)(npe - 1), div_nn(r, kPlanW2 * S));
-                const long long r2 = r - (long long)i * kPlanW2 * S;
+                const long long r = cb - wp[lo];
+                const int i = (int)min((long long)(npe - 1), div_nn(r, pass_cost(m, kPlanW2)));
+                const long long r2 = r - (long long)i * pass_cost(m, kPlanW2);
                 const int wi = i < npe - 1 ? kPlanW2 : wl;
-                const long long st = min(S, div_nn(r2 + wi - 1, wi));
-                ub = (int32_t)(S * (s_pofs[lo] + i) + st);
+                const long long tc = (long long)N * wi + kPlanItem;  // a row tile of this pass
+                const int it = (int)min((long long)(T - 1), div_nn(r2, tc));
+                const long long r3 = r2 - (long long)it * tc;
+                const long long st = min((long long)N, div_nn(r3 + wi - 1, wi));
+                ub = (int32_t)(S * (s_pofs[lo] + i) + (long long)it * N + st);
             }
             const int4 t = pass_at((int)div_nn(ub, S), lo);  // the pass holding stage ub, if any
             (m ? pa.plan_dn : pa.plan_gu)[b] = make_int4(ub, t.x, t.y, t.z);
