@@ -60,6 +60,15 @@ int qmv_version(void);
 /* Human-readable name of a status code (static string, never NULL). */
 const char *qmv_status_str(int status);
 
+/* Test hook, not part of the method: from the next launch on, the compute
+ * warps of every odd CTA of the tensor-map MoE and dense kernels start `ns`
+ * nanoseconds late (0 turns it off; negative values are taken as 0). Items
+ * whose stages two CTAs share then meet every order of arrival, so tests can
+ * check that the output does not depend on it. Process-wide, host only,
+ * enqueues nothing; not thread-safe against concurrent launches. Returns the
+ * previous value. */
+int qmv_test_split_skew(int ns);
+
 /* ---------------------------------------------------------------- GEMV */
 
 /* Scratch needed by qmv_int4_gs / qmv_int8_row for S tokens of length K, in

@@ -59,6 +59,7 @@ def lib():
         P = ctypes.POINTER(MoeDesc)
         sig = {
             "qmv_version": ([], i32),
+            "qmv_test_split_skew": ([i32], i32),
             "qmv_status_str": ([i32], ctypes.c_char_p),
             "qmv_gemv_workspace_bytes": ([i32, i32], sz),
             "qmv_int4_gs": ([vp, vp, i32, i32, i32, vp, vp, i32, vp, sz, vp], i32),
@@ -122,6 +123,13 @@ def _need(t, dtype, name):
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t
+
+
+def qmv_test_split_skew(ns: int) -> int:
+    """Test hook (qmv.h): the compute warps of odd CTAs of the tensor-map kernels
+    start `ns` nanoseconds late from the next launch on (0: off). Returns the
+    previous value."""
+    return int(lib().qmv_test_split_skew(int(ns)))
 
 
 # ------------------------------------------------------------------ GEMV

@@ -83,6 +83,12 @@ extern "C" {
 
 int qmv_version(void) { return 100; }
 
+int qmv_test_split_skew(int ns) {
+    const int old = qmv::g_split_skew_ns;
+    qmv::g_split_skew_ns = ns > 0 ? ns : 0;
+    return old;
+}
+
 const char *qmv_status_str(int status) {
     switch (status) {
         case QMV_OK: return "ok";

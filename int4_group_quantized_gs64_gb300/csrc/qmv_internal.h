@@ -74,6 +74,9 @@ struct PlanArgs {
 };
 // CTAs of a tensor-map decode launch.
 int tma_grid();
+// Test hook of the tensor-map kernel's split items: the consumers of odd CTAs
+// start this many ns late (0: off). Set through qmv_test_split_skew.
+extern int g_split_skew_ns;
 
 // Grouping plus the split of the T activation rows, in one launch (with
 // logits: routing too, ids / w then written to ids_out / w_out). With

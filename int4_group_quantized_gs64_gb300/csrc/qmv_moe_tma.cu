@@ -101,6 +101,7 @@ struct TmaArgs {
     int32_t *status;
     int32_t *cnt;        // per CTA: contributors done on the split item that starts in it
     float *part;         // per CTA: partial sums [2][kTRows][kMaxTok] (head / tail item)
+    int skew_ns;         // test hook: the consumers of odd CTAs start this much later
 };
 
 __device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -202,6 +203,12 @@ __device__ __forceinline__ void start_cursor(PassCursor &c, const TmaArgs &a, in
     } else {
         c.seek(a, nu, p);
     }
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
@@ -860,6 +867,13 @@ __global__ void __launch_bounds__(kTRegBound, 1) k_moe_tma(const __grid_constant
         }
     } else {
         // ---------------- consumers
+        if (a.skew_ns > 0 && (blockIdx.x & 1)) {
+            // test hook (qmv_test_split_skew): odd CTAs start late, so that
+            // their neighbours finish first and the split items take the
+            // fallback and deferred paths
+            const unsigned long long t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < (unsigned long long)a.skew_ns) __nanosleep(1000);
+        }
         for (int i = threadIdx.x; i <= g; i += 32 * kTConsumers) sh.ub[i] = ub_at(i);
         const TRoles ro = t_roles(u0, u1, (int)blockIdx.x + 1 < g ? ub_at(blockIdx.x + 2) : u1, ns, g);
         int j = 0, cur_pi = -1;
@@ -1012,6 +1026,7 @@ cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const 
     a.status = status;
     a.cnt = cnt;
     a.part = part;
+    a.skew_ns = g_split_skew_ns;
     a.tiles0 = (m.H + kTDnRows - 1) / kTDnRows;  // down: every row tile is the first matrix's
     bool ok;
     if (mode == 0) {
@@ -1026,6 +1041,8 @@ cudaError_t launch_moe_tma(const MoeDims &m, int mode, const void *cells, const 
     if (e != cudaSuccess) return e;
     return launch(k_moe_tma, dim3(tma_grid()), dim3(kTThreads), (size_t)kTSmem, st, true, a);
 }
+
+int g_split_skew_ns = 0;
 
 int tma_grid() {
     set_smem(k_moe_tma, kTSmem);
@@ -1062,6 +1079,7 @@ cudaError_t launch_dense_tma(const uint8_t *wq, const float *scales, int N, int 
     a.status = status;
     a.cnt = cnt;
     a.part = part;
+    a.skew_ns = g_split_skew_ns;
     if (!make_maps(a, wq, scales, 1, N, K)) return cudaErrorInvalidValue;
     if (wq2) {
         a.H2 = N2;

@@ -89,6 +89,32 @@ def test_int4_tma_shapes(N, K, S):
         assert norm_err(y.cpu().numpy(), ref, den) <= TOL_FP32
 
 
+@pytest.mark.parametrize("N,K,S", [(14336, 4096, 8), (256, 16384, 2)])
+def test_int4_tma_split_items_any_arrival_order(N, K, S):
+    """Dense mode of the tensor-map kernel with the compute warps of odd CTAs
+    started 100 us late (qmv_test_split_skew): the items two CTAs share are
+    finished by whichever arrives last, and y is bit-identical to the
+    undelayed call's."""
+    rng = np.random.default_rng(N + K + S + 5)
+    wq = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sc = (np.abs(rng.normal(0, 0.02, size=(N, K // 64))) + 1e-4).astype(np.float32)
+    x = rng.normal(size=(S, K)).astype(np.float32)
+    ws = torch.zeros((q.qmv_gemv_workspace_bytes(K, S),), dtype=torch.uint8, device="cuda")
+    dw, ds, dx = dev(wq), dev(sc), dev(x)
+    ref = q.qmv_int4_gs(dw, ds, dx, ws=ws).cpu().numpy()
+    old = q.qmv_test_split_skew(100_000)
+    try:
+        a = q.qmv_int4_gs(dw, ds, dx, ws=ws).cpu().numpy()
+    finally:
+        q.qmv_test_split_skew(old)
+    b = q.qmv_int4_gs(dw, ds, dx, ws=ws).cpu().numpy()
+    assert int(ws[:4].view(torch.int32).cpu()[0]) == 0
+    assert np.array_equal(a, ref)
+    assert np.array_equal(b, ref)
+    ref64, den = oracle.qmv_int4_gs(wq, sc, x, 64, with_den=True)
+    assert norm_err(a, ref64, den) <= TOL_FP32
+
+
 # Pairs of matrices against one x: the pages' q_a + kv_a shape 6144 -> (2048, 576),
 # ragged last row tiles (N not a multiple of 256), several token passes, and
 # a pair that does not qualify for the tensor-map kernel (two GEMVs).

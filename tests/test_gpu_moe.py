@@ -402,6 +402,36 @@ def test_ffn_deterministic(pool_160):
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("skew_us", [30, 150])
+def test_ffn_split_items_any_arrival_order(pool_160, skew_us):
+    """An item whose stages two CTAs share comes out the same whatever order
+    they reach it in. With the compute warps of odd CTAs started late (the
+    qmv_test_split_skew hook; 150 us is longer than a CTA's whole range), an
+    even CTA ends before its odd successor has published the rest of their
+    shared item, so it publishes instead of adding the fetched partial sums,
+    and the successor, publishing last, writes the item after its own range;
+    an odd CTA ends after its even successor published, and adds the fetched
+    partial sums. The outputs must equal the undelayed call's bit for bit,
+    twice on one workspace (the counters return to zero) and once more after
+    the hook is off."""
+    x, ids, w = _route_oracle(W3)
+    dx, dids, dw = dev(x), dev(ids), dev(w)
+    ref = q.moe_expert_ffn_int4(pool_160, dx, dids, dw).cpu().numpy()
+    T, k = ids.shape
+    ws = torch.empty(q.moe_workspace_bytes(pool_160, T, k), dtype=torch.uint8, device="cuda")
+    old = q.qmv_test_split_skew(skew_us * 1000)
+    try:
+        a = q.moe_expert_ffn_int4(pool_160, dx, dids, dw, ws=ws).cpu().numpy()
+        b = q.moe_expert_ffn_int4(pool_160, dx, dids, dw, ws=ws).cpu().numpy()
+    finally:
+        q.qmv_test_split_skew(old)
+    c = q.moe_expert_ffn_int4(pool_160, dx, dids, dw, ws=ws).cpu().numpy()
+    assert int(ws[:4].view(torch.int32).cpu()[0]) == 0
+    assert np.array_equal(a, ref)
+    assert np.array_equal(b, ref)
+    assert np.array_equal(c, ref)
+
+
 def test_ffn_phases_repeat_match_fused():
     """The four phases reproduce the fused call bit for bit, also when gate+up
     and down run again on one prepared workspace (items split between CTAs
